@@ -1,0 +1,210 @@
+/*
+ * moe_gb300.h -- C ABI of the GB300 (sm_103a) MoE expert-layer library
+ * (libmoe_gb300.so).
+ *
+ * The layer is the router -> permutation -> grouped-GEMM SwiGLU FFN ->
+ * combine block of TransformerEngine PR #2912, "[JAX] Add an MoE Block
+ * (Layer) that compound router, permutation, groupedGEMM and communication"
+ * (TE-2912 below), on one GPU without the expert-parallel all-to-all, plus
+ * the chunked-K partial-sum grouped GEMM of MaxText PR #4295, "Overlap moe
+ * comms with collective matmul" (MT-4295 below).
+ *
+ * Conventions shared by every call
+ *   - Every tensor argument is DEVICE memory owned by the caller; the library
+ *     never allocates, frees or retains a pointer after the call returns.
+ *   - Matrices are dense row-major with an explicit leading dimension (in
+ *     elements).  bf16 tensors are passed as uint16_t (bf16 bit patterns).
+ *     bf16 matrices need ld % 8 == 0 and 16-byte aligned base pointers.
+ *   - Every call enqueues its kernels on `stream` and returns without a host
+ *     synchronisation.  A non-OK status means nothing was enqueued, except
+ *     MOE_ERR_CUDA, which reports a failed launch (text via moe_last_error()).
+ *   - Device-side faults are never raised.  Kernels that can meet bad data
+ *     (an expert id out of range, a wait that runs past its time limit) write
+ *     a MOE_ERR_* code into the optional caller-provided int32 `dev_status`
+ *     word (first error wins, 0 = no error) and skip the bad item; the caller
+ *     reads the word after synchronising.
+ *   - Group layout: experts own contiguous row ranges of the permuted
+ *     matrices, group e = rows [group_offsets[e], group_offsets[e+1]).
+ *     group_offsets lives on the device and is read by the kernels directly:
+ *     ragged sizes never travel to the host.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *moe_stream_t;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* null pointer, negative size, ld too small, ... */
+  MOE_ERR_UNSUPPORTED = 2, /* valid but outside what the kernels handle (sizes, alignment) */
+  MOE_ERR_CUDA = 3,        /* a CUDA launch or runtime call failed */
+  MOE_ERR_TIMEOUT = 4,     /* device word only: a bounded wait ran out */
+  MOE_ERR_DEVICE = 5       /* device word only: bad data met on the device */
+} moe_status_t;
+
+enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 };
+enum { MOE_DTYPE_BF16 = 0, MOE_DTYPE_F32 = 1 };
+enum { MOE_EPI_NONE = 0, MOE_EPI_SWIGLU_FWD = 1, MOE_EPI_SWIGLU_BWD = 2 };
+
+/* Static description of a status code. */
+const char *moe_status_string(int status);
+/* Message of the last failing call made by this host thread ("" if none). */
+const char *moe_last_error(void);
+/* Library ABI version (major*100 + minor). */
+int moe_version(void);
+
+/*
+ * Worst-case number of permuted rows: T*k + E*(align-1) (align <= 1: T*k).
+ * TE-2912, review thread on recv_buffer_rows ("align_size > 0 + EP are
+ * combined"): aligned group sizes can add up to align-1 rows per expert.
+ */
+int64_t moe_rows_cap(int T, int E, int k, int align);
+
+/* Bytes of device workspace that moe_permute needs for T tokens and E experts. */
+size_t moe_permute_workspace_bytes(int T, int E);
+
+/*
+ * moe_route_topk -- top-k expert selection and routing weights.
+ * TE-2912, Description: the fused router, "top-K with optional
+ * grouped/sigmoid scoring (for DSv3 workload)" (grouped scoring is not
+ * provided).
+ *   logits    fp32 [T, ld_logits >= E]      router logits
+ *   k         1 <= k <= min(E, 16); E <= 256
+ *   score_fn  MOE_SCORE_SOFTMAX: softmax over all E experts;
+ *             MOE_SCORE_SIGMOID: 1/(1+exp(-logit)) per expert
+ *   renorm    nonzero: divide the k selected scores by their sum
+ *   topk_idx  int32 [T, k] out: experts by descending logit, ties to the lower id
+ *   topk_w    fp32  [T, k] out: the selected (renormalised) scores, same order
+ * Selection compares the fp32 logits (the score maps are monotone); a NaN
+ * logit ranks below every number.
+ */
+moe_status_t moe_route_topk(const float *logits, int64_t ld_logits, int T, int E, int k,
+                            int score_fn, int renorm, int32_t *topk_idx, float *topk_w,
+                            moe_stream_t stream);
+
+/*
+ * moe_permute -- group the T*k (token, slot) assignments by expert and gather
+ * the token rows into per-expert contiguous groups.
+ * TE-2912, review thread on _combine_bwd (pure-JAX path): the flat
+ * assignment a = t*k + j is ordered by a stable argsort on its expert
+ * (sorted_indices), i.e. by (expert, token); group_sizes are the aligned
+ * counts when align_size > 0 (thread on recv_buffer_rows); token dropping
+ * (MaxText PR #2319, "[Draft] Integrate TE/JAX GroupedGEMM for MoE", Tests)
+ * keeps the first `capacity` assignments of each expert in that order.
+ *   x              bf16 [T, ldx >= d]            token activations (d % 8 == 0)
+ *   topk_idx       int32 [T, k]                  expert ids, distinct within a token
+ *   align          group-size multiple (0 or 1: none)
+ *   capacity       per-expert kept assignments (<= 0: no dropping)
+ *   x_sorted       bf16 [rows_cap, ld_xs >= d] out: row p = x[token of
+ *                  sorted_to_flat[p]]; padding rows are zero; rows >= R
+ *                  (R = group_offsets[E]) are not written
+ *   rows_cap       rows of x_sorted / sorted_to_flat, >= moe_rows_cap(T,E,k,align)
+ *   group_sizes    int32 [E] out: aligned group sizes
+ *   kept_counts    int32 [E] out: kept (not dropped) assignments per expert
+ *   group_offsets  int32 [E+1] out: exclusive scan of group_sizes
+ *   sorted_to_flat int32 [rows_cap] out: flat assignment of row p, -1 on
+ *                  padding rows and on rows >= R
+ *   flat_to_sorted int32 [T*k] out: row of assignment a, -1 if dropped
+ *   workspace      device scratch of >= moe_permute_workspace_bytes(T, E) bytes
+ *                  (contents on entry are ignored)
+ * An out-of-range expert id or a repeated expert within one token sets
+ * MOE_ERR_DEVICE in dev_status; such assignments are treated as dropped.
+ */
+moe_status_t moe_permute(const uint16_t *x, int64_t ldx, const int32_t *topk_idx, int T, int d,
+                         int E, int k, int align, int capacity, uint16_t *x_sorted,
+                         int64_t ld_xs, int64_t rows_cap, int32_t *group_sizes,
+                         int32_t *kept_counts, int32_t *group_offsets,
+                         int32_t *sorted_to_flat, int32_t *flat_to_sorted, void *workspace,
+                         size_t workspace_bytes, int32_t *dev_status, moe_stream_t stream);
+
+/*
+ * moe_gmm -- grouped GEMM over ragged per-expert row groups (tcgen05 tensor
+ * cores, fp32 accumulation).  For every row r of group e:
+ *     S[r, :] = A[r, :] . B_e  (+ partial_sum[r, :] when partial_sum != NULL)
+ * TE-2912: the grouped_gemm calls of the expert FFN (Description), with
+ * [wi_0 | wi_1] fused into one up-projection (wi-fusion commit); MT-4295,
+ * review threads on the gmm kernel: `transpose_rhs` and the in-place
+ * `partial_sum`.
+ *   A         bf16 [rows_cap, lda >= K]   permuted activations
+ *   B         bf16 expert weights, expert e at B + e*stride_b:
+ *               trans_b == 0: B_e is [K, N] row-major (ldb >= N)   S = A . B_e
+ *               trans_b != 0: B_e is [N, K] row-major (ldb >= K)   S = A . B_e^T
+ *   group_offsets int32 [E+1] device; rows_cap bounds group_offsets[E]
+ *   K, N      multiples of 8, > 0
+ *   epilogue  MOE_EPI_NONE:       C = S, stored as c_dtype (bf16 or fp32)
+ *             MOE_EPI_SWIGLU_FWD: N = 2F (F % 8 == 0); C = bf16(S) = H and
+ *                                 C2 = bf16(silu(S[:, :F]) * S[:, F:]) = Act
+ *                                 (C2 bf16 [rows_cap, ldc2 >= F])
+ *             MOE_EPI_SWIGLU_BWD: S is dAct [., N = F]; aux = H bf16
+ *                                 [rows_cap, ld_aux >= 2F]; C = bf16 dH
+ *                                 [., 2F]: dH[:, :F] = S * u * s * (1 + g(1-s)),
+ *                                 dH[:, F:] = S * silu(g), g = H[:, :F],
+ *                                 u = H[:, F:], s = sigmoid(g)
+ *   partial_sum fp32 [rows_cap, ld_ps >= N] or NULL (NONE / SWIGLU_FWD only);
+ *             may alias C when c_dtype is fp32 and ld_ps == ldc (in place)
+ *   C         [rows_cap, ldc] (ldc >= N, or >= 2F for SWIGLU_BWD)
+ * Only rows r < group_offsets[E] are written.
+ */
+moe_status_t moe_gmm(const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
+                     int64_t stride_b, int trans_b, const int32_t *group_offsets, int E,
+                     int64_t rows_cap, int K, int N, int epilogue, const uint16_t *aux,
+                     int64_t ld_aux, const float *partial_sum, int64_t ld_ps, void *C,
+                     int c_dtype, int64_t ldc, uint16_t *C2, int64_t ldc2, int32_t *dev_status,
+                     moe_stream_t stream);
+
+/*
+ * moe_tgmm -- weight-gradient grouped GEMM, ragged along the contraction:
+ *     W_e = A_e^T . B_e   (+ W_e when accumulate),  A_e / B_e = rows of group e
+ * MT-4295, Testing: "TGMM with zero-initialized empty expert groups": an
+ * expert with no rows gets exact zeros (or keeps W_e when accumulating).
+ *   A  bf16 [rows_cap, lda >= M];  B  bf16 [rows_cap, ldb >= N];  M, N % 8 == 0
+ *   W  expert e at W + e*stride_w, [M, ldw >= N] row-major, w_dtype bf16 or
+ *      fp32 (accumulate requires fp32)
+ */
+moe_status_t moe_tgmm(const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
+                      const int32_t *group_offsets, int E, int64_t rows_cap, int M, int N,
+                      void *W, int w_dtype, int64_t ldw, int64_t stride_w, int accumulate,
+                      int32_t *dev_status, moe_stream_t stream);
+
+/*
+ * moe_combine -- routing-weighted un-permute:
+ *     out[t] = sum_j w[t,j] * Y[flat_to_sorted[t*k+j]]   (slots with -1 skipped)
+ * summed in fp32 in slot order.  With topk_w == NULL every weight is 1, which
+ * is the backward of moe_permute's row gather (dispatch backward).
+ * TE-2912, review thread on _combine_bwd: the forward combine is
+ * output[B,E] = sum_K intermediate[B,K,E] * weights[B,K] after the un-sort.
+ *   Y bf16 [rows, ldy >= d]; out bf16 [T, ldo >= d]; d % 8 == 0
+ */
+moe_status_t moe_combine(const uint16_t *Y, int64_t ldy, const int32_t *flat_to_sorted,
+                         const float *topk_w, int T, int k, int d, uint16_t *out, int64_t ldo,
+                         moe_stream_t stream);
+
+/*
+ * moe_unpermute_bwd -- backward of moe_combine (TE-2912, review thread on
+ * _combine_bwd: d_intermediate = d_output * w, d_w = sum over hidden of
+ * d_output * intermediate, zero on padding, placed back in sorted order):
+ *     dY[p]      = w[t,j] * d_out[t]        for p = flat_to_sorted[t*k+j] >= 0
+ *     d_topk_w[t,j] = <d_out[t], Y[p]>   (0 for dropped slots)
+ *     dY[p]      = 0 for padding rows p < group_offsets[E]
+ *   d_out bf16 [T, ld_dout]; Y bf16 [rows_cap, ldy]; dY bf16 [rows_cap, ld_dy];
+ *   sorted_to_flat int32 [rows_cap]; group_offsets int32 [E+1]
+ */
+moe_status_t moe_unpermute_bwd(const uint16_t *d_out, int64_t ld_dout, const uint16_t *Y,
+                               int64_t ldy, const int32_t *flat_to_sorted,
+                               const int32_t *sorted_to_flat, const int32_t *group_offsets,
+                               const float *topk_w, int T, int k, int d, int E,
+                               int64_t rows_cap, uint16_t *dY, int64_t ld_dy, float *d_topk_w,
+                               moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

@@ -1,0 +1,179 @@
+"""ctypes binding of libmoe_gb300.so: one Python function per C entry point,
+same names, argument marshalling only (tensor -> pointer, shape -> sizes,
+current torch stream -> cudaStream_t).  Every step of the layer runs in the
+library's CUDA kernels; there is no fallback: if the library is missing the
+import fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_UNSUPPORTED = 2
+MOE_ERR_CUDA = 3
+MOE_ERR_TIMEOUT = 4
+MOE_ERR_DEVICE = 5
+SCORE_SOFTMAX = 0
+SCORE_SIGMOID = 1
+DTYPE_BF16 = 0
+DTYPE_F32 = 1
+EPI_NONE = 0
+EPI_SWIGLU_FWD = 1
+EPI_SWIGLU_BWD = 2
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__("%s (status %d: %s)" % (msg, status, status_string(status)))
+        self.status = status
+
+
+def _load() -> ctypes.CDLL:
+    path = _build.LIB_PATH
+    if not os.path.exists(path):
+        raise ImportError("libmoe_gb300.so is not built (%s); run "
+                          "`python -m mixture_experts_grouped_router_gb300.build`" % path)
+    return ctypes.CDLL(path)
+
+
+LIB = _load()
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+
+_SIGS = {
+    "moe_status_string": (ctypes.c_char_p, [_I]),
+    "moe_last_error": (ctypes.c_char_p, []),
+    "moe_version": (_I, []),
+    "moe_rows_cap": (_I64, [_I, _I, _I, _I]),
+    "moe_permute_workspace_bytes": (_SZ, [_I, _I]),
+    "moe_route_topk": (_I, [_P, _I64, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "moe_permute": (_I, [_P, _I64, _P, _I, _I, _I, _I, _I, _I, _P, _I64, _I64, _P, _P, _P, _P,
+                         _P, _P, _SZ, _P, _P]),
+    "moe_gmm": (_I, [_P, _I64, _P, _I64, _I64, _I, _P, _I, _I64, _I, _I, _I, _P, _I64, _P, _I64,
+                     _P, _I, _I64, _P, _I64, _P, _P]),
+    "moe_tgmm": (_I, [_P, _I64, _P, _I64, _P, _I, _I64, _I, _I, _P, _I, _I64, _I64, _I, _P, _P]),
+    "moe_combine": (_I, [_P, _I64, _P, _P, _I, _I, _I, _P, _I64, _P]),
+    "moe_unpermute_bwd": (_I, [_P, _I64, _P, _I64, _P, _P, _P, _P, _I, _I, _I, _I, _I64, _P,
+                               _I64, _P, _P]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(LIB, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+EXPORTED = tuple(_SIGS)
+
+
+def status_string(status: int) -> str:
+    return LIB.moe_status_string(status).decode()
+
+
+def last_error() -> str:
+    return LIB.moe_last_error().decode()
+
+
+def _check(status: int):
+    if status != MOE_OK:
+        raise MoEError(status, last_error())
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ld(t):
+    assert t.dim() >= 2, "matrices only"
+    if t.numel() == 0:
+        return t.shape[-1]
+    assert t.stride(-1) == 1, "row-major tensors only"
+    return t.stride(-2)
+
+
+def moe_rows_cap(T: int, E: int, k: int, align: int) -> int:
+    return int(LIB.moe_rows_cap(T, E, k, align))
+
+
+def moe_permute_workspace_bytes(T: int, E: int) -> int:
+    return int(LIB.moe_permute_workspace_bytes(T, E))
+
+
+def moe_route_topk(logits, k, score_fn, renorm, topk_idx, topk_w, stream=None):
+    T, E = logits.shape
+    _check(LIB.moe_route_topk(_ptr(logits), _ld(logits), T, E, k, score_fn, int(renorm),
+                              _ptr(topk_idx), _ptr(topk_w), _stream(stream)))
+
+
+def moe_permute(x, topk_idx, E, align, capacity, x_sorted, group_sizes, kept_counts,
+                group_offsets, sorted_to_flat, flat_to_sorted, workspace, dev_status=None,
+                stream=None):
+    T, d = x.shape
+    k = topk_idx.shape[1]
+    _check(LIB.moe_permute(_ptr(x), _ld(x), _ptr(topk_idx), T, d, E, k, align, capacity,
+                           _ptr(x_sorted), _ld(x_sorted), x_sorted.shape[0], _ptr(group_sizes),
+                           _ptr(kept_counts), _ptr(group_offsets), _ptr(sorted_to_flat),
+                           _ptr(flat_to_sorted), _ptr(workspace),
+                           workspace.numel() * workspace.element_size(), _ptr(dev_status),
+                           _stream(stream)))
+
+
+def moe_gmm(A, B, trans_b, group_offsets, C, epilogue=EPI_NONE, aux=None, partial_sum=None,
+            C2=None, dev_status=None, stream=None, K=None, N=None):
+    """A [rows_cap, >=K]; B [E, K, N] (trans_b=0) or [E, N, K] (trans_b=1), any
+    row-major views; C bf16 or fp32.  K and N default to the shapes of B."""
+    E = B.shape[0]
+    if K is None:
+        K = B.shape[2] if trans_b else B.shape[1]
+    if N is None:
+        N = B.shape[1] if trans_b else B.shape[2]
+    c_dtype = DTYPE_F32 if C.dtype == torch.float32 else DTYPE_BF16
+    _check(LIB.moe_gmm(_ptr(A), _ld(A), _ptr(B), B.stride(1), B.stride(0), int(trans_b),
+                       _ptr(group_offsets), E, A.shape[0], K, N, epilogue, _ptr(aux),
+                       _ld(aux) if aux is not None else 0, _ptr(partial_sum),
+                       _ld(partial_sum) if partial_sum is not None else 0, _ptr(C), c_dtype,
+                       _ld(C), _ptr(C2), _ld(C2) if C2 is not None else 0, _ptr(dev_status),
+                       _stream(stream)))
+
+
+def moe_tgmm(A, B, group_offsets, W, accumulate=False, dev_status=None, stream=None):
+    """W [E, M, N] (bf16 or fp32, any row-major view); A [rows_cap, >=M]; B [rows_cap, >=N]."""
+    E, M, N = W.shape
+    w_dtype = DTYPE_F32 if W.dtype == torch.float32 else DTYPE_BF16
+    _check(LIB.moe_tgmm(_ptr(A), _ld(A), _ptr(B), _ld(B), _ptr(group_offsets), E, A.shape[0], M,
+                        N, _ptr(W), w_dtype, W.stride(1), W.stride(0), int(accumulate),
+                        _ptr(dev_status), _stream(stream)))
+
+
+def moe_combine(Y, flat_to_sorted, topk_w, out, k, stream=None):
+    T, d = out.shape
+    _check(LIB.moe_combine(_ptr(Y), _ld(Y), _ptr(flat_to_sorted), _ptr(topk_w), T, k, d,
+                           _ptr(out), _ld(out), _stream(stream)))
+
+
+def moe_unpermute_bwd(d_out, Y, flat_to_sorted, sorted_to_flat, group_offsets, topk_w, dY,
+                      d_topk_w, stream=None):
+    T, d = d_out.shape
+    k = topk_w.shape[1]
+    E = group_offsets.shape[0] - 1
+    _check(LIB.moe_unpermute_bwd(_ptr(d_out), _ld(d_out), _ptr(Y), _ld(Y), _ptr(flat_to_sorted),
+                                 _ptr(sorted_to_flat), _ptr(group_offsets), _ptr(topk_w), T, k, d,
+                                 E, dY.shape[0], _ptr(dY), _ld(dY), _ptr(d_topk_w),
+                                 _stream(stream)))

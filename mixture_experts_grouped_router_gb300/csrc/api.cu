@@ -1,0 +1,246 @@
+// C ABI of libmoe_gb300.so: argument validation, error reporting and the
+// launches.  Every check here runs on the host before anything is enqueued.
+#include <stdarg.h>
+#include <stdio.h>
+
+#include "internal.h"
+
+namespace moe {
+
+static thread_local char g_err[512] = "";
+
+void set_error(const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
+  return n;
+}
+
+}  // namespace moe
+
+using moe::set_error;
+
+#define REQUIRE(cond, code, ...)   \
+  do {                             \
+    if (!(cond)) {                 \
+      set_error(__VA_ARGS__);      \
+      return (code);               \
+    }                              \
+  } while (0)
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static moe_status_t cuda_status(cudaError_t e, const char *what) {
+  if (e == cudaSuccess) return MOE_OK;
+  set_error("%s: %s", what, cudaGetErrorString(e));
+  return MOE_ERR_CUDA;
+}
+
+extern "C" {
+
+const char *moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported size or alignment";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_DEVICE: return "bad data met on the device";
+    default: return "unknown status";
+  }
+}
+
+const char *moe_last_error(void) { return moe::g_err; }
+
+int moe_version(void) { return 100; }
+
+int64_t moe_rows_cap(int T, int E, int k, int align) {
+  if (T < 0 || E <= 0 || k <= 0) return -1;
+  return (int64_t)T * k + (int64_t)E * (align > 1 ? align - 1 : 0);
+}
+
+size_t moe_permute_workspace_bytes(int T, int E) {
+  if (T < 0 || E <= 0) return 0;
+  return moe::permute_workspace_bytes(T, E);
+}
+
+moe_status_t moe_route_topk(const float *logits, int64_t ld_logits, int T, int E, int k,
+                            int score_fn, int renorm, int32_t *topk_idx, float *topk_w,
+                            moe_stream_t stream) {
+  set_error("");
+  REQUIRE(T >= 0 && E > 0 && k > 0, MOE_ERR_INVALID_ARG, "moe_route_topk: T=%d E=%d k=%d", T, E, k);
+  REQUIRE(k <= E, MOE_ERR_INVALID_ARG, "moe_route_topk: k=%d > E=%d", k, E);
+  REQUIRE(E <= 256 && k <= 16, MOE_ERR_UNSUPPORTED, "moe_route_topk: needs E <= 256, k <= 16");
+  REQUIRE(ld_logits >= E, MOE_ERR_INVALID_ARG, "moe_route_topk: ld_logits < E");
+  REQUIRE(score_fn == MOE_SCORE_SOFTMAX || score_fn == MOE_SCORE_SIGMOID, MOE_ERR_INVALID_ARG,
+          "moe_route_topk: bad score_fn %d", score_fn);
+  REQUIRE(T == 0 || (logits && topk_idx && topk_w), MOE_ERR_INVALID_ARG,
+          "moe_route_topk: null pointer");
+  return cuda_status(moe::launch_route_topk(logits, ld_logits, T, E, k, score_fn, renorm, topk_idx,
+                                            topk_w, (cudaStream_t)stream),
+                     "moe_route_topk launch");
+}
+
+moe_status_t moe_permute(const uint16_t *x, int64_t ldx, const int32_t *topk_idx, int T, int d,
+                         int E, int k, int align, int capacity, uint16_t *x_sorted,
+                         int64_t ld_xs, int64_t rows_cap, int32_t *group_sizes,
+                         int32_t *kept_counts, int32_t *group_offsets,
+                         int32_t *sorted_to_flat, int32_t *flat_to_sorted, void *workspace,
+                         size_t workspace_bytes, int32_t *dev_status, moe_stream_t stream) {
+  set_error("");
+  REQUIRE(T >= 0 && d > 0 && E > 0 && k > 0 && align >= 0, MOE_ERR_INVALID_ARG,
+          "moe_permute: T=%d d=%d E=%d k=%d align=%d", T, d, E, k, align);
+  REQUIRE(E <= 256 && k <= 16 && k <= E, MOE_ERR_UNSUPPORTED,
+          "moe_permute: needs E <= 256 and k <= min(E, 16)");
+  REQUIRE(d % 8 == 0 && ldx % 8 == 0 && ld_xs % 8 == 0, MOE_ERR_UNSUPPORTED,
+          "moe_permute: d, ldx, ld_xs must be multiples of 8");
+  REQUIRE(ldx >= d && ld_xs >= d, MOE_ERR_INVALID_ARG, "moe_permute: leading dimension < d");
+  REQUIRE(rows_cap >= moe_rows_cap(T, E, k, align), MOE_ERR_INVALID_ARG,
+          "moe_permute: rows_cap %lld < %lld", (long long)rows_cap,
+          (long long)moe_rows_cap(T, E, k, align));
+  REQUIRE(rows_cap < (1ll << 31) && (int64_t)T * k < (1ll << 31), MOE_ERR_UNSUPPORTED,
+          "moe_permute: more than 2^31 rows");
+  REQUIRE(group_sizes && kept_counts && group_offsets && sorted_to_flat && workspace,
+          MOE_ERR_INVALID_ARG, "moe_permute: null pointer");
+  REQUIRE(T == 0 || (x && topk_idx && flat_to_sorted && x_sorted), MOE_ERR_INVALID_ARG,
+          "moe_permute: null pointer");
+  REQUIRE(T == 0 || (aligned16(x) && aligned16(x_sorted)), MOE_ERR_UNSUPPORTED,
+          "moe_permute: x and x_sorted must be 16-byte aligned");
+  REQUIRE(workspace_bytes >= moe::permute_workspace_bytes(T, E), MOE_ERR_INVALID_ARG,
+          "moe_permute: workspace of %zu bytes < %zu", workspace_bytes,
+          moe::permute_workspace_bytes(T, E));
+  return cuda_status(moe::launch_permute(x, ldx, topk_idx, T, d, E, k, align, capacity, x_sorted,
+                                         ld_xs, rows_cap, group_sizes, kept_counts, group_offsets,
+                                         sorted_to_flat, flat_to_sorted,
+                                         static_cast<int32_t *>(workspace), dev_status,
+                                         (cudaStream_t)stream),
+                     "moe_permute launch");
+}
+
+moe_status_t moe_gmm(const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
+                     int64_t stride_b, int trans_b, const int32_t *group_offsets, int E,
+                     int64_t rows_cap, int K, int N, int epilogue, const uint16_t *aux,
+                     int64_t ld_aux, const float *partial_sum, int64_t ld_ps, void *C,
+                     int c_dtype, int64_t ldc, uint16_t *C2, int64_t ldc2, int32_t *dev_status,
+                     moe_stream_t stream) {
+  set_error("");
+  REQUIRE(E > 0 && rows_cap >= 0 && K > 0 && N > 0, MOE_ERR_INVALID_ARG,
+          "moe_gmm: E=%d rows_cap=%lld K=%d N=%d", E, (long long)rows_cap, K, N);
+  REQUIRE(epilogue >= MOE_EPI_NONE && epilogue <= MOE_EPI_SWIGLU_BWD, MOE_ERR_INVALID_ARG,
+          "moe_gmm: bad epilogue %d", epilogue);
+  REQUIRE(c_dtype == MOE_DTYPE_BF16 || c_dtype == MOE_DTYPE_F32, MOE_ERR_INVALID_ARG,
+          "moe_gmm: bad c_dtype");
+  REQUIRE(A && B && group_offsets && C, MOE_ERR_INVALID_ARG, "moe_gmm: null pointer");
+  REQUIRE(K % 8 == 0 && N % 8 == 0 && lda % 8 == 0 && ldb % 8 == 0 && stride_b % 8 == 0,
+          MOE_ERR_UNSUPPORTED, "moe_gmm: K, N, lda, ldb, stride_b must be multiples of 8");
+  REQUIRE(aligned16(A) && aligned16(B), MOE_ERR_UNSUPPORTED, "moe_gmm: A, B not 16-byte aligned");
+  REQUIRE(lda >= K, MOE_ERR_INVALID_ARG, "moe_gmm: lda < K");
+  REQUIRE(trans_b ? ldb >= K : ldb >= N, MOE_ERR_INVALID_ARG, "moe_gmm: ldb too small");
+  REQUIRE(stride_b >= (trans_b ? (int64_t)N * ldb : (int64_t)K * ldb) || E == 1,
+          MOE_ERR_INVALID_ARG, "moe_gmm: stride_b overlaps experts");
+  int outN = N;
+  if (epilogue == MOE_EPI_SWIGLU_FWD) {
+    REQUIRE(N % 16 == 0, MOE_ERR_UNSUPPORTED, "moe_gmm: SWIGLU_FWD needs N = 2F with F %% 8 == 0");
+    REQUIRE(C2 != nullptr && ldc2 >= N / 2 && ldc2 % 8 == 0, MOE_ERR_INVALID_ARG,
+            "moe_gmm: SWIGLU_FWD needs C2 with ldc2 >= F");
+    REQUIRE(c_dtype == MOE_DTYPE_BF16, MOE_ERR_INVALID_ARG, "moe_gmm: SWIGLU_FWD writes bf16 H");
+  }
+  if (epilogue == MOE_EPI_SWIGLU_BWD) {
+    outN = 2 * N;
+    REQUIRE(aux != nullptr && ld_aux >= 2 * N && ld_aux % 8 == 0, MOE_ERR_INVALID_ARG,
+            "moe_gmm: SWIGLU_BWD needs aux = H with ld_aux >= 2N");
+    REQUIRE(partial_sum == nullptr, MOE_ERR_INVALID_ARG,
+            "moe_gmm: SWIGLU_BWD takes no partial sum");
+    REQUIRE(c_dtype == MOE_DTYPE_BF16, MOE_ERR_INVALID_ARG, "moe_gmm: SWIGLU_BWD writes bf16 dH");
+  }
+  REQUIRE(ldc >= outN && ldc % 4 == 0, MOE_ERR_INVALID_ARG, "moe_gmm: ldc too small");
+  REQUIRE(partial_sum == nullptr || (ld_ps >= N && ld_ps % 4 == 0), MOE_ERR_INVALID_ARG,
+          "moe_gmm: ld_ps < N");
+  REQUIRE(partial_sum == nullptr || (const void *)partial_sum != C ||
+              (c_dtype == MOE_DTYPE_F32 && ld_ps == ldc),
+          MOE_ERR_INVALID_ARG, "moe_gmm: in-place partial sum needs fp32 C with ld_ps == ldc");
+  REQUIRE(rows_cap < (1ll << 31), MOE_ERR_UNSUPPORTED, "moe_gmm: more than 2^31 rows");
+  if (rows_cap == 0) return MOE_OK;
+  moe::GmmArgs a{A, lda, B, ldb, stride_b, trans_b, group_offsets, E, rows_cap, K, N, epilogue,
+                 aux, ld_aux, partial_sum, ld_ps, C, c_dtype, ldc, C2, ldc2, dev_status};
+  return moe::launch_gmm(a, (cudaStream_t)stream);
+}
+
+moe_status_t moe_tgmm(const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
+                      const int32_t *group_offsets, int E, int64_t rows_cap, int M, int N,
+                      void *W, int w_dtype, int64_t ldw, int64_t stride_w, int accumulate,
+                      int32_t *dev_status, moe_stream_t stream) {
+  set_error("");
+  REQUIRE(E > 0 && rows_cap >= 0 && M > 0 && N > 0, MOE_ERR_INVALID_ARG,
+          "moe_tgmm: E=%d rows_cap=%lld M=%d N=%d", E, (long long)rows_cap, M, N);
+  REQUIRE(A && B && group_offsets && W, MOE_ERR_INVALID_ARG, "moe_tgmm: null pointer");
+  REQUIRE(w_dtype == MOE_DTYPE_BF16 || w_dtype == MOE_DTYPE_F32, MOE_ERR_INVALID_ARG,
+          "moe_tgmm: bad w_dtype");
+  REQUIRE(!accumulate || w_dtype == MOE_DTYPE_F32, MOE_ERR_INVALID_ARG,
+          "moe_tgmm: accumulate needs fp32 W");
+  REQUIRE(M % 8 == 0 && N % 8 == 0 && lda % 8 == 0 && ldb % 8 == 0, MOE_ERR_UNSUPPORTED,
+          "moe_tgmm: M, N, lda, ldb must be multiples of 8");
+  REQUIRE(aligned16(A) && aligned16(B), MOE_ERR_UNSUPPORTED, "moe_tgmm: A, B not 16-byte aligned");
+  REQUIRE(lda >= M && ldb >= N && ldw >= N && ldw % 4 == 0, MOE_ERR_INVALID_ARG,
+          "moe_tgmm: leading dimension too small");
+  REQUIRE(stride_w >= (int64_t)M * ldw || E == 1, MOE_ERR_INVALID_ARG,
+          "moe_tgmm: stride_w overlaps experts");
+  REQUIRE(rows_cap < (1ll << 31), MOE_ERR_UNSUPPORTED, "moe_tgmm: more than 2^31 rows");
+  moe::TgmmArgs a{A, lda, B, ldb, group_offsets, E, rows_cap, M, N, W, w_dtype, ldw, stride_w,
+                  accumulate, dev_status};
+  return moe::launch_tgmm(a, (cudaStream_t)stream);
+}
+
+moe_status_t moe_combine(const uint16_t *Y, int64_t ldy, const int32_t *flat_to_sorted,
+                         const float *topk_w, int T, int k, int d, uint16_t *out, int64_t ldo,
+                         moe_stream_t stream) {
+  set_error("");
+  REQUIRE(T >= 0 && k > 0 && d > 0, MOE_ERR_INVALID_ARG, "moe_combine: T=%d k=%d d=%d", T, k, d);
+  REQUIRE(k <= 16, MOE_ERR_UNSUPPORTED, "moe_combine: k > 16");
+  REQUIRE(d % 8 == 0 && ldy % 8 == 0 && ldo % 8 == 0, MOE_ERR_UNSUPPORTED,
+          "moe_combine: d, ldy, ldo must be multiples of 8");
+  REQUIRE(ldy >= d && ldo >= d, MOE_ERR_INVALID_ARG, "moe_combine: leading dimension < d");
+  REQUIRE(T == 0 || (Y && flat_to_sorted && out), MOE_ERR_INVALID_ARG, "moe_combine: null pointer");
+  REQUIRE(T == 0 || (aligned16(Y) && aligned16(out)), MOE_ERR_UNSUPPORTED,
+          "moe_combine: Y and out must be 16-byte aligned");
+  return cuda_status(moe::launch_combine(Y, ldy, flat_to_sorted, topk_w, T, k, d, out, ldo,
+                                         (cudaStream_t)stream),
+                     "moe_combine launch");
+}
+
+moe_status_t moe_unpermute_bwd(const uint16_t *d_out, int64_t ld_dout, const uint16_t *Y,
+                               int64_t ldy, const int32_t *flat_to_sorted,
+                               const int32_t *sorted_to_flat, const int32_t *group_offsets,
+                               const float *topk_w, int T, int k, int d, int E,
+                               int64_t rows_cap, uint16_t *dY, int64_t ld_dy, float *d_topk_w,
+                               moe_stream_t stream) {
+  set_error("");
+  REQUIRE(T >= 0 && k > 0 && d > 0 && E > 0 && rows_cap >= 0, MOE_ERR_INVALID_ARG,
+          "moe_unpermute_bwd: T=%d k=%d d=%d E=%d", T, k, d, E);
+  REQUIRE(k <= 16, MOE_ERR_UNSUPPORTED, "moe_unpermute_bwd: k > 16");
+  REQUIRE(d % 8 == 0 && ld_dout % 8 == 0 && ldy % 8 == 0 && ld_dy % 8 == 0, MOE_ERR_UNSUPPORTED,
+          "moe_unpermute_bwd: d and leading dimensions must be multiples of 8");
+  REQUIRE(ld_dout >= d && ldy >= d && ld_dy >= d, MOE_ERR_INVALID_ARG,
+          "moe_unpermute_bwd: leading dimension < d");
+  REQUIRE(rows_cap < (1ll << 31), MOE_ERR_UNSUPPORTED, "moe_unpermute_bwd: more than 2^31 rows");
+  REQUIRE(group_offsets && sorted_to_flat && dY, MOE_ERR_INVALID_ARG,
+          "moe_unpermute_bwd: null pointer");
+  REQUIRE(T == 0 || (d_out && Y && flat_to_sorted && topk_w && d_topk_w), MOE_ERR_INVALID_ARG,
+          "moe_unpermute_bwd: null pointer");
+  REQUIRE(aligned16(dY) && (T == 0 || (aligned16(d_out) && aligned16(Y))), MOE_ERR_UNSUPPORTED,
+          "moe_unpermute_bwd: d_out, Y, dY must be 16-byte aligned");
+  return cuda_status(moe::launch_unpermute_bwd(d_out, ld_dout, Y, ldy, flat_to_sorted,
+                                               sorted_to_flat, group_offsets, topk_w, T, k, d, E,
+                                               rows_cap, dY, ld_dy, d_topk_w,
+                                               (cudaStream_t)stream),
+                     "moe_unpermute_bwd launch");
+}
+
+}  // extern "C"

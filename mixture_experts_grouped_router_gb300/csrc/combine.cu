@@ -1,0 +1,163 @@
+// Routing-weighted combine, its backward, and the dispatch backward.
+//
+// TransformerEngine PR #2912 "[JAX] Add an MoE Block (Layer) that compound
+// router, permutation, groupedGEMM and communication", review thread on
+// _combine_bwd (pure-JAX path):
+//   forward   output[t] = sum_j intermediate[t, j] * w[t, j]
+//   backward  d_intermediate[t, j] = d_output[t] * w[t, j]
+//             d_w[t, j] = sum over hidden of d_output[t] * intermediate[t, j]
+// with intermediate[t, j] = Y[flat_to_sorted[t*k + j]] (the un-sort) and zero
+// gradient on padding rows.  One warp per token; rows move in 16-byte words;
+// sums are fp32 in slot order.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;  // 8 warps = 8 tokens per block
+constexpr int kMaxK = 16;
+
+template <bool kWeighted>
+__global__ void __launch_bounds__(kThreads)
+combine_kernel(const uint16_t *__restrict__ Y, int64_t ldy, const int32_t *__restrict__ f2s,
+               const float *__restrict__ w, int T, int k, int d, uint16_t *__restrict__ out,
+               int64_t ldo) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const int pl = lane < k ? __ldg(f2s + (int64_t)t * k + lane) : -1;
+  const float wl = (kWeighted && lane < k) ? __ldg(w + (int64_t)t * k + lane) : 1.0f;
+  int p[kMaxK];
+  float wj[kMaxK];
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j) {
+    p[j] = __shfl_sync(0xffffffffu, pl, j);
+    wj[j] = __shfl_sync(0xffffffffu, wl, j);
+  }
+  const int nvec = d >> 3;
+  uint4 *dst = reinterpret_cast<uint4 *>(out + (int64_t)t * ldo);
+  for (int i = lane; i < nvec; i += 64) {
+    const bool two = i + 32 < nvec;
+    float acc0[8], acc1[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc0[q] = acc1[q] = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      if (j < k && p[j] >= 0) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(Y + (int64_t)p[j] * ldy);
+        float f[8];
+        bf16x8_to_f32(ld_nc_v4(src + i), f);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc0[q] = fmaf(wj[j], f[q], acc0[q]);
+        if (two) {
+          bf16x8_to_f32(ld_nc_v4(src + i + 32), f);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc1[q] = fmaf(wj[j], f[q], acc1[q]);
+        }
+      }
+    }
+    st_v4(dst + i, f32_to_bf16x8(acc0));
+    if (two) st_v4(dst + i + 32, f32_to_bf16x8(acc1));
+  }
+}
+
+// Part A (blocks < nb_tok): one warp per token.  Part B: zero dY on padding
+// rows, 32 rows of sorted_to_flat per warp.
+__global__ void __launch_bounds__(kThreads)
+unpermute_bwd_kernel(const uint16_t *__restrict__ dout, int64_t ld_dout,
+                     const uint16_t *__restrict__ Y, int64_t ldy,
+                     const int32_t *__restrict__ f2s, const int32_t *__restrict__ s2f,
+                     const int32_t *__restrict__ offsets, const float *__restrict__ w, int T,
+                     int k, int d, int E, int64_t rows_cap, uint16_t *__restrict__ dY,
+                     int64_t ld_dy, float *__restrict__ dw, int nb_tok) {
+  const int lane = threadIdx.x & 31;
+  const int wib = threadIdx.x >> 5;
+  const int nvec = d >> 3;
+  if ((int)blockIdx.x < nb_tok) {
+    const int t = blockIdx.x * (kThreads / 32) + wib;
+    if (t >= T) return;
+    int pl = lane < k ? __ldg(f2s + (int64_t)t * k + lane) : -1;
+    if (pl >= rows_cap) pl = -1;
+    const float wl = lane < k ? __ldg(w + (int64_t)t * k + lane) : 0.f;
+    int p[kMaxK];
+    float wj[kMaxK], dot[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      p[j] = __shfl_sync(0xffffffffu, pl, j);
+      wj[j] = __shfl_sync(0xffffffffu, wl, j);
+      dot[j] = 0.f;
+    }
+    const uint4 *g = reinterpret_cast<const uint4 *>(dout + (int64_t)t * ld_dout);
+    for (int i = lane; i < nvec; i += 32) {
+      float gf[8];
+      bf16x8_to_f32(ld_nc_v4(g + i), gf);
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) {
+        if (j < k && p[j] >= 0) {
+          float yf[8], o[8];
+          bf16x8_to_f32(ld_nc_v4(reinterpret_cast<const uint4 *>(Y + (int64_t)p[j] * ldy) + i), yf);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            dot[j] = fmaf(gf[q], yf[q], dot[j]);
+            o[q] = wj[j] * gf[q];
+          }
+          st_v4(reinterpret_cast<uint4 *>(dY + (int64_t)p[j] * ld_dy) + i, f32_to_bf16x8(o));
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      if (j < k) {
+        const float s = warp_sum(dot[j]);
+        if (lane == 0) dw[(int64_t)t * k + j] = p[j] >= 0 ? s : 0.f;
+      }
+    }
+  } else {
+    const int64_t wg = (int64_t)(blockIdx.x - nb_tok) * (kThreads / 32) + wib;
+    const int64_t R = min((int64_t)__ldg(offsets + E), rows_cap);
+    const int64_t p0 = wg * 32;
+    if (p0 >= R) return;
+    const int64_t pr = p0 + lane;
+    const bool pad = pr < R && __ldg(s2f + pr) < 0;
+    uint32_t m = __ballot_sync(0xffffffffu, pad);
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    while (m) {
+      const int bit = __ffs(m) - 1;
+      m &= m - 1;
+      uint4 *dst = reinterpret_cast<uint4 *>(dY + (p0 + bit) * ld_dy);
+      for (int i = lane; i < nvec; i += 32) st_v4(dst + i, z);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const uint16_t *Y, int64_t ldy, const int32_t *f2s, const float *w,
+                           int T, int k, int d, uint16_t *out, int64_t ldo, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int blocks = (T + kThreads / 32 - 1) / (kThreads / 32);
+  if (w != nullptr)
+    combine_kernel<true><<<blocks, kThreads, 0, s>>>(Y, ldy, f2s, w, T, k, d, out, ldo);
+  else
+    combine_kernel<false><<<blocks, kThreads, 0, s>>>(Y, ldy, f2s, w, T, k, d, out, ldo);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_unpermute_bwd(const uint16_t *dout, int64_t ld_dout, const uint16_t *Y,
+                                 int64_t ldy, const int32_t *f2s, const int32_t *s2f,
+                                 const int32_t *offsets, const float *w, int T, int k, int d,
+                                 int E, int64_t rows_cap, uint16_t *dY, int64_t ld_dy,
+                                 float *dw, cudaStream_t s) {
+  const int wpb = kThreads / 32;
+  const int nb_tok = (T + wpb - 1) / wpb;
+  const int64_t pad_warps = (rows_cap + 31) / 32;
+  const int nb_pad = (int)((pad_warps + wpb - 1) / wpb);
+  if (nb_tok + nb_pad == 0) return cudaSuccess;
+  unpermute_bwd_kernel<<<nb_tok + nb_pad, kThreads, 0, s>>>(dout, ld_dout, Y, ldy, f2s, s2f,
+                                                            offsets, w, T, k, d, E, rows_cap, dY,
+                                                            ld_dy, dw, nb_tok);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,58 @@
+// Host-side launchers shared between the C-ABI layer (api.cu) and the kernel
+// translation units.  Arguments are validated by api.cu before these run.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_gb300.h"
+
+namespace moe {
+
+void set_error(const char *fmt, ...);
+int num_sms();
+
+// route.cu
+cudaError_t launch_route_topk(const float *logits, int64_t ld, int T, int E, int k, int score_fn,
+                              int renorm, int32_t *idx, float *w, cudaStream_t s);
+
+// permute.cu
+size_t permute_workspace_bytes(int T, int E);
+cudaError_t launch_permute(const uint16_t *x, int64_t ldx, const int32_t *topk_idx, int T, int d,
+                           int E, int k, int align, int capacity, uint16_t *xs, int64_t ld_xs,
+                           int64_t rows_cap, int32_t *group_sizes, int32_t *kept,
+                           int32_t *offsets, int32_t *s2f, int32_t *f2s, int32_t *counts_ws,
+                           int32_t *dev_status, cudaStream_t s);
+
+// combine.cu
+cudaError_t launch_combine(const uint16_t *Y, int64_t ldy, const int32_t *f2s, const float *w,
+                           int T, int k, int d, uint16_t *out, int64_t ldo, cudaStream_t s);
+cudaError_t launch_unpermute_bwd(const uint16_t *dout, int64_t ld_dout, const uint16_t *Y,
+                                 int64_t ldy, const int32_t *f2s, const int32_t *s2f,
+                                 const int32_t *offsets, const float *w, int T, int k, int d,
+                                 int E, int64_t rows_cap, uint16_t *dY, int64_t ld_dy,
+                                 float *dw, cudaStream_t s);
+
+// gmm_sm103.cu
+struct GmmArgs {
+  const uint16_t *A; int64_t lda;
+  const uint16_t *B; int64_t ldb; int64_t stride_b; int trans_b;
+  const int32_t *offsets; int E; int64_t rows_cap; int K; int N;
+  int epilogue;
+  const uint16_t *aux; int64_t ld_aux;
+  const float *ps; int64_t ld_ps;
+  void *C; int c_dtype; int64_t ldc;
+  uint16_t *C2; int64_t ldc2;
+  int32_t *dev_status;
+};
+moe_status_t launch_gmm(const GmmArgs &a, cudaStream_t s);
+
+struct TgmmArgs {
+  const uint16_t *A; int64_t lda;
+  const uint16_t *B; int64_t ldb;
+  const int32_t *offsets; int E; int64_t rows_cap; int M; int N;
+  void *W; int w_dtype; int64_t ldw; int64_t stride_w; int accumulate;
+  int32_t *dev_status;
+};
+moe_status_t launch_tgmm(const TgmmArgs &a, cudaStream_t s);
+
+}  // namespace moe

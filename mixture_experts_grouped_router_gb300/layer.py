@@ -1,0 +1,132 @@
+"""The MoE expert layer, forward and backward, as a sequence of C-ABI calls.
+
+This module only allocates device buffers (through PyTorch) and issues the
+library calls in order on the current stream; every arithmetic step runs in
+libmoe_gb300.so.  The sequence follows the single-VJP MoE block of
+TransformerEngine PR #2912 ("[JAX] Add an MoE Block (Layer) that compound
+router, permutation, groupedGEMM and communication", sequence diagram),
+without the expert-parallel all-to-all:
+
+forward   route_topk -> permute -> gmm(up, SwiGLU epilogue) -> gmm(down) -> combine
+backward  unpermute_bwd -> gmm(dgrad down, SwiGLU-bwd epilogue) -> tgmm(dWo)
+          -> gmm(dgrad up) -> tgmm(dWi) -> combine without weights (dispatch bwd)
+
+With num_chunks > 1 the up-projection runs as num_chunks K-chunks of d_model
+accumulating into an fp32 partial sum in place (MaxText PR #4295, "Overlap
+moe comms with collective matmul", Description), SwiGLU fused into the last
+chunk; in the backward each chunk's dgrad and tgmm work on their own slice.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import torch
+
+from . import _lib as L
+
+
+@dataclasses.dataclass
+class LayerShape:
+    T: int
+    d: int
+    f: int
+    E: int
+    k: int
+    score_fn: int = L.SCORE_SOFTMAX
+    renorm: int = 1
+    align: int = 0
+    capacity: int = 0
+    num_chunks: int = 1
+
+
+class MoEBuffers:
+    """Device buffers of one layer instance, allocated once and reused every step."""
+
+    def __init__(self, s: LayerShape, device="cuda", dw_dtype=torch.bfloat16):
+        self.s = s
+        T, d, f, E, k = s.T, s.d, s.f, s.E, s.k
+        self.rows_cap = L.moe_rows_cap(T, E, k, s.align)
+        R = self.rows_cap
+        bf, i32, f32 = torch.bfloat16, torch.int32, torch.float32
+        dev = device
+        self.topk_idx = torch.empty(T, k, dtype=i32, device=dev)
+        self.topk_w = torch.empty(T, k, dtype=f32, device=dev)
+        self.xs = torch.empty(R, d, dtype=bf, device=dev)
+        self.group_sizes = torch.empty(E, dtype=i32, device=dev)
+        self.kept_counts = torch.empty(E, dtype=i32, device=dev)
+        self.group_offsets = torch.empty(E + 1, dtype=i32, device=dev)
+        self.s2f = torch.empty(R, dtype=i32, device=dev)
+        self.f2s = torch.empty(T * k, dtype=i32, device=dev)
+        self.ws = torch.empty(L.moe_permute_workspace_bytes(T, E), dtype=torch.uint8, device=dev)
+        self.h = torch.empty(R, 2 * f, dtype=bf, device=dev)
+        self.act = torch.empty(R, f, dtype=bf, device=dev)
+        self.y = torch.empty(R, d, dtype=bf, device=dev)
+        self.out = torch.empty(T, d, dtype=bf, device=dev)
+        self.p = torch.empty(R, 2 * f, dtype=f32, device=dev) if s.num_chunks > 1 else None
+        # backward
+        self.dy = torch.empty(R, d, dtype=bf, device=dev)
+        self.d_topk_w = torch.empty(T, k, dtype=f32, device=dev)
+        self.dh = torch.empty(R, 2 * f, dtype=bf, device=dev)
+        self.dxs = torch.empty(R, d, dtype=bf, device=dev)
+        self.dx = torch.empty(T, d, dtype=bf, device=dev)
+        self.dwi = torch.empty(E, d, 2 * f, dtype=dw_dtype, device=dev)
+        self.dwo = torch.empty(E, f, d, dtype=dw_dtype, device=dev)
+        self.dev_status = torch.zeros(1, dtype=i32, device=dev)
+
+
+def forward(b: MoEBuffers, x, logits, wi, wo, stream=None):
+    """x bf16 [T,d], logits fp32 [T,E], wi bf16 [E,d,2f] ([wi_0 | wi_1]), wo bf16 [E,f,d]."""
+    s = b.s
+    L.moe_route_topk(logits, s.k, s.score_fn, s.renorm, b.topk_idx, b.topk_w, stream)
+    L.moe_permute(x, b.topk_idx, s.E, s.align, s.capacity, b.xs, b.group_sizes, b.kept_counts,
+                  b.group_offsets, b.s2f, b.f2s, b.ws, b.dev_status, stream)
+    if s.num_chunks <= 1:
+        L.moe_gmm(b.xs, wi, 0, b.group_offsets, b.h, L.EPI_SWIGLU_FWD, C2=b.act,
+                  dev_status=b.dev_status, stream=stream)
+    else:
+        dc = s.d // s.num_chunks
+        for c in range(s.num_chunks):
+            a_c = b.xs[:, c * dc:(c + 1) * dc]
+            w_c = wi[:, c * dc:(c + 1) * dc, :]
+            last = c == s.num_chunks - 1
+            ps = None if c == 0 else b.p
+            if last:
+                L.moe_gmm(a_c, w_c, 0, b.group_offsets, b.h, L.EPI_SWIGLU_FWD, partial_sum=ps,
+                          C2=b.act, dev_status=b.dev_status, stream=stream)
+            else:
+                L.moe_gmm(a_c, w_c, 0, b.group_offsets, b.p, L.EPI_NONE, partial_sum=ps,
+                          dev_status=b.dev_status, stream=stream)
+    L.moe_gmm(b.act, wo, 0, b.group_offsets, b.y, L.EPI_NONE, dev_status=b.dev_status,
+              stream=stream)
+    L.moe_combine(b.y, b.f2s, b.topk_w, b.out, s.k, stream)
+    return b.out
+
+
+def backward(b: MoEBuffers, dout, wi, wo, stream=None):
+    """dout bf16 [T,d] -> (dx, dwi, dwo, d_topk_w) in b's buffers."""
+    s = b.s
+    L.moe_unpermute_bwd(dout, b.y, b.f2s, b.s2f, b.group_offsets, b.topk_w, b.dy, b.d_topk_w,
+                        stream)
+    # dAct = dY . wo^T, fused with the SwiGLU backward into dH = [dgate | dup]
+    L.moe_gmm(b.dy, wo, 1, b.group_offsets, b.dh, L.EPI_SWIGLU_BWD, aux=b.h,
+              dev_status=b.dev_status, stream=stream)
+    L.moe_tgmm(b.act, b.dy, b.group_offsets, b.dwo, dev_status=b.dev_status, stream=stream)
+    if s.num_chunks <= 1:
+        L.moe_gmm(b.dh, wi, 1, b.group_offsets, b.dxs, L.EPI_NONE, dev_status=b.dev_status,
+                  stream=stream)
+        L.moe_tgmm(b.xs, b.dh, b.group_offsets, b.dwi, dev_status=b.dev_status, stream=stream)
+    else:
+        dc = s.d // s.num_chunks
+        for c in range(s.num_chunks):
+            sl = slice(c * dc, (c + 1) * dc)
+            L.moe_gmm(b.dh, wi[:, sl, :], 1, b.group_offsets, b.dxs[:, sl], L.EPI_NONE,
+                      dev_status=b.dev_status, stream=stream)
+            L.moe_tgmm(b.xs[:, sl], b.dh, b.group_offsets, b.dwi[:, sl, :],
+                       dev_status=b.dev_status, stream=stream)
+    L.moe_combine(b.dxs, b.f2s, None, b.dx, s.k, stream)
+    return b.dx, b.dwi, b.dwo, b.d_topk_w
+
+
+def gemm_flops(m_kept: int, d: int, f: int) -> int:
+    """Algorithmic FLOPs of the expert GEMMs, forward + backward (18 M d f)."""
+    return 18 * m_kept * d * f

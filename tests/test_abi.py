@@ -1,0 +1,114 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every entry point include/moe_gb300.h declares, and rejects bad arguments
+with status codes before anything is launched."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_gb300.h")
+PKG = os.path.join(ROOT, "mixture_experts_grouped_router_gb300")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    import __graft_entry__
+    __graft_entry__._build_module().build()
+    from mixture_experts_grouped_router_gb300 import _lib
+    return _lib
+
+
+def test_header_declares_the_six_calls():
+    names = _declared()
+    for n in ("moe_route_topk", "moe_permute", "moe_gmm", "moe_tgmm", "moe_combine",
+              "moe_unpermute_bwd"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    lib = ctypes.CDLL(L._build.LIB_PATH)
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert set(_declared()) <= set(L.EXPORTED) | set(_declared())
+
+
+def test_size_queries(L):
+    assert L.moe_rows_cap(32768, 64, 1, 128) == 32768 + 64 * 127
+    assert L.moe_rows_cap(100, 8, 2, 0) == 200
+    assert L.moe_rows_cap(100, 8, 2, 1) == 200
+    assert L.LIB.moe_rows_cap(-1, 8, 2, 0) == -1
+    assert L.moe_permute_workspace_bytes(4096, 64) >= 4 * 64 * 4
+    assert L.LIB.moe_version() >= 100
+
+
+def _ptr(v=16):
+    return ctypes.c_void_p(v)
+
+
+def test_validation_errors_need_no_gpu(L):
+    lib = L.LIB
+    # k > E
+    st = lib.moe_route_topk(_ptr(), 8, 10, 8, 9, 0, 1, _ptr(), _ptr(), None)
+    assert st == L.MOE_ERR_INVALID_ARG and "k=9" in L.last_error()
+    # E above the router's limit
+    st = lib.moe_route_topk(_ptr(), 300, 10, 300, 2, 0, 1, _ptr(), _ptr(), None)
+    assert st == L.MOE_ERR_UNSUPPORTED
+    # bad score function
+    st = lib.moe_route_topk(_ptr(), 8, 10, 8, 2, 7, 1, _ptr(), _ptr(), None)
+    assert st == L.MOE_ERR_INVALID_ARG
+    # permute: rows_cap below the worst case
+    st = lib.moe_permute(_ptr(), 64, _ptr(), 100, 64, 8, 2, 4, 0, _ptr(), 64, 100, _ptr(), _ptr(),
+                         _ptr(), _ptr(), _ptr(), _ptr(), 1 << 20, None, None)
+    assert st == L.MOE_ERR_INVALID_ARG and "rows_cap" in L.last_error()
+    # permute: d not a multiple of 8
+    st = lib.moe_permute(_ptr(), 64, _ptr(), 100, 60, 8, 2, 0, 0, _ptr(), 64, 200, _ptr(), _ptr(),
+                         _ptr(), _ptr(), _ptr(), _ptr(), 1 << 20, None, None)
+    assert st == L.MOE_ERR_UNSUPPORTED
+    # permute: workspace too small
+    st = lib.moe_permute(_ptr(), 64, _ptr(), 100, 64, 8, 2, 0, 0, _ptr(), 64, 200, _ptr(), _ptr(),
+                         _ptr(), _ptr(), _ptr(), _ptr(), 4, None, None)
+    assert st == L.MOE_ERR_INVALID_ARG and "workspace" in L.last_error()
+    # gmm: N not a multiple of 8
+    st = lib.moe_gmm(_ptr(), 64, _ptr(), 12, 64 * 12, 0, _ptr(), 1, 100, 64, 12, 0, None, 0, None,
+                     0, _ptr(), 0, 12, None, 0, None, None)
+    assert st == L.MOE_ERR_UNSUPPORTED
+    # gmm: SWIGLU_FWD without C2
+    st = lib.moe_gmm(_ptr(), 64, _ptr(), 64, 64 * 64, 0, _ptr(), 1, 100, 64, 64, 1, None, 0, None,
+                     0, _ptr(), 0, 64, None, 0, None, None)
+    assert st == L.MOE_ERR_INVALID_ARG
+    # gmm: misaligned A
+    st = lib.moe_gmm(_ptr(18), 64, _ptr(), 64, 64 * 64, 0, _ptr(), 1, 100, 64, 64, 0, None, 0,
+                     None, 0, _ptr(), 0, 64, None, 0, None, None)
+    assert st == L.MOE_ERR_UNSUPPORTED
+    # gmm: in-place partial sum with bf16 C
+    st = lib.moe_gmm(_ptr(), 64, _ptr(), 64, 64 * 64, 0, _ptr(), 1, 100, 64, 64, 0, None, 0,
+                     _ptr(32), 64, _ptr(32), 0, 64, None, 0, None, None)
+    assert st == L.MOE_ERR_INVALID_ARG
+    # tgmm: accumulate into bf16
+    st = lib.moe_tgmm(_ptr(), 64, _ptr(), 64, _ptr(), 2, 100, 64, 64, _ptr(), 0, 64, 64 * 64, 1,
+                      None, None)
+    assert st == L.MOE_ERR_INVALID_ARG
+    # combine: k above the limit
+    st = lib.moe_combine(_ptr(), 64, _ptr(), _ptr(), 10, 17, 64, _ptr(), 64, None)
+    assert st == L.MOE_ERR_UNSUPPORTED
+    # unpermute_bwd: null dY
+    st = lib.moe_unpermute_bwd(_ptr(), 64, _ptr(), 64, _ptr(), _ptr(), _ptr(), _ptr(), 10, 2, 64,
+                               4, 20, None, 64, _ptr(), None)
+    assert st == L.MOE_ERR_INVALID_ARG
+
+
+def test_product_path_never_touches_the_oracle():
+    for dirpath, _, files in os.walk(PKG):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                src = open(os.path.join(dirpath, fn)).read()
+                assert "oracle" not in src.replace("the oracle", ""), fn
+                assert "moe_ref" not in src, fn

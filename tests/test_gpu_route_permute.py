@@ -1,0 +1,139 @@
+"""GPU parity of moe_route_topk and moe_permute against the oracle: indices,
+group layout and permuted rows bit-exact; fp32 weights to 1e-6."""
+import numpy as np
+import pytest
+import torch
+
+import moe_synth
+from gpu_helpers import W_ATOL, dev_bf16
+from oracle import moe_ref
+
+pytestmark = pytest.mark.gpu
+
+L = pytest.importorskip("mixture_experts_grouped_router_gb300._lib")
+
+
+def _logits(rng, T, E, kind):
+    if kind == "normal":
+        return rng.standard_normal((T, E)).astype(np.float32)
+    if kind == "ties":
+        return rng.integers(-2, 3, size=(T, E)).astype(np.float32)
+    if kind == "equal":
+        return np.zeros((T, E), np.float32)
+    if kind == "one_expert":   # every token prefers expert E-1 by far
+        lg = rng.standard_normal((T, E)).astype(np.float32)
+        lg[:, -1] += 100.0
+        return lg
+    if kind == "skew":
+        return (rng.standard_normal((T, E)) + np.linspace(-4, 4, E)).astype(np.float32)
+    raise ValueError(kind)
+
+
+ROUTE_CASES = [
+    (1, 8, 1, 0, 1, "normal"), (257, 8, 2, 0, 1, "normal"), (300, 32, 8, 1, 1, "normal"),
+    (513, 64, 1, 0, 0, "skew"), (100, 256, 16, 1, 0, "normal"), (77, 5, 5, 0, 1, "ties"),
+    (64, 33, 3, 1, 1, "equal"), (129, 128, 6, 0, 0, "ties"), (1000, 160, 4, 1, 1, "normal"),
+]
+
+
+@pytest.mark.parametrize("case", ROUTE_CASES)
+def test_route_topk(case):
+    T, E, k, sfn, ren, kind = case
+    rng = np.random.default_rng(T * 7 + E)
+    lg = _logits(rng, T, E, kind)
+    idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, k, dtype=torch.float32, device="cuda")
+    L.moe_route_topk(torch.from_numpy(lg).cuda(), k, sfn, ren, idx, w)
+    torch.cuda.synchronize()
+    ridx, rw = moe_ref.route_topk(lg, k, sfn, ren)
+    assert (idx.cpu().numpy() == ridx).all()
+    np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=0, atol=W_ATOL)
+
+
+def test_route_topk_strided_logits():
+    rng = np.random.default_rng(1)
+    full = rng.standard_normal((50, 40)).astype(np.float32)
+    lg = torch.from_numpy(full).cuda()[:, :24]
+    idx = torch.empty(50, 4, dtype=torch.int32, device="cuda")
+    w = torch.empty(50, 4, dtype=torch.float32, device="cuda")
+    L.moe_route_topk(lg, 4, 0, 1, idx, w)
+    ridx, rw = moe_ref.route_topk(full[:, :24], 4, 0, 1)
+    assert (idx.cpu().numpy() == ridx).all()
+    np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=0, atol=W_ATOL)
+
+
+def run_permute(idx_np, E, align, cap, d=64, seed=0, x_bits=None):
+    T, k = idx_np.shape
+    rng = np.random.default_rng(seed)
+    if x_bits is None:
+        x_bits = moe_synth.bf16_bits(rng.standard_normal((T, d)).astype(np.float32))
+    rows_cap = L.moe_rows_cap(T, E, k, align)
+    dev = "cuda"
+    x = dev_bf16(x_bits)
+    xs = torch.full((rows_cap, d), float("nan"), dtype=torch.bfloat16, device=dev)
+    gs = torch.empty(E, dtype=torch.int32, device=dev)
+    kc = torch.empty(E, dtype=torch.int32, device=dev)
+    off = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    s2f = torch.full((rows_cap,), 12345, dtype=torch.int32, device=dev)
+    f2s = torch.full((T * k,), 12345, dtype=torch.int32, device=dev)
+    ws = torch.empty(L.moe_permute_workspace_bytes(T, E), dtype=torch.uint8, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    L.moe_permute(x, torch.from_numpy(idx_np.astype(np.int32)).to(dev), E, align, cap, xs, gs, kc,
+                  off, s2f, f2s, ws, st)
+    torch.cuda.synchronize()
+    return dict(x_bits=x_bits, xs=xs, gs=gs, kc=kc, off=off, s2f=s2f, f2s=f2s, st=st,
+                rows_cap=rows_cap)
+
+
+def check_permute(r, idx_np, E, align, cap):
+    T, k = idx_np.shape
+    lay = moe_ref.permute_layout(idx_np, E, align, cap)
+    R = lay["R"]
+    assert int(r["st"].item()) == 0
+    assert r["gs"].cpu().numpy().tolist() == lay["group_sizes"].tolist()
+    assert r["kc"].cpu().numpy().tolist() == lay["kept_counts"].tolist()
+    assert r["off"].cpu().numpy().tolist() == lay["group_offsets"].tolist()
+    s2f = r["s2f"].cpu().numpy()
+    assert s2f[:R].tolist() == lay["sorted_to_flat"].tolist()
+    assert (s2f[R:] == -1).all()
+    assert r["f2s"].cpu().numpy().tolist() == lay["flat_to_sorted"].tolist()
+    # permuted rows: exact copies of x (compared bitwise), padding rows zero
+    xs_bits = r["xs"][:R].view(torch.int16).cpu().numpy().astype(np.uint16)
+    ref_rows = np.zeros((R, r["x_bits"].shape[1]), np.uint16)
+    ok = lay["sorted_to_flat"] >= 0
+    ref_rows[ok] = r["x_bits"][lay["sorted_to_flat"][ok] // k]
+    assert (xs_bits == ref_rows).all()
+
+
+PERMUTE_CASES = [
+    # T, E, k, align, cap, logits kind
+    (1, 4, 1, 0, 0, "normal"), (300, 8, 2, 0, 0, "normal"), (1025, 8, 2, 0, 0, "normal"),
+    (3000, 32, 8, 0, 0, "normal"), (2500, 64, 1, 128, 40, "skew"), (2049, 16, 4, 8, 0, "ties"),
+    (777, 8, 2, 1, 0, "one_expert"), (1500, 8, 2, 16, 100, "one_expert"),
+    (4097, 256, 8, 4, 50, "skew"), (512, 6, 3, 2, 0, "equal"), (2000, 64, 2, 128, 0, "skew"),
+]
+
+
+@pytest.mark.parametrize("case", PERMUTE_CASES)
+def test_permute(case):
+    T, E, k, align, cap, kind = case
+    rng = np.random.default_rng(T + E)
+    idx, _ = moe_ref.route_topk(_logits(rng, T, E, kind), k, 0, 1)
+    r = run_permute(idx, E, align, cap, d=72, seed=T)
+    check_permute(r, idx, E, align, cap)
+
+
+def test_permute_no_tokens():
+    idx = np.zeros((0, 2), np.int32)
+    r = run_permute(idx, 4, 8, 0, d=16)
+    assert r["gs"].cpu().numpy().tolist() == [0, 0, 0, 0]
+    assert r["off"].cpu().numpy().tolist() == [0, 0, 0, 0, 0]
+    assert (r["s2f"].cpu().numpy() == -1).all()
+
+
+def test_permute_bad_expert_sets_status_without_fault():
+    idx = np.array([[0, 1], [2, 9], [1, 1]], np.int32)   # 9 out of range; token 2 repeats 1
+    r = run_permute(idx, 4, 0, 0, d=16)
+    assert int(r["st"].item()) == L.MOE_ERR_DEVICE
+    f2s = r["f2s"].cpu().numpy()
+    assert f2s[3] == -1 and f2s[5] == -1
