@@ -151,7 +151,8 @@ moe_status_t moe_permute(const uint16_t *x, int64_t ldx, const int32_t *topk_idx
  *   partial_sum fp32 [rows_cap, ld_ps >= N] or NULL (NONE / SWIGLU_FWD only);
  *             may alias C when c_dtype is fp32 and ld_ps == ldc (in place)
  *   C         [rows_cap, ldc] (ldc >= N, or >= 2F for SWIGLU_BWD)
- * Only rows r < group_offsets[E] are written.
+ * Only rows r < group_offsets[E] are written.  E <= 256; A, B, C, C2, aux and
+ * partial_sum 16-byte aligned; SWIGLU_FWD needs trans_b == 0.
  */
 moe_status_t moe_gmm(const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
                      int64_t stride_b, int trans_b, const int32_t *group_offsets, int E,
@@ -167,7 +168,7 @@ moe_status_t moe_gmm(const uint16_t *A, int64_t lda, const uint16_t *B, int64_t 
  * expert with no rows gets exact zeros (or keeps W_e when accumulating).
  *   A  bf16 [rows_cap, lda >= M];  B  bf16 [rows_cap, ldb >= N];  M, N % 8 == 0
  *   W  expert e at W + e*stride_w, [M, ldw >= N] row-major, w_dtype bf16 or
- *      fp32 (accumulate requires fp32)
+ *      fp32 (accumulate requires fp32); E <= 256; A, B, W 16-byte aligned
  */
 moe_status_t moe_tgmm(const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
                       const int32_t *group_offsets, int E, int64_t rows_cap, int M, int N,

@@ -140,7 +140,10 @@ moe_status_t moe_gmm(const uint16_t *A, int64_t lda, const uint16_t *B, int64_t 
   REQUIRE(A && B && group_offsets && C, MOE_ERR_INVALID_ARG, "moe_gmm: null pointer");
   REQUIRE(K % 8 == 0 && N % 8 == 0 && lda % 8 == 0 && ldb % 8 == 0 && stride_b % 8 == 0,
           MOE_ERR_UNSUPPORTED, "moe_gmm: K, N, lda, ldb, stride_b must be multiples of 8");
-  REQUIRE(aligned16(A) && aligned16(B), MOE_ERR_UNSUPPORTED, "moe_gmm: A, B not 16-byte aligned");
+  REQUIRE(E <= 256, MOE_ERR_UNSUPPORTED, "moe_gmm: E=%d > 256", E);
+  REQUIRE(aligned16(A) && aligned16(B) && aligned16(C) && aligned16(C2) && aligned16(aux) &&
+              aligned16(partial_sum),
+          MOE_ERR_UNSUPPORTED, "moe_gmm: A, B, C, C2, aux and partial_sum must be 16-byte aligned");
   REQUIRE(lda >= K, MOE_ERR_INVALID_ARG, "moe_gmm: lda < K");
   REQUIRE(trans_b ? ldb >= K : ldb >= N, MOE_ERR_INVALID_ARG, "moe_gmm: ldb too small");
   REQUIRE(stride_b >= (trans_b ? (int64_t)N * ldb : (int64_t)K * ldb) || E == 1,
@@ -151,6 +154,7 @@ moe_status_t moe_gmm(const uint16_t *A, int64_t lda, const uint16_t *B, int64_t 
     REQUIRE(C2 != nullptr && ldc2 >= N / 2 && ldc2 % 8 == 0, MOE_ERR_INVALID_ARG,
             "moe_gmm: SWIGLU_FWD needs C2 with ldc2 >= F");
     REQUIRE(c_dtype == MOE_DTYPE_BF16, MOE_ERR_INVALID_ARG, "moe_gmm: SWIGLU_FWD writes bf16 H");
+    REQUIRE(!trans_b, MOE_ERR_UNSUPPORTED, "moe_gmm: SWIGLU_FWD needs trans_b = 0");
   }
   if (epilogue == MOE_EPI_SWIGLU_BWD) {
     outN = 2 * N;
@@ -187,7 +191,9 @@ moe_status_t moe_tgmm(const uint16_t *A, int64_t lda, const uint16_t *B, int64_t
           "moe_tgmm: accumulate needs fp32 W");
   REQUIRE(M % 8 == 0 && N % 8 == 0 && lda % 8 == 0 && ldb % 8 == 0, MOE_ERR_UNSUPPORTED,
           "moe_tgmm: M, N, lda, ldb must be multiples of 8");
-  REQUIRE(aligned16(A) && aligned16(B), MOE_ERR_UNSUPPORTED, "moe_tgmm: A, B not 16-byte aligned");
+  REQUIRE(E <= 256, MOE_ERR_UNSUPPORTED, "moe_tgmm: E=%d > 256", E);
+  REQUIRE(aligned16(A) && aligned16(B) && aligned16(W), MOE_ERR_UNSUPPORTED,
+          "moe_tgmm: A, B and W must be 16-byte aligned");
   REQUIRE(lda >= M && ldb >= N && ldw >= N && ldw % 4 == 0, MOE_ERR_INVALID_ARG,
           "moe_tgmm: leading dimension too small");
   REQUIRE(stride_w >= (int64_t)M * ldw || E == 1, MOE_ERR_INVALID_ARG,

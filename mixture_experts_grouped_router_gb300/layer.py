@@ -74,15 +74,25 @@ class MoEBuffers:
         self.dev_status = torch.zeros(1, dtype=i32, device=dev)
 
 
-def forward(b: MoEBuffers, x, logits, wi, wo, stream=None):
-    """x bf16 [T,d], logits fp32 [T,E], wi bf16 [E,d,2f] ([wi_0 | wi_1]), wo bf16 [E,f,d]."""
+def _noop(_name):
+    pass
+
+
+def forward(b: MoEBuffers, x, logits, wi, wo, stream=None, mark=_noop):
+    """x bf16 [T,d], logits fp32 [T,E], wi bf16 [E,d,2f] ([wi_0 | wi_1]), wo bf16 [E,f,d].
+
+    ``mark(name)`` is called after each library call (the benchmark records a
+    CUDA event there)."""
     s = b.s
     L.moe_route_topk(logits, s.k, s.score_fn, s.renorm, b.topk_idx, b.topk_w, stream)
+    mark("route")
     L.moe_permute(x, b.topk_idx, s.E, s.align, s.capacity, b.xs, b.group_sizes, b.kept_counts,
                   b.group_offsets, b.s2f, b.f2s, b.ws, b.dev_status, stream)
+    mark("permute")
     if s.num_chunks <= 1:
         L.moe_gmm(b.xs, wi, 0, b.group_offsets, b.h, L.EPI_SWIGLU_FWD, C2=b.act,
                   dev_status=b.dev_status, stream=stream)
+        mark("gmm_up_swiglu")
     else:
         dc = s.d // s.num_chunks
         for c in range(s.num_chunks):
@@ -93,38 +103,59 @@ def forward(b: MoEBuffers, x, logits, wi, wo, stream=None):
             if last:
                 L.moe_gmm(a_c, w_c, 0, b.group_offsets, b.h, L.EPI_SWIGLU_FWD, partial_sum=ps,
                           C2=b.act, dev_status=b.dev_status, stream=stream)
+                mark("gmm_up_chunk_swiglu")
             else:
                 L.moe_gmm(a_c, w_c, 0, b.group_offsets, b.p, L.EPI_NONE, partial_sum=ps,
                           dev_status=b.dev_status, stream=stream)
+                mark("gmm_up_chunk")
     L.moe_gmm(b.act, wo, 0, b.group_offsets, b.y, L.EPI_NONE, dev_status=b.dev_status,
               stream=stream)
+    mark("gmm_down")
     L.moe_combine(b.y, b.f2s, b.topk_w, b.out, s.k, stream)
+    mark("combine")
     return b.out
 
 
-def backward(b: MoEBuffers, dout, wi, wo, stream=None):
+def backward(b: MoEBuffers, dout, wi, wo, stream=None, mark=_noop):
     """dout bf16 [T,d] -> (dx, dwi, dwo, d_topk_w) in b's buffers."""
     s = b.s
     L.moe_unpermute_bwd(dout, b.y, b.f2s, b.s2f, b.group_offsets, b.topk_w, b.dy, b.d_topk_w,
                         stream)
+    mark("unpermute_bwd")
     # dAct = dY . wo^T, fused with the SwiGLU backward into dH = [dgate | dup]
     L.moe_gmm(b.dy, wo, 1, b.group_offsets, b.dh, L.EPI_SWIGLU_BWD, aux=b.h,
               dev_status=b.dev_status, stream=stream)
+    mark("gmm_dgrad_down_swiglu_bwd")
     L.moe_tgmm(b.act, b.dy, b.group_offsets, b.dwo, dev_status=b.dev_status, stream=stream)
+    mark("tgmm_dwo")
     if s.num_chunks <= 1:
         L.moe_gmm(b.dh, wi, 1, b.group_offsets, b.dxs, L.EPI_NONE, dev_status=b.dev_status,
                   stream=stream)
+        mark("gmm_dgrad_up")
         L.moe_tgmm(b.xs, b.dh, b.group_offsets, b.dwi, dev_status=b.dev_status, stream=stream)
+        mark("tgmm_dwi")
     else:
         dc = s.d // s.num_chunks
         for c in range(s.num_chunks):
             sl = slice(c * dc, (c + 1) * dc)
             L.moe_gmm(b.dh, wi[:, sl, :], 1, b.group_offsets, b.dxs[:, sl], L.EPI_NONE,
                       dev_status=b.dev_status, stream=stream)
+            mark("gmm_dgrad_up_chunk")
             L.moe_tgmm(b.xs[:, sl], b.dh, b.group_offsets, b.dwi[:, sl, :],
                        dev_status=b.dev_status, stream=stream)
+            mark("tgmm_dwi_chunk")
     L.moe_combine(b.dxs, b.f2s, None, b.dx, s.k, stream)
+    mark("dispatch_bwd")
     return b.dx, b.dwi, b.dwo, b.d_topk_w
+
+
+def kernels_per_step(s: LayerShape) -> int:
+    """Kernels one forward + backward launches (route 1, permute 3, each GEMM 1,
+    combine 1, unpermute_bwd 1, dispatch backward 1)."""
+    up = max(1, s.num_chunks)
+    fwd = 1 + 3 + up + 1 + 1
+    bwd = 1 + 1 + 1 + 2 * up + 1
+    return fwd + bwd
 
 
 def gemm_flops(m_kept: int, d: int, f: int) -> int:
