@@ -126,6 +126,31 @@ moe_status_t moe_permute(const uint16_t *x, int64_t ldx, const int32_t *topk_idx
                          size_t workspace_bytes, int32_t *dev_status, moe_stream_t stream);
 
 /*
+ * moe_permute_noalloc -- moe_permute without a caller-provided workspace.
+ * The pages have no counterpart of this call; it exists for callers that
+ * cannot allocate device memory where they permute (plugin-style interfaces
+ * that receive only their input and output buffers, or processes whose device
+ * memory is reserved up front by their own pool, where an extra cudaMalloc
+ * fails or fragments the pool).  Arguments and results are those of
+ * moe_permute without `workspace` / `workspace_bytes`.
+ * Scratch: a fixed 128 KB array of library-owned device memory, held by every
+ * GPU that loads the library until the process exits.  Sizes that need more
+ * (moe_permute_workspace_bytes(T, E) > 131072: T > 130048 with E = 256,
+ * T > 523264 with E = 64) return MOE_ERR_UNSUPPORTED.  The call allocates and frees nothing.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls share the array: calls whose kernels overlap on the GPU
+ * race and must be serialised by the caller.
+ */
+moe_status_t moe_permute_noalloc(const uint16_t *x, int64_t ldx, const int32_t *topk_idx, int T,
+                                 int d, int E, int k, int align, int capacity,
+                                 uint16_t *x_sorted, int64_t ld_xs, int64_t rows_cap,
+                                 int32_t *group_sizes, int32_t *kept_counts,
+                                 int32_t *group_offsets, int32_t *sorted_to_flat,
+                                 int32_t *flat_to_sorted, int32_t *dev_status,
+                                 moe_stream_t stream);
+
+/*
  * moe_gmm -- grouped GEMM over ragged per-expert row groups (tcgen05 tensor
  * cores, fp32 accumulation).  For every row r of group e:
  *     S[r, :] = A[r, :] . B_e  (+ partial_sum[r, :] when partial_sum != NULL)

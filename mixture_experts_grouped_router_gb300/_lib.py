@@ -60,6 +60,8 @@ _SIGS = {
     "moe_route_topk": (_I, [_P, _I64, _I, _I, _I, _I, _I, _P, _P, _P]),
     "moe_permute": (_I, [_P, _I64, _P, _I, _I, _I, _I, _I, _I, _P, _I64, _I64, _P, _P, _P, _P,
                          _P, _P, _SZ, _P, _P]),
+    "moe_permute_noalloc": (_I, [_P, _I64, _P, _I, _I, _I, _I, _I, _I, _P, _I64, _I64, _P, _P,
+                                 _P, _P, _P, _P, _P]),
     "moe_gmm": (_I, [_P, _I64, _P, _I64, _I64, _I, _P, _I, _I64, _I, _I, _I, _P, _I64, _P, _I64,
                      _P, _I, _I64, _P, _I64, _P, _P]),
     "moe_tgmm": (_I, [_P, _I64, _P, _I64, _P, _I, _I64, _I, _I, _P, _I, _I64, _I64, _I, _P, _P]),
@@ -133,6 +135,19 @@ def moe_permute(x, topk_idx, E, align, capacity, x_sorted, group_sizes, kept_cou
                            _ptr(flat_to_sorted), _ptr(workspace),
                            workspace.numel() * workspace.element_size(), _ptr(dev_status),
                            _stream(stream)))
+
+
+def moe_permute_noalloc(x, topk_idx, E, align, capacity, x_sorted, group_sizes, kept_counts,
+                        group_offsets, sorted_to_flat, flat_to_sorted, dev_status=None,
+                        stream=None):
+    """moe_permute with the library's built-in scratch array instead of a workspace."""
+    T, d = x.shape
+    k = topk_idx.shape[1]
+    _check(LIB.moe_permute_noalloc(_ptr(x), _ld(x), _ptr(topk_idx), T, d, E, k, align, capacity,
+                                   _ptr(x_sorted), _ld(x_sorted), x_sorted.shape[0],
+                                   _ptr(group_sizes), _ptr(kept_counts), _ptr(group_offsets),
+                                   _ptr(sorted_to_flat), _ptr(flat_to_sorted), _ptr(dev_status),
+                                   _stream(stream)))
 
 
 def moe_gmm(A, B, trans_b, group_offsets, C, epilogue=EPI_NONE, aux=None, partial_sum=None,
