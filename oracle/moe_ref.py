@@ -34,7 +34,7 @@ SIGMOID = 1
 # ----------------------------------------------------------------------------
 # routing
 # ----------------------------------------------------------------------------
-def route_topk(logits: np.ndarray, k: int, score_fn: int, renorm: int):
+def route_topk(logits: np.ndarray, k: int, score_fn: int, renorm: int, expert_bias=None):
     """Top-k expert selection and routing weights.
 
     TE-2912, Description ("TE's fused router ... top-K with optional
@@ -43,6 +43,12 @@ def route_topk(logits: np.ndarray, k: int, score_fn: int, renorm: int):
     all E) or sigmoid scores of the selected experts, optionally divided by
     their sum over the k selected.
 
+    With ``expert_bias`` (DeepSeek-V3's per-expert bias; TE-2912, the
+    ``expert_bias`` field of the body residuals; MaxText PR #2579 "Onboard
+    explicit sharding to deepseek", the routing code that keeps pre-bias
+    logits) the selection ranks the fp32 sums logit + bias while the weights
+    still come from the unbiased logits.
+
     Returns (topk_idx int32 [T,k], topk_w float64 [T,k]).
     """
     logits = np.asarray(logits, dtype=np.float32)
@@ -50,9 +56,11 @@ def route_topk(logits: np.ndarray, k: int, score_fn: int, renorm: int):
     assert np.isfinite(logits).all(), "the oracle assumes finite router logits"
     assert 1 <= k <= E
     l64 = logits.astype(np.float64)           # exact widening: same order as fp32
+    key = logits if expert_bias is None else \
+        (logits + np.asarray(expert_bias, dtype=np.float32)[None, :]).astype(np.float32)
     ids = np.broadcast_to(np.arange(E), (T, E))
-    # np.lexsort sorts by the last key first: -logit descending, then expert id ascending
-    order = np.lexsort((ids, -l64), axis=-1)
+    # np.lexsort sorts by the last key first: -key descending, then expert id ascending
+    order = np.lexsort((ids, -key.astype(np.float64)), axis=-1)
     topk_idx = order[:, :k].astype(np.int32)
     if score_fn == SOFTMAX:
         m = l64.max(axis=1, keepdims=True)
@@ -66,6 +74,46 @@ def route_topk(logits: np.ndarray, k: int, score_fn: int, renorm: int):
     if renorm:
         w = w / w.sum(axis=1, keepdims=True)
     return topk_idx, w
+
+
+def route_topk_bwd(logits: np.ndarray, topk_idx: np.ndarray, d_topk_w: np.ndarray,
+                   score_fn: int, renorm: int, chunk: int = 2048):
+    """Gradient of the routing weights w.r.t. the router logits, selection fixed.
+
+    TE-2912, sequence diagram / ``_moe_bwd_rule``: the block's backward returns
+    the gate-kernel gradient, i.e. it carries d_w back through the router.
+    Written as the chain rule with explicit Jacobians: the score Jacobian
+    (softmax: diag(p) - p p^T over all E; sigmoid: diag(s (1 - s))), the rows of
+    the selected experts, then the renormalisation Jacobian
+    d(v_j / S)/d v_m = (delta_jm - w_j) / S with S = sum of the selected v.
+    Returns d_logits float64 [T, E].
+    """
+    l = np.asarray(logits, dtype=np.float32).astype(np.float64)
+    T, E = l.shape
+    k = topk_idx.shape[1]
+    out = np.zeros((T, E))
+    for c0 in range(0, T, chunk):
+        lc = l[c0:c0 + chunk]
+        n = lc.shape[0]
+        if score_fn == SOFTMAX:
+            ex = np.exp(lc - lc.max(axis=1, keepdims=True))
+            sc = ex / ex.sum(axis=1, keepdims=True)
+            js = np.einsum("te,ef->tef", sc, np.eye(E)) - np.einsum("te,tf->tef", sc, sc)
+        else:
+            sc = 1.0 / (1.0 + np.exp(-lc))
+            js = np.einsum("te,ef->tef", sc * (1.0 - sc), np.eye(E))
+        idx = topk_idx[c0:c0 + chunk].astype(np.int64)
+        jv = np.take_along_axis(js, idx[:, :, None], axis=1)          # [n, k, E]
+        if renorm:
+            v = np.take_along_axis(sc, idx, axis=1)                  # [n, k]
+            S = v.sum(axis=1)
+            w = v / S[:, None]
+            jr = (np.eye(k)[None] - w[:, :, None]) / S[:, None, None]   # [n, j, m]
+            jw = np.einsum("tjm,tme->tje", jr, jv)
+        else:
+            jw = jv
+        out[c0:c0 + n] = np.einsum("tje,tj->te", jw, d_topk_w[c0:c0 + chunk])
+    return out
 
 
 # ----------------------------------------------------------------------------

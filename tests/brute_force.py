@@ -101,3 +101,20 @@ def layer_dense(x, logits, wi, wo, dout, k, score_fn, renorm, capacity=0):
     return dict(sel=sel, slot=slot, weight=weight, kept=kept, out=out.detach().numpy(),
                 dx=xt.grad.numpy(), dwi=wit.grad.numpy(), dwo=wot.grad.numpy(),
                 dgate=gt.grad.numpy())
+
+
+def route_bwd_dense_torch(logits, sel, d_gate, score_fn, renorm, bias=None):
+    """d_logits of L = sum d_gate * gate(logits), the selection mask held fixed:
+    the gate of every (token, expert) pair is written as a dense formula in
+    torch fp64 and differentiated by autograd."""
+    lt = torch.tensor(np.asarray(logits, np.float64), requires_grad=True)
+    mask = torch.tensor(sel, dtype=torch.float64)
+    if score_fn == 0:
+        score = torch.softmax(lt, dim=1)
+    else:
+        score = torch.sigmoid(lt)
+    gate = score * mask
+    if renorm:
+        gate = gate / gate.sum(dim=1, keepdim=True)
+    (gate * torch.tensor(d_gate, dtype=torch.float64)).sum().backward()
+    return lt.grad.numpy()

@@ -348,3 +348,81 @@ def test_planted_mistakes_are_caught(monkeypatch, mutant):
         monkeypatch.setattr(ref, "combine_bwd", _mut_combine_bwd_transposed)
         errs = _fd_check()
         assert errs["w"] > 1e-3
+
+
+# ---------------------------------------------------------------------------
+# routing backward and expert bias
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("sfn,ren,k", [(0, 1, 2), (0, 0, 3), (1, 1, 8), (1, 0, 1), (0, 1, 1)])
+def test_route_bwd_vs_autograd_and_fd(sfn, ren, k):
+    rng = np.random.default_rng(31 + 7 * sfn + ren + k)
+    T, E = 40, 12
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    idx, w = ref.route_topk(logits, k, sfn, ren)
+    dw = rng.standard_normal((T, k))
+    got = ref.route_topk_bwd(logits, idx, dw, sfn, ren)
+    sel = np.zeros((T, E), bool)
+    d_gate = np.zeros((T, E))
+    for t in range(T):
+        sel[t, idx[t]] = True
+        d_gate[t, idx[t]] = dw[t]
+    want = bf.route_bwd_dense_torch(logits, sel, d_gate, sfn, ren)
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-14)
+
+    # central differences of L(l) = <dw, w(l)> with the selection held fixed
+    def weights(lg):
+        if sfn == 0:
+            ex = np.exp(lg - lg.max(1, keepdims=True))
+            sc = ex / ex.sum(1, keepdims=True)
+        else:
+            sc = 1 / (1 + np.exp(-lg))
+        v = np.take_along_axis(sc, idx.astype(np.int64), 1)
+        return v / v.sum(1, keepdims=True) if ren else v
+    l64 = logits.astype(np.float64)
+    np.testing.assert_allclose(weights(l64), w, rtol=1e-14)
+    v = rng.standard_normal(l64.shape)
+    eps = 1e-6
+    fd = ((dw * weights(l64 + eps * v)).sum() - (dw * weights(l64 - eps * v)).sum()) / (2 * eps)
+    assert fd == pytest.approx((got * v).sum(), rel=1e-7, abs=1e-12)
+
+
+def test_route_bwd_closed_forms():
+    rng = np.random.default_rng(41)
+    logits = rng.standard_normal((25, 6)).astype(np.float32)
+    # top-1 with renorm: the weight is identically 1, so the gradient is exactly 0
+    idx, _ = ref.route_topk(logits, 1, 0, 1)
+    assert (ref.route_topk_bwd(logits, idx, rng.standard_normal((25, 1)), 0, 1) == 0).all()
+    # sigmoid without renorm: d_l = dw * s (1 - s) on the selected experts (scipy expit)
+    idx, w = ref.route_topk(logits, 3, 1, 0)
+    dw = rng.standard_normal((25, 3))
+    got = ref.route_topk_bwd(logits, idx, dw, 1, 0)
+    s = scipy.special.expit(logits.astype(np.float64))
+    want = np.zeros_like(got)
+    np.put_along_axis(want, idx.astype(np.int64),
+                      dw * np.take_along_axis(s * (1 - s), idx.astype(np.int64), 1), 1)
+    np.testing.assert_allclose(got, want, rtol=1e-13)
+    # softmax (renormalised or over all E) is shift invariant: rows sum to 0
+    for ren in (0, 1):
+        idx, _ = ref.route_topk(logits, 3, 0, ren)
+        g = ref.route_topk_bwd(logits, idx, rng.standard_normal((25, 3)), 0, ren)
+        np.testing.assert_allclose(g.sum(1), 0, atol=1e-14)
+
+
+def test_expert_bias_changes_selection_not_weights():
+    rng = np.random.default_rng(43)
+    logits = rng.standard_normal((60, 8)).astype(np.float32)
+    bias = np.zeros(8, np.float32)
+    bias[5] = 10.0           # expert 5 always selected first
+    idx, w = ref.route_topk(logits, 2, 1, 0, expert_bias=bias)
+    assert (idx[:, 0] == 5).all()
+    s = scipy.special.expit(logits.astype(np.float64))
+    np.testing.assert_allclose(w, np.take_along_axis(s, idx.astype(np.int64), 1), rtol=1e-14)
+    # brute force: rank by logit + bias in fp32, ties to the lower id
+    key = (logits + bias).astype(np.float32)
+    for t in range(60):
+        order = sorted(range(8), key=lambda e: (-float(key[t, e]), e))
+        assert idx[t].tolist() == order[:2]
+    # zero bias is the unbiased router
+    i0, w0 = ref.route_topk(logits, 2, 1, 0, expert_bias=np.zeros(8, np.float32))
+    i1, w1 = ref.route_topk(logits, 2, 1, 0)
+    assert (i0 == i1).all() and (w0 == w1).all()
