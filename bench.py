@@ -412,11 +412,12 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=60)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="mixtral", choices=sorted(moe_synth.CONFIGS))
+    ap.add_argument("--config", default="mixtral",
+                    choices=sorted(moe_synth.CONFIGS) + sorted(moe_synth.PROFILE_CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
-    cfg = moe_synth.CONFIGS[args.config]
+    cfg = {**moe_synth.CONFIGS, **moe_synth.PROFILE_CONFIGS}[args.config]
     ws, rank, local = dist_env()
     if args.impl == "reference":
         res = run_reference(args, cfg, ws, rank)

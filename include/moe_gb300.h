@@ -81,14 +81,35 @@ size_t moe_permute_workspace_bytes(int T, int E);
  *   score_fn  MOE_SCORE_SOFTMAX: softmax over all E experts;
  *             MOE_SCORE_SIGMOID: 1/(1+exp(-logit)) per expert
  *   renorm    nonzero: divide the k selected scores by their sum
- *   topk_idx  int32 [T, k] out: experts by descending logit, ties to the lower id
+ *   expert_bias fp32 [E] or NULL: DeepSeek-V3's per-expert selection bias
+ *             (TE-2912, the expert_bias residual; MaxText PR #2579 "Onboard
+ *             explicit sharding to deepseek", pre-bias logits): experts are
+ *             ranked by the fp32 sum logit + bias, weights use the logits
+ *   topk_idx  int32 [T, k] out: experts by descending key, ties to the lower id
  *   topk_w    fp32  [T, k] out: the selected (renormalised) scores, same order
- * Selection compares the fp32 logits (the score maps are monotone); a NaN
- * logit ranks below every number.
+ * Selection compares fp32 keys (the score maps are monotone); a NaN key ranks
+ * below every number.
  */
 moe_status_t moe_route_topk(const float *logits, int64_t ld_logits, int T, int E, int k,
-                            int score_fn, int renorm, int32_t *topk_idx, float *topk_w,
-                            moe_stream_t stream);
+                            int score_fn, int renorm, const float *expert_bias,
+                            int32_t *topk_idx, float *topk_w, moe_stream_t stream);
+
+/*
+ * moe_route_topk_bwd -- gradient of the routing weights w.r.t. the logits,
+ * the selection held fixed (TE-2912, sequence diagram: the block's backward
+ * carries d_w back to the gate kernel):
+ *   softmax, renorm:   d_l[i_j] = w_j (dw_j - c),   c = sum_j dw_j w_j
+ *   softmax:           d_l[e] = p_e ([e = i_j] dw_j - c) for all e
+ *   sigmoid, renorm:   d_l[i_j] = s_j (1 - s_j) (dw_j - c) / sum_m s_m
+ *   sigmoid:           d_l[i_j] = dw_j s_j (1 - s_j)
+ * other entries 0.  logits, topk_idx, topk_w as moe_route_topk produced them;
+ * d_topk_w fp32 [T, k]; d_logits fp32 [T, ld_dlogits >= E] out (every entry
+ * written).  E <= 256, k <= 16.
+ */
+moe_status_t moe_route_topk_bwd(const float *logits, int64_t ld_logits, const int32_t *topk_idx,
+                                const float *topk_w, const float *d_topk_w, int T, int E, int k,
+                                int score_fn, int renorm, float *d_logits, int64_t ld_dlogits,
+                                moe_stream_t stream);
 
 /*
  * moe_permute -- group the T*k (token, slot) assignments by expert and gather
@@ -135,8 +156,8 @@ moe_status_t moe_permute(const uint16_t *x, int64_t ldx, const int32_t *topk_idx
  * moe_permute without `workspace` / `workspace_bytes`.
  * Scratch: a fixed 128 KB array of library-owned device memory, held by every
  * GPU that loads the library until the process exits.  Sizes that need more
- * (moe_permute_workspace_bytes(T, E) > 131072: T > 130048 with E = 256,
- * T > 523264 with E = 64) return MOE_ERR_UNSUPPORTED.  The call allocates and frees nothing.
+ * (moe_permute_workspace_bytes(T, E) > 131072: with E = 256, T > 32512;
+ * E <= 64 always fits) return MOE_ERR_UNSUPPORTED.  The call allocates and frees nothing.
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
  * capture.  All calls share the array: calls whose kernels overlap on the GPU

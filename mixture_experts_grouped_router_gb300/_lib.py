@@ -57,7 +57,8 @@ _SIGS = {
     "moe_version": (_I, []),
     "moe_rows_cap": (_I64, [_I, _I, _I, _I]),
     "moe_permute_workspace_bytes": (_SZ, [_I, _I]),
-    "moe_route_topk": (_I, [_P, _I64, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "moe_route_topk": (_I, [_P, _I64, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
+    "moe_route_topk_bwd": (_I, [_P, _I64, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I64, _P]),
     "moe_permute": (_I, [_P, _I64, _P, _I, _I, _I, _I, _I, _I, _P, _I64, _I64, _P, _P, _P, _P,
                          _P, _P, _SZ, _P, _P]),
     "moe_permute_noalloc": (_I, [_P, _I64, _P, _I, _I, _I, _I, _I, _I, _P, _I64, _I64, _P, _P,
@@ -118,10 +119,20 @@ def moe_permute_workspace_bytes(T: int, E: int) -> int:
     return int(LIB.moe_permute_workspace_bytes(T, E))
 
 
-def moe_route_topk(logits, k, score_fn, renorm, topk_idx, topk_w, stream=None):
+def moe_route_topk(logits, k, score_fn, renorm, topk_idx, topk_w, stream=None,
+                   expert_bias=None):
     T, E = logits.shape
     _check(LIB.moe_route_topk(_ptr(logits), _ld(logits), T, E, k, score_fn, int(renorm),
-                              _ptr(topk_idx), _ptr(topk_w), _stream(stream)))
+                              _ptr(expert_bias), _ptr(topk_idx), _ptr(topk_w), _stream(stream)))
+
+
+def moe_route_topk_bwd(logits, topk_idx, topk_w, d_topk_w, score_fn, renorm, d_logits,
+                       stream=None):
+    T, E = logits.shape
+    k = topk_idx.shape[1]
+    _check(LIB.moe_route_topk_bwd(_ptr(logits), _ld(logits), _ptr(topk_idx), _ptr(topk_w),
+                                  _ptr(d_topk_w), T, E, k, score_fn, int(renorm), _ptr(d_logits),
+                                  _ld(d_logits), _stream(stream)))
 
 
 def moe_permute(x, topk_idx, E, align, capacity, x_sorted, group_sizes, kept_counts,

@@ -72,8 +72,8 @@ size_t moe_permute_workspace_bytes(int T, int E) {
 }
 
 moe_status_t moe_route_topk(const float *logits, int64_t ld_logits, int T, int E, int k,
-                            int score_fn, int renorm, int32_t *topk_idx, float *topk_w,
-                            moe_stream_t stream) {
+                            int score_fn, int renorm, const float *expert_bias,
+                            int32_t *topk_idx, float *topk_w, moe_stream_t stream) {
   set_error("");
   REQUIRE(T >= 0 && E > 0 && k > 0, MOE_ERR_INVALID_ARG, "moe_route_topk: T=%d E=%d k=%d", T, E, k);
   REQUIRE(k <= E, MOE_ERR_INVALID_ARG, "moe_route_topk: k=%d > E=%d", k, E);
@@ -83,9 +83,29 @@ moe_status_t moe_route_topk(const float *logits, int64_t ld_logits, int T, int E
           "moe_route_topk: bad score_fn %d", score_fn);
   REQUIRE(T == 0 || (logits && topk_idx && topk_w), MOE_ERR_INVALID_ARG,
           "moe_route_topk: null pointer");
-  return cuda_status(moe::launch_route_topk(logits, ld_logits, T, E, k, score_fn, renorm, topk_idx,
-                                            topk_w, (cudaStream_t)stream),
+  return cuda_status(moe::launch_route_topk(logits, ld_logits, T, E, k, score_fn, renorm,
+                                            expert_bias, topk_idx, topk_w, (cudaStream_t)stream),
                      "moe_route_topk launch");
+}
+
+moe_status_t moe_route_topk_bwd(const float *logits, int64_t ld_logits, const int32_t *topk_idx,
+                                const float *topk_w, const float *d_topk_w, int T, int E, int k,
+                                int score_fn, int renorm, float *d_logits, int64_t ld_dlogits,
+                                moe_stream_t stream) {
+  set_error("");
+  REQUIRE(T >= 0 && E > 0 && k > 0 && k <= E, MOE_ERR_INVALID_ARG,
+          "moe_route_topk_bwd: T=%d E=%d k=%d", T, E, k);
+  REQUIRE(E <= 256 && k <= 16, MOE_ERR_UNSUPPORTED, "moe_route_topk_bwd: needs E <= 256, k <= 16");
+  REQUIRE(ld_logits >= E && ld_dlogits >= E, MOE_ERR_INVALID_ARG,
+          "moe_route_topk_bwd: leading dimension < E");
+  REQUIRE(score_fn == MOE_SCORE_SOFTMAX || score_fn == MOE_SCORE_SIGMOID, MOE_ERR_INVALID_ARG,
+          "moe_route_topk_bwd: bad score_fn %d", score_fn);
+  REQUIRE(T == 0 || (logits && topk_idx && topk_w && d_topk_w && d_logits), MOE_ERR_INVALID_ARG,
+          "moe_route_topk_bwd: null pointer");
+  return cuda_status(moe::launch_route_topk_bwd(logits, ld_logits, topk_idx, topk_w, d_topk_w, T,
+                                                E, k, score_fn, renorm, d_logits, ld_dlogits,
+                                                (cudaStream_t)stream),
+                     "moe_route_topk_bwd launch");
 }
 
 moe_status_t moe_permute(const uint16_t *x, int64_t ldx, const int32_t *topk_idx, int T, int d,

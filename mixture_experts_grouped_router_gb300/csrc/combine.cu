@@ -16,9 +16,9 @@ namespace moe {
 namespace {
 
 constexpr int kThreads = 256;  // 8 warps = 8 tokens per block
-constexpr int kMaxK = 16;
 
-template <bool kWeighted>
+// KT: compile-time slot bound (k <= KT), so the per-slot arrays stay in registers.
+template <bool kWeighted, int KT>
 __global__ void __launch_bounds__(kThreads)
 combine_kernel(const uint16_t *__restrict__ Y, int64_t ldy, const int32_t *__restrict__ f2s,
                const float *__restrict__ w, int T, int k, int d, uint16_t *__restrict__ out,
@@ -28,10 +28,10 @@ combine_kernel(const uint16_t *__restrict__ Y, int64_t ldy, const int32_t *__res
   if (t >= T) return;
   const int pl = lane < k ? __ldg(f2s + (int64_t)t * k + lane) : -1;
   const float wl = (kWeighted && lane < k) ? __ldg(w + (int64_t)t * k + lane) : 1.0f;
-  int p[kMaxK];
-  float wj[kMaxK];
+  int p[KT];
+  float wj[KT];
 #pragma unroll
-  for (int j = 0; j < kMaxK; ++j) {
+  for (int j = 0; j < KT; ++j) {
     p[j] = __shfl_sync(0xffffffffu, pl, j);
     wj[j] = __shfl_sync(0xffffffffu, wl, j);
   }
@@ -43,7 +43,7 @@ combine_kernel(const uint16_t *__restrict__ Y, int64_t ldy, const int32_t *__res
 #pragma unroll
     for (int q = 0; q < 8; ++q) acc0[q] = acc1[q] = 0.f;
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
+    for (int j = 0; j < KT; ++j) {
       if (j < k && p[j] >= 0) {
         const uint4 *src = reinterpret_cast<const uint4 *>(Y + (int64_t)p[j] * ldy);
         float f[8];
@@ -62,8 +62,10 @@ combine_kernel(const uint16_t *__restrict__ Y, int64_t ldy, const int32_t *__res
   }
 }
 
-// Part A (blocks < nb_tok): one warp per token.  Part B: zero dY on padding
-// rows, 32 rows of sorted_to_flat per warp.
+// Part A (blocks < nb_tok): one warp per token, two 16-byte chunks per lane
+// in flight per slot.  Part B: zero dY on padding rows, 32 rows of
+// sorted_to_flat per warp.
+template <int KT>
 __global__ void __launch_bounds__(kThreads)
 unpermute_bwd_kernel(const uint16_t *__restrict__ dout, int64_t ld_dout,
                      const uint16_t *__restrict__ Y, int64_t ldy,
@@ -80,34 +82,51 @@ unpermute_bwd_kernel(const uint16_t *__restrict__ dout, int64_t ld_dout,
     int pl = lane < k ? __ldg(f2s + (int64_t)t * k + lane) : -1;
     if (pl >= rows_cap) pl = -1;
     const float wl = lane < k ? __ldg(w + (int64_t)t * k + lane) : 0.f;
-    int p[kMaxK];
-    float wj[kMaxK], dot[kMaxK];
+    int p[KT];
+    float wj[KT], dot[KT];
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
+    for (int j = 0; j < KT; ++j) {
       p[j] = __shfl_sync(0xffffffffu, pl, j);
       wj[j] = __shfl_sync(0xffffffffu, wl, j);
       dot[j] = 0.f;
     }
     const uint4 *g = reinterpret_cast<const uint4 *>(dout + (int64_t)t * ld_dout);
-    for (int i = lane; i < nvec; i += 32) {
-      float gf[8];
-      bf16x8_to_f32(ld_nc_v4(g + i), gf);
+    for (int i = lane; i < nvec; i += 64) {
+      const bool two = i + 32 < nvec;
+      uint4 gq[2], yq[KT][2];
+      gq[0] = ld_nc_v4(g + i);
+      if (two) gq[1] = ld_nc_v4(g + i + 32);
 #pragma unroll
-      for (int j = 0; j < kMaxK; ++j) {
+      for (int j = 0; j < KT; ++j) {
         if (j < k && p[j] >= 0) {
-          float yf[8], o[8];
-          bf16x8_to_f32(ld_nc_v4(reinterpret_cast<const uint4 *>(Y + (int64_t)p[j] * ldy) + i), yf);
+          const uint4 *yr = reinterpret_cast<const uint4 *>(Y + (int64_t)p[j] * ldy);
+          yq[j][0] = ld_nc_v4(yr + i);
+          if (two) yq[j][1] = ld_nc_v4(yr + i + 32);
+        }
+      }
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            dot[j] = fmaf(gf[q], yf[q], dot[j]);
-            o[q] = wj[j] * gf[q];
+      for (int h = 0; h < 2; ++h) {
+        if (h == 1 && !two) break;
+        float gf[8];
+        bf16x8_to_f32(gq[h], gf);
+#pragma unroll
+        for (int j = 0; j < KT; ++j) {
+          if (j < k && p[j] >= 0) {
+            float yf[8], o[8];
+            bf16x8_to_f32(yq[j][h], yf);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              dot[j] = fmaf(gf[q], yf[q], dot[j]);
+              o[q] = wj[j] * gf[q];
+            }
+            st_v4(reinterpret_cast<uint4 *>(dY + (int64_t)p[j] * ld_dy) + i + 32 * h,
+                  f32_to_bf16x8(o));
           }
-          st_v4(reinterpret_cast<uint4 *>(dY + (int64_t)p[j] * ld_dy) + i, f32_to_bf16x8(o));
         }
       }
     }
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
+    for (int j = 0; j < KT; ++j) {
       if (j < k) {
         const float s = warp_sum(dot[j]);
         if (lane == 0) dw[(int64_t)t * k + j] = p[j] >= 0 ? s : 0.f;
@@ -137,10 +156,19 @@ cudaError_t launch_combine(const uint16_t *Y, int64_t ldy, const int32_t *f2s, c
                            int T, int k, int d, uint16_t *out, int64_t ldo, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const int blocks = (T + kThreads / 32 - 1) / (kThreads / 32);
-  if (w != nullptr)
-    combine_kernel<true><<<blocks, kThreads, 0, s>>>(Y, ldy, f2s, w, T, k, d, out, ldo);
-  else
-    combine_kernel<false><<<blocks, kThreads, 0, s>>>(Y, ldy, f2s, w, T, k, d, out, ldo);
+#define MOE_COMBINE(KT)                                                                   \
+  do {                                                                                    \
+    if (w != nullptr)                                                                     \
+      combine_kernel<true, KT><<<blocks, kThreads, 0, s>>>(Y, ldy, f2s, w, T, k, d, out, ldo); \
+    else                                                                                  \
+      combine_kernel<false, KT><<<blocks, kThreads, 0, s>>>(Y, ldy, f2s, w, T, k, d, out, ldo); \
+  } while (0)
+  if (k <= 1) MOE_COMBINE(1);
+  else if (k <= 2) MOE_COMBINE(2);
+  else if (k <= 4) MOE_COMBINE(4);
+  else if (k <= 8) MOE_COMBINE(8);
+  else MOE_COMBINE(16);
+#undef MOE_COMBINE
   return cudaGetLastError();
 }
 
@@ -154,9 +182,15 @@ cudaError_t launch_unpermute_bwd(const uint16_t *dout, int64_t ld_dout, const ui
   const int64_t pad_warps = (rows_cap + 31) / 32;
   const int nb_pad = (int)((pad_warps + wpb - 1) / wpb);
   if (nb_tok + nb_pad == 0) return cudaSuccess;
-  unpermute_bwd_kernel<<<nb_tok + nb_pad, kThreads, 0, s>>>(dout, ld_dout, Y, ldy, f2s, s2f,
-                                                            offsets, w, T, k, d, E, rows_cap, dY,
-                                                            ld_dy, dw, nb_tok);
+#define MOE_UNPERMUTE(KT)                                                               \
+  unpermute_bwd_kernel<KT><<<nb_tok + nb_pad, kThreads, 0, s>>>(                        \
+      dout, ld_dout, Y, ldy, f2s, s2f, offsets, w, T, k, d, E, rows_cap, dY, ld_dy, dw, nb_tok)
+  if (k <= 1) MOE_UNPERMUTE(1);
+  else if (k <= 2) MOE_UNPERMUTE(2);
+  else if (k <= 4) MOE_UNPERMUTE(4);
+  else if (k <= 8) MOE_UNPERMUTE(8);
+  else MOE_UNPERMUTE(16);
+#undef MOE_UNPERMUTE
   return cudaGetLastError();
 }
 

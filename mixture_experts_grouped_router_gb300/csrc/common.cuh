@@ -66,5 +66,7 @@ MOE_DEVINL void st_v4(void *p, const uint4 &v) {
                : "memory");
 }
 
-// silu(z) = z * sigmoid(z) and the SwiGLU pieces, in fp32.
-MOE_DEVINL float sigmoid_f(float z) { return 1.0f / (1.0f + expf(-z)); }
+// sigmoid(z) = 1 / (1 + e^-z) in fp32 with the hardware exponential and
+// reciprocal (relative error ~1e-6, far below the bf16 rounding of the
+// SwiGLU outputs it feeds).  e^-z overflowing to inf gives exactly 0.
+MOE_DEVINL float sigmoid_f(float z) { return __frcp_rn(1.0f + __expf(-z)); }

@@ -11,18 +11,20 @@
 // moe_tgmm (ragged K): W_e = A_e^T B_e over the rows of expert e; an expert
 //          without rows gets exact zeros (MaxText PR #4295, Testing).
 //
-// Design (one persistent CTA per SM, 192 threads, warp-specialised):
+// Design (one persistent CTA per SM, 320 threads, warp-specialised):
 //   warp 0      TMA producer: 128x64 A tiles and 256x64 B tiles (bf16,
 //               128-byte swizzle) into a 4-stage shared-memory ring;
 //   warp 1      TMEM owner and MMA issuer: tcgen05.mma kind::f16,
 //               M=128 N=256 K=16, fp32 accumulators in TMEM, two 256-column
 //               accumulators so the epilogue of one tile overlaps the
 //               mainloop of the next;
-//   warps 2-5   epilogue: tcgen05.ld of one TMEM lane (= one output row) per
-//               thread, fused SwiGLU / partial-sum / cast, 16-byte stores.
+//   warps 2-9   epilogue: tcgen05.ld of one TMEM lane (= one output row) per
+//               thread, fused SwiGLU / partial-sum / cast, 16-byte stores; two
+//               warps per TMEM lane quarter, each taking half of the columns,
+//               so that the SwiGLU math keeps pace with the mainloop.
 // Tiles never straddle two experts.  The tile list is derived on the device
 // from group_offsets (no host synchronisation); tiles are visited expert by
-// expert in groups of 16 row tiles so that concurrently running CTAs share
+// expert in groups of 32 row tiles so that concurrently running CTAs share
 // their A rows and B columns in L2.  Every wait is bounded: on time-out the
 // CTA raises an abort flag, winds down, drains its in-flight copies and
 // MMAs, frees TMEM and reports MOE_ERR_TIMEOUT through dev_status.
@@ -38,13 +40,14 @@ namespace {
 
 constexpr int BM = 128, BN = 256, BK = 64, UK = 16;
 constexpr int kStages = 4;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // producer, MMA, 8 epilogue warps
+constexpr int kEpiWarps = 8;
 constexpr int A_BYTES = BM * BK * 2;   // 16 KB
 constexpr int B_BYTES = BN * BK * 2;   // 32 KB
 constexpr int BOX_BYTES = 64 * 64 * 2; // one 64x64 MN-major box, 8 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int kMaxE = 256;
-constexpr int kGroupM = 16;
+constexpr int kGroupM = 32;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr int kTmemCols = 2 * BN;                 // two accumulators
 
@@ -139,22 +142,82 @@ MOE_DEVINL void ld_f32x8(const float *src, float *v) {
   v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
-MOE_DEVINL void ld_bf16x8(const uint16_t *src, float *v) {
-  bf16x8_to_f32(*reinterpret_cast<const uint4 *>(src), v);
+MOE_DEVINL uint4 ld_v4_no_l1(const void *ptr) {
+  uint4 r;
+  asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(ptr));
+  return r;
 }
 
-// One tile's epilogue for the ragged-M GEMM.  Thread = one output row.
+MOE_DEVINL void prefetch_l2(const void *ptr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
+
+// Before a tile's accumulator is ready: pull the epilogue's global inputs
+// (SwiGLU-backward H, partial sums) into L2 so that the epilogue's loads do
+// not wait on HBM one after another.  Thread = one output row.
+template <int KIND, int EPI>
+MOE_DEVINL void epilogue_prefetch(const TcParams &p, const TileInfo &ti, int rit, int half) {
+  if (KIND == KIND_GMM) {
+    const int64_t row = (int64_t)ti.row0 + rit;
+    if (row >= ti.row_end) return;
+    if (EPI == MOE_EPI_SWIGLU_BWD) {
+      const uint16_t *h = p.aux + row * p.ld_aux;
+      const int n0 = ti.n_idx * BN + half * (BN / 2);
+      for (int n = n0; n < min(n0 + BN / 2, p.N); n += 64) {
+        prefetch_l2(h + n);
+        prefetch_l2(h + p.N + n);
+      }
+    } else if (p.ps != nullptr) {
+      const float *q = p.ps + row * p.ld_ps;
+      if (EPI == MOE_EPI_SWIGLU_FWD) {
+        const int n0 = ti.n_idx * (BN / 2) + half * (BN / 4);
+        for (int n = n0; n < min(n0 + BN / 4, p.F); n += 32) {
+          prefetch_l2(q + n);
+          prefetch_l2(q + p.F + n);
+        }
+      } else {
+        const int n0 = ti.n_idx * BN + half * (BN / 2);
+        for (int n = n0; n < min(n0 + BN / 2, p.N); n += 32) prefetch_l2(q + n);
+      }
+    }
+  } else if (p.accumulate) {
+    const int m = ti.m_idx * BM + rit;
+    if (m >= p.M) return;
+    const float *w = static_cast<const float *>(p.C) + (int64_t)ti.e * p.stride_w +
+                     (int64_t)m * p.ldc;
+    const int n0 = ti.n_idx * BN + half * (BN / 2);
+    for (int n = n0; n < min(n0 + BN / 2, p.N); n += 32) prefetch_l2(w + n);
+  }
+}
+
+// One tile's epilogue for the ragged-M GEMM.  Thread = one output row.  The
+// global inputs of a 32-column chunk are loaded before its TMEM read so that
+// the two latencies overlap.
 template <int EPI>
-MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t taddr, int rit) {
+MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t taddr, int rit,
+                             int half) {
   const int64_t row = (int64_t)ti.row0 + rit;
   const bool valid = row < ti.row_end;
   if (EPI == MOE_EPI_SWIGLU_FWD) {
     const int F = p.F;
     const int n0 = ti.n_idx * (BN / 2);
 #pragma unroll 1
-    for (int c = 0; c < BN / 2 / 32; ++c) {
+    for (int c = half * (BN / 2 / 32 / 2); c < (half + 1) * (BN / 2 / 32 / 2); ++c) {
       const int nc = n0 + c * 32;
       if (nc >= F) break;
+      float pg[32], pu[32];
+      const bool has_ps = valid && p.ps != nullptr;
+      if (has_ps) {
+#pragma unroll
+        for (int j8 = 0; j8 < 4; ++j8) {
+          if (nc + j8 * 8 < F) {
+            ld_f32x8(p.ps + row * p.ld_ps + nc + j8 * 8, pg + j8 * 8);
+            ld_f32x8(p.ps + row * p.ld_ps + F + nc + j8 * 8, pu + j8 * 8);
+          }
+        }
+      }
       float g[32], u[32];
       tc::tmem_ld32(taddr + c * 32, g);
       tc::tmem_ld32(taddr + BN / 2 + c * 32, u);
@@ -166,14 +229,11 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
         const int n = nc + j8 * 8;
         if (n >= F) break;
         float *gv = g + j8 * 8, *uv = u + j8 * 8;
-        if (p.ps != nullptr) {
-          float pg[8], pu[8];
-          ld_f32x8(p.ps + row * p.ld_ps + n, pg);
-          ld_f32x8(p.ps + row * p.ld_ps + F + n, pu);
+        if (has_ps) {
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
-            gv[q] += pg[q];
-            uv[q] += pu[q];
+            gv[q] += pg[j8 * 8 + q];
+            uv[q] += pu[j8 * 8 + q];
           }
         }
         float act[8];
@@ -187,44 +247,68 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
   } else {
     const int N = p.N;
     const int n0 = ti.n_idx * BN;
-#pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    const int c_begin = half * (BN / 32 / 2);
+    const int c_end = c_begin + BN / 32 / 2;
+    // Global inputs of a 32-column chunk (SwiGLU backward: 4 x 16 B of gate and
+    // 4 x 16 B of up from H; partial sum: 8 x 16 B of fp32), loaded one chunk
+    // ahead so that their latency overlaps the previous chunk's work.
+    const bool has_in = valid && (EPI == MOE_EPI_SWIGLU_BWD || p.ps != nullptr);
+    auto load_chunk = [&](int c, uint4 *buf) {
       const int nc = n0 + c * 32;
-      if (nc >= N) break;
-      float v[32];
-      tc::tmem_ld32(taddr + c * 32, v);
-      if (!valid) continue;
 #pragma unroll
-      for (int j8 = 0; j8 < 4; ++j8) {
-        const int n = nc + j8 * 8;
-        if (n >= N) break;
-        float *x = v + j8 * 8;
-        if (EPI == MOE_EPI_NONE) {
-          if (p.ps != nullptr) {
-            float pv[8];
-            ld_f32x8(p.ps + row * p.ld_ps + n, pv);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) x[q] += pv[q];
-          }
-          if (p.c_f32)
-            st_f32x8(static_cast<float *>(p.C) + row * p.ldc + n, x);
-          else
-            st_bf16x8(static_cast<uint16_t *>(p.C) + row * p.ldc + n, x);
-        } else {  // SWIGLU_BWD: x = dAct, aux = H = [gate | up]
-          float g[8], u[8], dg[8], du[8];
-          ld_bf16x8(p.aux + row * p.ld_aux + n, g);
-          ld_bf16x8(p.aux + row * p.ld_aux + N + n, u);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const float s = sigmoid_f(g[q]);
-            dg[q] = x[q] * u[q] * s * (1.0f + g[q] * (1.0f - s));
-            du[q] = x[q] * g[q] * s;
-          }
-          uint16_t *dH = static_cast<uint16_t *>(p.C) + row * p.ldc;
-          st_bf16x8(dH + n, dg);
-          st_bf16x8(dH + N + n, du);
+      for (int q = 0; q < 8; ++q) {
+        if (EPI == MOE_EPI_SWIGLU_BWD) {
+          const int n = nc + (q & 3) * 8;
+          if (n < N) buf[q] = ld_nc_v4(p.aux + row * p.ld_aux + (q < 4 ? 0 : N) + n);
+        } else {
+          const int n = nc + q * 4;
+          if (n < N) buf[q] = ld_v4_no_l1(p.ps + row * p.ld_ps + n);
         }
       }
+    };
+    uint4 cur[8], nxt[8];
+    if (has_in && n0 + c_begin * 32 < N) load_chunk(c_begin, cur);
+#pragma unroll 1
+    for (int c = c_begin; c < c_end; ++c) {
+      const int nc = n0 + c * 32;
+      if (nc >= N) break;
+      if (has_in && c + 1 < c_end && nc + 32 < N) load_chunk(c + 1, nxt);
+      float v[32];
+      tc::tmem_ld32(taddr + c * 32, v);
+      if (valid) {
+#pragma unroll
+        for (int j8 = 0; j8 < 4; ++j8) {
+          const int n = nc + j8 * 8;
+          if (n >= N) break;
+          float *x = v + j8 * 8;
+          if (EPI == MOE_EPI_NONE) {
+            if (p.ps != nullptr) {
+              const float *pv = reinterpret_cast<const float *>(&cur[2 * j8]);
+#pragma unroll
+              for (int q = 0; q < 8; ++q) x[q] += pv[q];
+            }
+            if (p.c_f32)
+              st_f32x8(static_cast<float *>(p.C) + row * p.ldc + n, x);
+            else
+              st_bf16x8(static_cast<uint16_t *>(p.C) + row * p.ldc + n, x);
+          } else {  // SWIGLU_BWD: x = dAct, aux = H = [gate | up]
+            float g[8], u[8], dg[8], du[8];
+            bf16x8_to_f32(cur[j8], g);
+            bf16x8_to_f32(cur[4 + j8], u);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const float sg = sigmoid_f(g[q]);
+              dg[q] = x[q] * u[q] * sg * (1.0f + g[q] * (1.0f - sg));
+              du[q] = x[q] * g[q] * sg;
+            }
+            uint16_t *dH = static_cast<uint16_t *>(p.C) + row * p.ldc;
+            st_bf16x8(dH + n, dg);
+            st_bf16x8(dH + N + n, du);
+          }
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) cur[q] = nxt[q];
     }
   }
 }
@@ -232,13 +316,13 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
 // tgmm epilogue: thread = one output row m of W_e.  `zero`: the expert had no
 // rows, so TMEM is not read.
 MOE_DEVINL void epilogue_tgmm(const TcParams &p, const TileInfo &ti, uint32_t taddr, int rit,
-                              bool zero) {
+                              int half, bool zero) {
   const int m = ti.m_idx * BM + rit;
   const bool valid = m < p.M;
   const int n0 = ti.n_idx * BN;
   const int64_t base = (int64_t)ti.e * p.stride_w + (int64_t)m * p.ldc;
 #pragma unroll 1
-  for (int c = 0; c < BN / 32; ++c) {
+  for (int c = half * (BN / 32 / 2); c < (half + 1) * (BN / 32 / 2); ++c) {
     const int nc = n0 + c * 32;
     if (nc >= p.N) break;
     float v[32];
@@ -289,7 +373,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     }
     for (int a = 0; a < 2; ++a) {
       tc::mbar_init(&bk.tfull[a], 1);
-      tc::mbar_init(&bk.tempty[a], 4);
+      tc::mbar_init(&bk.tempty[a], kEpiWarps);
     }
     tc::mbar_init(&bk.drain, 1);
     bk.abort_flag = 0;
@@ -457,25 +541,27 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     __syncwarp();
     tc::mbar_wait_drain(&bk.drain, 0, kWaitLimitNs);
   } else {
-    const int q = warp & 3;
+    const int q = warp & 3;              // TMEM lane quarter this warp may read
+    const int half = (warp - 2) >> 2;    // column half of the tile
     const int rit = q * 32 + lane;
     uint32_t acc_it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const TileInfo ti = decode_tile<KIND>(bk, p, t);
       if (KIND == KIND_GMM && ti.row_end <= ti.row0) continue;
       if (KIND == KIND_TGMM && ti.kblocks == 0) {
-        if (!p.accumulate) epilogue_tgmm(p, ti, 0, rit, true);
+        if (!p.accumulate) epilogue_tgmm(p, ti, 0, rit, half, true);
         continue;
       }
+      epilogue_prefetch<KIND, EPI>(p, ti, rit, half);
       const uint32_t a = acc_it & 1;
       const uint32_t aph = (acc_it >> 1) & 1;
       if (!tc::mbar_wait(&bk.tfull[a], aph, abort_flag, kWaitLimitNs)) break;
       tc::tc_fence_after();
       const uint32_t taddr = tmem + a * BN + (static_cast<uint32_t>(q * 32) << 16);
       if (KIND == KIND_GMM)
-        epilogue_gmm<EPI>(p, ti, taddr, rit);
+        epilogue_gmm<EPI>(p, ti, taddr, rit, half);
       else
-        epilogue_tgmm(p, ti, taddr, rit, false);
+        epilogue_tgmm(p, ti, taddr, rit, half, false);
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&bk.tempty[a]);

@@ -13,7 +13,12 @@ int num_sms();
 
 // route.cu
 cudaError_t launch_route_topk(const float *logits, int64_t ld, int T, int E, int k, int score_fn,
-                              int renorm, int32_t *idx, float *w, cudaStream_t s);
+                              int renorm, const float *bias, int32_t *idx, float *w,
+                              cudaStream_t s);
+cudaError_t launch_route_topk_bwd(const float *logits, int64_t ld, const int32_t *idx,
+                                  const float *w, const float *dw, int T, int E, int k,
+                                  int score_fn, int renorm, float *d_logits, int64_t ld_out,
+                                  cudaStream_t s);
 
 // permute.cu
 size_t permute_workspace_bytes(int T, int E);

@@ -5,7 +5,8 @@
 // _combine_bwd: the flat (token, slot) assignments are ordered by a stable
 // argsort on their expert, i.e. by (expert, token).  Here that order is
 // produced by a counting sort instead of a comparison sort:
-//   1. count:  per block of 1024 tokens, a shared-memory histogram over E;
+//   1. count:  per block of `tpb` tokens (a multiple of 256 chosen so that
+//              there are at most 256 blocks), a shared-memory histogram over E;
 //   2. rank:   every block derives the per-expert base of its tokens from the
 //              earlier blocks' counts, the kept counts (capacity), the aligned
 //              group sizes and their exclusive scan (warp-shuffle scan), then
@@ -16,27 +17,35 @@
 //              zero-filled by warps that scan sorted_to_flat 32 rows at a time.
 // Capacity (MaxText PR #2319, Tests: token-dropping) keeps rank < C; align
 // padding follows the aligned group_sizes of the recv_buffer_rows thread.
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
 namespace moe {
 namespace {
 
-constexpr int kPermTok = 1024;       // tokens per count / rank block
+constexpr int kMaxPermBlocks = 256;  // count / rank blocks per call
 constexpr int kRankThreads = 256;    // 8 warps, 256 tokens per round
 constexpr int kRankWarps = kRankThreads / 32;
 constexpr int kMaxE = 256;
 constexpr int kMaxK = 16;
 constexpr int kGatherThreads = 256;  // 8 warps
 
+// Tokens per count / rank block: a multiple of 256, at most kMaxPermBlocks blocks.
+inline int perm_tokens_per_block(int T) {
+  const int64_t per = ((int64_t)T + kMaxPermBlocks - 1) / kMaxPermBlocks;
+  return (int)std::max<int64_t>(256, (per + 255) / 256 * 256);
+}
+
 __global__ void __launch_bounds__(256)
-permute_count_kernel(const int32_t *__restrict__ topk_idx, int T, int E, int k,
+permute_count_kernel(const int32_t *__restrict__ topk_idx, int T, int E, int k, int tpb,
                      int32_t *__restrict__ counts, int32_t *dev_status) {
   __shared__ int32_t hist[kMaxE];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
-  const int64_t a0 = (int64_t)blockIdx.x * kPermTok * k;
-  const int64_t a1 = (int64_t)min(T, (int)((blockIdx.x + 1) * kPermTok)) * k;
+  const int64_t a0 = (int64_t)blockIdx.x * tpb * k;
+  const int64_t a1 = min((int64_t)T, (int64_t)(blockIdx.x + 1) * tpb) * k;
   for (int64_t a = a0 + threadIdx.x; a < a1; a += blockDim.x) {
     const int e = __ldg(topk_idx + a);
     if (e >= 0 && e < E)
@@ -50,7 +59,8 @@ permute_count_kernel(const int32_t *__restrict__ topk_idx, int T, int E, int k,
 
 __global__ void __launch_bounds__(kRankThreads)
 permute_rank_kernel(const int32_t *__restrict__ topk_idx, int T, int E, int k, int align,
-                    int capacity, const int32_t *__restrict__ counts, int nb, int64_t rows_cap,
+                    int capacity, int tpb, const int32_t *__restrict__ counts, int nb,
+                    int64_t rows_cap,
                     int32_t *__restrict__ group_sizes, int32_t *__restrict__ kept_counts,
                     int32_t *__restrict__ group_offsets, int32_t *__restrict__ s2f,
                     int32_t *__restrict__ f2s, int32_t *dev_status) {
@@ -116,8 +126,8 @@ permute_rank_kernel(const int32_t *__restrict__ topk_idx, int T, int E, int k, i
     s2f[p] = -1;
 
   // 4. rank this block's tokens, 256 per round
-  const int tok0 = b * kPermTok;
-  const int tok1 = min(T, tok0 + kPermTok);
+  const int tok0 = b * tpb;
+  const int tok1 = (int)min((int64_t)T, (int64_t)tok0 + tpb);
   for (int r0 = tok0; r0 < tok1; r0 += kRankThreads) {
     const int t = r0 + tid;
     const bool valid = t < tok1;
@@ -180,6 +190,7 @@ permute_rank_kernel(const int32_t *__restrict__ topk_idx, int T, int E, int k, i
   }
 }
 
+template <int KT>
 __global__ void __launch_bounds__(kGatherThreads)
 permute_gather_kernel(const uint16_t *__restrict__ x, int64_t ldx,
                       const int32_t *__restrict__ f2s, int T, int k, int d,
@@ -197,9 +208,9 @@ permute_gather_kernel(const uint16_t *__restrict__ x, int64_t ldx,
       moe_set_status(dev_status, MOE_ERR_DEVICE);
       pl = -1;
     }
-    int p[kMaxK];
+    int p[KT];
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j) p[j] = __shfl_sync(0xffffffffu, pl, j);
+    for (int j = 0; j < KT; ++j) p[j] = __shfl_sync(0xffffffffu, pl, j);
     const uint4 *src = reinterpret_cast<const uint4 *>(x + (int64_t)t * ldx);
     int i = lane;
     for (; i + 96 < nvec; i += 128) {
@@ -207,7 +218,7 @@ permute_gather_kernel(const uint16_t *__restrict__ x, int64_t ldx,
 #pragma unroll
       for (int u = 0; u < 4; ++u) v[u] = ld_nc_v4(src + i + 32 * u);
 #pragma unroll
-      for (int j = 0; j < kMaxK; ++j) {
+      for (int j = 0; j < KT; ++j) {
         if (j < k && p[j] >= 0) {
           uint4 *dst = reinterpret_cast<uint4 *>(xs + (int64_t)p[j] * ld_xs);
 #pragma unroll
@@ -218,7 +229,7 @@ permute_gather_kernel(const uint16_t *__restrict__ x, int64_t ldx,
     for (; i < nvec; i += 32) {
       const uint4 v = ld_nc_v4(src + i);
 #pragma unroll
-      for (int j = 0; j < kMaxK; ++j)
+      for (int j = 0; j < KT; ++j)
         if (j < k && p[j] >= 0) st_v4(reinterpret_cast<uint4 *>(xs + (int64_t)p[j] * ld_xs) + i, v);
     }
   } else {
@@ -243,7 +254,8 @@ permute_gather_kernel(const uint16_t *__restrict__ x, int64_t ldx,
 }  // namespace
 
 size_t permute_workspace_bytes(int T, int E) {
-  const int64_t nb = T > 0 ? (T + kPermTok - 1) / kPermTok : 1;
+  const int tpb = perm_tokens_per_block(T);
+  const int64_t nb = T > 0 ? ((int64_t)T + tpb - 1) / tpb : 1;
   return (size_t)(nb * E * sizeof(int32_t) + 256);
 }
 
@@ -252,22 +264,32 @@ cudaError_t launch_permute(const uint16_t *x, int64_t ldx, const int32_t *topk_i
                            int64_t rows_cap, int32_t *group_sizes, int32_t *kept,
                            int32_t *offsets, int32_t *s2f, int32_t *f2s, int32_t *counts_ws,
                            int32_t *dev_status, cudaStream_t s) {
-  const int nb = T > 0 ? (T + kPermTok - 1) / kPermTok : 1;
-  if (T > 0) permute_count_kernel<<<nb, 256, 0, s>>>(topk_idx, T, E, k, counts_ws, dev_status);
+  const int tpb = perm_tokens_per_block(T);
+  const int nb = T > 0 ? (int)(((int64_t)T + tpb - 1) / tpb) : 1;
+  if (T > 0)
+    permute_count_kernel<<<nb, 256, 0, s>>>(topk_idx, T, E, k, tpb, counts_ws, dev_status);
   else {
     cudaError_t e = cudaMemsetAsync(counts_ws, 0, sizeof(int32_t) * E, s);
     if (e != cudaSuccess) return e;
   }
-  permute_rank_kernel<<<nb, kRankThreads, 0, s>>>(topk_idx, T, E, k, align, capacity, counts_ws,
-                                                  nb, rows_cap, group_sizes, kept, offsets, s2f,
-                                                  f2s, dev_status);
+  permute_rank_kernel<<<nb, kRankThreads, 0, s>>>(topk_idx, T, E, k, align, capacity, tpb,
+                                                  counts_ws, nb, rows_cap, group_sizes, kept,
+                                                  offsets, s2f, f2s, dev_status);
   const int wpb = kGatherThreads / 32;
   const int nb_tok = (T + wpb - 1) / wpb;
   const int64_t pad_warps = (rows_cap + 31) / 32;
   const int nb_pad = (int)((pad_warps + wpb - 1) / wpb);
-  if (nb_tok + nb_pad > 0)
-    permute_gather_kernel<<<nb_tok + nb_pad, kGatherThreads, 0, s>>>(
-        x, ldx, f2s, T, k, d, xs, ld_xs, s2f, offsets, E, rows_cap, nb_tok, dev_status);
+  if (nb_tok + nb_pad > 0) {
+#define MOE_GATHER(KT)                                                                    \
+  permute_gather_kernel<KT><<<nb_tok + nb_pad, kGatherThreads, 0, s>>>(                   \
+      x, ldx, f2s, T, k, d, xs, ld_xs, s2f, offsets, E, rows_cap, nb_tok, dev_status)
+    if (k <= 1) MOE_GATHER(1);
+    else if (k <= 2) MOE_GATHER(2);
+    else if (k <= 4) MOE_GATHER(4);
+    else if (k <= 8) MOE_GATHER(8);
+    else MOE_GATHER(16);
+#undef MOE_GATHER
+  }
   return cudaGetLastError();
 }
 

@@ -26,9 +26,9 @@ static __device__ __align__(256) int32_t g_permute_scratch[32768];
 namespace moe {
 namespace {
 
-// 32768 counters = 128 KB.  A call needs ceil(T / 1024) * E counters plus 64
-// of slack: up to T = 130048 tokens with E = 256 experts, or T = 523264 with
-// E = 64.
+// 32768 counters = 128 KB.  A call needs (number of count blocks) * E counters
+// plus 64 of slack, with ceil(T / 256) count blocks for T <= 65536 and 256
+// above: E <= 64 always fits; E = 256 fits up to T = 32512 tokens.
 constexpr size_t kNoallocScratchInts = sizeof(g_permute_scratch) / sizeof(int32_t);
 
 constexpr int kMaxDevices = 64;

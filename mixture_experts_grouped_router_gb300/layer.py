@@ -8,8 +8,9 @@ router, permutation, groupedGEMM and communication", sequence diagram),
 without the expert-parallel all-to-all:
 
 forward   route_topk -> permute -> gmm(up, SwiGLU epilogue) -> gmm(down) -> combine
-backward  unpermute_bwd -> gmm(dgrad down, SwiGLU-bwd epilogue) -> tgmm(dWo)
-          -> gmm(dgrad up) -> tgmm(dWi) -> combine without weights (dispatch bwd)
+backward  unpermute_bwd -> route_topk_bwd (d_logits) -> gmm(dgrad down, SwiGLU-bwd
+          epilogue) -> tgmm(dWo) -> gmm(dgrad up) -> tgmm(dWi) -> combine without
+          weights (dispatch bwd)
 
 With num_chunks > 1 the up-projection runs as num_chunks K-chunks of d_model
 accumulating into an fp32 partial sum in place (MaxText PR #4295, "Overlap
@@ -66,6 +67,8 @@ class MoEBuffers:
         # backward
         self.dy = torch.empty(R, d, dtype=bf, device=dev)
         self.d_topk_w = torch.empty(T, k, dtype=f32, device=dev)
+        self.d_logits = torch.empty(T, E, dtype=f32, device=dev)
+        self.logits = None
         self.dh = torch.empty(R, 2 * f, dtype=bf, device=dev)
         self.dxs = torch.empty(R, d, dtype=bf, device=dev)
         self.dx = torch.empty(T, d, dtype=bf, device=dev)
@@ -84,6 +87,7 @@ def forward(b: MoEBuffers, x, logits, wi, wo, stream=None, mark=_noop):
     ``mark(name)`` is called after each library call (the benchmark records a
     CUDA event there)."""
     s = b.s
+    b.logits = logits
     L.moe_route_topk(logits, s.k, s.score_fn, s.renorm, b.topk_idx, b.topk_w, stream)
     mark("route")
     L.moe_permute(x, b.topk_idx, s.E, s.align, s.capacity, b.xs, b.group_sizes, b.kept_counts,
@@ -117,11 +121,15 @@ def forward(b: MoEBuffers, x, logits, wi, wo, stream=None, mark=_noop):
 
 
 def backward(b: MoEBuffers, dout, wi, wo, stream=None, mark=_noop):
-    """dout bf16 [T,d] -> (dx, dwi, dwo, d_topk_w) in b's buffers."""
+    """dout bf16 [T,d] -> (dx, dwi, dwo, d_topk_w) in b's buffers; the router-logit
+    gradient lands in b.d_logits."""
     s = b.s
     L.moe_unpermute_bwd(dout, b.y, b.f2s, b.s2f, b.group_offsets, b.topk_w, b.dy, b.d_topk_w,
                         stream)
     mark("unpermute_bwd")
+    L.moe_route_topk_bwd(b.logits, b.topk_idx, b.topk_w, b.d_topk_w, s.score_fn, s.renorm,
+                         b.d_logits, stream)
+    mark("route_bwd")
     # dAct = dY . wo^T, fused with the SwiGLU backward into dH = [dgate | dup]
     L.moe_gmm(b.dy, wo, 1, b.group_offsets, b.dh, L.EPI_SWIGLU_BWD, aux=b.h,
               dev_status=b.dev_status, stream=stream)
@@ -151,10 +159,10 @@ def backward(b: MoEBuffers, dout, wi, wo, stream=None, mark=_noop):
 
 def kernels_per_step(s: LayerShape) -> int:
     """Kernels one forward + backward launches (route 1, permute 3, each GEMM 1,
-    combine 1, unpermute_bwd 1, dispatch backward 1)."""
+    combine 1, unpermute_bwd 1, route_bwd 1, dispatch backward 1)."""
     up = max(1, s.num_chunks)
     fwd = 1 + 3 + up + 1 + 1
-    bwd = 1 + 1 + 1 + 2 * up + 1
+    bwd = 1 + 1 + 1 + 1 + 2 * up + 1
     return fwd + bwd
 
 

@@ -73,6 +73,16 @@ CONFIGS = {
 }
 
 
+# Reduced workloads used for profiling captures: the GEMM kernels at the same
+# per-expert shapes on a few GB of device memory.
+PROFILE_CONFIGS = {
+    "mixtral_e2": MoEConfig("mixtral_e2", T=8192, d=4096, f=14336, E=2, k=1, score_fn=SOFTMAX,
+                            renorm=0),
+    "dsv3_e8": MoEConfig("dsv3_e8", T=2048, d=7168, f=2048, E=8, k=8, score_fn=SIGMOID,
+                         renorm=1),
+}
+
+
 def bf16_bits(a: np.ndarray) -> np.ndarray:
     """Round fp32 values to bf16 (round to nearest, ties to even); return the uint16 bits."""
     u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)

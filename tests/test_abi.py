@@ -29,7 +29,7 @@ def L():
 def test_header_declares_the_six_calls():
     names = _declared()
     for n in ("moe_route_topk", "moe_permute", "moe_gmm", "moe_tgmm", "moe_combine",
-              "moe_unpermute_bwd"):
+              "moe_unpermute_bwd", "moe_route_topk_bwd"):
         assert n in names
 
 
@@ -56,13 +56,18 @@ def _ptr(v=16):
 def test_validation_errors_need_no_gpu(L):
     lib = L.LIB
     # k > E
-    st = lib.moe_route_topk(_ptr(), 8, 10, 8, 9, 0, 1, _ptr(), _ptr(), None)
+    st = lib.moe_route_topk(_ptr(), 8, 10, 8, 9, 0, 1, None, _ptr(), _ptr(), None)
     assert st == L.MOE_ERR_INVALID_ARG and "k=9" in L.last_error()
     # E above the router's limit
-    st = lib.moe_route_topk(_ptr(), 300, 10, 300, 2, 0, 1, _ptr(), _ptr(), None)
+    st = lib.moe_route_topk(_ptr(), 300, 10, 300, 2, 0, 1, None, _ptr(), _ptr(), None)
     assert st == L.MOE_ERR_UNSUPPORTED
     # bad score function
-    st = lib.moe_route_topk(_ptr(), 8, 10, 8, 2, 7, 1, _ptr(), _ptr(), None)
+    st = lib.moe_route_topk(_ptr(), 8, 10, 8, 2, 7, 1, None, _ptr(), _ptr(), None)
+    assert st == L.MOE_ERR_INVALID_ARG
+    # route backward: k > E, bad leading dimension
+    st = lib.moe_route_topk_bwd(_ptr(), 8, _ptr(), _ptr(), _ptr(), 10, 8, 9, 0, 1, _ptr(), 8, None)
+    assert st == L.MOE_ERR_INVALID_ARG
+    st = lib.moe_route_topk_bwd(_ptr(), 8, _ptr(), _ptr(), _ptr(), 10, 8, 2, 0, 1, _ptr(), 4, None)
     assert st == L.MOE_ERR_INVALID_ARG
     # permute: rows_cap below the worst case
     st = lib.moe_permute(_ptr(), 64, _ptr(), 100, 64, 8, 2, 4, 0, _ptr(), 64, 100, _ptr(), _ptr(),

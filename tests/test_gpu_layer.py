@@ -47,6 +47,9 @@ def test_layer_small(name):
     assert_close("out", b.out, fw["out"])
     assert_close("dy", b.dy[:R], bw["dy"])
     assert_close("d_topk_w", b.d_topk_w, bw["d_topk_w"])
+    assert_close("d_logits", b.d_logits,
+                 moe_ref.route_topk_bwd(inp["logits"], fw["topk_idx"], bw["d_topk_w"],
+                                        cfg.score_fn, cfg.renorm))
     assert_close("dh", b.dh[:R], bw["dh"])
     assert_close("dxs", b.dxs[:R], bw["d_xs"])
     assert_close("dx", b.dx, bw["dx"])

@@ -137,3 +137,51 @@ def test_permute_bad_expert_sets_status_without_fault():
     assert int(r["st"].item()) == L.MOE_ERR_DEVICE
     f2s = r["f2s"].cpu().numpy()
     assert f2s[3] == -1 and f2s[5] == -1
+
+
+BIAS_CASES = [(300, 8, 2, 1, 1), (513, 64, 8, 1, 1), (100, 256, 4, 0, 0), (77, 32, 3, 0, 1)]
+
+
+@pytest.mark.parametrize("case", BIAS_CASES)
+def test_route_topk_expert_bias(case):
+    T, E, k, sfn, ren = case
+    rng = np.random.default_rng(T + E + k)
+    lg = rng.standard_normal((T, E)).astype(np.float32)
+    bias = (rng.standard_normal(E) * 2).astype(np.float32)
+    idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, k, dtype=torch.float32, device="cuda")
+    L.moe_route_topk(torch.from_numpy(lg).cuda(), k, sfn, ren, idx, w,
+                     expert_bias=torch.from_numpy(bias).cuda())
+    torch.cuda.synchronize()
+    ridx, rw = moe_ref.route_topk(lg, k, sfn, ren, expert_bias=bias)
+    assert (idx.cpu().numpy() == ridx).all()
+    np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=0, atol=W_ATOL)
+
+
+ROUTE_BWD_CASES = [(257, 8, 2, 0, 1), (300, 32, 8, 1, 1), (513, 64, 1, 0, 0), (100, 256, 16, 1, 0),
+                   (129, 128, 6, 0, 0), (64, 5, 5, 1, 1), (33, 40, 1, 0, 1)]
+
+
+@pytest.mark.parametrize("case", ROUTE_BWD_CASES)
+def test_route_topk_bwd(case):
+    T, E, k, sfn, ren = case
+    rng = np.random.default_rng(3 * T + E)
+    lg = rng.standard_normal((T, E)).astype(np.float32)
+    lgd = torch.from_numpy(lg).cuda()
+    idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, k, dtype=torch.float32, device="cuda")
+    L.moe_route_topk(lgd, k, sfn, ren, idx, w)
+    dw_np = rng.standard_normal((T, k)).astype(np.float32)
+    dl = torch.full((T, E), float("nan"), dtype=torch.float32, device="cuda")
+    L.moe_route_topk_bwd(lgd, idx, w, torch.from_numpy(dw_np).cuda(), sfn, ren, dl)
+    torch.cuda.synchronize()
+    ridx, _ = moe_ref.route_topk(lg, k, sfn, ren)
+    assert (idx.cpu().numpy() == ridx).all()
+    want = moe_ref.route_topk_bwd(lg, ridx, dw_np.astype(np.float64), sfn, ren)
+    got = dl.cpu().numpy().astype(np.float64)
+    # fp32 arithmetic on fp32 inputs: far tighter than the layer's bf16 tolerance
+    np.testing.assert_allclose(got, want, rtol=0, atol=2e-6 * max(1.0, np.abs(want).max()))
+    if not (sfn == 0 and ren == 0):
+        sel = np.zeros((T, E), bool)
+        np.put_along_axis(sel, ridx.astype(np.int64), True, 1)
+        assert (got[~sel] == 0).all()
