@@ -11,17 +11,20 @@
 // moe_tgmm (ragged K): W_e = A_e^T B_e over the rows of expert e; an expert
 //          without rows gets exact zeros (MaxText PR #4295, Testing).
 //
-// Design (one persistent CTA per SM, 320 threads, warp-specialised):
+// Design (one persistent CTA per SM, 192 threads, warp-specialised):
 //   warp 0      TMA producer: 128x64 A tiles and 256x64 B tiles (bf16,
 //               128-byte swizzle) into a 4-stage shared-memory ring;
 //   warp 1      TMEM owner and MMA issuer: tcgen05.mma kind::f16,
 //               M=128 N=256 K=16, fp32 accumulators in TMEM, two 256-column
 //               accumulators so the epilogue of one tile overlaps the
 //               mainloop of the next;
-//   warps 2-9   epilogue: tcgen05.ld of one TMEM lane (= one output row) per
-//               thread, fused SwiGLU / partial-sum / cast, 16-byte stores; two
-//               warps per TMEM lane quarter, each taking half of the columns,
-//               so that the SwiGLU math keeps pace with the mainloop.
+//   warps 2-5   epilogue: tcgen05.ld of one TMEM lane (= one output row) per
+//               thread, fused SwiGLU / partial-sum / cast; each warp stages
+//               its 32x32 output blocks in swizzled shared memory and writes
+//               them with TMA bulk stores, so that the outputs leave as whole
+//               lines and never contend with the operand loads of the
+//               mainloop (a block that straddles the expert's last row is
+//               written with plain stores instead).
 // Tiles never straddle two experts.  The tile list is derived on the device
 // from group_offsets (no host synchronisation); tiles are visited expert by
 // expert in groups of 32 row tiles so that concurrently running CTAs share
@@ -40,8 +43,9 @@ namespace {
 
 constexpr int BM = 128, BN = 256, BK = 64, UK = 16;
 constexpr int kStages = 4;
-constexpr int kThreads = 320;  // producer, MMA, 8 epilogue warps
-constexpr int kEpiWarps = 8;
+constexpr int kThreads = 192;  // producer, MMA, 4 epilogue warps
+constexpr int kEpiWarps = 4;
+constexpr int kStgBytes = 6144;  // per epilogue warp: three 32x32 bf16 blocks (or one fp32)
 constexpr int A_BYTES = BM * BK * 2;   // 16 KB
 constexpr int B_BYTES = BN * BK * 2;   // 32 KB
 constexpr int BOX_BYTES = 64 * 64 * 2; // one 64x64 MN-major box, 8 KB
@@ -65,7 +69,8 @@ struct Book {
   int off[kMaxE + 1];
   int cum[kMaxE + 1];
 };
-constexpr int SMEM_BYTES = 1024 + kStages * STAGE_BYTES + (int)((sizeof(Book) + 127) / 128 * 128);
+constexpr int BOOK_BYTES = (int)((sizeof(Book) + 1023) / 1024 * 1024);
+constexpr int SMEM_BYTES = 1024 + kStages * STAGE_BYTES + BOOK_BYTES + kEpiWarps * kStgBytes;
 
 struct TcParams {
   int E;
@@ -154,32 +159,69 @@ MOE_DEVINL void prefetch_l2(const void *ptr) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
 }
 
+// Staging of one thread's 32-value row segment in the layout the TMA store
+// reads: bf16 rows of 64 bytes under the 64-byte swizzle (16-byte chunk c of
+// row r at chunk c ^ ((r >> 1) & 3)), fp32 rows of 128 bytes under the
+// 128-byte swizzle (chunk c ^ (r & 7)).  Both are free of bank conflicts
+// when the 32 lanes of a warp write the same chunk of their 32 rows.
+MOE_DEVINL void stage_bf16(uint8_t *buf, int r, const float *v) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    *reinterpret_cast<uint4 *>(buf + r * 64 + ((c ^ ((r >> 1) & 3)) << 4)) =
+        f32_to_bf16x8(v + 8 * c);
+}
+
+MOE_DEVINL void stage_f32(uint8_t *buf, int r, const float *v) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    *reinterpret_cast<uint4 *>(buf + r * 128 + ((c ^ (r & 7)) << 4)) =
+        make_uint4(__float_as_uint(v[4 * c]), __float_as_uint(v[4 * c + 1]),
+                   __float_as_uint(v[4 * c + 2]), __float_as_uint(v[4 * c + 3]));
+}
+
+// The warp's staging buffers may be rewritten once the previous bulk stores
+// have read them.
+MOE_DEVINL void stage_acquire(int lane) {
+  if (lane == 0) tc::bulk_wait_read0();
+  __syncwarp();
+}
+
+// Staged writes become visible to the TMA engine; lane 0 then issues the stores.
+MOE_DEVINL void stage_release() {
+  tc::fence_proxy_async_smem();
+  __syncwarp();
+}
+
+struct OutMaps {
+  const CUtensorMap *m0, *m1, *m2;
+};
+
 // Before a tile's accumulator is ready: pull the epilogue's global inputs
 // (SwiGLU-backward H, partial sums) into L2 so that the epilogue's loads do
 // not wait on HBM one after another.  Thread = one output row.
 template <int KIND, int EPI>
-MOE_DEVINL void epilogue_prefetch(const TcParams &p, const TileInfo &ti, int rit, int half) {
+MOE_DEVINL void epilogue_prefetch(const TcParams &p, const TileInfo &ti, int rit) {
   if (KIND == KIND_GMM) {
     const int64_t row = (int64_t)ti.row0 + rit;
     if (row >= ti.row_end) return;
     if (EPI == MOE_EPI_SWIGLU_BWD) {
       const uint16_t *h = p.aux + row * p.ld_aux;
-      const int n0 = ti.n_idx * BN + half * (BN / 2);
-      for (int n = n0; n < min(n0 + BN / 2, p.N); n += 64) {
+      const int n0 = ti.n_idx * BN;
+      for (int n = n0; n < min(n0 + BN, p.N); n += 64) {
         prefetch_l2(h + n);
         prefetch_l2(h + p.N + n);
       }
     } else if (p.ps != nullptr) {
       const float *q = p.ps + row * p.ld_ps;
       if (EPI == MOE_EPI_SWIGLU_FWD) {
-        const int n0 = ti.n_idx * (BN / 2) + half * (BN / 4);
-        for (int n = n0; n < min(n0 + BN / 4, p.F); n += 32) {
+        const int n0 = ti.n_idx * (BN / 2);
+        for (int n = n0; n < min(n0 + BN / 2, p.F); n += 32) {
           prefetch_l2(q + n);
           prefetch_l2(q + p.F + n);
         }
       } else {
-        const int n0 = ti.n_idx * BN + half * (BN / 2);
-        for (int n = n0; n < min(n0 + BN / 2, p.N); n += 32) prefetch_l2(q + n);
+        const int n0 = ti.n_idx * BN;
+        for (int n = n0; n < min(n0 + BN, p.N); n += 32) prefetch_l2(q + n);
       }
     }
   } else if (p.accumulate) {
@@ -187,150 +229,204 @@ MOE_DEVINL void epilogue_prefetch(const TcParams &p, const TileInfo &ti, int rit
     if (m >= p.M) return;
     const float *w = static_cast<const float *>(p.C) + (int64_t)ti.e * p.stride_w +
                      (int64_t)m * p.ldc;
-    const int n0 = ti.n_idx * BN + half * (BN / 2);
-    for (int n = n0; n < min(n0 + BN / 2, p.N); n += 32) prefetch_l2(w + n);
+    const int n0 = ti.n_idx * BN;
+    for (int n = n0; n < min(n0 + BN, p.N); n += 32) prefetch_l2(w + n);
   }
 }
 
-// One tile's epilogue for the ragged-M GEMM.  Thread = one output row.  The
-// global inputs of a 32-column chunk are loaded before its TMEM read so that
-// the two latencies overlap.
+// One tile's epilogue for the ragged-M GEMM.  Warp q owns tile rows
+// [32q, 32q+32), thread = one row; 32-column chunks.  The global inputs of a
+// chunk are loaded one chunk ahead so that their latency overlaps the work
+// of the previous chunk.
 template <int EPI>
-MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t taddr, int rit,
-                             int half) {
-  const int64_t row = (int64_t)ti.row0 + rit;
+MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t taddr, int q,
+                             int lane, uint8_t *stg, const OutMaps &om) {
+  const int wrow0 = ti.row0 + q * 32;
+  const int64_t row = (int64_t)wrow0 + lane;
   const bool valid = row < ti.row_end;
+  const bool bulk = wrow0 + 32 <= ti.row_end;  // every row of the block is this expert's
   if (EPI == MOE_EPI_SWIGLU_FWD) {
     const int F = p.F;
     const int n0 = ti.n_idx * (BN / 2);
+    const bool has_ps = valid && p.ps != nullptr;
 #pragma unroll 1
-    for (int c = half * (BN / 2 / 32 / 2); c < (half + 1) * (BN / 2 / 32 / 2); ++c) {
+    for (int c = 0; c < BN / 2 / 32; ++c) {
       const int nc = n0 + c * 32;
       if (nc >= F) break;
-      float pg[32], pu[32];
-      const bool has_ps = valid && p.ps != nullptr;
+      uint4 pg[8], pu[8];
       if (has_ps) {
 #pragma unroll
-        for (int j8 = 0; j8 < 4; ++j8) {
-          if (nc + j8 * 8 < F) {
-            ld_f32x8(p.ps + row * p.ld_ps + nc + j8 * 8, pg + j8 * 8);
-            ld_f32x8(p.ps + row * p.ld_ps + F + nc + j8 * 8, pu + j8 * 8);
+        for (int j = 0; j < 8; ++j) {
+          if (nc + j * 4 < F) {
+            pg[j] = ld_v4_no_l1(p.ps + row * p.ld_ps + nc + j * 4);
+            pu[j] = ld_v4_no_l1(p.ps + row * p.ld_ps + F + nc + j * 4);
           }
         }
       }
-      float g[32], u[32];
+      float g[32], u[32], act[32];
       tc::tmem_ld32(taddr + c * 32, g);
       tc::tmem_ld32(taddr + BN / 2 + c * 32, u);
-      if (!valid) continue;
-      uint16_t *H = static_cast<uint16_t *>(p.C) + row * p.ldc;
-      uint16_t *A = p.C2 + row * p.ldc2;
+      if (has_ps) {
+        const float *fg = reinterpret_cast<const float *>(pg);
+        const float *fu = reinterpret_cast<const float *>(pu);
 #pragma unroll
-      for (int j8 = 0; j8 < 4; ++j8) {
-        const int n = nc + j8 * 8;
-        if (n >= F) break;
-        float *gv = g + j8 * 8, *uv = u + j8 * 8;
-        if (has_ps) {
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            gv[q] += pg[j8 * 8 + q];
-            uv[q] += pu[j8 * 8 + q];
-          }
+        for (int j = 0; j < 32; ++j) {
+          g[j] += fg[j];
+          u[j] += fu[j];
         }
-        float act[8];
+      }
 #pragma unroll
-        for (int q = 0; q < 8; ++q) act[q] = gv[q] * sigmoid_f(gv[q]) * uv[q];
-        st_bf16x8(H + n, gv);
-        st_bf16x8(H + F + n, uv);
-        st_bf16x8(A + n, act);
+      for (int j = 0; j < 32; ++j) act[j] = g[j] * sigmoid_f(g[j]) * u[j];
+      if (bulk) {
+        stage_acquire(lane);
+        stage_bf16(stg, lane, g);
+        stage_bf16(stg + 2048, lane, u);
+        stage_bf16(stg + 4096, lane, act);
+        stage_release();
+        if (lane == 0) {
+          tc::tma_store_2d(om.m0, stg, nc, wrow0);
+          tc::tma_store_2d(om.m1, stg + 2048, nc, wrow0);
+          tc::tma_store_2d(om.m2, stg + 4096, nc, wrow0);
+          tc::bulk_commit();
+        }
+      } else if (valid) {
+        uint16_t *H = static_cast<uint16_t *>(p.C) + row * p.ldc;
+        uint16_t *A = p.C2 + row * p.ldc2;
+#pragma unroll
+        for (int j8 = 0; j8 < 4; ++j8) {
+          const int n = nc + j8 * 8;
+          if (n >= F) break;
+          st_bf16x8(H + n, g + j8 * 8);
+          st_bf16x8(H + F + n, u + j8 * 8);
+          st_bf16x8(A + n, act + j8 * 8);
+        }
       }
     }
   } else {
     const int N = p.N;
     const int n0 = ti.n_idx * BN;
-    const int c_begin = half * (BN / 32 / 2);
-    const int c_end = c_begin + BN / 32 / 2;
-    // Global inputs of a 32-column chunk (SwiGLU backward: 4 x 16 B of gate and
-    // 4 x 16 B of up from H; partial sum: 8 x 16 B of fp32), loaded one chunk
-    // ahead so that their latency overlaps the previous chunk's work.
+    // inputs of a chunk: SwiGLU backward 4 x 16 B of gate and 4 x 16 B of up
+    // from H; partial sum 8 x 16 B of fp32
     const bool has_in = valid && (EPI == MOE_EPI_SWIGLU_BWD || p.ps != nullptr);
     auto load_chunk = [&](int c, uint4 *buf) {
       const int nc = n0 + c * 32;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
+      for (int j = 0; j < 8; ++j) {
         if (EPI == MOE_EPI_SWIGLU_BWD) {
-          const int n = nc + (q & 3) * 8;
-          if (n < N) buf[q] = ld_nc_v4(p.aux + row * p.ld_aux + (q < 4 ? 0 : N) + n);
+          const int n = nc + (j & 3) * 8;
+          if (n < N) buf[j] = ld_nc_v4(p.aux + row * p.ld_aux + (j < 4 ? 0 : N) + n);
         } else {
-          const int n = nc + q * 4;
-          if (n < N) buf[q] = ld_v4_no_l1(p.ps + row * p.ld_ps + n);
+          const int n = nc + j * 4;
+          if (n < N) buf[j] = ld_v4_no_l1(p.ps + row * p.ld_ps + n);
         }
       }
     };
     uint4 cur[8], nxt[8];
-    if (has_in && n0 + c_begin * 32 < N) load_chunk(c_begin, cur);
+    if (has_in) load_chunk(0, cur);
 #pragma unroll 1
-    for (int c = c_begin; c < c_end; ++c) {
+    for (int c = 0; c < BN / 32; ++c) {
       const int nc = n0 + c * 32;
       if (nc >= N) break;
-      if (has_in && c + 1 < c_end && nc + 32 < N) load_chunk(c + 1, nxt);
+      if (has_in && c + 1 < BN / 32 && nc + 32 < N) load_chunk(c + 1, nxt);
       float v[32];
       tc::tmem_ld32(taddr + c * 32, v);
-      if (valid) {
+      if (EPI == MOE_EPI_NONE) {
+        if (p.ps != nullptr && valid) {
+          const float *pv = reinterpret_cast<const float *>(cur);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] += pv[j];
+        }
+        if (bulk) {
+          stage_acquire(lane);
+          if (p.c_f32) stage_f32(stg, lane, v);
+          else stage_bf16(stg, lane, v);
+          stage_release();
+          if (lane == 0) {
+            tc::tma_store_2d(om.m0, stg, nc, wrow0);
+            tc::bulk_commit();
+          }
+        } else if (valid) {
+#pragma unroll
+          for (int j8 = 0; j8 < 4; ++j8) {
+            const int n = nc + j8 * 8;
+            if (n >= N) break;
+            if (p.c_f32) st_f32x8(static_cast<float *>(p.C) + row * p.ldc + n, v + j8 * 8);
+            else st_bf16x8(static_cast<uint16_t *>(p.C) + row * p.ldc + n, v + j8 * 8);
+          }
+        }
+      } else {  // SWIGLU_BWD: v = dAct, H = [gate | up]
+        float dg[32], du[32];
 #pragma unroll
         for (int j8 = 0; j8 < 4; ++j8) {
-          const int n = nc + j8 * 8;
-          if (n >= N) break;
-          float *x = v + j8 * 8;
-          if (EPI == MOE_EPI_NONE) {
-            if (p.ps != nullptr) {
-              const float *pv = reinterpret_cast<const float *>(&cur[2 * j8]);
+          float g[8], u[8];
+          bf16x8_to_f32(cur[j8], g);
+          bf16x8_to_f32(cur[4 + j8], u);
 #pragma unroll
-              for (int q = 0; q < 8; ++q) x[q] += pv[q];
-            }
-            if (p.c_f32)
-              st_f32x8(static_cast<float *>(p.C) + row * p.ldc + n, x);
-            else
-              st_bf16x8(static_cast<uint16_t *>(p.C) + row * p.ldc + n, x);
-          } else {  // SWIGLU_BWD: x = dAct, aux = H = [gate | up]
-            float g[8], u[8], dg[8], du[8];
-            bf16x8_to_f32(cur[j8], g);
-            bf16x8_to_f32(cur[4 + j8], u);
+          for (int k = 0; k < 8; ++k) {
+            const float x = v[j8 * 8 + k];
+            const float sg = sigmoid_f(g[k]);
+            dg[j8 * 8 + k] = x * u[k] * sg * (1.0f + g[k] * (1.0f - sg));
+            du[j8 * 8 + k] = x * g[k] * sg;
+          }
+        }
+        if (bulk) {
+          stage_acquire(lane);
+          stage_bf16(stg, lane, dg);
+          stage_bf16(stg + 2048, lane, du);
+          stage_release();
+          if (lane == 0) {
+            tc::tma_store_2d(om.m0, stg, nc, wrow0);
+            tc::tma_store_2d(om.m1, stg + 2048, nc, wrow0);
+            tc::bulk_commit();
+          }
+        } else if (valid) {
+          uint16_t *dH = static_cast<uint16_t *>(p.C) + row * p.ldc;
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const float sg = sigmoid_f(g[q]);
-              dg[q] = x[q] * u[q] * sg * (1.0f + g[q] * (1.0f - sg));
-              du[q] = x[q] * g[q] * sg;
-            }
-            uint16_t *dH = static_cast<uint16_t *>(p.C) + row * p.ldc;
-            st_bf16x8(dH + n, dg);
-            st_bf16x8(dH + N + n, du);
+          for (int j8 = 0; j8 < 4; ++j8) {
+            const int n = nc + j8 * 8;
+            if (n >= N) break;
+            st_bf16x8(dH + n, dg + j8 * 8);
+            st_bf16x8(dH + N + n, du + j8 * 8);
           }
         }
       }
 #pragma unroll
-      for (int q = 0; q < 8; ++q) cur[q] = nxt[q];
+      for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
     }
   }
 }
 
-// tgmm epilogue: thread = one output row m of W_e.  `zero`: the expert had no
-// rows, so TMEM is not read.
-MOE_DEVINL void epilogue_tgmm(const TcParams &p, const TileInfo &ti, uint32_t taddr, int rit,
-                              int half, bool zero) {
-  const int m = ti.m_idx * BM + rit;
+// tgmm epilogue: warp q owns output rows m in [m_idx*128 + 32q, +32) of W_e.
+// `zero`: the expert had no rows, so TMEM is not read.  Bulk stores unless
+// accumulating into fp32 W (read-modify-write with plain loads and stores).
+MOE_DEVINL void epilogue_tgmm(const TcParams &p, const TileInfo &ti, uint32_t taddr, int q,
+                              int lane, uint8_t *stg, const OutMaps &om, bool zero) {
+  const int wm0 = ti.m_idx * BM + q * 32;
+  const int m = wm0 + lane;
   const bool valid = m < p.M;
   const int n0 = ti.n_idx * BN;
   const int64_t base = (int64_t)ti.e * p.stride_w + (int64_t)m * p.ldc;
 #pragma unroll 1
-  for (int c = half * (BN / 32 / 2); c < (half + 1) * (BN / 32 / 2); ++c) {
+  for (int c = 0; c < BN / 32; ++c) {
     const int nc = n0 + c * 32;
     if (nc >= p.N) break;
     float v[32];
     if (zero) {
 #pragma unroll
-      for (int q = 0; q < 32; ++q) v[q] = 0.f;
+      for (int j = 0; j < 32; ++j) v[j] = 0.f;
     } else {
       tc::tmem_ld32(taddr + c * 32, v);
+    }
+    if (!p.accumulate) {
+      stage_acquire(lane);
+      if (p.c_f32) stage_f32(stg, lane, v);
+      else stage_bf16(stg, lane, v);
+      stage_release();
+      if (lane == 0) {
+        tc::tma_store_3d(om.m0, stg, nc, wm0, ti.e);
+        tc::bulk_commit();
+      }
+      continue;
     }
     if (!valid) continue;
 #pragma unroll
@@ -338,18 +434,12 @@ MOE_DEVINL void epilogue_tgmm(const TcParams &p, const TileInfo &ti, uint32_t ta
       const int n = nc + j8 * 8;
       if (n >= p.N) break;
       float *x = v + j8 * 8;
-      if (p.c_f32) {
-        float *W = static_cast<float *>(p.C) + base + n;
-        if (p.accumulate) {
-          float o[8];
-          ld_f32x8(W, o);
+      float *W = static_cast<float *>(p.C) + base + n;
+      float o[8];
+      ld_f32x8(W, o);
 #pragma unroll
-          for (int q = 0; q < 8; ++q) x[q] += o[q];
-        }
-        st_f32x8(W, x);
-      } else {
-        st_bf16x8(static_cast<uint16_t *>(p.C) + base + n, x);
-      }
+      for (int k = 0; k < 8; ++k) x[k] += o[k];
+      st_f32x8(W, x);
     }
   }
 }
@@ -358,7 +448,8 @@ MOE_DEVINL void epilogue_tgmm(const TcParams &p, const TileInfo &ti, uint32_t ta
 template <int KIND, bool B_MN, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
 gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-              const TcParams p) {
+              const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1,
+              const __grid_constant__ CUtensorMap tmC2, const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -382,6 +473,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   if (warp == 0 && lane == 0) {
     tc::tma_prefetch(&tmA);
     tc::tma_prefetch(&tmB);
+    tc::tma_prefetch(&tmC0);
   }
   for (int i = threadIdx.x; i <= p.E; i += kThreads)
     bk.off[i] = min(max(__ldg(p.offsets + i), 0), p.rows_cap);
@@ -541,32 +633,36 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     __syncwarp();
     tc::mbar_wait_drain(&bk.drain, 0, kWaitLimitNs);
   } else {
-    const int q = warp & 3;              // TMEM lane quarter this warp may read
-    const int half = (warp - 2) >> 2;    // column half of the tile
+    const int q = warp & 3;  // TMEM lane quarter this warp may read = its tile rows
     const int rit = q * 32 + lane;
+    uint8_t *stg = smem + kStages * STAGE_BYTES + BOOK_BYTES + (warp - 2) * kStgBytes;
+    const OutMaps om{&tmC0, &tmC1, &tmC2};
     uint32_t acc_it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const TileInfo ti = decode_tile<KIND>(bk, p, t);
       if (KIND == KIND_GMM && ti.row_end <= ti.row0) continue;
       if (KIND == KIND_TGMM && ti.kblocks == 0) {
-        if (!p.accumulate) epilogue_tgmm(p, ti, 0, rit, half, true);
+        if (!p.accumulate) epilogue_tgmm(p, ti, 0, q, lane, stg, om, true);
         continue;
       }
-      epilogue_prefetch<KIND, EPI>(p, ti, rit, half);
+      epilogue_prefetch<KIND, EPI>(p, ti, rit);
       const uint32_t a = acc_it & 1;
       const uint32_t aph = (acc_it >> 1) & 1;
       if (!tc::mbar_wait(&bk.tfull[a], aph, abort_flag, kWaitLimitNs)) break;
       tc::tc_fence_after();
       const uint32_t taddr = tmem + a * BN + (static_cast<uint32_t>(q * 32) << 16);
       if (KIND == KIND_GMM)
-        epilogue_gmm<EPI>(p, ti, taddr, rit, half);
+        epilogue_gmm<EPI>(p, ti, taddr, q, lane, stg, om);
       else
-        epilogue_tgmm(p, ti, taddr, rit, half, false);
+        epilogue_tgmm(p, ti, taddr, q, lane, stg, om, false);
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&bk.tempty[a]);
       ++acc_it;
     }
+    // every bulk store of this warp has completed before the CTA exits
+    if (lane == 0) tc::bulk_wait0();
+    __syncwarp();
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -592,7 +688,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // bf16 tensor map with 128-byte swizzle; dims[0] is the contiguous dimension.
 bool make_map(CUtensorMap *m, const void *base, int rank, const uint64_t *dims,
-              const uint64_t *strides_bytes, const uint32_t *box) {
+              const uint64_t *strides_bytes, const uint32_t *box,
+              CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t d[3], st[2];
@@ -602,14 +700,26 @@ bool make_map(CUtensorMap *m, const void *base, int rank, const uint64_t *dims,
     b[i] = box[i];
   }
   for (int i = 0; i < rank - 1; ++i) st[i] = strides_bytes[i];
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), d, st, b, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return fn(m, dtype, rank, const_cast<void *>(base), d, st, b, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Output map of a [rows, cols] row-major matrix written in 32 x 32 blocks
+// (bf16: 64-byte rows, 64-byte swizzle; fp32: 128-byte rows, 128-byte swizzle).
+bool make_out_map(CUtensorMap *m, const void *base, bool f32, int64_t cols, int64_t rows,
+                  int64_t ld) {
+  const uint64_t dims[2] = {(uint64_t)cols, (uint64_t)rows};
+  const uint64_t st[1] = {(uint64_t)ld * (f32 ? 4 : 2)};
+  const uint32_t box[2] = {32, 32};
+  return make_map(m, base, 2, dims, st, box,
+                  f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                  f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 template <int KIND, bool B_MN, int EPI>
-moe_status_t launch_tc(const CUtensorMap &ma, const CUtensorMap &mb, const TcParams &p,
-                       int64_t tiles_upper, cudaStream_t s) {
+moe_status_t launch_tc(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap *mc,
+                       const TcParams &p, int64_t tiles_upper, cudaStream_t s) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
@@ -622,7 +732,8 @@ moe_status_t launch_tc(const CUtensorMap &ma, const CUtensorMap &mb, const TcPar
     return MOE_ERR_CUDA;
   }
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(num_sms(), tiles_upper));
-  gmm_tc_kernel<KIND, B_MN, EPI><<<grid, kThreads, SMEM_BYTES, s>>>(ma, mb, p);
+  gmm_tc_kernel<KIND, B_MN, EPI><<<grid, kThreads, SMEM_BYTES, s>>>(ma, mb, mc[0], mc[1], mc[2],
+                                                                    p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_error("grouped GEMM launch: %s", cudaGetErrorString(e));
@@ -689,16 +800,40 @@ moe_status_t launch_gmm(const GmmArgs &a, cudaStream_t s) {
   p.aux = a.aux;
   p.ld_aux = a.ld_aux;
   p.dev_status = a.dev_status;
+  // output maps (unused slots repeat the first)
+  CUtensorMap mc[3];
+  bool ok = true;
+  const bool f32 = a.c_dtype == MOE_DTYPE_F32;
+  if (a.epilogue == MOE_EPI_SWIGLU_FWD) {
+    const uint16_t *H = static_cast<const uint16_t *>(a.C);
+    ok = make_out_map(&mc[0], H, false, p.F, a.rows_cap, a.ldc) &&
+         make_out_map(&mc[1], H + p.F, false, p.F, a.rows_cap, a.ldc) &&
+         make_out_map(&mc[2], a.C2, false, p.F, a.rows_cap, a.ldc2);
+  } else if (a.epilogue == MOE_EPI_SWIGLU_BWD) {
+    const uint16_t *dH = static_cast<const uint16_t *>(a.C);
+    ok = make_out_map(&mc[0], dH, false, a.N, a.rows_cap, a.ldc) &&
+         make_out_map(&mc[1], dH + a.N, false, a.N, a.rows_cap, a.ldc);
+    mc[2] = mc[0];
+  } else {
+    ok = make_out_map(&mc[0], a.C, f32, a.N, a.rows_cap, a.ldc);
+    mc[1] = mc[2] = mc[0];
+  }
+  if (!ok) {
+    set_error("moe_gmm: cannot encode the TMA descriptor of the output");
+    return MOE_ERR_CUDA;
+  }
   const int64_t tiles_upper = ((a.rows_cap + BM - 1) / BM + a.E) * p.n_tiles;
   switch (a.epilogue * 2 + (b_mn ? 1 : 0)) {
-    case MOE_EPI_NONE * 2 + 1: return launch_tc<KIND_GMM, true, MOE_EPI_NONE>(ma, mb, p, tiles_upper, s);
-    case MOE_EPI_NONE * 2 + 0: return launch_tc<KIND_GMM, false, MOE_EPI_NONE>(ma, mb, p, tiles_upper, s);
+    case MOE_EPI_NONE * 2 + 1:
+      return launch_tc<KIND_GMM, true, MOE_EPI_NONE>(ma, mb, mc, p, tiles_upper, s);
+    case MOE_EPI_NONE * 2 + 0:
+      return launch_tc<KIND_GMM, false, MOE_EPI_NONE>(ma, mb, mc, p, tiles_upper, s);
     case MOE_EPI_SWIGLU_FWD * 2 + 1:
-      return launch_tc<KIND_GMM, true, MOE_EPI_SWIGLU_FWD>(ma, mb, p, tiles_upper, s);
+      return launch_tc<KIND_GMM, true, MOE_EPI_SWIGLU_FWD>(ma, mb, mc, p, tiles_upper, s);
     case MOE_EPI_SWIGLU_BWD * 2 + 1:
-      return launch_tc<KIND_GMM, true, MOE_EPI_SWIGLU_BWD>(ma, mb, p, tiles_upper, s);
+      return launch_tc<KIND_GMM, true, MOE_EPI_SWIGLU_BWD>(ma, mb, mc, p, tiles_upper, s);
     case MOE_EPI_SWIGLU_BWD * 2 + 0:
-      return launch_tc<KIND_GMM, false, MOE_EPI_SWIGLU_BWD>(ma, mb, p, tiles_upper, s);
+      return launch_tc<KIND_GMM, false, MOE_EPI_SWIGLU_BWD>(ma, mb, mc, p, tiles_upper, s);
     default:
       set_error("moe_gmm: unsupported epilogue / layout");
       return MOE_ERR_UNSUPPORTED;
@@ -742,8 +877,24 @@ moe_status_t launch_tgmm(const TgmmArgs &a, cudaStream_t s) {
   p.stride_w = a.stride_w;
   p.accumulate = a.accumulate;
   p.dev_status = a.dev_status;
+  CUtensorMap mc[3];
+  {
+    const bool f32 = a.w_dtype == MOE_DTYPE_F32;
+    const int64_t es = f32 ? 4 : 2;
+    const int64_t stride_w = a.E > 1 ? a.stride_w : (int64_t)a.M * a.ldw;
+    const uint64_t dims[3] = {(uint64_t)a.N, (uint64_t)a.M, (uint64_t)a.E};
+    const uint64_t st[2] = {(uint64_t)(a.ldw * es), (uint64_t)(stride_w * es)};
+    const uint32_t box[3] = {32, 32, 1};
+    if (!make_map(&mc[0], a.W, 3, dims, st, box,
+                  f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                  f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B)) {
+      set_error("moe_tgmm: cannot encode the TMA descriptor of W");
+      return MOE_ERR_CUDA;
+    }
+    mc[1] = mc[2] = mc[0];
+  }
   const int64_t tiles_upper = (int64_t)a.E * p.m_tiles * p.n_tiles;
-  return launch_tc<KIND_TGMM, true, MOE_EPI_NONE>(ma, mb, p, tiles_upper, s);
+  return launch_tc<KIND_TGMM, true, MOE_EPI_NONE>(ma, mb, mc, p, tiles_upper, s);
 }
 
 }  // namespace moe

@@ -103,6 +103,28 @@ MOE_DEVINL void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar, in
       : "memory");
 }
 
+// Bulk tensor stores shared -> global (the box is clipped at the tensor's
+// bounds), grouped per thread; wait_read(0) returns once every committed
+// store has finished reading its shared-memory source.
+MOE_DEVINL void tma_store_2d(const CUtensorMap *map, const void *src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1)
+               : "memory");
+}
+
+MOE_DEVINL void tma_store_3d(const CUtensorMap *map, const void *src, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+MOE_DEVINL void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+MOE_DEVINL void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+MOE_DEVINL void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Generic-proxy writes to shared memory made visible to the async proxy
 // (tensor-core operand reads).
 MOE_DEVINL void fence_proxy_async_smem() {
