@@ -45,7 +45,7 @@ constexpr int BM = 128, BN = 256, BK = 64, UK = 16;
 constexpr int kStages = 4;
 constexpr int kThreads = 192;  // producer, MMA, 4 epilogue warps
 constexpr int kEpiWarps = 4;
-constexpr int kStgBytes = 6144;  // per epilogue warp: three 32x32 bf16 blocks (or one fp32)
+constexpr int kStgBytes = 8192;  // per epilogue warp: up to four 32x32 bf16 blocks (or two fp32)
 constexpr int A_BYTES = BM * BK * 2;   // 16 KB
 constexpr int B_BYTES = BN * BK * 2;   // 32 KB
 constexpr int BOX_BYTES = 64 * 64 * 2; // one 64x64 MN-major box, 8 KB
@@ -63,14 +63,16 @@ struct Book {
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
+  uint64_t aux_full[kEpiWarps];  // SwiGLU backward: H blocks landed in a warp's staging
   uint32_t tmem_base;
   int abort_flag;
   int total_tiles;
-  int off[kMaxE + 1];
-  int cum[kMaxE + 1];
+  int cum[kMaxE + 1];            // per-expert tile prefix
 };
-constexpr int BOOK_BYTES = (int)((sizeof(Book) + 1023) / 1024 * 1024);
-constexpr int SMEM_BYTES = 1024 + kStages * STAGE_BYTES + BOOK_BYTES + kEpiWarps * kStgBytes;
+constexpr int STG_OFFSET = kStages * STAGE_BYTES;                    // 1024-aligned
+constexpr int BOOK_OFFSET = STG_OFFSET + kEpiWarps * kStgBytes;
+constexpr int SMEM_BYTES = 1024 + BOOK_OFFSET + (int)((sizeof(Book) + 127) / 128 * 128);
+static_assert(SMEM_BYTES <= 232448, "shared memory budget of one CTA");
 
 struct TcParams {
   int E;
@@ -100,6 +102,11 @@ struct TileInfo {
   int e, m_idx, n_idx, row0, row_end, kblocks;
 };
 
+// Group offsets read from global memory (through L1), clamped to [0, rows_cap].
+MOE_DEVINL int group_offset(const TcParams &p, int e) {
+  return min(max(__ldg(p.offsets + e), 0), p.rows_cap);
+}
+
 template <int KIND>
 MOE_DEVINL TileInfo decode_tile(const Book &bk, const TcParams &p, int t) {
   int lo = 0, hi = p.E - 1;
@@ -111,8 +118,8 @@ MOE_DEVINL TileInfo decode_tile(const Book &bk, const TcParams &p, int t) {
   TileInfo ti;
   ti.e = lo;
   const int local = t - bk.cum[lo];
-  ti.row0 = bk.off[lo];
-  ti.row_end = bk.off[lo + 1];
+  ti.row0 = group_offset(p, lo);
+  ti.row_end = max(group_offset(p, lo + 1), ti.row0);
   const int size = ti.row_end - ti.row0;
   const int mt = KIND == KIND_GMM ? (size + BM - 1) / BM : p.m_tiles;
   const int group = kGroupM * p.n_tiles;
@@ -138,13 +145,6 @@ MOE_DEVINL void st_f32x8(float *dst, const float *v) {
                         __float_as_uint(v[3])));
   st_v4(dst + 4, make_uint4(__float_as_uint(v[4]), __float_as_uint(v[5]), __float_as_uint(v[6]),
                             __float_as_uint(v[7])));
-}
-
-MOE_DEVINL void ld_f32x8(const float *src, float *v) {
-  const float4 a = *reinterpret_cast<const float4 *>(src);
-  const float4 b = *reinterpret_cast<const float4 *>(src + 4);
-  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
 MOE_DEVINL uint4 ld_v4_no_l1(const void *ptr) {
@@ -192,8 +192,14 @@ MOE_DEVINL void stage_release() {
   __syncwarp();
 }
 
+// Output maps of an epilogue warp (m0..m2), the H maps it loads from in the
+// SwiGLU backward (m2 = gate, m3 = up), its aux barrier and that barrier's
+// phase count.
 struct OutMaps {
-  const CUtensorMap *m0, *m1, *m2;
+  const CUtensorMap *m0, *m1, *m2, *m3;
+  uint64_t *aux_bar;
+  uint32_t aux_phase;   // H loads waited for
+  uint32_t aux_issued;  // H loads issued
 };
 
 // Before a tile's accumulator is ready: pull the epilogue's global inputs
@@ -238,9 +244,20 @@ MOE_DEVINL void epilogue_prefetch(const TcParams &p, const TileInfo &ti, int rit
 // [32q, 32q+32), thread = one row; 32-column chunks.  The global inputs of a
 // chunk are loaded one chunk ahead so that their latency overlaps the work
 // of the previous chunk.
+// SwiGLU backward: TMA loads of the warp's 32x32 gate and up blocks of H for
+// the chunk starting at column nc into its staging area (lane 0 issues).
+MOE_DEVINL void issue_aux_load(OutMaps &om, uint8_t *stg, int nc, int wrow0) {
+  ++om.aux_issued;
+  tc::mbar_expect_tx(om.aux_bar, 4096);
+  tc::tma_load_2d(stg + 4096, om.m2, om.aux_bar, nc, wrow0);
+  tc::tma_load_2d(stg + 6144, om.m3, om.aux_bar, nc, wrow0);
+}
+
+// One tile's epilogue for the ragged-M GEMM.  Warp q owns tile rows
+// [32q, 32q+32), thread = one row; 32-column chunks.
 template <int EPI>
 MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t taddr, int q,
-                             int lane, uint8_t *stg, const OutMaps &om) {
+                             int lane, uint8_t *stg, OutMaps &om, volatile int *abort_flag) {
   const int wrow0 = ti.row0 + q * 32;
   const int64_t row = (int64_t)wrow0 + lane;
   const bool valid = row < ti.row_end;
@@ -249,20 +266,23 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
     const int F = p.F;
     const int n0 = ti.n_idx * (BN / 2);
     const bool has_ps = valid && p.ps != nullptr;
+    auto load_ps = [&](int c, uint4 *g4, uint4 *u4) {
+      const int nc = n0 + c * 32;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (nc + j * 4 < F) {
+          g4[j] = ld_v4_no_l1(p.ps + row * p.ld_ps + nc + j * 4);
+          u4[j] = ld_v4_no_l1(p.ps + row * p.ld_ps + F + nc + j * 4);
+        }
+      }
+    };
+    uint4 pg[8], pu[8], ng[8], nu[8];
+    if (has_ps) load_ps(0, pg, pu);
 #pragma unroll 1
     for (int c = 0; c < BN / 2 / 32; ++c) {
       const int nc = n0 + c * 32;
       if (nc >= F) break;
-      uint4 pg[8], pu[8];
-      if (has_ps) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (nc + j * 4 < F) {
-            pg[j] = ld_v4_no_l1(p.ps + row * p.ld_ps + nc + j * 4);
-            pu[j] = ld_v4_no_l1(p.ps + row * p.ld_ps + F + nc + j * 4);
-          }
-        }
-      }
+      if (has_ps && c + 1 < BN / 2 / 32 && nc + 32 < F) load_ps(c + 1, ng, nu);
       float g[32], u[32], act[32];
       tc::tmem_ld32(taddr + c * 32, g);
       tc::tmem_ld32(taddr + BN / 2 + c * 32, u);
@@ -273,6 +293,11 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
         for (int j = 0; j < 32; ++j) {
           g[j] += fg[j];
           u[j] += fu[j];
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          pg[j] = ng[j];
+          pu[j] = nu[j];
         }
       }
 #pragma unroll
@@ -302,23 +327,72 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
         }
       }
     }
-  } else {
+  } else if (EPI == MOE_EPI_SWIGLU_BWD) {
     const int N = p.N;
     const int n0 = ti.n_idx * BN;
-    // inputs of a chunk: SwiGLU backward 4 x 16 B of gate and 4 x 16 B of up
-    // from H; partial sum 8 x 16 B of fp32
-    const bool has_in = valid && (EPI == MOE_EPI_SWIGLU_BWD || p.ps != nullptr);
+    const uint8_t *aux_g = stg + 4096;
+    const uint8_t *aux_u = stg + 6144;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      const int nc = n0 + c * 32;
+      if (nc >= N) break;
+      // this chunk's H blocks (issued one chunk ahead) -> registers
+      if (!tc::mbar_wait(om.aux_bar, om.aux_phase & 1, abort_flag, kWaitLimitNs)) return;
+      ++om.aux_phase;
+      float g[32], u[32];
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        const int off = lane * 64 + ((cc ^ ((lane >> 1) & 3)) << 4);
+        bf16x8_to_f32(*reinterpret_cast<const uint4 *>(aux_g + off), g + 8 * cc);
+        bf16x8_to_f32(*reinterpret_cast<const uint4 *>(aux_u + off), u + 8 * cc);
+      }
+      __syncwarp();
+      if (lane == 0 && c + 1 < BN / 32 && nc + 32 < N) {
+        tc::fence_proxy_async_smem();
+        issue_aux_load(om, stg, nc + 32, wrow0);
+      }
+      float v[32];
+      tc::tmem_ld32(taddr + c * 32, v);
+      float dg[32], du[32];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const float sg = sigmoid_f(g[k]);
+        dg[k] = v[k] * u[k] * sg * (1.0f + g[k] * (1.0f - sg));
+        du[k] = v[k] * g[k] * sg;
+      }
+      if (bulk) {
+        stage_acquire(lane);
+        stage_bf16(stg, lane, dg);
+        stage_bf16(stg + 2048, lane, du);
+        stage_release();
+        if (lane == 0) {
+          tc::tma_store_2d(om.m0, stg, nc, wrow0);
+          tc::tma_store_2d(om.m1, stg + 2048, nc, wrow0);
+          tc::bulk_commit();
+        }
+      } else if (valid) {
+        uint16_t *dH = static_cast<uint16_t *>(p.C) + row * p.ldc;
+#pragma unroll
+        for (int j8 = 0; j8 < 4; ++j8) {
+          const int n = nc + j8 * 8;
+          if (n >= N) break;
+          st_bf16x8(dH + n, dg + j8 * 8);
+          st_bf16x8(dH + N + n, du + j8 * 8);
+        }
+      }
+    }
+  } else {  // MOE_EPI_NONE
+    const int N = p.N;
+    const int n0 = ti.n_idx * BN;
+    // in place (C is the fp32 partial sum): the TMA engine adds the block in L2
+    const bool in_place = p.ps != nullptr && static_cast<const void *>(p.ps) == p.C;
+    const bool has_in = valid && p.ps != nullptr && !(in_place && bulk);
     auto load_chunk = [&](int c, uint4 *buf) {
       const int nc = n0 + c * 32;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        if (EPI == MOE_EPI_SWIGLU_BWD) {
-          const int n = nc + (j & 3) * 8;
-          if (n < N) buf[j] = ld_nc_v4(p.aux + row * p.ld_aux + (j < 4 ? 0 : N) + n);
-        } else {
-          const int n = nc + j * 4;
-          if (n < N) buf[j] = ld_v4_no_l1(p.ps + row * p.ld_ps + n);
-        }
+        const int n = nc + j * 4;
+        if (n < N) buf[j] = ld_v4_no_l1(p.ps + row * p.ld_ps + n);
       }
     };
     uint4 cur[8], nxt[8];
@@ -330,82 +404,43 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
       if (has_in && c + 1 < BN / 32 && nc + 32 < N) load_chunk(c + 1, nxt);
       float v[32];
       tc::tmem_ld32(taddr + c * 32, v);
-      if (EPI == MOE_EPI_NONE) {
-        if (p.ps != nullptr && valid) {
-          const float *pv = reinterpret_cast<const float *>(cur);
+      if (has_in) {
+        const float *pv = reinterpret_cast<const float *>(cur);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] += pv[j];
-        }
-        if (bulk) {
-          stage_acquire(lane);
-          if (p.c_f32) stage_f32(stg, lane, v);
-          else stage_bf16(stg, lane, v);
-          stage_release();
-          if (lane == 0) {
-            tc::tma_store_2d(om.m0, stg, nc, wrow0);
-            tc::bulk_commit();
-          }
-        } else if (valid) {
+        for (int j = 0; j < 32; ++j) v[j] += pv[j];
 #pragma unroll
-          for (int j8 = 0; j8 < 4; ++j8) {
-            const int n = nc + j8 * 8;
-            if (n >= N) break;
-            if (p.c_f32) st_f32x8(static_cast<float *>(p.C) + row * p.ldc + n, v + j8 * 8);
-            else st_bf16x8(static_cast<uint16_t *>(p.C) + row * p.ldc + n, v + j8 * 8);
-          }
+        for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
+      }
+      if (bulk) {
+        stage_acquire(lane);
+        if (p.c_f32) stage_f32(stg, lane, v);
+        else stage_bf16(stg, lane, v);
+        stage_release();
+        if (lane == 0) {
+          if (in_place) tc::tma_reduce_add_2d(om.m0, stg, nc, wrow0);
+          else tc::tma_store_2d(om.m0, stg, nc, wrow0);
+          tc::bulk_commit();
         }
-      } else {  // SWIGLU_BWD: v = dAct, H = [gate | up]
-        float dg[32], du[32];
+      } else if (valid) {
 #pragma unroll
         for (int j8 = 0; j8 < 4; ++j8) {
-          float g[8], u[8];
-          bf16x8_to_f32(cur[j8], g);
-          bf16x8_to_f32(cur[4 + j8], u);
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const float x = v[j8 * 8 + k];
-            const float sg = sigmoid_f(g[k]);
-            dg[j8 * 8 + k] = x * u[k] * sg * (1.0f + g[k] * (1.0f - sg));
-            du[j8 * 8 + k] = x * g[k] * sg;
-          }
-        }
-        if (bulk) {
-          stage_acquire(lane);
-          stage_bf16(stg, lane, dg);
-          stage_bf16(stg + 2048, lane, du);
-          stage_release();
-          if (lane == 0) {
-            tc::tma_store_2d(om.m0, stg, nc, wrow0);
-            tc::tma_store_2d(om.m1, stg + 2048, nc, wrow0);
-            tc::bulk_commit();
-          }
-        } else if (valid) {
-          uint16_t *dH = static_cast<uint16_t *>(p.C) + row * p.ldc;
-#pragma unroll
-          for (int j8 = 0; j8 < 4; ++j8) {
-            const int n = nc + j8 * 8;
-            if (n >= N) break;
-            st_bf16x8(dH + n, dg + j8 * 8);
-            st_bf16x8(dH + N + n, du + j8 * 8);
-          }
+          const int n = nc + j8 * 8;
+          if (n >= N) break;
+          if (p.c_f32) st_f32x8(static_cast<float *>(p.C) + row * p.ldc + n, v + j8 * 8);
+          else st_bf16x8(static_cast<uint16_t *>(p.C) + row * p.ldc + n, v + j8 * 8);
         }
       }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
     }
   }
 }
 
 // tgmm epilogue: warp q owns output rows m in [m_idx*128 + 32q, +32) of W_e.
-// `zero`: the expert had no rows, so TMEM is not read.  Bulk stores unless
-// accumulating into fp32 W (read-modify-write with plain loads and stores).
+// `zero`: the expert had no rows, so TMEM is not read.  Bulk stores, or bulk
+// fp32 reduce-adds into W when accumulating; the box is clipped at M and N.
 MOE_DEVINL void epilogue_tgmm(const TcParams &p, const TileInfo &ti, uint32_t taddr, int q,
                               int lane, uint8_t *stg, const OutMaps &om, bool zero) {
   const int wm0 = ti.m_idx * BM + q * 32;
-  const int m = wm0 + lane;
-  const bool valid = m < p.M;
   const int n0 = ti.n_idx * BN;
-  const int64_t base = (int64_t)ti.e * p.stride_w + (int64_t)m * p.ldc;
 #pragma unroll 1
   for (int c = 0; c < BN / 32; ++c) {
     const int nc = n0 + c * 32;
@@ -417,29 +452,14 @@ MOE_DEVINL void epilogue_tgmm(const TcParams &p, const TileInfo &ti, uint32_t ta
     } else {
       tc::tmem_ld32(taddr + c * 32, v);
     }
-    if (!p.accumulate) {
-      stage_acquire(lane);
-      if (p.c_f32) stage_f32(stg, lane, v);
-      else stage_bf16(stg, lane, v);
-      stage_release();
-      if (lane == 0) {
-        tc::tma_store_3d(om.m0, stg, nc, wm0, ti.e);
-        tc::bulk_commit();
-      }
-      continue;
-    }
-    if (!valid) continue;
-#pragma unroll
-    for (int j8 = 0; j8 < 4; ++j8) {
-      const int n = nc + j8 * 8;
-      if (n >= p.N) break;
-      float *x = v + j8 * 8;
-      float *W = static_cast<float *>(p.C) + base + n;
-      float o[8];
-      ld_f32x8(W, o);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) x[k] += o[k];
-      st_f32x8(W, x);
+    stage_acquire(lane);
+    if (p.c_f32) stage_f32(stg, lane, v);
+    else stage_bf16(stg, lane, v);
+    stage_release();
+    if (lane == 0) {
+      if (p.accumulate) tc::tma_reduce_add_3d(om.m0, stg, nc, wm0, ti.e);
+      else tc::tma_store_3d(om.m0, stg, nc, wm0, ti.e);
+      tc::bulk_commit();
     }
   }
 }
@@ -449,11 +469,12 @@ template <int KIND, bool B_MN, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
 gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1,
-              const __grid_constant__ CUtensorMap tmC2, const TcParams p) {
+              const __grid_constant__ CUtensorMap tmC2, const __grid_constant__ CUtensorMap tmC3,
+              const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  Book &bk = *reinterpret_cast<Book *>(smem + kStages * STAGE_BYTES);
+  Book &bk = *reinterpret_cast<Book *>(smem + BOOK_OFFSET);
   volatile int *abort_flag = &bk.abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -467,6 +488,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       tc::mbar_init(&bk.tempty[a], kEpiWarps);
     }
     tc::mbar_init(&bk.drain, 1);
+    for (int w = 0; w < kEpiWarps; ++w) tc::mbar_init(&bk.aux_full[w], 1);
     bk.abort_flag = 0;
     tc::fence_mbar_init();
   }
@@ -475,8 +497,6 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     tc::tma_prefetch(&tmB);
     tc::tma_prefetch(&tmC0);
   }
-  for (int i = threadIdx.x; i <= p.E; i += kThreads)
-    bk.off[i] = min(max(__ldg(p.offsets + i), 0), p.rows_cap);
   __syncthreads();
   if (warp == 0) {
     // per-expert tile counts and their exclusive scan (warp shuffles)
@@ -485,7 +505,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       const int e = c0 + lane;
       int tiles = 0;
       if (e < p.E) {
-        const int size = max(bk.off[e + 1] - bk.off[e], 0);
+        const int size = max(group_offset(p, e + 1) - group_offset(p, e), 0);
         tiles = (KIND == KIND_GMM ? (size + BM - 1) / BM : p.m_tiles) * p.n_tiles;
       }
       int incl = tiles;
@@ -503,7 +523,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     }
     // offsets must be non-decreasing; clamp a bad table to empty groups
     for (int e = lane; e < p.E; e += 32)
-      if (bk.off[e + 1] < bk.off[e]) moe_set_status(p.dev_status, MOE_ERR_DEVICE);
+      if (group_offset(p, e + 1) < group_offset(p, e)) moe_set_status(p.dev_status, MOE_ERR_DEVICE);
   }
   if (warp == 1) {
     tc::tmem_alloc(&bk.tmem_base, kTmemCols);
@@ -635,8 +655,8 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   } else {
     const int q = warp & 3;  // TMEM lane quarter this warp may read = its tile rows
     const int rit = q * 32 + lane;
-    uint8_t *stg = smem + kStages * STAGE_BYTES + BOOK_BYTES + (warp - 2) * kStgBytes;
-    const OutMaps om{&tmC0, &tmC1, &tmC2};
+    uint8_t *stg = smem + STG_OFFSET + (warp - 2) * kStgBytes;
+    OutMaps om{&tmC0, &tmC1, &tmC2, &tmC3, &bk.aux_full[warp - 2], 0u, 0u};
     uint32_t acc_it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const TileInfo ti = decode_tile<KIND>(bk, p, t);
@@ -646,13 +666,15 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         continue;
       }
       epilogue_prefetch<KIND, EPI>(p, ti, rit);
+      if (KIND == KIND_GMM && EPI == MOE_EPI_SWIGLU_BWD && lane == 0)
+        issue_aux_load(om, stg, ti.n_idx * BN, ti.row0 + q * 32);  // first chunk's H blocks
       const uint32_t a = acc_it & 1;
       const uint32_t aph = (acc_it >> 1) & 1;
       if (!tc::mbar_wait(&bk.tfull[a], aph, abort_flag, kWaitLimitNs)) break;
       tc::tc_fence_after();
       const uint32_t taddr = tmem + a * BN + (static_cast<uint32_t>(q * 32) << 16);
       if (KIND == KIND_GMM)
-        epilogue_gmm<EPI>(p, ti, taddr, q, lane, stg, om);
+        epilogue_gmm<EPI>(p, ti, taddr, q, lane, stg, om, abort_flag);
       else
         epilogue_tgmm(p, ti, taddr, q, lane, stg, om, false);
       tc::tc_fence_before();
@@ -660,8 +682,11 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       if (lane == 0) tc::mbar_arrive(&bk.tempty[a]);
       ++acc_it;
     }
-    // every bulk store of this warp has completed before the CTA exits
+    // every bulk store and H load of this warp has completed before the CTA exits
     if (lane == 0) tc::bulk_wait0();
+    if (KIND == KIND_GMM && EPI == MOE_EPI_SWIGLU_BWD &&
+        __shfl_sync(0xffffffffu, om.aux_issued, 0) != om.aux_phase)
+      tc::mbar_wait_drain(om.aux_bar, om.aux_phase & 1, kWaitLimitNs / 4);
     __syncwarp();
   }
   tc::tc_fence_before();
@@ -733,7 +758,7 @@ moe_status_t launch_tc(const CUtensorMap &ma, const CUtensorMap &mb, const CUten
   }
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(num_sms(), tiles_upper));
   gmm_tc_kernel<KIND, B_MN, EPI><<<grid, kThreads, SMEM_BYTES, s>>>(ma, mb, mc[0], mc[1], mc[2],
-                                                                    p);
+                                                                    mc[3], p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_error("grouped GEMM launch: %s", cudaGetErrorString(e));
@@ -801,7 +826,7 @@ moe_status_t launch_gmm(const GmmArgs &a, cudaStream_t s) {
   p.ld_aux = a.ld_aux;
   p.dev_status = a.dev_status;
   // output maps (unused slots repeat the first)
-  CUtensorMap mc[3];
+  CUtensorMap mc[4];
   bool ok = true;
   const bool f32 = a.c_dtype == MOE_DTYPE_F32;
   if (a.epilogue == MOE_EPI_SWIGLU_FWD) {
@@ -809,14 +834,17 @@ moe_status_t launch_gmm(const GmmArgs &a, cudaStream_t s) {
     ok = make_out_map(&mc[0], H, false, p.F, a.rows_cap, a.ldc) &&
          make_out_map(&mc[1], H + p.F, false, p.F, a.rows_cap, a.ldc) &&
          make_out_map(&mc[2], a.C2, false, p.F, a.rows_cap, a.ldc2);
+    mc[3] = mc[0];
   } else if (a.epilogue == MOE_EPI_SWIGLU_BWD) {
     const uint16_t *dH = static_cast<const uint16_t *>(a.C);
+    // m0/m1: dH gate / up (stores); m2/m3: H gate / up (loads, same block shape)
     ok = make_out_map(&mc[0], dH, false, a.N, a.rows_cap, a.ldc) &&
-         make_out_map(&mc[1], dH + a.N, false, a.N, a.rows_cap, a.ldc);
-    mc[2] = mc[0];
+         make_out_map(&mc[1], dH + a.N, false, a.N, a.rows_cap, a.ldc) &&
+         make_out_map(&mc[2], a.aux, false, a.N, a.rows_cap, a.ld_aux) &&
+         make_out_map(&mc[3], a.aux + a.N, false, a.N, a.rows_cap, a.ld_aux);
   } else {
     ok = make_out_map(&mc[0], a.C, f32, a.N, a.rows_cap, a.ldc);
-    mc[1] = mc[2] = mc[0];
+    mc[1] = mc[2] = mc[3] = mc[0];
   }
   if (!ok) {
     set_error("moe_gmm: cannot encode the TMA descriptor of the output");
@@ -877,7 +905,7 @@ moe_status_t launch_tgmm(const TgmmArgs &a, cudaStream_t s) {
   p.stride_w = a.stride_w;
   p.accumulate = a.accumulate;
   p.dev_status = a.dev_status;
-  CUtensorMap mc[3];
+  CUtensorMap mc[4];
   {
     const bool f32 = a.w_dtype == MOE_DTYPE_F32;
     const int64_t es = f32 ? 4 : 2;
@@ -891,7 +919,7 @@ moe_status_t launch_tgmm(const TgmmArgs &a, cudaStream_t s) {
       set_error("moe_tgmm: cannot encode the TMA descriptor of W");
       return MOE_ERR_CUDA;
     }
-    mc[1] = mc[2] = mc[0];
+    mc[1] = mc[2] = mc[3] = mc[0];
   }
   const int64_t tiles_upper = (int64_t)a.E * p.m_tiles * p.n_tiles;
   return launch_tc<KIND_TGMM, true, MOE_EPI_NONE>(ma, mb, mc, p, tiles_upper, s);
