@@ -28,7 +28,11 @@
 // Tiles never straddle two experts.  The tile list is derived on the device
 // from group_offsets (no host synchronisation); tiles are visited expert by
 // expert in groups of 32 row tiles so that concurrently running CTAs share
-// their A rows and B columns in L2.  Every wait is bounded: on time-out the
+// their A rows and B columns in L2.  CTAs run in clusters of two that take
+// adjacent row tiles of the same expert and column tile: each fetches its
+// own A tile and half of the shared B tile, multicast into both CTAs, so a
+// CTA pulls 32 KB instead of 48 KB per 128x256x64 step from L2; the MMA
+// warps release a stage in both CTAs.  Every wait is bounded: on time-out the
 // CTA raises an abort flag, winds down, drains its in-flight copies and
 // MMAs, frees TMEM and reports MOE_ERR_TIMEOUT through dev_status.
 #include <cudaTypedefs.h>
@@ -51,7 +55,7 @@ constexpr int B_BYTES = BN * BK * 2;   // 32 KB
 constexpr int BOX_BYTES = 64 * 64 * 2; // one 64x64 MN-major box, 8 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int kMaxE = 256;
-constexpr int kGroupM = 32;
+constexpr int kGroupPairs = 16;  // raster group: 16 row-tile pairs x all column tiles
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr int kTmemCols = 2 * BN;                 // two accumulators
 
@@ -107,8 +111,11 @@ MOE_DEVINL int group_offset(const TcParams &p, int e) {
   return min(max(__ldg(p.offsets + e), 0), p.rows_cap);
 }
 
+// Tiles are handed out in pairs: the two CTAs of a cluster take row tiles
+// 2*pm and 2*pm + 1 of the same expert and column tile (the second one may lie
+// past the expert's rows; it then runs through the pipeline and stores nothing).
 template <int KIND>
-MOE_DEVINL TileInfo decode_tile(const Book &bk, const TcParams &p, int t) {
+MOE_DEVINL TileInfo decode_tile(const Book &bk, const TcParams &p, int t, int crank) {
   int lo = 0, hi = p.E - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -122,12 +129,13 @@ MOE_DEVINL TileInfo decode_tile(const Book &bk, const TcParams &p, int t) {
   ti.row_end = max(group_offset(p, lo + 1), ti.row0);
   const int size = ti.row_end - ti.row0;
   const int mt = KIND == KIND_GMM ? (size + BM - 1) / BM : p.m_tiles;
-  const int group = kGroupM * p.n_tiles;
+  const int mp = (mt + 1) / 2;                   // row-tile pairs
+  const int group = kGroupPairs * p.n_tiles;
   const int g = local / group;
   const int within = local - g * group;
-  const int gm = min(kGroupM, mt - g * kGroupM);
+  const int gm = min(kGroupPairs, mp - g * kGroupPairs);
   ti.n_idx = within / gm;
-  ti.m_idx = g * kGroupM + (within - ti.n_idx * gm);
+  ti.m_idx = 2 * (g * kGroupPairs + (within - ti.n_idx * gm)) + crank;
   if (KIND == KIND_GMM) {
     ti.row0 += ti.m_idx * BM;
     ti.kblocks = (p.K + BK - 1) / BK;
@@ -466,7 +474,7 @@ MOE_DEVINL void epilogue_tgmm(const TcParams &p, const TileInfo &ti, uint32_t ta
 
 // ------------------------------------------------------------------ kernel
 template <int KIND, bool B_MN, int EPI>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1,
               const __grid_constant__ CUtensorMap tmC2, const __grid_constant__ CUtensorMap tmC3,
@@ -477,11 +485,15 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   Book &bk = *reinterpret_cast<Book *>(smem + BOOK_OFFSET);
   volatile int *abort_flag = &bk.abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int crank = (int)tc::cluster_ctarank();
+  const int cid = (int)tc::cluster_id_x();
+  const int ncl = (int)tc::nclusters_x();
+  constexpr uint16_t kPair = 0x3;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       tc::mbar_init(&bk.full[s], 1);
-      tc::mbar_init(&bk.empty[s], 1);
+      tc::mbar_init(&bk.empty[s], 2);  // both CTAs' MMA warps release a stage
     }
     for (int a = 0; a < 2; ++a) {
       tc::mbar_init(&bk.tfull[a], 1);
@@ -506,7 +518,8 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       int tiles = 0;
       if (e < p.E) {
         const int size = max(group_offset(p, e + 1) - group_offset(p, e), 0);
-        tiles = (KIND == KIND_GMM ? (size + BM - 1) / BM : p.m_tiles) * p.n_tiles;
+        const int mt = KIND == KIND_GMM ? (size + BM - 1) / BM : p.m_tiles;
+        tiles = (mt + 1) / 2 * p.n_tiles;
       }
       int incl = tiles;
 #pragma unroll
@@ -531,6 +544,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   }
   tc::tc_fence_before();
   __syncthreads();
+  tc::cluster_sync();  // both CTAs' barriers exist before any multicast lands
   tc::tc_fence_after();
   const uint32_t tmem = bk.tmem_base;
   const int total = bk.total_tiles;
@@ -538,9 +552,8 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   uint32_t issued = 0;  // producer: k-blocks issued (ring position)
   if (warp == 0) {
     if (lane == 0) {
-      for (int t = blockIdx.x; t < total; t += gridDim.x) {
-        const TileInfo ti = decode_tile<KIND>(bk, p, t);
-        if (ti.row_end <= ti.row0 && KIND == KIND_GMM) continue;
+      for (int t = cid; t < total; t += ncl) {
+        const TileInfo ti = decode_tile<KIND>(bk, p, t, crank);
         bool ok = true;
         for (int kb = 0; kb < ti.kblocks; ++kb) {
           const int s = issued % kStages;
@@ -553,23 +566,22 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
           uint8_t *sb = sa + A_BYTES;
           uint64_t *fb = &bk.full[s];
           tc::mbar_expect_tx(fb, STAGE_BYTES);
+          // own A tile; this CTA's half of the shared B tile, multicast to the pair
           if (KIND == KIND_GMM) {
             tc::tma_load_2d(sa, &tmA, fb, kb * BK, ti.row0);
             if (B_MN) {
-              if (EPI == MOE_EPI_SWIGLU_FWD) {
-                const int n0 = ti.n_idx * (BN / 2);
-                tc::tma_load_3d(sb, &tmB, fb, n0, kb * BK, ti.e);
-                tc::tma_load_3d(sb + BOX_BYTES, &tmB, fb, n0 + 64, kb * BK, ti.e);
-                tc::tma_load_3d(sb + 2 * BOX_BYTES, &tmB, fb, p.F + n0, kb * BK, ti.e);
-                tc::tma_load_3d(sb + 3 * BOX_BYTES, &tmB, fb, p.F + n0 + 64, kb * BK, ti.e);
-              } else {
-                const int n0 = ti.n_idx * BN;
+              // MN-major B: four 64-column boxes, boxes 2*crank and 2*crank+1 from here
+              const int n0 = EPI == MOE_EPI_SWIGLU_FWD ? ti.n_idx * (BN / 2) : ti.n_idx * BN;
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                  tc::tma_load_3d(sb + i * BOX_BYTES, &tmB, fb, n0 + 64 * i, kb * BK, ti.e);
+              for (int i = 2 * crank; i < 2 * crank + 2; ++i) {
+                const int x = EPI == MOE_EPI_SWIGLU_FWD ? (i < 2 ? n0 + 64 * i : p.F + n0 + 64 * (i - 2))
+                                                        : n0 + 64 * i;
+                tc::tma_load_3d_mc(sb + i * BOX_BYTES, &tmB, fb, x, kb * BK, ti.e, kPair);
               }
             } else {
-              tc::tma_load_3d(sb, &tmB, fb, kb * BK, ti.n_idx * BN, ti.e);
+              // K-major B: two 128-row boxes, row half `crank` from here
+              tc::tma_load_3d_mc(sb + crank * (B_BYTES / 2), &tmB, fb, kb * BK,
+                                 ti.n_idx * BN + crank * (BN / 2), ti.e, kPair);
             }
           } else {
             const int r = ti.row0 + kb * BK;
@@ -578,7 +590,8 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             tc::tma_load_2d(sa, &tmA, fb, m0, r);
             tc::tma_load_2d(sa + BOX_BYTES, &tmA, fb, m0 + 64, r);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) tc::tma_load_2d(sb + i * BOX_BYTES, &tmB, fb, n0 + 64 * i, r);
+            for (int i = 2 * crank; i < 2 * crank + 2; ++i)
+              tc::tma_load_2d_mc(sb + i * BOX_BYTES, &tmB, fb, n0 + 64 * i, r, kPair);
           }
           ++issued;
         }
@@ -592,9 +605,9 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     constexpr uint32_t IDESC = tc::idesc_bf16(BM, BN, KIND == KIND_TGMM, B_MN);
     uint32_t it = 0, acc_it = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      const TileInfo ti = decode_tile<KIND>(bk, p, t);
-      if (ti.kblocks == 0 || (KIND == KIND_GMM && ti.row_end <= ti.row0)) continue;
+    for (int t = cid; t < total && ok; t += ncl) {
+      const TileInfo ti = decode_tile<KIND>(bk, p, t, crank);
+      if (ti.kblocks == 0) continue;
       const uint32_t a = acc_it & 1;
       const uint32_t aph = (acc_it >> 1) & 1;
       if (!tc::mbar_wait(&bk.tempty[a], aph ^ 1, abort_flag, kWaitLimitNs)) break;
@@ -638,7 +651,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                                      : tc::sdesc(b_base + kk * UK * 2, 16, 1024);
             tc::umma_bf16(d_tmem, ad, bd, IDESC, (kb | kk) != 0);
           }
-          tc::umma_commit(&bk.empty[s]);
+          tc::umma_commit_mc(&bk.empty[s], kPair);  // release the stage in both CTAs
         }
         __syncwarp();
         ++it;
@@ -658,9 +671,8 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     uint8_t *stg = smem + STG_OFFSET + (warp - 2) * kStgBytes;
     OutMaps om{&tmC0, &tmC1, &tmC2, &tmC3, &bk.aux_full[warp - 2], 0u, 0u};
     uint32_t acc_it = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const TileInfo ti = decode_tile<KIND>(bk, p, t);
-      if (KIND == KIND_GMM && ti.row_end <= ti.row0) continue;
+    for (int t = cid; t < total; t += ncl) {
+      const TileInfo ti = decode_tile<KIND>(bk, p, t, crank);
       if (KIND == KIND_TGMM && ti.kblocks == 0) {
         if (!p.accumulate) epilogue_tgmm(p, ti, 0, q, lane, stg, om, true);
         continue;
@@ -694,6 +706,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   tc::tc_fence_after();
   if (warp == 1) tc::tmem_dealloc(tmem, kTmemCols);
   if (threadIdx.x == 0 && bk.abort_flag) moe_set_status(p.dev_status, MOE_ERR_TIMEOUT);
+  tc::cluster_sync();  // the peer sends nothing more into this CTA's shared memory
 }
 
 // --------------------------------------------------------------- host side
@@ -747,16 +760,30 @@ moe_status_t launch_tc(const CUtensorMap &ma, const CUtensorMap &mb, const CUten
                        const TcParams &p, int64_t tiles_upper, cudaStream_t s) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
+  static int max_clusters = 0;
   std::call_once(once, [] {
     attr_err = cudaFuncSetAttribute(gmm_tc_kernel<KIND, B_MN, EPI>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (attr_err != cudaSuccess) return;
+    // clusters of two CTAs (one per SM) that can be resident at once
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (unsigned)num_sms());
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, gmm_tc_kernel<KIND, B_MN, EPI>, &cfg) !=
+            cudaSuccess ||
+        max_clusters <= 0) {
+      cudaGetLastError();
+      max_clusters = num_sms() / 2;
+    }
   });
   if (attr_err != cudaSuccess) {
     set_error("grouped GEMM: cannot reserve %d bytes of shared memory: %s", SMEM_BYTES,
               cudaGetErrorString(attr_err));
     return MOE_ERR_CUDA;
   }
-  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(num_sms(), tiles_upper));
+  const int64_t pairs = (tiles_upper + 1) / 2;
+  const int grid = 2 * (int)std::max<int64_t>(1, std::min<int64_t>(max_clusters, pairs));
   gmm_tc_kernel<KIND, B_MN, EPI><<<grid, kThreads, SMEM_BYTES, s>>>(ma, mb, mc[0], mc[1], mc[2],
                                                                     mc[3], p);
   cudaError_t e = cudaGetLastError();
@@ -801,7 +828,7 @@ moe_status_t launch_gmm(const GmmArgs &a, cudaStream_t s) {
   } else {
     const uint64_t dims[3] = {(uint64_t)a.K, (uint64_t)a.N, (uint64_t)a.E};
     const uint64_t st[2] = {(uint64_t)a.ldb * 2, (uint64_t)stride_b * 2};
-    const uint32_t box[3] = {BK, BN, 1};
+    const uint32_t box[3] = {BK, BN / 2, 1};
     if (!make_map(&mb, a.B, 3, dims, st, box)) {
       set_error("moe_gmm: cannot encode the TMA descriptor of B");
       return MOE_ERR_CUDA;
