@@ -62,6 +62,24 @@ const char *moe_last_error(void);
 int moe_version(void);
 
 /*
+ * Failure detection (no counterpart on the pages).  Every wait inside the
+ * grouped-GEMM kernels (pipeline barriers between the copy, tensor-core and
+ * epilogue roles) gives up after this many nanoseconds: the kernel then winds
+ * down without faulting, frees its tensor memory and writes MOE_ERR_TIMEOUT to
+ * dev_status, and the CUDA context stays usable.  Default 2 s; accepted range
+ * 1 ms .. 600 s (else MOE_ERR_INVALID_ARG).  Applies to launches made after the
+ * call, process-wide.
+ */
+moe_status_t moe_set_wait_limit_ns(uint64_t limit_ns);
+uint64_t moe_wait_limit_ns(void);
+/*
+ * Test hook for the above: while enabled, the grouped-GEMM kernels launched
+ * issue no operand loads, so their first pipeline wait runs out.  Only tests
+ * use it.
+ */
+void moe_test_stall_loads(int enable);
+
+/*
  * Worst-case number of permuted rows: T*k + E*(align-1) (align <= 1: T*k).
  * TE-2912, review thread on recv_buffer_rows ("align_size > 0 + EP are
  * combined"): aligned group sizes can add up to align-1 rows per expert.

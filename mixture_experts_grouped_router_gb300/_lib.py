@@ -55,6 +55,9 @@ _SIGS = {
     "moe_status_string": (ctypes.c_char_p, [_I]),
     "moe_last_error": (ctypes.c_char_p, []),
     "moe_version": (_I, []),
+    "moe_set_wait_limit_ns": (_I, [ctypes.c_uint64]),
+    "moe_wait_limit_ns": (ctypes.c_uint64, []),
+    "moe_test_stall_loads": (None, [_I]),
     "moe_rows_cap": (_I64, [_I, _I, _I, _I]),
     "moe_permute_workspace_bytes": (_SZ, [_I, _I]),
     "moe_route_topk": (_I, [_P, _I64, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
@@ -109,6 +112,18 @@ def _ld(t):
         return t.shape[-1]
     assert t.stride(-1) == 1, "row-major tensors only"
     return t.stride(-2)
+
+
+def moe_set_wait_limit_ns(limit_ns: int):
+    _check(LIB.moe_set_wait_limit_ns(int(limit_ns)))
+
+
+def moe_wait_limit_ns() -> int:
+    return int(LIB.moe_wait_limit_ns())
+
+
+def moe_test_stall_loads(enable: bool):
+    LIB.moe_test_stall_loads(int(bool(enable)))
 
 
 def moe_rows_cap(T: int, E: int, k: int, align: int) -> int:

@@ -3,6 +3,8 @@
 #include <stdarg.h>
 #include <stdio.h>
 
+#include <atomic>
+
 #include "internal.h"
 
 namespace moe {
@@ -15,6 +17,12 @@ void set_error(const char *fmt, ...) {
   vsnprintf(g_err, sizeof(g_err), fmt, ap);
   va_end(ap);
 }
+
+static std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+static std::atomic<int> g_stall_loads{0};
+
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+int test_stall_loads() { return g_stall_loads.load(std::memory_order_relaxed); }
 
 int num_sms() {
   int dev = 0, n = 0;
@@ -60,6 +68,18 @@ const char *moe_status_string(int status) {
 const char *moe_last_error(void) { return moe::g_err; }
 
 int moe_version(void) { return 100; }
+
+moe_status_t moe_set_wait_limit_ns(uint64_t limit_ns) {
+  set_error("");
+  REQUIRE(limit_ns >= 1000000ull && limit_ns <= 600000000000ull, MOE_ERR_INVALID_ARG,
+          "moe_set_wait_limit_ns: %llu ns outside [1 ms, 600 s]", (unsigned long long)limit_ns);
+  moe::g_wait_limit_ns.store(limit_ns);
+  return MOE_OK;
+}
+
+uint64_t moe_wait_limit_ns(void) { return moe::wait_limit_ns(); }
+
+void moe_test_stall_loads(int enable) { moe::g_stall_loads.store(enable ? 1 : 0); }
 
 int64_t moe_rows_cap(int T, int E, int k, int align) {
   if (T < 0 || E <= 0 || k <= 0) return -1;

@@ -56,7 +56,7 @@ constexpr int BOX_BYTES = 64 * 64 * 2; // one 64x64 MN-major box, 8 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int kMaxE = 256;
 constexpr int kGroupPairs = 16;  // raster group: 16 row-tile pairs x all column tiles
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
 constexpr int kTmemCols = 2 * BN;                 // two accumulators
 
 enum { KIND_GMM = 0, KIND_TGMM = 1 };
@@ -100,6 +100,8 @@ struct TcParams {
   int64_t stride_w;
   int accumulate;
   int32_t *dev_status;
+  uint64_t wait_limit_ns;  // bound of every wait before the CTA gives up
+  int stall_loads;         // test hook: the producer issues no loads
 };
 
 struct TileInfo {
@@ -345,7 +347,7 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
       const int nc = n0 + c * 32;
       if (nc >= N) break;
       // this chunk's H blocks (issued one chunk ahead) -> registers
-      if (!tc::mbar_wait(om.aux_bar, om.aux_phase & 1, abort_flag, kWaitLimitNs)) return;
+      if (!tc::mbar_wait_warp(om.aux_bar, om.aux_phase & 1, abort_flag, p.wait_limit_ns)) return;
       ++om.aux_phase;
       float g[32], u[32];
 #pragma unroll
@@ -551,14 +553,14 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
 
   uint32_t issued = 0;  // producer: k-blocks issued (ring position)
   if (warp == 0) {
-    if (lane == 0) {
+    if (lane == 0 && !p.stall_loads) {
       for (int t = cid; t < total; t += ncl) {
         const TileInfo ti = decode_tile<KIND>(bk, p, t, crank);
         bool ok = true;
         for (int kb = 0; kb < ti.kblocks; ++kb) {
           const int s = issued % kStages;
           const uint32_t ph = (issued / kStages) & 1;
-          if (!tc::mbar_wait(&bk.empty[s], ph ^ 1, abort_flag, kWaitLimitNs)) {
+          if (!tc::mbar_wait(&bk.empty[s], ph ^ 1, abort_flag, p.wait_limit_ns)) {
             ok = false;
             break;
           }
@@ -599,7 +601,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       }
       // drain: every issued copy has landed before the CTA may exit
       for (uint32_t i = issued > (uint32_t)kStages ? issued - kStages : 0; i < issued; ++i)
-        tc::mbar_wait_drain(&bk.full[i % kStages], (i / kStages) & 1, kWaitLimitNs / 4);
+        tc::mbar_wait_drain(&bk.full[i % kStages], (i / kStages) & 1, p.wait_limit_ns / 4);
     }
   } else if (warp == 1) {
     constexpr uint32_t IDESC = tc::idesc_bf16(BM, BN, KIND == KIND_TGMM, B_MN);
@@ -610,13 +612,13 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       if (ti.kblocks == 0) continue;
       const uint32_t a = acc_it & 1;
       const uint32_t aph = (acc_it >> 1) & 1;
-      if (!tc::mbar_wait(&bk.tempty[a], aph ^ 1, abort_flag, kWaitLimitNs)) break;
+      if (!tc::mbar_wait_warp(&bk.tempty[a], aph ^ 1, abort_flag, p.wait_limit_ns)) break;
       tc::tc_fence_after();
       const uint32_t d_tmem = tmem + a * BN;
       for (int kb = 0; kb < ti.kblocks; ++kb) {
         const int s = it % kStages;
         const uint32_t ph = (it / kStages) & 1;
-        if (!tc::mbar_wait(&bk.full[s], ph, abort_flag, kWaitLimitNs)) {
+        if (!tc::mbar_wait_warp(&bk.full[s], ph, abort_flag, p.wait_limit_ns)) {
           ok = false;
           break;
         }
@@ -664,7 +666,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     // drain: no MMA of this CTA is in flight once `drain` completes
     if (lane == 0) tc::umma_commit(&bk.drain);
     __syncwarp();
-    tc::mbar_wait_drain(&bk.drain, 0, kWaitLimitNs);
+    tc::mbar_wait_drain(&bk.drain, 0, p.wait_limit_ns);
   } else {
     const int q = warp & 3;  // TMEM lane quarter this warp may read = its tile rows
     const int rit = q * 32 + lane;
@@ -682,7 +684,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         issue_aux_load(om, stg, ti.n_idx * BN, ti.row0 + q * 32);  // first chunk's H blocks
       const uint32_t a = acc_it & 1;
       const uint32_t aph = (acc_it >> 1) & 1;
-      if (!tc::mbar_wait(&bk.tfull[a], aph, abort_flag, kWaitLimitNs)) break;
+      if (!tc::mbar_wait_warp(&bk.tfull[a], aph, abort_flag, p.wait_limit_ns)) break;
       tc::tc_fence_after();
       const uint32_t taddr = tmem + a * BN + (static_cast<uint32_t>(q * 32) << 16);
       if (KIND == KIND_GMM)
@@ -698,7 +700,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     if (lane == 0) tc::bulk_wait0();
     if (KIND == KIND_GMM && EPI == MOE_EPI_SWIGLU_BWD &&
         __shfl_sync(0xffffffffu, om.aux_issued, 0) != om.aux_phase)
-      tc::mbar_wait_drain(om.aux_bar, om.aux_phase & 1, kWaitLimitNs / 4);
+      tc::mbar_wait_drain(om.aux_bar, om.aux_phase & 1, p.wait_limit_ns / 4);
     __syncwarp();
   }
   tc::tc_fence_before();
@@ -852,6 +854,8 @@ moe_status_t launch_gmm(const GmmArgs &a, cudaStream_t s) {
   p.aux = a.aux;
   p.ld_aux = a.ld_aux;
   p.dev_status = a.dev_status;
+  p.wait_limit_ns = wait_limit_ns();
+  p.stall_loads = test_stall_loads();
   // output maps (unused slots repeat the first)
   CUtensorMap mc[4];
   bool ok = true;
@@ -932,6 +936,8 @@ moe_status_t launch_tgmm(const TgmmArgs &a, cudaStream_t s) {
   p.stride_w = a.stride_w;
   p.accumulate = a.accumulate;
   p.dev_status = a.dev_status;
+  p.wait_limit_ns = wait_limit_ns();
+  p.stall_loads = test_stall_loads();
   CUtensorMap mc[4];
   {
     const bool f32 = a.w_dtype == MOE_DTYPE_F32;

@@ -10,6 +10,8 @@ namespace moe {
 
 void set_error(const char *fmt, ...);
 int num_sms();
+uint64_t wait_limit_ns();  // bound of the kernels' waits (moe_set_wait_limit_ns)
+int test_stall_loads();    // test hook (moe_test_stall_loads)
 
 // route.cu
 cudaError_t launch_route_topk(const float *logits, int64_t ld, int T, int E, int k, int score_fn,

@@ -69,6 +69,14 @@ MOE_DEVINL bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_fl
   }
 }
 
+// mbar_wait by every lane of a warp with one warp-wide verdict, so that the
+// lanes never part ways when a wait gives up just as the phase completes.
+MOE_DEVINL bool mbar_wait_warp(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                               uint64_t limit_ns) {
+  const bool ok = mbar_wait(bar, parity, abort_flag, limit_ns);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // Bounded wait used while winding down: ignores the abort flag.
 MOE_DEVINL bool mbar_wait_drain(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;

@@ -110,6 +110,16 @@ def test_validation_errors_need_no_gpu(L):
     assert st == L.MOE_ERR_INVALID_ARG
 
 
+def test_wait_limit_setting(L):
+    default = L.moe_wait_limit_ns()
+    assert default == 2_000_000_000
+    assert L.LIB.moe_set_wait_limit_ns(10) == L.MOE_ERR_INVALID_ARG      # below 1 ms
+    L.moe_set_wait_limit_ns(50_000_000)
+    assert L.moe_wait_limit_ns() == 50_000_000
+    L.moe_set_wait_limit_ns(default)
+    assert L.moe_wait_limit_ns() == default
+
+
 def test_product_path_never_touches_the_oracle():
     for dirpath, _, files in os.walk(PKG):
         for fn in files:
