@@ -89,11 +89,14 @@ def oracle_sample(cfg, inp, n_tok, w64=None):
 
 
 def cpu_baseline(cfg, inp, target_s=12.0):
+    """Time the oracle on a growing token sample until one run takes ~target_s
+    (its cost is not linear in the tokens: every expert's weights are read)."""
     cores = len(os.sched_getaffinity(0))
-    n0 = min(cfg.T, 64)
-    dt0, _, w64 = oracle_sample(cfg, inp, n0)
-    n = int(min(cfg.T, max(n0, n0 * target_s / max(dt0, 1e-3))))
-    dt, m_kept, _ = oracle_sample(cfg, inp, n, w64)
+    n = min(cfg.T, 64)
+    dt, m_kept, w64 = oracle_sample(cfg, inp, n)
+    while dt < target_s and n < cfg.T:
+        n = int(min(cfg.T, n * max(2.0, min(8.0, 0.8 * target_s / max(dt, 1e-3)))))
+        dt, m_kept, _ = oracle_sample(cfg, inp, n, w64)
     flops = 18.0 * m_kept * cfg.d * cfg.f
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "tokens_per_s": n / dt, "seconds": dt,
