@@ -301,7 +301,33 @@ def dispatch_bwd(d_xs: np.ndarray, flat_to_sorted: np.ndarray, T: int, k: int):
 # ----------------------------------------------------------------------------
 # whole layer
 # ----------------------------------------------------------------------------
-def forward(x, logits, wi, wo, k, score_fn, renorm, align=0, capacity=0, num_chunks=1):
+def add_group_bias(m: np.ndarray, bias, group_offsets):
+    """Adds bias[e] to every row of group e (padding rows included).
+
+    MLP biases of the expert FFN: MaxText PR #4295, Testing (chunked GMM with
+    ``mlp_bias=True``); TE-2912, the ``has_wi_bias`` static info of the body
+    residuals."""
+    if bias is None:
+        return m
+    out = m.copy()
+    for e in range(bias.shape[0]):
+        s, t = int(group_offsets[e]), int(group_offsets[e + 1])
+        out[s:t] += bias[e][None, :]
+    return out
+
+
+def group_colsum(g: np.ndarray, group_offsets, E: int):
+    """Per-expert column sums: out[e] = sum of rows [off_e, off_e+1) of g (the
+    gradient of a bias that every row of the group received)."""
+    out = np.zeros((E, g.shape[1]))
+    for e in range(E):
+        s, t = int(group_offsets[e]), int(group_offsets[e + 1])
+        out[e] = g[s:t].sum(axis=0)
+    return out
+
+
+def forward(x, logits, wi, wo, k, score_fn, renorm, align=0, capacity=0, num_chunks=1,
+            bi=None, bo=None):
     """The layer's forward pass (TE-2912, sequence diagram of ``_moe_fwd_rule``
     without the expert-parallel all-to-all).
 
@@ -309,6 +335,7 @@ def forward(x, logits, wi, wo, k, score_fn, renorm, align=0, capacity=0, num_chu
     With num_chunks > 1 the up-projection is accumulated chunk by chunk along
     d_model into an fp32-style partial sum P (MT-4295, Description: each
     chunk's gmm adds into the partial sum in place), then SwiGLU runs on P.
+    Optional MLP biases bi [E, 2f] (added to [gate | up]) and bo [E, d].
     Returns a dict of every intermediate the backward needs.
     """
     T, d = x.shape
@@ -327,8 +354,9 @@ def forward(x, logits, wi, wo, k, score_fn, renorm, align=0, capacity=0, num_chu
             sl = slice(c * dc, (c + 1) * dc)
             p = gmm(xs[:, sl], wi[:, sl, :], off, partial_sum=p)
         h = p
+    h = add_group_bias(h, bi, off)
     act = swiglu(h)
-    y = gmm(act, wo, off)
+    y = add_group_bias(gmm(act, wo, off), bo, off)
     out = combine(y, lay["flat_to_sorted"], topk_w)
     return dict(topk_idx=topk_idx, topk_w=topk_w, layout=lay, xs=xs, h=h, act=act, y=y,
                 out=out)
@@ -366,7 +394,7 @@ def backward(fw: dict, d_out, wi, wo, k, num_chunks=1):
             d_wi[:, sl, :] = tgmm(fw["xs"][:, sl], dh, off, E)
     dx = dispatch_bwd(d_xs, lay["flat_to_sorted"], T, k)
     return dict(dy=dy, d_topk_w=d_topk_w, d_act=d_act, dh=dh, d_wo=d_wo, d_xs=d_xs,
-                d_wi=d_wi, dx=dx)
+                d_wi=d_wi, dx=dx, d_bi=group_colsum(dh, off, E), d_bo=group_colsum(dy, off, E))
 
 
 def flops_fwd_bwd(m_kept: int, d: int, f: int) -> int:

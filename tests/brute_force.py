@@ -73,21 +73,28 @@ def layout_dense(sel, kept, align):
     return pos, np.array(sizes), start
 
 
-def ffn_dense_torch(x, wi, wo, gate):
-    """out[t] = sum_e gate[t,e] * ((silu(x wi_0[e]) * (x wi_1[e])) wo[e]), all torch fp64."""
+def ffn_dense_torch(x, wi, wo, gate, bi=None, bo=None):
+    """out[t] = sum_e gate[t,e] * ((silu(x wi_0[e] + bi_0[e]) * (x wi_1[e] + bi_1[e])) wo[e]
+    + bo[e]), all torch fp64."""
     E, d, f2 = wi.shape
     f = f2 // 2
     out = torch.zeros(x.shape[0], wo.shape[2], dtype=torch.float64)
     for e in range(E):
         g = x @ wi[e, :, :f]
         u = x @ wi[e, :, f:]
+        if bi is not None:
+            g = g + bi[e, :f]
+            u = u + bi[e, f:]
         act = g * torch.sigmoid(g) * u
-        out = out + gate[:, e:e + 1] * (act @ wo[e])
+        y = act @ wo[e]
+        if bo is not None:
+            y = y + bo[e]
+        out = out + gate[:, e:e + 1] * y
     return out
 
 
-def layer_dense(x, logits, wi, wo, dout, k, score_fn, renorm, capacity=0):
-    """Forward output and gradients (dx, dwi, dwo, dgate) of L = <dout, out>."""
+def layer_dense(x, logits, wi, wo, dout, k, score_fn, renorm, capacity=0, bi=None, bo=None):
+    """Forward output and gradients (dx, dwi, dwo, dgate[, dbi, dbo]) of L = <dout, out>."""
     sel, slot, weight = route_dense(logits, k, score_fn, renorm)
     kept = kept_dense(sel, capacity)
     gate_np = np.where(kept, weight, 0.0)
@@ -95,12 +102,18 @@ def layer_dense(x, logits, wi, wo, dout, k, score_fn, renorm, capacity=0):
     wit = torch.tensor(wi, dtype=torch.float64, requires_grad=True)
     wot = torch.tensor(wo, dtype=torch.float64, requires_grad=True)
     gt = torch.tensor(gate_np, dtype=torch.float64, requires_grad=True)
-    out = ffn_dense_torch(xt, wit, wot, gt)
+    bit = None if bi is None else torch.tensor(bi, dtype=torch.float64, requires_grad=True)
+    bot = None if bo is None else torch.tensor(bo, dtype=torch.float64, requires_grad=True)
+    out = ffn_dense_torch(xt, wit, wot, gt, bit, bot)
     loss = (out * torch.tensor(dout, dtype=torch.float64)).sum()
     loss.backward()
-    return dict(sel=sel, slot=slot, weight=weight, kept=kept, out=out.detach().numpy(),
-                dx=xt.grad.numpy(), dwi=wit.grad.numpy(), dwo=wot.grad.numpy(),
-                dgate=gt.grad.numpy())
+    res = dict(sel=sel, slot=slot, weight=weight, kept=kept, out=out.detach().numpy(),
+               dx=xt.grad.numpy(), dwi=wit.grad.numpy(), dwo=wot.grad.numpy(),
+               dgate=gt.grad.numpy())
+    if bit is not None:
+        res["dbi"] = bit.grad.numpy()
+        res["dbo"] = bot.grad.numpy()
+    return res
 
 
 def route_bwd_dense_torch(logits, sel, d_gate, score_fn, renorm, bias=None):

@@ -426,3 +426,42 @@ def test_expert_bias_changes_selection_not_weights():
     i0, w0 = ref.route_topk(logits, 2, 1, 0, expert_bias=np.zeros(8, np.float32))
     i1, w1 = ref.route_topk(logits, 2, 1, 0)
     assert (i0 == i1).all() and (w0 == w1).all()
+
+
+# ---------------------------------------------------------------------------
+# MLP biases
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("case", [(14, 5, 4, 4, 2, 0, 1, 0, 0), (20, 4, 3, 5, 1, 0, 0, 4, 3),
+                                  (16, 6, 4, 6, 3, 1, 1, 2, 0)])
+def test_biases_vs_brute_force(case):
+    T, d, f, E, k, sfn, ren, align, cap = case
+    logits, x, wi, wo, dout = _rand_layer(zlib.crc32(repr(case).encode()) % 1000, T, d, f, E)
+    rng = np.random.default_rng(77)
+    bi = rng.standard_normal((E, 2 * f)) * 0.5
+    bo = rng.standard_normal((E, d)) * 0.5
+    b = bf.layer_dense(x, logits, wi, wo, dout, k, sfn, ren, cap, bi=bi, bo=bo)
+    fw = ref.forward(x, logits, wi, wo, k, sfn, ren, align, cap, bi=bi, bo=bo)
+    bw = ref.backward(fw, dout, wi, wo, k)
+    np.testing.assert_allclose(fw["out"], b["out"], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(bw["dx"], b["dx"], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(bw["d_wi"], b["dwi"], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(bw["d_wo"], b["dwo"], rtol=1e-11, atol=1e-12)
+    # bias gradients: only kept assignments reach the output
+    np.testing.assert_allclose(bw["d_bi"], b["dbi"], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(bw["d_bo"], b["dbo"], rtol=1e-11, atol=1e-12)
+
+
+def test_bias_free_layer_is_zero_bias_layer():
+    logits, x, wi, wo, dout = _rand_layer(5, 12, 4, 3, 3)
+    f0 = ref.forward(x, logits, wi, wo, 2, 0, 1, bi=np.zeros((3, 6)), bo=np.zeros((3, 4)))
+    f1 = ref.forward(x, logits, wi, wo, 2, 0, 1)
+    np.testing.assert_array_equal(f0["out"], f1["out"])
+
+
+def test_group_colsum_closed_form():
+    g = np.arange(30, dtype=np.float64).reshape(10, 3)
+    off = np.array([0, 4, 4, 10])
+    out = ref.group_colsum(g, off, 3)
+    np.testing.assert_array_equal(out[0], g[:4].sum(0))
+    np.testing.assert_array_equal(out[1], 0)
+    np.testing.assert_array_equal(out[2], [sum(3 * r + c for r in range(4, 10)) for c in range(3)])
