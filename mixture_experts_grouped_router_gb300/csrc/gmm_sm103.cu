@@ -11,28 +11,32 @@
 // moe_tgmm (ragged K): W_e = A_e^T B_e over the rows of expert e; an expert
 //          without rows gets exact zeros (MaxText PR #4295, Testing).
 //
-// Design (one persistent CTA per SM, 192 threads, warp-specialised):
-//   warp 0      TMA producer: 128x64 A tiles and 256x64 B tiles (bf16,
-//               128-byte swizzle) into a 4-stage shared-memory ring;
-//   warp 1      TMEM owner and MMA issuer: tcgen05.mma kind::f16,
-//               M=128 N=256 K=16, fp32 accumulators in TMEM, two 256-column
-//               accumulators so the epilogue of one tile overlaps the
-//               mainloop of the next;
+// Design (persistent, one CTA per SM, CTAs in clusters of two that take
+// adjacent 128-row tiles of the same expert and 256-column tile; 192 threads,
+// warp-specialised):
+//   warp 0      TMA producer.  Forward / dgrad GEMMs: 2-SM MMA pairs; each
+//               CTA loads its own 128x64 A tile and its half (128 columns) of
+//               the 256x64 B tile, both completing on the leader CTA's
+//               barrier (6 stages of 32 KB).  Weight-gradient GEMM and the
+//               SwiGLU-backward dgrad: each CTA loads its A tile and half of
+//               the B tile multicast into both CTAs (4 stages of 48 KB).
+//               128-byte swizzle throughout.
+//   warp 1      TMEM owner and MMA issuer: tcgen05.mma kind::f16, K=16, fp32
+//               accumulators in TMEM (two 256-column accumulators so that the
+//               epilogue of one tile overlaps the mainloop of the next); 2-SM
+//               kernels issue cta_group::2 MMAs (M=256) from the leader CTA.
+//               Stages are released in both CTAs by multicast commits.
 //   warps 2-5   epilogue: tcgen05.ld of one TMEM lane (= one output row) per
 //               thread, fused SwiGLU / partial-sum / cast; each warp stages
 //               its 32x32 output blocks in swizzled shared memory and writes
-//               them with TMA bulk stores, so that the outputs leave as whole
-//               lines and never contend with the operand loads of the
-//               mainloop (a block that straddles the expert's last row is
-//               written with plain stores instead).
+//               them with TMA bulk stores (bulk reduce-add for fp32 partial
+//               sums), so that outputs leave as whole lines and never contend
+//               with the mainloop's operand loads (a block that straddles the
+//               expert's last row is written with plain stores instead).
 // Tiles never straddle two experts.  The tile list is derived on the device
 // from group_offsets (no host synchronisation); tiles are visited expert by
 // expert in groups of 32 row tiles so that concurrently running CTAs share
-// their A rows and B columns in L2.  CTAs run in clusters of two that take
-// adjacent row tiles of the same expert and column tile: each fetches its
-// own A tile and half of the shared B tile, multicast into both CTAs, so a
-// CTA pulls 32 KB instead of 48 KB per 128x256x64 step from L2; the MMA
-// warps release a stage in both CTAs.  Every wait is bounded: on time-out the
+// their A rows and B columns in L2.  Every wait is bounded: on time-out the
 // CTA raises an abort flag, winds down, drains its in-flight copies and
 // MMAs, frees TMEM and reports MOE_ERR_TIMEOUT through dev_status.
 #include <cudaTypedefs.h>
@@ -46,7 +50,7 @@ namespace moe {
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 64, UK = 16;
-constexpr int kStages = 4;
+constexpr int kStages = 6;  // ring slots allocated (the weight-gradient kernel uses 4)
 constexpr int kThreads = 192;  // producer, MMA, 4 epilogue warps
 constexpr int kEpiWarps = 4;
 constexpr int kStgBytes = 8192;  // per epilogue warp: up to four 32x32 bf16 blocks (or two fp32)
@@ -73,7 +77,20 @@ struct Book {
   int total_tiles;
   int cum[kMaxE + 1];            // per-expert tile prefix
 };
-constexpr int STG_OFFSET = kStages * STAGE_BYTES;                    // 1024-aligned
+constexpr int STG_OFFSET = 4 * STAGE_BYTES;  // = 6 x 32 KB; 1024-aligned
+
+// Per-kernel ring.  The forward and dgrad GEMMs run as 2-SM MMAs whose stage
+// holds this CTA's 128-row A tile and half of the B tile (32 KB, 6 stages).
+// The weight-gradient GEMM (whose last K block of an expert is zeroed per
+// CTA) and the SwiGLU-backward dgrad (measured faster this way) keep whole B
+// tiles multicast within the pair (48 KB, 4 stages).
+template <int KIND, int EPI>
+struct Ring {
+  static constexpr bool two_sm = KIND == 0 && EPI != MOE_EPI_SWIGLU_BWD;
+  static constexpr int stages = two_sm ? 6 : 4;
+  static constexpr int b_bytes = two_sm ? B_BYTES / 2 : B_BYTES;
+  static constexpr int stage_bytes = A_BYTES + b_bytes;
+};
 constexpr int BOOK_OFFSET = STG_OFFSET + kEpiWarps * kStgBytes;
 constexpr int SMEM_BYTES = 1024 + BOOK_OFFSET + (int)((sizeof(Book) + 127) / 128 * 128);
 static_assert(SMEM_BYTES <= 232448, "shared memory budget of one CTA");
@@ -491,15 +508,22 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   const int cid = (int)tc::cluster_id_x();
   const int ncl = (int)tc::nclusters_x();
   constexpr uint16_t kPair = 0x3;
+  constexpr bool k2SM = Ring<KIND, EPI>::two_sm;
+  constexpr int kSt = Ring<KIND, EPI>::stages;
+  constexpr int kStageB = Ring<KIND, EPI>::stage_bytes;
+  const bool leader = crank == 0;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kSt; ++s) {
       tc::mbar_init(&bk.full[s], 1);
-      tc::mbar_init(&bk.empty[s], 2);  // both CTAs' MMA warps release a stage
+      // 2-SM: the leader's MMA commit releases a stage in both CTAs once;
+      // else both CTAs' MMA warps release it
+      tc::mbar_init(&bk.empty[s], k2SM ? 1 : 2);
     }
     for (int a = 0; a < 2; ++a) {
       tc::mbar_init(&bk.tfull[a], 1);
-      tc::mbar_init(&bk.tempty[a], kEpiWarps);
+      // 2-SM: the leader's accumulator is free once both CTAs' epilogues are done
+      tc::mbar_init(&bk.tempty[a], k2SM ? 2 * kEpiWarps : kEpiWarps);
     }
     tc::mbar_init(&bk.drain, 1);
     for (int w = 0; w < kEpiWarps; ++w) tc::mbar_init(&bk.aux_full[w], 1);
@@ -541,8 +565,13 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       if (group_offset(p, e + 1) < group_offset(p, e)) moe_set_status(p.dev_status, MOE_ERR_DEVICE);
   }
   if (warp == 1) {
-    tc::tmem_alloc(&bk.tmem_base, kTmemCols);
-    tc::tmem_relinquish();
+    if (k2SM) {
+      tc::tmem_alloc_2sm(&bk.tmem_base, kTmemCols);
+      tc::tmem_relinquish_2sm();
+    } else {
+      tc::tmem_alloc(&bk.tmem_base, kTmemCols);
+      tc::tmem_relinquish();
+    }
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -558,53 +587,73 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         const TileInfo ti = decode_tile<KIND>(bk, p, t, crank);
         bool ok = true;
         for (int kb = 0; kb < ti.kblocks; ++kb) {
-          const int s = issued % kStages;
-          const uint32_t ph = (issued / kStages) & 1;
+          const int s = issued % kSt;
+          const uint32_t ph = (issued / kSt) & 1;
           if (!tc::mbar_wait(&bk.empty[s], ph ^ 1, abort_flag, p.wait_limit_ns)) {
             ok = false;
             break;
           }
-          uint8_t *sa = smem + s * STAGE_BYTES;
+          uint8_t *sa = smem + s * kStageB;
           uint8_t *sb = sa + A_BYTES;
           uint64_t *fb = &bk.full[s];
-          tc::mbar_expect_tx(fb, STAGE_BYTES);
-          // own A tile; this CTA's half of the shared B tile, multicast to the pair
-          if (KIND == KIND_GMM) {
-            tc::tma_load_2d(sa, &tmA, fb, kb * BK, ti.row0);
+          if (k2SM) {
+            // both CTAs' copies complete on the leader's full barrier, which
+            // expects the whole pair's stage
+            const uint32_t fbl = tc::mapa_shared(tc::smem_u32(fb), 0);
+            if (leader) tc::mbar_expect_tx(fb, 2 * kStageB);
+            tc::tma_load_2d_2sm(sa, &tmA, fbl, kb * BK, ti.row0);
             if (B_MN) {
-              // MN-major B: four 64-column boxes, boxes 2*crank and 2*crank+1 from here
+              // this CTA's 128 columns of B: two 64-column boxes
               const int n0 = EPI == MOE_EPI_SWIGLU_FWD ? ti.n_idx * (BN / 2) : ti.n_idx * BN;
 #pragma unroll
-              for (int i = 2 * crank; i < 2 * crank + 2; ++i) {
-                const int x = EPI == MOE_EPI_SWIGLU_FWD ? (i < 2 ? n0 + 64 * i : p.F + n0 + 64 * (i - 2))
-                                                        : n0 + 64 * i;
-                tc::tma_load_3d_mc(sb + i * BOX_BYTES, &tmB, fb, x, kb * BK, ti.e, kPair);
+              for (int j = 0; j < 2; ++j) {
+                const int i = 2 * crank + j;
+                const int x = EPI == MOE_EPI_SWIGLU_FWD
+                                  ? (i < 2 ? n0 + 64 * i : p.F + n0 + 64 * (i - 2))
+                                  : n0 + 64 * i;
+                tc::tma_load_3d_2sm(sb + j * BOX_BYTES, &tmB, fbl, x, kb * BK, ti.e);
               }
             } else {
-              // K-major B: two 128-row boxes, row half `crank` from here
-              tc::tma_load_3d_mc(sb + crank * (B_BYTES / 2), &tmB, fb, kb * BK,
-                                 ti.n_idx * BN + crank * (BN / 2), ti.e, kPair);
+              tc::tma_load_3d_2sm(sb, &tmB, fbl, kb * BK, ti.n_idx * BN + crank * (BN / 2), ti.e);
             }
           } else {
-            const int r = ti.row0 + kb * BK;
-            const int m0 = ti.m_idx * BM;
-            const int n0 = ti.n_idx * BN;
-            tc::tma_load_2d(sa, &tmA, fb, m0, r);
-            tc::tma_load_2d(sa + BOX_BYTES, &tmA, fb, m0 + 64, r);
+            tc::mbar_expect_tx(fb, kStageB);
+            // own A tile; this CTA's half of the shared B tile, multicast to the pair
+            if (KIND == KIND_GMM) {
+              tc::tma_load_2d(sa, &tmA, fb, kb * BK, ti.row0);
+              if (B_MN) {
+                const int n0 = ti.n_idx * BN;
 #pragma unroll
-            for (int i = 2 * crank; i < 2 * crank + 2; ++i)
-              tc::tma_load_2d_mc(sb + i * BOX_BYTES, &tmB, fb, n0 + 64 * i, r, kPair);
+                for (int i = 2 * crank; i < 2 * crank + 2; ++i)
+                  tc::tma_load_3d_mc(sb + i * BOX_BYTES, &tmB, fb, n0 + 64 * i, kb * BK, ti.e, kPair);
+              } else {
+                tc::tma_load_3d_mc(sb + crank * (B_BYTES / 2), &tmB, fb, kb * BK,
+                                   ti.n_idx * BN + crank * (BN / 2), ti.e, kPair);
+              }
+            } else {
+              const int r = ti.row0 + kb * BK;
+              const int m0 = ti.m_idx * BM;
+              const int n0 = ti.n_idx * BN;
+              tc::tma_load_2d(sa, &tmA, fb, m0, r);
+              tc::tma_load_2d(sa + BOX_BYTES, &tmA, fb, m0 + 64, r);
+#pragma unroll
+              for (int i = 2 * crank; i < 2 * crank + 2; ++i)
+                tc::tma_load_2d_mc(sb + i * BOX_BYTES, &tmB, fb, n0 + 64 * i, r, kPair);
+            }
           }
           ++issued;
         }
         if (!ok) break;
       }
       // drain: every issued copy has landed before the CTA may exit
-      for (uint32_t i = issued > (uint32_t)kStages ? issued - kStages : 0; i < issued; ++i)
-        tc::mbar_wait_drain(&bk.full[i % kStages], (i / kStages) & 1, p.wait_limit_ns / 4);
+      // (2-SM: a CTA's copies complete on the leader's barrier; the leader's
+      // MMA consumed them all before the pair's final cluster barrier)
+      if (!k2SM || leader)
+        for (uint32_t i = issued > (uint32_t)kSt ? issued - kSt : 0; i < issued; ++i)
+          tc::mbar_wait_drain(&bk.full[i % kSt], (i / kSt) & 1, p.wait_limit_ns / 4);
     }
-  } else if (warp == 1) {
-    constexpr uint32_t IDESC = tc::idesc_bf16(BM, BN, KIND == KIND_TGMM, B_MN);
+  } else if (warp == 1 && (!k2SM || leader)) {
+    constexpr uint32_t IDESC = tc::idesc_bf16(k2SM ? 2 * BM : BM, BN, KIND == KIND_TGMM, B_MN);
     uint32_t it = 0, acc_it = 0;
     bool ok = true;
     for (int t = cid; t < total && ok; t += ncl) {
@@ -616,14 +665,14 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       tc::tc_fence_after();
       const uint32_t d_tmem = tmem + a * BN;
       for (int kb = 0; kb < ti.kblocks; ++kb) {
-        const int s = it % kStages;
-        const uint32_t ph = (it / kStages) & 1;
+        const int s = it % kSt;
+        const uint32_t ph = (it / kSt) & 1;
         if (!tc::mbar_wait_warp(&bk.full[s], ph, abort_flag, p.wait_limit_ns)) {
           ok = false;
           break;
         }
         tc::tc_fence_after();
-        uint8_t *sa = smem + s * STAGE_BYTES;
+        uint8_t *sa = smem + s * kStageB;
         uint8_t *sb = sa + A_BYTES;
         if (KIND == KIND_TGMM) {
           // rows past the expert's last row belong to the next expert: zero
@@ -651,23 +700,32 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                                                   : tc::sdesc(a_base + kk * UK * 2, 16, 1024);
             const uint64_t bd = B_MN ? tc::sdesc(b_base + kk * UK * 128, BOX_BYTES, 1024)
                                      : tc::sdesc(b_base + kk * UK * 2, 16, 1024);
-            tc::umma_bf16(d_tmem, ad, bd, IDESC, (kb | kk) != 0);
+            if (k2SM) tc::umma_bf16_2sm(d_tmem, ad, bd, IDESC, (kb | kk) != 0);
+            else tc::umma_bf16(d_tmem, ad, bd, IDESC, (kb | kk) != 0);
           }
-          tc::umma_commit_mc(&bk.empty[s], kPair);  // release the stage in both CTAs
+          // release the stage in both CTAs
+          if (k2SM) tc::umma_commit_2sm_mc(&bk.empty[s], kPair);
+          else tc::umma_commit_mc(&bk.empty[s], kPair);
         }
         __syncwarp();
         ++it;
       }
       if (!ok) break;
-      if (lane == 0) tc::umma_commit(&bk.tfull[a]);
+      if (lane == 0) {
+        if (k2SM) tc::umma_commit_2sm_mc(&bk.tfull[a], kPair);  // both CTAs' epilogues
+        else tc::umma_commit(&bk.tfull[a]);
+      }
       __syncwarp();
       ++acc_it;
     }
     // drain: no MMA of this CTA is in flight once `drain` completes
-    if (lane == 0) tc::umma_commit(&bk.drain);
+    if (lane == 0) {
+      if (k2SM) tc::umma_commit_2sm_mc(&bk.drain, 0x1);
+      else tc::umma_commit(&bk.drain);
+    }
     __syncwarp();
     tc::mbar_wait_drain(&bk.drain, 0, p.wait_limit_ns);
-  } else {
+  } else if (warp >= 2) {
     const int q = warp & 3;  // TMEM lane quarter this warp may read = its tile rows
     const int rit = q * 32 + lane;
     uint8_t *stg = smem + STG_OFFSET + (warp - 2) * kStgBytes;
@@ -693,7 +751,10 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         epilogue_tgmm(p, ti, taddr, q, lane, stg, om, false);
       tc::tc_fence_before();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&bk.tempty[a]);
+      if (lane == 0) {
+        if (k2SM) tc::mbar_arrive_cluster(tc::mapa_shared(tc::smem_u32(&bk.tempty[a]), 0));
+        else tc::mbar_arrive(&bk.tempty[a]);
+      }
       ++acc_it;
     }
     // every bulk store and H load of this warp has completed before the CTA exits
@@ -705,10 +766,14 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   }
   tc::tc_fence_before();
   __syncthreads();
+  // the pair is done with each other's barriers, shared memory and TMEM
+  tc::cluster_sync();
   tc::tc_fence_after();
-  if (warp == 1) tc::tmem_dealloc(tmem, kTmemCols);
+  if (warp == 1) {
+    if (k2SM) tc::tmem_dealloc_2sm(tmem, kTmemCols);
+    else tc::tmem_dealloc(tmem, kTmemCols);
+  }
   if (threadIdx.x == 0 && bk.abort_flag) moe_set_status(p.dev_status, MOE_ERR_TIMEOUT);
-  tc::cluster_sync();  // the peer sends nothing more into this CTA's shared memory
 }
 
 // --------------------------------------------------------------- host side
