@@ -163,8 +163,10 @@ class ClockSampler:
 # our arm
 # ---------------------------------------------------------------------------
 def algorithmic_bytes(cfg, m_kept, R, t_kept):
-    T, d, k = cfg.T, cfg.d, cfg.k
+    T, d, k, f, E = cfg.T, cfg.d, cfg.k, cfg.f, cfg.E
     return {
+        "colsum_dbo": R * d * 2 + E * d * 4,
+        "colsum_dbi": R * 2 * f * 2 + E * 2 * f * 4,
         "permute": (t_kept + R) * d * 2 + 8 * T * k + 4 * R,
         "combine": m_kept * d * 2 + T * d * 2 + 8 * T * k,
         "unpermute_bwd": t_kept * d * 2 + 2 * m_kept * d * 2 + (R - m_kept) * d * 2 + 8 * T * k,
@@ -211,12 +213,16 @@ def run_ours(args, cfg, ws, rank, local):
     dout = bf16(inp["dout"]).to(dev)
     logits = torch.from_numpy(inp["logits"]).to(dev)
     shape = layer.LayerShape(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.score_fn, cfg.renorm,
-                             cfg.align, cfg.capacity, cfg.num_chunks)
+                             cfg.align, cfg.capacity, cfg.num_chunks, args.bias)
     b = layer.MoEBuffers(shape, device=dev)
     stream = torch.cuda.current_stream(dev)
+    bi = bo = None
+    if args.bias:
+        bias_inp = moe_synth.make_biases(cfg, seed=rank)
+        bi, bo = bf16(bias_inp["bi"]).to(dev), bf16(bias_inp["bo"]).to(dev)
 
     def step(mark=layer._noop):
-        layer.forward(b, x, logits, wi, wo, mark=mark)
+        layer.forward(b, x, logits, wi, wo, mark=mark, bi=bi, bo=bo)
         layer.backward(b, dout, wi, wo, mark=mark)
 
     for _ in range(max(3, args.warmup)):
@@ -307,7 +313,7 @@ def run_ours(args, cfg, ws, rank, local):
         stream.wait_event(in_ready[sl])
         if i >= 2:
             stream.wait_event(d2h_done[sl])
-        layer.forward(b, din[sl]["x"], din[sl]["logits"], wi, wo)
+        layer.forward(b, din[sl]["x"], din[sl]["logits"], wi, wo, bi=bi, bo=bo)
         layer.backward(b, din[sl]["dout"], wi, wo)
         dres[sl]["out"].copy_(b.out)
         dres[sl]["dx"].copy_(b.dx)
@@ -368,7 +374,7 @@ def run_ours(args, cfg, ws, rank, local):
     if os.path.exists(tp):
         tj = json.load(open(tp))
         ent = tj.get(cfg.name, {}).get(dom)
-        if ent and ent.get("source_hash") == gemm_source_hash():
+        if ent and ent.get("source_hash") == gemm_source_hash() and not args.bias:
             traffic = ent["dram_bytes_per_launch"]
     roofline = {"bound": "tensor", "kernel": dom, "achieved": kernels[dom]["tflops"],
                 "peak": peak_t, "unit": "TFLOP/s", "frac": kernels[dom]["tflops"] / peak_t,
@@ -390,6 +396,7 @@ def run_ours(args, cfg, ws, rank, local):
                    "experts": cfg.E, "top_k": cfg.k,
                    "score": "sigmoid" if cfg.score_fn else "softmax", "renorm": cfg.renorm,
                    "align": cfg.align, "capacity": cfg.capacity, "num_chunks": cfg.num_chunks,
+                   "mlp_bias": bool(args.bias),
                    "m_kept": m_kept, "rows": R, "empty_experts": empty,
                    "gemm_tflop_per_step": flops_step / 1e12,
                    "l2": "inputs larger than L2 (weights %.2f GB)" % ((inp["wi"].nbytes +
@@ -454,6 +461,8 @@ def main():
                     choices=sorted(moe_synth.CONFIGS) + sorted(moe_synth.PROFILE_CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--bias", action="store_true",
+                    help="expert FFN with biases (bi on [gate | up], bo on the output)")
     args = ap.parse_args()
     cfg = {**moe_synth.CONFIGS, **moe_synth.PROFILE_CONFIGS}[args.config]
     ws, rank, local = dist_env()

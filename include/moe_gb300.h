@@ -192,7 +192,7 @@ moe_status_t moe_permute_noalloc(const uint16_t *x, int64_t ldx, const int32_t *
 /*
  * moe_gmm -- grouped GEMM over ragged per-expert row groups (tcgen05 tensor
  * cores, fp32 accumulation).  For every row r of group e:
- *     S[r, :] = A[r, :] . B_e  (+ partial_sum[r, :] when partial_sum != NULL)
+ *     S[r, :] = A[r, :] . B_e  (+ partial_sum[r, :]) (+ bias_e)
  * TE-2912: the grouped_gemm calls of the expert FFN (Description), with
  * [wi_0 | wi_1] fused into one up-projection (wi-fusion commit); MT-4295,
  * review threads on the gmm kernel: `transpose_rhs` and the in-place
@@ -214,6 +214,9 @@ moe_status_t moe_permute_noalloc(const uint16_t *x, int64_t ldx, const int32_t *
  *                                 u = H[:, F:], s = sigmoid(g)
  *   partial_sum fp32 [rows_cap, ld_ps >= N] or NULL (NONE / SWIGLU_FWD only);
  *             may alias C when c_dtype is fp32 and ld_ps == ldc (in place)
+ *   bias      bf16 or NULL (NONE / SWIGLU_FWD only): expert e's N-vector at
+ *             bias + e*stride_bias, added to every row of group e after the
+ *             partial sum (SWIGLU_FWD: [gate | up] bias, before the SwiGLU)
  *   C         [rows_cap, ldc] (ldc >= N, or >= 2F for SWIGLU_BWD)
  * Only rows r < group_offsets[E] are written.  E <= 256; A, B, C, C2, aux and
  * partial_sum 16-byte aligned; SWIGLU_FWD needs trans_b == 0.
@@ -221,9 +224,25 @@ moe_status_t moe_permute_noalloc(const uint16_t *x, int64_t ldx, const int32_t *
 moe_status_t moe_gmm(const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
                      int64_t stride_b, int trans_b, const int32_t *group_offsets, int E,
                      int64_t rows_cap, int K, int N, int epilogue, const uint16_t *aux,
-                     int64_t ld_aux, const float *partial_sum, int64_t ld_ps, void *C,
-                     int c_dtype, int64_t ldc, uint16_t *C2, int64_t ldc2, int32_t *dev_status,
+                     int64_t ld_aux, const float *partial_sum, int64_t ld_ps,
+                     const uint16_t *bias, int64_t stride_bias, void *C, int c_dtype,
+                     int64_t ldc, uint16_t *C2, int64_t ldc2, int32_t *dev_status,
                      moe_stream_t stream);
+
+/*
+ * moe_group_colsum -- per-expert column sums, the gradient of a bias that
+ * every row of a group received (the expert-FFN biases: MT-4295, Testing,
+ * `mlp_bias`; TE-2912, `has_wi_bias`):
+ *     out[e, n] = sum over rows r of group e of G[r, n]
+ *   summed in fp32 in a fixed order (the result does not vary between runs);
+ *   G bf16 [rows_cap, ldg >= N] (16-byte aligned, ldg % 8 == 0), N % 8 == 0;
+ *   out fp32 [E, ld_out >= N] (16-byte aligned, ld_out % 4 == 0; columns < N
+ *   of every row written, empty experts get 0).  Rows at or past
+ *   group_offsets[E] are not read.  E <= 65535.
+ */
+moe_status_t moe_group_colsum(const uint16_t *G, int64_t ldg, const int32_t *group_offsets,
+                              int E, int64_t rows_cap, int N, float *out, int64_t ld_out,
+                              moe_stream_t stream);
 
 /*
  * moe_tgmm -- weight-gradient grouped GEMM, ragged along the contraction:

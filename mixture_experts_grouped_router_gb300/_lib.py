@@ -67,7 +67,8 @@ _SIGS = {
     "moe_permute_noalloc": (_I, [_P, _I64, _P, _I, _I, _I, _I, _I, _I, _P, _I64, _I64, _P, _P,
                                  _P, _P, _P, _P, _P]),
     "moe_gmm": (_I, [_P, _I64, _P, _I64, _I64, _I, _P, _I, _I64, _I, _I, _I, _P, _I64, _P, _I64,
-                     _P, _I, _I64, _P, _I64, _P, _P]),
+                     _P, _I64, _P, _I, _I64, _P, _I64, _P, _P]),
+    "moe_group_colsum": (_I, [_P, _I64, _P, _I, _I64, _I, _P, _I64, _P]),
     "moe_tgmm": (_I, [_P, _I64, _P, _I64, _P, _I, _I64, _I, _I, _P, _I, _I64, _I64, _I, _P, _P]),
     "moe_combine": (_I, [_P, _I64, _P, _P, _I, _I, _I, _P, _I64, _P]),
     "moe_unpermute_bwd": (_I, [_P, _I64, _P, _I64, _P, _P, _P, _P, _I, _I, _I, _I, _I64, _P,
@@ -177,9 +178,10 @@ def moe_permute_noalloc(x, topk_idx, E, align, capacity, x_sorted, group_sizes, 
 
 
 def moe_gmm(A, B, trans_b, group_offsets, C, epilogue=EPI_NONE, aux=None, partial_sum=None,
-            C2=None, dev_status=None, stream=None, K=None, N=None):
+            C2=None, dev_status=None, stream=None, K=None, N=None, bias=None):
     """A [rows_cap, >=K]; B [E, K, N] (trans_b=0) or [E, N, K] (trans_b=1), any
-    row-major views; C bf16 or fp32.  K and N default to the shapes of B."""
+    row-major views; C bf16 or fp32; bias bf16 [E, >=N] (row e added to expert
+    e's rows).  K and N default to the shapes of B."""
     E = B.shape[0]
     if K is None:
         K = B.shape[2] if trans_b else B.shape[1]
@@ -189,9 +191,18 @@ def moe_gmm(A, B, trans_b, group_offsets, C, epilogue=EPI_NONE, aux=None, partia
     _check(LIB.moe_gmm(_ptr(A), _ld(A), _ptr(B), B.stride(1), B.stride(0), int(trans_b),
                        _ptr(group_offsets), E, A.shape[0], K, N, epilogue, _ptr(aux),
                        _ld(aux) if aux is not None else 0, _ptr(partial_sum),
-                       _ld(partial_sum) if partial_sum is not None else 0, _ptr(C), c_dtype,
+                       _ld(partial_sum) if partial_sum is not None else 0, _ptr(bias),
+                       bias.stride(0) if bias is not None else 0, _ptr(C), c_dtype,
                        _ld(C), _ptr(C2), _ld(C2) if C2 is not None else 0, _ptr(dev_status),
                        _stream(stream)))
+
+
+def moe_group_colsum(G, group_offsets, out, stream=None):
+    """out fp32 [E, >=N] = per-expert column sums of G bf16 [rows_cap, N]."""
+    E = out.shape[0]
+    N = G.shape[1]
+    _check(LIB.moe_group_colsum(_ptr(G), _ld(G), _ptr(group_offsets), E, G.shape[0], N,
+                                _ptr(out), out.stride(0), _stream(stream)))
 
 
 def moe_tgmm(A, B, group_offsets, W, accumulate=False, dev_status=None, stream=None):

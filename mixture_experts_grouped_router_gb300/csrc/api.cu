@@ -147,7 +147,8 @@ moe_status_t moe_permute(const uint16_t *x, int64_t ldx, const int32_t *topk_idx
           (long long)moe_rows_cap(T, E, k, align));
   REQUIRE(rows_cap < (1ll << 31) && (int64_t)T * k < (1ll << 31), MOE_ERR_UNSUPPORTED,
           "moe_permute: more than 2^31 rows");
-  REQUIRE(group_sizes && kept_counts && group_offsets && sorted_to_flat && workspace,
+  REQUIRE(group_sizes && kept_counts && group_offsets && workspace &&
+              (rows_cap == 0 || sorted_to_flat),
           MOE_ERR_INVALID_ARG, "moe_permute: null pointer");
   REQUIRE(T == 0 || (x && topk_idx && flat_to_sorted && x_sorted), MOE_ERR_INVALID_ARG,
           "moe_permute: null pointer");
@@ -167,8 +168,9 @@ moe_status_t moe_permute(const uint16_t *x, int64_t ldx, const int32_t *topk_idx
 moe_status_t moe_gmm(const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
                      int64_t stride_b, int trans_b, const int32_t *group_offsets, int E,
                      int64_t rows_cap, int K, int N, int epilogue, const uint16_t *aux,
-                     int64_t ld_aux, const float *partial_sum, int64_t ld_ps, void *C,
-                     int c_dtype, int64_t ldc, uint16_t *C2, int64_t ldc2, int32_t *dev_status,
+                     int64_t ld_aux, const float *partial_sum, int64_t ld_ps,
+                     const uint16_t *bias, int64_t stride_bias, void *C, int c_dtype,
+                     int64_t ldc, uint16_t *C2, int64_t ldc2, int32_t *dev_status,
                      moe_stream_t stream) {
   set_error("");
   REQUIRE(E > 0 && rows_cap >= 0 && K > 0 && N > 0, MOE_ERR_INVALID_ARG,
@@ -177,7 +179,8 @@ moe_status_t moe_gmm(const uint16_t *A, int64_t lda, const uint16_t *B, int64_t 
           "moe_gmm: bad epilogue %d", epilogue);
   REQUIRE(c_dtype == MOE_DTYPE_BF16 || c_dtype == MOE_DTYPE_F32, MOE_ERR_INVALID_ARG,
           "moe_gmm: bad c_dtype");
-  REQUIRE(A && B && group_offsets && C, MOE_ERR_INVALID_ARG, "moe_gmm: null pointer");
+  REQUIRE(B && group_offsets && (rows_cap == 0 || (A && C)), MOE_ERR_INVALID_ARG,
+          "moe_gmm: null pointer");
   REQUIRE(K % 8 == 0 && N % 8 == 0 && lda % 8 == 0 && ldb % 8 == 0 && stride_b % 8 == 0,
           MOE_ERR_UNSUPPORTED, "moe_gmm: K, N, lda, ldb, stride_b must be multiples of 8");
   REQUIRE(E <= 256, MOE_ERR_UNSUPPORTED, "moe_gmm: E=%d > 256", E);
@@ -191,14 +194,15 @@ moe_status_t moe_gmm(const uint16_t *A, int64_t lda, const uint16_t *B, int64_t 
   int outN = N;
   if (epilogue == MOE_EPI_SWIGLU_FWD) {
     REQUIRE(N % 16 == 0, MOE_ERR_UNSUPPORTED, "moe_gmm: SWIGLU_FWD needs N = 2F with F %% 8 == 0");
-    REQUIRE(C2 != nullptr && ldc2 >= N / 2 && ldc2 % 8 == 0, MOE_ERR_INVALID_ARG,
+    REQUIRE((C2 != nullptr || rows_cap == 0) && ldc2 >= N / 2 && ldc2 % 8 == 0, MOE_ERR_INVALID_ARG,
             "moe_gmm: SWIGLU_FWD needs C2 with ldc2 >= F");
     REQUIRE(c_dtype == MOE_DTYPE_BF16, MOE_ERR_INVALID_ARG, "moe_gmm: SWIGLU_FWD writes bf16 H");
     REQUIRE(!trans_b, MOE_ERR_UNSUPPORTED, "moe_gmm: SWIGLU_FWD needs trans_b = 0");
   }
   if (epilogue == MOE_EPI_SWIGLU_BWD) {
     outN = 2 * N;
-    REQUIRE(aux != nullptr && ld_aux >= 2 * N && ld_aux % 8 == 0, MOE_ERR_INVALID_ARG,
+    REQUIRE((aux != nullptr || rows_cap == 0) && ld_aux >= 2 * N && ld_aux % 8 == 0,
+            MOE_ERR_INVALID_ARG,
             "moe_gmm: SWIGLU_BWD needs aux = H with ld_aux >= 2N");
     REQUIRE(partial_sum == nullptr, MOE_ERR_INVALID_ARG,
             "moe_gmm: SWIGLU_BWD takes no partial sum");
@@ -210,10 +214,17 @@ moe_status_t moe_gmm(const uint16_t *A, int64_t lda, const uint16_t *B, int64_t 
   REQUIRE(partial_sum == nullptr || (const void *)partial_sum != C ||
               (c_dtype == MOE_DTYPE_F32 && ld_ps == ldc),
           MOE_ERR_INVALID_ARG, "moe_gmm: in-place partial sum needs fp32 C with ld_ps == ldc");
+  REQUIRE(bias == nullptr || epilogue != MOE_EPI_SWIGLU_BWD, MOE_ERR_INVALID_ARG,
+          "moe_gmm: SWIGLU_BWD takes no bias");
+  REQUIRE(bias == nullptr || (stride_bias >= N && stride_bias % 8 == 0 && aligned16(bias)) ||
+              (bias != nullptr && E == 1 && aligned16(bias)),
+          MOE_ERR_INVALID_ARG, "moe_gmm: bias needs stride_bias >= N (multiple of 8) and a "
+          "16-byte aligned pointer");
   REQUIRE(rows_cap < (1ll << 31), MOE_ERR_UNSUPPORTED, "moe_gmm: more than 2^31 rows");
   if (rows_cap == 0) return MOE_OK;
   moe::GmmArgs a{A, lda, B, ldb, stride_b, trans_b, group_offsets, E, rows_cap, K, N, epilogue,
-                 aux, ld_aux, partial_sum, ld_ps, C, c_dtype, ldc, C2, ldc2, dev_status};
+                 aux, ld_aux, partial_sum, ld_ps, bias, stride_bias, C, c_dtype, ldc, C2, ldc2,
+                 dev_status};
   return moe::launch_gmm(a, (cudaStream_t)stream);
 }
 
@@ -224,7 +235,8 @@ moe_status_t moe_tgmm(const uint16_t *A, int64_t lda, const uint16_t *B, int64_t
   set_error("");
   REQUIRE(E > 0 && rows_cap >= 0 && M > 0 && N > 0, MOE_ERR_INVALID_ARG,
           "moe_tgmm: E=%d rows_cap=%lld M=%d N=%d", E, (long long)rows_cap, M, N);
-  REQUIRE(A && B && group_offsets && W, MOE_ERR_INVALID_ARG, "moe_tgmm: null pointer");
+  REQUIRE(group_offsets && W && (rows_cap == 0 || (A && B)), MOE_ERR_INVALID_ARG,
+          "moe_tgmm: null pointer");
   REQUIRE(w_dtype == MOE_DTYPE_BF16 || w_dtype == MOE_DTYPE_F32, MOE_ERR_INVALID_ARG,
           "moe_tgmm: bad w_dtype");
   REQUIRE(!accumulate || w_dtype == MOE_DTYPE_F32, MOE_ERR_INVALID_ARG,
@@ -239,9 +251,40 @@ moe_status_t moe_tgmm(const uint16_t *A, int64_t lda, const uint16_t *B, int64_t
   REQUIRE(stride_w >= (int64_t)M * ldw || E == 1, MOE_ERR_INVALID_ARG,
           "moe_tgmm: stride_w overlaps experts");
   REQUIRE(rows_cap < (1ll << 31), MOE_ERR_UNSUPPORTED, "moe_tgmm: more than 2^31 rows");
+  if (rows_cap == 0) {  // no rows at all: every expert is empty
+    if (accumulate) return MOE_OK;
+    const size_t es = w_dtype == MOE_DTYPE_F32 ? 4 : 2;
+    for (int e = 0; e < E; ++e) {
+      const cudaError_t ce =
+          cudaMemset2DAsync(static_cast<char *>(W) + (size_t)e * stride_w * es, (size_t)ldw * es,
+                            0, (size_t)N * es, (size_t)M, (cudaStream_t)stream);
+      if (ce != cudaSuccess) return cuda_status(ce, "moe_tgmm zero fill");
+    }
+    return MOE_OK;
+  }
   moe::TgmmArgs a{A, lda, B, ldb, group_offsets, E, rows_cap, M, N, W, w_dtype, ldw, stride_w,
                   accumulate, dev_status};
   return moe::launch_tgmm(a, (cudaStream_t)stream);
+}
+
+moe_status_t moe_group_colsum(const uint16_t *G, int64_t ldg, const int32_t *group_offsets,
+                              int E, int64_t rows_cap, int N, float *out, int64_t ld_out,
+                              moe_stream_t stream) {
+  set_error("");
+  REQUIRE(E > 0 && rows_cap >= 0 && N > 0, MOE_ERR_INVALID_ARG,
+          "moe_group_colsum: E=%d rows_cap=%lld N=%d", E, (long long)rows_cap, N);
+  REQUIRE(E <= 65535, MOE_ERR_UNSUPPORTED, "moe_group_colsum: E > 65535");
+  REQUIRE(N % 8 == 0 && ldg % 8 == 0, MOE_ERR_UNSUPPORTED,
+          "moe_group_colsum: N and ldg must be multiples of 8");
+  REQUIRE(ldg >= N && ld_out >= N, MOE_ERR_INVALID_ARG, "moe_group_colsum: leading dimension < N");
+  REQUIRE(group_offsets && out && (rows_cap == 0 || G), MOE_ERR_INVALID_ARG,
+          "moe_group_colsum: null pointer");
+  REQUIRE(aligned16(G) && aligned16(out) && ld_out % 4 == 0, MOE_ERR_UNSUPPORTED,
+          "moe_group_colsum: G and out must be 16-byte aligned, ld_out a multiple of 4");
+  REQUIRE(rows_cap < (1ll << 31), MOE_ERR_UNSUPPORTED, "moe_group_colsum: more than 2^31 rows");
+  return cuda_status(moe::launch_group_colsum(G, ldg, group_offsets, E, rows_cap, N, out, ld_out,
+                                              (cudaStream_t)stream),
+                     "moe_group_colsum launch");
 }
 
 moe_status_t moe_combine(const uint16_t *Y, int64_t ldy, const int32_t *flat_to_sorted,
@@ -276,7 +319,7 @@ moe_status_t moe_unpermute_bwd(const uint16_t *d_out, int64_t ld_dout, const uin
   REQUIRE(ld_dout >= d && ldy >= d && ld_dy >= d, MOE_ERR_INVALID_ARG,
           "moe_unpermute_bwd: leading dimension < d");
   REQUIRE(rows_cap < (1ll << 31), MOE_ERR_UNSUPPORTED, "moe_unpermute_bwd: more than 2^31 rows");
-  REQUIRE(group_offsets && sorted_to_flat && dY, MOE_ERR_INVALID_ARG,
+  REQUIRE(group_offsets && (rows_cap == 0 || (sorted_to_flat && dY)), MOE_ERR_INVALID_ARG,
           "moe_unpermute_bwd: null pointer");
   REQUIRE(T == 0 || (d_out && Y && flat_to_sorted && topk_w && d_topk_w), MOE_ERR_INVALID_ARG,
           "moe_unpermute_bwd: null pointer");

@@ -150,7 +150,86 @@ unpermute_bwd_kernel(const uint16_t *__restrict__ dout, int64_t ld_dout,
   }
 }
 
+// Per-expert column sums (bias gradients): block (column block, expert e)
+// sums every row of group e over 8*CW columns.  CW threads cover one row
+// segment with 16-byte loads; the other 256/CW thread rows stride down the
+// group, four rows in flight each; the partial sums meet in shared memory in
+// a fixed order (deterministic, no atomics).  CW is picked per call so that
+// the grid has a few blocks per SM even when N*E is small.
+template <int CW>
+__global__ void __launch_bounds__(256)
+group_colsum_kernel(const uint16_t *__restrict__ G, int64_t ldg,
+                    const int32_t *__restrict__ offsets, int64_t rows_cap, int N,
+                    float *__restrict__ out, int64_t ld_out) {
+  constexpr int RL = 256 / CW;  // row lanes
+  __shared__ float part[RL - 1][CW][8];
+  const int e = blockIdx.y;
+  const int tx = threadIdx.x % CW, ty = threadIdx.x / CW;
+  const int col = blockIdx.x * (8 * CW) + tx * 8;
+  const int64_t r0 = min(max((int64_t)__ldg(offsets + e), (int64_t)0), rows_cap);
+  const int64_t r1 = max(min((int64_t)__ldg(offsets + e + 1), rows_cap), r0);
+  float acc[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+  if (col < N) {
+    const uint16_t *base = G + col;
+    int64_t r = r0 + ty;
+    for (; r + 3 * RL < r1; r += 4 * RL) {
+      uint4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = ld_nc_v4(base + (r + u * RL) * ldg);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        float f[8];
+        bf16x8_to_f32(v[u], f);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q] += f[q];
+      }
+    }
+    for (; r < r1; r += RL) {
+      float f[8];
+      bf16x8_to_f32(ld_nc_v4(base + r * ldg), f);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] += f[q];
+    }
+  }
+  if (ty > 0) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) part[ty - 1][tx][q] = acc[q];
+  }
+  __syncthreads();
+  if (ty == 0 && col < N) {
+    for (int w = 0; w < RL - 1; ++w)
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] += part[w][tx][q];
+    float *o = out + (int64_t)e * ld_out + col;
+    *reinterpret_cast<float4 *>(o) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    *reinterpret_cast<float4 *>(o + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_group_colsum(const uint16_t *G, int64_t ldg, const int32_t *offsets, int E,
+                               int64_t rows_cap, int N, float *out, int64_t ld_out,
+                               cudaStream_t s) {
+  if ((ld_out & 3) != 0 || (reinterpret_cast<uintptr_t>(out) & 15) != 0) {
+    // fp32 output written with 16-byte stores
+    return cudaErrorMisalignedAddress;
+  }
+  // widest column block that still gives >= 2 blocks per SM
+  const int64_t want = 2 * (int64_t)num_sms();
+  int cw = 64;
+  while (cw > 8 && (int64_t)((N + 8 * cw - 1) / (8 * cw)) * E < want) cw >>= 1;
+  dim3 grid((N + 8 * cw - 1) / (8 * cw), E);
+  switch (cw) {
+    case 64: group_colsum_kernel<64><<<grid, 256, 0, s>>>(G, ldg, offsets, rows_cap, N, out, ld_out); break;
+    case 32: group_colsum_kernel<32><<<grid, 256, 0, s>>>(G, ldg, offsets, rows_cap, N, out, ld_out); break;
+    case 16: group_colsum_kernel<16><<<grid, 256, 0, s>>>(G, ldg, offsets, rows_cap, N, out, ld_out); break;
+    default: group_colsum_kernel<8><<<grid, 256, 0, s>>>(G, ldg, offsets, rows_cap, N, out, ld_out); break;
+  }
+  return cudaGetLastError();
+}
 
 cudaError_t launch_combine(const uint16_t *Y, int64_t ldy, const int32_t *f2s, const float *w,
                            int T, int k, int d, uint16_t *out, int64_t ldo, cudaStream_t s) {

@@ -112,6 +112,8 @@ struct TcParams {
   int64_t ldc2;
   const float *ps;
   int64_t ld_ps;
+  const uint16_t *bias;   // expert e's vector at bias + e * stride_bias, or null
+  int64_t stride_bias;
   const uint16_t *aux;
   int64_t ld_aux;
   int64_t stride_w;
@@ -327,6 +329,22 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
           pu[j] = nu[j];
         }
       }
+      if (p.bias != nullptr) {
+        const uint16_t *be = p.bias + (int64_t)ti.e * p.stride_bias;
+#pragma unroll
+        for (int j8 = 0; j8 < 4; ++j8) {
+          if (nc + j8 * 8 < F) {
+            float bg[8], bu[8];
+            bf16x8_to_f32(__ldg(reinterpret_cast<const uint4 *>(be + nc + j8 * 8)), bg);
+            bf16x8_to_f32(__ldg(reinterpret_cast<const uint4 *>(be + F + nc + j8 * 8)), bu);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              g[j8 * 8 + i] += bg[i];
+              u[j8 * 8 + i] += bu[i];
+            }
+          }
+        }
+      }
 #pragma unroll
       for (int j = 0; j < 32; ++j) act[j] = g[j] * sigmoid_f(g[j]) * u[j];
       if (bulk) {
@@ -437,6 +455,18 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
         for (int j = 0; j < 32; ++j) v[j] += pv[j];
 #pragma unroll
         for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
+      }
+      if (p.bias != nullptr) {
+        const uint16_t *be = p.bias + (int64_t)ti.e * p.stride_bias;
+#pragma unroll
+        for (int j8 = 0; j8 < 4; ++j8) {
+          if (nc + j8 * 8 < N) {
+            float bv[8];
+            bf16x8_to_f32(__ldg(reinterpret_cast<const uint4 *>(be + nc + j8 * 8)), bv);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[j8 * 8 + i] += bv[i];
+          }
+        }
       }
       if (bulk) {
         stage_acquire(lane);
@@ -916,6 +946,8 @@ moe_status_t launch_gmm(const GmmArgs &a, cudaStream_t s) {
   p.ldc2 = a.ldc2;
   p.ps = a.ps;
   p.ld_ps = a.ld_ps;
+  p.bias = a.bias;
+  p.stride_bias = a.stride_bias;
   p.aux = a.aux;
   p.ld_aux = a.ld_aux;
   p.dev_status = a.dev_status;

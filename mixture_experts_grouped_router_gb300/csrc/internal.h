@@ -39,6 +39,10 @@ cudaError_t launch_unpermute_bwd(const uint16_t *dout, int64_t ld_dout, const ui
                                  int E, int64_t rows_cap, uint16_t *dY, int64_t ld_dy,
                                  float *dw, cudaStream_t s);
 
+cudaError_t launch_group_colsum(const uint16_t *G, int64_t ldg, const int32_t *offsets, int E,
+                               int64_t rows_cap, int N, float *out, int64_t ld_out,
+                               cudaStream_t s);
+
 // gmm_sm103.cu
 struct GmmArgs {
   const uint16_t *A; int64_t lda;
@@ -47,6 +51,7 @@ struct GmmArgs {
   int epilogue;
   const uint16_t *aux; int64_t ld_aux;
   const float *ps; int64_t ld_ps;
+  const uint16_t *bias; int64_t stride_bias;
   void *C; int c_dtype; int64_t ldc;
   uint16_t *C2; int64_t ldc2;
   int32_t *dev_status;

@@ -12,6 +12,10 @@ backward  unpermute_bwd -> route_topk_bwd (d_logits) -> gmm(dgrad down, SwiGLU-b
           epilogue) -> tgmm(dWo) -> gmm(dgrad up) -> tgmm(dWi) -> combine without
           weights (dispatch bwd)
 
+With bias=True the expert FFN carries biases (bi [E, 2f] on [gate | up],
+bo [E, d] on the output), added in the GEMM epilogues; their gradients are
+per-expert column sums of dH and dY (moe_group_colsum).
+
 With num_chunks > 1 the up-projection runs as num_chunks K-chunks of d_model
 accumulating into an fp32 partial sum in place (MaxText PR #4295, "Overlap
 moe comms with collective matmul", Description), SwiGLU fused into the last
@@ -38,6 +42,7 @@ class LayerShape:
     align: int = 0
     capacity: int = 0
     num_chunks: int = 1
+    bias: bool = False
 
 
 class MoEBuffers:
@@ -74,6 +79,8 @@ class MoEBuffers:
         self.dx = torch.empty(T, d, dtype=bf, device=dev)
         self.dwi = torch.empty(E, d, 2 * f, dtype=dw_dtype, device=dev)
         self.dwo = torch.empty(E, f, d, dtype=dw_dtype, device=dev)
+        self.dbi = torch.empty(E, 2 * f, dtype=f32, device=dev) if s.bias else None
+        self.dbo = torch.empty(E, d, dtype=f32, device=dev) if s.bias else None
         self.dev_status = torch.zeros(1, dtype=i32, device=dev)
 
 
@@ -81,12 +88,15 @@ def _noop(_name):
     pass
 
 
-def forward(b: MoEBuffers, x, logits, wi, wo, stream=None, mark=_noop):
-    """x bf16 [T,d], logits fp32 [T,E], wi bf16 [E,d,2f] ([wi_0 | wi_1]), wo bf16 [E,f,d].
+def forward(b: MoEBuffers, x, logits, wi, wo, stream=None, mark=_noop, bi=None, bo=None):
+    """x bf16 [T,d], logits fp32 [T,E], wi bf16 [E,d,2f] ([wi_0 | wi_1]), wo bf16 [E,f,d];
+    with a bias layer shape also bi bf16 [E,2f] and bo bf16 [E,d].
 
     ``mark(name)`` is called after each library call (the benchmark records a
     CUDA event there)."""
     s = b.s
+    if s.bias != (bi is not None and bo is not None):
+        raise ValueError("forward: pass bi and bo exactly when the layer shape has bias=True")
     b.logits = logits
     L.moe_route_topk(logits, s.k, s.score_fn, s.renorm, b.topk_idx, b.topk_w, stream)
     mark("route")
@@ -95,7 +105,7 @@ def forward(b: MoEBuffers, x, logits, wi, wo, stream=None, mark=_noop):
     mark("permute")
     if s.num_chunks <= 1:
         L.moe_gmm(b.xs, wi, 0, b.group_offsets, b.h, L.EPI_SWIGLU_FWD, C2=b.act,
-                  dev_status=b.dev_status, stream=stream)
+                  dev_status=b.dev_status, stream=stream, bias=bi)
         mark("gmm_up_swiglu")
     else:
         dc = s.d // s.num_chunks
@@ -106,14 +116,14 @@ def forward(b: MoEBuffers, x, logits, wi, wo, stream=None, mark=_noop):
             ps = None if c == 0 else b.p
             if last:
                 L.moe_gmm(a_c, w_c, 0, b.group_offsets, b.h, L.EPI_SWIGLU_FWD, partial_sum=ps,
-                          C2=b.act, dev_status=b.dev_status, stream=stream)
+                          C2=b.act, dev_status=b.dev_status, stream=stream, bias=bi)
                 mark("gmm_up_chunk_swiglu")
             else:
                 L.moe_gmm(a_c, w_c, 0, b.group_offsets, b.p, L.EPI_NONE, partial_sum=ps,
                           dev_status=b.dev_status, stream=stream)
                 mark("gmm_up_chunk")
     L.moe_gmm(b.act, wo, 0, b.group_offsets, b.y, L.EPI_NONE, dev_status=b.dev_status,
-              stream=stream)
+              stream=stream, bias=bo)
     mark("gmm_down")
     L.moe_combine(b.y, b.f2s, b.topk_w, b.out, s.k, stream)
     mark("combine")
@@ -122,7 +132,7 @@ def forward(b: MoEBuffers, x, logits, wi, wo, stream=None, mark=_noop):
 
 def backward(b: MoEBuffers, dout, wi, wo, stream=None, mark=_noop):
     """dout bf16 [T,d] -> (dx, dwi, dwo, d_topk_w) in b's buffers; the router-logit
-    gradient lands in b.d_logits."""
+    gradient lands in b.d_logits, the bias gradients (bias layers) in b.dbi, b.dbo."""
     s = b.s
     L.moe_unpermute_bwd(dout, b.y, b.f2s, b.s2f, b.group_offsets, b.topk_w, b.dy, b.d_topk_w,
                         stream)
@@ -136,6 +146,11 @@ def backward(b: MoEBuffers, dout, wi, wo, stream=None, mark=_noop):
     mark("gmm_dgrad_down_swiglu_bwd")
     L.moe_tgmm(b.act, b.dy, b.group_offsets, b.dwo, dev_status=b.dev_status, stream=stream)
     mark("tgmm_dwo")
+    if s.bias:
+        L.moe_group_colsum(b.dy, b.group_offsets, b.dbo, stream)
+        mark("colsum_dbo")
+        L.moe_group_colsum(b.dh, b.group_offsets, b.dbi, stream)
+        mark("colsum_dbi")
     if s.num_chunks <= 1:
         L.moe_gmm(b.dh, wi, 1, b.group_offsets, b.dxs, L.EPI_NONE, dev_status=b.dev_status,
                   stream=stream)
@@ -159,10 +174,10 @@ def backward(b: MoEBuffers, dout, wi, wo, stream=None, mark=_noop):
 
 def kernels_per_step(s: LayerShape) -> int:
     """Kernels one forward + backward launches (route 1, permute 3, each GEMM 1,
-    combine 1, unpermute_bwd 1, route_bwd 1, dispatch backward 1)."""
+    combine 1, unpermute_bwd 1, route_bwd 1, dispatch backward 1, bias gradients 2)."""
     up = max(1, s.num_chunks)
     fwd = 1 + 3 + up + 1 + 1
-    bwd = 1 + 1 + 1 + 1 + 2 * up + 1
+    bwd = 1 + 1 + 1 + 1 + 2 * up + 1 + (2 if s.bias else 0)
     return fwd + bwd
 
 

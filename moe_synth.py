@@ -142,6 +142,16 @@ def make_inputs(cfg: MoEConfig, seed: int = 0) -> dict:
     return res
 
 
+def make_biases(cfg: MoEConfig, seed: int = 0, std: float = 0.5) -> dict:
+    """Seeded expert-FFN biases, drawn from their own stream so that the
+    bias-free inputs of ``make_inputs`` stay unchanged.
+
+    Keys: ``bi`` bf16 bits [E, 2f] ([gate | up]); ``bo`` bf16 bits [E, d]."""
+    rng = np.random.default_rng([seed, 0xB1A5])
+    return {"bi": _normal_bf16(rng, (cfg.E, 2 * cfg.f), std),
+            "bo": _normal_bf16(rng, (cfg.E, cfg.d), std)}
+
+
 def scaled(cfg: MoEConfig, **kw) -> MoEConfig:
     """A copy of a preset with some sizes replaced (used for small parity cases)."""
     return dataclasses.replace(cfg, **kw)

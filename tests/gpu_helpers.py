@@ -41,28 +41,35 @@ def assert_close(name, got, want, rel_fro=REL_FRO, max_rel=MAX_REL):
     assert mdiff <= max_rel * mref, "%s: max diff %.3g > %g * %.3g" % (name, mdiff, max_rel, mref)
 
 
-def layer_shape(cfg):
+def layer_shape(cfg, bias=False):
     from mixture_experts_grouped_router_gb300 import layer
     return layer.LayerShape(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.score_fn, cfg.renorm,
-                            cfg.align, cfg.capacity, cfg.num_chunks)
+                            cfg.align, cfg.capacity, cfg.num_chunks, bias)
 
 
-def run_gpu_layer(cfg, inp, device="cuda", dw_dtype=torch.bfloat16):
+def run_gpu_layer(cfg, inp, device="cuda", dw_dtype=torch.bfloat16, biases=None):
+    """biases: None or the dict of moe_synth.make_biases."""
     from mixture_experts_grouped_router_gb300 import layer
     x, wi, wo, dout = (dev_bf16(inp[n], device) for n in ("x", "wi", "wo", "dout"))
     logits = torch.from_numpy(inp["logits"]).to(device)
-    b = layer.MoEBuffers(layer_shape(cfg), device=device, dw_dtype=dw_dtype)
-    layer.forward(b, x, logits, wi, wo)
+    b = layer.MoEBuffers(layer_shape(cfg, biases is not None), device=device, dw_dtype=dw_dtype)
+    bi = bo = None
+    if biases is not None:
+        bi, bo = dev_bf16(biases["bi"], device), dev_bf16(biases["bo"], device)
+    layer.forward(b, x, logits, wi, wo, bi=bi, bo=bo)
     layer.backward(b, dout, wi, wo)
     torch.cuda.synchronize()
     return b
 
 
-def run_oracle(cfg, inp):
+def run_oracle(cfg, inp, biases=None):
     f64 = moe_synth.bits_to_f64
     x, wi, wo, dout = (f64(inp[n]) for n in ("x", "wi", "wo", "dout"))
+    bi = bo = None
+    if biases is not None:
+        bi, bo = f64(biases["bi"]), f64(biases["bo"])
     fw = moe_ref.forward(x, inp["logits"], wi, wo, cfg.k, cfg.score_fn, cfg.renorm, cfg.align,
-                         cfg.capacity, cfg.num_chunks)
+                         cfg.capacity, cfg.num_chunks, bi=bi, bo=bo)
     bw = moe_ref.backward(fw, dout, wi, wo, cfg.k, cfg.num_chunks)
     return fw, bw
 

@@ -83,19 +83,33 @@ def test_validation_errors_need_no_gpu(L):
     assert st == L.MOE_ERR_INVALID_ARG and "workspace" in L.last_error()
     # gmm: N not a multiple of 8
     st = lib.moe_gmm(_ptr(), 64, _ptr(), 12, 64 * 12, 0, _ptr(), 1, 100, 64, 12, 0, None, 0, None,
-                     0, _ptr(), 0, 12, None, 0, None, None)
+                     0, None, 0, _ptr(), 0, 12, None, 0, None, None)
     assert st == L.MOE_ERR_UNSUPPORTED
     # gmm: SWIGLU_FWD without C2
     st = lib.moe_gmm(_ptr(), 64, _ptr(), 64, 64 * 64, 0, _ptr(), 1, 100, 64, 64, 1, None, 0, None,
-                     0, _ptr(), 0, 64, None, 0, None, None)
+                     0, None, 0, _ptr(), 0, 64, None, 0, None, None)
     assert st == L.MOE_ERR_INVALID_ARG
     # gmm: misaligned A
     st = lib.moe_gmm(_ptr(18), 64, _ptr(), 64, 64 * 64, 0, _ptr(), 1, 100, 64, 64, 0, None, 0,
-                     None, 0, _ptr(), 0, 64, None, 0, None, None)
+                     None, 0, None, 0, _ptr(), 0, 64, None, 0, None, None)
     assert st == L.MOE_ERR_UNSUPPORTED
     # gmm: in-place partial sum with bf16 C
     st = lib.moe_gmm(_ptr(), 64, _ptr(), 64, 64 * 64, 0, _ptr(), 1, 100, 64, 64, 0, None, 0,
-                     _ptr(32), 64, _ptr(32), 0, 64, None, 0, None, None)
+                     _ptr(32), 64, None, 0, _ptr(32), 0, 64, None, 0, None, None)
+    assert st == L.MOE_ERR_INVALID_ARG
+    # gmm: bias with a stride shorter than N
+    st = lib.moe_gmm(_ptr(), 64, _ptr(), 64, 64 * 64, 0, _ptr(), 2, 100, 64, 64, 0, None, 0,
+                     None, 0, _ptr(), 32, _ptr(), 0, 64, None, 0, None, None)
+    assert st == L.MOE_ERR_INVALID_ARG and "bias" in L.last_error()
+    # gmm: bias with the SwiGLU backward
+    st = lib.moe_gmm(_ptr(), 64, _ptr(), 64, 64 * 64, 1, _ptr(), 2, 100, 64, 64, 2, _ptr(), 128,
+                     None, 0, _ptr(), 64, _ptr(), 0, 128, None, 0, None, None)
+    assert st == L.MOE_ERR_INVALID_ARG and "bias" in L.last_error()
+    # group_colsum: N not a multiple of 8
+    st = lib.moe_group_colsum(_ptr(), 64, _ptr(), 4, 100, 60, _ptr(), 64, None)
+    assert st == L.MOE_ERR_UNSUPPORTED
+    # group_colsum: null output
+    st = lib.moe_group_colsum(_ptr(), 64, _ptr(), 4, 100, 64, None, 64, None)
     assert st == L.MOE_ERR_INVALID_ARG
     # tgmm: accumulate into bf16
     st = lib.moe_tgmm(_ptr(), 64, _ptr(), 64, _ptr(), 2, 100, 64, 64, _ptr(), 0, 64, 64 * 64, 1,
