@@ -21,7 +21,11 @@ the design notes of the repository):
   * capacity C keeps the first C assignments of each expert in (expert,
     token) order, before align_size padding; dropped slots contribute 0;
   * SwiGLU is act = silu(x wi_0) * (x wi_1), silu(z) = z * sigmoid(z);
-  * padding rows of the permuted activations and of dY are zero.
+  * padding rows of the permuted activations and of dY are zero;
+  * group-limited routing: a group scores the fp32 sum of its k/topk_group
+    largest selection keys; the best topk_group groups stay open;
+  * the auxiliary load-balancing loss is coeff * sum_e f_e P_e (Switch /
+    DeepSeek-V3 form) with routing counts taken before capacity drops.
 """
 from __future__ import annotations
 
@@ -34,7 +38,38 @@ SIGMOID = 1
 # ----------------------------------------------------------------------------
 # routing
 # ----------------------------------------------------------------------------
-def route_topk(logits: np.ndarray, k: int, score_fn: int, renorm: int, expert_bias=None):
+def group_limit_mask(key: np.ndarray, k: int, num_groups: int, topk_group: int) -> np.ndarray:
+    """Experts a token may choose under group-limited routing.
+
+    TE-2912, Description ("top-K with optional grouped/sigmoid scoring (for
+    DSv3 workload)") and the ``group_topk`` argument of the router.  The E
+    experts form ``num_groups`` contiguous groups of E / num_groups.  A
+    group's score is the sum of its m = k / topk_group largest selection keys,
+    added in fp32 from the largest down (DeepSeek-V3 sums the top two of each
+    of its 8 groups for k = 8 over 4 groups); the ``topk_group`` groups with
+    the highest scores (ties to the lower group id) stay open.
+
+    key: fp32 [T, E] selection keys.  Returns bool [T, E].
+    """
+    T, E = key.shape
+    G = num_groups
+    assert E % G == 0 and 1 <= topk_group <= G and k % topk_group == 0
+    gs = E // G
+    m = k // topk_group
+    assert m <= gs
+    grouped = np.sort(key.reshape(T, G, gs).astype(np.float32), axis=-1)[:, :, ::-1]
+    score = grouped[:, :, 0].copy()
+    for i in range(1, m):
+        score = (score + grouped[:, :, i]).astype(np.float32)
+    gid = np.broadcast_to(np.arange(G), (T, G))
+    order = np.lexsort((gid, -score.astype(np.float64)), axis=-1)
+    open_g = np.zeros((T, G), bool)
+    np.put_along_axis(open_g, order[:, :topk_group], True, axis=1)
+    return np.repeat(open_g, gs, axis=1)
+
+
+def route_topk(logits: np.ndarray, k: int, score_fn: int, renorm: int, expert_bias=None,
+               num_groups: int = 0, topk_group: int = 0):
     """Top-k expert selection and routing weights.
 
     TE-2912, Description ("TE's fused router ... top-K with optional
@@ -49,6 +84,9 @@ def route_topk(logits: np.ndarray, k: int, score_fn: int, renorm: int, expert_bi
     logits) the selection ranks the fp32 sums logit + bias while the weights
     still come from the unbiased logits.
 
+    With ``num_groups`` > 1, selection is group-limited (group_limit_mask):
+    only experts of the ``topk_group`` best groups compete.
+
     Returns (topk_idx int32 [T,k], topk_w float64 [T,k]).
     """
     logits = np.asarray(logits, dtype=np.float32)
@@ -59,8 +97,12 @@ def route_topk(logits: np.ndarray, k: int, score_fn: int, renorm: int, expert_bi
     key = logits if expert_bias is None else \
         (logits + np.asarray(expert_bias, dtype=np.float32)[None, :]).astype(np.float32)
     ids = np.broadcast_to(np.arange(E), (T, E))
+    rank_key = -key.astype(np.float64)
+    if num_groups > 1:
+        closed = ~group_limit_mask(key, k, num_groups, topk_group)
+        rank_key = np.where(closed, np.inf, rank_key)     # closed experts rank last
     # np.lexsort sorts by the last key first: -key descending, then expert id ascending
-    order = np.lexsort((ids, -key.astype(np.float64)), axis=-1)
+    order = np.lexsort((ids, rank_key), axis=-1)
     topk_idx = order[:, :k].astype(np.int32)
     if score_fn == SOFTMAX:
         m = l64.max(axis=1, keepdims=True)
@@ -119,6 +161,68 @@ def route_topk_bwd(logits: np.ndarray, topk_idx: np.ndarray, d_topk_w: np.ndarra
 # ----------------------------------------------------------------------------
 # permutation layout
 # ----------------------------------------------------------------------------
+def router_probs(logits: np.ndarray, score_fn: int) -> np.ndarray:
+    """Per-token expert probabilities for the load-balancing loss: the softmax
+    over all E, or (sigmoid scoring) the sigmoid scores divided by their sum
+    over all E (DeepSeek-V3's normalised affinities)."""
+    l = np.asarray(logits, dtype=np.float64)
+    if score_fn == SOFTMAX:
+        ex = np.exp(l - l.max(axis=1, keepdims=True))
+        return ex / ex.sum(axis=1, keepdims=True)
+    s = 1.0 / (1.0 + np.exp(-l))
+    return s / s.sum(axis=1, keepdims=True)
+
+
+def aux_loss(logits: np.ndarray, topk_idx: np.ndarray, E: int, score_fn: int, coeff: float):
+    """Auxiliary load-balancing loss (TE-2912, Description: "optional auxiliary
+    load-balancing loss"; the block returns it beside the output, sequence
+    diagram).  The pages name the loss but not its form; this is the standard
+    one (Switch Transformer; DeepSeek-V3's balance loss):
+
+        loss = coeff * sum_e f_e * P_e,
+        f_e  = E / (k T) * (number of (token, slot) choices of expert e),
+        P_e  = mean over tokens of router_probs[:, e].
+
+    Counts come from the routing decision (before any capacity drop).
+    Returns (loss, counts int64 [E], P float64 [E]).
+    """
+    T, k = topk_idx.shape
+    p = router_probs(logits, score_fn)
+    counts = np.bincount(topk_idx.reshape(-1).astype(np.int64), minlength=E)[:E]
+    f = E / (k * T) * counts if T > 0 else np.zeros(E)
+    P = p.mean(axis=0) if T > 0 else np.zeros(E)
+    return coeff * float((f * P).sum()), counts, P
+
+
+def aux_loss_bwd(logits: np.ndarray, counts: np.ndarray, k: int, score_fn: int, coeff: float,
+                 d_loss: float = 1.0) -> np.ndarray:
+    """Gradient of aux_loss w.r.t. the router logits (counts fixed), by the
+    chain rule with explicit Jacobians: dloss/dp[t, e] = coeff f_e / T, then
+    each token's probability Jacobian dp_e / dl_e' (softmax: p_e (delta_ee' -
+    p_e'); normalised sigmoid p = s / S: (delta_ee' - p_e) s_e' (1 - s_e') / S).
+    Returns float64 [T, E]."""
+    l = np.asarray(logits, dtype=np.float64)
+    T, E = l.shape
+    if T == 0:
+        return np.zeros((0, E))
+    f = E / (k * T) * np.asarray(counts, dtype=np.float64)
+    g = d_loss * coeff * f / T                        # dloss / dp[t, e], same for every t
+    out = np.zeros((T, E))
+    for t in range(T):
+        if score_fn == SOFTMAX:
+            p = router_probs(l[t:t + 1], SOFTMAX)[0]
+            jac = np.diag(p) - np.outer(p, p)          # jac[e, e'] = dp_e / dl_e'
+        else:
+            s = 1.0 / (1.0 + np.exp(-l[t]))
+            S = s.sum()
+            p = s / S
+            ds = s * (1.0 - s)                         # ds_e' / dl_e'
+            # dp_e / dl_e' = (delta_ee' - p_e) ds_e' / S
+            jac = (np.eye(E) - p[:, None]) * (ds / S)[None, :]
+        out[t] = g @ jac
+    return out
+
+
 def rows_cap(T: int, E: int, k: int, align: int) -> int:
     """Worst-case permuted rows, T*k + E*(align-1): TE-2912, review thread on
     ``recv_buffer_rows`` ("align_size > 0 + EP are combined")."""

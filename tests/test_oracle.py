@@ -16,6 +16,7 @@ import zlib
 import numpy as np
 import pytest
 import scipy.special
+import torch
 
 import brute_force as bf
 from oracle import moe_ref as ref
@@ -465,3 +466,160 @@ def test_group_colsum_closed_form():
     np.testing.assert_array_equal(out[0], g[:4].sum(0))
     np.testing.assert_array_equal(out[1], 0)
     np.testing.assert_array_equal(out[2], [sum(3 * r + c for r in range(4, 10)) for c in range(3)])
+
+
+# ---------------------------------------------------------------------------
+# group-limited routing
+# ---------------------------------------------------------------------------
+def test_golden_group_limited_hand():
+    g = json.load(open(os.path.join(GOLDEN, "route_group_limited_hand.json")))
+    for c in g["cases"]:
+        lg = np.array(c["logits"], np.float32)
+        bias = None if c["expert_bias"] is None else np.array(c["expert_bias"], np.float32)
+        idx, w = ref.route_topk(lg, c["k"], c["score_fn"], c["renorm"], expert_bias=bias,
+                                num_groups=c["num_groups"], topk_group=c["topk_group"])
+        assert idx.tolist() == c["topk_idx"], c["name"]
+        np.testing.assert_allclose(w, c["topk_w"], rtol=1e-13, atol=0)
+
+
+@pytest.mark.parametrize("E,G,k", [(8, 4, 2), (64, 8, 6), (256, 8, 8)])
+def test_group_limited_with_every_group_open_is_plain_topk(E, G, k):
+    rng = np.random.default_rng(E + k)
+    lg = rng.standard_normal((200, E)).astype(np.float32)
+    for sfn in (0, 1):
+        a = ref.route_topk(lg, k, sfn, 1)
+        b = ref.route_topk(lg, k, sfn, 1, num_groups=G, topk_group=G if k % G == 0 else 1)
+        if k % G == 0:
+            assert (a[0] == b[0]).all()
+            np.testing.assert_array_equal(a[1], b[1])
+    # one group holding all experts
+    c = ref.route_topk(lg, k, 0, 1, num_groups=1, topk_group=1)
+    assert (c[0] == ref.route_topk(lg, k, 0, 1)[0]).all()
+
+
+def _group_scores_by_hand(keys, G, m):
+    """Python-list restatement: per group, sort the keys descending and add the
+    first m in fp32 one by one."""
+    gs = len(keys) // G
+    out = []
+    for g in range(G):
+        vals = sorted((float(v) for v in keys[g * gs:(g + 1) * gs]), reverse=True)
+        acc = np.float32(vals[0])
+        for v in vals[1:m]:
+            acc = np.float32(acc + np.float32(v))
+        out.append(float(acc))
+    return out
+
+
+@pytest.mark.parametrize("E,G,tg,k,ties", [(64, 8, 3, 6, False), (256, 8, 4, 8, False),
+                                          (32, 4, 2, 4, True), (16, 16, 4, 4, True)])
+def test_group_limited_properties(E, G, tg, k, ties):
+    rng = np.random.default_rng(E * 3 + k)
+    T = 300
+    if ties:
+        lg = rng.integers(-2, 3, size=(T, E)).astype(np.float32)
+    else:
+        lg = rng.standard_normal((T, E)).astype(np.float32)
+    bias = (rng.standard_normal(E) * 0.5).astype(np.float32)
+    idx, _ = ref.route_topk(lg, k, 1, 1, expert_bias=bias, num_groups=G, topk_group=tg)
+    key = (lg + bias[None, :]).astype(np.float32)
+    gs, m = E // G, k // tg
+    for t in range(T):
+        sc = _group_scores_by_hand(key[t], G, m)
+        order = sorted(range(G), key=lambda g: (-sc[g], g))
+        open_g = set(order[:tg])
+        # (a) every chosen expert lies in an open group
+        assert all(int(e) // gs in open_g for e in idx[t])
+        # (b) open groups outrank closed ones
+        for go in open_g:
+            for gc in set(range(G)) - open_g:
+                assert sc[go] > sc[gc] or (sc[go] == sc[gc] and go < gc)
+        # (c) the choice is the top-k of the open experts by (key desc, id asc)
+        cand = [e for e in range(E) if e // gs in open_g]
+        want = sorted(cand, key=lambda e: (-float(key[t, e]), e))[:k]
+        assert idx[t].tolist() == want
+
+
+def test_group_limited_planted_max_instead_of_sum_is_caught(monkeypatch):
+    """A group score taken as the group's maximum (a plausible misreading)
+    fails the hand-worked fixture."""
+    orig = ref.group_limit_mask
+
+    def by_max(key, k, num_groups, topk_group):
+        return orig(key, topk_group, num_groups, topk_group)   # m = 1: the maximum
+    monkeypatch.setattr(ref, "group_limit_mask", by_max)
+    with pytest.raises(AssertionError):
+        test_golden_group_limited_hand()
+
+
+# ---------------------------------------------------------------------------
+# auxiliary load-balancing loss
+# ---------------------------------------------------------------------------
+def test_golden_aux_loss_hand():
+    g = json.load(open(os.path.join(GOLDEN, "aux_loss_hand.json")))
+    lg = np.log(np.array(g["logits_ln_of"], np.float64))
+    idx, _ = ref.route_topk(lg.astype(np.float32), g["k"], g["score_fn"], 1)
+    assert idx.tolist() == g["topk_idx"]
+    loss, counts, _ = ref.aux_loss(lg, idx, g["E"], g["score_fn"], g["coeff"])
+    assert counts.tolist() == g["counts"]
+    np.testing.assert_allclose(loss, g["loss"], rtol=1e-14)
+    d = ref.aux_loss_bwd(lg, counts, g["k"], g["score_fn"], g["coeff"])
+    np.testing.assert_allclose(d, g["d_logits"], rtol=1e-13, atol=1e-18)
+
+
+@pytest.mark.parametrize("E,k", [(4, 1), (8, 2), (64, 8), (5, 5)])
+@pytest.mark.parametrize("sfn", [0, 1])
+def test_aux_loss_equal_logits_closed_form(E, k, sfn):
+    """Equal logits: p = 1/E for every expert and every token picks experts
+    0..k-1, so sum_e f_e P_e = k * (E/k) * (1/E) = 1 and loss = coeff."""
+    lg = np.full((37, E), 0.25, np.float32)
+    idx, _ = ref.route_topk(lg, k, sfn, 1)
+    loss, counts, P = ref.aux_loss(lg, idx, E, sfn, 0.03)
+    np.testing.assert_allclose(P, 1.0 / E, rtol=1e-15)
+    assert counts.tolist() == [37] * k + [0] * (E - k)
+    np.testing.assert_allclose(loss, 0.03, rtol=1e-14)
+
+
+def test_aux_loss_uses_scipy_softmax_and_is_permutation_invariant():
+    rng = np.random.default_rng(9)
+    lg = rng.standard_normal((50, 12)).astype(np.float32)
+    idx, _ = ref.route_topk(lg, 3, 0, 1)
+    loss, counts, P = ref.aux_loss(lg, idx, 12, 0, 1.0)
+    np.testing.assert_allclose(P, scipy.special.softmax(lg.astype(np.float64), axis=1).mean(0),
+                               rtol=1e-13)
+    perm = rng.permutation(12)
+    inv = np.argsort(perm)
+    loss_p, _, _ = ref.aux_loss(lg[:, perm], inv[idx], 12, 0, 1.0)
+    np.testing.assert_allclose(loss_p, loss, rtol=1e-13)
+    # sigmoid probabilities are expit normalised over the experts
+    _, _, Ps = ref.aux_loss(lg, idx, 12, 1, 1.0)
+    s = scipy.special.expit(lg.astype(np.float64))
+    np.testing.assert_allclose(Ps, (s / s.sum(1, keepdims=True)).mean(0), rtol=1e-13)
+
+
+@pytest.mark.parametrize("sfn,E,k", [(0, 8, 2), (1, 16, 4), (0, 5, 1)])
+def test_aux_loss_bwd_vs_fd_and_autograd(sfn, E, k):
+    rng = np.random.default_rng(E + 10 * sfn)
+    T = 9
+    lg = rng.standard_normal((T, E))
+    idx, _ = ref.route_topk(lg.astype(np.float32), k, sfn, 1)
+    coeff = 0.7
+    _, counts, _ = ref.aux_loss(lg, idx, E, sfn, coeff)
+    d = ref.aux_loss_bwd(lg, counts, k, sfn, coeff, d_loss=1.3)
+    # central differences of 1.3 * loss, routing decision held fixed
+    h = 1e-6
+    fd = np.zeros_like(lg)
+    for t in range(T):
+        for e in range(E):
+            lp, lm = lg.copy(), lg.copy()
+            lp[t, e] += h
+            lm[t, e] -= h
+            fd[t, e] = 1.3 * (ref.aux_loss(lp, idx, E, sfn, coeff)[0] -
+                              ref.aux_loss(lm, idx, E, sfn, coeff)[0]) / (2 * h)
+    np.testing.assert_allclose(d, fd, rtol=1e-6, atol=1e-10)
+    # autograd of the loss written with torch ops
+    l_t = torch.tensor(lg, dtype=torch.float64, requires_grad=True)
+    p = torch.softmax(l_t, 1) if sfn == 0 else torch.sigmoid(l_t) / torch.sigmoid(l_t).sum(1, keepdim=True)
+    f = torch.tensor(counts, dtype=torch.float64) * E / (k * T)
+    (1.3 * coeff * (f * p.mean(0)).sum()).backward()
+    np.testing.assert_allclose(d, l_t.grad.numpy(), rtol=1e-12, atol=1e-15)
