@@ -79,14 +79,14 @@ struct Book {
 };
 constexpr int STG_OFFSET = 4 * STAGE_BYTES;  // = 6 x 32 KB; 1024-aligned
 
-// Per-kernel ring.  The forward and dgrad GEMMs run as 2-SM MMAs whose stage
-// holds this CTA's 128-row A tile and half of the B tile (32 KB, 6 stages).
-// The weight-gradient GEMM (whose last K block of an expert is zeroed per
-// CTA) and the SwiGLU-backward dgrad (measured faster this way) keep whole B
-// tiles multicast within the pair (48 KB, 4 stages).
+// Per-kernel ring.  The forward, dgrad and weight-gradient GEMMs run as 2-SM
+// MMAs whose stage holds this CTA's 128-row (tgmm: 128-column) A tile and
+// half of the B tile (32 KB, 6 stages).  The SwiGLU-backward dgrad (measured
+// faster this way) keeps whole B tiles multicast within the pair (48 KB,
+// 4 stages).
 template <int KIND, int EPI>
 struct Ring {
-  static constexpr bool two_sm = KIND == 0 && EPI != MOE_EPI_SWIGLU_BWD;
+  static constexpr bool two_sm = KIND == 1 || EPI != MOE_EPI_SWIGLU_BWD;
   static constexpr int stages = two_sm ? 6 : 4;
   static constexpr int b_bytes = two_sm ? B_BYTES / 2 : B_BYTES;
   static constexpr int stage_bytes = A_BYTES + b_bytes;
@@ -631,6 +631,17 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             // expects the whole pair's stage
             const uint32_t fbl = tc::mapa_shared(tc::smem_u32(fb), 0);
             if (leader) tc::mbar_expect_tx(fb, 2 * kStageB);
+            if (KIND == KIND_TGMM) {
+              // this CTA's 128 output rows of A (two 64-column boxes) and its
+              // 128 columns of B, both over the K block's 64 rows
+              const int r = ti.row0 + kb * BK;
+              const int m0 = ti.m_idx * BM;
+              const int nb = ti.n_idx * BN + crank * (BN / 2);
+              tc::tma_load_2d_2sm(sa, &tmA, fbl, m0, r);
+              tc::tma_load_2d_2sm(sa + BOX_BYTES, &tmA, fbl, m0 + 64, r);
+              tc::tma_load_2d_2sm(sb, &tmB, fbl, nb, r);
+              tc::tma_load_2d_2sm(sb + BOX_BYTES, &tmB, fbl, nb + 64, r);
+            } else {
             tc::tma_load_2d_2sm(sa, &tmA, fbl, kb * BK, ti.row0);
             if (B_MN) {
               // this CTA's 128 columns of B: two 64-column boxes
@@ -645,6 +656,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
               }
             } else {
               tc::tma_load_3d_2sm(sb, &tmB, fbl, kb * BK, ti.n_idx * BN + crank * (BN / 2), ti.e);
+            }
             }
           } else {
             tc::mbar_expect_tx(fb, kStageB);
@@ -706,18 +718,25 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         uint8_t *sb = sa + A_BYTES;
         if (KIND == KIND_TGMM) {
           // rows past the expert's last row belong to the next expert: zero
-          // them in both operands (one 128-byte row per K index per box)
+          // them in both operands (one 128-byte row per K index per box).
+          // 2-SM: this CTA's four boxes and the same four in the partner
+          // CTA, whose copies have landed too (they complete on this CTA's
+          // full barrier) and whose boxes this MMA reads.
           const int valid = ti.row_end - (ti.row0 + kb * BK);
           if (valid < BK) {
+            constexpr int kBoxes = k2SM ? 4 : 6;
             const int nrows = BK - valid;
-            for (int i = lane; i < nrows * 6 * 8; i += 32) {
+            for (int i = lane; i < nrows * kBoxes * 8; i += 32) {
               const int chunk = i & 7;
               const int rr = valid + ((i >> 3) % nrows);
               const int box = (i >> 3) / nrows;
               uint8_t *base = box < 2 ? sa + box * BOX_BYTES : sb + (box - 2) * BOX_BYTES;
-              *reinterpret_cast<uint4 *>(base + rr * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
+              uint8_t *at = base + rr * 128 + chunk * 16;
+              *reinterpret_cast<uint4 *>(at) = make_uint4(0, 0, 0, 0);
+              if (k2SM) tc::st_cluster_zero16(tc::mapa_shared(tc::smem_u32(at), 1));
             }
             tc::fence_proxy_async_smem();
+            if (k2SM) tc::fence_proxy_async_smem_cluster();
           }
           __syncwarp();
         }

@@ -236,6 +236,17 @@ MOE_DEVINL void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// The same for writes into the partner CTA's shared memory.
+MOE_DEVINL void fence_proxy_async_smem_cluster() {
+  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+}
+
+// 16 zero bytes at a shared::cluster address (the partner CTA's shared memory).
+MOE_DEVINL void st_cluster_zero16(uint32_t cluster_addr) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(cluster_addr), "r"(0u)
+               : "memory");
+}
+
 // ------------------------------------------------- tcgen05 descriptors
 // Shared-memory matrix descriptor, 128-byte swizzle, descriptor version 1.
 //   bits 0-13 start address >> 4, 16-29 leading byte offset >> 4,
