@@ -92,8 +92,8 @@ size_t moe_permute_workspace_bytes(int T, int E);
 /*
  * moe_route_topk -- top-k expert selection and routing weights.
  * TE-2912, Description: the fused router, "top-K with optional
- * grouped/sigmoid scoring (for DSv3 workload)" (grouped scoring is not
- * provided).
+ * grouped/sigmoid scoring (for DSv3 workload)"; the router's group_topk
+ * argument (the commit passing None as group_topk).
  *   logits    fp32 [T, ld_logits >= E]      router logits
  *   k         1 <= k <= min(E, 16); E <= 256
  *   score_fn  MOE_SCORE_SOFTMAX: softmax over all E experts;
@@ -103,14 +103,61 @@ size_t moe_permute_workspace_bytes(int T, int E);
  *             (TE-2912, the expert_bias residual; MaxText PR #2579 "Onboard
  *             explicit sharding to deepseek", pre-bias logits): experts are
  *             ranked by the fp32 sum logit + bias, weights use the logits
+ *   num_groups, topk_group  group-limited selection when num_groups > 1
+ *             (0 or 1: off): the E experts form num_groups contiguous groups
+ *             (E % num_groups == 0); a group scores the fp32 sum of its
+ *             m = k / topk_group largest keys, added from the largest down
+ *             (topk_group must divide k, m <= E / num_groups); only experts of
+ *             the topk_group best groups (ties to the lower group id) compete
  *   topk_idx  int32 [T, k] out: experts by descending key, ties to the lower id
  *   topk_w    fp32  [T, k] out: the selected (renormalised) scores, same order
  * Selection compares fp32 keys (the score maps are monotone); a NaN key ranks
  * below every number.
  */
 moe_status_t moe_route_topk(const float *logits, int64_t ld_logits, int T, int E, int k,
-                            int score_fn, int renorm, const float *expert_bias,
-                            int32_t *topk_idx, float *topk_w, moe_stream_t stream);
+                            int score_fn, int renorm, const float *expert_bias, int num_groups,
+                            int topk_group, int32_t *topk_idx, float *topk_w,
+                            moe_stream_t stream);
+
+/*
+ * moe_aux_loss -- auxiliary load-balancing loss of the routing decision.
+ * TE-2912, Description ("optional auxiliary load-balancing loss") and the
+ * sequence diagram (the block returns it beside the output).  The pages do
+ * not print the formula; this is the Switch-Transformer / DeepSeek-V3 form:
+ *     loss = coeff * sum_e f_e P_e,   f_e = E / (k T) * counts[e],
+ *     P_e  = mean over tokens of p[t, e],
+ * p = softmax of the logits over all E (MOE_SCORE_SOFTMAX) or the sigmoid
+ * scores divided by their sum over all E (MOE_SCORE_SIGMOID).
+ *   logits      fp32 [T, ld_logits >= E]; topk_idx int32 [T, k] (the routing
+ *               decision, before any capacity drop)
+ *   counts      int32 [E] out: choices of each expert
+ *   probs_mean  fp32 [E] out: P_e
+ *   loss        fp32 [1] out (device)
+ *   workspace   >= moe_aux_loss_workspace_bytes(T, E) bytes of device memory
+ *               (4-byte aligned), caller-owned scratch
+ * fp32 sums in a fixed order: the result does not vary between runs.
+ * E <= 256, k <= 16.  T = 0 gives zeros.
+ */
+size_t moe_aux_loss_workspace_bytes(int T, int E);
+moe_status_t moe_aux_loss(const float *logits, int64_t ld_logits, int T, int E, int k,
+                          int score_fn, const int32_t *topk_idx, float coeff, int32_t *counts,
+                          float *probs_mean, float *loss, void *workspace,
+                          size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * moe_aux_loss_bwd -- logit gradient of moe_aux_loss (counts fixed), scaled
+ * by d_loss (host scalar):
+ *     softmax:  d_l[t, e] = g p_e (f_e - c_t)
+ *     sigmoid:  d_l[t, e] = g s_e (1 - s_e) / S_t (f_e - c_t)
+ * with g = d_loss coeff / T, c_t = sum_j f_j p[t, j], S_t = sum_j s_j.
+ *   counts    int32 [E] as moe_aux_loss wrote them
+ *   d_logits  fp32 [T, ld_dlogits >= E]: written, or added to when
+ *             accumulate != 0 (e.g. on top of moe_route_topk_bwd's output)
+ */
+moe_status_t moe_aux_loss_bwd(const float *logits, int64_t ld_logits, int T, int E, int k,
+                              int score_fn, const int32_t *counts, float coeff, float d_loss,
+                              float *d_logits, int64_t ld_dlogits, int accumulate,
+                              moe_stream_t stream);
 
 /*
  * moe_route_topk_bwd -- gradient of the routing weights w.r.t. the logits,

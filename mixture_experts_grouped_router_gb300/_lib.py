@@ -60,7 +60,12 @@ _SIGS = {
     "moe_test_stall_loads": (None, [_I]),
     "moe_rows_cap": (_I64, [_I, _I, _I, _I]),
     "moe_permute_workspace_bytes": (_SZ, [_I, _I]),
-    "moe_route_topk": (_I, [_P, _I64, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
+    "moe_route_topk": (_I, [_P, _I64, _I, _I, _I, _I, _I, _P, _I, _I, _P, _P, _P]),
+    "moe_aux_loss_workspace_bytes": (_SZ, [_I, _I]),
+    "moe_aux_loss": (_I, [_P, _I64, _I, _I, _I, _I, _P, ctypes.c_float, _P, _P, _P, _P, _SZ,
+                          _P]),
+    "moe_aux_loss_bwd": (_I, [_P, _I64, _I, _I, _I, _I, _P, ctypes.c_float, ctypes.c_float, _P,
+                              _I64, _I, _P]),
     "moe_route_topk_bwd": (_I, [_P, _I64, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I64, _P]),
     "moe_permute": (_I, [_P, _I64, _P, _I, _I, _I, _I, _I, _I, _P, _I64, _I64, _P, _P, _P, _P,
                          _P, _P, _SZ, _P, _P]),
@@ -136,10 +141,34 @@ def moe_permute_workspace_bytes(T: int, E: int) -> int:
 
 
 def moe_route_topk(logits, k, score_fn, renorm, topk_idx, topk_w, stream=None,
-                   expert_bias=None):
+                   expert_bias=None, num_groups=0, topk_group=0):
     T, E = logits.shape
     _check(LIB.moe_route_topk(_ptr(logits), _ld(logits), T, E, k, score_fn, int(renorm),
-                              _ptr(expert_bias), _ptr(topk_idx), _ptr(topk_w), _stream(stream)))
+                              _ptr(expert_bias), int(num_groups), int(topk_group),
+                              _ptr(topk_idx), _ptr(topk_w), _stream(stream)))
+
+
+def moe_aux_loss_workspace_bytes(T: int, E: int) -> int:
+    return int(LIB.moe_aux_loss_workspace_bytes(T, E))
+
+
+def moe_aux_loss(logits, topk_idx, score_fn, coeff, counts, probs_mean, loss, workspace,
+                 stream=None):
+    """counts int32 [E], probs_mean fp32 [E], loss fp32 [1] (device outputs)."""
+    T, E = logits.shape
+    k = topk_idx.shape[1]
+    _check(LIB.moe_aux_loss(_ptr(logits), _ld(logits), T, E, k, score_fn, _ptr(topk_idx),
+                            float(coeff), _ptr(counts), _ptr(probs_mean), _ptr(loss),
+                            _ptr(workspace), workspace.numel() * workspace.element_size(),
+                            _stream(stream)))
+
+
+def moe_aux_loss_bwd(logits, counts, k, score_fn, coeff, d_logits, d_loss=1.0, accumulate=True,
+                     stream=None):
+    T, E = logits.shape
+    _check(LIB.moe_aux_loss_bwd(_ptr(logits), _ld(logits), T, E, k, score_fn, _ptr(counts),
+                                float(coeff), float(d_loss), _ptr(d_logits), _ld(d_logits),
+                                int(accumulate), _stream(stream)))
 
 
 def moe_route_topk_bwd(logits, topk_idx, topk_w, d_topk_w, score_fn, renorm, d_logits,

@@ -92,8 +92,9 @@ size_t moe_permute_workspace_bytes(int T, int E) {
 }
 
 moe_status_t moe_route_topk(const float *logits, int64_t ld_logits, int T, int E, int k,
-                            int score_fn, int renorm, const float *expert_bias,
-                            int32_t *topk_idx, float *topk_w, moe_stream_t stream) {
+                            int score_fn, int renorm, const float *expert_bias, int num_groups,
+                            int topk_group, int32_t *topk_idx, float *topk_w,
+                            moe_stream_t stream) {
   set_error("");
   REQUIRE(T >= 0 && E > 0 && k > 0, MOE_ERR_INVALID_ARG, "moe_route_topk: T=%d E=%d k=%d", T, E, k);
   REQUIRE(k <= E, MOE_ERR_INVALID_ARG, "moe_route_topk: k=%d > E=%d", k, E);
@@ -103,9 +104,70 @@ moe_status_t moe_route_topk(const float *logits, int64_t ld_logits, int T, int E
           "moe_route_topk: bad score_fn %d", score_fn);
   REQUIRE(T == 0 || (logits && topk_idx && topk_w), MOE_ERR_INVALID_ARG,
           "moe_route_topk: null pointer");
+  REQUIRE(num_groups >= 0 && topk_group >= 0, MOE_ERR_INVALID_ARG,
+          "moe_route_topk: num_groups=%d topk_group=%d", num_groups, topk_group);
+  if (num_groups > 1) {
+    REQUIRE(E % num_groups == 0, MOE_ERR_INVALID_ARG,
+            "moe_route_topk: E=%d not a multiple of num_groups=%d", E, num_groups);
+    REQUIRE(topk_group >= 1 && topk_group <= num_groups && k % topk_group == 0 &&
+                k / topk_group <= E / num_groups,
+            MOE_ERR_INVALID_ARG,
+            "moe_route_topk: topk_group=%d must divide k=%d, be <= num_groups=%d, and "
+            "k/topk_group <= E/num_groups", topk_group, k, num_groups);
+  }
   return cuda_status(moe::launch_route_topk(logits, ld_logits, T, E, k, score_fn, renorm,
-                                            expert_bias, topk_idx, topk_w, (cudaStream_t)stream),
+                                            expert_bias, num_groups, topk_group, topk_idx,
+                                            topk_w, (cudaStream_t)stream),
                      "moe_route_topk launch");
+}
+
+size_t moe_aux_loss_workspace_bytes(int T, int E) {
+  if (T < 0 || E <= 0) return 0;
+  return moe::aux_loss_workspace_bytes(T, E);
+}
+
+moe_status_t moe_aux_loss(const float *logits, int64_t ld_logits, int T, int E, int k,
+                          int score_fn, const int32_t *topk_idx, float coeff, int32_t *counts,
+                          float *probs_mean, float *loss, void *workspace,
+                          size_t workspace_bytes, moe_stream_t stream) {
+  set_error("");
+  REQUIRE(T >= 0 && E > 0 && k > 0 && k <= E, MOE_ERR_INVALID_ARG,
+          "moe_aux_loss: T=%d E=%d k=%d", T, E, k);
+  REQUIRE(E <= 256 && k <= 16, MOE_ERR_UNSUPPORTED, "moe_aux_loss: needs E <= 256, k <= 16");
+  REQUIRE(ld_logits >= E, MOE_ERR_INVALID_ARG, "moe_aux_loss: ld_logits < E");
+  REQUIRE(score_fn == MOE_SCORE_SOFTMAX || score_fn == MOE_SCORE_SIGMOID, MOE_ERR_INVALID_ARG,
+          "moe_aux_loss: bad score_fn %d", score_fn);
+  REQUIRE(counts && probs_mean && loss && workspace && (T == 0 || (logits && topk_idx)),
+          MOE_ERR_INVALID_ARG, "moe_aux_loss: null pointer");
+  REQUIRE(workspace_bytes >= moe::aux_loss_workspace_bytes(T, E), MOE_ERR_INVALID_ARG,
+          "moe_aux_loss: workspace of %zu bytes < %zu", workspace_bytes,
+          moe::aux_loss_workspace_bytes(T, E));
+  REQUIRE((reinterpret_cast<uintptr_t>(workspace) & 3u) == 0, MOE_ERR_INVALID_ARG,
+          "moe_aux_loss: workspace must be 4-byte aligned");
+  return cuda_status(moe::launch_aux_loss(logits, ld_logits, T, E, k, score_fn, topk_idx, coeff,
+                                          counts, probs_mean, loss, workspace,
+                                          (cudaStream_t)stream),
+                     "moe_aux_loss launch");
+}
+
+moe_status_t moe_aux_loss_bwd(const float *logits, int64_t ld_logits, int T, int E, int k,
+                              int score_fn, const int32_t *counts, float coeff, float d_loss,
+                              float *d_logits, int64_t ld_dlogits, int accumulate,
+                              moe_stream_t stream) {
+  set_error("");
+  REQUIRE(T >= 0 && E > 0 && k > 0 && k <= E, MOE_ERR_INVALID_ARG,
+          "moe_aux_loss_bwd: T=%d E=%d k=%d", T, E, k);
+  REQUIRE(E <= 256, MOE_ERR_UNSUPPORTED, "moe_aux_loss_bwd: needs E <= 256");
+  REQUIRE(ld_logits >= E && ld_dlogits >= E, MOE_ERR_INVALID_ARG,
+          "moe_aux_loss_bwd: leading dimension < E");
+  REQUIRE(score_fn == MOE_SCORE_SOFTMAX || score_fn == MOE_SCORE_SIGMOID, MOE_ERR_INVALID_ARG,
+          "moe_aux_loss_bwd: bad score_fn %d", score_fn);
+  REQUIRE(T == 0 || (logits && counts && d_logits), MOE_ERR_INVALID_ARG,
+          "moe_aux_loss_bwd: null pointer");
+  return cuda_status(moe::launch_aux_loss_bwd(logits, ld_logits, T, E, k, score_fn, counts, coeff,
+                                              d_loss, d_logits, ld_dlogits, accumulate,
+                                              (cudaStream_t)stream),
+                     "moe_aux_loss_bwd launch");
 }
 
 moe_status_t moe_route_topk_bwd(const float *logits, int64_t ld_logits, const int32_t *topk_idx,

@@ -15,8 +15,15 @@ int test_stall_loads();    // test hook (moe_test_stall_loads)
 
 // route.cu
 cudaError_t launch_route_topk(const float *logits, int64_t ld, int T, int E, int k, int score_fn,
-                              int renorm, const float *bias, int32_t *idx, float *w,
-                              cudaStream_t s);
+                              int renorm, const float *bias, int num_groups, int topk_group,
+                              int32_t *idx, float *w, cudaStream_t s);
+size_t aux_loss_workspace_bytes(int T, int E);
+cudaError_t launch_aux_loss(const float *logits, int64_t ld, int T, int E, int k, int score_fn,
+                            const int32_t *idx, float coeff, int32_t *counts, float *P,
+                            float *loss, void *ws, cudaStream_t s);
+cudaError_t launch_aux_loss_bwd(const float *logits, int64_t ld, int T, int E, int k,
+                                int score_fn, const int32_t *counts, float coeff, float d_loss,
+                                float *d_logits, int64_t ld_out, int accumulate, cudaStream_t s);
 cudaError_t launch_route_topk_bwd(const float *logits, int64_t ld, const int32_t *idx,
                                   const float *w, const float *dw, int T, int E, int k,
                                   int score_fn, int renorm, float *d_logits, int64_t ld_out,

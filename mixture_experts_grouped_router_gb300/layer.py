@@ -12,6 +12,11 @@ backward  unpermute_bwd -> route_topk_bwd (d_logits) -> gmm(dgrad down, SwiGLU-b
           epilogue) -> tgmm(dWo) -> gmm(dgrad up) -> tgmm(dWi) -> combine without
           weights (dispatch bwd)
 
+Routing options: group-limited top-k (num_groups > 1: only the topk_group
+best expert groups compete) and, with aux_coeff > 0, the auxiliary
+load-balancing loss (forward: b.aux_loss; backward: its logit gradient is
+added to b.d_logits).
+
 With bias=True the expert FFN carries biases (bi [E, 2f] on [gate | up],
 bo [E, d] on the output), added in the GEMM epilogues; their gradients are
 per-expert column sums of dH and dY (moe_group_colsum).
@@ -43,6 +48,9 @@ class LayerShape:
     capacity: int = 0
     num_chunks: int = 1
     bias: bool = False
+    num_groups: int = 0
+    topk_group: int = 0
+    aux_coeff: float = 0.0
 
 
 class MoEBuffers:
@@ -82,6 +90,12 @@ class MoEBuffers:
         self.dbi = torch.empty(E, 2 * f, dtype=f32, device=dev) if s.bias else None
         self.dbo = torch.empty(E, d, dtype=f32, device=dev) if s.bias else None
         self.dev_status = torch.zeros(1, dtype=i32, device=dev)
+        if s.aux_coeff:
+            self.aux_counts = torch.empty(E, dtype=i32, device=dev)
+            self.aux_probs = torch.empty(E, dtype=f32, device=dev)
+            self.aux_loss = torch.empty(1, dtype=f32, device=dev)
+            self.aux_ws = torch.empty(L.moe_aux_loss_workspace_bytes(T, E), dtype=torch.uint8,
+                                      device=dev)
 
 
 def _noop(_name):
@@ -98,8 +112,13 @@ def forward(b: MoEBuffers, x, logits, wi, wo, stream=None, mark=_noop, bi=None, 
     if s.bias != (bi is not None and bo is not None):
         raise ValueError("forward: pass bi and bo exactly when the layer shape has bias=True")
     b.logits = logits
-    L.moe_route_topk(logits, s.k, s.score_fn, s.renorm, b.topk_idx, b.topk_w, stream)
+    L.moe_route_topk(logits, s.k, s.score_fn, s.renorm, b.topk_idx, b.topk_w, stream,
+                     num_groups=s.num_groups, topk_group=s.topk_group)
     mark("route")
+    if s.aux_coeff:
+        L.moe_aux_loss(logits, b.topk_idx, s.score_fn, s.aux_coeff, b.aux_counts, b.aux_probs,
+                       b.aux_loss, b.aux_ws, stream)
+        mark("aux_loss")
     L.moe_permute(x, b.topk_idx, s.E, s.align, s.capacity, b.xs, b.group_sizes, b.kept_counts,
                   b.group_offsets, b.s2f, b.f2s, b.ws, b.dev_status, stream)
     mark("permute")
@@ -140,6 +159,10 @@ def backward(b: MoEBuffers, dout, wi, wo, stream=None, mark=_noop):
     L.moe_route_topk_bwd(b.logits, b.topk_idx, b.topk_w, b.d_topk_w, s.score_fn, s.renorm,
                          b.d_logits, stream)
     mark("route_bwd")
+    if s.aux_coeff:
+        L.moe_aux_loss_bwd(b.logits, b.aux_counts, s.k, s.score_fn, s.aux_coeff, b.d_logits,
+                           d_loss=1.0, accumulate=True, stream=stream)
+        mark("aux_loss_bwd")
     # dAct = dY . wo^T, fused with the SwiGLU backward into dH = [dgate | dup]
     L.moe_gmm(b.dy, wo, 1, b.group_offsets, b.dh, L.EPI_SWIGLU_BWD, aux=b.h,
               dev_status=b.dev_status, stream=stream)
@@ -174,10 +197,12 @@ def backward(b: MoEBuffers, dout, wi, wo, stream=None, mark=_noop):
 
 def kernels_per_step(s: LayerShape) -> int:
     """Kernels one forward + backward launches (route 1, permute 3, each GEMM 1,
-    combine 1, unpermute_bwd 1, route_bwd 1, dispatch backward 1, bias gradients 2)."""
+    combine 1, unpermute_bwd 1, route_bwd 1, dispatch backward 1, bias gradients 2,
+    auxiliary loss 2 + 1)."""
     up = max(1, s.num_chunks)
-    fwd = 1 + 3 + up + 1 + 1
-    bwd = 1 + 1 + 1 + 1 + 2 * up + 1 + (2 if s.bias else 0)
+    aux = bool(s.aux_coeff)
+    fwd = 1 + 3 + up + 1 + 1 + (2 if aux and s.T > 0 else 1 if aux else 0)
+    bwd = 1 + 1 + 1 + 1 + 2 * up + 1 + (2 if s.bias else 0) + (1 if aux and s.T > 0 else 0)
     return fwd + bwd
 
 

@@ -62,14 +62,15 @@ def run_gpu_layer(cfg, inp, device="cuda", dw_dtype=torch.bfloat16, biases=None)
     return b
 
 
-def run_oracle(cfg, inp, biases=None):
+def run_oracle(cfg, inp, biases=None, num_groups=0, topk_group=0):
     f64 = moe_synth.bits_to_f64
     x, wi, wo, dout = (f64(inp[n]) for n in ("x", "wi", "wo", "dout"))
     bi = bo = None
     if biases is not None:
         bi, bo = f64(biases["bi"]), f64(biases["bo"])
     fw = moe_ref.forward(x, inp["logits"], wi, wo, cfg.k, cfg.score_fn, cfg.renorm, cfg.align,
-                         cfg.capacity, cfg.num_chunks, bi=bi, bo=bo)
+                         cfg.capacity, cfg.num_chunks, bi=bi, bo=bo, num_groups=num_groups,
+                         topk_group=topk_group)
     bw = moe_ref.backward(fw, dout, wi, wo, cfg.k, cfg.num_chunks)
     return fw, bw
 

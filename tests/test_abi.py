@@ -56,13 +56,24 @@ def _ptr(v=16):
 def test_validation_errors_need_no_gpu(L):
     lib = L.LIB
     # k > E
-    st = lib.moe_route_topk(_ptr(), 8, 10, 8, 9, 0, 1, None, _ptr(), _ptr(), None)
+    st = lib.moe_route_topk(_ptr(), 8, 10, 8, 9, 0, 1, None, 0, 0, _ptr(), _ptr(), None)
     assert st == L.MOE_ERR_INVALID_ARG and "k=9" in L.last_error()
     # E above the router's limit
-    st = lib.moe_route_topk(_ptr(), 300, 10, 300, 2, 0, 1, None, _ptr(), _ptr(), None)
+    st = lib.moe_route_topk(_ptr(), 300, 10, 300, 2, 0, 1, None, 0, 0, _ptr(), _ptr(), None)
     assert st == L.MOE_ERR_UNSUPPORTED
     # bad score function
-    st = lib.moe_route_topk(_ptr(), 8, 10, 8, 2, 7, 1, None, _ptr(), _ptr(), None)
+    st = lib.moe_route_topk(_ptr(), 8, 10, 8, 2, 7, 1, None, 0, 0, _ptr(), _ptr(), None)
+    assert st == L.MOE_ERR_INVALID_ARG
+    # route: E not a multiple of num_groups; topk_group not dividing k
+    st = lib.moe_route_topk(_ptr(), 10, 10, 10, 4, 0, 1, None, 4, 2, _ptr(), _ptr(), None)
+    assert st == L.MOE_ERR_INVALID_ARG and "num_groups" in L.last_error()
+    st = lib.moe_route_topk(_ptr(), 16, 10, 16, 4, 0, 1, None, 4, 3, _ptr(), _ptr(), None)
+    assert st == L.MOE_ERR_INVALID_ARG and "topk_group" in L.last_error()
+    # aux loss: workspace too small; bad score_fn in the backward
+    st = lib.moe_aux_loss(_ptr(), 8, 1000, 8, 2, 0, _ptr(), 0.01, _ptr(), _ptr(), _ptr(), _ptr(),
+                          4, None)
+    assert st == L.MOE_ERR_INVALID_ARG and "workspace" in L.last_error()
+    st = lib.moe_aux_loss_bwd(_ptr(), 8, 1000, 8, 2, 5, _ptr(), 0.01, 1.0, _ptr(), 8, 1, None)
     assert st == L.MOE_ERR_INVALID_ARG
     # route backward: k > E, bad leading dimension
     st = lib.moe_route_topk_bwd(_ptr(), 8, _ptr(), _ptr(), _ptr(), 10, 8, 9, 0, 1, _ptr(), 8, None)

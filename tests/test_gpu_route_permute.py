@@ -185,3 +185,30 @@ def test_route_topk_bwd(case):
         sel = np.zeros((T, E), bool)
         np.put_along_axis(sel, ridx.astype(np.int64), True, 1)
         assert (got[~sel] == 0).all()
+
+
+GROUP_CASES = [
+    # T, E, k, num_groups, topk_group, score_fn, renorm, bias, logits kind
+    (300, 8, 4, 4, 2, 0, 1, False, "normal"), (513, 64, 6, 8, 3, 1, 1, True, "normal"),
+    (1000, 256, 8, 8, 4, 1, 1, True, "normal"), (257, 32, 4, 4, 2, 0, 0, False, "ties"),
+    (129, 16, 4, 16, 4, 1, 0, False, "ties"), (100, 160, 8, 5, 2, 0, 1, True, "skew"),
+    (64, 256, 16, 32, 8, 1, 1, False, "normal"), (77, 12, 3, 3, 3, 0, 1, False, "equal"),
+]
+
+
+@pytest.mark.parametrize("case", GROUP_CASES)
+def test_route_topk_group_limited(case):
+    T, E, k, G, tg, sfn, ren, with_bias, kind = case
+    rng = np.random.default_rng(T + E + G)
+    lg = _logits(rng, T, E, kind)
+    bias = (rng.standard_normal(E) * 0.5).astype(np.float32) if with_bias else None
+    idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, k, dtype=torch.float32, device="cuda")
+    L.moe_route_topk(torch.from_numpy(lg).cuda(), k, sfn, ren, idx, w,
+                     expert_bias=None if bias is None else torch.from_numpy(bias).cuda(),
+                     num_groups=G, topk_group=tg)
+    torch.cuda.synchronize()
+    ridx, rw = moe_ref.route_topk(lg, k, sfn, ren, expert_bias=bias, num_groups=G,
+                                  topk_group=tg)
+    assert (idx.cpu().numpy() == ridx).all()
+    np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=0, atol=W_ATOL)
