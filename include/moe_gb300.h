@@ -53,6 +53,8 @@ typedef enum {
 enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 };
 enum { MOE_DTYPE_BF16 = 0, MOE_DTYPE_F32 = 1 };
 enum { MOE_EPI_NONE = 0, MOE_EPI_SWIGLU_FWD = 1, MOE_EPI_SWIGLU_BWD = 2 };
+/* 8-bit float formats (OCP): E4M3FN (max 448, no infinities), E5M2 (max 57344) */
+enum { MOE_FP8_E4M3 = 0, MOE_FP8_E5M2 = 1 };
 
 /* Static description of a status code. */
 const char *moe_status_string(int status);
@@ -290,6 +292,63 @@ moe_status_t moe_gmm(const uint16_t *A, int64_t lda, const uint16_t *B, int64_t 
 moe_status_t moe_group_colsum(const uint16_t *G, int64_t ldg, const int32_t *group_offsets,
                               int E, int64_t rows_cap, int N, float *out, int64_t ld_out,
                               moe_stream_t stream);
+
+/* ------------------------------------------------------------------ FP8 --
+ * Current tensor scaling for the FP8 expert GEMMs.  MaxText PR #2319
+ * "[Draft] Integrate TE/JAX GroupedGEMM for MoE", review thread on the
+ * quantizer settings of moe.py: current tensor scaling, float8_e4m3fn
+ * forward, float8_e5m2 backward, 2x (row- and column-wise) quantization;
+ * TE-2912, wi-fusion commit: one amax per expert for the fused weight.
+ *   scale = fp8_max / amax (fp32; 1 when amax is 0 or not finite)
+ *   code  = round-to-nearest-even(fp32(x * scale)), saturated to +-fp8_max
+ *   value = code / scale
+ */
+
+/*
+ * moe_fp8_amax -- amax[g] = max |x| over the rows of group g.
+ *   x        bf16 [rows, ldx >= cols] (16-byte aligned, ldx % 8 == 0, cols % 8 == 0)
+ *   groups   1, or E for per-expert weights (rows % groups == 0: group g is
+ *            rows [g * rows / groups, (g + 1) * rows / groups))
+ *   group_offsets (groups == 1 only; may be NULL): only rows < group_offsets[E]
+ *            are read (permuted activations)
+ *   amax     fp32 [groups] out (device)
+ */
+moe_status_t moe_fp8_amax(const uint16_t *x, int64_t ldx, int64_t rows, int cols, int groups,
+                          const int32_t *group_offsets, int E, float *amax,
+                          moe_stream_t stream);
+
+/*
+ * moe_fp8_padded_rows -- columns of the column-wise copy of a grouped
+ * activation with rows_cap rows: group e occupies columns [poff_e, poff_e +
+ * size_e) with poff_e the sum of the previous sizes each rounded up to 128,
+ * zeros up to the next group; the result is rows_cap + 127 E rounded up to 128.
+ */
+int64_t moe_fp8_padded_rows(int64_t rows_cap, int E);
+
+/*
+ * moe_fp8_quantize_act -- row-wise and column-wise codes of a permuted
+ * activation (rows [0, group_offsets[E]) of x), one scale from amax[0].
+ *   x        bf16 [rows_cap, ldx >= cols]; cols % 16 == 0
+ *   q        uint8 [rows_cap, ldq >= cols] out (ldq % 16 == 0); rows past
+ *            group_offsets[E] are not written
+ *   qt       uint8 [cols, ldqt >= moe_fp8_padded_rows(rows_cap, E)] out
+ *            (ldqt % 16 == 0): columns [0, poff_E) written, padding zero
+ *   scale_inv fp32 [1] out: 1 / scale
+ */
+moe_status_t moe_fp8_quantize_act(const uint16_t *x, int64_t ldx, const int32_t *group_offsets,
+                                  int E, int64_t rows_cap, int cols, int fmt, const float *amax,
+                                  uint8_t *q, int64_t ldq, uint8_t *qt, int64_t ldqt,
+                                  float *scale_inv, moe_stream_t stream);
+
+/*
+ * moe_fp8_quantize_weights -- per-expert codes of w bf16 [E, K, N]
+ * (contiguous), scale of expert e from amax[e]:
+ *   q  uint8 [E, K, N] out (row-wise), qt uint8 [E, N, K] out (transposed),
+ *   scale_inv fp32 [E] out.  K % 16 == 0, N % 16 == 0.
+ */
+moe_status_t moe_fp8_quantize_weights(const uint16_t *w, int E, int K, int N, int fmt,
+                                      const float *amax, uint8_t *q, uint8_t *qt,
+                                      float *scale_inv, moe_stream_t stream);
 
 /*
  * moe_tgmm -- weight-gradient grouped GEMM, ragged along the contraction:

@@ -76,6 +76,11 @@ _SIGS = {
     "moe_group_colsum": (_I, [_P, _I64, _P, _I, _I64, _I, _P, _I64, _P]),
     "moe_tgmm": (_I, [_P, _I64, _P, _I64, _P, _I, _I64, _I, _I, _P, _I, _I64, _I64, _I, _P, _P]),
     "moe_combine": (_I, [_P, _I64, _P, _P, _I, _I, _I, _P, _I64, _P]),
+    "moe_fp8_amax": (_I, [_P, _I64, _I64, _I, _I, _P, _I, _P, _P]),
+    "moe_fp8_padded_rows": (_I64, [_I64, _I]),
+    "moe_fp8_quantize_act": (_I, [_P, _I64, _P, _I, _I64, _I, _I, _P, _P, _I64, _P, _I64, _P,
+                                  _P]),
+    "moe_fp8_quantize_weights": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_unpermute_bwd": (_I, [_P, _I64, _P, _I64, _P, _P, _P, _P, _I, _I, _I, _I, _I64, _P,
                                _I64, _P, _P]),
 }
@@ -241,6 +246,35 @@ def moe_tgmm(A, B, group_offsets, W, accumulate=False, dev_status=None, stream=N
     _check(LIB.moe_tgmm(_ptr(A), _ld(A), _ptr(B), _ld(B), _ptr(group_offsets), E, A.shape[0], M,
                         N, _ptr(W), w_dtype, W.stride(1), W.stride(0), int(accumulate),
                         _ptr(dev_status), _stream(stream)))
+
+
+FP8_E4M3 = 0
+FP8_E5M2 = 1
+
+
+def moe_fp8_amax(x, amax, groups=1, group_offsets=None, E=0, stream=None):
+    """x bf16 2-D [rows, cols] (a [E, K, N] weight as x.view(E * K, N) with groups=E)."""
+    _check(LIB.moe_fp8_amax(_ptr(x), _ld(x), x.shape[0], x.shape[1], groups, _ptr(group_offsets),
+                            E, _ptr(amax), _stream(stream)))
+
+
+def moe_fp8_padded_rows(rows_cap: int, E: int) -> int:
+    return int(LIB.moe_fp8_padded_rows(rows_cap, E))
+
+
+def moe_fp8_quantize_act(x, group_offsets, fmt, amax, q, qt, scale_inv, stream=None):
+    """x bf16 [rows_cap, cols]; q uint8 [rows_cap, >=cols]; qt uint8 [cols, >=padded rows]."""
+    E = group_offsets.shape[0] - 1
+    _check(LIB.moe_fp8_quantize_act(_ptr(x), _ld(x), _ptr(group_offsets), E, x.shape[0],
+                                    x.shape[1], fmt, _ptr(amax), _ptr(q), _ld(q), _ptr(qt),
+                                    _ld(qt), _ptr(scale_inv), _stream(stream)))
+
+
+def moe_fp8_quantize_weights(w, fmt, amax, q, qt, scale_inv, stream=None):
+    """w bf16 [E, K, N] contiguous -> q uint8 [E, K, N], qt uint8 [E, N, K]."""
+    E, K, N = w.shape
+    _check(LIB.moe_fp8_quantize_weights(_ptr(w), E, K, N, fmt, _ptr(amax), _ptr(q), _ptr(qt),
+                                        _ptr(scale_inv), _stream(stream)))
 
 
 def moe_combine(Y, flat_to_sorted, topk_w, out, k, stream=None):

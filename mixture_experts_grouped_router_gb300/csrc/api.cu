@@ -349,6 +349,72 @@ moe_status_t moe_group_colsum(const uint16_t *G, int64_t ldg, const int32_t *gro
                      "moe_group_colsum launch");
 }
 
+moe_status_t moe_fp8_amax(const uint16_t *x, int64_t ldx, int64_t rows, int cols, int groups,
+                          const int32_t *group_offsets, int E, float *amax,
+                          moe_stream_t stream) {
+  set_error("");
+  REQUIRE(rows >= 0 && cols > 0 && groups >= 1, MOE_ERR_INVALID_ARG,
+          "moe_fp8_amax: rows=%lld cols=%d groups=%d", (long long)rows, cols, groups);
+  REQUIRE(rows % groups == 0, MOE_ERR_INVALID_ARG, "moe_fp8_amax: rows %% groups != 0");
+  REQUIRE(cols % 8 == 0 && ldx % 8 == 0 && ldx >= cols, MOE_ERR_UNSUPPORTED,
+          "moe_fp8_amax: cols and ldx must be multiples of 8, ldx >= cols");
+  REQUIRE(group_offsets == nullptr || (groups == 1 && E > 0), MOE_ERR_INVALID_ARG,
+          "moe_fp8_amax: group_offsets needs groups == 1 and E > 0");
+  REQUIRE(amax && (rows == 0 || x), MOE_ERR_INVALID_ARG, "moe_fp8_amax: null pointer");
+  REQUIRE(aligned16(x), MOE_ERR_UNSUPPORTED, "moe_fp8_amax: x must be 16-byte aligned");
+  return cuda_status(moe::launch_fp8_amax(x, ldx, rows, cols, groups, group_offsets, E, amax,
+                                          (cudaStream_t)stream),
+                     "moe_fp8_amax launch");
+}
+
+int64_t moe_fp8_padded_rows(int64_t rows_cap, int E) {
+  if (rows_cap < 0 || E <= 0) return -1;
+  return moe::f8_padded_rows(rows_cap, E);
+}
+
+moe_status_t moe_fp8_quantize_act(const uint16_t *x, int64_t ldx, const int32_t *group_offsets,
+                                  int E, int64_t rows_cap, int cols, int fmt, const float *amax,
+                                  uint8_t *q, int64_t ldq, uint8_t *qt, int64_t ldqt,
+                                  float *scale_inv, moe_stream_t stream) {
+  set_error("");
+  REQUIRE(E > 0 && E <= moe::kMaxGroups && rows_cap >= 0 && cols > 0, MOE_ERR_INVALID_ARG,
+          "moe_fp8_quantize_act: E=%d rows_cap=%lld cols=%d", E, (long long)rows_cap, cols);
+  REQUIRE(fmt == MOE_FP8_E4M3 || fmt == MOE_FP8_E5M2, MOE_ERR_INVALID_ARG,
+          "moe_fp8_quantize_act: bad fmt %d", fmt);
+  REQUIRE(cols % 16 == 0 && ldx % 8 == 0 && ldq % 16 == 0 && ldqt % 16 == 0, MOE_ERR_UNSUPPORTED,
+          "moe_fp8_quantize_act: cols, ldq, ldqt must be multiples of 16, ldx of 8");
+  REQUIRE(ldx >= cols && ldq >= cols && ldqt >= moe::f8_padded_rows(rows_cap, E),
+          MOE_ERR_INVALID_ARG, "moe_fp8_quantize_act: leading dimension too small");
+  REQUIRE(rows_cap < (1ll << 31), MOE_ERR_UNSUPPORTED, "moe_fp8_quantize_act: 2^31 rows");
+  REQUIRE(group_offsets && amax && scale_inv && (rows_cap == 0 || (x && q && qt)),
+          MOE_ERR_INVALID_ARG, "moe_fp8_quantize_act: null pointer");
+  REQUIRE(aligned16(x) && aligned16(q) && aligned16(qt), MOE_ERR_UNSUPPORTED,
+          "moe_fp8_quantize_act: x, q, qt must be 16-byte aligned");
+  return cuda_status(moe::launch_fp8_quant_act(x, ldx, group_offsets, E, rows_cap, cols, fmt,
+                                               amax, q, ldq, qt, ldqt, scale_inv,
+                                               (cudaStream_t)stream),
+                     "moe_fp8_quantize_act launch");
+}
+
+moe_status_t moe_fp8_quantize_weights(const uint16_t *w, int E, int K, int N, int fmt,
+                                      const float *amax, uint8_t *q, uint8_t *qt,
+                                      float *scale_inv, moe_stream_t stream) {
+  set_error("");
+  REQUIRE(E > 0 && E <= 65535 && K > 0 && N > 0, MOE_ERR_INVALID_ARG,
+          "moe_fp8_quantize_weights: E=%d K=%d N=%d", E, K, N);
+  REQUIRE(fmt == MOE_FP8_E4M3 || fmt == MOE_FP8_E5M2, MOE_ERR_INVALID_ARG,
+          "moe_fp8_quantize_weights: bad fmt %d", fmt);
+  REQUIRE(K % 16 == 0 && N % 16 == 0, MOE_ERR_UNSUPPORTED,
+          "moe_fp8_quantize_weights: K and N must be multiples of 16");
+  REQUIRE(w && amax && q && qt && scale_inv, MOE_ERR_INVALID_ARG,
+          "moe_fp8_quantize_weights: null pointer");
+  REQUIRE(aligned16(w) && aligned16(q) && aligned16(qt), MOE_ERR_UNSUPPORTED,
+          "moe_fp8_quantize_weights: w, q, qt must be 16-byte aligned");
+  return cuda_status(moe::launch_fp8_quant_weights(w, E, K, N, fmt, amax, q, qt, scale_inv,
+                                                   (cudaStream_t)stream),
+                     "moe_fp8_quantize_weights launch");
+}
+
 moe_status_t moe_combine(const uint16_t *Y, int64_t ldy, const int32_t *flat_to_sorted,
                          const float *topk_w, int T, int k, int d, uint16_t *out, int64_t ldo,
                          moe_stream_t stream) {

@@ -29,6 +29,20 @@ cudaError_t launch_route_topk_bwd(const float *logits, int64_t ld, const int32_t
                                   int score_fn, int renorm, float *d_logits, int64_t ld_out,
                                   cudaStream_t s);
 
+// fp8.cu
+constexpr int kF8PadRows = 128;  // group padding of column-wise FP8 copies
+constexpr int kMaxGroups = 256;
+int64_t f8_padded_rows(int64_t rows_cap, int E);
+cudaError_t launch_fp8_amax(const uint16_t *x, int64_t ldx, int64_t rows, int cols, int groups,
+                            const int32_t *offsets, int E, float *amax, cudaStream_t s);
+cudaError_t launch_fp8_quant_act(const uint16_t *x, int64_t ldx, const int32_t *offsets, int E,
+                                 int64_t rows_cap, int cols, int fmt, const float *amax,
+                                 uint8_t *q, int64_t ldq, uint8_t *qt, int64_t ldqt,
+                                 float *scale_inv, cudaStream_t s);
+cudaError_t launch_fp8_quant_weights(const uint16_t *w, int E, int K, int N, int fmt,
+                                     const float *amax, uint8_t *q, uint8_t *qt,
+                                     float *scale_inv, cudaStream_t s);
+
 // permute.cu
 size_t permute_workspace_bytes(int T, int E);
 cudaError_t launch_permute(const uint16_t *x, int64_t ldx, const int32_t *topk_idx, int T, int d,
