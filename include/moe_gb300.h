@@ -351,6 +351,43 @@ moe_status_t moe_fp8_quantize_weights(const uint16_t *w, int E, int K, int N, in
                                       float *scale_inv, moe_stream_t stream);
 
 /*
+ * moe_gmm_fp8 -- moe_gmm on 8-bit float codes (tcgen05 kind::f8f6f4, fp32
+ * accumulation), the row-wise copies of the 2x quantization:
+ *     S[r, :] = (A_q[r, :] . B_q,e^T) * a_scale_inv[0] * b_scale_inv[e]
+ * then the epilogue of moe_gmm (NONE, SWIGLU_FWD, SWIGLU_BWD; no partial sum,
+ * no bias).
+ *   A     uint8 codes [rows_cap, lda >= K] (format a_fmt), K-major
+ *   B     uint8 codes [E, N, K] K-major: row n of expert e at B + e*stride_b +
+ *         n*ldb (the transposed copy for [K, N] weights, the row-wise copy of
+ *         a [N, K] weight for dgrad); SWIGLU_FWD: rows [0, F) gate, [F, 2F) up
+ *   a_scale_inv fp32 [1], b_scale_inv fp32 [E] (device)
+ *   K, lda, ldb, stride_b multiples of 16; other arguments as moe_gmm.
+ * FP8 recipe (TE-2912, the fused up-projection; MaxText PR #2319, quantizer
+ * settings): E4M3 operands forward, E5M2 gradients backward.
+ */
+moe_status_t moe_gmm_fp8(const uint8_t *A, int64_t lda, int a_fmt, const float *a_scale_inv,
+                         const uint8_t *B, int64_t ldb, int64_t stride_b, int b_fmt,
+                         const float *b_scale_inv, const int32_t *group_offsets, int E,
+                         int64_t rows_cap, int K, int N, int epilogue, const uint16_t *aux,
+                         int64_t ld_aux, void *C, int c_dtype, int64_t ldc, uint16_t *C2,
+                         int64_t ldc2, int32_t *dev_status, moe_stream_t stream);
+
+/*
+ * moe_tgmm_fp8 -- moe_tgmm on the column-wise copies of two permuted
+ * activations (moe_fp8_quantize_act's qt):
+ *     W_e = (At_e . Bt_e^T) * a_scale_inv[0] * b_scale_inv[0]
+ * where At_e / Bt_e are columns [poff_e, poff_e+1) of At [M, ldat] and Bt
+ * [N, ldbt] (group e's rows, zero padded to a multiple of 128); an expert
+ * without rows gets zeros (or nothing when accumulating).  ldat, ldbt >=
+ * moe_fp8_padded_rows(rows_cap, E); W as moe_tgmm.
+ */
+moe_status_t moe_tgmm_fp8(const uint8_t *At, int64_t ldat, int a_fmt, const float *a_scale_inv,
+                          const uint8_t *Bt, int64_t ldbt, int b_fmt, const float *b_scale_inv,
+                          const int32_t *group_offsets, int E, int64_t rows_cap, int M, int N,
+                          void *W, int w_dtype, int64_t ldw, int64_t stride_w, int accumulate,
+                          int32_t *dev_status, moe_stream_t stream);
+
+/*
  * moe_tgmm -- weight-gradient grouped GEMM, ragged along the contraction:
  *     W_e = A_e^T . B_e   (+ W_e when accumulate),  A_e / B_e = rows of group e
  * MT-4295, Testing: "TGMM with zero-initialized empty expert groups": an

@@ -81,6 +81,10 @@ _SIGS = {
     "moe_fp8_quantize_act": (_I, [_P, _I64, _P, _I, _I64, _I, _I, _P, _P, _I64, _P, _I64, _P,
                                   _P]),
     "moe_fp8_quantize_weights": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "moe_gmm_fp8": (_I, [_P, _I64, _I, _P, _P, _I64, _I64, _I, _P, _P, _I, _I64, _I, _I, _I, _P,
+                         _I64, _P, _I, _I64, _P, _I64, _P, _P]),
+    "moe_tgmm_fp8": (_I, [_P, _I64, _I, _P, _P, _I64, _I, _P, _P, _I, _I64, _I, _I, _P, _I, _I64,
+                          _I64, _I, _P, _P]),
     "moe_unpermute_bwd": (_I, [_P, _I64, _P, _I64, _P, _P, _P, _P, _I, _I, _I, _I, _I64, _P,
                                _I64, _P, _P]),
 }
@@ -275,6 +279,30 @@ def moe_fp8_quantize_weights(w, fmt, amax, q, qt, scale_inv, stream=None):
     E, K, N = w.shape
     _check(LIB.moe_fp8_quantize_weights(_ptr(w), E, K, N, fmt, _ptr(amax), _ptr(q), _ptr(qt),
                                         _ptr(scale_inv), _stream(stream)))
+
+
+def moe_gmm_fp8(A, a_fmt, a_scale_inv, B, b_fmt, b_scale_inv, group_offsets, C,
+                epilogue=EPI_NONE, aux=None, C2=None, dev_status=None, stream=None):
+    """A uint8 codes [rows_cap, K]; B uint8 codes [E, N, K] (K-major); C bf16 or fp32."""
+    E, N, K = B.shape
+    c_dtype = DTYPE_F32 if C.dtype == torch.float32 else DTYPE_BF16
+    _check(LIB.moe_gmm_fp8(_ptr(A), _ld(A), a_fmt, _ptr(a_scale_inv), _ptr(B), B.stride(1),
+                           B.stride(0), b_fmt, _ptr(b_scale_inv), _ptr(group_offsets), E,
+                           A.shape[0], K, N, epilogue, _ptr(aux),
+                           _ld(aux) if aux is not None else 0, _ptr(C), c_dtype, _ld(C),
+                           _ptr(C2), _ld(C2) if C2 is not None else 0, _ptr(dev_status),
+                           _stream(stream)))
+
+
+def moe_tgmm_fp8(At, a_fmt, a_scale_inv, Bt, b_fmt, b_scale_inv, group_offsets, rows_cap, W,
+                 accumulate=False, dev_status=None, stream=None):
+    """At uint8 [M, >=padded rows], Bt uint8 [N, >=padded rows]; W [E, M, N] bf16 / fp32."""
+    E, M, N = W.shape
+    w_dtype = DTYPE_F32 if W.dtype == torch.float32 else DTYPE_BF16
+    _check(LIB.moe_tgmm_fp8(_ptr(At), _ld(At), a_fmt, _ptr(a_scale_inv), _ptr(Bt), _ld(Bt), b_fmt,
+                            _ptr(b_scale_inv), _ptr(group_offsets), E, rows_cap, M, N, _ptr(W),
+                            w_dtype, W.stride(1), W.stride(0), int(accumulate), _ptr(dev_status),
+                            _stream(stream)))
 
 
 def moe_combine(Y, flat_to_sorted, topk_w, out, k, stream=None):

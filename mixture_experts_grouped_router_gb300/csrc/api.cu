@@ -415,6 +415,90 @@ moe_status_t moe_fp8_quantize_weights(const uint16_t *w, int E, int K, int N, in
                      "moe_fp8_quantize_weights launch");
 }
 
+moe_status_t moe_gmm_fp8(const uint8_t *A, int64_t lda, int a_fmt, const float *a_scale_inv,
+                         const uint8_t *B, int64_t ldb, int64_t stride_b, int b_fmt,
+                         const float *b_scale_inv, const int32_t *group_offsets, int E,
+                         int64_t rows_cap, int K, int N, int epilogue, const uint16_t *aux,
+                         int64_t ld_aux, void *C, int c_dtype, int64_t ldc, uint16_t *C2,
+                         int64_t ldc2, int32_t *dev_status, moe_stream_t stream) {
+  set_error("");
+  REQUIRE(E > 0 && rows_cap >= 0 && K > 0 && N > 0, MOE_ERR_INVALID_ARG,
+          "moe_gmm_fp8: E=%d rows_cap=%lld K=%d N=%d", E, (long long)rows_cap, K, N);
+  REQUIRE(E <= 256, MOE_ERR_UNSUPPORTED, "moe_gmm_fp8: E=%d > 256", E);
+  REQUIRE((a_fmt == MOE_FP8_E4M3 || a_fmt == MOE_FP8_E5M2) &&
+              (b_fmt == MOE_FP8_E4M3 || b_fmt == MOE_FP8_E5M2),
+          MOE_ERR_INVALID_ARG, "moe_gmm_fp8: bad operand format");
+  REQUIRE(epilogue >= MOE_EPI_NONE && epilogue <= MOE_EPI_SWIGLU_BWD, MOE_ERR_INVALID_ARG,
+          "moe_gmm_fp8: bad epilogue %d", epilogue);
+  REQUIRE(c_dtype == MOE_DTYPE_BF16 || c_dtype == MOE_DTYPE_F32, MOE_ERR_INVALID_ARG,
+          "moe_gmm_fp8: bad c_dtype");
+  REQUIRE(K % 16 == 0 && lda % 16 == 0 && ldb % 16 == 0 && stride_b % 16 == 0 && N % 8 == 0,
+          MOE_ERR_UNSUPPORTED,
+          "moe_gmm_fp8: K, lda, ldb, stride_b must be multiples of 16, N of 8");
+  REQUIRE(lda >= K && ldb >= K && (E == 1 || stride_b >= (int64_t)N * ldb), MOE_ERR_INVALID_ARG,
+          "moe_gmm_fp8: leading dimension or expert stride too small");
+  REQUIRE(B && group_offsets && a_scale_inv && b_scale_inv && (rows_cap == 0 || (A && C)),
+          MOE_ERR_INVALID_ARG, "moe_gmm_fp8: null pointer");
+  REQUIRE(aligned16(A) && aligned16(B) && aligned16(C) && aligned16(C2) && aligned16(aux),
+          MOE_ERR_UNSUPPORTED, "moe_gmm_fp8: operands must be 16-byte aligned");
+  int outN = N;
+  if (epilogue == MOE_EPI_SWIGLU_FWD) {
+    REQUIRE(N % 16 == 0, MOE_ERR_UNSUPPORTED, "moe_gmm_fp8: SWIGLU_FWD needs N = 2F, F %% 8 == 0");
+    REQUIRE((C2 != nullptr || rows_cap == 0) && ldc2 >= N / 2 && ldc2 % 8 == 0,
+            MOE_ERR_INVALID_ARG, "moe_gmm_fp8: SWIGLU_FWD needs C2 with ldc2 >= F");
+    REQUIRE(c_dtype == MOE_DTYPE_BF16, MOE_ERR_INVALID_ARG, "moe_gmm_fp8: SWIGLU_FWD writes bf16");
+  }
+  if (epilogue == MOE_EPI_SWIGLU_BWD) {
+    outN = 2 * N;
+    REQUIRE((aux != nullptr || rows_cap == 0) && ld_aux >= 2 * N && ld_aux % 8 == 0,
+            MOE_ERR_INVALID_ARG, "moe_gmm_fp8: SWIGLU_BWD needs aux = H with ld_aux >= 2N");
+    REQUIRE(c_dtype == MOE_DTYPE_BF16, MOE_ERR_INVALID_ARG, "moe_gmm_fp8: SWIGLU_BWD writes bf16");
+  }
+  REQUIRE(ldc >= (epilogue == MOE_EPI_SWIGLU_FWD ? N : outN) && ldc % 8 == 0, MOE_ERR_INVALID_ARG,
+          "moe_gmm_fp8: ldc too small or not a multiple of 8");
+  REQUIRE(rows_cap < (1ll << 31), MOE_ERR_UNSUPPORTED, "moe_gmm_fp8: more than 2^31 rows");
+  if (rows_cap == 0) return MOE_OK;
+  moe::GmmF8Args a{A, lda, a_fmt, a_scale_inv, B, ldb, stride_b, b_fmt, b_scale_inv,
+                   group_offsets, E, rows_cap, K, N, epilogue, aux, ld_aux, C, c_dtype, ldc,
+                   C2, ldc2, dev_status};
+  return moe::launch_gmm_f8(a, (cudaStream_t)stream);
+}
+
+moe_status_t moe_tgmm_fp8(const uint8_t *At, int64_t ldat, int a_fmt, const float *a_scale_inv,
+                          const uint8_t *Bt, int64_t ldbt, int b_fmt, const float *b_scale_inv,
+                          const int32_t *group_offsets, int E, int64_t rows_cap, int M, int N,
+                          void *W, int w_dtype, int64_t ldw, int64_t stride_w, int accumulate,
+                          int32_t *dev_status, moe_stream_t stream) {
+  set_error("");
+  REQUIRE(E > 0 && rows_cap >= 0 && M > 0 && N > 0, MOE_ERR_INVALID_ARG,
+          "moe_tgmm_fp8: E=%d rows_cap=%lld M=%d N=%d", E, (long long)rows_cap, M, N);
+  REQUIRE(E <= 256, MOE_ERR_UNSUPPORTED, "moe_tgmm_fp8: E=%d > 256", E);
+  REQUIRE((a_fmt == MOE_FP8_E4M3 || a_fmt == MOE_FP8_E5M2) &&
+              (b_fmt == MOE_FP8_E4M3 || b_fmt == MOE_FP8_E5M2),
+          MOE_ERR_INVALID_ARG, "moe_tgmm_fp8: bad operand format");
+  REQUIRE(w_dtype == MOE_DTYPE_BF16 || w_dtype == MOE_DTYPE_F32, MOE_ERR_INVALID_ARG,
+          "moe_tgmm_fp8: bad w_dtype");
+  REQUIRE(!accumulate || w_dtype == MOE_DTYPE_F32, MOE_ERR_INVALID_ARG,
+          "moe_tgmm_fp8: accumulate needs fp32 W");
+  const int64_t P = moe::f8_padded_rows(rows_cap, E);
+  REQUIRE(P / moe::kF8PadRows < 65536, MOE_ERR_UNSUPPORTED,
+          "moe_tgmm_fp8: more than 2^16 blocks of 128 rows");
+  REQUIRE(ldat >= P && ldbt >= P && ldat % 16 == 0 && ldbt % 16 == 0, MOE_ERR_INVALID_ARG,
+          "moe_tgmm_fp8: ldat, ldbt must be >= moe_fp8_padded_rows (%lld) and multiples of 16",
+          (long long)P);
+  REQUIRE(N % 8 == 0 && ldw >= N && ldw % 8 == 0, MOE_ERR_UNSUPPORTED,
+          "moe_tgmm_fp8: N and ldw must be multiples of 8, ldw >= N");
+  REQUIRE(stride_w >= (int64_t)M * ldw || E == 1, MOE_ERR_INVALID_ARG,
+          "moe_tgmm_fp8: stride_w overlaps experts");
+  REQUIRE(At && Bt && a_scale_inv && b_scale_inv && group_offsets && W, MOE_ERR_INVALID_ARG,
+          "moe_tgmm_fp8: null pointer");
+  REQUIRE(aligned16(At) && aligned16(Bt) && aligned16(W), MOE_ERR_UNSUPPORTED,
+          "moe_tgmm_fp8: operands must be 16-byte aligned");
+  moe::TgmmF8Args a{At, ldat, a_fmt, a_scale_inv, Bt, ldbt, b_fmt, b_scale_inv, group_offsets, E,
+                    rows_cap, M, N, W, w_dtype, ldw, stride_w, accumulate, dev_status};
+  return moe::launch_tgmm_f8(a, (cudaStream_t)stream);
+}
+
 moe_status_t moe_combine(const uint16_t *Y, int64_t ldy, const int32_t *flat_to_sorted,
                          const float *topk_w, int T, int k, int d, uint16_t *out, int64_t ldo,
                          moe_stream_t stream) {

@@ -63,6 +63,15 @@ constexpr int kGroupPairs = 16;  // raster group: 16 row-tile pairs x all column
 
 constexpr int kTmemCols = 2 * BN;                 // two accumulators
 
+// Operand elements: bf16 (K blocks of 64, MMA K = 16) or 8-bit float codes
+// (K blocks of 128, MMA K = 32).  Either way a K block of one tile row is one
+// 128-byte swizzle row, so stages, boxes and descriptors keep their byte sizes.
+template <bool F8>
+struct Elem {
+  static constexpr int BKE = F8 ? 128 : 64;
+  static constexpr int UKE = F8 ? 32 : 16;
+};
+
 enum { KIND_GMM = 0, KIND_TGMM = 1 };
 
 struct Book {
@@ -76,6 +85,9 @@ struct Book {
   int abort_flag;
   int total_tiles;
   int cum[kMaxE + 1];            // per-expert tile prefix
+  // FP8 weight gradients: start of each expert's zero-padded K range, in K
+  // blocks (rows / 128; the column-wise copies hold < 2^16 blocks)
+  uint16_t poff[kMaxE + 1];
 };
 constexpr int STG_OFFSET = 4 * STAGE_BYTES;  // = 6 x 32 KB; 1024-aligned
 
@@ -121,6 +133,10 @@ struct TcParams {
   int32_t *dev_status;
   uint64_t wait_limit_ns;  // bound of every wait before the CTA gives up
   int stall_loads;         // test hook: the producer issues no loads
+  // FP8: 1 / scale of A (one) and of B (one per expert), operand formats
+  const float *a_sinv;
+  const float *b_sinv;
+  int a_fmt, b_fmt;
 };
 
 struct TileInfo {
@@ -135,7 +151,7 @@ MOE_DEVINL int group_offset(const TcParams &p, int e) {
 // Tiles are handed out in pairs: the two CTAs of a cluster take row tiles
 // 2*pm and 2*pm + 1 of the same expert and column tile (the second one may lie
 // past the expert's rows; it then runs through the pipeline and stores nothing).
-template <int KIND>
+template <int KIND, bool F8>
 MOE_DEVINL TileInfo decode_tile(const Book &bk, const TcParams &p, int t, int crank) {
   int lo = 0, hi = p.E - 1;
   while (lo < hi) {
@@ -157,11 +173,18 @@ MOE_DEVINL TileInfo decode_tile(const Book &bk, const TcParams &p, int t, int cr
   const int gm = min(kGroupPairs, mp - g * kGroupPairs);
   ti.n_idx = within / gm;
   ti.m_idx = 2 * (g * kGroupPairs + (within - ti.n_idx * gm)) + crank;
+  constexpr int BKE = Elem<F8>::BKE;
   if (KIND == KIND_GMM) {
     ti.row0 += ti.m_idx * BM;
-    ti.kblocks = (p.K + BK - 1) / BK;
+    ti.kblocks = (p.K + BKE - 1) / BKE;
+  } else if (F8) {
+    // FP8 weight gradients read the column-wise copies, where expert e's rows
+    // fill whole K blocks from poff[e] on (zero padded)
+    ti.row0 = (int)bk.poff[lo] * BKE;
+    ti.row_end = (int)bk.poff[lo + 1] * BKE;
+    ti.kblocks = (int)bk.poff[lo + 1] - (int)bk.poff[lo];
   } else {
-    ti.kblocks = (size + BK - 1) / BK;
+    ti.kblocks = (size + BKE - 1) / BKE;
   }
   return ti;
 }
@@ -284,9 +307,11 @@ MOE_DEVINL void issue_aux_load(OutMaps &om, uint8_t *stg, int nc, int wrow0) {
 
 // One tile's epilogue for the ragged-M GEMM.  Warp q owns tile rows
 // [32q, 32q+32), thread = one row; 32-column chunks.
-template <int EPI>
+template <int EPI, bool F8>
 MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t taddr, int q,
                              int lane, uint8_t *stg, OutMaps &om, volatile int *abort_flag) {
+  // FP8: the accumulator holds code products; dequantize with both scales
+  const float sc = F8 ? __ldg(p.a_sinv) * __ldg(p.b_sinv + ti.e) : 1.0f;
   const int wrow0 = ti.row0 + q * 32;
   const int64_t row = (int64_t)wrow0 + lane;
   const bool valid = row < ti.row_end;
@@ -315,6 +340,13 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
       float g[32], u[32], act[32];
       tc::tmem_ld32(taddr + c * 32, g);
       tc::tmem_ld32(taddr + BN / 2 + c * 32, u);
+      if (F8) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          g[j] *= sc;
+          u[j] *= sc;
+        }
+      }
       if (has_ps) {
         const float *fg = reinterpret_cast<const float *>(pg);
         const float *fu = reinterpret_cast<const float *>(pu);
@@ -398,6 +430,10 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
       }
       float v[32];
       tc::tmem_ld32(taddr + c * 32, v);
+      if (F8) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] *= sc;
+      }
       float dg[32], du[32];
 #pragma unroll
       for (int k = 0; k < 32; ++k) {
@@ -449,6 +485,10 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
       if (has_in && c + 1 < BN / 32 && nc + 32 < N) load_chunk(c + 1, nxt);
       float v[32];
       tc::tmem_ld32(taddr + c * 32, v);
+      if (F8) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] *= sc;
+      }
       if (has_in) {
         const float *pv = reinterpret_cast<const float *>(cur);
 #pragma unroll
@@ -494,8 +534,10 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
 // tgmm epilogue: warp q owns output rows m in [m_idx*128 + 32q, +32) of W_e.
 // `zero`: the expert had no rows, so TMEM is not read.  Bulk stores, or bulk
 // fp32 reduce-adds into W when accumulating; the box is clipped at M and N.
+template <bool F8>
 MOE_DEVINL void epilogue_tgmm(const TcParams &p, const TileInfo &ti, uint32_t taddr, int q,
                               int lane, uint8_t *stg, const OutMaps &om, bool zero) {
+  const float sc = F8 && !zero ? __ldg(p.a_sinv) * __ldg(p.b_sinv) : 1.0f;
   const int wm0 = ti.m_idx * BM + q * 32;
   const int n0 = ti.n_idx * BN;
 #pragma unroll 1
@@ -508,6 +550,10 @@ MOE_DEVINL void epilogue_tgmm(const TcParams &p, const TileInfo &ti, uint32_t ta
       for (int j = 0; j < 32; ++j) v[j] = 0.f;
     } else {
       tc::tmem_ld32(taddr + c * 32, v);
+      if (F8) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] *= sc;
+      }
     }
     stage_acquire(lane);
     if (p.c_f32) stage_f32(stg, lane, v);
@@ -522,7 +568,7 @@ MOE_DEVINL void epilogue_tgmm(const TcParams &p, const TileInfo &ti, uint32_t ta
 }
 
 // ------------------------------------------------------------------ kernel
-template <int KIND, bool B_MN, int EPI>
+template <int KIND, bool B_MN, int EPI, bool F8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1,
@@ -541,6 +587,8 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   constexpr bool k2SM = Ring<KIND, EPI>::two_sm;
   constexpr int kSt = Ring<KIND, EPI>::stages;
   constexpr int kStageB = Ring<KIND, EPI>::stage_bytes;
+  constexpr int BKE = Elem<F8>::BKE;
+  constexpr bool A_MN = KIND == KIND_TGMM && !F8;  // bf16 weight gradients read A as stored
   const bool leader = crank == 0;
 
   if (threadIdx.x == 0) {
@@ -567,27 +615,38 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   }
   __syncthreads();
   if (warp == 0) {
-    // per-expert tile counts and their exclusive scan (warp shuffles)
-    int carry = 0;
+    // per-expert tile counts and their exclusive scan (warp shuffles); FP8
+    // weight gradients also scan the sizes rounded up to whole K blocks
+    int carry = 0, pcarry = 0;
     for (int c0 = 0; c0 < p.E; c0 += 32) {
       const int e = c0 + lane;
-      int tiles = 0;
+      int tiles = 0, padded = 0;
       if (e < p.E) {
         const int size = max(group_offset(p, e + 1) - group_offset(p, e), 0);
         const int mt = KIND == KIND_GMM ? (size + BM - 1) / BM : p.m_tiles;
         tiles = (mt + 1) / 2 * p.n_tiles;
+        padded = (size + BKE - 1) / BKE;
       }
-      int incl = tiles;
+      int incl = tiles, pincl = padded;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
+        const int py = __shfl_up_sync(0xffffffffu, pincl, o);
+        if (lane >= o) {
+          incl += y;
+          pincl += py;
+        }
       }
-      if (e < p.E) bk.cum[e] = carry + incl - tiles;
+      if (e < p.E) {
+        bk.cum[e] = carry + incl - tiles;
+        bk.poff[e] = (uint16_t)(pcarry + pincl - padded);
+      }
       carry += __shfl_sync(0xffffffffu, incl, 31);
+      pcarry += __shfl_sync(0xffffffffu, pincl, 31);
     }
     if (lane == 0) {
       bk.cum[p.E] = carry;
+      bk.poff[p.E] = (uint16_t)pcarry;
       bk.total_tiles = carry;
     }
     // offsets must be non-decreasing; clamp a bad table to empty groups
@@ -614,7 +673,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   if (warp == 0) {
     if (lane == 0 && !p.stall_loads) {
       for (int t = cid; t < total; t += ncl) {
-        const TileInfo ti = decode_tile<KIND>(bk, p, t, crank);
+        const TileInfo ti = decode_tile<KIND, F8>(bk, p, t, crank);
         bool ok = true;
         for (int kb = 0; kb < ti.kblocks; ++kb) {
           const int s = issued % kSt;
@@ -631,7 +690,13 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             // expects the whole pair's stage
             const uint32_t fbl = tc::mapa_shared(tc::smem_u32(fb), 0);
             if (leader) tc::mbar_expect_tx(fb, 2 * kStageB);
-            if (KIND == KIND_TGMM) {
+            if (KIND == KIND_TGMM && F8) {
+              // K-major column-wise copies: this CTA's 128 rows of A^T (output
+              // rows) and of B^T (its half of the 256 output columns)
+              const int k = ti.row0 + kb * BKE;
+              tc::tma_load_2d_2sm(sa, &tmA, fbl, k, ti.m_idx * BM);
+              tc::tma_load_2d_2sm(sb, &tmB, fbl, k, ti.n_idx * BN + crank * (BN / 2));
+            } else if (KIND == KIND_TGMM) {
               // this CTA's 128 output rows of A (two 64-column boxes) and its
               // 128 columns of B, both over the K block's 64 rows
               const int r = ti.row0 + kb * BK;
@@ -642,7 +707,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
               tc::tma_load_2d_2sm(sb, &tmB, fbl, nb, r);
               tc::tma_load_2d_2sm(sb + BOX_BYTES, &tmB, fbl, nb + 64, r);
             } else {
-            tc::tma_load_2d_2sm(sa, &tmA, fbl, kb * BK, ti.row0);
+            tc::tma_load_2d_2sm(sa, &tmA, fbl, kb * BKE, ti.row0);
             if (B_MN) {
               // this CTA's 128 columns of B: two 64-column boxes
               const int n0 = EPI == MOE_EPI_SWIGLU_FWD ? ti.n_idx * (BN / 2) : ti.n_idx * BN;
@@ -652,24 +717,29 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                 const int x = EPI == MOE_EPI_SWIGLU_FWD
                                   ? (i < 2 ? n0 + 64 * i : p.F + n0 + 64 * (i - 2))
                                   : n0 + 64 * i;
-                tc::tma_load_3d_2sm(sb + j * BOX_BYTES, &tmB, fbl, x, kb * BK, ti.e);
+                tc::tma_load_3d_2sm(sb + j * BOX_BYTES, &tmB, fbl, x, kb * BKE, ti.e);
               }
             } else {
-              tc::tma_load_3d_2sm(sb, &tmB, fbl, kb * BK, ti.n_idx * BN + crank * (BN / 2), ti.e);
+              // K-major B: this CTA's 128 of the tile's 256 columns (SwiGLU
+              // forward: gate columns in the first CTA, up columns in the second)
+              const int nrow = EPI == MOE_EPI_SWIGLU_FWD
+                                   ? (crank == 0 ? 0 : p.F) + ti.n_idx * (BN / 2)
+                                   : ti.n_idx * BN + crank * (BN / 2);
+              tc::tma_load_3d_2sm(sb, &tmB, fbl, kb * BKE, nrow, ti.e);
             }
             }
           } else {
             tc::mbar_expect_tx(fb, kStageB);
             // own A tile; this CTA's half of the shared B tile, multicast to the pair
             if (KIND == KIND_GMM) {
-              tc::tma_load_2d(sa, &tmA, fb, kb * BK, ti.row0);
+              tc::tma_load_2d(sa, &tmA, fb, kb * BKE, ti.row0);
               if (B_MN) {
                 const int n0 = ti.n_idx * BN;
 #pragma unroll
                 for (int i = 2 * crank; i < 2 * crank + 2; ++i)
-                  tc::tma_load_3d_mc(sb + i * BOX_BYTES, &tmB, fb, n0 + 64 * i, kb * BK, ti.e, kPair);
+                  tc::tma_load_3d_mc(sb + i * BOX_BYTES, &tmB, fb, n0 + 64 * i, kb * BKE, ti.e, kPair);
               } else {
-                tc::tma_load_3d_mc(sb + crank * (B_BYTES / 2), &tmB, fb, kb * BK,
+                tc::tma_load_3d_mc(sb + crank * (B_BYTES / 2), &tmB, fb, kb * BKE,
                                    ti.n_idx * BN + crank * (BN / 2), ti.e, kPair);
               }
             } else {
@@ -695,11 +765,12 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
           tc::mbar_wait_drain(&bk.full[i % kSt], (i / kSt) & 1, p.wait_limit_ns / 4);
     }
   } else if (warp == 1 && (!k2SM || leader)) {
-    constexpr uint32_t IDESC = tc::idesc_bf16(k2SM ? 2 * BM : BM, BN, KIND == KIND_TGMM, B_MN);
+    const uint32_t IDESC = F8 ? tc::idesc_f8(k2SM ? 2 * BM : BM, BN, p.a_fmt, p.b_fmt)
+                              : tc::idesc_bf16(k2SM ? 2 * BM : BM, BN, A_MN, B_MN);
     uint32_t it = 0, acc_it = 0;
     bool ok = true;
     for (int t = cid; t < total && ok; t += ncl) {
-      const TileInfo ti = decode_tile<KIND>(bk, p, t, crank);
+      const TileInfo ti = decode_tile<KIND, F8>(bk, p, t, crank);
       if (ti.kblocks == 0) continue;
       const uint32_t a = acc_it & 1;
       const uint32_t aph = (acc_it >> 1) & 1;
@@ -716,7 +787,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         tc::tc_fence_after();
         uint8_t *sa = smem + s * kStageB;
         uint8_t *sb = sa + A_BYTES;
-        if (KIND == KIND_TGMM) {
+        if (KIND == KIND_TGMM && !F8) {
           // rows past the expert's last row belong to the next expert: zero
           // them in both operands (one 128-byte row per K index per box).
           // 2-SM: this CTA's four boxes and the same four in the partner
@@ -745,12 +816,19 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
           const uint32_t b_base = tc::smem_u32(sb);
 #pragma unroll
           for (int kk = 0; kk < BK / UK; ++kk) {
-            const uint64_t ad = KIND == KIND_TGMM ? tc::sdesc(a_base + kk * UK * 128, BOX_BYTES, 1024)
-                                                  : tc::sdesc(a_base + kk * UK * 2, 16, 1024);
+            // K-major: the kk-th MMA starts 32 bytes further along the row
+            // (16 bf16 or 32 codes); MN-major: 16 rows of 128 bytes further
+            const uint64_t ad = A_MN ? tc::sdesc(a_base + kk * UK * 128, BOX_BYTES, 1024)
+                                     : tc::sdesc(a_base + kk * 32, 16, 1024);
             const uint64_t bd = B_MN ? tc::sdesc(b_base + kk * UK * 128, BOX_BYTES, 1024)
-                                     : tc::sdesc(b_base + kk * UK * 2, 16, 1024);
-            if (k2SM) tc::umma_bf16_2sm(d_tmem, ad, bd, IDESC, (kb | kk) != 0);
-            else tc::umma_bf16(d_tmem, ad, bd, IDESC, (kb | kk) != 0);
+                                     : tc::sdesc(b_base + kk * 32, 16, 1024);
+            if (F8) {
+              if (k2SM) tc::umma_f8_2sm(d_tmem, ad, bd, IDESC, (kb | kk) != 0);
+              else tc::umma_f8(d_tmem, ad, bd, IDESC, (kb | kk) != 0);
+            } else {
+              if (k2SM) tc::umma_bf16_2sm(d_tmem, ad, bd, IDESC, (kb | kk) != 0);
+              else tc::umma_bf16(d_tmem, ad, bd, IDESC, (kb | kk) != 0);
+            }
           }
           // release the stage in both CTAs
           if (k2SM) tc::umma_commit_2sm_mc(&bk.empty[s], kPair);
@@ -781,9 +859,9 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     OutMaps om{&tmC0, &tmC1, &tmC2, &tmC3, &bk.aux_full[warp - 2], 0u, 0u};
     uint32_t acc_it = 0;
     for (int t = cid; t < total; t += ncl) {
-      const TileInfo ti = decode_tile<KIND>(bk, p, t, crank);
+      const TileInfo ti = decode_tile<KIND, F8>(bk, p, t, crank);
       if (KIND == KIND_TGMM && ti.kblocks == 0) {
-        if (!p.accumulate) epilogue_tgmm(p, ti, 0, q, lane, stg, om, true);
+        if (!p.accumulate) epilogue_tgmm<F8>(p, ti, 0, q, lane, stg, om, true);
         continue;
       }
       epilogue_prefetch<KIND, EPI>(p, ti, rit);
@@ -795,9 +873,9 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       tc::tc_fence_after();
       const uint32_t taddr = tmem + a * BN + (static_cast<uint32_t>(q * 32) << 16);
       if (KIND == KIND_GMM)
-        epilogue_gmm<EPI>(p, ti, taddr, q, lane, stg, om, abort_flag);
+        epilogue_gmm<EPI, F8>(p, ti, taddr, q, lane, stg, om, abort_flag);
       else
-        epilogue_tgmm(p, ti, taddr, q, lane, stg, om, false);
+        epilogue_tgmm<F8>(p, ti, taddr, q, lane, stg, om, false);
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -871,14 +949,14 @@ bool make_out_map(CUtensorMap *m, const void *base, bool f32, int64_t cols, int6
                   f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-template <int KIND, bool B_MN, int EPI>
+template <int KIND, bool B_MN, int EPI, bool F8 = false>
 moe_status_t launch_tc(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap *mc,
                        const TcParams &p, int64_t tiles_upper, cudaStream_t s) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   static int max_clusters = 0;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gmm_tc_kernel<KIND, B_MN, EPI>,
+    attr_err = cudaFuncSetAttribute(gmm_tc_kernel<KIND, B_MN, EPI, F8>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (attr_err != cudaSuccess) return;
     // clusters of two CTAs (one per SM) that can be resident at once
@@ -886,7 +964,7 @@ moe_status_t launch_tc(const CUtensorMap &ma, const CUtensorMap &mb, const CUten
     cfg.gridDim = dim3(2 * (unsigned)num_sms());
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = SMEM_BYTES;
-    if (cudaOccupancyMaxActiveClusters(&max_clusters, gmm_tc_kernel<KIND, B_MN, EPI>, &cfg) !=
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, gmm_tc_kernel<KIND, B_MN, EPI, F8>, &cfg) !=
             cudaSuccess ||
         max_clusters <= 0) {
       cudaGetLastError();
@@ -900,8 +978,8 @@ moe_status_t launch_tc(const CUtensorMap &ma, const CUtensorMap &mb, const CUten
   }
   const int64_t pairs = (tiles_upper + 1) / 2;
   const int grid = 2 * (int)std::max<int64_t>(1, std::min<int64_t>(max_clusters, pairs));
-  gmm_tc_kernel<KIND, B_MN, EPI><<<grid, kThreads, SMEM_BYTES, s>>>(ma, mb, mc[0], mc[1], mc[2],
-                                                                    mc[3], p);
+  gmm_tc_kernel<KIND, B_MN, EPI, F8><<<grid, kThreads, SMEM_BYTES, s>>>(ma, mb, mc[0], mc[1],
+                                                                        mc[2], mc[3], p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_error("grouped GEMM launch: %s", cudaGetErrorString(e));
@@ -1072,6 +1150,164 @@ moe_status_t launch_tgmm(const TgmmArgs &a, cudaStream_t s) {
   }
   const int64_t tiles_upper = (int64_t)a.E * p.m_tiles * p.n_tiles;
   return launch_tc<KIND_TGMM, true, MOE_EPI_NONE>(ma, mb, mc, p, tiles_upper, s);
+}
+
+// Output maps shared by the bf16 and FP8 ragged-M GEMMs (unused slots repeat
+// the first).
+static bool gmm_out_maps(CUtensorMap *mc, int epilogue, void *C, int c_dtype, int64_t ldc,
+                         uint16_t *C2, int64_t ldc2, const uint16_t *aux, int64_t ld_aux, int N,
+                         int F, int64_t rows_cap) {
+  const bool f32 = c_dtype == MOE_DTYPE_F32;
+  if (epilogue == MOE_EPI_SWIGLU_FWD) {
+    const uint16_t *H = static_cast<const uint16_t *>(C);
+    if (!make_out_map(&mc[0], H, false, F, rows_cap, ldc) ||
+        !make_out_map(&mc[1], H + F, false, F, rows_cap, ldc) ||
+        !make_out_map(&mc[2], C2, false, F, rows_cap, ldc2))
+      return false;
+    mc[3] = mc[0];
+    return true;
+  }
+  if (epilogue == MOE_EPI_SWIGLU_BWD) {
+    const uint16_t *dH = static_cast<const uint16_t *>(C);
+    return make_out_map(&mc[0], dH, false, N, rows_cap, ldc) &&
+           make_out_map(&mc[1], dH + N, false, N, rows_cap, ldc) &&
+           make_out_map(&mc[2], aux, false, N, rows_cap, ld_aux) &&
+           make_out_map(&mc[3], aux + N, false, N, rows_cap, ld_aux);
+  }
+  if (!make_out_map(&mc[0], C, f32, N, rows_cap, ldc)) return false;
+  mc[1] = mc[2] = mc[3] = mc[0];
+  return true;
+}
+
+moe_status_t launch_gmm_f8(const GmmF8Args &a, cudaStream_t s) {
+  if (a.E > kMaxE) {
+    set_error("moe_gmm_fp8: E=%d > %d", a.E, kMaxE);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  const int64_t stride_b = a.E > 1 ? a.stride_b : (int64_t)a.N * a.ldb;
+  CUtensorMap ma, mb;
+  {
+    const uint64_t dims[2] = {(uint64_t)a.K, (uint64_t)a.rows_cap};
+    const uint64_t st[1] = {(uint64_t)a.lda};
+    const uint32_t box[2] = {Elem<true>::BKE, BM};
+    if (!make_map(&ma, a.A, 2, dims, st, box, CU_TENSOR_MAP_DATA_TYPE_UINT8)) {
+      set_error("moe_gmm_fp8: cannot encode the TMA descriptor of A");
+      return MOE_ERR_CUDA;
+    }
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)a.K, (uint64_t)a.N, (uint64_t)a.E};
+    const uint64_t st[2] = {(uint64_t)a.ldb, (uint64_t)stride_b};
+    const uint32_t box[3] = {Elem<true>::BKE, BN / 2, 1};
+    if (!make_map(&mb, a.B, 3, dims, st, box, CU_TENSOR_MAP_DATA_TYPE_UINT8)) {
+      set_error("moe_gmm_fp8: cannot encode the TMA descriptor of B");
+      return MOE_ERR_CUDA;
+    }
+  }
+  TcParams p{};
+  p.E = a.E;
+  p.rows_cap = (int)a.rows_cap;
+  p.K = a.K;
+  p.N = a.N;
+  p.F = a.epilogue == MOE_EPI_SWIGLU_FWD ? a.N / 2 : a.N;
+  p.n_tiles = a.epilogue == MOE_EPI_SWIGLU_FWD ? (p.F + BN / 2 - 1) / (BN / 2) : (a.N + BN - 1) / BN;
+  p.offsets = a.offsets;
+  p.C = a.C;
+  p.ldc = a.ldc;
+  p.c_f32 = a.c_dtype == MOE_DTYPE_F32;
+  p.C2 = a.C2;
+  p.ldc2 = a.ldc2;
+  p.aux = a.aux;
+  p.ld_aux = a.ld_aux;
+  p.dev_status = a.dev_status;
+  p.wait_limit_ns = wait_limit_ns();
+  p.stall_loads = test_stall_loads();
+  p.a_sinv = a.a_sinv;
+  p.b_sinv = a.b_sinv;
+  p.a_fmt = a.a_fmt;
+  p.b_fmt = a.b_fmt;
+  CUtensorMap mc[4];
+  if (!gmm_out_maps(mc, a.epilogue, a.C, a.c_dtype, a.ldc, a.C2, a.ldc2, a.aux, a.ld_aux, a.N,
+                    p.F, a.rows_cap)) {
+    set_error("moe_gmm_fp8: cannot encode the TMA descriptor of the output");
+    return MOE_ERR_CUDA;
+  }
+  const int64_t tiles_upper = ((a.rows_cap + BM - 1) / BM + a.E) * p.n_tiles;
+  switch (a.epilogue) {
+    case MOE_EPI_NONE:
+      return launch_tc<KIND_GMM, false, MOE_EPI_NONE, true>(ma, mb, mc, p, tiles_upper, s);
+    case MOE_EPI_SWIGLU_FWD:
+      return launch_tc<KIND_GMM, false, MOE_EPI_SWIGLU_FWD, true>(ma, mb, mc, p, tiles_upper, s);
+    case MOE_EPI_SWIGLU_BWD:
+      return launch_tc<KIND_GMM, false, MOE_EPI_SWIGLU_BWD, true>(ma, mb, mc, p, tiles_upper, s);
+    default:
+      set_error("moe_gmm_fp8: unsupported epilogue");
+      return MOE_ERR_UNSUPPORTED;
+  }
+}
+
+moe_status_t launch_tgmm_f8(const TgmmF8Args &a, cudaStream_t s) {
+  if (a.E > kMaxE) {
+    set_error("moe_tgmm_fp8: E=%d > %d", a.E, kMaxE);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  const int64_t P = f8_padded_rows(a.rows_cap, a.E);  // columns the copies may use
+  CUtensorMap ma, mb;
+  const uint32_t box[2] = {Elem<true>::BKE, BM};
+  {
+    const uint64_t dims[2] = {(uint64_t)P, (uint64_t)a.M};
+    const uint64_t st[1] = {(uint64_t)a.ldat};
+    if (!make_map(&ma, a.At, 2, dims, st, box, CU_TENSOR_MAP_DATA_TYPE_UINT8)) {
+      set_error("moe_tgmm_fp8: cannot encode the TMA descriptor of A");
+      return MOE_ERR_CUDA;
+    }
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)P, (uint64_t)a.N};
+    const uint64_t st[1] = {(uint64_t)a.ldbt};
+    if (!make_map(&mb, a.Bt, 2, dims, st, box, CU_TENSOR_MAP_DATA_TYPE_UINT8)) {
+      set_error("moe_tgmm_fp8: cannot encode the TMA descriptor of B");
+      return MOE_ERR_CUDA;
+    }
+  }
+  TcParams p{};
+  p.E = a.E;
+  p.rows_cap = (int)a.rows_cap;
+  p.M = a.M;
+  p.N = a.N;
+  p.m_tiles = (a.M + BM - 1) / BM;
+  p.n_tiles = (a.N + BN - 1) / BN;
+  p.offsets = a.offsets;
+  p.C = a.W;
+  p.ldc = a.ldw;
+  p.c_f32 = a.w_dtype == MOE_DTYPE_F32;
+  p.stride_w = a.stride_w;
+  p.accumulate = a.accumulate;
+  p.dev_status = a.dev_status;
+  p.wait_limit_ns = wait_limit_ns();
+  p.stall_loads = test_stall_loads();
+  p.a_sinv = a.a_sinv;
+  p.b_sinv = a.b_sinv;
+  p.a_fmt = a.a_fmt;
+  p.b_fmt = a.b_fmt;
+  CUtensorMap mc[4];
+  {
+    const bool f32 = a.w_dtype == MOE_DTYPE_F32;
+    const int64_t es = f32 ? 4 : 2;
+    const int64_t stride_w = a.E > 1 ? a.stride_w : (int64_t)a.M * a.ldw;
+    const uint64_t dims[3] = {(uint64_t)a.N, (uint64_t)a.M, (uint64_t)a.E};
+    const uint64_t st[2] = {(uint64_t)(a.ldw * es), (uint64_t)(stride_w * es)};
+    const uint32_t wbox[3] = {32, 32, 1};
+    if (!make_map(&mc[0], a.W, 3, dims, st, wbox,
+                  f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                  f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B)) {
+      set_error("moe_tgmm_fp8: cannot encode the TMA descriptor of W");
+      return MOE_ERR_CUDA;
+    }
+    mc[1] = mc[2] = mc[3] = mc[0];
+  }
+  const int64_t tiles_upper = (int64_t)a.E * p.m_tiles * p.n_tiles;
+  return launch_tc<KIND_TGMM, false, MOE_EPI_NONE, true>(ma, mb, mc, p, tiles_upper, s);
 }
 
 }  // namespace moe

@@ -88,4 +88,27 @@ struct TgmmArgs {
 };
 moe_status_t launch_tgmm(const TgmmArgs &a, cudaStream_t s);
 
+// FP8 (8-bit float codes, K-major operands, fp32 accumulation; the epilogue
+// multiplies by the scales' inverses)
+struct GmmF8Args {
+  const uint8_t *A; int64_t lda; int a_fmt; const float *a_sinv;
+  const uint8_t *B; int64_t ldb; int64_t stride_b; int b_fmt; const float *b_sinv;
+  const int32_t *offsets; int E; int64_t rows_cap; int K; int N;
+  int epilogue;
+  const uint16_t *aux; int64_t ld_aux;
+  void *C; int c_dtype; int64_t ldc;
+  uint16_t *C2; int64_t ldc2;
+  int32_t *dev_status;
+};
+moe_status_t launch_gmm_f8(const GmmF8Args &a, cudaStream_t s);
+
+struct TgmmF8Args {
+  const uint8_t *At; int64_t ldat; int a_fmt; const float *a_sinv;
+  const uint8_t *Bt; int64_t ldbt; int b_fmt; const float *b_sinv;
+  const int32_t *offsets; int E; int64_t rows_cap; int M; int N;
+  void *W; int w_dtype; int64_t ldw; int64_t stride_w; int accumulate;
+  int32_t *dev_status;
+};
+moe_status_t launch_tgmm_f8(const TgmmF8Args &a, cudaStream_t s);
+
 }  // namespace moe

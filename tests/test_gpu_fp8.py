@@ -105,3 +105,143 @@ def test_quantize_act_padded_transpose(sizes, cols, fmt):
         assert (seg[:, :b - a] == want[a:b].T).all(), e
         assert (seg[:, b - a:] == 0).all(), e
     assert (qtn[:, po[-1]:] == 0xAB).all()
+
+
+# ---------------------------------------------------------------------------
+# FP8 grouped GEMMs: both sides quantize the same bf16 inputs (codes are
+# bit-exact, see above); the oracle multiplies the dequantized values in fp64
+# ---------------------------------------------------------------------------
+from gpu_helpers import assert_close  # noqa: E402
+from oracle import moe_ref  # noqa: E402
+
+SIZES = {"mixed": [0, 7, 300, 128, 129, 0, 1, 640], "one": [517], "tiny": [1, 2, 3],
+         "empty_tail": [256, 0, 0]}
+
+
+def _act_gpu(x_bits, off, fmt):
+    """GPU quantization of a permuted activation; oracle dequantized values."""
+    E = len(off) - 1
+    x = dev_bf16(x_bits)
+    offd = torch.from_numpy(off).cuda()
+    rows_cap, cols = x.shape
+    amax = torch.empty(1, device="cuda")
+    L.moe_fp8_amax(x, amax, group_offsets=offd, E=E)
+    q = torch.zeros(rows_cap, cols, dtype=torch.uint8, device="cuda")
+    pr = L.moe_fp8_padded_rows(rows_cap, E)
+    qt = torch.zeros(cols, pr, dtype=torch.uint8, device="cuda")
+    sinv = torch.empty(1, device="cuda")
+    L.moe_fp8_quantize_act(x, offd, fmt, amax, q, qt, sinv)
+    R = int(off[-1])
+    xf = _f32(x_bits[:R])
+    s = q8.current_scale(np.abs(xf).max() if R else 0.0, FMTS[fmt])
+    deq = q8.dequantize(q8.quantize(xf, s, FMTS[fmt]), s, FMTS[fmt])
+    return q, qt, sinv, deq
+
+
+def _w_gpu(w_bits, fmt):
+    E, K, N = w_bits.shape
+    w = dev_bf16(w_bits)
+    amax = torch.empty(E, device="cuda")
+    L.moe_fp8_amax(w.view(E * K, N), amax, groups=E)
+    q = torch.empty(E, K, N, dtype=torch.uint8, device="cuda")
+    qt = torch.empty(E, N, K, dtype=torch.uint8, device="cuda")
+    sinv = torch.empty(E, device="cuda")
+    L.moe_fp8_quantize_weights(w, fmt, amax, q, qt, sinv)
+    deq = np.stack([q8.qdq_tensor(_f32(w_bits[e]), FMTS[fmt])[0] for e in range(E)])
+    return q, qt, sinv, deq
+
+
+# sizes of quantized operands are multiples of 16 (codes move in 16-byte rows)
+GMM8_CASES = [("mixed", 256, 384), ("one", 1024, 144), ("tiny", 128, 64), ("empty_tail", 512, 1024),
+              ("mixed", 4096, 256)]
+SAME_FMT = [(0, 0)]
+MIXED_FMT = [(1, 0)]
+
+
+@pytest.mark.parametrize("case", GMM8_CASES)
+@pytest.mark.parametrize("fmts", SAME_FMT + MIXED_FMT)
+@pytest.mark.parametrize("transposed_weight", [False, True])
+def test_gmm_fp8_none(case, fmts, transposed_weight):
+    sz, K, N = case
+    fa, fb = fmts
+    rng = np.random.default_rng(K + N + 10 * fa + fb)
+    off = _offsets(SIZES[sz])
+    E, R = len(SIZES[sz]), int(off[-1])
+    rows_cap = R + 19
+    a_q, _, a_sinv, a_deq = _act_gpu(_bf(rng, (rows_cap, K), 2.0), off, fa)
+    if transposed_weight:   # dgrad: weight stored [E, N, K], used as is
+        w_bits = _bf(rng, (E, N, K), 0.05)
+        w_q, _, b_sinv, w_deq = _w_gpu(w_bits, fb)
+        b_op, w_ref, tr = w_q, w_deq, True
+    else:                   # forward: weight stored [E, K, N], its transposed copy
+        w_bits = _bf(rng, (E, K, N), 0.05)
+        _, w_qt, b_sinv, w_deq = _w_gpu(w_bits, fb)
+        b_op, w_ref, tr = w_qt, w_deq, False
+    C = torch.full((rows_cap, N), 7.0, dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    L.moe_gmm_fp8(a_q, fa, a_sinv, b_op, fb, b_sinv, torch.from_numpy(off).cuda(), C,
+                  dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    want = moe_ref.gmm(a_deq, w_ref, off, transpose_rhs=tr)
+    assert_close("gmm_fp8", C[:R], want)
+    assert (C[R:].float() == 7.0).all()
+
+
+@pytest.mark.parametrize("sz,K,F", [("mixed", 256, 192), ("one", 512, 200), ("tiny", 128, 64)])
+def test_gmm_fp8_swiglu_fwd(sz, K, F):
+    rng = np.random.default_rng(K + F)
+    off = _offsets(SIZES[sz])
+    E, R = len(SIZES[sz]), int(off[-1])
+    rows_cap = R + 5
+    a_q, _, a_sinv, a_deq = _act_gpu(_bf(rng, (rows_cap, K), 2.0), off, 0)
+    _, w_qt, b_sinv, w_deq = _w_gpu(_bf(rng, (E, K, 2 * F), 0.05), 0)
+    H = torch.empty(rows_cap, 2 * F, dtype=torch.bfloat16, device="cuda")
+    Act = torch.empty(rows_cap, F, dtype=torch.bfloat16, device="cuda")
+    L.moe_gmm_fp8(a_q, 0, a_sinv, w_qt, 0, b_sinv, torch.from_numpy(off).cuda(), H,
+                  L.EPI_SWIGLU_FWD, C2=Act)
+    torch.cuda.synchronize()
+    h = moe_ref.gmm(a_deq, w_deq, off)
+    assert_close("H", H[:R], h)
+    assert_close("Act", Act[:R], moe_ref.swiglu(h))
+
+
+@pytest.mark.parametrize("sz,K,F", [("mixed", 256, 192), ("one", 512, 208), ("tiny", 128, 64)])
+@pytest.mark.parametrize("fmts", SAME_FMT + MIXED_FMT)
+def test_gmm_fp8_swiglu_bwd(sz, K, F, fmts):
+    fa, fb = fmts
+    rng = np.random.default_rng(K * F + fa)
+    off = _offsets(SIZES[sz])
+    E, R = len(SIZES[sz]), int(off[-1])
+    rows_cap = R + 5
+    a_q, _, a_sinv, a_deq = _act_gpu(_bf(rng, (rows_cap, K), 1.0), off, fa)
+    w_q, _, b_sinv, w_deq = _w_gpu(_bf(rng, (E, F, K), 0.05), fb)      # wo [E, F, d]
+    h_bits = _bf(rng, (rows_cap, 2 * F), 2.0)
+    dH = torch.empty(rows_cap, 2 * F, dtype=torch.bfloat16, device="cuda")
+    L.moe_gmm_fp8(a_q, fa, a_sinv, w_q, fb, b_sinv, torch.from_numpy(off).cuda(), dH,
+                  L.EPI_SWIGLU_BWD, aux=dev_bf16(h_bits))
+    torch.cuda.synchronize()
+    d_act = moe_ref.gmm(a_deq, w_deq, off, transpose_rhs=True)
+    want = moe_ref.swiglu_bwd(moe_synth.bits_to_f64(h_bits)[:R], d_act)
+    assert_close("dH", dH[:R], want)
+
+
+@pytest.mark.parametrize("sz,M,N", [("mixed", 256, 384), ("one", 144, 208), ("tiny", 64, 64),
+                                    ("empty_tail", 128, 528)])
+@pytest.mark.parametrize("fmts", SAME_FMT + MIXED_FMT)
+@pytest.mark.parametrize("w_f32", [False, True])
+def test_tgmm_fp8(sz, M, N, fmts, w_f32):
+    fa, fb = fmts
+    rng = np.random.default_rng(M + N + fa + 3 * w_f32)
+    off = _offsets(SIZES[sz])
+    E, R = len(SIZES[sz]), int(off[-1])
+    rows_cap = R + 11
+    _, a_qt, a_sinv, a_deq = _act_gpu(_bf(rng, (rows_cap, M), 1.0), off, fa)
+    _, b_qt, b_sinv, b_deq = _act_gpu(_bf(rng, (rows_cap, N), 1.0), off, fb)
+    W = torch.full((E, M, N), 5.0, dtype=torch.float32 if w_f32 else torch.bfloat16, device="cuda")
+    L.moe_tgmm_fp8(a_qt, fa, a_sinv, b_qt, fb, b_sinv, torch.from_numpy(off).cuda(), rows_cap, W)
+    torch.cuda.synchronize()
+    want = moe_ref.tgmm(a_deq, b_deq, off, E)
+    assert_close("W", W, want)
+    for e in np.nonzero(np.diff(off) == 0)[0]:
+        assert (W[e].float() == 0).all()
