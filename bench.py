@@ -165,6 +165,9 @@ class ClockSampler:
 def algorithmic_bytes(cfg, m_kept, R, t_kept):
     T, d, k, f, E = cfg.T, cfg.d, cfg.k, cfg.f, cfg.E
     return {
+        # FP8: amax read + quantize read (bf16) + row-wise and column-wise codes
+        "quant_x": 6 * R * d, "quant_act": 6 * R * f, "quant_dy": 6 * R * d,
+        "quant_dh": 6 * R * 2 * f, "quant_wi": 6 * E * d * 2 * f, "quant_wo": 6 * E * f * d,
         "colsum_dbo": R * d * 2 + E * d * 4,
         "colsum_dbi": R * 2 * f * 2 + E * 2 * f * 4,
         "permute": (t_kept + R) * d * 2 + 8 * T * k + 4 * R,
@@ -213,7 +216,8 @@ def run_ours(args, cfg, ws, rank, local):
     dout = bf16(inp["dout"]).to(dev)
     logits = torch.from_numpy(inp["logits"]).to(dev)
     shape = layer.LayerShape(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.score_fn, cfg.renorm,
-                             cfg.align, cfg.capacity, cfg.num_chunks, args.bias)
+                             cfg.align, cfg.capacity, cfg.num_chunks, args.bias,
+                             fp8=args.fp8)
     b = layer.MoEBuffers(shape, device=dev)
     stream = torch.cuda.current_stream(dev)
     bi = bo = None
@@ -369,17 +373,20 @@ def run_ours(args, cfg, ws, rank, local):
     gemm_names = [n for n in kernels if n in fl]
     dom = max(gemm_names, key=lambda n: kernels[n]["share"])
     peak_t = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+    if args.fp8:   # measured bf16 peak x the nominal dense fp8 / bf16 ratio (4.5 / 2.25)
+        peak_t *= 2.0
     traffic = None
     tp = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tp):
         tj = json.load(open(tp))
         ent = tj.get(cfg.name, {}).get(dom)
-        if ent and ent.get("source_hash") == gemm_source_hash() and not args.bias:
+        if ent and ent.get("source_hash") == gemm_source_hash() and not args.bias \
+                and not args.fp8:
             traffic = ent["dram_bytes_per_launch"]
     roofline = {"bound": "tensor", "kernel": dom, "achieved": kernels[dom]["tflops"],
                 "peak": peak_t, "unit": "TFLOP/s", "frac": kernels[dom]["tflops"] / peak_t,
-                "traffic": traffic, "peak_kind": "%s sustained bf16 (burst %.1f)"
-                % (pk_kind, pk["bf16_tflops"]),
+                "traffic": traffic, "peak_kind": "%s sustained bf16 (burst %.1f)%s"
+                % (pk_kind, pk["bf16_tflops"], " x 2 (nominal fp8 / bf16)" if args.fp8 else ""),
                 "algorithmic_per_launch": fl[dom], "algorithmic_unit": "FLOP"}
     gemm_ms = sum(kernels[n]["avg_ms"] * kernels[n]["launches_per_step"] for n in gemm_names)
     mem = {}
@@ -390,13 +397,14 @@ def run_ours(args, cfg, ws, rank, local):
     out = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "tokens_per_s": tokens_s,
         "n_gpus": ws, "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8 (e4m3 forward, e5m2 gradients), fp32 accumulation" if args.fp8 else "bf16",
         "data": "synthetic (seeded N(0,1) activations / N(0,0.02) weights, rank-seeded)",
         "config": {"workload": cfg.name, "T": cfg.T, "d_model": cfg.d, "d_ff": cfg.f,
                    "experts": cfg.E, "top_k": cfg.k,
                    "score": "sigmoid" if cfg.score_fn else "softmax", "renorm": cfg.renorm,
                    "align": cfg.align, "capacity": cfg.capacity, "num_chunks": cfg.num_chunks,
-                   "mlp_bias": bool(args.bias),
+                   "mlp_bias": bool(args.bias), "fp8": bool(args.fp8),
                    "m_kept": m_kept, "rows": R, "empty_experts": empty,
                    "gemm_tflop_per_step": flops_step / 1e12,
                    "l2": "inputs larger than L2 (weights %.2f GB)" % ((inp["wi"].nbytes +
@@ -461,6 +469,8 @@ def main():
                     choices=sorted(moe_synth.CONFIGS) + sorted(moe_synth.PROFILE_CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fp8", action="store_true",
+                    help="FP8 expert GEMMs with current tensor scaling")
     ap.add_argument("--bias", action="store_true",
                     help="expert FFN with biases (bi on [gate | up], bo on the output)")
     args = ap.parse_args()

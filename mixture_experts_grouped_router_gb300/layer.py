@@ -17,6 +17,12 @@ best expert groups compete) and, with aux_coeff > 0, the auxiliary
 load-balancing loss (forward: b.aux_loss; backward: its logit gradient is
 added to b.d_logits).
 
+With fp8=True the four GEMMs run on 8-bit float codes with current tensor
+scaling (MaxText PR #2319, "[Draft] Integrate TE/JAX GroupedGEMM for MoE",
+review thread on the quantizer settings): Xs, Act, wi, wo in E4M3 (weights
+one scale per expert), dY and dH in E5M2, each quantized to a row-wise copy
+and a column-wise copy (the latter feeds the weight-gradient GEMMs).
+
 With bias=True the expert FFN carries biases (bi [E, 2f] on [gate | up],
 bo [E, d] on the output), added in the GEMM epilogues; their gradients are
 per-expert column sums of dH and dY (moe_group_colsum).
@@ -51,6 +57,7 @@ class LayerShape:
     num_groups: int = 0
     topk_group: int = 0
     aux_coeff: float = 0.0
+    fp8: bool = False
 
 
 class MoEBuffers:
@@ -90,6 +97,27 @@ class MoEBuffers:
         self.dbi = torch.empty(E, 2 * f, dtype=f32, device=dev) if s.bias else None
         self.dbo = torch.empty(E, d, dtype=f32, device=dev) if s.bias else None
         self.dev_status = torch.zeros(1, dtype=i32, device=dev)
+        if s.fp8:
+            if s.bias or s.num_chunks > 1:
+                raise ValueError("the FP8 layer takes neither biases nor K-chunks")
+            u8 = torch.uint8
+            P = L.moe_fp8_padded_rows(R, E)
+            self.f8_P = P
+            self.xs_q = torch.empty(R, d, dtype=u8, device=dev)
+            self.xs_qt = torch.empty(d, P, dtype=u8, device=dev)
+            self.act_q = torch.empty(R, f, dtype=u8, device=dev)
+            self.act_qt = torch.empty(f, P, dtype=u8, device=dev)
+            self.dy_q = torch.empty(R, d, dtype=u8, device=dev)
+            self.dy_qt = torch.empty(d, P, dtype=u8, device=dev)
+            self.dh_q = torch.empty(R, 2 * f, dtype=u8, device=dev)
+            self.dh_qt = torch.empty(2 * f, P, dtype=u8, device=dev)
+            self.wi_q = torch.empty(E, d, 2 * f, dtype=u8, device=dev)
+            self.wi_qt = torch.empty(E, 2 * f, d, dtype=u8, device=dev)
+            self.wo_q = torch.empty(E, f, d, dtype=u8, device=dev)
+            self.wo_qt = torch.empty(E, d, f, dtype=u8, device=dev)
+            # amax / 1 / scale per quantized tensor: x, act, dy, dh (one each), wi, wo (E each)
+            self.f8_amax = torch.empty(4 + 2 * E, dtype=f32, device=dev)
+            self.f8_sinv = torch.empty(4 + 2 * E, dtype=f32, device=dev)
         if s.aux_coeff:
             self.aux_counts = torch.empty(E, dtype=i32, device=dev)
             self.aux_probs = torch.empty(E, dtype=f32, device=dev)
@@ -100,6 +128,62 @@ class MoEBuffers:
 
 def _noop(_name):
     pass
+
+
+def _fp8_slots(b):
+    """(amax, 1/scale) views per quantized tensor."""
+    E = b.s.E
+    a, v = b.f8_amax, b.f8_sinv
+    return dict(x=(a[0:1], v[0:1]), act=(a[1:2], v[1:2]), dy=(a[2:3], v[2:3]),
+                dh=(a[3:4], v[3:4]), wi=(a[4:4 + E], v[4:4 + E]),
+                wo=(a[4 + E:4 + 2 * E], v[4 + E:4 + 2 * E]))
+
+
+def _quant_act(b, name, x, fmt, q, qt, stream, mark):
+    amax, sinv = _fp8_slots(b)[name]
+    L.moe_fp8_amax(x, amax, group_offsets=b.group_offsets, E=b.s.E, stream=stream)
+    L.moe_fp8_quantize_act(x, b.group_offsets, fmt, amax, q, qt, sinv, stream)
+    mark("quant_" + name)
+
+
+def _forward_fp8(b, x, logits, wi, wo, stream, mark):
+    s = b.s
+    E = s.E
+    sl = _fp8_slots(b)
+    _quant_act(b, "x", b.xs, L.FP8_E4M3, b.xs_q, b.xs_qt, stream, mark)
+    for name, w, q, qt in (("wi", wi, b.wi_q, b.wi_qt), ("wo", wo, b.wo_q, b.wo_qt)):
+        amax, sinv = sl[name]
+        L.moe_fp8_amax(w.view(E * w.shape[1], w.shape[2]), amax, groups=E, stream=stream)
+        L.moe_fp8_quantize_weights(w, L.FP8_E4M3, amax, q, qt, sinv, stream)
+        mark("quant_" + name)
+    L.moe_gmm_fp8(b.xs_q, L.FP8_E4M3, sl["x"][1], b.wi_qt, L.FP8_E4M3, sl["wi"][1],
+                  b.group_offsets, b.h, L.EPI_SWIGLU_FWD, C2=b.act, dev_status=b.dev_status,
+                  stream=stream)
+    mark("gmm_up_swiglu")
+    _quant_act(b, "act", b.act, L.FP8_E4M3, b.act_q, b.act_qt, stream, mark)
+    L.moe_gmm_fp8(b.act_q, L.FP8_E4M3, sl["act"][1], b.wo_qt, L.FP8_E4M3, sl["wo"][1],
+                  b.group_offsets, b.y, dev_status=b.dev_status, stream=stream)
+    mark("gmm_down")
+
+
+def _backward_fp8(b, stream, mark):
+    s = b.s
+    sl = _fp8_slots(b)
+    _quant_act(b, "dy", b.dy, L.FP8_E5M2, b.dy_q, b.dy_qt, stream, mark)
+    L.moe_gmm_fp8(b.dy_q, L.FP8_E5M2, sl["dy"][1], b.wo_q, L.FP8_E4M3, sl["wo"][1],
+                  b.group_offsets, b.dh, L.EPI_SWIGLU_BWD, aux=b.h, dev_status=b.dev_status,
+                  stream=stream)
+    mark("gmm_dgrad_down_swiglu_bwd")
+    L.moe_tgmm_fp8(b.act_qt, L.FP8_E4M3, sl["act"][1], b.dy_qt, L.FP8_E5M2, sl["dy"][1],
+                   b.group_offsets, b.rows_cap, b.dwo, dev_status=b.dev_status, stream=stream)
+    mark("tgmm_dwo")
+    _quant_act(b, "dh", b.dh, L.FP8_E5M2, b.dh_q, b.dh_qt, stream, mark)
+    L.moe_gmm_fp8(b.dh_q, L.FP8_E5M2, sl["dh"][1], b.wi_q, L.FP8_E4M3, sl["wi"][1],
+                  b.group_offsets, b.dxs, dev_status=b.dev_status, stream=stream)
+    mark("gmm_dgrad_up")
+    L.moe_tgmm_fp8(b.xs_qt, L.FP8_E4M3, sl["x"][1], b.dh_qt, L.FP8_E5M2, sl["dh"][1],
+                   b.group_offsets, b.rows_cap, b.dwi, dev_status=b.dev_status, stream=stream)
+    mark("tgmm_dwi")
 
 
 def forward(b: MoEBuffers, x, logits, wi, wo, stream=None, mark=_noop, bi=None, bo=None):
@@ -122,6 +206,11 @@ def forward(b: MoEBuffers, x, logits, wi, wo, stream=None, mark=_noop, bi=None, 
     L.moe_permute(x, b.topk_idx, s.E, s.align, s.capacity, b.xs, b.group_sizes, b.kept_counts,
                   b.group_offsets, b.s2f, b.f2s, b.ws, b.dev_status, stream)
     mark("permute")
+    if s.fp8:
+        _forward_fp8(b, x, logits, wi, wo, stream, mark)
+        L.moe_combine(b.y, b.f2s, b.topk_w, b.out, s.k, stream)
+        mark("combine")
+        return b.out
     if s.num_chunks <= 1:
         L.moe_gmm(b.xs, wi, 0, b.group_offsets, b.h, L.EPI_SWIGLU_FWD, C2=b.act,
                   dev_status=b.dev_status, stream=stream, bias=bi)
@@ -163,6 +252,11 @@ def backward(b: MoEBuffers, dout, wi, wo, stream=None, mark=_noop):
         L.moe_aux_loss_bwd(b.logits, b.aux_counts, s.k, s.score_fn, s.aux_coeff, b.d_logits,
                            d_loss=1.0, accumulate=True, stream=stream)
         mark("aux_loss_bwd")
+    if s.fp8:
+        _backward_fp8(b, stream, mark)
+        L.moe_combine(b.dxs, b.f2s, None, b.dx, s.k, stream)
+        mark("dispatch_bwd")
+        return b.dx, b.dwi, b.dwo, b.d_topk_w
     # dAct = dY . wo^T, fused with the SwiGLU backward into dH = [dgate | dup]
     L.moe_gmm(b.dy, wo, 1, b.group_offsets, b.dh, L.EPI_SWIGLU_BWD, aux=b.h,
               dev_status=b.dev_status, stream=stream)
@@ -203,6 +297,9 @@ def kernels_per_step(s: LayerShape) -> int:
     aux = bool(s.aux_coeff)
     fwd = 1 + 3 + up + 1 + 1 + (2 if aux and s.T > 0 else 1 if aux else 0)
     bwd = 1 + 1 + 1 + 1 + 2 * up + 1 + (2 if s.bias else 0) + (1 if aux and s.T > 0 else 0)
+    if s.fp8:   # amax + quantize for x, wi, wo, act (forward) and dy, dh (backward)
+        fwd += 8
+        bwd += 4
     return fwd + bwd
 
 

@@ -27,7 +27,11 @@ Readings (the pages name the recipe, not its arithmetic):
     one per expert; gradients dY and dH are quantized to E5M2 per tensor;
   * quantization points: Xs, Act (forward inputs of the two GEMMs), wi, wo
     (per expert), dY and dH (backward inputs); every GEMM accumulates the
-    dequantized products exactly (fp64 here, fp32 on the GPU).
+    dequantized products exactly (fp64 here, fp32 on the GPU);
+  * the quantized activations are the layer's bf16 tensors (the pages train
+    in bf16): Act, dY and dH are rounded to bf16 (round-to-nearest-even)
+    before their amax and codes are taken, and the SwiGLU backward reads the
+    stored bf16 H.
 """
 from __future__ import annotations
 
@@ -39,6 +43,15 @@ E4M3 = "e4m3"
 E5M2 = "e5m2"
 _FMT = {E4M3: dict(ebits=4, mbits=3, bias=7, max=448.0),
         E5M2: dict(ebits=5, mbits=2, bias=15, max=57344.0)}
+
+
+def round_bf16(x) -> np.ndarray:
+    """Round to bf16 (nearest, ties to even) through fp32; returns float64."""
+    f = np.asarray(x, dtype=np.float64).astype(np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    out = u.astype(np.uint32).view(np.float32).astype(np.float64)
+    return np.where(np.isnan(f), np.nan, out)
 
 
 def fp8_max(fmt: str) -> float:
@@ -142,7 +155,7 @@ def forward(x, logits, wi, wo, k, score_fn, renorm, align=0, capacity=0):
     wi_q, _, s_wi = qdq_per_expert(wi, E4M3)
     wo_q, _, s_wo = qdq_per_expert(wo, E4M3)
     h = moe_ref.gmm(xs_q, wi_q, off)
-    act = moe_ref.swiglu(h)
+    act = round_bf16(moe_ref.swiglu(h))
     act_q, _, s_act = qdq_tensor(act, E4M3)
     y = moe_ref.gmm(act_q, wo_q, off)
     out = moe_ref.combine(y, lay["flat_to_sorted"], topk_w)
@@ -161,9 +174,10 @@ def backward(fw: dict, d_out, k):
     T = d_out.shape[0]
     R = lay["R"]
     dy, d_topk_w = moe_ref.combine_bwd(d_out, fw["y"], lay["flat_to_sorted"], fw["topk_w"], R)
+    dy = round_bf16(dy)
     dy_q, _, s_dy = qdq_tensor(dy, E5M2)
     d_act = moe_ref.gmm(dy_q, fw["wo_q"], off, transpose_rhs=True)
-    dh = moe_ref.swiglu_bwd(fw["h"], d_act)
+    dh = round_bf16(moe_ref.swiglu_bwd(round_bf16(fw["h"]), d_act))
     d_wo = moe_ref.tgmm(fw["act_q"], dy_q, off, E)
     dh_q, _, s_dh = qdq_tensor(dh, E5M2)
     d_xs = moe_ref.gmm(dh_q, fw["wi_q"], off, transpose_rhs=True)

@@ -7,13 +7,16 @@ The recipe is the pages' configuration of the expert GEMMs (MaxText PR #2319,
 "[Draft] Integrate TE/JAX GroupedGEMM for MoE", review thread on the quantizer
 settings: current tensor scaling, float8_e4m3fn forward, float8_e5m2
 backward, row- and column-wise copies)."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
 
 import moe_synth
-from gpu_helpers import dev_bf16
+from gpu_helpers import assert_close, dev_bf16, layer_shape
 from oracle import moe_fp8_ref as q8
+from oracle import moe_ref
 
 pytestmark = pytest.mark.gpu
 L = pytest.importorskip("mixture_experts_grouped_router_gb300._lib")
@@ -111,8 +114,6 @@ def test_quantize_act_padded_transpose(sizes, cols, fmt):
 # FP8 grouped GEMMs: both sides quantize the same bf16 inputs (codes are
 # bit-exact, see above); the oracle multiplies the dequantized values in fp64
 # ---------------------------------------------------------------------------
-from gpu_helpers import assert_close  # noqa: E402
-from oracle import moe_ref  # noqa: E402
 
 SIZES = {"mixed": [0, 7, 300, 128, 129, 0, 1, 640], "one": [517], "tiny": [1, 2, 3],
          "empty_tail": [256, 0, 0]}
@@ -245,3 +246,64 @@ def test_tgmm_fp8(sz, M, N, fmts, w_f32):
     assert_close("W", W, want)
     for e in np.nonzero(np.diff(off) == 0)[0]:
         assert (W[e].float() == 0).all()
+
+
+# ---------------------------------------------------------------------------
+# the FP8 layer against the FP8 oracle
+# ---------------------------------------------------------------------------
+C = moe_synth.CONFIGS
+FP8_LAYERS = {
+    "mixtral": moe_synth.scaled(C["mixtral"], T=1024, d=256, f=448),
+    "dsv3": moe_synth.scaled(C["dsv3"], T=512, d=448, f=256),
+    "skewed": moe_synth.scaled(C["skewed"], T=4096, d=256, f=128, capacity=64),
+    "odd": moe_synth.MoEConfig("odd", T=999, d=208, f=144, E=7, k=3, score_fn=1, renorm=0,
+                               align=16, capacity=300),
+}
+
+
+def _rel(a, b):
+    a = a.detach().float().cpu().numpy().astype(np.float64) if isinstance(a, torch.Tensor) else a
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
+
+
+@pytest.mark.parametrize("name", list(FP8_LAYERS))
+def test_layer_fp8(name):
+    """The GPU follows the FP8 recipe: every output is within 1e-2 (relative
+    Frobenius) of the FP8 oracle and at most half as far from it as the FP8
+    oracle is from the unquantized layer.  Both sides quantize the same bf16
+    tensors; the residual is fp32 against fp64 accumulation, which now and then
+    moves a bf16 rounding and with it one code."""
+    from mixture_experts_grouped_router_gb300 import layer
+    cfg = FP8_LAYERS[name]
+    inp = moe_synth.make_inputs(cfg, seed=4)
+    f64 = moe_synth.bits_to_f64
+    x, wi, wo, dout = (dev_bf16(inp[n]) for n in ("x", "wi", "wo", "dout"))
+    logits = torch.from_numpy(inp["logits"]).cuda()
+    shape = dataclasses.replace(layer_shape(cfg), fp8=True)
+    b = layer.MoEBuffers(shape)
+    layer.forward(b, x, logits, wi, wo)
+    layer.backward(b, dout, wi, wo)
+    torch.cuda.synchronize()
+    assert int(b.dev_status.item()) == 0
+    xs, wis, wos, douts = (f64(inp[n]) for n in ("x", "wi", "wo", "dout"))
+    f8 = q8.forward(xs, inp["logits"], wis, wos, cfg.k, cfg.score_fn, cfg.renorm, cfg.align,
+                    cfg.capacity)
+    b8 = q8.backward(f8, douts, cfg.k)
+    fr = moe_ref.forward(xs, inp["logits"], wis, wos, cfg.k, cfg.score_fn, cfg.renorm, cfg.align,
+                         cfg.capacity)
+    br = moe_ref.backward(fr, douts, wis, wos, cfg.k)
+    assert (b.topk_idx.cpu().numpy() == f8["topk_idx"]).all()
+    # the forward input of the up-projection is quantized from identical bf16 rows: exact codes
+    R = f8["layout"]["R"]
+    assert (b.xs_q[:R].cpu().numpy() ==
+            q8.quantize(f8["xs"][:R].astype(np.float32), f8["scales"]["x"], "e4m3")).all()
+    errs = {}
+    for key, got, want8, want16 in (
+            ("h", b.h[:R], f8["h"], fr["h"]), ("act", b.act[:R], f8["act"], fr["act"]),
+            ("out", b.out, f8["out"], fr["out"]), ("dy", b.dy[:R], b8["dy"], br["dy"]),
+            ("dh", b.dh[:R], b8["dh"], br["dh"]), ("dx", b.dx, b8["dx"], br["dx"]),
+            ("dwi", b.dwi, b8["d_wi"], br["d_wi"]), ("dwo", b.dwo, b8["d_wo"], br["d_wo"]),
+            ("d_topk_w", b.d_topk_w, b8["d_topk_w"], br["d_topk_w"])):
+        errs[key] = (_rel(got, want8), _rel(want8, want16))
+    bad = {k: v for k, v in errs.items() if not (v[0] <= 1e-2 and v[0] <= 0.5 * v[1])}
+    assert not bad, errs

@@ -107,9 +107,21 @@ def _layer_inputs(seed, T=40, d=16, f=24, E=5):
     return logits, x, wi, wo, dout
 
 
+def test_round_bf16_matches_torch():
+    rng = np.random.default_rng(5)
+    x = np.concatenate([rng.standard_normal(50000) * 10.0 ** rng.uniform(-30, 30, 50000),
+                        [0.0, -0.0, 1.0, 3.0e38, -1e-40, np.inf, -np.inf]])
+    x32 = x.astype(np.float32)
+    want = torch.from_numpy(x32).to(torch.bfloat16).to(torch.float64).numpy()
+    got = q8.round_bf16(x32)
+    assert ((got == want) | (np.isnan(got) & np.isnan(want))).all()
+
+
 def test_without_quantization_fp8_layer_is_bf16_layer(monkeypatch):
-    """Identity quantizers: the FP8 forward / backward reduce exactly to the
-    bf16 oracle's (same operands in every GEMM, same transposes)."""
+    """Identity quantizers and no bf16 rounding: the FP8 forward / backward
+    reduce exactly to the bf16 oracle's (same operands in every GEMM, same
+    transposes)."""
+    monkeypatch.setattr(q8, "round_bf16", lambda x: np.asarray(x, np.float64))
     monkeypatch.setattr(q8, "qdq_tensor", lambda x, fmt: (np.asarray(x, np.float64), None, 1.0))
     monkeypatch.setattr(q8, "qdq_per_expert", lambda w, fmt: (np.asarray(w, np.float64), None,
                                                                np.ones(w.shape[0])))
