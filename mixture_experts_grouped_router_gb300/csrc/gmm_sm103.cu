@@ -51,8 +51,7 @@ namespace {
 
 constexpr int BM = 128, BN = 256, BK = 64, UK = 16;
 constexpr int kStages = 6;  // ring slots allocated (the weight-gradient kernel uses 4)
-constexpr int kThreads = 192;  // producer, MMA, 4 epilogue warps
-constexpr int kEpiWarps = 4;
+constexpr int kMaxEpiWarps = 8;
 constexpr int kStgBytes = 8192;  // per epilogue warp: up to four 32x32 bf16 blocks (or two fp32)
 constexpr int A_BYTES = BM * BK * 2;   // 16 KB
 constexpr int B_BYTES = BN * BK * 2;   // 32 KB
@@ -80,7 +79,7 @@ struct Book {
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
-  uint64_t aux_full[kEpiWarps];  // SwiGLU backward: H blocks landed in a warp's staging
+  uint64_t aux_full[kMaxEpiWarps];  // SwiGLU backward: H blocks landed in a warp's staging
   uint32_t tmem_base;
   int abort_flag;
   int total_tiles;
@@ -89,23 +88,29 @@ struct Book {
   // blocks (rows / 128; the column-wise copies hold < 2^16 blocks)
   uint16_t poff[kMaxE + 1];
 };
-constexpr int STG_OFFSET = 4 * STAGE_BYTES;  // = 6 x 32 KB; 1024-aligned
 
-// Per-kernel ring.  The forward, dgrad and weight-gradient GEMMs run as 2-SM
-// MMAs whose stage holds this CTA's 128-row (tgmm: 128-column) A tile and
-// half of the B tile (32 KB, 6 stages).  The SwiGLU-backward dgrad (measured
-// faster this way) keeps whole B tiles multicast within the pair (48 KB,
-// 4 stages).
+// Per-kernel layout.  The forward, dgrad and weight-gradient GEMMs run as
+// 2-SM MMAs whose stage holds this CTA's 128-row (tgmm: 128-column) A tile
+// and half of the B tile (32 KB, 6 stages), with 4 epilogue warps.  The
+// SwiGLU-backward dgrad, whose epilogue (H reads, two outputs) is longer than
+// its mainloop, keeps whole B tiles multicast within the pair (48 KB stages)
+// and runs 8 epilogue warps (two per TMEM lane quarter, each on half of the
+// tile's columns) in exchange for one stage.
 template <int KIND, int EPI>
 struct Ring {
   static constexpr bool two_sm = KIND == 1 || EPI != MOE_EPI_SWIGLU_BWD;
-  static constexpr int stages = two_sm ? 6 : 4;
+  static constexpr int epi_warps = two_sm ? 4 : 8;
+  static constexpr int stages = two_sm ? 6 : 3;
   static constexpr int b_bytes = two_sm ? B_BYTES / 2 : B_BYTES;
   static constexpr int stage_bytes = A_BYTES + b_bytes;
+  static constexpr int threads = 64 + 32 * epi_warps;  // producer, MMA, epilogue
+  static constexpr int stg_offset = stages * stage_bytes;  // 1024-aligned
+  static constexpr int book_offset = stg_offset + epi_warps * kStgBytes;
+  static constexpr int smem_bytes =
+      1024 + book_offset + (int)((sizeof(Book) + 127) / 128 * 128);
+  static_assert(stg_offset % 1024 == 0, "staging alignment");
+  static_assert(smem_bytes <= 232448, "shared memory budget of one CTA");
 };
-constexpr int BOOK_OFFSET = STG_OFFSET + kEpiWarps * kStgBytes;
-constexpr int SMEM_BYTES = 1024 + BOOK_OFFSET + (int)((sizeof(Book) + 127) / 128 * 128);
-static_assert(SMEM_BYTES <= 232448, "shared memory budget of one CTA");
 
 struct TcParams {
   int E;
@@ -258,14 +263,15 @@ struct OutMaps {
 // (SwiGLU-backward H, partial sums) into L2 so that the epilogue's loads do
 // not wait on HBM one after another.  Thread = one output row.
 template <int KIND, int EPI>
-MOE_DEVINL void epilogue_prefetch(const TcParams &p, const TileInfo &ti, int rit) {
+MOE_DEVINL void epilogue_prefetch(const TcParams &p, const TileInfo &ti, int rit, int c_begin,
+                                  int c_end) {
   if (KIND == KIND_GMM) {
     const int64_t row = (int64_t)ti.row0 + rit;
     if (row >= ti.row_end) return;
     if (EPI == MOE_EPI_SWIGLU_BWD) {
       const uint16_t *h = p.aux + row * p.ld_aux;
-      const int n0 = ti.n_idx * BN;
-      for (int n = n0; n < min(n0 + BN, p.N); n += 64) {
+      const int n0 = ti.n_idx * BN + c_begin * 32;
+      for (int n = n0; n < min(ti.n_idx * BN + c_end * 32, p.N); n += 64) {
         prefetch_l2(h + n);
         prefetch_l2(h + p.N + n);
       }
@@ -307,9 +313,11 @@ MOE_DEVINL void issue_aux_load(OutMaps &om, uint8_t *stg, int nc, int wrow0) {
 
 // One tile's epilogue for the ragged-M GEMM.  Warp q owns tile rows
 // [32q, 32q+32), thread = one row; 32-column chunks.
+// Chunks [c_begin, c_end) of the tile's 32-column chunks are this warp's.
 template <int EPI, bool F8>
 MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t taddr, int q,
-                             int lane, uint8_t *stg, OutMaps &om, volatile int *abort_flag) {
+                             int lane, uint8_t *stg, OutMaps &om, volatile int *abort_flag,
+                             int c_begin, int c_end) {
   // FP8: the accumulator holds code products; dequantize with both scales
   const float sc = F8 ? __ldg(p.a_sinv) * __ldg(p.b_sinv + ti.e) : 1.0f;
   const int wrow0 = ti.row0 + q * 32;
@@ -331,12 +339,12 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
       }
     };
     uint4 pg[8], pu[8], ng[8], nu[8];
-    if (has_ps) load_ps(0, pg, pu);
+    if (has_ps) load_ps(c_begin, pg, pu);
 #pragma unroll 1
-    for (int c = 0; c < BN / 2 / 32; ++c) {
+    for (int c = c_begin; c < min(c_end, BN / 2 / 32); ++c) {
       const int nc = n0 + c * 32;
       if (nc >= F) break;
-      if (has_ps && c + 1 < BN / 2 / 32 && nc + 32 < F) load_ps(c + 1, ng, nu);
+      if (has_ps && c + 1 < min(c_end, BN / 2 / 32) && nc + 32 < F) load_ps(c + 1, ng, nu);
       float g[32], u[32], act[32];
       tc::tmem_ld32(taddr + c * 32, g);
       tc::tmem_ld32(taddr + BN / 2 + c * 32, u);
@@ -410,7 +418,7 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
     const uint8_t *aux_g = stg + 4096;
     const uint8_t *aux_u = stg + 6144;
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    for (int c = c_begin; c < c_end; ++c) {
       const int nc = n0 + c * 32;
       if (nc >= N) break;
       // this chunk's H blocks (issued one chunk ahead) -> registers
@@ -424,7 +432,7 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
         bf16x8_to_f32(*reinterpret_cast<const uint4 *>(aux_u + off), u + 8 * cc);
       }
       __syncwarp();
-      if (lane == 0 && c + 1 < BN / 32 && nc + 32 < N) {
+      if (lane == 0 && c + 1 < c_end && nc + 32 < N) {
         tc::fence_proxy_async_smem();
         issue_aux_load(om, stg, nc + 32, wrow0);
       }
@@ -477,12 +485,12 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
       }
     };
     uint4 cur[8], nxt[8];
-    if (has_in) load_chunk(0, cur);
+    if (has_in) load_chunk(c_begin, cur);
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    for (int c = c_begin; c < c_end; ++c) {
       const int nc = n0 + c * 32;
       if (nc >= N) break;
-      if (has_in && c + 1 < BN / 32 && nc + 32 < N) load_chunk(c + 1, nxt);
+      if (has_in && c + 1 < c_end && nc + 32 < N) load_chunk(c + 1, nxt);
       float v[32];
       tc::tmem_ld32(taddr + c * 32, v);
       if (F8) {
@@ -569,7 +577,7 @@ MOE_DEVINL void epilogue_tgmm(const TcParams &p, const TileInfo &ti, uint32_t ta
 
 // ------------------------------------------------------------------ kernel
 template <int KIND, bool B_MN, int EPI, bool F8>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Ring<KIND, EPI>::threads, 1)
 gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1,
               const __grid_constant__ CUtensorMap tmC2, const __grid_constant__ CUtensorMap tmC3,
@@ -577,7 +585,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  Book &bk = *reinterpret_cast<Book *>(smem + BOOK_OFFSET);
+  Book &bk = *reinterpret_cast<Book *>(smem + Ring<KIND, EPI>::book_offset);
   volatile int *abort_flag = &bk.abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int crank = (int)tc::cluster_ctarank();
@@ -588,6 +596,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   constexpr int kSt = Ring<KIND, EPI>::stages;
   constexpr int kStageB = Ring<KIND, EPI>::stage_bytes;
   constexpr int BKE = Elem<F8>::BKE;
+  constexpr int kEW = Ring<KIND, EPI>::epi_warps;
   constexpr bool A_MN = KIND == KIND_TGMM && !F8;  // bf16 weight gradients read A as stored
   const bool leader = crank == 0;
 
@@ -601,10 +610,10 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     for (int a = 0; a < 2; ++a) {
       tc::mbar_init(&bk.tfull[a], 1);
       // 2-SM: the leader's accumulator is free once both CTAs' epilogues are done
-      tc::mbar_init(&bk.tempty[a], k2SM ? 2 * kEpiWarps : kEpiWarps);
+      tc::mbar_init(&bk.tempty[a], k2SM ? 2 * kEW : kEW);
     }
     tc::mbar_init(&bk.drain, 1);
-    for (int w = 0; w < kEpiWarps; ++w) tc::mbar_init(&bk.aux_full[w], 1);
+    for (int w = 0; w < kEW; ++w) tc::mbar_init(&bk.aux_full[w], 1);
     bk.abort_flag = 0;
     tc::fence_mbar_init();
   }
@@ -855,7 +864,10 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   } else if (warp >= 2) {
     const int q = warp & 3;  // TMEM lane quarter this warp may read = its tile rows
     const int rit = q * 32 + lane;
-    uint8_t *stg = smem + STG_OFFSET + (warp - 2) * kStgBytes;
+    uint8_t *stg = smem + Ring<KIND, EPI>::stg_offset + (warp - 2) * kStgBytes;
+    // 8 epilogue warps: the second four take the upper half of the columns
+    constexpr int kChunks = BN / 32 / (kEW / 4);
+    const int c_begin = ((warp - 2) >> 2) * kChunks;
     OutMaps om{&tmC0, &tmC1, &tmC2, &tmC3, &bk.aux_full[warp - 2], 0u, 0u};
     uint32_t acc_it = 0;
     for (int t = cid; t < total; t += ncl) {
@@ -864,16 +876,17 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         if (!p.accumulate) epilogue_tgmm<F8>(p, ti, 0, q, lane, stg, om, true);
         continue;
       }
-      epilogue_prefetch<KIND, EPI>(p, ti, rit);
+      epilogue_prefetch<KIND, EPI>(p, ti, rit, c_begin, c_begin + kChunks);
       if (KIND == KIND_GMM && EPI == MOE_EPI_SWIGLU_BWD && lane == 0)
-        issue_aux_load(om, stg, ti.n_idx * BN, ti.row0 + q * 32);  // first chunk's H blocks
+        issue_aux_load(om, stg, ti.n_idx * BN + c_begin * 32, ti.row0 + q * 32);  // first chunk
       const uint32_t a = acc_it & 1;
       const uint32_t aph = (acc_it >> 1) & 1;
       if (!tc::mbar_wait_warp(&bk.tfull[a], aph, abort_flag, p.wait_limit_ns)) break;
       tc::tc_fence_after();
       const uint32_t taddr = tmem + a * BN + (static_cast<uint32_t>(q * 32) << 16);
       if (KIND == KIND_GMM)
-        epilogue_gmm<EPI, F8>(p, ti, taddr, q, lane, stg, om, abort_flag);
+        epilogue_gmm<EPI, F8>(p, ti, taddr, q, lane, stg, om, abort_flag, c_begin,
+                              c_begin + kChunks);
       else
         epilogue_tgmm<F8>(p, ti, taddr, q, lane, stg, om, false);
       tc::tc_fence_before();
@@ -952,18 +965,19 @@ bool make_out_map(CUtensorMap *m, const void *base, bool f32, int64_t cols, int6
 template <int KIND, bool B_MN, int EPI, bool F8 = false>
 moe_status_t launch_tc(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap *mc,
                        const TcParams &p, int64_t tiles_upper, cudaStream_t s) {
+  constexpr int kSmem = Ring<KIND, EPI>::smem_bytes;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   static int max_clusters = 0;
   std::call_once(once, [] {
     attr_err = cudaFuncSetAttribute(gmm_tc_kernel<KIND, B_MN, EPI, F8>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (attr_err != cudaSuccess) return;
     // clusters of two CTAs (one per SM) that can be resident at once
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (unsigned)num_sms());
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.blockDim = dim3(Ring<KIND, EPI>::threads);
+    cfg.dynamicSmemBytes = kSmem;
     if (cudaOccupancyMaxActiveClusters(&max_clusters, gmm_tc_kernel<KIND, B_MN, EPI, F8>, &cfg) !=
             cudaSuccess ||
         max_clusters <= 0) {
@@ -972,14 +986,14 @@ moe_status_t launch_tc(const CUtensorMap &ma, const CUtensorMap &mb, const CUten
     }
   });
   if (attr_err != cudaSuccess) {
-    set_error("grouped GEMM: cannot reserve %d bytes of shared memory: %s", SMEM_BYTES,
+    set_error("grouped GEMM: cannot reserve %d bytes of shared memory: %s", kSmem,
               cudaGetErrorString(attr_err));
     return MOE_ERR_CUDA;
   }
   const int64_t pairs = (tiles_upper + 1) / 2;
   const int grid = 2 * (int)std::max<int64_t>(1, std::min<int64_t>(max_clusters, pairs));
-  gmm_tc_kernel<KIND, B_MN, EPI, F8><<<grid, kThreads, SMEM_BYTES, s>>>(ma, mb, mc[0], mc[1],
-                                                                        mc[2], mc[3], p);
+  gmm_tc_kernel<KIND, B_MN, EPI, F8><<<grid, Ring<KIND, EPI>::threads, kSmem, s>>>(
+      ma, mb, mc[0], mc[1], mc[2], mc[3], p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_error("grouped GEMM launch: %s", cudaGetErrorString(e));

@@ -75,6 +75,20 @@ def test_validation_errors_need_no_gpu(L):
     assert st == L.MOE_ERR_INVALID_ARG and "workspace" in L.last_error()
     st = lib.moe_aux_loss_bwd(_ptr(), 8, 1000, 8, 2, 5, _ptr(), 0.01, 1.0, _ptr(), 8, 1, None)
     assert st == L.MOE_ERR_INVALID_ARG
+    # fp8: bad format, column-wise copy too narrow, K not a multiple of 16
+    st = lib.moe_fp8_quantize_act(_ptr(), 64, _ptr(), 4, 100, 64, 7, _ptr(), _ptr(), 64, _ptr(),
+                                  1024, _ptr(), None)
+    assert st == L.MOE_ERR_INVALID_ARG and "fmt" in L.last_error()
+    st = lib.moe_fp8_quantize_act(_ptr(), 64, _ptr(), 4, 100, 64, 0, _ptr(), _ptr(), 64, _ptr(),
+                                  128, _ptr(), None)
+    assert st == L.MOE_ERR_INVALID_ARG and "leading dimension" in L.last_error()
+    assert L.moe_fp8_padded_rows(100, 4) == 640 and L.moe_fp8_padded_rows(0, 1) == 128
+    st = lib.moe_gmm_fp8(_ptr(), 64, 0, _ptr(), _ptr(), 24, 24 * 64, 0, _ptr(), _ptr(), 1, 100,
+                         24, 64, 0, None, 0, _ptr(), 0, 64, None, 0, None, None)
+    assert st == L.MOE_ERR_UNSUPPORTED
+    st = lib.moe_tgmm_fp8(_ptr(), 64, 0, _ptr(), _ptr(), 1024, 1, _ptr(), _ptr(), 4, 100, 64, 64,
+                          _ptr(), 0, 64, 64 * 64, 0, None, None)
+    assert st == L.MOE_ERR_INVALID_ARG and "ldat" in L.last_error()
     # route backward: k > E, bad leading dimension
     st = lib.moe_route_topk_bwd(_ptr(), 8, _ptr(), _ptr(), _ptr(), 10, 8, 9, 0, 1, _ptr(), 8, None)
     assert st == L.MOE_ERR_INVALID_ARG
