@@ -93,14 +93,15 @@ struct Book {
 // 2-SM MMAs whose stage holds this CTA's 128-row (tgmm: 128-column) A tile
 // and half of the B tile (32 KB, 6 stages), with 4 epilogue warps.  The
 // SwiGLU-backward dgrad, whose epilogue (H reads, two outputs) is longer than
-// its mainloop, keeps whole B tiles multicast within the pair (48 KB stages)
-// and runs 8 epilogue warps (two per TMEM lane quarter, each on half of the
-// tile's columns) in exchange for one stage.
-template <int KIND, int EPI>
+// its mainloop, keeps whole B tiles multicast within the pair (48 KB stages,
+// 4 of them).  On 8-bit codes its mainloop is twice as fast, so it runs 8
+// epilogue warps (two per TMEM lane quarter, each on half of the tile's
+// columns) in exchange for one stage (bf16 measured 15% slower that way).
+template <int KIND, int EPI, bool F8>
 struct Ring {
   static constexpr bool two_sm = KIND == 1 || EPI != MOE_EPI_SWIGLU_BWD;
-  static constexpr int epi_warps = two_sm ? 4 : 8;
-  static constexpr int stages = two_sm ? 6 : 3;
+  static constexpr int epi_warps = !two_sm && F8 ? 8 : 4;
+  static constexpr int stages = two_sm ? 6 : (epi_warps == 8 ? 3 : 4);
   static constexpr int b_bytes = two_sm ? B_BYTES / 2 : B_BYTES;
   static constexpr int stage_bytes = A_BYTES + b_bytes;
   static constexpr int threads = 64 + 32 * epi_warps;  // producer, MMA, epilogue
@@ -577,7 +578,7 @@ MOE_DEVINL void epilogue_tgmm(const TcParams &p, const TileInfo &ti, uint32_t ta
 
 // ------------------------------------------------------------------ kernel
 template <int KIND, bool B_MN, int EPI, bool F8>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Ring<KIND, EPI>::threads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Ring<KIND, EPI, F8>::threads, 1)
 gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1,
               const __grid_constant__ CUtensorMap tmC2, const __grid_constant__ CUtensorMap tmC3,
@@ -585,18 +586,18 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  Book &bk = *reinterpret_cast<Book *>(smem + Ring<KIND, EPI>::book_offset);
+  Book &bk = *reinterpret_cast<Book *>(smem + Ring<KIND, EPI, F8>::book_offset);
   volatile int *abort_flag = &bk.abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int crank = (int)tc::cluster_ctarank();
   const int cid = (int)tc::cluster_id_x();
   const int ncl = (int)tc::nclusters_x();
   constexpr uint16_t kPair = 0x3;
-  constexpr bool k2SM = Ring<KIND, EPI>::two_sm;
-  constexpr int kSt = Ring<KIND, EPI>::stages;
-  constexpr int kStageB = Ring<KIND, EPI>::stage_bytes;
+  constexpr bool k2SM = Ring<KIND, EPI, F8>::two_sm;
+  constexpr int kSt = Ring<KIND, EPI, F8>::stages;
+  constexpr int kStageB = Ring<KIND, EPI, F8>::stage_bytes;
   constexpr int BKE = Elem<F8>::BKE;
-  constexpr int kEW = Ring<KIND, EPI>::epi_warps;
+  constexpr int kEW = Ring<KIND, EPI, F8>::epi_warps;
   constexpr bool A_MN = KIND == KIND_TGMM && !F8;  // bf16 weight gradients read A as stored
   const bool leader = crank == 0;
 
@@ -864,7 +865,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   } else if (warp >= 2) {
     const int q = warp & 3;  // TMEM lane quarter this warp may read = its tile rows
     const int rit = q * 32 + lane;
-    uint8_t *stg = smem + Ring<KIND, EPI>::stg_offset + (warp - 2) * kStgBytes;
+    uint8_t *stg = smem + Ring<KIND, EPI, F8>::stg_offset + (warp - 2) * kStgBytes;
     // 8 epilogue warps: the second four take the upper half of the columns
     constexpr int kChunks = BN / 32 / (kEW / 4);
     const int c_begin = ((warp - 2) >> 2) * kChunks;
@@ -965,7 +966,7 @@ bool make_out_map(CUtensorMap *m, const void *base, bool f32, int64_t cols, int6
 template <int KIND, bool B_MN, int EPI, bool F8 = false>
 moe_status_t launch_tc(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap *mc,
                        const TcParams &p, int64_t tiles_upper, cudaStream_t s) {
-  constexpr int kSmem = Ring<KIND, EPI>::smem_bytes;
+  constexpr int kSmem = Ring<KIND, EPI, F8>::smem_bytes;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   static int max_clusters = 0;
@@ -976,7 +977,7 @@ moe_status_t launch_tc(const CUtensorMap &ma, const CUtensorMap &mb, const CUten
     // clusters of two CTAs (one per SM) that can be resident at once
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (unsigned)num_sms());
-    cfg.blockDim = dim3(Ring<KIND, EPI>::threads);
+    cfg.blockDim = dim3(Ring<KIND, EPI, F8>::threads);
     cfg.dynamicSmemBytes = kSmem;
     if (cudaOccupancyMaxActiveClusters(&max_clusters, gmm_tc_kernel<KIND, B_MN, EPI, F8>, &cfg) !=
             cudaSuccess ||
@@ -992,7 +993,7 @@ moe_status_t launch_tc(const CUtensorMap &ma, const CUtensorMap &mb, const CUten
   }
   const int64_t pairs = (tiles_upper + 1) / 2;
   const int grid = 2 * (int)std::max<int64_t>(1, std::min<int64_t>(max_clusters, pairs));
-  gmm_tc_kernel<KIND, B_MN, EPI, F8><<<grid, Ring<KIND, EPI>::threads, kSmem, s>>>(
+  gmm_tc_kernel<KIND, B_MN, EPI, F8><<<grid, Ring<KIND, EPI, F8>::threads, kSmem, s>>>(
       ma, mb, mc[0], mc[1], mc[2], mc[3], p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
