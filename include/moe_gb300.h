@@ -279,6 +279,30 @@ moe_status_t moe_gmm(const uint16_t *A, int64_t lda, const uint16_t *B, int64_t 
                      moe_stream_t stream);
 
 /*
+ * moe_transpose_act -- column-wise bf16 copy of a permuted activation in the
+ * padded group layout (see moe_fp8_padded_rows): xt[c, poff_e + i] =
+ * x[group_offsets[e] + i, c] for the rows of group e, zeros up to poff_e+1.
+ *   x   bf16 [rows_cap, ldx >= cols], cols % 8 == 0
+ *   xt  bf16 [cols, ldxt >= moe_fp8_padded_rows(rows_cap, E)] out (columns
+ *       [0, poff_E) written)
+ * The K-major A operand of moe_tgmm_kt (MaxText PR #4295, Testing: tgmm).
+ */
+moe_status_t moe_transpose_act(const uint16_t *x, int64_t ldx, const int32_t *group_offsets,
+                               int E, int64_t rows_cap, int cols, uint16_t *xt, int64_t ldxt,
+                               moe_stream_t stream);
+
+/*
+ * moe_tgmm_kt -- moe_tgmm with A given as its column-wise copy At [M, ldat]
+ * (moe_transpose_act of A); B bf16 [rows_cap, ldb] as in moe_tgmm.  Reading A
+ * K-major feeds the tensor cores faster than the row-major A of moe_tgmm.
+ * Same result, zeros for empty experts, same W arguments.
+ */
+moe_status_t moe_tgmm_kt(const uint16_t *At, int64_t ldat, const uint16_t *B, int64_t ldb,
+                         const int32_t *group_offsets, int E, int64_t rows_cap, int M, int N,
+                         void *W, int w_dtype, int64_t ldw, int64_t stride_w, int accumulate,
+                         int32_t *dev_status, moe_stream_t stream);
+
+/*
  * moe_group_colsum -- per-expert column sums, the gradient of a bias that
  * every row of a group received (the expert-FFN biases: MT-4295, Testing,
  * `mlp_bias`; TE-2912, `has_wi_bias`):

@@ -81,6 +81,9 @@ _SIGS = {
     "moe_fp8_quantize_act": (_I, [_P, _I64, _P, _I, _I64, _I, _I, _P, _P, _I64, _P, _I64, _P,
                                   _P]),
     "moe_fp8_quantize_weights": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "moe_transpose_act": (_I, [_P, _I64, _P, _I, _I64, _I, _P, _I64, _P]),
+    "moe_tgmm_kt": (_I, [_P, _I64, _P, _I64, _P, _I, _I64, _I, _I, _P, _I, _I64, _I64, _I, _P,
+                         _P]),
     "moe_gmm_fp8": (_I, [_P, _I64, _I, _P, _P, _I64, _I64, _I, _P, _P, _I, _I64, _I, _I, _I, _P,
                          _I64, _P, _I, _I64, _P, _I64, _P, _P]),
     "moe_tgmm_fp8": (_I, [_P, _I64, _I, _P, _P, _I64, _I, _P, _P, _I, _I64, _I, _I, _P, _I, _I64,
@@ -279,6 +282,23 @@ def moe_fp8_quantize_weights(w, fmt, amax, q, qt, scale_inv, stream=None):
     E, K, N = w.shape
     _check(LIB.moe_fp8_quantize_weights(_ptr(w), E, K, N, fmt, _ptr(amax), _ptr(q), _ptr(qt),
                                         _ptr(scale_inv), _stream(stream)))
+
+
+def moe_transpose_act(x, group_offsets, xt, stream=None):
+    """x bf16 [rows_cap, cols] -> xt bf16 [cols, >= padded rows] (padded group layout)."""
+    E = group_offsets.shape[0] - 1
+    _check(LIB.moe_transpose_act(_ptr(x), _ld(x), _ptr(group_offsets), E, x.shape[0], x.shape[1],
+                                 _ptr(xt), _ld(xt), _stream(stream)))
+
+
+def moe_tgmm_kt(At, B, group_offsets, rows_cap, W, accumulate=False, dev_status=None,
+                stream=None):
+    """W [E, M, N] = per-expert A^T B with A given as its column-wise copy At [M, >=P]."""
+    E, M, N = W.shape
+    w_dtype = DTYPE_F32 if W.dtype == torch.float32 else DTYPE_BF16
+    _check(LIB.moe_tgmm_kt(_ptr(At), _ld(At), _ptr(B), _ld(B), _ptr(group_offsets), E, rows_cap,
+                           M, N, _ptr(W), w_dtype, W.stride(1), W.stride(0), int(accumulate),
+                           _ptr(dev_status), _stream(stream)))
 
 
 def moe_gmm_fp8(A, a_fmt, a_scale_inv, B, b_fmt, b_scale_inv, group_offsets, C,

@@ -329,6 +329,69 @@ moe_status_t moe_tgmm(const uint16_t *A, int64_t lda, const uint16_t *B, int64_t
   return moe::launch_tgmm(a, (cudaStream_t)stream);
 }
 
+moe_status_t moe_transpose_act(const uint16_t *x, int64_t ldx, const int32_t *group_offsets,
+                               int E, int64_t rows_cap, int cols, uint16_t *xt, int64_t ldxt,
+                               moe_stream_t stream) {
+  set_error("");
+  REQUIRE(E > 0 && E <= moe::kMaxGroups && rows_cap >= 0 && cols > 0, MOE_ERR_INVALID_ARG,
+          "moe_transpose_act: E=%d rows_cap=%lld cols=%d", E, (long long)rows_cap, cols);
+  REQUIRE(cols % 8 == 0 && ldx % 8 == 0 && ldxt % 8 == 0, MOE_ERR_UNSUPPORTED,
+          "moe_transpose_act: cols, ldx, ldxt must be multiples of 8");
+  REQUIRE(ldx >= cols && ldxt >= moe::f8_padded_rows(rows_cap, E), MOE_ERR_INVALID_ARG,
+          "moe_transpose_act: leading dimension too small");
+  REQUIRE(rows_cap < (1ll << 31), MOE_ERR_UNSUPPORTED, "moe_transpose_act: 2^31 rows");
+  REQUIRE(group_offsets && xt && (rows_cap == 0 || x), MOE_ERR_INVALID_ARG,
+          "moe_transpose_act: null pointer");
+  REQUIRE(aligned16(x) && aligned16(xt), MOE_ERR_UNSUPPORTED,
+          "moe_transpose_act: x and xt must be 16-byte aligned");
+  return cuda_status(moe::launch_transpose_act(x, ldx, group_offsets, E, rows_cap, cols, xt, ldxt,
+                                               (cudaStream_t)stream),
+                     "moe_transpose_act launch");
+}
+
+moe_status_t moe_tgmm_kt(const uint16_t *At, int64_t ldat, const uint16_t *B, int64_t ldb,
+                         const int32_t *group_offsets, int E, int64_t rows_cap, int M, int N,
+                         void *W, int w_dtype, int64_t ldw, int64_t stride_w, int accumulate,
+                         int32_t *dev_status, moe_stream_t stream) {
+  set_error("");
+  REQUIRE(E > 0 && rows_cap >= 0 && M > 0 && N > 0, MOE_ERR_INVALID_ARG,
+          "moe_tgmm_kt: E=%d rows_cap=%lld M=%d N=%d", E, (long long)rows_cap, M, N);
+  REQUIRE(w_dtype == MOE_DTYPE_BF16 || w_dtype == MOE_DTYPE_F32, MOE_ERR_INVALID_ARG,
+          "moe_tgmm_kt: bad w_dtype");
+  REQUIRE(!accumulate || w_dtype == MOE_DTYPE_F32, MOE_ERR_INVALID_ARG,
+          "moe_tgmm_kt: accumulate needs fp32 W");
+  const int64_t P = moe::f8_padded_rows(rows_cap, E);
+  REQUIRE(P / moe::kF8PadRows < 65536, MOE_ERR_UNSUPPORTED,
+          "moe_tgmm_kt: more than 2^16 blocks of 128 rows");
+  REQUIRE(ldat >= P && ldat % 8 == 0, MOE_ERR_INVALID_ARG,
+          "moe_tgmm_kt: ldat must be >= moe_fp8_padded_rows (%lld) and a multiple of 8",
+          (long long)P);
+  REQUIRE(N % 8 == 0 && ldb % 8 == 0 && ldw % 8 == 0, MOE_ERR_UNSUPPORTED,
+          "moe_tgmm_kt: N, ldb, ldw must be multiples of 8");
+  REQUIRE(ldb >= N && ldw >= N, MOE_ERR_INVALID_ARG, "moe_tgmm_kt: leading dimension < N");
+  REQUIRE(stride_w >= (int64_t)M * ldw || E == 1, MOE_ERR_INVALID_ARG,
+          "moe_tgmm_kt: stride_w overlaps experts");
+  REQUIRE(group_offsets && W && (rows_cap == 0 || (At && B)), MOE_ERR_INVALID_ARG,
+          "moe_tgmm_kt: null pointer");
+  REQUIRE(aligned16(At) && aligned16(B) && aligned16(W), MOE_ERR_UNSUPPORTED,
+          "moe_tgmm_kt: operands must be 16-byte aligned");
+  REQUIRE(rows_cap < (1ll << 31), MOE_ERR_UNSUPPORTED, "moe_tgmm_kt: more than 2^31 rows");
+  if (rows_cap == 0) {  // no rows at all: every expert is empty
+    if (accumulate) return MOE_OK;
+    const size_t es = w_dtype == MOE_DTYPE_F32 ? 4 : 2;
+    for (int e = 0; e < E; ++e) {
+      const cudaError_t ce =
+          cudaMemset2DAsync(static_cast<char *>(W) + (size_t)e * stride_w * es, (size_t)ldw * es,
+                            0, (size_t)N * es, (size_t)M, (cudaStream_t)stream);
+      if (ce != cudaSuccess) return cuda_status(ce, "moe_tgmm_kt zero fill");
+    }
+    return MOE_OK;
+  }
+  moe::TgmmArgs a{nullptr, 0, B, ldb, group_offsets, E, rows_cap, M, N, W, w_dtype, ldw,
+                  stride_w, accumulate, dev_status};
+  return moe::launch_tgmm_kt(a, At, ldat, (cudaStream_t)stream);
+}
+
 moe_status_t moe_group_colsum(const uint16_t *G, int64_t ldg, const int32_t *group_offsets,
                               int E, int64_t rows_cap, int N, float *out, int64_t ld_out,
                               moe_stream_t stream) {

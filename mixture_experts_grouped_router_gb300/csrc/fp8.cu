@@ -22,7 +22,8 @@
 namespace moe {
 namespace {
 
-constexpr int kQT = 64;  // tile: 64 rows x 64 columns
+constexpr int kQT = 64;   // tile: 64 rows x 64 columns
+constexpr int kQCT = 8;   // column tiles per block (amortises the group-offset scan)
 
 MOE_DEVINL float fp8_max_of(int fmt) { return fmt == MOE_FP8_E4M3 ? 448.0f : 57344.0f; }
 
@@ -99,7 +100,6 @@ quant_kernel(const uint16_t *__restrict__ x, int64_t ldx, int64_t rpg, int cols,
   __shared__ int s_poff[kMaxGroups + 1];
   const int g = PADDED ? 0 : blockIdx.z;
   const int64_t j0 = (int64_t)blockIdx.x * kQT;  // first (padded) row of the tile
-  const int c0 = blockIdx.y * kQT;
   const float scale = scale_of(__ldg(amax + g), fmt);
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) scale_inv[g] = __frcp_rn(scale);
 
@@ -144,38 +144,43 @@ quant_kernel(const uint16_t *__restrict__ x, int64_t ldx, int64_t rpg, int cols,
   }
   const uint16_t *xg = x + (int64_t)g * rpg * ldx;
   uint8_t *qg = q + (int64_t)g * stride_q;
-  // load, quantize, write row-wise codes, keep the tile in shared memory
+  for (int ct = 0; ct < kQCT; ++ct) {
+    const int c0 = (blockIdx.y * kQCT + ct) * kQT;
+    if (c0 >= cols) break;
+    if (ct > 0) __syncthreads();  // the previous tile's column-wise reads are done
+    // load, quantize, write row-wise codes, keep the tile in shared memory
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int v = threadIdx.x + h * 256;
-    const int i = v >> 3;            // tile row
-    const int cc = (v & 7) * 8;      // tile column
-    const int64_t r = src0 + i;
-    const int c = c0 + cc;
-    uint2 codes = make_uint2(0, 0);
-    if (r < src_end && c < cols) {
-      codes = quant8(ld_nc_v4(xg + r * ldx + c), scale, fmt);
-      *reinterpret_cast<uint2 *>(qg + r * ldq + c) = codes;
-    }
-    *reinterpret_cast<uint2 *>(&tile[i][cc]) = codes;
-  }
-  __syncthreads();
-  // column-wise: output row c (= input column), 16 consecutive padded rows
-  {
-    const int cr = threadIdx.x >> 2;       // tile column -> output row
-    const int k16 = (threadIdx.x & 3) * 16;
-    const int c = c0 + cr;
-    const int64_t jj = j0 + k16;
-    if (c < cols && (PADDED || jj < rpg)) {
-      uint32_t w[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        w[u] = 0;
-#pragma unroll
-        for (int b = 0; b < 4; ++b) w[u] |= (uint32_t)tile[k16 + 4 * u + b][cr] << (8 * b);
+    for (int h = 0; h < 2; ++h) {
+      const int v = threadIdx.x + h * 256;
+      const int i = v >> 3;            // tile row
+      const int cc = (v & 7) * 8;      // tile column
+      const int64_t r = src0 + i;
+      const int c = c0 + cc;
+      uint2 codes = make_uint2(0, 0);
+      if (r < src_end && c < cols) {
+        codes = quant8(ld_nc_v4(xg + r * ldx + c), scale, fmt);
+        *reinterpret_cast<uint2 *>(qg + r * ldq + c) = codes;
       }
-      *reinterpret_cast<uint4 *>(qt + (int64_t)g * stride_qt + (int64_t)c * ldqt + jj) =
-          make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint2 *>(&tile[i][cc]) = codes;
+    }
+    __syncthreads();
+    // column-wise: output row c (= input column), 16 consecutive padded rows
+    {
+      const int cr = threadIdx.x >> 2;       // tile column -> output row
+      const int k16 = (threadIdx.x & 3) * 16;
+      const int c = c0 + cr;
+      const int64_t jj = j0 + k16;
+      if (c < cols && (PADDED || jj < rpg)) {
+        uint32_t w[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          w[u] = 0;
+#pragma unroll
+          for (int b = 0; b < 4; ++b) w[u] |= (uint32_t)tile[k16 + 4 * u + b][cr] << (8 * b);
+        }
+        *reinterpret_cast<uint4 *>(qt + (int64_t)g * stride_qt + (int64_t)c * ldqt + jj) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+      }
     }
   }
 }
@@ -204,7 +209,7 @@ cudaError_t launch_fp8_quant_act(const uint16_t *x, int64_t ldx, const int32_t *
                                  uint8_t *q, int64_t ldq, uint8_t *qt, int64_t ldqt,
                                  float *scale_inv, cudaStream_t s) {
   const int64_t pr = f8_padded_rows(rows_cap, E);
-  dim3 grid((unsigned)(pr / kQT), (cols + kQT - 1) / kQT, 1);
+  dim3 grid((unsigned)(pr / kQT), (cols + kQT * kQCT - 1) / (kQT * kQCT), 1);
   quant_kernel<true><<<grid, 256, 0, s>>>(x, ldx, rows_cap, cols, offsets, E, rows_cap, amax,
                                           fmt, q, ldq, 0, qt, ldqt, 0, scale_inv);
   return cudaGetLastError();
@@ -213,7 +218,7 @@ cudaError_t launch_fp8_quant_act(const uint16_t *x, int64_t ldx, const int32_t *
 cudaError_t launch_fp8_quant_weights(const uint16_t *w, int E, int K, int N, int fmt,
                                      const float *amax, uint8_t *q, uint8_t *qt,
                                      float *scale_inv, cudaStream_t s) {
-  dim3 grid((K + kQT - 1) / kQT, (N + kQT - 1) / kQT, E);
+  dim3 grid((K + kQT - 1) / kQT, (N + kQT * kQCT - 1) / (kQT * kQCT), E);
   quant_kernel<false><<<grid, 256, 0, s>>>(w, N, K, N, nullptr, E, K, amax, fmt, q, N,
                                            (int64_t)K * N, qt, K, (int64_t)N * K, scale_inv);
   return cudaGetLastError();

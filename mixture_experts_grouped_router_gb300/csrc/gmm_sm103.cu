@@ -52,6 +52,7 @@ namespace {
 constexpr int BM = 128, BN = 256, BK = 64, UK = 16;
 constexpr int kStages = 6;  // ring slots allocated (the weight-gradient kernel uses 4)
 constexpr int kMaxEpiWarps = 8;
+constexpr int kPadRows = kF8PadRows;  // group padding of column-wise copies (128 rows)
 constexpr int kStgBytes = 8192;  // per epilogue warp: up to four 32x32 bf16 blocks (or two fp32)
 constexpr int A_BYTES = BM * BK * 2;   // 16 KB
 constexpr int B_BYTES = BN * BK * 2;   // 32 KB
@@ -84,8 +85,8 @@ struct Book {
   int abort_flag;
   int total_tiles;
   int cum[kMaxE + 1];            // per-expert tile prefix
-  // FP8 weight gradients: start of each expert's zero-padded K range, in K
-  // blocks (rows / 128; the column-wise copies hold < 2^16 blocks)
+  // weight gradients from column-wise copies: start of each expert's
+  // zero-padded K range in units of kPadRows (the copies hold < 2^16 of them)
   uint16_t poff[kMaxE + 1];
 };
 
@@ -147,6 +148,7 @@ struct TcParams {
 
 struct TileInfo {
   int e, m_idx, n_idx, row0, row_end, kblocks;
+  int k0;  // weight gradients from a column-wise copy of A: the expert's first column
 };
 
 // Group offsets read from global memory (through L1), clamped to [0, rows_cap].
@@ -157,7 +159,7 @@ MOE_DEVINL int group_offset(const TcParams &p, int e) {
 // Tiles are handed out in pairs: the two CTAs of a cluster take row tiles
 // 2*pm and 2*pm + 1 of the same expert and column tile (the second one may lie
 // past the expert's rows; it then runs through the pipeline and stores nothing).
-template <int KIND, bool F8>
+template <int KIND, bool F8, bool AK>
 MOE_DEVINL TileInfo decode_tile(const Book &bk, const TcParams &p, int t, int crank) {
   int lo = 0, hi = p.E - 1;
   while (lo < hi) {
@@ -185,12 +187,14 @@ MOE_DEVINL TileInfo decode_tile(const Book &bk, const TcParams &p, int t, int cr
     ti.kblocks = (p.K + BKE - 1) / BKE;
   } else if (F8) {
     // FP8 weight gradients read the column-wise copies, where expert e's rows
-    // fill whole K blocks from poff[e] on (zero padded)
-    ti.row0 = (int)bk.poff[lo] * BKE;
-    ti.row_end = (int)bk.poff[lo + 1] * BKE;
-    ti.kblocks = (int)bk.poff[lo + 1] - (int)bk.poff[lo];
+    // fill whole K blocks from poff[e] on (zero padded to 128 rows)
+    ti.row0 = (int)bk.poff[lo] * kPadRows;
+    ti.row_end = (int)bk.poff[lo + 1] * kPadRows;
+    ti.kblocks = (ti.row_end - ti.row0) / BKE;
+    ti.k0 = ti.row0;
   } else {
     ti.kblocks = (size + BKE - 1) / BKE;
+    ti.k0 = AK ? (int)bk.poff[lo] * kPadRows : 0;
   }
   return ti;
 }
@@ -577,7 +581,7 @@ MOE_DEVINL void epilogue_tgmm(const TcParams &p, const TileInfo &ti, uint32_t ta
 }
 
 // ------------------------------------------------------------------ kernel
-template <int KIND, bool B_MN, int EPI, bool F8>
+template <int KIND, bool B_MN, int EPI, bool F8, bool AK>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Ring<KIND, EPI, F8>::threads, 1)
 gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1,
@@ -598,7 +602,9 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   constexpr int kStageB = Ring<KIND, EPI, F8>::stage_bytes;
   constexpr int BKE = Elem<F8>::BKE;
   constexpr int kEW = Ring<KIND, EPI, F8>::epi_warps;
-  constexpr bool A_MN = KIND == KIND_TGMM && !F8;  // bf16 weight gradients read A as stored
+  // bf16 weight gradients read A as stored (MN-major) unless AK: then from a
+  // zero-padded column-wise copy (K-major), like FP8 always does
+  constexpr bool A_MN = KIND == KIND_TGMM && !AK;
   const bool leader = crank == 0;
 
   if (threadIdx.x == 0) {
@@ -635,7 +641,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         const int size = max(group_offset(p, e + 1) - group_offset(p, e), 0);
         const int mt = KIND == KIND_GMM ? (size + BM - 1) / BM : p.m_tiles;
         tiles = (mt + 1) / 2 * p.n_tiles;
-        padded = (size + BKE - 1) / BKE;
+        padded = (size + kPadRows - 1) / kPadRows;
       }
       int incl = tiles, pincl = padded;
 #pragma unroll
@@ -683,7 +689,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   if (warp == 0) {
     if (lane == 0 && !p.stall_loads) {
       for (int t = cid; t < total; t += ncl) {
-        const TileInfo ti = decode_tile<KIND, F8>(bk, p, t, crank);
+        const TileInfo ti = decode_tile<KIND, F8, AK>(bk, p, t, crank);
         bool ok = true;
         for (int kb = 0; kb < ti.kblocks; ++kb) {
           const int s = issued % kSt;
@@ -706,6 +712,14 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
               const int k = ti.row0 + kb * BKE;
               tc::tma_load_2d_2sm(sa, &tmA, fbl, k, ti.m_idx * BM);
               tc::tma_load_2d_2sm(sb, &tmB, fbl, k, ti.n_idx * BN + crank * (BN / 2));
+            } else if (KIND == KIND_TGMM && AK) {
+              // K-major A from the column-wise copy (zero padded past the
+              // expert's rows); MN-major B rows as stored (tail zeroed below)
+              const int r = ti.row0 + kb * BKE;
+              const int nb = ti.n_idx * BN + crank * (BN / 2);
+              tc::tma_load_2d_2sm(sa, &tmA, fbl, ti.k0 + kb * BKE, ti.m_idx * BM);
+              tc::tma_load_2d_2sm(sb, &tmB, fbl, nb, r);
+              tc::tma_load_2d_2sm(sb + BOX_BYTES, &tmB, fbl, nb + 64, r);
             } else if (KIND == KIND_TGMM) {
               // this CTA's 128 output rows of A (two 64-column boxes) and its
               // 128 columns of B, both over the K block's 64 rows
@@ -780,7 +794,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     uint32_t it = 0, acc_it = 0;
     bool ok = true;
     for (int t = cid; t < total && ok; t += ncl) {
-      const TileInfo ti = decode_tile<KIND, F8>(bk, p, t, crank);
+      const TileInfo ti = decode_tile<KIND, F8, AK>(bk, p, t, crank);
       if (ti.kblocks == 0) continue;
       const uint32_t a = acc_it & 1;
       const uint32_t aph = (acc_it >> 1) & 1;
@@ -803,14 +817,15 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
           // 2-SM: this CTA's four boxes and the same four in the partner
           // CTA, whose copies have landed too (they complete on this CTA's
           // full barrier) and whose boxes this MMA reads.
+          // (AK: A's copy is zero past the rows already; only B's boxes)
           const int valid = ti.row_end - (ti.row0 + kb * BK);
           if (valid < BK) {
-            constexpr int kBoxes = k2SM ? 4 : 6;
+            constexpr int kBoxes = AK ? 2 : (k2SM ? 4 : 6);
             const int nrows = BK - valid;
             for (int i = lane; i < nrows * kBoxes * 8; i += 32) {
               const int chunk = i & 7;
               const int rr = valid + ((i >> 3) % nrows);
-              const int box = (i >> 3) / nrows;
+              const int box = (i >> 3) / nrows + (AK ? 2 : 0);
               uint8_t *base = box < 2 ? sa + box * BOX_BYTES : sb + (box - 2) * BOX_BYTES;
               uint8_t *at = base + rr * 128 + chunk * 16;
               *reinterpret_cast<uint4 *>(at) = make_uint4(0, 0, 0, 0);
@@ -872,7 +887,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     OutMaps om{&tmC0, &tmC1, &tmC2, &tmC3, &bk.aux_full[warp - 2], 0u, 0u};
     uint32_t acc_it = 0;
     for (int t = cid; t < total; t += ncl) {
-      const TileInfo ti = decode_tile<KIND, F8>(bk, p, t, crank);
+      const TileInfo ti = decode_tile<KIND, F8, AK>(bk, p, t, crank);
       if (KIND == KIND_TGMM && ti.kblocks == 0) {
         if (!p.accumulate) epilogue_tgmm<F8>(p, ti, 0, q, lane, stg, om, true);
         continue;
@@ -963,7 +978,7 @@ bool make_out_map(CUtensorMap *m, const void *base, bool f32, int64_t cols, int6
                   f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-template <int KIND, bool B_MN, int EPI, bool F8 = false>
+template <int KIND, bool B_MN, int EPI, bool F8 = false, bool AK = F8>
 moe_status_t launch_tc(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap *mc,
                        const TcParams &p, int64_t tiles_upper, cudaStream_t s) {
   constexpr int kSmem = Ring<KIND, EPI, F8>::smem_bytes;
@@ -971,7 +986,7 @@ moe_status_t launch_tc(const CUtensorMap &ma, const CUtensorMap &mb, const CUten
   static cudaError_t attr_err = cudaSuccess;
   static int max_clusters = 0;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gmm_tc_kernel<KIND, B_MN, EPI, F8>,
+    attr_err = cudaFuncSetAttribute(gmm_tc_kernel<KIND, B_MN, EPI, F8, AK>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (attr_err != cudaSuccess) return;
     // clusters of two CTAs (one per SM) that can be resident at once
@@ -979,7 +994,7 @@ moe_status_t launch_tc(const CUtensorMap &ma, const CUtensorMap &mb, const CUten
     cfg.gridDim = dim3(2 * (unsigned)num_sms());
     cfg.blockDim = dim3(Ring<KIND, EPI, F8>::threads);
     cfg.dynamicSmemBytes = kSmem;
-    if (cudaOccupancyMaxActiveClusters(&max_clusters, gmm_tc_kernel<KIND, B_MN, EPI, F8>, &cfg) !=
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, gmm_tc_kernel<KIND, B_MN, EPI, F8, AK>, &cfg) !=
             cudaSuccess ||
         max_clusters <= 0) {
       cudaGetLastError();
@@ -993,7 +1008,7 @@ moe_status_t launch_tc(const CUtensorMap &ma, const CUtensorMap &mb, const CUten
   }
   const int64_t pairs = (tiles_upper + 1) / 2;
   const int grid = 2 * (int)std::max<int64_t>(1, std::min<int64_t>(max_clusters, pairs));
-  gmm_tc_kernel<KIND, B_MN, EPI, F8><<<grid, Ring<KIND, EPI, F8>::threads, kSmem, s>>>(
+  gmm_tc_kernel<KIND, B_MN, EPI, F8, AK><<<grid, Ring<KIND, EPI, F8>::threads, kSmem, s>>>(
       ma, mb, mc[0], mc[1], mc[2], mc[3], p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
@@ -1108,14 +1123,25 @@ moe_status_t launch_gmm(const GmmArgs &a, cudaStream_t s) {
   }
 }
 
-moe_status_t launch_tgmm(const TgmmArgs &a, cudaStream_t s) {
+// At == nullptr: A read as stored (MN-major); else K-major from its
+// column-wise copy At [M, ldat] (zero-padded group layout).
+static moe_status_t tgmm_impl(const TgmmArgs &a, const uint16_t *At, int64_t ldat,
+                              cudaStream_t s) {
   if (a.E > kMaxE) {
     set_error("moe_tgmm: E=%d > %d", a.E, kMaxE);
     return MOE_ERR_UNSUPPORTED;
   }
   CUtensorMap ma, mb;
   const uint32_t box[2] = {64, BK};
-  {
+  if (At != nullptr) {
+    const uint64_t dims[2] = {(uint64_t)f8_padded_rows(a.rows_cap, a.E), (uint64_t)a.M};
+    const uint64_t st[1] = {(uint64_t)ldat * 2};
+    const uint32_t abox[2] = {BK, BM};
+    if (!make_map(&ma, At, 2, dims, st, abox)) {
+      set_error("moe_tgmm: cannot encode the TMA descriptor of A");
+      return MOE_ERR_CUDA;
+    }
+  } else {
     const uint64_t dims[2] = {(uint64_t)a.M, (uint64_t)a.rows_cap};
     const uint64_t st[1] = {(uint64_t)a.lda * 2};
     if (!make_map(&ma, a.A, 2, dims, st, box)) {
@@ -1164,7 +1190,15 @@ moe_status_t launch_tgmm(const TgmmArgs &a, cudaStream_t s) {
     mc[1] = mc[2] = mc[3] = mc[0];
   }
   const int64_t tiles_upper = (int64_t)a.E * p.m_tiles * p.n_tiles;
+  if (At != nullptr)
+    return launch_tc<KIND_TGMM, true, MOE_EPI_NONE, false, true>(ma, mb, mc, p, tiles_upper, s);
   return launch_tc<KIND_TGMM, true, MOE_EPI_NONE>(ma, mb, mc, p, tiles_upper, s);
+}
+
+moe_status_t launch_tgmm(const TgmmArgs &a, cudaStream_t s) { return tgmm_impl(a, nullptr, 0, s); }
+
+moe_status_t launch_tgmm_kt(const TgmmArgs &a, const uint16_t *At, int64_t ldat, cudaStream_t s) {
+  return tgmm_impl(a, At, ldat, s);
 }
 
 // Output maps shared by the bf16 and FP8 ragged-M GEMMs (unused slots repeat

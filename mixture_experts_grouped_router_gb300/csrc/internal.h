@@ -43,6 +43,11 @@ cudaError_t launch_fp8_quant_weights(const uint16_t *w, int E, int K, int N, int
                                      const float *amax, uint8_t *q, uint8_t *qt,
                                      float *scale_inv, cudaStream_t s);
 
+// transpose.cu
+cudaError_t launch_transpose_act(const uint16_t *x, int64_t ldx, const int32_t *offsets, int E,
+                                 int64_t rows_cap, int cols, uint16_t *xt, int64_t ldxt,
+                                 cudaStream_t s);
+
 // permute.cu
 size_t permute_workspace_bytes(int T, int E);
 cudaError_t launch_permute(const uint16_t *x, int64_t ldx, const int32_t *topk_idx, int T, int d,
@@ -87,6 +92,8 @@ struct TgmmArgs {
   int32_t *dev_status;
 };
 moe_status_t launch_tgmm(const TgmmArgs &a, cudaStream_t s);
+// the same with A read K-major from its column-wise copy At [M, ldat]
+moe_status_t launch_tgmm_kt(const TgmmArgs &a, const uint16_t *At, int64_t ldat, cudaStream_t s);
 
 // FP8 (8-bit float codes, K-major operands, fp32 accumulation; the epilogue
 // multiplies by the scales' inverses)

@@ -164,3 +164,68 @@ def test_gmm_rejects_bad_args_before_launch():
     with pytest.raises(L.MoEError) as ei:
         L.moe_gmm(a, b, 0, off, c)     # K = 12 is not a multiple of 8
     assert ei.value.status == L.MOE_ERR_UNSUPPORTED
+
+
+# ---------------------------------------------------------------------------
+# weight gradients from the column-wise copy of A (K-major operand)
+# ---------------------------------------------------------------------------
+def _poff(sizes, pad=128):
+    p = [0]
+    for s in sizes:
+        p.append(p[-1] + (s + pad - 1) // pad * pad)
+    return p
+
+
+@pytest.mark.parametrize("sz,cols", [("mixed", 64), ("one", 200), ("tiny", 8), ("empty_tail", 136)])
+def test_transpose_act_padded(sz, cols):
+    rng = np.random.default_rng(cols + len(SIZES[sz]))
+    off = _offsets(SIZES[sz])
+    E, R = len(SIZES[sz]), int(off[-1])
+    rows_cap = R + 9
+    x_bits = _bf(rng, (rows_cap, cols))
+    x = dev_bf16(x_bits)
+    x[R:] = float("nan")
+    P = L.moe_fp8_padded_rows(rows_cap, E)
+    xt = torch.full((cols, P), 3.0, dtype=torch.bfloat16, device="cuda")
+    L.moe_transpose_act(x, torch.from_numpy(off).cuda(), xt)
+    torch.cuda.synchronize()
+    got = xt.view(torch.int16).cpu().numpy().astype(np.uint16)
+    po = _poff(SIZES[sz])
+    for e in range(E):
+        a, b = int(off[e]), int(off[e + 1])
+        assert (got[:, po[e]:po[e] + b - a] == x_bits[a:b].T).all(), e
+        assert (got[:, po[e] + b - a:po[e + 1]] == 0).all(), e
+
+
+@pytest.mark.parametrize("sz,M,N", TGMM_CASES)
+@pytest.mark.parametrize("mode", ["bf16", "f32", "f32_acc"])
+def test_tgmm_kt(sz, M, N, mode):
+    rng = np.random.default_rng(M * 7 + N)
+    off = _offsets(SIZES[sz])
+    E, R = len(SIZES[sz]), int(off[-1])
+    rows_cap = R + 37
+    a_bits = _bf(rng, (rows_cap, M))
+    b_bits = _bf(rng, (rows_cap, N))
+    A = dev_bf16(a_bits)
+    B = dev_bf16(b_bits)
+    A[R:] = float("nan")          # rows past the groups are never read
+    B[R:] = float("nan")
+    offd = torch.from_numpy(off).cuda()
+    At = torch.empty(M, L.moe_fp8_padded_rows(rows_cap, E), dtype=torch.bfloat16, device="cuda")
+    L.moe_transpose_act(A, offd, At)
+    dt = torch.bfloat16 if mode == "bf16" else torch.float32
+    W = torch.full((E, M, N), 0.0, dtype=dt, device="cuda")
+    init = None
+    if mode == "f32_acc":
+        init = rng.standard_normal((E, M, N)).astype(np.float32)
+        W.copy_(torch.from_numpy(init))
+    L.moe_tgmm_kt(At, B, offd, rows_cap, W, accumulate=mode == "f32_acc")
+    torch.cuda.synchronize()
+    a64 = moe_synth.bits_to_f64(a_bits)
+    b64 = moe_synth.bits_to_f64(b_bits)
+    want = moe_ref.tgmm(a64[:R], b64[:R], off, E,
+                        partial_sum=None if init is None else init.astype(np.float64))
+    assert_close("tgmm_kt", W, want)
+    if mode != "f32_acc":
+        for e in np.nonzero(np.diff(off) == 0)[0]:
+            assert (W[e].float() == 0).all()
