@@ -90,19 +90,19 @@ struct Book {
   uint16_t poff[kMaxE + 1];
 };
 
-// Per-kernel layout.  The forward, dgrad and weight-gradient GEMMs run as
-// 2-SM MMAs whose stage holds this CTA's 128-row (tgmm: 128-column) A tile
-// and half of the B tile (32 KB, 6 stages), with 4 epilogue warps.  The
-// SwiGLU-backward dgrad, whose epilogue (H reads, two outputs) is longer than
-// its mainloop, keeps whole B tiles multicast within the pair (48 KB stages,
-// 4 of them).  On 8-bit codes its mainloop is twice as fast, so it runs 8
-// epilogue warps (two per TMEM lane quarter, each on half of the tile's
-// columns) in exchange for one stage (bf16 measured 15% slower that way).
+// Per-kernel layout.  The GEMMs run as 2-SM MMAs whose stage holds this
+// CTA's 128-row (tgmm: 128-column) A tile and half of the B tile (32 KB), 6
+// stages, 4 epilogue warps.  The SwiGLU-backward dgrad, whose epilogue (H
+// reads, two outputs) is the longest, runs 8 epilogue warps (two per TMEM
+// lane quarter, each on half of the tile's columns) and 4 stages; on 8-bit
+// codes it keeps whole B tiles multicast within the pair (48 KB stages, 3 of
+// them), which measured faster there.
 template <int KIND, int EPI, bool F8>
 struct Ring {
-  static constexpr bool two_sm = KIND == 1 || EPI != MOE_EPI_SWIGLU_BWD;
-  static constexpr int epi_warps = !two_sm && F8 ? 8 : 4;
-  static constexpr int stages = two_sm ? 6 : (epi_warps == 8 ? 3 : 4);
+  static constexpr bool swiglu_bwd = KIND == 0 && EPI == MOE_EPI_SWIGLU_BWD;
+  static constexpr bool two_sm = !(swiglu_bwd && F8);
+  static constexpr int epi_warps = swiglu_bwd ? 8 : 4;
+  static constexpr int stages = two_sm ? (swiglu_bwd ? 4 : 6) : 3;
   static constexpr int b_bytes = two_sm ? B_BYTES / 2 : B_BYTES;
   static constexpr int stage_bytes = A_BYTES + b_bytes;
   static constexpr int threads = 64 + 32 * epi_warps;  // producer, MMA, epilogue
