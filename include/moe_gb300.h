@@ -385,6 +385,9 @@ moe_status_t moe_fp8_quantize_weights(const uint16_t *w, int E, int K, int N, in
  *         n*ldb (the transposed copy for [K, N] weights, the row-wise copy of
  *         a [N, K] weight for dgrad); SWIGLU_FWD: rows [0, F) gate, [F, 2F) up
  *   a_scale_inv fp32 [1], b_scale_inv fp32 [E] (device)
+ *   amax_out  fp32 [1] (device) or NULL: set to max |x| over the bf16 values
+ *             the epilogue writes (Act for SWIGLU_FWD, dH for SWIGLU_BWD, C
+ *             for NONE), the amax that quantizes them next (no extra pass)
  *   K, lda, ldb, stride_b multiples of 16; other arguments as moe_gmm.
  * FP8 recipe (TE-2912, the fused up-projection; MaxText PR #2319, quantizer
  * settings): E4M3 operands forward, E5M2 gradients backward.
@@ -394,7 +397,8 @@ moe_status_t moe_gmm_fp8(const uint8_t *A, int64_t lda, int a_fmt, const float *
                          const float *b_scale_inv, const int32_t *group_offsets, int E,
                          int64_t rows_cap, int K, int N, int epilogue, const uint16_t *aux,
                          int64_t ld_aux, void *C, int c_dtype, int64_t ldc, uint16_t *C2,
-                         int64_t ldc2, int32_t *dev_status, moe_stream_t stream);
+                         int64_t ldc2, float *amax_out, int32_t *dev_status,
+                         moe_stream_t stream);
 
 /*
  * moe_tgmm_fp8 -- moe_tgmm on the column-wise copies of two permuted

@@ -85,7 +85,7 @@ _SIGS = {
     "moe_tgmm_kt": (_I, [_P, _I64, _P, _I64, _P, _I, _I64, _I, _I, _P, _I, _I64, _I64, _I, _P,
                          _P]),
     "moe_gmm_fp8": (_I, [_P, _I64, _I, _P, _P, _I64, _I64, _I, _P, _P, _I, _I64, _I, _I, _I, _P,
-                         _I64, _P, _I, _I64, _P, _I64, _P, _P]),
+                         _I64, _P, _I, _I64, _P, _I64, _P, _P, _P]),
     "moe_tgmm_fp8": (_I, [_P, _I64, _I, _P, _P, _I64, _I, _P, _P, _I, _I64, _I, _I, _P, _I, _I64,
                           _I64, _I, _P, _P]),
     "moe_unpermute_bwd": (_I, [_P, _I64, _P, _I64, _P, _P, _P, _P, _I, _I, _I, _I, _I64, _P,
@@ -302,7 +302,8 @@ def moe_tgmm_kt(At, B, group_offsets, rows_cap, W, accumulate=False, dev_status=
 
 
 def moe_gmm_fp8(A, a_fmt, a_scale_inv, B, b_fmt, b_scale_inv, group_offsets, C,
-                epilogue=EPI_NONE, aux=None, C2=None, dev_status=None, stream=None):
+                epilogue=EPI_NONE, aux=None, C2=None, dev_status=None, stream=None,
+                amax_out=None):
     """A uint8 codes [rows_cap, K]; B uint8 codes [E, N, K] (K-major); C bf16 or fp32."""
     E, N, K = B.shape
     c_dtype = DTYPE_F32 if C.dtype == torch.float32 else DTYPE_BF16
@@ -310,8 +311,8 @@ def moe_gmm_fp8(A, a_fmt, a_scale_inv, B, b_fmt, b_scale_inv, group_offsets, C,
                            B.stride(0), b_fmt, _ptr(b_scale_inv), _ptr(group_offsets), E,
                            A.shape[0], K, N, epilogue, _ptr(aux),
                            _ld(aux) if aux is not None else 0, _ptr(C), c_dtype, _ld(C),
-                           _ptr(C2), _ld(C2) if C2 is not None else 0, _ptr(dev_status),
-                           _stream(stream)))
+                           _ptr(C2), _ld(C2) if C2 is not None else 0, _ptr(amax_out),
+                           _ptr(dev_status), _stream(stream)))
 
 
 def moe_tgmm_fp8(At, a_fmt, a_scale_inv, Bt, b_fmt, b_scale_inv, group_offsets, rows_cap, W,

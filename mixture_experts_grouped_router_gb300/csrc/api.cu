@@ -483,7 +483,8 @@ moe_status_t moe_gmm_fp8(const uint8_t *A, int64_t lda, int a_fmt, const float *
                          const float *b_scale_inv, const int32_t *group_offsets, int E,
                          int64_t rows_cap, int K, int N, int epilogue, const uint16_t *aux,
                          int64_t ld_aux, void *C, int c_dtype, int64_t ldc, uint16_t *C2,
-                         int64_t ldc2, int32_t *dev_status, moe_stream_t stream) {
+                         int64_t ldc2, float *amax_out, int32_t *dev_status,
+                         moe_stream_t stream) {
   set_error("");
   REQUIRE(E > 0 && rows_cap >= 0 && K > 0 && N > 0, MOE_ERR_INVALID_ARG,
           "moe_gmm_fp8: E=%d rows_cap=%lld K=%d N=%d", E, (long long)rows_cap, K, N);
@@ -520,10 +521,15 @@ moe_status_t moe_gmm_fp8(const uint8_t *A, int64_t lda, int a_fmt, const float *
   REQUIRE(ldc >= (epilogue == MOE_EPI_SWIGLU_FWD ? N : outN) && ldc % 8 == 0, MOE_ERR_INVALID_ARG,
           "moe_gmm_fp8: ldc too small or not a multiple of 8");
   REQUIRE(rows_cap < (1ll << 31), MOE_ERR_UNSUPPORTED, "moe_gmm_fp8: more than 2^31 rows");
-  if (rows_cap == 0) return MOE_OK;
+  if (rows_cap == 0) {
+    if (amax_out != nullptr)
+      return cuda_status(cudaMemsetAsync(amax_out, 0, sizeof(float), (cudaStream_t)stream),
+                         "moe_gmm_fp8 amax reset");
+    return MOE_OK;
+  }
   moe::GmmF8Args a{A, lda, a_fmt, a_scale_inv, B, ldb, stride_b, b_fmt, b_scale_inv,
                    group_offsets, E, rows_cap, K, N, epilogue, aux, ld_aux, C, c_dtype, ldc,
-                   C2, ldc2, dev_status};
+                   C2, ldc2, amax_out, dev_status};
   return moe::launch_gmm_f8(a, (cudaStream_t)stream);
 }
 

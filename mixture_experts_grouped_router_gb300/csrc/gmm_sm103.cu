@@ -144,6 +144,7 @@ struct TcParams {
   const float *a_sinv;
   const float *b_sinv;
   int a_fmt, b_fmt;
+  float *amax_out;  // or null: max |value| of the bf16 output the epilogue writes
 };
 
 struct TileInfo {
@@ -319,20 +320,25 @@ MOE_DEVINL void issue_aux_load(OutMaps &om, uint8_t *stg, int nc, int wrow0) {
 // One tile's epilogue for the ragged-M GEMM.  Warp q owns tile rows
 // [32q, 32q+32), thread = one row; 32-column chunks.
 // Chunks [c_begin, c_end) of the tile's 32-column chunks are this warp's.
+// amx: the warp thread's running max |value| over the outputs it wrote
+// (Act for the SwiGLU forward, dH for the SwiGLU backward), when amax_out.
 template <int EPI, bool F8>
 MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t taddr, int q,
                              int lane, uint8_t *stg, OutMaps &om, volatile int *abort_flag,
-                             int c_begin, int c_end) {
+                             int c_begin, int c_end, float &amx) {
   // FP8: the accumulator holds code products; dequantize with both scales
   const float sc = F8 ? __ldg(p.a_sinv) * __ldg(p.b_sinv + ti.e) : 1.0f;
   const int wrow0 = ti.row0 + q * 32;
   const int64_t row = (int64_t)wrow0 + lane;
   const bool valid = row < ti.row_end;
   const bool bulk = wrow0 + 32 <= ti.row_end;  // every row of the block is this expert's
+  // FP8 GEMMs track their output amax and take no partial sum or bias; bf16
+  // ones the reverse (compile-time, so neither pays the other's registers)
+  const bool track = F8 && p.amax_out != nullptr && valid;
   if (EPI == MOE_EPI_SWIGLU_FWD) {
     const int F = p.F;
     const int n0 = ti.n_idx * (BN / 2);
-    const bool has_ps = valid && p.ps != nullptr;
+    const bool has_ps = !F8 && valid && p.ps != nullptr;
     auto load_ps = [&](int c, uint4 *g4, uint4 *u4) {
       const int nc = n0 + c * 32;
 #pragma unroll
@@ -374,7 +380,7 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
           pu[j] = nu[j];
         }
       }
-      if (p.bias != nullptr) {
+      if (!F8 && p.bias != nullptr) {
         const uint16_t *be = p.bias + (int64_t)ti.e * p.stride_bias;
 #pragma unroll
         for (int j8 = 0; j8 < 4; ++j8) {
@@ -392,6 +398,11 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
       }
 #pragma unroll
       for (int j = 0; j < 32; ++j) act[j] = g[j] * sigmoid_f(g[j]) * u[j];
+      if (track) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (nc + j < F) amx = fmaxf(amx, fabsf(act[j]));
+      }
       if (bulk) {
         stage_acquire(lane);
         stage_bf16(stg, lane, g);
@@ -454,6 +465,11 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
         dg[k] = v[k] * u[k] * sg * (1.0f + g[k] * (1.0f - sg));
         du[k] = v[k] * g[k] * sg;
       }
+      if (track) {
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+          if (nc + k < N) amx = fmaxf(amx, fmaxf(fabsf(dg[k]), fabsf(du[k])));
+      }
       if (bulk) {
         stage_acquire(lane);
         stage_bf16(stg, lane, dg);
@@ -480,7 +496,7 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
     const int n0 = ti.n_idx * BN;
     // in place (C is the fp32 partial sum): the TMA engine adds the block in L2
     const bool in_place = p.ps != nullptr && static_cast<const void *>(p.ps) == p.C;
-    const bool has_in = valid && p.ps != nullptr && !(in_place && bulk);
+    const bool has_in = !F8 && valid && p.ps != nullptr && !(in_place && bulk);
     auto load_chunk = [&](int c, uint4 *buf) {
       const int nc = n0 + c * 32;
 #pragma unroll
@@ -509,7 +525,7 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
 #pragma unroll
         for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
       }
-      if (p.bias != nullptr) {
+      if (!F8 && p.bias != nullptr) {
         const uint16_t *be = p.bias + (int64_t)ti.e * p.stride_bias;
 #pragma unroll
         for (int j8 = 0; j8 < 4; ++j8) {
@@ -520,6 +536,11 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
             for (int i = 0; i < 8; ++i) v[j8 * 8 + i] += bv[i];
           }
         }
+      }
+      if (track) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (nc + j < N) amx = fmaxf(amx, fabsf(v[j]));
       }
       if (bulk) {
         stage_acquire(lane);
@@ -886,6 +907,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     const int c_begin = ((warp - 2) >> 2) * kChunks;
     OutMaps om{&tmC0, &tmC1, &tmC2, &tmC3, &bk.aux_full[warp - 2], 0u, 0u};
     uint32_t acc_it = 0;
+    float amx = 0.0f;
     for (int t = cid; t < total; t += ncl) {
       const TileInfo ti = decode_tile<KIND, F8, AK>(bk, p, t, crank);
       if (KIND == KIND_TGMM && ti.kblocks == 0) {
@@ -902,7 +924,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       const uint32_t taddr = tmem + a * BN + (static_cast<uint32_t>(q * 32) << 16);
       if (KIND == KIND_GMM)
         epilogue_gmm<EPI, F8>(p, ti, taddr, q, lane, stg, om, abort_flag, c_begin,
-                              c_begin + kChunks);
+                              c_begin + kChunks, amx);
       else
         epilogue_tgmm<F8>(p, ti, taddr, q, lane, stg, om, false);
       tc::tc_fence_before();
@@ -912,6 +934,17 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         else tc::mbar_arrive(&bk.tempty[a]);
       }
       ++acc_it;
+    }
+    // the warp's output amax, once per kernel (bf16 rounding is monotone: the
+    // rounded maximum is the maximum of the rounded outputs)
+    if (KIND == KIND_GMM && F8 && p.amax_out != nullptr) {
+      amx = warp_max(amx);
+      if (lane == 0 && amx > 0.0f) {
+        const float r = p.c_f32 && EPI == MOE_EPI_NONE
+                            ? amx
+                            : __bfloat162float(__float2bfloat16_rn(amx));
+        atomicMax(reinterpret_cast<unsigned int *>(p.amax_out), __float_as_uint(r));
+      }
     }
     // every bulk store and H load of this warp has completed before the CTA exits
     if (lane == 0) tc::bulk_wait0();
@@ -1275,6 +1308,14 @@ moe_status_t launch_gmm_f8(const GmmF8Args &a, cudaStream_t s) {
   p.b_sinv = a.b_sinv;
   p.a_fmt = a.a_fmt;
   p.b_fmt = a.b_fmt;
+  p.amax_out = a.amax_out;
+  if (a.amax_out != nullptr) {
+    const cudaError_t e = cudaMemsetAsync(a.amax_out, 0, sizeof(float), s);
+    if (e != cudaSuccess) {
+      set_error("moe_gmm_fp8: amax reset: %s", cudaGetErrorString(e));
+      return MOE_ERR_CUDA;
+    }
+  }
   CUtensorMap mc[4];
   if (!gmm_out_maps(mc, a.epilogue, a.C, a.c_dtype, a.ldc, a.C2, a.ldc2, a.aux, a.ld_aux, a.N,
                     p.F, a.rows_cap)) {

@@ -105,6 +105,7 @@ struct GmmF8Args {
   const uint16_t *aux; int64_t ld_aux;
   void *C; int c_dtype; int64_t ldc;
   uint16_t *C2; int64_t ldc2;
+  float *amax_out;
   int32_t *dev_status;
 };
 moe_status_t launch_gmm_f8(const GmmF8Args &a, cudaStream_t s);

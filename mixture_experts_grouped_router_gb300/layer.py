@@ -139,9 +139,11 @@ def _fp8_slots(b):
                 wo=(a[4 + E:4 + 2 * E], v[4 + E:4 + 2 * E]))
 
 
-def _quant_act(b, name, x, fmt, q, qt, stream, mark):
+def _quant_act(b, name, x, fmt, q, qt, stream, mark, amax_done=False):
+    """amax_done: the GEMM that wrote x already left its amax in the slot."""
     amax, sinv = _fp8_slots(b)[name]
-    L.moe_fp8_amax(x, amax, group_offsets=b.group_offsets, E=b.s.E, stream=stream)
+    if not amax_done:
+        L.moe_fp8_amax(x, amax, group_offsets=b.group_offsets, E=b.s.E, stream=stream)
     L.moe_fp8_quantize_act(x, b.group_offsets, fmt, amax, q, qt, sinv, stream)
     mark("quant_" + name)
 
@@ -158,9 +160,9 @@ def _forward_fp8(b, x, logits, wi, wo, stream, mark):
         mark("quant_" + name)
     L.moe_gmm_fp8(b.xs_q, L.FP8_E4M3, sl["x"][1], b.wi_qt, L.FP8_E4M3, sl["wi"][1],
                   b.group_offsets, b.h, L.EPI_SWIGLU_FWD, C2=b.act, dev_status=b.dev_status,
-                  stream=stream)
+                  stream=stream, amax_out=sl["act"][0])
     mark("gmm_up_swiglu")
-    _quant_act(b, "act", b.act, L.FP8_E4M3, b.act_q, b.act_qt, stream, mark)
+    _quant_act(b, "act", b.act, L.FP8_E4M3, b.act_q, b.act_qt, stream, mark, amax_done=True)
     L.moe_gmm_fp8(b.act_q, L.FP8_E4M3, sl["act"][1], b.wo_qt, L.FP8_E4M3, sl["wo"][1],
                   b.group_offsets, b.y, dev_status=b.dev_status, stream=stream)
     mark("gmm_down")
@@ -172,12 +174,12 @@ def _backward_fp8(b, stream, mark):
     _quant_act(b, "dy", b.dy, L.FP8_E5M2, b.dy_q, b.dy_qt, stream, mark)
     L.moe_gmm_fp8(b.dy_q, L.FP8_E5M2, sl["dy"][1], b.wo_q, L.FP8_E4M3, sl["wo"][1],
                   b.group_offsets, b.dh, L.EPI_SWIGLU_BWD, aux=b.h, dev_status=b.dev_status,
-                  stream=stream)
+                  stream=stream, amax_out=sl["dh"][0])
     mark("gmm_dgrad_down_swiglu_bwd")
     L.moe_tgmm_fp8(b.act_qt, L.FP8_E4M3, sl["act"][1], b.dy_qt, L.FP8_E5M2, sl["dy"][1],
                    b.group_offsets, b.rows_cap, b.dwo, dev_status=b.dev_status, stream=stream)
     mark("tgmm_dwo")
-    _quant_act(b, "dh", b.dh, L.FP8_E5M2, b.dh_q, b.dh_qt, stream, mark)
+    _quant_act(b, "dh", b.dh, L.FP8_E5M2, b.dh_q, b.dh_qt, stream, mark, amax_done=True)
     L.moe_gmm_fp8(b.dh_q, L.FP8_E5M2, sl["dh"][1], b.wi_q, L.FP8_E4M3, sl["wi"][1],
                   b.group_offsets, b.dxs, dev_status=b.dev_status, stream=stream)
     mark("gmm_dgrad_up")
@@ -297,9 +299,9 @@ def kernels_per_step(s: LayerShape) -> int:
     aux = bool(s.aux_coeff)
     fwd = 1 + 3 + up + 1 + 1 + (2 if aux and s.T > 0 else 1 if aux else 0)
     bwd = 1 + 1 + 1 + 1 + 2 * up + 1 + (2 if s.bias else 0) + (1 if aux and s.T > 0 else 0)
-    if s.fp8:   # amax + quantize for x, wi, wo, act (forward) and dy, dh (backward)
-        fwd += 8
-        bwd += 4
+    if s.fp8:   # amax + quantize for x, wi, wo; quantize for act (amax in the GEMM);
+        fwd += 7   # amax + quantize for dy; quantize for dh
+        bwd += 3
     return fwd + bwd
 
 

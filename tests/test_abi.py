@@ -84,7 +84,7 @@ def test_validation_errors_need_no_gpu(L):
     assert st == L.MOE_ERR_INVALID_ARG and "leading dimension" in L.last_error()
     assert L.moe_fp8_padded_rows(100, 4) == 640 and L.moe_fp8_padded_rows(0, 1) == 128
     st = lib.moe_gmm_fp8(_ptr(), 64, 0, _ptr(), _ptr(), 24, 24 * 64, 0, _ptr(), _ptr(), 1, 100,
-                         24, 64, 0, None, 0, _ptr(), 0, 64, None, 0, None, None)
+                         24, 64, 0, None, 0, _ptr(), 0, 64, None, 0, None, None, None)
     assert st == L.MOE_ERR_UNSUPPORTED
     st = lib.moe_tgmm_fp8(_ptr(), 64, 0, _ptr(), _ptr(), 1024, 1, _ptr(), _ptr(), 4, 100, 64, 64,
                           _ptr(), 0, 64, 64 * 64, 0, None, None)

@@ -189,6 +189,35 @@ def test_gmm_fp8_none(case, fmts, transposed_weight):
     assert (C[R:].float() == 7.0).all()
 
 
+def test_gmm_fp8_epilogue_amax_is_the_outputs_amax():
+    """amax_out of the SwiGLU forward / backward / plain epilogues is max |.| of
+    the bf16 tensor the GEMM wrote (the amax that quantizes it next)."""
+    rng = np.random.default_rng(77)
+    off = _offsets(SIZES["mixed"])
+    E, R = len(SIZES["mixed"]), int(off[-1])
+    rows_cap = R + 5
+    K, F = 256, 192
+    offd = torch.from_numpy(off).cuda()
+    a_q, _, a_sinv, _ = _act_gpu(_bf(rng, (rows_cap, K), 2.0), off, 0)
+    _, w_qt, b_sinv, _ = _w_gpu(_bf(rng, (E, K, 2 * F), 0.05), 0)
+    H = torch.empty(rows_cap, 2 * F, dtype=torch.bfloat16, device="cuda")
+    Act = torch.full((rows_cap, F), 1e4, dtype=torch.bfloat16, device="cuda")
+    amax = torch.full((1,), -1.0, device="cuda")
+    L.moe_gmm_fp8(a_q, 0, a_sinv, w_qt, 0, b_sinv, offd, H, L.EPI_SWIGLU_FWD, C2=Act,
+                  amax_out=amax)
+    torch.cuda.synchronize()
+    assert float(amax.item()) == float(Act[:R].float().abs().max().item())
+    w_q, _, wsinv, _ = _w_gpu(_bf(rng, (E, F, K), 0.05), 1)
+    dH = torch.full((rows_cap, 2 * F), 1e4, dtype=torch.bfloat16, device="cuda")
+    L.moe_gmm_fp8(a_q, 0, a_sinv, w_q, 1, wsinv, offd, dH, L.EPI_SWIGLU_BWD, aux=H, amax_out=amax)
+    torch.cuda.synchronize()
+    assert float(amax.item()) == float(dH[:R].float().abs().max().item())
+    C = torch.full((rows_cap, F), 1e4, dtype=torch.bfloat16, device="cuda")
+    L.moe_gmm_fp8(a_q, 0, a_sinv, w_q, 1, wsinv, offd, C, amax_out=amax)
+    torch.cuda.synchronize()
+    assert float(amax.item()) == float(C[:R].float().abs().max().item())
+
+
 @pytest.mark.parametrize("sz,K,F", [("mixed", 256, 192), ("one", 512, 200), ("tiny", 128, 64)])
 def test_gmm_fp8_swiglu_fwd(sz, K, F):
     rng = np.random.default_rng(K + F)
