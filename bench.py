@@ -55,6 +55,24 @@ def gemm_source_hash():
     return h.hexdigest()[:16]
 
 
+def reduce_over_ranks(ms_total, ms_e2e, flops_step, dist, device):
+    """Replicas: the job's timed regions are the slowest rank's, its work the sum
+    of every rank's (whole-job throughput = summed work / max time)."""
+    import torch
+    if dist is None:
+        return ms_total, ms_e2e, flops_step
+    t = torch.tensor([ms_total, ms_e2e], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    f = torch.tensor([flops_step], device=device, dtype=torch.float64)
+    dist.all_reduce(f)
+    return float(t[0].item()), float(t[1].item()), float(f.item())
+
+
+def job_value(flops_job, steps, ms_total):
+    """Whole-job TFLOP/s of `steps` steps that took ms_total (max over ranks)."""
+    return flops_job * steps / (ms_total * 1e-3) / 1e12
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -339,23 +357,13 @@ def run_ours(args, cfg, ws, rank, local):
     d2h_bytes = sum(t.numel() * t.element_size() for t in hres[0].values())
 
     # ---- max over ranks
-    times = [ms_total, ms_e2e]
-    if dist is not None:
-        t = torch.tensor(times, device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        times = t.tolist()
-        flops_all = torch.tensor([flops_step], device=dev, dtype=torch.float64)
-        dist.all_reduce(flops_all)
-        flops_job = float(flops_all.item())
-    else:
-        flops_job = flops_step
-    ms_total, ms_e2e = times
+    ms_total, ms_e2e, flops_job = reduce_over_ranks(ms_total, ms_e2e, flops_step, dist, dev)
     if rank != 0:
         dist.destroy_process_group()
         return None
 
     ms_step = ms_total / args.steps
-    value = flops_job * args.steps / (ms_total * 1e-3) / 1e12
+    value = job_value(flops_job, args.steps, ms_total)
     tokens_s = cfg.T * ws * args.steps / (ms_total * 1e-3)
     pk, pk_kind = peaks()
     kernels = {}
