@@ -293,12 +293,13 @@ moe_status_t moe_transpose_act(const uint16_t *x, int64_t ldx, const int32_t *gr
 
 /*
  * moe_tgmm_kt -- moe_tgmm with A given as its column-wise copy At [M, ldat]
- * (moe_transpose_act of A); B bf16 [rows_cap, ldb] as in moe_tgmm.  Reading A
- * K-major feeds the tensor cores faster than the row-major A of moe_tgmm.
- * Same result, zeros for empty experts, same W arguments.
+ * (moe_transpose_act of A); B bf16 [rows_cap, ldb] as in moe_tgmm, or with
+ * b_colwise != 0 its column-wise copy Bt [N, ldb >= moe_fp8_padded_rows].
+ * Reading operands K-major feeds the tensor cores faster than the row-major
+ * operands of moe_tgmm.  Same result, zeros for empty experts, same W.
  */
 moe_status_t moe_tgmm_kt(const uint16_t *At, int64_t ldat, const uint16_t *B, int64_t ldb,
-                         const int32_t *group_offsets, int E, int64_t rows_cap, int M, int N,
+                         int b_colwise, const int32_t *group_offsets, int E, int64_t rows_cap, int M, int N,
                          void *W, int w_dtype, int64_t ldw, int64_t stride_w, int accumulate,
                          int32_t *dev_status, moe_stream_t stream);
 

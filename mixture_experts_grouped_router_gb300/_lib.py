@@ -82,8 +82,8 @@ _SIGS = {
                                   _P]),
     "moe_fp8_quantize_weights": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_transpose_act": (_I, [_P, _I64, _P, _I, _I64, _I, _P, _I64, _P]),
-    "moe_tgmm_kt": (_I, [_P, _I64, _P, _I64, _P, _I, _I64, _I, _I, _P, _I, _I64, _I64, _I, _P,
-                         _P]),
+    "moe_tgmm_kt": (_I, [_P, _I64, _P, _I64, _I, _P, _I, _I64, _I, _I, _P, _I, _I64, _I64, _I,
+                         _P, _P]),
     "moe_gmm_fp8": (_I, [_P, _I64, _I, _P, _P, _I64, _I64, _I, _P, _P, _I, _I64, _I, _I, _I, _P,
                          _I64, _P, _I, _I64, _P, _I64, _P, _P, _P]),
     "moe_tgmm_fp8": (_I, [_P, _I64, _I, _P, _P, _I64, _I, _P, _P, _I, _I64, _I, _I, _P, _I, _I64,
@@ -292,11 +292,13 @@ def moe_transpose_act(x, group_offsets, xt, stream=None):
 
 
 def moe_tgmm_kt(At, B, group_offsets, rows_cap, W, accumulate=False, dev_status=None,
-                stream=None):
-    """W [E, M, N] = per-expert A^T B with A given as its column-wise copy At [M, >=P]."""
+                stream=None, b_colwise=False):
+    """W [E, M, N] = per-expert A^T B with A given as its column-wise copy At [M, >=P];
+    B row-wise [rows_cap, N], or (b_colwise) its column-wise copy [N, >=P]."""
     E, M, N = W.shape
     w_dtype = DTYPE_F32 if W.dtype == torch.float32 else DTYPE_BF16
-    _check(LIB.moe_tgmm_kt(_ptr(At), _ld(At), _ptr(B), _ld(B), _ptr(group_offsets), E, rows_cap,
+    _check(LIB.moe_tgmm_kt(_ptr(At), _ld(At), _ptr(B), _ld(B), int(b_colwise),
+                           _ptr(group_offsets), E, rows_cap,
                            M, N, _ptr(W), w_dtype, W.stride(1), W.stride(0), int(accumulate),
                            _ptr(dev_status), _stream(stream)))
 

@@ -350,7 +350,7 @@ moe_status_t moe_transpose_act(const uint16_t *x, int64_t ldx, const int32_t *gr
 }
 
 moe_status_t moe_tgmm_kt(const uint16_t *At, int64_t ldat, const uint16_t *B, int64_t ldb,
-                         const int32_t *group_offsets, int E, int64_t rows_cap, int M, int N,
+                         int b_colwise, const int32_t *group_offsets, int E, int64_t rows_cap, int M, int N,
                          void *W, int w_dtype, int64_t ldw, int64_t stride_w, int accumulate,
                          int32_t *dev_status, moe_stream_t stream) {
   set_error("");
@@ -368,7 +368,8 @@ moe_status_t moe_tgmm_kt(const uint16_t *At, int64_t ldat, const uint16_t *B, in
           (long long)P);
   REQUIRE(N % 8 == 0 && ldb % 8 == 0 && ldw % 8 == 0, MOE_ERR_UNSUPPORTED,
           "moe_tgmm_kt: N, ldb, ldw must be multiples of 8");
-  REQUIRE(ldb >= N && ldw >= N, MOE_ERR_INVALID_ARG, "moe_tgmm_kt: leading dimension < N");
+  REQUIRE((b_colwise ? ldb >= P : ldb >= N) && ldw >= N, MOE_ERR_INVALID_ARG,
+          "moe_tgmm_kt: leading dimension too small");
   REQUIRE(stride_w >= (int64_t)M * ldw || E == 1, MOE_ERR_INVALID_ARG,
           "moe_tgmm_kt: stride_w overlaps experts");
   REQUIRE(group_offsets && W && (rows_cap == 0 || (At && B)), MOE_ERR_INVALID_ARG,
@@ -389,7 +390,7 @@ moe_status_t moe_tgmm_kt(const uint16_t *At, int64_t ldat, const uint16_t *B, in
   }
   moe::TgmmArgs a{nullptr, 0, B, ldb, group_offsets, E, rows_cap, M, N, W, w_dtype, ldw,
                   stride_w, accumulate, dev_status};
-  return moe::launch_tgmm_kt(a, At, ldat, (cudaStream_t)stream);
+  return moe::launch_tgmm_kt(a, At, ldat, b_colwise != 0, (cudaStream_t)stream);
 }
 
 moe_status_t moe_group_colsum(const uint16_t *G, int64_t ldg, const int32_t *group_offsets,

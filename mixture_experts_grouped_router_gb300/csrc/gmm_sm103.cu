@@ -727,10 +727,10 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             // expects the whole pair's stage
             const uint32_t fbl = tc::mapa_shared(tc::smem_u32(fb), 0);
             if (leader) tc::mbar_expect_tx(fb, 2 * kStageB);
-            if (KIND == KIND_TGMM && F8) {
+            if (KIND == KIND_TGMM && (F8 || (AK && !B_MN))) {
               // K-major column-wise copies: this CTA's 128 rows of A^T (output
               // rows) and of B^T (its half of the 256 output columns)
-              const int k = ti.row0 + kb * BKE;
+              const int k = ti.k0 + kb * BKE;
               tc::tma_load_2d_2sm(sa, &tmA, fbl, k, ti.m_idx * BM);
               tc::tma_load_2d_2sm(sb, &tmB, fbl, k, ti.n_idx * BN + crank * (BN / 2));
             } else if (KIND == KIND_TGMM && AK) {
@@ -832,7 +832,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         tc::tc_fence_after();
         uint8_t *sa = smem + s * kStageB;
         uint8_t *sb = sa + A_BYTES;
-        if (KIND == KIND_TGMM && !F8) {
+        if (KIND == KIND_TGMM && !F8 && (!AK || B_MN)) {
           // rows past the expert's last row belong to the next expert: zero
           // them in both operands (one 128-byte row per K index per box).
           // 2-SM: this CTA's four boxes and the same four in the partner
@@ -858,16 +858,19 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
           __syncwarp();
         }
         if (lane == 0) {
-          const uint32_t a_base = tc::smem_u32(sa);
-          const uint32_t b_base = tc::smem_u32(sb);
+          // descriptors of the stage's first MMA; the kk-th MMA starts 32 bytes
+          // further along the row (K-major: 16 bf16 or 32 codes) or 16 rows of
+          // 128 bytes further (MN-major), i.e. 2 or 128 in the address field
+          const uint64_t ad0 = A_MN ? tc::sdesc(tc::smem_u32(sa), BOX_BYTES, 1024)
+                                    : tc::sdesc(tc::smem_u32(sa), 16, 1024);
+          const uint64_t bd0 = B_MN ? tc::sdesc(tc::smem_u32(sb), BOX_BYTES, 1024)
+                                    : tc::sdesc(tc::smem_u32(sb), 16, 1024);
+          constexpr uint64_t kAStep = A_MN ? (UK * 128) >> 4 : 32 >> 4;
+          constexpr uint64_t kBStep = B_MN ? (UK * 128) >> 4 : 32 >> 4;
 #pragma unroll
           for (int kk = 0; kk < BK / UK; ++kk) {
-            // K-major: the kk-th MMA starts 32 bytes further along the row
-            // (16 bf16 or 32 codes); MN-major: 16 rows of 128 bytes further
-            const uint64_t ad = A_MN ? tc::sdesc(a_base + kk * UK * 128, BOX_BYTES, 1024)
-                                     : tc::sdesc(a_base + kk * 32, 16, 1024);
-            const uint64_t bd = B_MN ? tc::sdesc(b_base + kk * UK * 128, BOX_BYTES, 1024)
-                                     : tc::sdesc(b_base + kk * 32, 16, 1024);
+            const uint64_t ad = ad0 + kk * kAStep;
+            const uint64_t bd = bd0 + kk * kBStep;
             if (F8) {
               if (k2SM) tc::umma_f8_2sm(d_tmem, ad, bd, IDESC, (kb | kk) != 0);
               else tc::umma_f8(d_tmem, ad, bd, IDESC, (kb | kk) != 0);
@@ -1159,7 +1162,7 @@ moe_status_t launch_gmm(const GmmArgs &a, cudaStream_t s) {
 // At == nullptr: A read as stored (MN-major); else K-major from its
 // column-wise copy At [M, ldat] (zero-padded group layout).
 static moe_status_t tgmm_impl(const TgmmArgs &a, const uint16_t *At, int64_t ldat,
-                              cudaStream_t s) {
+                              bool b_colwise, cudaStream_t s) {
   if (a.E > kMaxE) {
     set_error("moe_tgmm: E=%d > %d", a.E, kMaxE);
     return MOE_ERR_UNSUPPORTED;
@@ -1182,7 +1185,15 @@ static moe_status_t tgmm_impl(const TgmmArgs &a, const uint16_t *At, int64_t lda
       return MOE_ERR_CUDA;
     }
   }
-  {
+  if (b_colwise) {
+    const uint64_t dims[2] = {(uint64_t)f8_padded_rows(a.rows_cap, a.E), (uint64_t)a.N};
+    const uint64_t st[1] = {(uint64_t)a.ldb * 2};
+    const uint32_t bbox[2] = {BK, BN / 2};
+    if (!make_map(&mb, a.B, 2, dims, st, bbox)) {
+      set_error("moe_tgmm: cannot encode the TMA descriptor of B");
+      return MOE_ERR_CUDA;
+    }
+  } else {
     const uint64_t dims[2] = {(uint64_t)a.N, (uint64_t)a.rows_cap};
     const uint64_t st[1] = {(uint64_t)a.ldb * 2};
     if (!make_map(&mb, a.B, 2, dims, st, box)) {
@@ -1223,15 +1234,20 @@ static moe_status_t tgmm_impl(const TgmmArgs &a, const uint16_t *At, int64_t lda
     mc[1] = mc[2] = mc[3] = mc[0];
   }
   const int64_t tiles_upper = (int64_t)a.E * p.m_tiles * p.n_tiles;
+  if (At != nullptr && b_colwise)
+    return launch_tc<KIND_TGMM, false, MOE_EPI_NONE, false, true>(ma, mb, mc, p, tiles_upper, s);
   if (At != nullptr)
     return launch_tc<KIND_TGMM, true, MOE_EPI_NONE, false, true>(ma, mb, mc, p, tiles_upper, s);
   return launch_tc<KIND_TGMM, true, MOE_EPI_NONE>(ma, mb, mc, p, tiles_upper, s);
 }
 
-moe_status_t launch_tgmm(const TgmmArgs &a, cudaStream_t s) { return tgmm_impl(a, nullptr, 0, s); }
+moe_status_t launch_tgmm(const TgmmArgs &a, cudaStream_t s) {
+  return tgmm_impl(a, nullptr, 0, false, s);
+}
 
-moe_status_t launch_tgmm_kt(const TgmmArgs &a, const uint16_t *At, int64_t ldat, cudaStream_t s) {
-  return tgmm_impl(a, At, ldat, s);
+moe_status_t launch_tgmm_kt(const TgmmArgs &a, const uint16_t *At, int64_t ldat, bool b_colwise,
+                            cudaStream_t s) {
+  return tgmm_impl(a, At, ldat, b_colwise, s);
 }
 
 // Output maps shared by the bf16 and FP8 ragged-M GEMMs (unused slots repeat

@@ -93,7 +93,8 @@ struct TgmmArgs {
 };
 moe_status_t launch_tgmm(const TgmmArgs &a, cudaStream_t s);
 // the same with A read K-major from its column-wise copy At [M, ldat]
-moe_status_t launch_tgmm_kt(const TgmmArgs &a, const uint16_t *At, int64_t ldat, cudaStream_t s);
+moe_status_t launch_tgmm_kt(const TgmmArgs &a, const uint16_t *At, int64_t ldat, bool b_colwise,
+                            cudaStream_t s);
 
 // FP8 (8-bit float codes, K-major operands, fp32 accumulation; the epilogue
 // multiplies by the scales' inverses)

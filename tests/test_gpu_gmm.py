@@ -199,7 +199,8 @@ def test_transpose_act_padded(sz, cols):
 
 @pytest.mark.parametrize("sz,M,N", TGMM_CASES)
 @pytest.mark.parametrize("mode", ["bf16", "f32", "f32_acc"])
-def test_tgmm_kt(sz, M, N, mode):
+@pytest.mark.parametrize("b_colwise", [False, True])
+def test_tgmm_kt(sz, M, N, mode, b_colwise):
     rng = np.random.default_rng(M * 7 + N)
     off = _offsets(SIZES[sz])
     E, R = len(SIZES[sz]), int(off[-1])
@@ -219,7 +220,13 @@ def test_tgmm_kt(sz, M, N, mode):
     if mode == "f32_acc":
         init = rng.standard_normal((E, M, N)).astype(np.float32)
         W.copy_(torch.from_numpy(init))
-    L.moe_tgmm_kt(At, B, offd, rows_cap, W, accumulate=mode == "f32_acc")
+    if b_colwise:
+        Bt = torch.empty(N, L.moe_fp8_padded_rows(rows_cap, E), dtype=torch.bfloat16,
+                         device="cuda")
+        L.moe_transpose_act(B, offd, Bt)
+        L.moe_tgmm_kt(At, Bt, offd, rows_cap, W, accumulate=mode == "f32_acc", b_colwise=True)
+    else:
+        L.moe_tgmm_kt(At, B, offd, rows_cap, W, accumulate=mode == "f32_acc")
     torch.cuda.synchronize()
     a64 = moe_synth.bits_to_f64(a_bits)
     b64 = moe_synth.bits_to_f64(b_bits)
