@@ -94,15 +94,15 @@ struct Book {
 // CTA's 128-row (tgmm: 128-column) A tile and half of the B tile (32 KB), 6
 // stages, 4 epilogue warps.  The SwiGLU-backward dgrad, whose epilogue (H
 // reads, two outputs) is the longest, runs 8 epilogue warps (two per TMEM
-// lane quarter, each on half of the tile's columns) and 4 stages; on 8-bit
-// codes it keeps whole B tiles multicast within the pair (48 KB stages, 3 of
-// them), which measured faster there.
+// lane quarter, each on half of the tile's columns) and 5 stages.  (The
+// multicast CTA-pair form, whole B tiles in 48 KB stages, is kept for kernels
+// that set two_sm false.)
 template <int KIND, int EPI, bool F8>
 struct Ring {
   static constexpr bool swiglu_bwd = KIND == 0 && EPI == MOE_EPI_SWIGLU_BWD;
-  static constexpr bool two_sm = !(swiglu_bwd && F8);
+  static constexpr bool two_sm = true;
   static constexpr int epi_warps = swiglu_bwd ? 8 : 4;
-  static constexpr int stages = two_sm ? (swiglu_bwd ? 4 : 6) : 3;
+  static constexpr int stages = two_sm ? (swiglu_bwd ? 5 : 6) : 3;
   static constexpr int b_bytes = two_sm ? B_BYTES / 2 : B_BYTES;
   static constexpr int stage_bytes = A_BYTES + b_bytes;
   static constexpr int threads = 64 + 32 * epi_warps;  // producer, MMA, epilogue
