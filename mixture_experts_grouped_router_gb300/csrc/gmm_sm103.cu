@@ -841,16 +841,18 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
           // (AK: A's copy is zero past the rows already; only B's boxes)
           const int valid = ti.row_end - (ti.row0 + kb * BK);
           if (valid < BK) {
+            // lane = (row phase, 16-byte chunk): 4 rows per step, every box
+            constexpr int kBox0 = AK ? 2 : 0;
             constexpr int kBoxes = AK ? 2 : (k2SM ? 4 : 6);
-            const int nrows = BK - valid;
-            for (int i = lane; i < nrows * kBoxes * 8; i += 32) {
-              const int chunk = i & 7;
-              const int rr = valid + ((i >> 3) % nrows);
-              const int box = (i >> 3) / nrows + (AK ? 2 : 0);
-              uint8_t *base = box < 2 ? sa + box * BOX_BYTES : sb + (box - 2) * BOX_BYTES;
-              uint8_t *at = base + rr * 128 + chunk * 16;
-              *reinterpret_cast<uint4 *>(at) = make_uint4(0, 0, 0, 0);
-              if (k2SM) tc::st_cluster_zero16(tc::mapa_shared(tc::smem_u32(at), 1));
+            const int chunk = lane & 7;
+            for (int rr = valid + (lane >> 3); rr < BK; rr += 4) {
+#pragma unroll
+              for (int box = kBox0; box < kBox0 + kBoxes; ++box) {
+                uint8_t *base = box < 2 ? sa + box * BOX_BYTES : sb + (box - 2) * BOX_BYTES;
+                const uint32_t off = rr * 128 + chunk * 16;
+                *reinterpret_cast<uint4 *>(base + off) = make_uint4(0, 0, 0, 0);
+                if (k2SM) tc::st_cluster_zero16(tc::mapa_shared(tc::smem_u32(base), 1) + off);
+              }
             }
             tc::fence_proxy_async_smem();
             if (k2SM) tc::fence_proxy_async_smem_cluster();
