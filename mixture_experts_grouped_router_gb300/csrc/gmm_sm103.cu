@@ -709,12 +709,12 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   uint32_t issued = 0;  // producer: k-blocks issued (ring position)
   if (warp == 0) {
     if (lane == 0 && !p.stall_loads) {
+      int s = 0;         // ring slot of the next K block
+      uint32_t ph = 0;   // its pass over the ring (parity)
       for (int t = cid; t < total; t += ncl) {
         const TileInfo ti = decode_tile<KIND, F8, AK>(bk, p, t, crank);
         bool ok = true;
         for (int kb = 0; kb < ti.kblocks; ++kb) {
-          const int s = issued % kSt;
-          const uint32_t ph = (issued / kSt) & 1;
           if (!tc::mbar_wait(&bk.empty[s], ph ^ 1, abort_flag, p.wait_limit_ns)) {
             ok = false;
             break;
@@ -799,6 +799,10 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             }
           }
           ++issued;
+          if (++s == kSt) {
+            s = 0;
+            ph ^= 1;
+          }
         }
         if (!ok) break;
       }
@@ -812,7 +816,9 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   } else if (warp == 1 && (!k2SM || leader)) {
     const uint32_t IDESC = F8 ? tc::idesc_f8(k2SM ? 2 * BM : BM, BN, p.a_fmt, p.b_fmt)
                               : tc::idesc_bf16(k2SM ? 2 * BM : BM, BN, A_MN, B_MN);
-    uint32_t it = 0, acc_it = 0;
+    uint32_t acc_it = 0;
+    int s = 0;         // ring slot of the next K block
+    uint32_t ph = 0;   // its pass over the ring (parity)
     bool ok = true;
     for (int t = cid; t < total && ok; t += ncl) {
       const TileInfo ti = decode_tile<KIND, F8, AK>(bk, p, t, crank);
@@ -823,8 +829,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       tc::tc_fence_after();
       const uint32_t d_tmem = tmem + a * BN;
       for (int kb = 0; kb < ti.kblocks; ++kb) {
-        const int s = it % kSt;
-        const uint32_t ph = (it / kSt) & 1;
+
         if (!tc::mbar_wait_warp(&bk.full[s], ph, abort_flag, p.wait_limit_ns)) {
           ok = false;
           break;
@@ -886,7 +891,10 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
           else tc::umma_commit_mc(&bk.empty[s], kPair);
         }
         __syncwarp();
-        ++it;
+        if (++s == kSt) {
+          s = 0;
+          ph ^= 1;
+        }
       }
       if (!ok) break;
       if (lane == 0) {
