@@ -15,6 +15,10 @@ MOE_DEVINL void moe_set_status(int32_t *status, int code) {
   if (status != nullptr) atomicCAS(status, 0, code);
 }
 
+// Programmatic dependent launch: wait until the grids this one depends on
+// have completed and their writes are visible (a no-op for a plain launch).
+MOE_DEVINL void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 MOE_DEVINL float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

@@ -72,6 +72,7 @@ permute_rank_kernel(const int32_t *__restrict__ topk_idx, int T, int E, int k, i
   __shared__ int32_t pre[kRankWarps][kMaxE];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = blockIdx.x;
+  grid_dependency_wait();  // the counts of the previous kernel
 
   // 1. this block's base and the totals, from the count blocks
   for (int e = tid; e < E; e += kRankThreads) {
@@ -200,6 +201,7 @@ permute_gather_kernel(const uint16_t *__restrict__ x, int64_t ldx,
   const int lane = threadIdx.x & 31;
   const int wib = threadIdx.x >> 5;
   const int nvec = d >> 3;
+  grid_dependency_wait();  // the layout of the rank kernel
   if ((int)blockIdx.x < nb_tok) {
     const int t = blockIdx.x * (kGatherThreads / 32) + wib;
     if (t >= T) return;
@@ -272,23 +274,40 @@ cudaError_t launch_permute(const uint16_t *x, int64_t ldx, const int32_t *topk_i
     cudaError_t e = cudaMemsetAsync(counts_ws, 0, sizeof(int32_t) * E, s);
     if (e != cudaSuccess) return e;
   }
-  permute_rank_kernel<<<nb, kRankThreads, 0, s>>>(topk_idx, T, E, k, align, capacity, tpb,
-                                                  counts_ws, nb, rows_cap, group_sizes, kept,
-                                                  offsets, s2f, f2s, dev_status);
+  // the rank and gather kernels launch while their predecessor finishes and
+  // wait for its results in their first instruction (programmatic dependent
+  // launch), which hides the launch gaps of this three-kernel chain
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = s;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(nb);
+  cfg.blockDim = dim3(kRankThreads);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, permute_rank_kernel, topk_idx, T, E, k, align,
+                                     capacity, tpb, (const int32_t *)counts_ws, nb, rows_cap,
+                                     group_sizes, kept, offsets, s2f, f2s, dev_status);
+  if (e != cudaSuccess) return e;
   const int wpb = kGatherThreads / 32;
   const int nb_tok = (T + wpb - 1) / wpb;
   const int64_t pad_warps = (rows_cap + 31) / 32;
   const int nb_pad = (int)((pad_warps + wpb - 1) / wpb);
   if (nb_tok + nb_pad > 0) {
-#define MOE_GATHER(KT)                                                                    \
-  permute_gather_kernel<KT><<<nb_tok + nb_pad, kGatherThreads, 0, s>>>(                   \
-      x, ldx, f2s, T, k, d, xs, ld_xs, s2f, offsets, E, rows_cap, nb_tok, dev_status)
+    cfg.gridDim = dim3(nb_tok + nb_pad);
+    cfg.blockDim = dim3(kGatherThreads);
+#define MOE_GATHER(KT)                                                                      \
+  e = cudaLaunchKernelEx(&cfg, permute_gather_kernel<KT>, x, ldx, (const int32_t *)f2s, T, k, d, \
+                         xs, ld_xs, (const int32_t *)s2f, (const int32_t *)offsets, E,          \
+                         rows_cap, nb_tok, dev_status)
     if (k <= 1) MOE_GATHER(1);
     else if (k <= 2) MOE_GATHER(2);
     else if (k <= 4) MOE_GATHER(4);
     else if (k <= 8) MOE_GATHER(8);
     else MOE_GATHER(16);
 #undef MOE_GATHER
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }
