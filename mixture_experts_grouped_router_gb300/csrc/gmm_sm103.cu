@@ -11,28 +11,30 @@
 // moe_tgmm (ragged K): W_e = A_e^T B_e over the rows of expert e; an expert
 //          without rows gets exact zeros (MaxText PR #4295, Testing).
 //
-// Design (persistent, one CTA per SM, CTAs in clusters of two that take
-// adjacent 128-row tiles of the same expert and 256-column tile; 192 threads,
-// warp-specialised):
-//   warp 0      TMA producer.  Forward / dgrad GEMMs: 2-SM MMA pairs; each
-//               CTA loads its own 128x64 A tile and its half (128 columns) of
-//               the 256x64 B tile, both completing on the leader CTA's
-//               barrier (6 stages of 32 KB).  Weight-gradient GEMM and the
-//               SwiGLU-backward dgrad: each CTA loads its A tile and half of
-//               the B tile multicast into both CTAs (4 stages of 48 KB).
-//               128-byte swizzle throughout.
-//   warp 1      TMEM owner and MMA issuer: tcgen05.mma kind::f16, K=16, fp32
-//               accumulators in TMEM (two 256-column accumulators so that the
-//               epilogue of one tile overlaps the mainloop of the next); 2-SM
-//               kernels issue cta_group::2 MMAs (M=256) from the leader CTA.
-//               Stages are released in both CTAs by multicast commits.
-//   warps 2-5   epilogue: tcgen05.ld of one TMEM lane (= one output row) per
-//               thread, fused SwiGLU / partial-sum / cast; each warp stages
-//               its 32x32 output blocks in swizzled shared memory and writes
-//               them with TMA bulk stores (bulk reduce-add for fp32 partial
-//               sums), so that outputs leave as whole lines and never contend
-//               with the mainloop's operand loads (a block that straddles the
-//               expert's last row is written with plain stores instead).
+// Design (persistent, one CTA per SM, CTAs in clusters of two whose pair
+// issues 2-SM MMAs (tcgen05 cta_group::2, M = 256) on adjacent 128-row tiles
+// of the same expert and one 256-column tile; warp-specialised):
+//   warp 0      TMA producer: each CTA loads its own 128-row A tile and its
+//               half (128 columns) of the B tile for every K block, both
+//               completing on the leader CTA's barrier (32 KB per CTA and
+//               stage, 6 stages; 5 for the SwiGLU-backward dgrad).  128-byte
+//               swizzle throughout; a K block is one 128-byte row per tile
+//               row (64 bf16 or 128 8-bit codes).
+//   warp 1      TMEM owner; in the leader CTA the MMA issuer: kind::f16
+//               (bf16) or kind::f8f6f4 (E4M3 / E5M2 codes), fp32 accumulators
+//               in TMEM (two 256-column accumulators so that the epilogue of
+//               one tile overlaps the mainloop of the next).  Stages and
+//               finished accumulators are signalled to both CTAs by
+//               multicast commits.
+//   warps 2-5   epilogue (2-9 for the SwiGLU backward: two warps per TMEM
+//               lane quarter, each on half of the columns): tcgen05.ld of one
+//               TMEM lane (= one output row) per thread, fused SwiGLU /
+//               partial-sum / bias / FP8-dequantization / cast; each warp
+//               stages its 32x32 output blocks in swizzled shared memory and
+//               writes them with TMA bulk stores (bulk reduce-add for fp32
+//               partial sums), so that outputs leave as whole lines and never
+//               contend with the mainloop's operand loads (a block that
+//               straddles the expert's last row is written with plain stores).
 // Tiles never straddle two experts.  The tile list is derived on the device
 // from group_offsets (no host synchronisation); tiles are visited expert by
 // expert in groups of 32 row tiles so that concurrently running CTAs share
@@ -90,20 +92,17 @@ struct Book {
   uint16_t poff[kMaxE + 1];
 };
 
-// Per-kernel layout.  The GEMMs run as 2-SM MMAs whose stage holds this
+// Per-kernel layout.  Every GEMM runs as 2-SM MMAs whose stage holds this
 // CTA's 128-row (tgmm: 128-column) A tile and half of the B tile (32 KB), 6
 // stages, 4 epilogue warps.  The SwiGLU-backward dgrad, whose epilogue (H
 // reads, two outputs) is the longest, runs 8 epilogue warps (two per TMEM
-// lane quarter, each on half of the tile's columns) and 5 stages.  (The
-// multicast CTA-pair form, whole B tiles in 48 KB stages, is kept for kernels
-// that set two_sm false.)
+// lane quarter, each on half of the tile's columns) and 5 stages.
 template <int KIND, int EPI, bool F8>
 struct Ring {
   static constexpr bool swiglu_bwd = KIND == 0 && EPI == MOE_EPI_SWIGLU_BWD;
-  static constexpr bool two_sm = true;
   static constexpr int epi_warps = swiglu_bwd ? 8 : 4;
-  static constexpr int stages = two_sm ? (swiglu_bwd ? 5 : 6) : 3;
-  static constexpr int b_bytes = two_sm ? B_BYTES / 2 : B_BYTES;
+  static constexpr int stages = swiglu_bwd ? 5 : 6;
+  static constexpr int b_bytes = B_BYTES / 2;
   static constexpr int stage_bytes = A_BYTES + b_bytes;
   static constexpr int threads = 64 + 32 * epi_warps;  // producer, MMA, epilogue
   static constexpr int stg_offset = stages * stage_bytes;  // 1024-aligned
@@ -618,7 +617,6 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   const int cid = (int)tc::cluster_id_x();
   const int ncl = (int)tc::nclusters_x();
   constexpr uint16_t kPair = 0x3;
-  constexpr bool k2SM = Ring<KIND, EPI, F8>::two_sm;
   constexpr int kSt = Ring<KIND, EPI, F8>::stages;
   constexpr int kStageB = Ring<KIND, EPI, F8>::stage_bytes;
   constexpr int BKE = Elem<F8>::BKE;
@@ -633,12 +631,12 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       tc::mbar_init(&bk.full[s], 1);
       // 2-SM: the leader's MMA commit releases a stage in both CTAs once;
       // else both CTAs' MMA warps release it
-      tc::mbar_init(&bk.empty[s], k2SM ? 1 : 2);
+      tc::mbar_init(&bk.empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       tc::mbar_init(&bk.tfull[a], 1);
       // 2-SM: the leader's accumulator is free once both CTAs' epilogues are done
-      tc::mbar_init(&bk.tempty[a], k2SM ? 2 * kEW : kEW);
+      tc::mbar_init(&bk.tempty[a], 2 * kEW);
     }
     tc::mbar_init(&bk.drain, 1);
     for (int w = 0; w < kEW; ++w) tc::mbar_init(&bk.aux_full[w], 1);
@@ -691,13 +689,8 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       if (group_offset(p, e + 1) < group_offset(p, e)) moe_set_status(p.dev_status, MOE_ERR_DEVICE);
   }
   if (warp == 1) {
-    if (k2SM) {
-      tc::tmem_alloc_2sm(&bk.tmem_base, kTmemCols);
-      tc::tmem_relinquish_2sm();
-    } else {
-      tc::tmem_alloc(&bk.tmem_base, kTmemCols);
-      tc::tmem_relinquish();
-    }
+    tc::tmem_alloc_2sm(&bk.tmem_base, kTmemCols);
+    tc::tmem_relinquish_2sm();
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -722,36 +715,35 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
           uint8_t *sa = smem + s * kStageB;
           uint8_t *sb = sa + A_BYTES;
           uint64_t *fb = &bk.full[s];
-          if (k2SM) {
-            // both CTAs' copies complete on the leader's full barrier, which
-            // expects the whole pair's stage
-            const uint32_t fbl = tc::mapa_shared(tc::smem_u32(fb), 0);
-            if (leader) tc::mbar_expect_tx(fb, 2 * kStageB);
-            if (KIND == KIND_TGMM && (F8 || (AK && !B_MN))) {
-              // K-major column-wise copies: this CTA's 128 rows of A^T (output
-              // rows) and of B^T (its half of the 256 output columns)
-              const int k = ti.k0 + kb * BKE;
-              tc::tma_load_2d_2sm(sa, &tmA, fbl, k, ti.m_idx * BM);
-              tc::tma_load_2d_2sm(sb, &tmB, fbl, k, ti.n_idx * BN + crank * (BN / 2));
-            } else if (KIND == KIND_TGMM && AK) {
-              // K-major A from the column-wise copy (zero padded past the
-              // expert's rows); MN-major B rows as stored (tail zeroed below)
-              const int r = ti.row0 + kb * BKE;
-              const int nb = ti.n_idx * BN + crank * (BN / 2);
-              tc::tma_load_2d_2sm(sa, &tmA, fbl, ti.k0 + kb * BKE, ti.m_idx * BM);
-              tc::tma_load_2d_2sm(sb, &tmB, fbl, nb, r);
-              tc::tma_load_2d_2sm(sb + BOX_BYTES, &tmB, fbl, nb + 64, r);
-            } else if (KIND == KIND_TGMM) {
-              // this CTA's 128 output rows of A (two 64-column boxes) and its
-              // 128 columns of B, both over the K block's 64 rows
-              const int r = ti.row0 + kb * BK;
-              const int m0 = ti.m_idx * BM;
-              const int nb = ti.n_idx * BN + crank * (BN / 2);
-              tc::tma_load_2d_2sm(sa, &tmA, fbl, m0, r);
-              tc::tma_load_2d_2sm(sa + BOX_BYTES, &tmA, fbl, m0 + 64, r);
-              tc::tma_load_2d_2sm(sb, &tmB, fbl, nb, r);
-              tc::tma_load_2d_2sm(sb + BOX_BYTES, &tmB, fbl, nb + 64, r);
-            } else {
+          // both CTAs' copies complete on the leader's full barrier, which
+          // expects the whole pair's stage
+          const uint32_t fbl = tc::mapa_shared(tc::smem_u32(fb), 0);
+          if (leader) tc::mbar_expect_tx(fb, 2 * kStageB);
+          if (KIND == KIND_TGMM && (F8 || (AK && !B_MN))) {
+            // K-major column-wise copies: this CTA's 128 rows of A^T (output
+            // rows) and of B^T (its half of the 256 output columns)
+            const int k = ti.k0 + kb * BKE;
+            tc::tma_load_2d_2sm(sa, &tmA, fbl, k, ti.m_idx * BM);
+            tc::tma_load_2d_2sm(sb, &tmB, fbl, k, ti.n_idx * BN + crank * (BN / 2));
+          } else if (KIND == KIND_TGMM && AK) {
+            // K-major A from the column-wise copy (zero padded past the
+            // expert's rows); MN-major B rows as stored (tail zeroed below)
+            const int r = ti.row0 + kb * BKE;
+            const int nb = ti.n_idx * BN + crank * (BN / 2);
+            tc::tma_load_2d_2sm(sa, &tmA, fbl, ti.k0 + kb * BKE, ti.m_idx * BM);
+            tc::tma_load_2d_2sm(sb, &tmB, fbl, nb, r);
+            tc::tma_load_2d_2sm(sb + BOX_BYTES, &tmB, fbl, nb + 64, r);
+          } else if (KIND == KIND_TGMM) {
+            // this CTA's 128 output rows of A (two 64-column boxes) and its
+            // 128 columns of B, both over the K block's 64 rows
+            const int r = ti.row0 + kb * BK;
+            const int m0 = ti.m_idx * BM;
+            const int nb = ti.n_idx * BN + crank * (BN / 2);
+            tc::tma_load_2d_2sm(sa, &tmA, fbl, m0, r);
+            tc::tma_load_2d_2sm(sa + BOX_BYTES, &tmA, fbl, m0 + 64, r);
+            tc::tma_load_2d_2sm(sb, &tmB, fbl, nb, r);
+            tc::tma_load_2d_2sm(sb + BOX_BYTES, &tmB, fbl, nb + 64, r);
+          } else {
             tc::tma_load_2d_2sm(sa, &tmA, fbl, kb * BKE, ti.row0);
             if (B_MN) {
               // this CTA's 128 columns of B: two 64-column boxes
@@ -772,31 +764,6 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                                    : ti.n_idx * BN + crank * (BN / 2);
               tc::tma_load_3d_2sm(sb, &tmB, fbl, kb * BKE, nrow, ti.e);
             }
-            }
-          } else {
-            tc::mbar_expect_tx(fb, kStageB);
-            // own A tile; this CTA's half of the shared B tile, multicast to the pair
-            if (KIND == KIND_GMM) {
-              tc::tma_load_2d(sa, &tmA, fb, kb * BKE, ti.row0);
-              if (B_MN) {
-                const int n0 = ti.n_idx * BN;
-#pragma unroll
-                for (int i = 2 * crank; i < 2 * crank + 2; ++i)
-                  tc::tma_load_3d_mc(sb + i * BOX_BYTES, &tmB, fb, n0 + 64 * i, kb * BKE, ti.e, kPair);
-              } else {
-                tc::tma_load_3d_mc(sb + crank * (B_BYTES / 2), &tmB, fb, kb * BKE,
-                                   ti.n_idx * BN + crank * (BN / 2), ti.e, kPair);
-              }
-            } else {
-              const int r = ti.row0 + kb * BK;
-              const int m0 = ti.m_idx * BM;
-              const int n0 = ti.n_idx * BN;
-              tc::tma_load_2d(sa, &tmA, fb, m0, r);
-              tc::tma_load_2d(sa + BOX_BYTES, &tmA, fb, m0 + 64, r);
-#pragma unroll
-              for (int i = 2 * crank; i < 2 * crank + 2; ++i)
-                tc::tma_load_2d_mc(sb + i * BOX_BYTES, &tmB, fb, n0 + 64 * i, r, kPair);
-            }
           }
           ++issued;
           if (++s == kSt) {
@@ -809,13 +776,13 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       // drain: every issued copy has landed before the CTA may exit
       // (2-SM: a CTA's copies complete on the leader's barrier; the leader's
       // MMA consumed them all before the pair's final cluster barrier)
-      if (!k2SM || leader)
+      if (leader)
         for (uint32_t i = issued > (uint32_t)kSt ? issued - kSt : 0; i < issued; ++i)
           tc::mbar_wait_drain(&bk.full[i % kSt], (i / kSt) & 1, p.wait_limit_ns / 4);
     }
-  } else if (warp == 1 && (!k2SM || leader)) {
-    const uint32_t IDESC = F8 ? tc::idesc_f8(k2SM ? 2 * BM : BM, BN, p.a_fmt, p.b_fmt)
-                              : tc::idesc_bf16(k2SM ? 2 * BM : BM, BN, A_MN, B_MN);
+  } else if (warp == 1 && leader) {
+    const uint32_t IDESC = F8 ? tc::idesc_f8(2 * BM, BN, p.a_fmt, p.b_fmt)
+                              : tc::idesc_bf16(2 * BM, BN, A_MN, B_MN);
     uint32_t acc_it = 0;
     int s = 0;         // ring slot of the next K block
     uint32_t ph = 0;   // its pass over the ring (parity)
@@ -848,7 +815,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
           if (valid < BK) {
             // lane = (row phase, 16-byte chunk): 4 rows per step, every box
             constexpr int kBox0 = AK ? 2 : 0;
-            constexpr int kBoxes = AK ? 2 : (k2SM ? 4 : 6);
+            constexpr int kBoxes = AK ? 2 : 4;
             const int chunk = lane & 7;
             for (int rr = valid + (lane >> 3); rr < BK; rr += 4) {
 #pragma unroll
@@ -856,11 +823,11 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                 uint8_t *base = box < 2 ? sa + box * BOX_BYTES : sb + (box - 2) * BOX_BYTES;
                 const uint32_t off = rr * 128 + chunk * 16;
                 *reinterpret_cast<uint4 *>(base + off) = make_uint4(0, 0, 0, 0);
-                if (k2SM) tc::st_cluster_zero16(tc::mapa_shared(tc::smem_u32(base), 1) + off);
+                tc::st_cluster_zero16(tc::mapa_shared(tc::smem_u32(base), 1) + off);
               }
             }
             tc::fence_proxy_async_smem();
-            if (k2SM) tc::fence_proxy_async_smem_cluster();
+            tc::fence_proxy_async_smem_cluster();
           }
           __syncwarp();
         }
@@ -878,17 +845,11 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
           for (int kk = 0; kk < BK / UK; ++kk) {
             const uint64_t ad = ad0 + kk * kAStep;
             const uint64_t bd = bd0 + kk * kBStep;
-            if (F8) {
-              if (k2SM) tc::umma_f8_2sm(d_tmem, ad, bd, IDESC, (kb | kk) != 0);
-              else tc::umma_f8(d_tmem, ad, bd, IDESC, (kb | kk) != 0);
-            } else {
-              if (k2SM) tc::umma_bf16_2sm(d_tmem, ad, bd, IDESC, (kb | kk) != 0);
-              else tc::umma_bf16(d_tmem, ad, bd, IDESC, (kb | kk) != 0);
-            }
+            if (F8) tc::umma_f8_2sm(d_tmem, ad, bd, IDESC, (kb | kk) != 0);
+            else tc::umma_bf16_2sm(d_tmem, ad, bd, IDESC, (kb | kk) != 0);
           }
           // release the stage in both CTAs
-          if (k2SM) tc::umma_commit_2sm_mc(&bk.empty[s], kPair);
-          else tc::umma_commit_mc(&bk.empty[s], kPair);
+          tc::umma_commit_2sm_mc(&bk.empty[s], kPair);
         }
         __syncwarp();
         if (++s == kSt) {
@@ -898,16 +859,14 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       }
       if (!ok) break;
       if (lane == 0) {
-        if (k2SM) tc::umma_commit_2sm_mc(&bk.tfull[a], kPair);  // both CTAs' epilogues
-        else tc::umma_commit(&bk.tfull[a]);
+        tc::umma_commit_2sm_mc(&bk.tfull[a], kPair);  // both CTAs' epilogues
       }
       __syncwarp();
       ++acc_it;
     }
     // drain: no MMA of this CTA is in flight once `drain` completes
     if (lane == 0) {
-      if (k2SM) tc::umma_commit_2sm_mc(&bk.drain, 0x1);
-      else tc::umma_commit(&bk.drain);
+      tc::umma_commit_2sm_mc(&bk.drain, 0x1);
     }
     __syncwarp();
     tc::mbar_wait_drain(&bk.drain, 0, p.wait_limit_ns);
@@ -943,8 +902,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        if (k2SM) tc::mbar_arrive_cluster(tc::mapa_shared(tc::smem_u32(&bk.tempty[a]), 0));
-        else tc::mbar_arrive(&bk.tempty[a]);
+        tc::mbar_arrive_cluster(tc::mapa_shared(tc::smem_u32(&bk.tempty[a]), 0));
       }
       ++acc_it;
     }
@@ -972,8 +930,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   tc::cluster_sync();
   tc::tc_fence_after();
   if (warp == 1) {
-    if (k2SM) tc::tmem_dealloc_2sm(tmem, kTmemCols);
-    else tc::tmem_dealloc(tmem, kTmemCols);
+    tc::tmem_dealloc_2sm(tmem, kTmemCols);
   }
   if (threadIdx.x == 0 && bk.abort_flag) moe_set_status(p.dev_status, MOE_ERR_TIMEOUT);
 }

@@ -34,10 +34,6 @@ MOE_DEVINL void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
                : "memory");
 }
 
-MOE_DEVINL void mbar_arrive(uint64_t *bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
 MOE_DEVINL bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -102,15 +98,6 @@ MOE_DEVINL void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar, in
       : "memory");
 }
 
-MOE_DEVINL void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar, int c0, int c1,
-                            int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-
 // Bulk tensor stores shared -> global (the box is clipped at the tensor's
 // bounds), grouped per thread; wait_read(0) returns once every committed
 // store has finished reading its shared-memory source.
@@ -150,28 +137,6 @@ MOE_DEVINL void tma_reduce_add_3d(const CUtensorMap *map, const void *src, int c
 MOE_DEVINL void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 MOE_DEVINL void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 MOE_DEVINL void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
-// Multicast variants: the box lands at the same shared-memory offset in every
-// CTA of `mask` within the cluster and completes the mbarrier at the same
-// offset in each of them.
-MOE_DEVINL void tma_load_2d_mc(void *dst, const CUtensorMap *map, uint64_t *bar, int c0, int c1,
-                               uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(mask)
-      : "memory");
-}
-
-MOE_DEVINL void tma_load_3d_mc(void *dst, const CUtensorMap *map, uint64_t *bar, int c0, int c1,
-                               int c2, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
-      "h"(mask)
-      : "memory");
-}
 
 // ------------------------------------------------------------- clusters
 MOE_DEVINL uint32_t cluster_ctarank() {
@@ -282,60 +247,8 @@ __host__ __device__ constexpr uint32_t idesc_f8(int M, int N, int a_fmt, int b_f
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// ---------------------------------------------------------- tcgen05 ops
-MOE_DEVINL void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                   smem_u32(dst_smem)),
-               "r"(ncols)
-               : "memory");
-}
-
-MOE_DEVINL void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-
-MOE_DEVINL void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
-}
-
-MOE_DEVINL void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                          uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-MOE_DEVINL void umma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                        uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Arrive on `bar` once every tcgen05.mma issued so far by this thread is done.
-MOE_DEVINL void umma_commit(uint64_t *bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
-      : "memory");
-}
-
-// Arrive on `bar` in every CTA of `mask` once this thread's MMAs are done.
-MOE_DEVINL void umma_commit_mc(uint64_t *bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(mask)
-      : "memory");
-}
-
+// Tensor-memory columns for the CTA pair (warp-collective, both CTAs), the
+// permit release after it, and the matching deallocation.
 MOE_DEVINL void tmem_alloc_2sm(uint32_t *dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                    smem_u32(dst_smem)),
@@ -374,6 +287,8 @@ MOE_DEVINL void umma_f8_2sm(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uin
       : "memory");
 }
 
+// Arrive once on `bar` in each CTA of `mask` when every MMA the leader issued
+// so far is done.
 MOE_DEVINL void umma_commit_2sm_mc(uint64_t *bar, uint16_t mask) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
