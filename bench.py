@@ -83,7 +83,7 @@ def dist_env():
 # ---------------------------------------------------------------------------
 # CPU oracle sample (the cpu_baseline leg and --impl reference)
 # ---------------------------------------------------------------------------
-def oracle_sample(cfg, inp, n_tok, w64=None):
+def oracle_sample(cfg, inp, n_tok, w64=None, groups=(0, 0)):
     """Run the oracle's forward + backward on the first n_tok tokens; returns
     (seconds, kept assignments, weights-in-fp64)."""
     from oracle import moe_ref
@@ -99,22 +99,22 @@ def oracle_sample(cfg, inp, n_tok, w64=None):
         cap = max(1, -(-cap * n_tok // cfg.T))
     t0 = time.perf_counter()
     fw = moe_ref.forward(x, logits, wi, wo, cfg.k, cfg.score_fn, cfg.renorm, cfg.align, cap,
-                         cfg.num_chunks)
+                         cfg.num_chunks, num_groups=groups[0], topk_group=groups[1])
     moe_ref.backward(fw, dout, wi, wo, cfg.k, cfg.num_chunks)
     dt = time.perf_counter() - t0
     m_kept = int(fw["layout"]["kept_counts"].sum())
     return dt, m_kept, w64
 
 
-def cpu_baseline(cfg, inp, target_s=12.0):
+def cpu_baseline(cfg, inp, target_s=12.0, groups=(0, 0)):
     """Time the oracle on a growing token sample until one run takes ~target_s
     (its cost is not linear in the tokens: every expert's weights are read)."""
     cores = len(os.sched_getaffinity(0))
     n = min(cfg.T, 64)
-    dt, m_kept, w64 = oracle_sample(cfg, inp, n)
+    dt, m_kept, w64 = oracle_sample(cfg, inp, n, groups=groups)
     while dt < target_s and n < cfg.T:
         n = int(min(cfg.T, n * max(2.0, min(8.0, 0.8 * target_s / max(dt, 1e-3)))))
-        dt, m_kept, _ = oracle_sample(cfg, inp, n, w64)
+        dt, m_kept, _ = oracle_sample(cfg, inp, n, w64, groups)
     flops = 18.0 * m_kept * cfg.d * cfg.f
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "tokens_per_s": n / dt, "seconds": dt,
@@ -236,7 +236,8 @@ def run_ours(args, cfg, ws, rank, local):
     logits = torch.from_numpy(inp["logits"]).to(dev)
     shape = layer.LayerShape(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.score_fn, cfg.renorm,
                              cfg.align, cfg.capacity, cfg.num_chunks, args.bias,
-                             fp8=args.fp8)
+                             num_groups=args.num_groups, topk_group=args.topk_group,
+                             aux_coeff=args.aux_coeff, fp8=args.fp8)
     b = layer.MoEBuffers(shape, device=dev)
     stream = torch.cuda.current_stream(dev)
     bi = bo = None
@@ -414,6 +415,8 @@ def run_ours(args, cfg, ws, rank, local):
                    "score": "sigmoid" if cfg.score_fn else "softmax", "renorm": cfg.renorm,
                    "align": cfg.align, "capacity": cfg.capacity, "num_chunks": cfg.num_chunks,
                    "mlp_bias": bool(args.bias), "fp8": bool(args.fp8),
+                   "num_groups": args.num_groups, "topk_group": args.topk_group,
+                   "aux_coeff": args.aux_coeff,
                    "m_kept": m_kept, "rows": R, "empty_experts": empty,
                    "gemm_tflop_per_step": flops_step / 1e12,
                    "l2": "inputs larger than L2 (weights %.2f GB)" % ((inp["wi"].nbytes +
@@ -431,7 +434,7 @@ def run_ours(args, cfg, ws, rank, local):
         "kernels": kernels,
     }
     if not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(cfg, inp)
+        out["cpu_baseline"] = cpu_baseline(cfg, inp, groups=(args.num_groups, args.topk_group))
     if dist is not None:
         dist.destroy_process_group()
     return out
@@ -444,14 +447,15 @@ def run_reference(args, cfg, ws, rank):
     cores = len(os.sched_getaffinity(0))
     # size the per-step sample so that warm-up + steps end within a few minutes
     n0 = min(cfg.T, 32)
-    dt0, _, w64 = oracle_sample(cfg, inp, n0)
+    groups = (args.num_groups, args.topk_group)
+    dt0, _, w64 = oracle_sample(cfg, inp, n0, groups=groups)
     budget = 150.0 / max(1, args.steps + args.warmup)
     n = int(min(cfg.T, max(n0, n0 * budget / max(dt0, 1e-3))))
     for _ in range(args.warmup):
-        oracle_sample(cfg, inp, n, w64)
+        oracle_sample(cfg, inp, n, w64, groups)
     secs, kept = 0.0, 0
     for _ in range(args.steps):
-        dt, m_kept, _ = oracle_sample(cfg, inp, n, w64)
+        dt, m_kept, _ = oracle_sample(cfg, inp, n, w64, groups)
         secs += dt
         kept = m_kept
     flops = 18.0 * kept * cfg.d * cfg.f
@@ -478,6 +482,12 @@ def main():
                     choices=sorted(moe_synth.CONFIGS) + sorted(moe_synth.PROFILE_CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--num-groups", type=int, default=0,
+                    help="group-limited routing: expert groups (0: off)")
+    ap.add_argument("--topk-group", type=int, default=0,
+                    help="group-limited routing: groups kept per token")
+    ap.add_argument("--aux-coeff", type=float, default=0.0,
+                    help="auxiliary load-balancing loss coefficient (0: off)")
     ap.add_argument("--fp8", action="store_true",
                     help="FP8 expert GEMMs with current tensor scaling")
     ap.add_argument("--bias", action="store_true",
