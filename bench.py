@@ -183,10 +183,11 @@ class ClockSampler:
 def algorithmic_bytes(cfg, m_kept, R, t_kept):
     T, d, k, f, E = cfg.T, cfg.d, cfg.k, cfg.f, cfg.E
     return {
-        # FP8: amax read + quantize read (bf16) + row-wise and column-wise codes
+        # FP8: amax read + quantize read (bf16) + row-wise and column-wise codes;
+        # Act and dH take their amax from the GEMM that wrote them (no amax read)
         "transpose_act": 4 * R * f, "transpose_xs": 4 * R * d,
-        "quant_x": 6 * R * d, "quant_act": 6 * R * f, "quant_dy": 6 * R * d,
-        "quant_dh": 6 * R * 2 * f, "quant_wi": 6 * E * d * 2 * f, "quant_wo": 6 * E * f * d,
+        "quant_x": 6 * R * d, "quant_act": 4 * R * f, "quant_dy": 6 * R * d,
+        "quant_dh": 4 * R * 2 * f, "quant_wi": 6 * E * d * 2 * f, "quant_wo": 6 * E * f * d,
         "colsum_dbo": R * d * 2 + E * d * 4,
         "colsum_dbi": R * 2 * f * 2 + E * 2 * f * 4,
         "permute": (t_kept + R) * d * 2 + 8 * T * k + 4 * R,

@@ -330,7 +330,8 @@ moe_status_t moe_group_colsum(const uint16_t *G, int64_t ldg, const int32_t *gro
  */
 
 /*
- * moe_fp8_amax -- amax[g] = max |x| over the rows of group g.
+ * moe_fp8_amax -- amax[g] = max |x| over the rows of group g (NaN when one of
+ *   them is NaN, 0 for a group with no rows).
  *   x        bf16 [rows, ldx >= cols] (16-byte aligned, ldx % 8 == 0, cols % 8 == 0)
  *   groups   1, or E for per-expert weights (rows % groups == 0: group g is
  *            rows [g * rows / groups, (g + 1) * rows / groups))

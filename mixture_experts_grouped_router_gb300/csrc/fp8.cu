@@ -52,43 +52,93 @@ MOE_DEVINL uint2 quant8(const uint4 &v, float scale, int fmt) {
   return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
 }
 
-// amax over rows [g * rpg, g * rpg + limit) of group g = blockIdx.y, where
-// limit = rpg, or group_offsets[E] (clamped) when offsets are given.
-__global__ void __launch_bounds__(256)
-amax_kernel(const uint16_t *__restrict__ x, int64_t ldx, int64_t rpg, int cols,
+// amax over rows [g * rpg, g * rpg + limit) of every group g, where limit =
+// rpg, or group_offsets[E] (clamped) when offsets are given (groups == 1).
+// The groups' rows, laid end to end, are split into one contiguous range per
+// block (a persistent grid of the resident blocks); a block reduces and
+// publishes its maximum once per group its range touches.
+// |x| of a bf16 is its bit pattern with the sign cleared, and non-negative
+// floats order like their bit patterns, so the max is an unsigned max of the
+// 16-bit patterns (two per word, __vmaxu2); a NaN pattern is above every
+// finite one and infinity, so a NaN input makes amax NaN.  Each thread keeps
+// kAmaxRows rows of loads in flight.
+constexpr int kAmaxRows = 4;
+constexpr int kAmaxThreads = 256;
+
+__global__ void __launch_bounds__(kAmaxThreads)
+amax_kernel(const uint16_t *__restrict__ x, int64_t ldx, int64_t rpg, int cols, int groups,
             const int32_t *__restrict__ offsets, int E, float *__restrict__ amax) {
-  const int g = blockIdx.y;
-  int64_t rows = rpg;
-  if (offsets != nullptr) rows = min(max((int64_t)__ldg(offsets + E), (int64_t)0), rpg);
-  const uint16_t *base = x + (int64_t)g * rpg * ldx;
-  float m = 0.0f;
-  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
-    const uint16_t *row = base + r * ldx;
-    for (int c = threadIdx.x * 8; c < cols; c += 256 * 8) {
-      float f[8];
-      bf16x8_to_f32(ld_nc_v4(row + c), f);
+  __shared__ uint32_t s_m[kAmaxThreads / 32];
+  int64_t limit = rpg;
+  if (offsets != nullptr) limit = min(max((int64_t)__ldg(offsets + E), (int64_t)0), rpg);
+  const int64_t total = offsets != nullptr ? limit : (int64_t)groups * rpg;
+  // this block's range of rows, in whole kAmaxRows steps
+  const int64_t steps = (total + kAmaxRows - 1) / kAmaxRows;
+  const int64_t per = (steps + gridDim.x - 1) / gridDim.x * kAmaxRows;
+  const int64_t begin = (int64_t)blockIdx.x * per;
+  const int64_t end = min(begin + per, total);
+  if (begin >= end) return;
+  for (int g = (int)(begin / rpg); (int64_t)g * rpg < end; ++g) {
+    const int64_t lo = max(begin - (int64_t)g * rpg, (int64_t)0);
+    const int64_t hi = min(end - (int64_t)g * rpg, limit);
+    const uint16_t *base = x + (int64_t)g * rpg * ldx;
+    uint32_t m2 = 0;  // two running maxima of 16-bit patterns
+    for (int64_t r0 = lo; r0 < hi; r0 += kAmaxRows) {
+      for (int c = threadIdx.x * 8; c < cols; c += kAmaxThreads * 8) {
+        uint4 v[kAmaxRows];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
+        for (int u = 0; u < kAmaxRows; ++u)
+          v[u] = r0 + u < hi ? ld_nc_v4(base + (r0 + u) * ldx + c) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int u = 0; u < kAmaxRows; ++u) {
+          m2 = __vmaxu2(m2, v[u].x & 0x7FFF7FFFu);
+          m2 = __vmaxu2(m2, v[u].y & 0x7FFF7FFFu);
+          m2 = __vmaxu2(m2, v[u].z & 0x7FFF7FFFu);
+          m2 = __vmaxu2(m2, v[u].w & 0x7FFF7FFFu);
+        }
+      }
     }
-  }
-  m = warp_max(m);
-  __shared__ float s_m[8];
-  if ((threadIdx.x & 31) == 0) s_m[threadIdx.x >> 5] = m;
-  __syncthreads();
-  if (threadIdx.x == 0) {
+    uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
 #pragma unroll
-    for (int w = 1; w < 8; ++w) m = fmaxf(m, s_m[w]);
-    // non-negative floats order like their bit patterns
-    if (m > 0.0f) atomicMax(reinterpret_cast<unsigned int *>(amax + g), __float_as_uint(m));
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    __syncthreads();  // s_m is free (the previous group's reduction is read)
+    if ((threadIdx.x & 31) == 0) s_m[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+#pragma unroll
+      for (int w = 1; w < kAmaxThreads / 32; ++w) m = max(m, s_m[w]);
+      // the fp32 bit pattern of the bf16 value orders the same way
+      if (m != 0) atomicMax(reinterpret_cast<unsigned int *>(amax + g), m << 16);
+    }
   }
 }
 
-// One 64 x 64 tile: row-wise codes to q, column-wise codes to qt.
+// 4 x 4 byte transpose: row[r] holds the codes of one row, column c at byte
+// c; col[c] gets column c, row r at byte r.
+MOE_DEVINL void transpose4x4(const uint32_t row[4], uint32_t col[4]) {
+  const uint32_t t0 = __byte_perm(row[0], row[1], 0x5140);  // a0 b0 a1 b1
+  const uint32_t t1 = __byte_perm(row[2], row[3], 0x5140);  // c0 d0 c1 d1
+  const uint32_t t2 = __byte_perm(row[0], row[1], 0x7362);  // a2 b2 a3 b3
+  const uint32_t t3 = __byte_perm(row[2], row[3], 0x7362);  // c2 d2 c3 d3
+  col[0] = __byte_perm(t0, t1, 0x5410);
+  col[1] = __byte_perm(t0, t1, 0x7632);
+  col[2] = __byte_perm(t2, t3, 0x5410);
+  col[3] = __byte_perm(t2, t3, 0x7632);
+}
+
+// 64 x 64 tiles, kQCT of them along the columns per block: row-wise codes to
+// q, column-wise codes to qt.
 //   PADDED (grouped activations, one scale): blockIdx.x walks the padded row
 //   space; the tile's 64 padded rows belong to one group e and map to source
 //   rows off_e + (j - poff_e) (zeros past the group's end).
 //   else (weights, one scale per expert g = blockIdx.z): plain transpose of
 //   each [rpg, cols] slab.
+// Row phase: a thread quantizes 8 codes of each of two rows, stores them
+// row-wise and as words into the tile (rows of 17 words); the next tile's
+// loads are issued before the barrier.  Column phase: a thread reads a 4 x 4
+// block of codes as four words (the 17-word rows make the warp's reads
+// conflict-free), transposes it with byte permutes and stores four 4-byte
+// column pieces (8 lanes per column piece: whole 32-byte sectors).
 template <bool PADDED>
 __global__ void __launch_bounds__(256)
 quant_kernel(const uint16_t *__restrict__ x, int64_t ldx, int64_t rpg, int cols,
@@ -96,7 +146,8 @@ quant_kernel(const uint16_t *__restrict__ x, int64_t ldx, int64_t rpg, int cols,
              const float *__restrict__ amax, int fmt, uint8_t *__restrict__ q, int64_t ldq,
              int64_t stride_q, uint8_t *__restrict__ qt, int64_t ldqt, int64_t stride_qt,
              float *__restrict__ scale_inv) {
-  __shared__ uint8_t tile[kQT][kQT + 16];
+  constexpr int kRowWords = kQT / 4 + 1;
+  __shared__ uint32_t tile[kQT][kRowWords];
   __shared__ int s_poff[kMaxGroups + 1];
   const int g = PADDED ? 0 : blockIdx.z;
   const int64_t j0 = (int64_t)blockIdx.x * kQT;  // first (padded) row of the tile
@@ -144,44 +195,62 @@ quant_kernel(const uint16_t *__restrict__ x, int64_t ldx, int64_t rpg, int cols,
   }
   const uint16_t *xg = x + (int64_t)g * rpg * ldx;
   uint8_t *qg = q + (int64_t)g * stride_q;
-  for (int ct = 0; ct < kQCT; ++ct) {
-    const int c0 = (blockIdx.y * kQCT + ct) * kQT;
-    if (c0 >= cols) break;
-    if (ct > 0) __syncthreads();  // the previous tile's column-wise reads are done
-    // load, quantize, write row-wise codes, keep the tile in shared memory
+  uint8_t *qtg = qt + (int64_t)g * stride_qt;
+  const int cbase = blockIdx.y * kQCT * kQT;
+  const int ntiles = min(kQCT, (cols - cbase + kQT - 1) / kQT);
+
+  // row phase: element v = threadIdx.x + h * 256 is tile row v >> 3, columns
+  // (v & 7) * 8 .. + 7
+  auto load = [&](int ct, uint4 raw[2]) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int v = threadIdx.x + h * 256;
-      const int i = v >> 3;            // tile row
-      const int cc = (v & 7) * 8;      // tile column
+      const int64_t r = src0 + (v >> 3);
+      const int c = cbase + ct * kQT + (v & 7) * 8;
+      raw[h] = r < src_end && c < cols ? ld_nc_v4(xg + r * ldx + c) : make_uint4(0, 0, 0, 0);
+    }
+  };
+  // column phase: rows 4 rq .. 4 rq + 3, columns 4 cq .. 4 cq + 3 of the tile
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cq = 4 * (warp & 3) + (lane >> 3);
+  const int rq = 8 * (warp >> 2) + (lane & 7);
+  const int64_t jj = j0 + 4 * rq;
+  const bool rows_ok = PADDED || jj < rpg;
+
+  uint4 raw[2];
+  load(0, raw);
+  for (int ct = 0; ct < ntiles; ++ct) {
+    const int c0 = cbase + ct * kQT;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int v = threadIdx.x + h * 256;
+      const int i = v >> 3;
+      const int cc = (v & 7) * 8;
       const int64_t r = src0 + i;
       const int c = c0 + cc;
       uint2 codes = make_uint2(0, 0);
       if (r < src_end && c < cols) {
-        codes = quant8(ld_nc_v4(xg + r * ldx + c), scale, fmt);
+        codes = quant8(raw[h], scale, fmt);
         *reinterpret_cast<uint2 *>(qg + r * ldq + c) = codes;
       }
-      *reinterpret_cast<uint2 *>(&tile[i][cc]) = codes;
+      tile[i][cc / 4] = codes.x;
+      tile[i][cc / 4 + 1] = codes.y;
     }
+    if (ct + 1 < ntiles) load(ct + 1, raw);
     __syncthreads();
-    // column-wise: output row c (= input column), 16 consecutive padded rows
     {
-      const int cr = threadIdx.x >> 2;       // tile column -> output row
-      const int k16 = (threadIdx.x & 3) * 16;
-      const int c = c0 + cr;
-      const int64_t jj = j0 + k16;
-      if (c < cols && (PADDED || jj < rpg)) {
-        uint32_t w[4];
+      uint32_t rw[4], cw[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          w[u] = 0;
+      for (int r = 0; r < 4; ++r) rw[r] = tile[4 * rq + r][cq];
+      transpose4x4(rw, cw);
 #pragma unroll
-          for (int b = 0; b < 4; ++b) w[u] |= (uint32_t)tile[k16 + 4 * u + b][cr] << (8 * b);
-        }
-        *reinterpret_cast<uint4 *>(qt + (int64_t)g * stride_qt + (int64_t)c * ldqt + jj) =
-            make_uint4(w[0], w[1], w[2], w[3]);
+      for (int i = 0; i < 4; ++i) {
+        const int c = c0 + 4 * cq + i;
+        if (c < cols && rows_ok)
+          *reinterpret_cast<uint32_t *>(qtg + (int64_t)c * ldqt + jj) = cw[i];
       }
     }
+    __syncthreads();  // the tile is read before the next row phase writes it
   }
 }
 
@@ -198,9 +267,20 @@ cudaError_t launch_fp8_amax(const uint16_t *x, int64_t ldx, int64_t rows, int co
   if (e != cudaSuccess) return e;
   const int64_t rpg = rows / groups;
   if (rpg == 0) return cudaSuccess;
-  const int want = 4 * num_sms() / groups + 1;
-  dim3 grid((unsigned)std::min<int64_t>(rpg, std::max(want, 1)), groups);
-  amax_kernel<<<grid, 256, 0, s>>>(x, ldx, rpg, cols, offsets, E, amax);
+  // one wave: every block resident at once
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, amax_kernel, kAmaxThreads, 0) !=
+            cudaSuccess ||
+        n < 1)
+      n = 1;
+    per_sm = n;
+  }
+  const int64_t steps = (rows + kAmaxRows - 1) / kAmaxRows;
+  const unsigned grid = (unsigned)std::max<int64_t>(
+      1, std::min<int64_t>(steps, (int64_t)per_sm * num_sms()));
+  amax_kernel<<<grid, kAmaxThreads, 0, s>>>(x, ldx, rpg, cols, groups, offsets, E, amax);
   return cudaGetLastError();
 }
 

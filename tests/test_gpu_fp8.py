@@ -69,6 +69,38 @@ def _poff(sizes, pad=128):
     return p
 
 
+@pytest.mark.parametrize("groups,rpg,cols", [(5, 37, 24), (3, 4099, 2056), (40, 9, 8)])
+def test_amax_groups_ragged(groups, rpg, cols):
+    """Per-group amax when groups straddle the blocks' row ranges (rows per
+    group not a multiple of the rows a block reads at once); each group's
+    maximum sits on its first or last row."""
+    rng = np.random.default_rng(groups * rpg + cols)
+    bits = _bf(rng, (groups * rpg, cols))
+    for g in range(groups):
+        r = g * rpg + (0 if g % 2 else rpg - 1)
+        v = -(8.0 + g) if g % 3 else 8.0 + g
+        bits[r, (g * 7) % cols] = moe_synth.bf16_bits(np.float32([v]))[0]
+    x = dev_bf16(bits)
+    amax = torch.full((groups,), -1.0, device="cuda")
+    L.moe_fp8_amax(x, amax, groups=groups)
+    got = amax.cpu().numpy()
+    want = np.abs(moe_synth.bits_to_f64(bits).reshape(groups, rpg * cols)).max(axis=1)
+    assert (got == want.astype(np.float32)).all(), (got, want)
+
+
+def test_amax_nan_propagates():
+    """A NaN element makes its group's amax NaN (the scale then falls back to 1)."""
+    rng = np.random.default_rng(7)
+    bits = _bf(rng, (2 * 64, 32))
+    x = dev_bf16(bits)
+    x[70, 5] = float("nan")                   # group 1
+    amax = torch.full((2,), -1.0, device="cuda")
+    L.moe_fp8_amax(x, amax, groups=2)
+    got = amax.cpu().numpy()
+    assert got[0] == np.abs(moe_synth.bits_to_f64(bits[:64])).max()
+    assert np.isnan(got[1])
+
+
 @pytest.mark.parametrize("sizes,cols", [([0, 7, 300, 128, 129, 0, 1, 640], 64),
                                         ([517], 96), ([1, 2, 3], 16), ([256, 0, 0], 512),
                                         ([0, 0], 32), ([64] * 40, 128)])
