@@ -73,4 +73,10 @@ MOE_DEVINL void st_v4(void *p, const uint4 &v) {
 // sigmoid(z) = 1 / (1 + e^-z) in fp32 with the hardware exponential and
 // reciprocal (relative error ~1e-6, far below the bf16 rounding of the
 // SwiGLU outputs it feeds).  e^-z overflowing to inf gives exactly 0.
-MOE_DEVINL float sigmoid_f(float z) { return __frcp_rn(1.0f + __expf(-z)); }
+// 1 / (1 + e^-z) with the approximate reciprocal (rcp.approx.ftz: within
+// 1 ulp; 1 / +inf = 0), far inside the bf16 rounding of the epilogue outputs
+MOE_DEVINL float sigmoid_f(float z) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + __expf(-z)));
+  return r;
+}
