@@ -303,6 +303,26 @@ MOE_DEVINL void epilogue_prefetch(const TcParams &p, const TileInfo &ti, int rit
   }
 }
 
+// amx = max(amx, |v[0]|, ..., |v[n - 1]|) over a 32-value chunk, by a tree
+// of pairwise maxima (max is exact, so the order does not matter); the
+// bounds check only on a ragged last chunk.
+MOE_DEVINL float chunk_amax(float amx, const float *v, int n) {
+  float m[16];
+  if (n >= 32) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) m[i] = fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1]));
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      m[i] = fmaxf(2 * i < n ? fabsf(v[2 * i]) : 0.0f, 2 * i + 1 < n ? fabsf(v[2 * i + 1]) : 0.0f);
+  }
+#pragma unroll
+  for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
+  return fmaxf(amx, m[0]);
+}
+
 // One tile's epilogue for the ragged-M GEMM.  Warp q owns tile rows
 // [32q, 32q+32), thread = one row; 32-column chunks.  The global inputs of a
 // chunk are loaded one chunk ahead so that their latency overlaps the work
@@ -397,11 +417,7 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
       }
 #pragma unroll
       for (int j = 0; j < 32; ++j) act[j] = g[j] * sigmoid_f(g[j]) * u[j];
-      if (track) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (nc + j < F) amx = fmaxf(amx, fabsf(act[j]));
-      }
+      if (track) amx = chunk_amax(amx, act, F - nc);
       if (bulk) {
         stage_acquire(lane);
         stage_bf16(stg, lane, g);
@@ -461,13 +477,13 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
 #pragma unroll
       for (int k = 0; k < 32; ++k) {
         const float sg = sigmoid_f(g[k]);
-        dg[k] = v[k] * u[k] * sg * (1.0f + g[k] * (1.0f - sg));
-        du[k] = v[k] * g[k] * sg;
+        const float vs = v[k] * sg;
+        du[k] = vs * g[k];
+        dg[k] = vs * u[k] * (1.0f + g[k] * (1.0f - sg));
       }
       if (track) {
-#pragma unroll
-        for (int k = 0; k < 32; ++k)
-          if (nc + k < N) amx = fmaxf(amx, fmaxf(fabsf(dg[k]), fabsf(du[k])));
+        amx = chunk_amax(amx, dg, N - nc);
+        amx = chunk_amax(amx, du, N - nc);
       }
       if (bulk) {
         stage_acquire(lane);
@@ -536,11 +552,7 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
           }
         }
       }
-      if (track) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (nc + j < N) amx = fmaxf(amx, fabsf(v[j]));
-      }
+      if (track) amx = chunk_amax(amx, v, N - nc);
       if (bulk) {
         stage_acquire(lane);
         if (p.c_f32) stage_f32(stg, lane, v);
