@@ -94,12 +94,13 @@ struct Book {
 
 // Per-kernel layout.  Every GEMM runs as 2-SM MMAs whose stage holds this
 // CTA's 128-row (tgmm: 128-column) A tile and half of the B tile (32 KB), 6
-// stages, 4 epilogue warps.  The SwiGLU-backward dgrad, whose epilogue (H
-// reads, two outputs) is the longest, runs 8 epilogue warps (two per TMEM
-// lane quarter, each on half of the tile's columns) and 5 stages.
+// stages, 4 epilogue warps.  The FP8 SwiGLU-backward dgrad, whose epilogue (H
+// reads, two outputs) is the longest against a mainloop half as long as the
+// bf16 one, runs 8 epilogue warps (two per TMEM lane quarter, each on half of
+// the tile's columns) and 5 stages.
 template <int KIND, int EPI, bool F8>
 struct Ring {
-  static constexpr bool swiglu_bwd = KIND == 0 && EPI == MOE_EPI_SWIGLU_BWD;
+  static constexpr bool swiglu_bwd = KIND == 0 && EPI == MOE_EPI_SWIGLU_BWD && F8;
   static constexpr int epi_warps = swiglu_bwd ? 8 : 4;
   static constexpr int stages = swiglu_bwd ? 5 : 6;
   static constexpr int b_bytes = B_BYTES / 2;
@@ -256,12 +257,14 @@ MOE_DEVINL void stage_release() {
 
 // Output maps of an epilogue warp (m0..m2), the H maps it loads from in the
 // SwiGLU backward (m2 = gate, m3 = up), its aux barrier and that barrier's
-// phase count.
+// phase count, and the evict-first L2 policy of the tensors it streams (H
+// written by the SwiGLU forward; H read and dH written by the backward).
 struct OutMaps {
   const CUtensorMap *m0, *m1, *m2, *m3;
   uint64_t *aux_bar;
   uint32_t aux_phase;   // H loads waited for
   uint32_t aux_issued;  // H loads issued
+  uint64_t stream_pol;
 };
 
 // Before a tile's accumulator is ready: pull the epilogue's global inputs
@@ -332,8 +335,8 @@ MOE_DEVINL float chunk_amax(float amx, const float *v, int n) {
 MOE_DEVINL void issue_aux_load(OutMaps &om, uint8_t *stg, int nc, int wrow0) {
   ++om.aux_issued;
   tc::mbar_expect_tx(om.aux_bar, 4096);
-  tc::tma_load_2d(stg + 4096, om.m2, om.aux_bar, nc, wrow0);
-  tc::tma_load_2d(stg + 6144, om.m3, om.aux_bar, nc, wrow0);
+  tc::tma_load_2d_hint(stg + 4096, om.m2, om.aux_bar, nc, wrow0, om.stream_pol);
+  tc::tma_load_2d_hint(stg + 6144, om.m3, om.aux_bar, nc, wrow0, om.stream_pol);
 }
 
 // One tile's epilogue for the ragged-M GEMM.  Warp q owns tile rows
@@ -425,8 +428,8 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
         stage_bf16(stg + 4096, lane, act);
         stage_release();
         if (lane == 0) {
-          tc::tma_store_2d(om.m0, stg, nc, wrow0);
-          tc::tma_store_2d(om.m1, stg + 2048, nc, wrow0);
+          tc::tma_store_2d_hint(om.m0, stg, nc, wrow0, om.stream_pol);
+          tc::tma_store_2d_hint(om.m1, stg + 2048, nc, wrow0, om.stream_pol);
           tc::tma_store_2d(om.m2, stg + 4096, nc, wrow0);
           tc::bulk_commit();
         }
@@ -491,8 +494,8 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
         stage_bf16(stg + 2048, lane, du);
         stage_release();
         if (lane == 0) {
-          tc::tma_store_2d(om.m0, stg, nc, wrow0);
-          tc::tma_store_2d(om.m1, stg + 2048, nc, wrow0);
+          tc::tma_store_2d_hint(om.m0, stg, nc, wrow0, om.stream_pol);
+          tc::tma_store_2d_hint(om.m1, stg + 2048, nc, wrow0, om.stream_pol);
           tc::bulk_commit();
         }
       } else if (valid) {
@@ -889,7 +892,8 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     // 8 epilogue warps: the second four take the upper half of the columns
     constexpr int kChunks = BN / 32 / (kEW / 4);
     const int c_begin = ((warp - 2) >> 2) * kChunks;
-    OutMaps om{&tmC0, &tmC1, &tmC2, &tmC3, &bk.aux_full[warp - 2], 0u, 0u};
+    OutMaps om{&tmC0, &tmC1, &tmC2, &tmC3, &bk.aux_full[warp - 2], 0u, 0u,
+               tc::l2_evict_first_policy()};
     uint32_t acc_it = 0;
     float amx = 0.0f;
     for (int t = cid; t < total; t += ncl) {

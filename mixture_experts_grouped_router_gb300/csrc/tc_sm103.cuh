@@ -98,6 +98,32 @@ MOE_DEVINL void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar, in
       : "memory");
 }
 
+// L2 policy that marks lines for eviction first: for tensors streamed through
+// once (so that they do not push the GEMM operands out of L2).
+MOE_DEVINL uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+MOE_DEVINL void tma_load_2d_hint(void *dst, const CUtensorMap *map, uint64_t *bar, int c0, int c1,
+                                 uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "l"(pol)
+      : "memory");
+}
+
+MOE_DEVINL void tma_store_2d_hint(const CUtensorMap *map, const void *src, int c0, int c1,
+                                  uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint"
+      " [%0, {%2, %3}], [%1], %4;" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1), "l"(pol)
+      : "memory");
+}
+
 // Bulk tensor stores shared -> global (the box is clipped at the tensor's
 // bounds), grouped per thread; wait_read(0) returns once every committed
 // store has finished reading its shared-memory source.
