@@ -41,18 +41,22 @@ def assert_close(name, got, want, rel_fro=REL_FRO, max_rel=MAX_REL):
     assert mdiff <= max_rel * mref, "%s: max diff %.3g > %g * %.3g" % (name, mdiff, max_rel, mref)
 
 
-def layer_shape(cfg, bias=False):
+def layer_shape(cfg, bias=False, num_groups=0, topk_group=0, aux_coeff=0.0):
     from mixture_experts_grouped_router_gb300 import layer
     return layer.LayerShape(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.score_fn, cfg.renorm,
-                            cfg.align, cfg.capacity, cfg.num_chunks, bias)
+                            cfg.align, cfg.capacity, cfg.num_chunks, bias,
+                            num_groups=num_groups, topk_group=topk_group, aux_coeff=aux_coeff)
 
 
-def run_gpu_layer(cfg, inp, device="cuda", dw_dtype=torch.bfloat16, biases=None):
-    """biases: None or the dict of moe_synth.make_biases."""
+def run_gpu_layer(cfg, inp, device="cuda", dw_dtype=torch.bfloat16, biases=None, num_groups=0,
+                  topk_group=0, aux_coeff=0.0):
+    """biases: None or the dict of moe_synth.make_biases; num_groups / topk_group /
+    aux_coeff: the routing options of the layer."""
     from mixture_experts_grouped_router_gb300 import layer
     x, wi, wo, dout = (dev_bf16(inp[n], device) for n in ("x", "wi", "wo", "dout"))
     logits = torch.from_numpy(inp["logits"]).to(device)
-    b = layer.MoEBuffers(layer_shape(cfg, biases is not None), device=device, dw_dtype=dw_dtype)
+    shape = layer_shape(cfg, biases is not None, num_groups, topk_group, aux_coeff)
+    b = layer.MoEBuffers(shape, device=device, dw_dtype=dw_dtype)
     bi = bo = None
     if biases is not None:
         bi, bo = dev_bf16(biases["bi"], device), dev_bf16(biases["bo"], device)
