@@ -91,7 +91,9 @@ unpermute_bwd_kernel(const uint16_t *__restrict__ dout, int64_t ld_dout,
       dot[j] = 0.f;
     }
     const uint4 *g = reinterpret_cast<const uint4 *>(dout + (int64_t)t * ld_dout);
-    for (int i = lane; i < nvec; i += 64) {
+    // a token whose assignments were all dropped reads nothing (its d_w are 0)
+    const int nv = __any_sync(0xffffffffu, pl >= 0) ? nvec : 0;
+    for (int i = lane; i < nv; i += 64) {
       const bool two = i + 32 < nvec;
       uint4 gq[2], yq[KT][2];
       gq[0] = ld_nc_v4(g + i);

@@ -210,6 +210,8 @@ permute_gather_kernel(const uint16_t *__restrict__ x, int64_t ldx,
       moe_set_status(dev_status, MOE_ERR_DEVICE);
       pl = -1;
     }
+    // a token whose assignments were all dropped is not read
+    if (!__any_sync(0xffffffffu, pl >= 0)) return;
     int p[KT];
 #pragma unroll
     for (int j = 0; j < KT; ++j) p[j] = __shfl_sync(0xffffffffu, pl, j);
