@@ -387,9 +387,10 @@ moe_status_t moe_fp8_quantize_weights(const uint16_t *w, int E, int K, int N, in
  *         n*ldb (the transposed copy for [K, N] weights, the row-wise copy of
  *         a [N, K] weight for dgrad); SWIGLU_FWD: rows [0, F) gate, [F, 2F) up
  *   a_scale_inv fp32 [1], b_scale_inv fp32 [E] (device)
- *   amax_out  fp32 [1] (device) or NULL: set to max |x| over the bf16 values
- *             the epilogue writes (Act for SWIGLU_FWD, dH for SWIGLU_BWD, C
- *             for NONE), the amax that quantizes them next (no extra pass)
+ *   amax_out  fp32 [1] (device) or NULL: set to max |x| over the values the
+ *             epilogue writes (Act for SWIGLU_FWD, dH for SWIGLU_BWD, C for
+ *             NONE; NaN values are skipped; 0 with no rows), the amax that
+ *             quantizes them next (no extra pass)
  *   K, lda, ldb, stride_b multiples of 16; other arguments as moe_gmm.
  * FP8 recipe (TE-2912, the fused up-projection; MaxText PR #2319, quantizer
  * settings): E4M3 operands forward, E5M2 gradients backward.
