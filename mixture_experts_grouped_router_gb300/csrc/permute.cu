@@ -8,7 +8,8 @@
 //   1. count:  per block of `tpb` tokens (a multiple of 256 chosen so that
 //              there are at most 256 blocks), a shared-memory histogram over E;
 //   2. rank:   every block derives the per-expert base of its tokens from the
-//              earlier blocks' counts, the kept counts (capacity), the aligned
+//              earlier blocks' counts (a warp per expert, lanes over the
+//              blocks), the kept counts (capacity), the aligned
 //              group sizes and their exclusive scan (warp-shuffle scan), then
 //              ranks its tokens 256 at a time with one ballot per expert per
 //              warp: rank = base + earlier warps + popc(ballot & lanes below);
@@ -74,16 +75,24 @@ permute_rank_kernel(const int32_t *__restrict__ topk_idx, int T, int E, int k, i
   const int b = blockIdx.x;
   grid_dependency_wait();  // the counts of the previous kernel
 
-  // 1. this block's base and the totals, from the count blocks
-  for (int e = tid; e < E; e += kRankThreads) {
+  // 1. this block's base and the totals, from the count blocks: one warp per
+  //    expert, its lanes over the blocks (loads in parallel, shuffle sums)
+  for (int e = warp; e < E; e += kRankWarps) {
     int base = 0, all = 0;
-    for (int bb = 0; bb < nb; ++bb) {
+    for (int bb = lane; bb < nb; bb += 32) {
       const int c = counts[(int64_t)bb * E + e];
       if (bb < b) base += c;
       all += c;
     }
-    run[e] = base;
-    tot[e] = all;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      base += __shfl_xor_sync(0xffffffffu, base, o);
+      all += __shfl_xor_sync(0xffffffffu, all, o);
+    }
+    if (lane == 0) {
+      run[e] = base;
+      tot[e] = all;
+    }
   }
   __syncthreads();
   // 2. kept counts, aligned sizes and their exclusive scan (one warp)
