@@ -53,7 +53,7 @@ namespace {
 
 constexpr int BM = 128, BN = 256, BK = 64, UK = 16;
 constexpr int kStages = 6;  // ring slots allocated (the weight-gradient kernel uses 4)
-constexpr int kMaxEpiWarps = 8;
+constexpr int kMaxEpiWarps = 4;
 constexpr int kPadRows = kF8PadRows;  // group padding of column-wise copies (128 rows)
 constexpr int kStgBytes = 8192;  // per epilogue warp: up to four 32x32 bf16 blocks (or two fp32)
 constexpr int A_BYTES = BM * BK * 2;   // 16 KB
@@ -94,15 +94,11 @@ struct Book {
 
 // Per-kernel layout.  Every GEMM runs as 2-SM MMAs whose stage holds this
 // CTA's 128-row (tgmm: 128-column) A tile and half of the B tile (32 KB), 6
-// stages, 4 epilogue warps.  The FP8 SwiGLU-backward dgrad, whose epilogue (H
-// reads, two outputs) is the longest against a mainloop half as long as the
-// bf16 one, runs 8 epilogue warps (two per TMEM lane quarter, each on half of
-// the tile's columns) and 5 stages.
+// stages, and 4 epilogue warps (one per TMEM lane quarter).
 template <int KIND, int EPI, bool F8>
 struct Ring {
-  static constexpr bool swiglu_bwd = KIND == 0 && EPI == MOE_EPI_SWIGLU_BWD && F8;
-  static constexpr int epi_warps = swiglu_bwd ? 8 : 4;
-  static constexpr int stages = swiglu_bwd ? 5 : 6;
+  static constexpr int epi_warps = 4;
+  static constexpr int stages = 6;
   static constexpr int b_bytes = B_BYTES / 2;
   static constexpr int stage_bytes = A_BYTES + b_bytes;
   static constexpr int threads = 64 + 32 * epi_warps;  // producer, MMA, epilogue
@@ -889,9 +885,8 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     const int q = warp & 3;  // TMEM lane quarter this warp may read = its tile rows
     const int rit = q * 32 + lane;
     uint8_t *stg = smem + Ring<KIND, EPI, F8>::stg_offset + (warp - 2) * kStgBytes;
-    // 8 epilogue warps: the second four take the upper half of the columns
-    constexpr int kChunks = BN / 32 / (kEW / 4);
-    const int c_begin = ((warp - 2) >> 2) * kChunks;
+    constexpr int kChunks = BN / 32;  // the tile's 32-column chunks, all this warp's
+    const int c_begin = 0;
     OutMaps om{&tmC0, &tmC1, &tmC2, &tmC3, &bk.aux_full[warp - 2], 0u, 0u,
                tc::l2_evict_first_policy()};
     uint32_t acc_it = 0;
