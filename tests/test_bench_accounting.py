@@ -7,7 +7,6 @@ Formulas (bf16 = 2 bytes, index = 4 bytes): permute (T_kept + R)·d·2 + 8·T·k
 combine M·d·2 + T·d·2 + 8·T·k; combine backward T_kept·d·2 + 2·M·d·2 + (R−M)·d·2 + 8·T·k;
 dispatch backward M·d·2 + T·d·2 + 4·T·k; GEMMs 18·M·d·f per forward + backward.
 """
-import numpy as np
 import pytest
 
 import bench
@@ -41,7 +40,7 @@ def test_gemm_flops_of_the_full_workloads(name, tflop):
     assert abs(step / 1e12 - tflop) < 0.01
 
 
-def test_bytes_match_a_brute_force_count():
+def test_bytes_match_the_counts_of_a_routed_layout():
     """The bytes each kernel must move, summed from the counts of a small routed
     layout with capacity drops and align padding (rows read and written, index
     arrays), against the benchmark's formulas."""
