@@ -185,7 +185,7 @@ def algorithmic_bytes(cfg, m_kept, R, t_kept):
     return {
         # FP8: amax read + quantize read (bf16) + row-wise and column-wise codes;
         # Act and dH take their amax from the GEMM that wrote them (no amax read)
-        "transpose_act": 4 * R * f, "transpose_xs": 4 * R * d,
+        "transpose_act": 4 * R * f, "transpose_xs": 4 * R * d, "transpose_dy": 4 * R * d,
         "quant_x": 6 * R * d, "quant_act": 4 * R * f, "quant_dy": 6 * R * d,
         "quant_dh": 4 * R * 2 * f, "quant_wi": 6 * E * d * 2 * f, "quant_wo": 6 * E * f * d,
         "colsum_dbo": R * d * 2 + E * d * 4,
@@ -238,7 +238,8 @@ def run_ours(args, cfg, ws, rank, local):
     shape = layer.LayerShape(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.score_fn, cfg.renorm,
                              cfg.align, cfg.capacity, cfg.num_chunks, args.bias,
                              num_groups=args.num_groups, topk_group=args.topk_group,
-                             aux_coeff=args.aux_coeff, fp8=args.fp8)
+                             aux_coeff=args.aux_coeff, fp8=args.fp8,
+                             wgrad_colwise=args.wgrad_colwise)
     b = layer.MoEBuffers(shape, device=dev)
     stream = torch.cuda.current_stream(dev)
     bi = bo = None
@@ -416,6 +417,9 @@ def run_ours(args, cfg, ws, rank, local):
                    "score": "sigmoid" if cfg.score_fn else "softmax", "renorm": cfg.renorm,
                    "align": cfg.align, "capacity": cfg.capacity, "num_chunks": cfg.num_chunks,
                    "mlp_bias": bool(args.bias), "fp8": bool(args.fp8),
+                   "wgrad_operands": ("column-wise FP8 codes (K-major)" if args.fp8 else
+                                      "column-wise bf16 copies (K-major)"
+                                      if args.wgrad_colwise else "row-wise (MN-major)"),
                    "num_groups": args.num_groups, "topk_group": args.topk_group,
                    "aux_coeff": args.aux_coeff,
                    "m_kept": m_kept, "rows": R, "empty_experts": empty,
@@ -493,6 +497,9 @@ def main():
                     help="FP8 expert GEMMs with current tensor scaling")
     ap.add_argument("--bias", action="store_true",
                     help="expert FFN with biases (bi on [gate | up], bo on the output)")
+    ap.add_argument("--wgrad-colwise", action="store_true",
+                    help="bf16 weight gradients read K-major column-wise copies written "
+                         "by the SwiGLU epilogues (default: the row-wise tensors)")
     args = ap.parse_args()
     cfg = {**moe_synth.CONFIGS, **moe_synth.PROFILE_CONFIGS}[args.config]
     ws, rank, local = dist_env()

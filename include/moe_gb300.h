@@ -60,7 +60,7 @@ enum { MOE_FP8_E4M3 = 0, MOE_FP8_E5M2 = 1 };
 const char *moe_status_string(int status);
 /* Message of the last failing call made by this host thread ("" if none). */
 const char *moe_last_error(void);
-/* Library ABI version (major*100 + minor). */
+/* Library ABI version (major*100 + minor); 200 since moe_rows_cap takes the capacity. */
 int moe_version(void);
 
 /*
@@ -82,11 +82,14 @@ uint64_t moe_wait_limit_ns(void);
 void moe_test_stall_loads(int enable);
 
 /*
- * Worst-case number of permuted rows: T*k + E*(align-1) (align <= 1: T*k).
+ * Worst-case number of permuted rows: min(T*k, E*capacity) + E*(align-1)
+ * (capacity <= 0: T*k kept assignments; align <= 1: no padding rows).
  * TE-2912, review thread on recv_buffer_rows ("align_size > 0 + EP are
- * combined"): aligned group sizes can add up to align-1 rows per expert.
+ * combined"): aligned group sizes can add up to align-1 rows per expert;
+ * with token dropping no expert keeps more than `capacity` assignments.
+ * Returns -1 for T < 0, E <= 0 or k <= 0.
  */
-int64_t moe_rows_cap(int T, int E, int k, int align);
+int64_t moe_rows_cap(int T, int E, int k, int align, int capacity);
 
 /* Bytes of device workspace that moe_permute needs for T tokens and E experts. */
 size_t moe_permute_workspace_bytes(int T, int E);
@@ -194,7 +197,8 @@ moe_status_t moe_route_topk_bwd(const float *logits, int64_t ld_logits, const in
  *   x_sorted       bf16 [rows_cap, ld_xs >= d] out: row p = x[token of
  *                  sorted_to_flat[p]]; padding rows are zero; rows >= R
  *                  (R = group_offsets[E]) are not written
- *   rows_cap       rows of x_sorted / sorted_to_flat, >= moe_rows_cap(T,E,k,align)
+ *   rows_cap       rows of x_sorted / sorted_to_flat,
+ *                  >= moe_rows_cap(T, E, k, align, capacity)
  *   group_sizes    int32 [E] out: aligned group sizes
  *   kept_counts    int32 [E] out: kept (not dropped) assignments per expert
  *   group_offsets  int32 [E+1] out: exclusive scan of group_sizes
@@ -227,8 +231,10 @@ moe_status_t moe_permute(const uint16_t *x, int64_t ldx, const int32_t *topk_idx
  * E <= 64 always fits) return MOE_ERR_UNSUPPORTED.  The call allocates and frees nothing.
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
- * capture.  All calls share the array: calls whose kernels overlap on the GPU
- * race and must be serialised by the caller.
+ * capture.  After cudaDeviceReset() the array belongs to the device's new
+ * context, and the first call made there looks the address up again (make it
+ * before any capture too).  All calls share the array: calls whose kernels
+ * overlap on the GPU race and must be serialised by the caller.
  */
 moe_status_t moe_permute_noalloc(const uint16_t *x, int64_t ldx, const int32_t *topk_idx, int T,
                                  int d, int E, int k, int align, int capacity,
@@ -267,16 +273,24 @@ moe_status_t moe_permute_noalloc(const uint16_t *x, int64_t ldx, const int32_t *
  *             bias + e*stride_bias, added to every row of group e after the
  *             partial sum (SWIGLU_FWD: [gate | up] bias, before the SwiGLU)
  *   C         [rows_cap, ldc] (ldc >= N, or >= 2F for SWIGLU_BWD)
- * Only rows r < group_offsets[E] are written.  E <= 256; A, B, C, C2, aux and
- * partial_sum 16-byte aligned; SWIGLU_FWD needs trans_b == 0.
+ *   Ct        bf16 or NULL (SWIGLU_FWD / SWIGLU_BWD only): the epilogue also
+ *             writes a column-wise copy of its activation output in the padded
+ *             group layout of moe_transpose_act, the K-major operand of the
+ *             weight gradient (moe_tgmm_kt):
+ *               SWIGLU_FWD: Act^T [F, ldct],  Ct[n, poff_e + i] = Act[off_e + i, n]
+ *               SWIGLU_BWD: dH^T [2F, ldct], Ct[n, poff_e + i] = dH[off_e + i, n]
+ *             with zeros in each group's padding up to its next multiple of 128
+ *             columns; ldct >= moe_fp8_padded_rows(rows_cap, E), ldct % 8 == 0
+ * Only rows r < group_offsets[E] are written.  E <= 256; A, B, C, C2, Ct, aux
+ * and partial_sum 16-byte aligned; SWIGLU_FWD needs trans_b == 0.
  */
 moe_status_t moe_gmm(const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
                      int64_t stride_b, int trans_b, const int32_t *group_offsets, int E,
                      int64_t rows_cap, int K, int N, int epilogue, const uint16_t *aux,
                      int64_t ld_aux, const float *partial_sum, int64_t ld_ps,
                      const uint16_t *bias, int64_t stride_bias, void *C, int c_dtype,
-                     int64_t ldc, uint16_t *C2, int64_t ldc2, int32_t *dev_status,
-                     moe_stream_t stream);
+                     int64_t ldc, uint16_t *C2, int64_t ldc2, uint16_t *Ct, int64_t ldct,
+                     int32_t *dev_status, moe_stream_t stream);
 
 /*
  * moe_transpose_act -- column-wise bf16 copy of a permuted activation in the
@@ -461,6 +475,78 @@ moe_status_t moe_unpermute_bwd(const uint16_t *d_out, int64_t ld_dout, const uin
                                const float *topk_w, int T, int k, int d, int E,
                                int64_t rows_cap, uint16_t *dY, int64_t ld_dy, float *d_topk_w,
                                moe_stream_t stream);
+
+/* ---------------------------------------------------- expert parallelism --
+ * Dispatch of the permuted rows to the shards that own their experts with a
+ * ragged all-to-all, and the local re-sort after it: TE-2912, sequence
+ * diagram (_dispatch -> ragged_all_to_all -> local permute; _combine the
+ * reverse; the backward re-runs the same exchanges with swapped roles) and
+ * its helpers compute_ragged_all_to_all_params / local_permute_after_a2a /
+ * local_unpermute_before_a2a; the receive-buffer bound of the recv_buffer_rows
+ * review thread.
+ * num_ep shards; shard r owns the El = E / num_ep experts [r*El, (r+1)*El).
+ * Every shard permutes its own tokens over all E experts (moe_permute), so
+ * the rows it sends to shard r are one contiguous block of its permuted
+ * buffer.  The exchange itself is the caller's collective (e.g. an NCCL
+ * all-to-all with these sizes); it needs the sizes on the host, so
+ * group_sizes of every shard (an all-gather of moe_permute's group_sizes) are
+ * HOST arrays here.
+ */
+
+/* Rows of the receive buffer (and of the local buffer) that suffice for any
+ * routing of T tokens per shard: num_ep * (T * min(k, El) + El * (align - 1));
+ * -1 for bad arguments. */
+int64_t moe_ep_recv_rows_cap(int T, int num_ep, int E, int k, int align);
+
+/*
+ * moe_ep_a2a_params -- sizes and offsets of the exchange for shard `shard`
+ * (host computation, no GPU work).
+ *   group_sizes  int32 [num_ep, E] HOST: row s = the group sizes of shard s
+ *   send_off, send_sz  int64 [num_ep] out: rows [send_off[r], +send_sz[r]) of
+ *                this shard's permuted buffer go to shard r
+ *   out_off      int64 [num_ep] out: where those rows start in shard r's
+ *                receive buffer
+ *   recv_off, recv_sz  int64 [num_ep] out: the rows from shard s land at
+ *                [recv_off[s], +recv_sz[s]) of this shard's receive buffer
+ *                (source-major, each source's rows by local expert)
+ * The reverse exchange (combine, dispatch backward) sends (recv_off, recv_sz)
+ * and receives (send_off, send_sz).  E % num_ep == 0, num_ep <= 1024, sizes
+ * >= 0, else MOE_ERR_INVALID_ARG.
+ */
+moe_status_t moe_ep_a2a_params(const int32_t *group_sizes, int num_ep, int E, int shard,
+                               int64_t *send_off, int64_t *send_sz, int64_t *out_off,
+                               int64_t *recv_off, int64_t *recv_sz);
+
+/*
+ * moe_ep_local_layout -- the local permute after the exchange (host
+ * computation).  Chunk (source s, local expert le) holds shard s's rows of
+ * expert shard*El + le, in their order; the local buffer is expert-major
+ * (local expert 0's rows from every source in source order, then local
+ * expert 1's, ...), the layout the grouped GEMMs take.
+ *   fwd_src, fwd_dst, fwd_len  int64 [num_ep * El] out: the chunks in
+ *        receive-buffer order (chunk s*El + le): moe_sort_chunks receive -> local
+ *   inv_src, inv_dst, inv_len  int64 [num_ep * El] out: the same chunks in
+ *        local-buffer order (chunk le*num_ep + s): moe_sort_chunks local -> receive
+ *   local_offsets  int32 [El + 1] out: group offsets of the local experts
+ * Aligned group sizes stay aligned: each source pads its own groups.
+ */
+moe_status_t moe_ep_local_layout(const int32_t *group_sizes, int num_ep, int E, int shard,
+                                 int64_t *fwd_src, int64_t *fwd_dst, int64_t *fwd_len,
+                                 int64_t *inv_src, int64_t *inv_dst, int64_t *inv_len,
+                                 int32_t *local_offsets);
+
+/*
+ * moe_sort_chunks -- move rows chunk by chunk (device): for every chunk c and
+ * 0 <= i < len[c], row src_off[c] + i of src is copied to row dst_off[c] + i
+ * of dst.  src_off, dst_off, len: int64 [n_chunks] DEVICE arrays, src_off
+ * non-decreasing, chunks disjoint in src and in dst; rows: src rows to scan
+ * (>= the end of the last chunk).  src, dst bf16 (16-byte aligned), d, ld_src,
+ * ld_dst multiples of 8.  Rows of dst outside every chunk are not written.
+ */
+moe_status_t moe_sort_chunks(const uint16_t *src, int64_t ld_src, uint16_t *dst, int64_t ld_dst,
+                             int d, const int64_t *src_off, const int64_t *dst_off,
+                             const int64_t *len, int n_chunks, int64_t rows,
+                             moe_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -58,7 +58,7 @@ _SIGS = {
     "moe_set_wait_limit_ns": (_I, [ctypes.c_uint64]),
     "moe_wait_limit_ns": (ctypes.c_uint64, []),
     "moe_test_stall_loads": (None, [_I]),
-    "moe_rows_cap": (_I64, [_I, _I, _I, _I]),
+    "moe_rows_cap": (_I64, [_I, _I, _I, _I, _I]),
     "moe_permute_workspace_bytes": (_SZ, [_I, _I]),
     "moe_route_topk": (_I, [_P, _I64, _I, _I, _I, _I, _I, _P, _I, _I, _P, _P, _P]),
     "moe_aux_loss_workspace_bytes": (_SZ, [_I, _I]),
@@ -72,7 +72,7 @@ _SIGS = {
     "moe_permute_noalloc": (_I, [_P, _I64, _P, _I, _I, _I, _I, _I, _I, _P, _I64, _I64, _P, _P,
                                  _P, _P, _P, _P, _P]),
     "moe_gmm": (_I, [_P, _I64, _P, _I64, _I64, _I, _P, _I, _I64, _I, _I, _I, _P, _I64, _P, _I64,
-                     _P, _I64, _P, _I, _I64, _P, _I64, _P, _P]),
+                     _P, _I64, _P, _I, _I64, _P, _I64, _P, _I64, _P, _P]),
     "moe_group_colsum": (_I, [_P, _I64, _P, _I, _I64, _I, _P, _I64, _P]),
     "moe_tgmm": (_I, [_P, _I64, _P, _I64, _P, _I, _I64, _I, _I, _P, _I, _I64, _I64, _I, _P, _P]),
     "moe_combine": (_I, [_P, _I64, _P, _P, _I, _I, _I, _P, _I64, _P]),
@@ -90,6 +90,10 @@ _SIGS = {
                           _I64, _I, _P, _P]),
     "moe_unpermute_bwd": (_I, [_P, _I64, _P, _I64, _P, _P, _P, _P, _I, _I, _I, _I, _I64, _P,
                                _I64, _P, _P]),
+    "moe_ep_recv_rows_cap": (_I64, [_I, _I, _I, _I, _I]),
+    "moe_ep_a2a_params": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "moe_ep_local_layout": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_sort_chunks": (_I, [_P, _I64, _P, _I64, _I, _P, _P, _P, _I, _I64, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(LIB, _name)
@@ -144,8 +148,8 @@ def moe_test_stall_loads(enable: bool):
     LIB.moe_test_stall_loads(int(bool(enable)))
 
 
-def moe_rows_cap(T: int, E: int, k: int, align: int) -> int:
-    return int(LIB.moe_rows_cap(T, E, k, align))
+def moe_rows_cap(T: int, E: int, k: int, align: int, capacity: int = 0) -> int:
+    return int(LIB.moe_rows_cap(T, E, k, align, capacity))
 
 
 def moe_permute_workspace_bytes(T: int, E: int) -> int:
@@ -219,10 +223,12 @@ def moe_permute_noalloc(x, topk_idx, E, align, capacity, x_sorted, group_sizes, 
 
 
 def moe_gmm(A, B, trans_b, group_offsets, C, epilogue=EPI_NONE, aux=None, partial_sum=None,
-            C2=None, dev_status=None, stream=None, K=None, N=None, bias=None):
+            C2=None, dev_status=None, stream=None, K=None, N=None, bias=None, Ct=None):
     """A [rows_cap, >=K]; B [E, K, N] (trans_b=0) or [E, N, K] (trans_b=1), any
     row-major views; C bf16 or fp32; bias bf16 [E, >=N] (row e added to expert
-    e's rows).  K and N default to the shapes of B."""
+    e's rows); Ct bf16 [F or 2F, >= moe_fp8_padded_rows(rows_cap, E)]: the
+    column-wise copy of Act / dH the SwiGLU epilogues also write.  K and N
+    default to the shapes of B."""
     E = B.shape[0]
     if K is None:
         K = B.shape[2] if trans_b else B.shape[1]
@@ -234,8 +240,8 @@ def moe_gmm(A, B, trans_b, group_offsets, C, epilogue=EPI_NONE, aux=None, partia
                        _ld(aux) if aux is not None else 0, _ptr(partial_sum),
                        _ld(partial_sum) if partial_sum is not None else 0, _ptr(bias),
                        bias.stride(0) if bias is not None else 0, _ptr(C), c_dtype,
-                       _ld(C), _ptr(C2), _ld(C2) if C2 is not None else 0, _ptr(dev_status),
-                       _stream(stream)))
+                       _ld(C), _ptr(C2), _ld(C2) if C2 is not None else 0, _ptr(Ct),
+                       _ld(Ct) if Ct is not None else 0, _ptr(dev_status), _stream(stream)))
 
 
 def moe_group_colsum(G, group_offsets, out, stream=None):
@@ -343,3 +349,57 @@ def moe_unpermute_bwd(d_out, Y, flat_to_sorted, sorted_to_flat, group_offsets, t
                                  _ptr(sorted_to_flat), _ptr(group_offsets), _ptr(topk_w), T, k, d,
                                  E, dY.shape[0], _ptr(dY), _ld(dY), _ptr(d_topk_w),
                                  _stream(stream)))
+
+
+# ------------------------------------------------------------ expert parallelism
+def _np_ptr(a):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def _gs_host(group_sizes):
+    import numpy as np
+    if isinstance(group_sizes, torch.Tensor):
+        group_sizes = group_sizes.cpu().numpy()
+    return np.ascontiguousarray(group_sizes, dtype=np.int32)
+
+
+def moe_ep_recv_rows_cap(T: int, num_ep: int, E: int, k: int, align: int) -> int:
+    return int(LIB.moe_ep_recv_rows_cap(T, num_ep, E, k, align))
+
+
+def moe_ep_a2a_params(group_sizes, shard: int) -> dict:
+    """group_sizes int32 [num_ep, E] (host) -> send_off, send_sz, out_off, recv_off,
+    recv_sz: int64 numpy arrays [num_ep]."""
+    import numpy as np
+    gs = _gs_host(group_sizes)
+    num_ep, E = gs.shape
+    out = {n: np.zeros(num_ep, np.int64)
+           for n in ("send_off", "send_sz", "out_off", "recv_off", "recv_sz")}
+    _check(LIB.moe_ep_a2a_params(_np_ptr(gs), num_ep, E, shard, *(_np_ptr(out[n]) for n in (
+        "send_off", "send_sz", "out_off", "recv_off", "recv_sz"))))
+    return out
+
+
+def moe_ep_local_layout(group_sizes, shard: int) -> dict:
+    """group_sizes int32 [num_ep, E] (host) -> the chunk tables fwd_* / inv_* (int64
+    [num_ep * El]) and local_offsets (int32 [El + 1]), numpy arrays."""
+    import numpy as np
+    gs = _gs_host(group_sizes)
+    num_ep, E = gs.shape
+    n = E  # num_ep * (E / num_ep) chunks
+    names = ("fwd_src", "fwd_dst", "fwd_len", "inv_src", "inv_dst", "inv_len")
+    out = {nm: np.zeros(n, np.int64) for nm in names}
+    out["local_offsets"] = np.zeros(E // num_ep + 1 if E % num_ep == 0 else 1, np.int32)
+    _check(LIB.moe_ep_local_layout(_np_ptr(gs), num_ep, E, shard,
+                                   *(_np_ptr(out[nm]) for nm in names),
+                                   _np_ptr(out["local_offsets"])))
+    return out
+
+
+def moe_sort_chunks(src, dst, src_off, dst_off, length, rows=None, stream=None):
+    """Row mover: src / dst bf16 [rows, d] (row-major views); src_off / dst_off /
+    length int64 device tensors [n_chunks]; rows defaults to src's rows."""
+    d = src.shape[1]
+    _check(LIB.moe_sort_chunks(_ptr(src), _ld(src), _ptr(dst), _ld(dst), d, _ptr(src_off),
+                               _ptr(dst_off), _ptr(length), src_off.shape[0],
+                               src.shape[0] if rows is None else rows, _stream(stream)))

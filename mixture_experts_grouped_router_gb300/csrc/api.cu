@@ -3,6 +3,7 @@
 #include <stdarg.h>
 #include <stdio.h>
 
+#include <algorithm>
 #include <atomic>
 
 #include "internal.h"
@@ -67,7 +68,7 @@ const char *moe_status_string(int status) {
 
 const char *moe_last_error(void) { return moe::g_err; }
 
-int moe_version(void) { return 100; }
+int moe_version(void) { return 200; }
 
 moe_status_t moe_set_wait_limit_ns(uint64_t limit_ns) {
   set_error("");
@@ -81,9 +82,11 @@ uint64_t moe_wait_limit_ns(void) { return moe::wait_limit_ns(); }
 
 void moe_test_stall_loads(int enable) { moe::g_stall_loads.store(enable ? 1 : 0); }
 
-int64_t moe_rows_cap(int T, int E, int k, int align) {
+int64_t moe_rows_cap(int T, int E, int k, int align, int capacity) {
   if (T < 0 || E <= 0 || k <= 0) return -1;
-  return (int64_t)T * k + (int64_t)E * (align > 1 ? align - 1 : 0);
+  int64_t kept = (int64_t)T * k;
+  if (capacity > 0) kept = std::min<int64_t>(kept, (int64_t)E * capacity);
+  return kept + (int64_t)E * (align > 1 ? align - 1 : 0);
 }
 
 size_t moe_permute_workspace_bytes(int T, int E) {
@@ -204,9 +207,9 @@ moe_status_t moe_permute(const uint16_t *x, int64_t ldx, const int32_t *topk_idx
   REQUIRE(d % 8 == 0 && ldx % 8 == 0 && ld_xs % 8 == 0, MOE_ERR_UNSUPPORTED,
           "moe_permute: d, ldx, ld_xs must be multiples of 8");
   REQUIRE(ldx >= d && ld_xs >= d, MOE_ERR_INVALID_ARG, "moe_permute: leading dimension < d");
-  REQUIRE(rows_cap >= moe_rows_cap(T, E, k, align), MOE_ERR_INVALID_ARG,
+  REQUIRE(rows_cap >= moe_rows_cap(T, E, k, align, capacity), MOE_ERR_INVALID_ARG,
           "moe_permute: rows_cap %lld < %lld", (long long)rows_cap,
-          (long long)moe_rows_cap(T, E, k, align));
+          (long long)moe_rows_cap(T, E, k, align, capacity));
   REQUIRE(rows_cap < (1ll << 31) && (int64_t)T * k < (1ll << 31), MOE_ERR_UNSUPPORTED,
           "moe_permute: more than 2^31 rows");
   REQUIRE(group_sizes && kept_counts && group_offsets && workspace &&
@@ -232,11 +235,18 @@ moe_status_t moe_gmm(const uint16_t *A, int64_t lda, const uint16_t *B, int64_t 
                      int64_t rows_cap, int K, int N, int epilogue, const uint16_t *aux,
                      int64_t ld_aux, const float *partial_sum, int64_t ld_ps,
                      const uint16_t *bias, int64_t stride_bias, void *C, int c_dtype,
-                     int64_t ldc, uint16_t *C2, int64_t ldc2, int32_t *dev_status,
-                     moe_stream_t stream) {
+                     int64_t ldc, uint16_t *C2, int64_t ldc2, uint16_t *Ct, int64_t ldct,
+                     int32_t *dev_status, moe_stream_t stream) {
   set_error("");
   REQUIRE(E > 0 && rows_cap >= 0 && K > 0 && N > 0, MOE_ERR_INVALID_ARG,
           "moe_gmm: E=%d rows_cap=%lld K=%d N=%d", E, (long long)rows_cap, K, N);
+  REQUIRE(Ct == nullptr || epilogue != MOE_EPI_NONE, MOE_ERR_INVALID_ARG,
+          "moe_gmm: a column-wise copy (Ct) is written by the SwiGLU epilogues only");
+  REQUIRE(Ct == nullptr || (aligned16(Ct) && ldct % 8 == 0 &&
+                            ldct >= moe::f8_padded_rows(rows_cap, E)),
+          MOE_ERR_INVALID_ARG,
+          "moe_gmm: Ct needs a 16-byte aligned base and ldct >= moe_fp8_padded_rows(rows_cap, "
+          "E), a multiple of 8");
   REQUIRE(epilogue >= MOE_EPI_NONE && epilogue <= MOE_EPI_SWIGLU_BWD, MOE_ERR_INVALID_ARG,
           "moe_gmm: bad epilogue %d", epilogue);
   REQUIRE(c_dtype == MOE_DTYPE_BF16 || c_dtype == MOE_DTYPE_F32, MOE_ERR_INVALID_ARG,
@@ -286,7 +296,7 @@ moe_status_t moe_gmm(const uint16_t *A, int64_t lda, const uint16_t *B, int64_t 
   if (rows_cap == 0) return MOE_OK;
   moe::GmmArgs a{A, lda, B, ldb, stride_b, trans_b, group_offsets, E, rows_cap, K, N, epilogue,
                  aux, ld_aux, partial_sum, ld_ps, bias, stride_bias, C, c_dtype, ldc, C2, ldc2,
-                 dev_status};
+                 Ct, ldct, dev_status};
   return moe::launch_gmm(a, (cudaStream_t)stream);
 }
 
@@ -567,6 +577,78 @@ moe_status_t moe_tgmm_fp8(const uint8_t *At, int64_t ldat, int a_fmt, const floa
   moe::TgmmF8Args a{At, ldat, a_fmt, a_scale_inv, Bt, ldbt, b_fmt, b_scale_inv, group_offsets, E,
                     rows_cap, M, N, W, w_dtype, ldw, stride_w, accumulate, dev_status};
   return moe::launch_tgmm_f8(a, (cudaStream_t)stream);
+}
+
+int64_t moe_ep_recv_rows_cap(int T, int num_ep, int E, int k, int align) {
+  if (T < 0 || num_ep <= 0 || E <= 0 || k <= 0 || E % num_ep != 0) return -1;
+  return moe::ep_recv_rows_cap(T, num_ep, E, k, align);
+}
+
+static moe_status_t ep_check(const char *what, const int32_t *group_sizes, int num_ep, int E,
+                             int shard) {
+  REQUIRE(group_sizes != nullptr, MOE_ERR_INVALID_ARG, "%s: null group_sizes", what);
+  REQUIRE(num_ep >= 1 && num_ep <= 1024 && E >= 1 && E <= 65536 && E % num_ep == 0,
+          MOE_ERR_INVALID_ARG, "%s: E=%d must be a multiple of num_ep=%d (<= 1024)", what, E,
+          num_ep);
+  REQUIRE(shard >= 0 && shard < num_ep, MOE_ERR_INVALID_ARG, "%s: shard %d of %d", what, shard,
+          num_ep);
+  for (int64_t i = 0; i < (int64_t)num_ep * E; ++i)
+    REQUIRE(group_sizes[i] >= 0, MOE_ERR_INVALID_ARG, "%s: group_sizes[%lld] = %d < 0", what,
+            (long long)i, group_sizes[i]);
+  return MOE_OK;
+}
+
+moe_status_t moe_ep_a2a_params(const int32_t *group_sizes, int num_ep, int E, int shard,
+                               int64_t *send_off, int64_t *send_sz, int64_t *out_off,
+                               int64_t *recv_off, int64_t *recv_sz) {
+  set_error("");
+  const moe_status_t st = ep_check("moe_ep_a2a_params", group_sizes, num_ep, E, shard);
+  if (st != MOE_OK) return st;
+  REQUIRE(send_off && send_sz && out_off && recv_off && recv_sz, MOE_ERR_INVALID_ARG,
+          "moe_ep_a2a_params: null output");
+  moe::ep_a2a_params(group_sizes, num_ep, E, shard, send_off, send_sz, out_off, recv_off,
+                     recv_sz);
+  return MOE_OK;
+}
+
+moe_status_t moe_ep_local_layout(const int32_t *group_sizes, int num_ep, int E, int shard,
+                                 int64_t *fwd_src, int64_t *fwd_dst, int64_t *fwd_len,
+                                 int64_t *inv_src, int64_t *inv_dst, int64_t *inv_len,
+                                 int32_t *local_offsets) {
+  set_error("");
+  const moe_status_t st = ep_check("moe_ep_local_layout", group_sizes, num_ep, E, shard);
+  if (st != MOE_OK) return st;
+  REQUIRE(fwd_src && fwd_dst && fwd_len && inv_src && inv_dst && inv_len && local_offsets,
+          MOE_ERR_INVALID_ARG, "moe_ep_local_layout: null output");
+  const int El = E / num_ep;
+  int64_t rows = 0;
+  for (int s = 0; s < num_ep; ++s)
+    for (int le = 0; le < El; ++le) rows += group_sizes[(int64_t)s * E + (int64_t)shard * El + le];
+  REQUIRE(rows < (1ll << 31), MOE_ERR_UNSUPPORTED, "moe_ep_local_layout: %lld rows >= 2^31",
+          (long long)rows);
+  moe::ep_local_layout(group_sizes, num_ep, E, shard, fwd_src, fwd_dst, fwd_len, inv_src, inv_dst,
+                       inv_len, local_offsets);
+  return MOE_OK;
+}
+
+moe_status_t moe_sort_chunks(const uint16_t *src, int64_t ld_src, uint16_t *dst, int64_t ld_dst,
+                             int d, const int64_t *src_off, const int64_t *dst_off,
+                             const int64_t *len, int n_chunks, int64_t rows,
+                             moe_stream_t stream) {
+  set_error("");
+  REQUIRE(d > 0 && n_chunks >= 0 && rows >= 0, MOE_ERR_INVALID_ARG,
+          "moe_sort_chunks: d=%d n_chunks=%d rows=%lld", d, n_chunks, (long long)rows);
+  REQUIRE(ld_src >= d && ld_dst >= d, MOE_ERR_INVALID_ARG, "moe_sort_chunks: ld < d");
+  REQUIRE(d % 8 == 0 && ld_src % 8 == 0 && ld_dst % 8 == 0, MOE_ERR_UNSUPPORTED,
+          "moe_sort_chunks: d, ld_src, ld_dst must be multiples of 8");
+  if (rows == 0 || n_chunks == 0) return MOE_OK;
+  REQUIRE(src && dst && src_off && dst_off && len, MOE_ERR_INVALID_ARG,
+          "moe_sort_chunks: null pointer");
+  REQUIRE(aligned16(src) && aligned16(dst), MOE_ERR_UNSUPPORTED,
+          "moe_sort_chunks: src and dst must be 16-byte aligned");
+  return cuda_status(moe::launch_sort_chunks(src, ld_src, dst, ld_dst, d, src_off, dst_off, len,
+                                             n_chunks, rows, (cudaStream_t)stream),
+                     "moe_sort_chunks launch");
 }
 
 moe_status_t moe_combine(const uint16_t *Y, int64_t ldy, const int32_t *flat_to_sorted,

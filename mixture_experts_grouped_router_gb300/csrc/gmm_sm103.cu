@@ -17,7 +17,7 @@
 //   warp 0      TMA producer: each CTA loads its own 128-row A tile and its
 //               half (128 columns) of the B tile for every K block, both
 //               completing on the leader CTA's barrier (32 KB per CTA and
-//               stage, 6 stages; 5 for the SwiGLU-backward dgrad).  128-byte
+//               stage, 6 stages for every GEMM).  128-byte
 //               swizzle throughout; a K block is one 128-byte row per tile
 //               row (64 bf16 or 128 8-bit codes).
 //   warp 1      TMEM owner; in the leader CTA the MMA issuer: kind::f16
@@ -26,8 +26,8 @@
 //               one tile overlaps the mainloop of the next).  Stages and
 //               finished accumulators are signalled to both CTAs by
 //               multicast commits.
-//   warps 2-5   epilogue (2-9 for the SwiGLU backward: two warps per TMEM
-//               lane quarter, each on half of the columns): tcgen05.ld of one
+//   warps 2-5   epilogue, one warp per TMEM lane quarter (every GEMM):
+//               tcgen05.ld of one
 //               TMEM lane (= one output row) per thread, fused SwiGLU /
 //               partial-sum / bias / FP8-dequantization / cast; each warp
 //               stages its 32x32 output blocks in swizzled shared memory and
@@ -52,7 +52,7 @@ namespace moe {
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 64, UK = 16;
-constexpr int kStages = 6;  // ring slots allocated (the weight-gradient kernel uses 4)
+constexpr int kStages = 6;  // ring slots of the barrier book (every GEMM uses all six)
 constexpr int kMaxEpiWarps = 4;
 constexpr int kPadRows = kF8PadRows;  // group padding of column-wise copies (128 rows)
 constexpr int kStgBytes = 8192;  // per epilogue warp: up to four 32x32 bf16 blocks (or two fp32)
@@ -125,6 +125,8 @@ struct TcParams {
   int c_f32;
   uint16_t *C2;
   int64_t ldc2;
+  uint16_t *Ct;   // column-wise copy of Act (SwiGLU forward) / dH (backward), or null
+  int64_t ldct;
   const float *ps;
   int64_t ld_ps;
   const uint16_t *bias;   // expert e's vector at bias + e * stride_bias, or null
@@ -146,6 +148,7 @@ struct TcParams {
 struct TileInfo {
   int e, m_idx, n_idx, row0, row_end, kblocks;
   int k0;  // weight gradients from a column-wise copy of A: the expert's first column
+  int pcol0;  // ragged-M GEMM: column of the tile's first row in a column-wise copy
 };
 
 // Group offsets read from global memory (through L1), clamped to [0, rows_cap].
@@ -182,6 +185,7 @@ MOE_DEVINL TileInfo decode_tile(const Book &bk, const TcParams &p, int t, int cr
   if (KIND == KIND_GMM) {
     ti.row0 += ti.m_idx * BM;
     ti.kblocks = (p.K + BKE - 1) / BKE;
+    ti.pcol0 = (int)bk.poff[lo] * kPadRows + ti.m_idx * BM;
   } else if (F8) {
     // FP8 weight gradients read the column-wise copies, where expert e's rows
     // fill whole K blocks from poff[e] on (zero padded to 128 rows)
@@ -236,6 +240,42 @@ MOE_DEVINL void stage_f32(uint8_t *buf, int r, const float *v) {
     *reinterpret_cast<uint4 *>(buf + r * 128 + ((c ^ (r & 7)) << 4)) =
         make_uint4(__float_as_uint(v[4 * c]), __float_as_uint(v[4 * c + 1]),
                    __float_as_uint(v[4 * c + 2]), __float_as_uint(v[4 * c + 3]));
+}
+
+// The transposed layout of stage_bf16: thread r's 32 values become column r
+// of the 32 x 32 block (block row n = value n), rows of 64 bytes under the
+// 64-byte swizzle.  Lanes r and r^1 trade one value per row pair so that each
+// writes 32-bit words (the even lane rows 2m, the odd lane rows 2m+1): every
+// store instruction fills two whole 64-byte rows, free of bank conflicts.
+MOE_DEVINL void stage_bf16_t(uint8_t *buf, int r, const float *v) {
+  const bool odd = r & 1;
+  const int off = ((r >> 1) & 3) * 4;  // byte of the word within its 16-byte chunk
+  const int chunk = r >> 3;
+#pragma unroll
+  for (int m = 0; m < 16; ++m) {
+    const float recv = __shfl_xor_sync(0xffffffffu, odd ? v[2 * m] : v[2 * m + 1], 1);
+    const int n = 2 * m + (odd ? 1 : 0);
+    const __nv_bfloat162 w = odd ? __floats2bfloat162_rn(recv, v[2 * m + 1])
+                                 : __floats2bfloat162_rn(v[2 * m], recv);
+    *reinterpret_cast<__nv_bfloat162 *>(buf + n * 64 + ((chunk ^ ((n >> 1) & 3)) << 4) + off) = w;
+  }
+}
+
+// The same transposed block written straight to global memory: column-wise
+// copy rows [nc, nc + 32) (those below nmax) at columns [pc0, pc0 + 32); each
+// store instruction writes two contiguous 64-byte row segments.
+MOE_DEVINL void store_bf16_t(uint16_t *Ct, int64_t ldct, int64_t pc0, int nc, int nmax, int r,
+                             const float *v) {
+  const bool odd = r & 1;
+  uint16_t *base = Ct + pc0 + (r & ~1);
+#pragma unroll
+  for (int m = 0; m < 16; ++m) {
+    const float recv = __shfl_xor_sync(0xffffffffu, odd ? v[2 * m] : v[2 * m + 1], 1);
+    const int n = 2 * m + (odd ? 1 : 0);
+    const __nv_bfloat162 w = odd ? __floats2bfloat162_rn(recv, v[2 * m + 1])
+                                 : __floats2bfloat162_rn(v[2 * m], recv);
+    if (nc + n < nmax) *reinterpret_cast<__nv_bfloat162 *>(base + (int64_t)(nc + n) * ldct) = w;
+  }
 }
 
 // The warp's staging buffers may be rewritten once the previous bulk stores
@@ -353,6 +393,11 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
   // FP8 GEMMs track their output amax and take no partial sum or bias; bf16
   // ones the reverse (compile-time, so neither pays the other's registers)
   const bool track = F8 && p.amax_out != nullptr && valid;
+  // column-wise copy of the activation output: every 32-row block of a tile
+  // that starts inside the expert, rows past the expert as zeros (they are the
+  // expert's padding in the copy); a tile past the expert writes nothing
+  const bool colwise = !F8 && p.Ct != nullptr && ti.row0 < ti.row_end;
+  const int64_t pc0 = (int64_t)ti.pcol0 + q * 32;
   if (EPI == MOE_EPI_SWIGLU_FWD) {
     const int F = p.F;
     const int n0 = ti.n_idx * (BN / 2);
@@ -417,19 +462,32 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
 #pragma unroll
       for (int j = 0; j < 32; ++j) act[j] = g[j] * sigmoid_f(g[j]) * u[j];
       if (track) amx = chunk_amax(amx, act, F - nc);
-      if (bulk) {
+      if (bulk || colwise) {
         stage_acquire(lane);
-        stage_bf16(stg, lane, g);
-        stage_bf16(stg + 2048, lane, u);
-        stage_bf16(stg + 4096, lane, act);
+        if (bulk) {
+          stage_bf16(stg, lane, g);
+          stage_bf16(stg + 2048, lane, u);
+          stage_bf16(stg + 4096, lane, act);
+        }
+        if (colwise) {
+          if (!valid) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) act[j] = 0.0f;
+          }
+          stage_bf16_t(stg + 6144, lane, act);
+        }
         stage_release();
         if (lane == 0) {
-          tc::tma_store_2d_hint(om.m0, stg, nc, wrow0, om.stream_pol);
-          tc::tma_store_2d_hint(om.m1, stg + 2048, nc, wrow0, om.stream_pol);
-          tc::tma_store_2d(om.m2, stg + 4096, nc, wrow0);
+          if (bulk) {
+            tc::tma_store_2d_hint(om.m0, stg, nc, wrow0, om.stream_pol);
+            tc::tma_store_2d_hint(om.m1, stg + 2048, nc, wrow0, om.stream_pol);
+            tc::tma_store_2d(om.m2, stg + 4096, nc, wrow0);
+          }
+          if (colwise) tc::tma_store_2d(om.m3, stg + 6144, (int)pc0, nc);
           tc::bulk_commit();
         }
-      } else if (valid) {
+      }
+      if (!bulk && valid) {
         uint16_t *H = static_cast<uint16_t *>(p.C) + row * p.ldc;
         uint16_t *A = p.C2 + row * p.ldc2;
 #pragma unroll
@@ -483,6 +541,14 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
       if (track) {
         amx = chunk_amax(amx, dg, N - nc);
         amx = chunk_amax(amx, du, N - nc);
+      }
+      if (colwise) {
+        if (!valid) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) dg[j] = du[j] = 0.0f;
+        }
+        store_bf16_t(p.Ct, p.ldct, pc0, nc, N, lane, dg);
+        store_bf16_t(p.Ct + (int64_t)N * p.ldct, p.ldct, pc0, nc, N, lane, du);
       }
       if (bulk) {
         stage_acquire(lane);
@@ -1085,6 +1151,8 @@ moe_status_t launch_gmm(const GmmArgs &a, cudaStream_t s) {
   p.c_f32 = a.c_dtype == MOE_DTYPE_F32;
   p.C2 = a.C2;
   p.ldc2 = a.ldc2;
+  p.Ct = a.Ct;
+  p.ldct = a.ldct;
   p.ps = a.ps;
   p.ld_ps = a.ld_ps;
   p.bias = a.bias;
@@ -1103,7 +1171,11 @@ moe_status_t launch_gmm(const GmmArgs &a, cudaStream_t s) {
     ok = make_out_map(&mc[0], H, false, p.F, a.rows_cap, a.ldc) &&
          make_out_map(&mc[1], H + p.F, false, p.F, a.rows_cap, a.ldc) &&
          make_out_map(&mc[2], a.C2, false, p.F, a.rows_cap, a.ldc2);
-    mc[3] = mc[0];
+    // m3: the column-wise copy Act^T [F, padded rows] (transposed 32 x 32 blocks)
+    if (a.Ct != nullptr)
+      ok = ok && make_out_map(&mc[3], a.Ct, false, f8_padded_rows(a.rows_cap, a.E), p.F, a.ldct);
+    else
+      mc[3] = mc[0];
   } else if (a.epilogue == MOE_EPI_SWIGLU_BWD) {
     const uint16_t *dH = static_cast<const uint16_t *>(a.C);
     // m0/m1: dH gate / up (stores); m2/m3: H gate / up (loads, same block shape)

@@ -69,6 +69,17 @@ cudaError_t launch_group_colsum(const uint16_t *G, int64_t ldg, const int32_t *o
                                int64_t rows_cap, int N, float *out, int64_t ld_out,
                                cudaStream_t s);
 
+// ep.cu (expert-parallel exchange: host bookkeeping and the row mover)
+int64_t ep_recv_rows_cap(int T, int num_ep, int E, int k, int align);
+void ep_a2a_params(const int32_t *gs, int num_ep, int E, int shard, int64_t *send_off,
+                   int64_t *send_sz, int64_t *out_off, int64_t *recv_off, int64_t *recv_sz);
+void ep_local_layout(const int32_t *gs, int num_ep, int E, int shard, int64_t *fwd_src,
+                     int64_t *fwd_dst, int64_t *fwd_len, int64_t *inv_src, int64_t *inv_dst,
+                     int64_t *inv_len, int32_t *local_offsets);
+cudaError_t launch_sort_chunks(const uint16_t *src, int64_t ld_src, uint16_t *dst, int64_t ld_dst,
+                               int d, const int64_t *src_off, const int64_t *dst_off,
+                               const int64_t *len, int n_chunks, int64_t rows, cudaStream_t s);
+
 // gmm_sm103.cu
 struct GmmArgs {
   const uint16_t *A; int64_t lda;
@@ -80,6 +91,7 @@ struct GmmArgs {
   const uint16_t *bias; int64_t stride_bias;
   void *C; int c_dtype; int64_t ldc;
   uint16_t *C2; int64_t ldc2;
+  uint16_t *Ct; int64_t ldct;  // column-wise copy of Act / dH (SwiGLU epilogues), or null
   int32_t *dev_status;
 };
 moe_status_t launch_gmm(const GmmArgs &a, cudaStream_t s);

@@ -45,14 +45,22 @@ permute_count_kernel(const int32_t *__restrict__ topk_idx, int T, int E, int k, 
   __shared__ int32_t hist[kMaxE];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
-  const int64_t a0 = (int64_t)blockIdx.x * tpb * k;
-  const int64_t a1 = min((int64_t)T, (int64_t)(blockIdx.x + 1) * tpb) * k;
-  for (int64_t a = a0 + threadIdx.x; a < a1; a += blockDim.x) {
-    const int e = __ldg(topk_idx + a);
-    if (e >= 0 && e < E)
-      atomicAdd(&hist[e], 1);
-    else
-      moe_set_status(dev_status, MOE_ERR_DEVICE);
+  // thread = token: an expert id out of range, or one the token already
+  // listed in an earlier slot, is not counted (the rank kernel drops the same
+  // assignments, so every counted assignment gets a row)
+  const int t0 = blockIdx.x * tpb;
+  const int t1 = (int)min((int64_t)T, (int64_t)t0 + tpb);
+  for (int t = t0 + threadIdx.x; t < t1; t += blockDim.x) {
+    const int32_t *ids = topk_idx + (int64_t)t * k;
+    for (int j = 0; j < k; ++j) {
+      const int e = __ldg(ids + j);
+      bool ok = e >= 0 && e < E;
+      for (int i = 0; i < j && ok; ++i) ok = __ldg(ids + i) != e;
+      if (ok)
+        atomicAdd(&hist[e], 1);
+      else
+        moe_set_status(dev_status, MOE_ERR_DEVICE);
+    }
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) counts[(int64_t)blockIdx.x * E + e] = hist[e];

@@ -12,11 +12,16 @@
 // The array is a file-scope __device__ variable: every GPU that loads the
 // library holds it (kNoallocScratchInts * 4 bytes) until the process exits.
 // Its address is looked up once per device, on the first call made while that
-// device is current; make that first call before any stream capture.  All
+// device is current; make that first call before any stream capture.  The
+// lookup is tied to the device's context: after cudaDeviceReset() the array
+// lives in a new context at a possibly different address, so the first call
+// made in the new context looks it up again (also before any capture).  All
 // calls share the one array, so calls whose kernels overlap on the GPU (two
 // streams, or two host threads) race on it and must be serialised by the
 // caller.  The counts are fully written by every call before they are read, so
 // nothing left from an earlier call is ever used.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "internal.h"
@@ -34,19 +39,52 @@ constexpr size_t kNoallocScratchInts = sizeof(g_permute_scratch) / sizeof(int32_
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
 int32_t *g_scratch_ptr[kMaxDevices] = {nullptr};
+unsigned long long g_scratch_ctx[kMaxDevices] = {0};  // context the address belongs to
 
-// Device address of the scratch array on the current device (set-up on first use).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+
+// Unique id of the calling thread's current context (0 if there is none yet
+// or the driver cannot tell); ids are never reused within a process.
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  if (get_current == nullptr || get_id == nullptr) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of the scratch array on the current device: looked up on
+// the first call in the device's context, kept for the later ones.
 cudaError_t scratch_address(int32_t **out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_mutex);
-  if (g_scratch_ptr[dev] == nullptr) {
+  const unsigned long long ctx = current_context_id();
+  if (g_scratch_ptr[dev] == nullptr || ctx == 0 || ctx != g_scratch_ctx[dev]) {
     void *ptr = nullptr;
     e = cudaGetSymbolAddress(&ptr, g_permute_scratch);
     if (e != cudaSuccess) return e;
     g_scratch_ptr[dev] = static_cast<int32_t *>(ptr);
+    // the lookup made the device's primary context current if it was not yet
+    g_scratch_ctx[dev] = ctx != 0 ? ctx : current_context_id();
   }
   *out = g_scratch_ptr[dev];
   return cudaSuccess;

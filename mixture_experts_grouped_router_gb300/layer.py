@@ -13,9 +13,11 @@ backward  unpermute_bwd -> route_topk_bwd (d_logits) -> gmm(dgrad down, SwiGLU-b
           weights (dispatch bwd)
 
 Routing options: group-limited top-k (num_groups > 1: only the topk_group
-best expert groups compete) and, with aux_coeff > 0, the auxiliary
-load-balancing loss (forward: b.aux_loss; backward: its logit gradient is
-added to b.d_logits).
+best expert groups compete), DeepSeek-V3's per-expert selection bias
+(``forward(..., expert_bias=...)``: experts are ranked by logit + bias, the
+routing weights use the unbiased logits) and, with aux_coeff > 0, the
+auxiliary load-balancing loss (forward: b.aux_loss; backward: its logit
+gradient is added to b.d_logits).
 
 With fp8=True the four GEMMs run on 8-bit float codes with current tensor
 scaling (MaxText PR #2319, "[Draft] Integrate TE/JAX GroupedGEMM for MoE",
@@ -26,6 +28,15 @@ and a column-wise copy (the latter feeds the weight-gradient GEMMs).
 With bias=True the expert FFN carries biases (bi [E, 2f] on [gate | up],
 bo [E, d] on the output), added in the GEMM epilogues; their gradients are
 per-expert column sums of dH and dY (moe_group_colsum).
+
+Weight gradients (bf16): by default the weight-gradient GEMMs read the
+row-wise tensors as stored (MN-major operands).  With wgrad_colwise both
+operands of dWo = Act^T dY and dWi = Xs^T dH are read K-major from
+column-wise copies in the padded group layout instead: the SwiGLU forward /
+backward epilogues write the copies of Act and dH beside their row-wise
+outputs, moe_transpose_act makes those of Xs and dY.  The weight gradients
+then run 10% faster, but writing the copies costs more than that on a
+power-capped GB300, so it is not the default.
 
 With num_chunks > 1 the up-projection runs as num_chunks K-chunks of d_model
 accumulating into an fp32 partial sum in place (MaxText PR #4295, "Overlap
@@ -58,6 +69,7 @@ class LayerShape:
     topk_group: int = 0
     aux_coeff: float = 0.0
     fp8: bool = False
+    wgrad_colwise: bool = False
 
 
 class MoEBuffers:
@@ -66,7 +78,11 @@ class MoEBuffers:
     def __init__(self, s: LayerShape, device="cuda", dw_dtype=torch.bfloat16):
         self.s = s
         T, d, f, E, k = s.T, s.d, s.f, s.E, s.k
-        self.rows_cap = L.moe_rows_cap(T, E, k, s.align)
+        if s.num_chunks > 1 and d % s.num_chunks != 0:
+            # the chunks must tile d_model exactly (MaxText PR #4295, Description:
+            # the up-projection is split evenly along d_model)
+            raise ValueError("num_chunks=%d does not divide d_model=%d" % (s.num_chunks, d))
+        self.rows_cap = L.moe_rows_cap(T, E, k, s.align, s.capacity)
         R = self.rows_cap
         bf, i32, f32 = torch.bfloat16, torch.int32, torch.float32
         dev = device
@@ -97,6 +113,14 @@ class MoEBuffers:
         self.dbi = torch.empty(E, 2 * f, dtype=f32, device=dev) if s.bias else None
         self.dbo = torch.empty(E, d, dtype=f32, device=dev) if s.bias else None
         self.dev_status = torch.zeros(1, dtype=i32, device=dev)
+        self.colwise = s.wgrad_colwise and not s.fp8
+        if self.colwise:
+            # column-wise copies (padded group layout) of the weight gradients' operands
+            P = L.moe_fp8_padded_rows(R, E)
+            self.xs_t = torch.empty(d, P, dtype=bf, device=dev)
+            self.act_t = torch.empty(f, P, dtype=bf, device=dev)
+            self.dy_t = torch.empty(d, P, dtype=bf, device=dev)
+            self.dh_t = torch.empty(2 * f, P, dtype=bf, device=dev)
         if s.fp8:
             if s.bias or s.num_chunks > 1:
                 raise ValueError("the FP8 layer takes neither biases nor K-chunks")
@@ -188,9 +212,12 @@ def _backward_fp8(b, stream, mark):
     mark("tgmm_dwi")
 
 
-def forward(b: MoEBuffers, x, logits, wi, wo, stream=None, mark=_noop, bi=None, bo=None):
+def forward(b: MoEBuffers, x, logits, wi, wo, stream=None, mark=_noop, bi=None, bo=None,
+            expert_bias=None):
     """x bf16 [T,d], logits fp32 [T,E], wi bf16 [E,d,2f] ([wi_0 | wi_1]), wo bf16 [E,f,d];
-    with a bias layer shape also bi bf16 [E,2f] and bo bf16 [E,d].
+    with a bias layer shape also bi bf16 [E,2f] and bo bf16 [E,d]; expert_bias fp32 [E]
+    or None: DeepSeek-V3's selection bias (MaxText PR #2579, "Onboard explicit sharding
+    to deepseek": the weights keep the pre-bias logits).
 
     ``mark(name)`` is called after each library call (the benchmark records a
     CUDA event there)."""
@@ -199,7 +226,8 @@ def forward(b: MoEBuffers, x, logits, wi, wo, stream=None, mark=_noop, bi=None, 
         raise ValueError("forward: pass bi and bo exactly when the layer shape has bias=True")
     b.logits = logits
     L.moe_route_topk(logits, s.k, s.score_fn, s.renorm, b.topk_idx, b.topk_w, stream,
-                     num_groups=s.num_groups, topk_group=s.topk_group)
+                     expert_bias=expert_bias, num_groups=s.num_groups,
+                     topk_group=s.topk_group)
     mark("route")
     if s.aux_coeff:
         L.moe_aux_loss(logits, b.topk_idx, s.score_fn, s.aux_coeff, b.aux_counts, b.aux_probs,
@@ -213,9 +241,10 @@ def forward(b: MoEBuffers, x, logits, wi, wo, stream=None, mark=_noop, bi=None, 
         L.moe_combine(b.y, b.f2s, b.topk_w, b.out, s.k, stream)
         mark("combine")
         return b.out
+    act_t = b.act_t if b.colwise else None
     if s.num_chunks <= 1:
         L.moe_gmm(b.xs, wi, 0, b.group_offsets, b.h, L.EPI_SWIGLU_FWD, C2=b.act,
-                  dev_status=b.dev_status, stream=stream, bias=bi)
+                  dev_status=b.dev_status, stream=stream, bias=bi, Ct=act_t)
         mark("gmm_up_swiglu")
     else:
         dc = s.d // s.num_chunks
@@ -226,7 +255,7 @@ def forward(b: MoEBuffers, x, logits, wi, wo, stream=None, mark=_noop, bi=None, 
             ps = None if c == 0 else b.p
             if last:
                 L.moe_gmm(a_c, w_c, 0, b.group_offsets, b.h, L.EPI_SWIGLU_FWD, partial_sum=ps,
-                          C2=b.act, dev_status=b.dev_status, stream=stream, bias=bi)
+                          C2=b.act, dev_status=b.dev_status, stream=stream, bias=bi, Ct=act_t)
                 mark("gmm_up_chunk_swiglu")
             else:
                 L.moe_gmm(a_c, w_c, 0, b.group_offsets, b.p, L.EPI_NONE, partial_sum=ps,
@@ -261,21 +290,39 @@ def backward(b: MoEBuffers, dout, wi, wo, stream=None, mark=_noop):
         return b.dx, b.dwi, b.dwo, b.d_topk_w
     # dAct = dY . wo^T, fused with the SwiGLU backward into dH = [dgate | dup]
     L.moe_gmm(b.dy, wo, 1, b.group_offsets, b.dh, L.EPI_SWIGLU_BWD, aux=b.h,
-              dev_status=b.dev_status, stream=stream)
+              dev_status=b.dev_status, stream=stream, Ct=b.dh_t if b.colwise else None)
     mark("gmm_dgrad_down_swiglu_bwd")
-    L.moe_tgmm(b.act, b.dy, b.group_offsets, b.dwo, dev_status=b.dev_status, stream=stream)
+    if b.colwise:
+        L.moe_transpose_act(b.dy, b.group_offsets, b.dy_t, stream)
+        mark("transpose_dy")
+        L.moe_tgmm_kt(b.act_t, b.dy_t, b.group_offsets, b.rows_cap, b.dwo,
+                      dev_status=b.dev_status, stream=stream, b_colwise=True)
+    else:
+        L.moe_tgmm(b.act, b.dy, b.group_offsets, b.dwo, dev_status=b.dev_status, stream=stream)
     mark("tgmm_dwo")
     if s.bias:
         L.moe_group_colsum(b.dy, b.group_offsets, b.dbo, stream)
         mark("colsum_dbo")
         L.moe_group_colsum(b.dh, b.group_offsets, b.dbi, stream)
         mark("colsum_dbi")
+    if b.colwise:
+        L.moe_transpose_act(b.xs, b.group_offsets, b.xs_t, stream)
+        mark("transpose_xs")
+
+    def tgmm_dwi(sl, name):
+        if b.colwise:
+            L.moe_tgmm_kt(b.xs_t[sl], b.dh_t, b.group_offsets, b.rows_cap, b.dwi[:, sl, :],
+                          dev_status=b.dev_status, stream=stream, b_colwise=True)
+        else:
+            L.moe_tgmm(b.xs[:, sl], b.dh, b.group_offsets, b.dwi[:, sl, :],
+                       dev_status=b.dev_status, stream=stream)
+        mark(name)
+
     if s.num_chunks <= 1:
         L.moe_gmm(b.dh, wi, 1, b.group_offsets, b.dxs, L.EPI_NONE, dev_status=b.dev_status,
                   stream=stream)
         mark("gmm_dgrad_up")
-        L.moe_tgmm(b.xs, b.dh, b.group_offsets, b.dwi, dev_status=b.dev_status, stream=stream)
-        mark("tgmm_dwi")
+        tgmm_dwi(slice(0, s.d), "tgmm_dwi")
     else:
         dc = s.d // s.num_chunks
         for c in range(s.num_chunks):
@@ -283,9 +330,7 @@ def backward(b: MoEBuffers, dout, wi, wo, stream=None, mark=_noop):
             L.moe_gmm(b.dh, wi[:, sl, :], 1, b.group_offsets, b.dxs[:, sl], L.EPI_NONE,
                       dev_status=b.dev_status, stream=stream)
             mark("gmm_dgrad_up_chunk")
-            L.moe_tgmm(b.xs[:, sl], b.dh, b.group_offsets, b.dwi[:, sl, :],
-                       dev_status=b.dev_status, stream=stream)
-            mark("tgmm_dwi_chunk")
+            tgmm_dwi(sl, "tgmm_dwi_chunk")
     L.moe_combine(b.dxs, b.f2s, None, b.dx, s.k, stream)
     mark("dispatch_bwd")
     return b.dx, b.dwi, b.dwo, b.d_topk_w
@@ -294,7 +339,7 @@ def backward(b: MoEBuffers, dout, wi, wo, stream=None, mark=_noop):
 def kernels_per_step(s: LayerShape) -> int:
     """Kernels one forward + backward launches (route 1, permute 3, each GEMM 1,
     combine 1, unpermute_bwd 1, route_bwd 1, dispatch backward 1, bias gradients 2,
-    auxiliary loss 2 + 1)."""
+    auxiliary loss 2 + 1, column-wise copies of dY and Xs 2)."""
     up = max(1, s.num_chunks)
     aux = bool(s.aux_coeff)
     fwd = 1 + 3 + up + 1 + 1 + (2 if aux and s.T > 0 else 1 if aux else 0)
@@ -302,6 +347,8 @@ def kernels_per_step(s: LayerShape) -> int:
     if s.fp8:   # amax + quantize for x, wi, wo; quantize for act (amax in the GEMM);
         fwd += 7   # amax + quantize for dy; quantize for dh
         bwd += 3
+    elif s.wgrad_colwise:
+        bwd += 2
     return fwd + bwd
 
 

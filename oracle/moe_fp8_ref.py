@@ -104,6 +104,20 @@ def encode(x, fmt: str) -> np.ndarray:
     return code.astype(np.uint8)
 
 
+def encode_lib(x, fmt: str) -> np.ndarray:
+    """The codes of encode() through PyTorch's float8 conversion (round to
+    nearest, ties to even) after saturating to the largest finite value; NaN
+    gives the NaN code 0x7F as in encode().  A library step for tensors of
+    billions of elements, where encode's per-element search over the value
+    grid is too slow; the CPU tests pin it to encode() code for code."""
+    import torch
+    x32 = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    mx = np.float32(fp8_max(fmt))
+    dt = torch.float8_e4m3fn if fmt == E4M3 else torch.float8_e5m2
+    codes = torch.from_numpy(np.clip(x32, -mx, mx)).to(dt).view(torch.uint8).numpy()
+    return np.where(np.isnan(x32), np.uint8(0x7F), codes).astype(np.uint8)
+
+
 def current_scale(amax: float, fmt: str) -> np.float32:
     """fp32 scale fp8_max / amax (1 when amax is 0 or not finite)."""
     amax = np.float32(amax)
@@ -185,3 +199,66 @@ def backward(fw: dict, d_out, k):
     dx = moe_ref.dispatch_bwd(d_xs, lay["flat_to_sorted"], T, k)
     return dict(dy=dy, dy_q=dy_q, d_topk_w=d_topk_w, d_act=d_act, dh=dh, dh_q=dh_q, d_wo=d_wo,
                 d_xs=d_xs, d_wi=d_wi, dx=dx, scales=dict(dy=s_dy, dh=s_dh))
+
+
+def _qdq_lib(x, scale, fmt):
+    """dequantize(quantize(x, scale)) with the codes from encode_lib."""
+    xs = (np.asarray(x, dtype=np.float32) * np.float32(scale)).astype(np.float32)
+    return dequantize(encode_lib(xs, fmt), scale, fmt)
+
+
+def layer_scales(x, logits, wi, wo, d_out, k, score_fn, renorm, align=0, capacity=0,
+                 block_rows=2048):
+    """The scales forward() and backward() take, for a layer too large to keep
+    every intermediate: x, Act, dY, dH one each, wi and wo one per expert.
+
+    The same steps as forward / backward (routing, permutation, per-tensor
+    amax of the bf16-rounded tensors, per-expert amax of the weights), with
+    the grouped GEMMs of Act = SwiGLU(Xs_q wi_q) and dH = SwiGLU'(H, dY_q wo_q^T)
+    taken expert by expert over blocks of rows in fp64, keeping only each
+    block's amax.  dY = w[t, j] * d_out[t] on the row of every kept assignment
+    (TE-2912, review thread on _combine_bwd), zero on padding rows.
+    wi, wo: anything that gives expert e's weights as wi[e] (converted to
+    float64 one expert at a time) and E as len(wi).
+    Returns the routing, the layout, Xs_q and dY_q (dequantized, R rows) and
+    the scales (fp32 numbers; wi, wo arrays of E)."""
+    E = len(wi)
+    T, d = x.shape
+    topk_idx, topk_w = moe_ref.route_topk(logits, k, score_fn, renorm)
+    lay = moe_ref.permute_layout(topk_idx, E, align, capacity)
+    off = lay["group_offsets"]
+    R = lay["R"]
+    xs = moe_ref.permute_rows(x, lay, k)[:R]
+    s_x = current_scale(np.abs(xs.astype(np.float32)).max() if R else 0.0, E4M3)
+    xs_q = _qdq_lib(xs, s_x, E4M3)
+    s2f = lay["sorted_to_flat"]
+    kept = s2f >= 0
+    dy = np.zeros((R, d))
+    a = s2f[kept]
+    dy[kept] = round_bf16(topk_w.reshape(-1)[a][:, None] * d_out[a // k])
+    s_dy = current_scale(np.abs(dy.astype(np.float32)).max() if R else 0.0, E5M2)
+    dy_q = _qdq_lib(dy, s_dy, E5M2)
+    s_wi = np.empty(E, np.float32)
+    s_wo = np.empty(E, np.float32)
+    amax_act = 0.0
+    amax_dh = 0.0
+    for e in range(E):
+        wi_e = np.asarray(wi[e], dtype=np.float64)
+        wo_e = np.asarray(wo[e], dtype=np.float64)
+        s_wi[e] = current_scale(np.abs(wi_e.astype(np.float32)).max(), E4M3)
+        s_wo[e] = current_scale(np.abs(wo_e.astype(np.float32)).max(), E4M3)
+        lo, hi = int(off[e]), int(off[e + 1])
+        if hi == lo:
+            continue
+        wi_q = _qdq_lib(wi_e, s_wi[e], E4M3)
+        wo_q = _qdq_lib(wo_e, s_wo[e], E4M3)
+        for r0 in range(lo, hi, block_rows):
+            r1 = min(hi, r0 + block_rows)
+            h = xs_q[r0:r1] @ wi_q
+            amax_act = max(amax_act, float(np.abs(round_bf16(moe_ref.swiglu(h))).max()))
+            d_act = dy_q[r0:r1] @ wo_q.T
+            dh = round_bf16(moe_ref.swiglu_bwd(round_bf16(h), d_act))
+            amax_dh = max(amax_dh, float(np.abs(dh).max()))
+    return dict(topk_idx=topk_idx, topk_w=topk_w, layout=lay, xs_q=xs_q, dy_q=dy_q,
+                scales=dict(x=s_x, act=current_scale(amax_act, E4M3), dy=s_dy,
+                            dh=current_scale(amax_dh, E5M2), wi=s_wi, wo=s_wo))

@@ -431,7 +431,7 @@ def group_colsum(g: np.ndarray, group_offsets, E: int):
 
 
 def forward(x, logits, wi, wo, k, score_fn, renorm, align=0, capacity=0, num_chunks=1,
-            bi=None, bo=None, num_groups=0, topk_group=0):
+            bi=None, bo=None, num_groups=0, topk_group=0, expert_bias=None):
     """The layer's forward pass (TE-2912, sequence diagram of ``_moe_fwd_rule``
     without the expert-parallel all-to-all).
 
@@ -440,13 +440,14 @@ def forward(x, logits, wi, wo, k, score_fn, renorm, align=0, capacity=0, num_chu
     d_model into an fp32-style partial sum P (MT-4295, Description: each
     chunk's gmm adds into the partial sum in place), then SwiGLU runs on P.
     Optional MLP biases bi [E, 2f] (added to [gate | up]) and bo [E, d];
-    optional group-limited routing (num_groups, topk_group; see route_topk).
+    optional group-limited routing (num_groups, topk_group) and selection
+    bias (expert_bias), both as in route_topk.
     Returns a dict of every intermediate the backward needs.
     """
     T, d = x.shape
     E = wi.shape[0]
-    topk_idx, topk_w = route_topk(logits, k, score_fn, renorm, num_groups=num_groups,
-                                  topk_group=topk_group)
+    topk_idx, topk_w = route_topk(logits, k, score_fn, renorm, expert_bias=expert_bias,
+                                  num_groups=num_groups, topk_group=topk_group)
     lay = permute_layout(topk_idx, E, align, capacity)
     xs = permute_rows(x, lay, k)
     off = lay["group_offsets"]

@@ -41,32 +41,38 @@ def assert_close(name, got, want, rel_fro=REL_FRO, max_rel=MAX_REL):
     assert mdiff <= max_rel * mref, "%s: max diff %.3g > %g * %.3g" % (name, mdiff, max_rel, mref)
 
 
-def layer_shape(cfg, bias=False, num_groups=0, topk_group=0, aux_coeff=0.0):
+def layer_shape(cfg, bias=False, num_groups=0, topk_group=0, aux_coeff=0.0,
+                wgrad_colwise=False):
     from mixture_experts_grouped_router_gb300 import layer
     return layer.LayerShape(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.score_fn, cfg.renorm,
                             cfg.align, cfg.capacity, cfg.num_chunks, bias,
-                            num_groups=num_groups, topk_group=topk_group, aux_coeff=aux_coeff)
+                            num_groups=num_groups, topk_group=topk_group, aux_coeff=aux_coeff,
+                            wgrad_colwise=wgrad_colwise)
 
 
 def run_gpu_layer(cfg, inp, device="cuda", dw_dtype=torch.bfloat16, biases=None, num_groups=0,
-                  topk_group=0, aux_coeff=0.0):
+                  topk_group=0, aux_coeff=0.0, expert_bias=None, wgrad_colwise=False):
     """biases: None or the dict of moe_synth.make_biases; num_groups / topk_group /
-    aux_coeff: the routing options of the layer."""
+    aux_coeff / expert_bias (fp32 [E] numpy or None): the routing options of the layer;
+    wgrad_colwise: weight gradients from column-wise copies."""
     from mixture_experts_grouped_router_gb300 import layer
     x, wi, wo, dout = (dev_bf16(inp[n], device) for n in ("x", "wi", "wo", "dout"))
     logits = torch.from_numpy(inp["logits"]).to(device)
-    shape = layer_shape(cfg, biases is not None, num_groups, topk_group, aux_coeff)
+    shape = layer_shape(cfg, biases is not None, num_groups, topk_group, aux_coeff,
+                        wgrad_colwise)
     b = layer.MoEBuffers(shape, device=device, dw_dtype=dw_dtype)
     bi = bo = None
     if biases is not None:
         bi, bo = dev_bf16(biases["bi"], device), dev_bf16(biases["bo"], device)
-    layer.forward(b, x, logits, wi, wo, bi=bi, bo=bo)
+    eb = None if expert_bias is None else torch.from_numpy(
+        np.asarray(expert_bias, np.float32)).to(device)
+    layer.forward(b, x, logits, wi, wo, bi=bi, bo=bo, expert_bias=eb)
     layer.backward(b, dout, wi, wo)
     torch.cuda.synchronize()
     return b
 
 
-def run_oracle(cfg, inp, biases=None, num_groups=0, topk_group=0):
+def run_oracle(cfg, inp, biases=None, num_groups=0, topk_group=0, expert_bias=None):
     f64 = moe_synth.bits_to_f64
     x, wi, wo, dout = (f64(inp[n]) for n in ("x", "wi", "wo", "dout"))
     bi = bo = None
@@ -74,7 +80,7 @@ def run_oracle(cfg, inp, biases=None, num_groups=0, topk_group=0):
         bi, bo = f64(biases["bi"]), f64(biases["bo"])
     fw = moe_ref.forward(x, inp["logits"], wi, wo, cfg.k, cfg.score_fn, cfg.renorm, cfg.align,
                          cfg.capacity, cfg.num_chunks, bi=bi, bo=bo, num_groups=num_groups,
-                         topk_group=topk_group)
+                         topk_group=topk_group, expert_bias=expert_bias)
     bw = moe_ref.backward(fw, dout, wi, wo, cfg.k, cfg.num_chunks)
     return fw, bw
 

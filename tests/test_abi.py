@@ -44,9 +44,14 @@ def test_size_queries(L):
     assert L.moe_rows_cap(32768, 64, 1, 128) == 32768 + 64 * 127
     assert L.moe_rows_cap(100, 8, 2, 0) == 200
     assert L.moe_rows_cap(100, 8, 2, 1) == 200
-    assert L.LIB.moe_rows_cap(-1, 8, 2, 0) == -1
+    assert L.LIB.moe_rows_cap(-1, 8, 2, 0, 0) == -1
+    # with token dropping no expert keeps more than `capacity` rows
+    assert L.moe_rows_cap(100, 8, 2, 0, capacity=10) == 80
+    assert L.moe_rows_cap(100, 8, 2, 16, capacity=10) == 80 + 8 * 15
+    assert L.moe_rows_cap(100, 8, 2, 0, capacity=1000) == 200
+    assert L.moe_rows_cap(32768, 64, 1, 128, capacity=512) == 32768 + 64 * 127
     assert L.moe_permute_workspace_bytes(4096, 64) >= 4 * 64 * 4
-    assert L.LIB.moe_version() >= 100
+    assert L.LIB.moe_version() >= 200
 
 
 def _ptr(v=16):
@@ -108,28 +113,36 @@ def test_validation_errors_need_no_gpu(L):
     assert st == L.MOE_ERR_INVALID_ARG and "workspace" in L.last_error()
     # gmm: N not a multiple of 8
     st = lib.moe_gmm(_ptr(), 64, _ptr(), 12, 64 * 12, 0, _ptr(), 1, 100, 64, 12, 0, None, 0, None,
-                     0, None, 0, _ptr(), 0, 12, None, 0, None, None)
+                     0, None, 0, _ptr(), 0, 12, None, 0, None, 0, None, None)
     assert st == L.MOE_ERR_UNSUPPORTED
     # gmm: SWIGLU_FWD without C2
     st = lib.moe_gmm(_ptr(), 64, _ptr(), 64, 64 * 64, 0, _ptr(), 1, 100, 64, 64, 1, None, 0, None,
-                     0, None, 0, _ptr(), 0, 64, None, 0, None, None)
+                     0, None, 0, _ptr(), 0, 64, None, 0, None, 0, None, None)
     assert st == L.MOE_ERR_INVALID_ARG
     # gmm: misaligned A
     st = lib.moe_gmm(_ptr(18), 64, _ptr(), 64, 64 * 64, 0, _ptr(), 1, 100, 64, 64, 0, None, 0,
-                     None, 0, None, 0, _ptr(), 0, 64, None, 0, None, None)
+                     None, 0, None, 0, _ptr(), 0, 64, None, 0, None, 0, None, None)
     assert st == L.MOE_ERR_UNSUPPORTED
     # gmm: in-place partial sum with bf16 C
     st = lib.moe_gmm(_ptr(), 64, _ptr(), 64, 64 * 64, 0, _ptr(), 1, 100, 64, 64, 0, None, 0,
-                     _ptr(32), 64, None, 0, _ptr(32), 0, 64, None, 0, None, None)
+                     _ptr(32), 64, None, 0, _ptr(32), 0, 64, None, 0, None, 0, None, None)
     assert st == L.MOE_ERR_INVALID_ARG
     # gmm: bias with a stride shorter than N
     st = lib.moe_gmm(_ptr(), 64, _ptr(), 64, 64 * 64, 0, _ptr(), 2, 100, 64, 64, 0, None, 0,
-                     None, 0, _ptr(), 32, _ptr(), 0, 64, None, 0, None, None)
+                     None, 0, _ptr(), 32, _ptr(), 0, 64, None, 0, None, 0, None, None)
     assert st == L.MOE_ERR_INVALID_ARG and "bias" in L.last_error()
     # gmm: bias with the SwiGLU backward
     st = lib.moe_gmm(_ptr(), 64, _ptr(), 64, 64 * 64, 1, _ptr(), 2, 100, 64, 64, 2, _ptr(), 128,
-                     None, 0, _ptr(), 64, _ptr(), 0, 128, None, 0, None, None)
+                     None, 0, _ptr(), 64, _ptr(), 0, 128, None, 0, None, 0, None, None)
     assert st == L.MOE_ERR_INVALID_ARG and "bias" in L.last_error()
+    # gmm: a column-wise copy from the plain epilogue
+    st = lib.moe_gmm(_ptr(), 64, _ptr(), 64, 64 * 64, 0, _ptr(), 1, 100, 64, 64, 0, None, 0,
+                     None, 0, None, 0, _ptr(), 0, 64, None, 0, _ptr(), 256, None, None)
+    assert st == L.MOE_ERR_INVALID_ARG and "Ct" in L.last_error()
+    # gmm: a column-wise copy narrower than the padded group layout
+    st = lib.moe_gmm(_ptr(), 64, _ptr(), 64, 64 * 64, 0, _ptr(), 2, 100, 64, 64, 1, None, 0,
+                     None, 0, None, 0, _ptr(), 0, 64, _ptr(), 32, _ptr(), 128, None, None)
+    assert st == L.MOE_ERR_INVALID_ARG and "ldct" in L.last_error()
     # group_colsum: N not a multiple of 8
     st = lib.moe_group_colsum(_ptr(), 64, _ptr(), 4, 100, 60, _ptr(), 64, None)
     assert st == L.MOE_ERR_UNSUPPORTED
@@ -166,3 +179,12 @@ def test_product_path_never_touches_the_oracle():
                 src = open(os.path.join(dirpath, fn)).read()
                 assert "oracle" not in src.replace("the oracle", ""), fn
                 assert "moe_ref" not in src, fn
+
+
+def test_layer_rejects_uneven_chunks(L):
+    """K-chunks must tile d_model: a remainder would leave columns of x and wi
+    out of the up-projection (checked before any device memory is touched)."""
+    from mixture_experts_grouped_router_gb300 import layer
+    with pytest.raises(ValueError, match="does not divide"):
+        layer.MoEBuffers(layer.LayerShape(T=8, d=264, f=64, E=2, k=1, num_chunks=16),
+                         device="cpu")

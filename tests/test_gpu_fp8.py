@@ -327,13 +327,20 @@ def _rel(a, b):
     return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
 
 
+def _max_rel(a, b):
+    """max |a - b| / max |b|: the elementwise half of the acceptance bar."""
+    a = a.detach().float().cpu().numpy().astype(np.float64) if isinstance(a, torch.Tensor) else a
+    return float(np.abs(a - b).max() / max(np.abs(b).max(), 1e-300))
+
+
 @pytest.mark.parametrize("name", list(FP8_LAYERS))
 def test_layer_fp8(name):
     """The GPU follows the FP8 recipe: every output is within 1e-2 (relative
-    Frobenius) of the FP8 oracle and at most half as far from it as the FP8
-    oracle is from the unquantized layer.  Both sides quantize the same bf16
-    tensors; the residual is fp32 against fp64 accumulation, which now and then
-    moves a bf16 rounding and with it one code."""
+    Frobenius) and 5e-2 * max|ref| (elementwise) of the FP8 oracle, and at
+    most half as far from it as the FP8 oracle is from the unquantized layer.
+    Both sides quantize the same bf16 tensors; the residual is fp32 against
+    fp64 accumulation, which now and then moves a bf16 rounding and with it
+    one code."""
     from mixture_experts_grouped_router_gb300 import layer
     cfg = FP8_LAYERS[name]
     inp = moe_synth.make_inputs(cfg, seed=4)
@@ -365,20 +372,34 @@ def test_layer_fp8(name):
             ("dh", b.dh[:R], b8["dh"], br["dh"]), ("dx", b.dx, b8["dx"], br["dx"]),
             ("dwi", b.dwi, b8["d_wi"], br["d_wi"]), ("dwo", b.dwo, b8["d_wo"], br["d_wo"]),
             ("d_topk_w", b.d_topk_w, b8["d_topk_w"], br["d_topk_w"])):
-        errs[key] = (_rel(got, want8), _rel(want8, want16))
-    bad = {k: v for k, v in errs.items() if not (v[0] <= 1e-2 and v[0] <= 0.5 * v[1])}
+        errs[key] = (_rel(got, want8), _rel(want8, want16), _max_rel(got, want8))
+    bad = {k: v for k, v in errs.items()
+           if not (v[0] <= 1e-2 and v[0] <= 0.5 * v[1] and v[2] <= 5e-2)}
     assert not bad, errs
+
+
+class _ExpertsF64:
+    """Expert e's bf16 weights as float64, converted when asked for."""
+
+    def __init__(self, bits):
+        self.bits = bits
+
+    def __len__(self):
+        return self.bits.shape[0]
+
+    def __getitem__(self, e):
+        return moe_synth.bits_to_f64(self.bits[e])
 
 
 @pytest.mark.parametrize("name", ["mixtral", "dsv3"])
 def test_layer_fp8_full_size_sampled(name):
-    """The FP8 layer at full size, in the configuration `bench.py --fp8` times.
-    The FP8 oracle needs every row of Act, dY and dH for their amax, which is
-    too slow at this size, so sampled tokens are checked against the bf16
-    oracle instead: the FP8 result lies within the quantization noise the FP8
-    oracle shows against the bf16 oracle at reduced size (relative error below
-    0.15 on out and dx, below 0.2 on sampled weight-gradient columns), and
-    the integer routing state is exact."""
+    """The FP8 layer at full size, in the configuration `bench.py --fp8` times,
+    against the FP8 oracle.  The oracle derives every scale itself over all
+    rows (layer_scales: Act and dH block by block in fp64, slow), then
+    recomputes one by one: out and dx of sampled tokens, one row of dWo and
+    one column of dWi of sampled experts; each within 1e-2 relative Frobenius
+    and 5e-2 * max|ref| elementwise.  Scales of x, wi and wo are bit-exact;
+    those of Act, dY and dH within one bf16 rounding of their amax."""
     from mixture_experts_grouped_router_gb300 import layer
     cfg = moe_synth.CONFIGS[name]
     inp = moe_synth.make_inputs(cfg, seed=0)
@@ -389,43 +410,73 @@ def test_layer_fp8_full_size_sampled(name):
     layer.backward(b, dout, wi, wo)
     torch.cuda.synchronize()
     assert int(b.dev_status.item()) == 0
+    del x, wi, wo, dout
     f64 = moe_synth.bits_to_f64
-    idx, w = moe_ref.route_topk(inp["logits"], cfg.k, cfg.score_fn, cfg.renorm)
-    assert (b.topk_idx.cpu().numpy() == idx).all()
-    lay = moe_ref.permute_layout(idx, cfg.E, cfg.align, cfg.capacity)
+    E, k, f = cfg.E, cfg.k, cfg.f
+    wi_b, wo_b = _ExpertsF64(inp["wi"]), _ExpertsF64(inp["wo"])
+    sc = q8.layer_scales(f64(inp["x"]), inp["logits"], wi_b, wo_b, f64(inp["dout"]), k,
+                         cfg.score_fn, cfg.renorm, cfg.align, cfg.capacity)
+    lay, S = sc["layout"], sc["scales"]
+    assert (b.topk_idx.cpu().numpy() == sc["topk_idx"]).all()
     assert b.group_offsets.cpu().numpy().tolist() == lay["group_offsets"].tolist()
+    # the GPU keeps 1 / scale: slots x, act, dy, dh, wi[E], wo[E]
+    g_scale = 1.0 / b.f8_sinv.double().cpu().numpy()
+    g_sinv = b.f8_sinv.cpu().numpy()
+    assert g_sinv[0] == np.float32(1) / S["x"]
+    assert (g_sinv[4:4 + E] == np.float32(1) / S["wi"]).all()
+    assert (g_sinv[4 + E:] == np.float32(1) / S["wo"]).all()
+    for i, key in ((1, "act"), (2, "dy"), (3, "dh")):
+        assert abs(g_scale[i] / float(S[key]) - 1) <= 2.0 ** -7, (key, g_scale[i], S[key])
     rng = np.random.default_rng(1)
     toks = rng.choice(cfg.T, size=6, replace=False)
-    f2s = lay["flat_to_sorted"].reshape(cfg.T, cfg.k)
+    f2s = lay["flat_to_sorted"].reshape(cfg.T, k)
     off = lay["group_offsets"]
+    col_experts = rng.choice(np.nonzero(lay["group_sizes"] > 0)[0], size=2, replace=False)
     out_ref = np.zeros((len(toks), cfg.d))
     dx_ref = np.zeros((len(toks), cfg.d))
-    for i, t in enumerate(toks):
-        xt = f64(inp["x"][t:t + 1])
-        for j in range(cfg.k):
-            p = f2s[t, j]
-            if p < 0:
-                continue
-            e = int(np.searchsorted(off, p, side="right") - 1)
-            wi_e, wo_e = f64(inp["wi"][e]), f64(inp["wo"][e])
-            h = xt @ wi_e
-            out_ref[i] += w[t, j] * (moe_ref.swiglu(h) @ wo_e)[0]
-            dh = moe_ref.swiglu_bwd(h, (w[t, j] * f64(inp["dout"][t:t + 1])) @ wo_e.T)
-            dx_ref[i] += (dh @ wi_e.T)[0]
+    dwo_rows, dwo_ref, dwi_cols, dwi_ref = [], [], [], []
+    xs_q, dy_q = sc["xs_q"], sc["dy_q"]
+    w = sc["topk_w"]
+
+    def qdq(v, key, fmt):
+        return q8.dequantize(q8.encode_lib((np.asarray(v, np.float32) *
+                                            np.float32(S[key])).astype(np.float32), fmt),
+                             S[key], fmt)
+
+    for e in range(E):
+        uses = [(i, j) for i, t in enumerate(toks) for j in range(k)
+                if f2s[t, j] >= 0 and off[e] <= f2s[t, j] < off[e + 1]]
+        if not uses and e not in col_experts:
+            continue
+        wi_q = q8.dequantize(q8.encode_lib((wi_b[e].astype(np.float32) * S["wi"][e]).astype(
+            np.float32), q8.E4M3), S["wi"][e], q8.E4M3)
+        wo_q = q8.dequantize(q8.encode_lib((wo_b[e].astype(np.float32) * S["wo"][e]).astype(
+            np.float32), q8.E4M3), S["wo"][e], q8.E4M3)
+        for i, j in uses:
+            p = f2s[toks[i], j]
+            h = xs_q[p:p + 1] @ wi_q
+            act_q = qdq(q8.round_bf16(moe_ref.swiglu(h)), "act", q8.E4M3)
+            out_ref[i] += w[toks[i], j] * (act_q @ wo_q)[0]
+            dh = q8.round_bf16(moe_ref.swiglu_bwd(q8.round_bf16(h), dy_q[p:p + 1] @ wo_q.T))
+            dx_ref[i] += (qdq(dh, "dh", q8.E5M2) @ wi_q.T)[0]
+        if e in col_experts:
+            rows = slice(int(off[e]), int(off[e + 1]))
+            c = int(rng.integers(f))
+            h2 = xs_q[rows] @ wi_q[:, [c, f + c]]
+            act_c = qdq(q8.round_bf16(moe_ref.swiglu(h2)), "act", q8.E4M3)[:, 0]
+            dwo_rows.append((e, c))
+            dwo_ref.append(act_c @ dy_q[rows])
+            n = int(rng.integers(2 * f))
+            cc = n % f
+            h3 = q8.round_bf16(xs_q[rows] @ wi_q[:, [cc, f + cc]])
+            dh2 = q8.round_bf16(moe_ref.swiglu_bwd(h3, dy_q[rows] @ wo_q[cc, :][:, None]))
+            dh_n = qdq(dh2[:, 1 if n >= f else 0], "dh", q8.E5M2)
+            dwi_cols.append((e, n))
+            dwi_ref.append(xs_q[rows].T @ dh_n)
     tsel = torch.from_numpy(toks).cuda()
-    assert _rel(b.out[tsel], out_ref) < 0.15
-    assert _rel(b.dx[tsel], dx_ref) < 0.15
-    # one column of dWo per sampled expert: act[:, c]^T dY over the expert's rows
-    for e in rng.choice(np.nonzero(lay["group_sizes"] > 0)[0], size=2, replace=False):
-        s, t_ = int(off[e]), int(off[e + 1])
-        rows = lay["sorted_to_flat"][s:t_]
-        real = rows >= 0
-        xs = np.zeros((t_ - s, cfg.d))
-        xs[real] = f64(inp["x"][rows[real] // cfg.k])
-        dy = np.zeros((t_ - s, cfg.d))
-        a = rows[real]
-        dy[real] = w.reshape(-1)[a][:, None] * f64(inp["dout"][a // cfg.k])
-        c = int(rng.integers(cfg.f))
-        wi_e = f64(inp["wi"][e])
-        act_c = moe_ref.swiglu(np.stack([xs @ wi_e[:, c], xs @ wi_e[:, cfg.f + c]], 1))[:, 0]
-        assert _rel(b.dwo[e][c, :], act_c @ dy) < 0.2
+    assert_close("out (sampled tokens)", b.out[tsel], out_ref)
+    assert_close("dx (sampled tokens)", b.dx[tsel], dx_ref)
+    assert_close("dWo (sampled rows)", torch.stack([b.dwo[e][c, :] for e, c in dwo_rows]),
+                 np.stack(dwo_ref))
+    assert_close("dWi (sampled columns)", torch.stack([b.dwi[e][:, n] for e, n in dwi_cols]),
+                 np.stack(dwi_ref))

@@ -121,6 +121,59 @@ def test_gmm_swiglu_bwd(sz, K, F):
     assert_close("dH", dH[:R], want)
 
 
+@pytest.mark.parametrize("sz,K,F", [("mixed", 256, 192), ("one", 136, 200), ("tiny", 64, 72),
+                                    ("mixed", 520, 1024), ("empty_tail", 64, 264)])
+@pytest.mark.parametrize("epi", [L.EPI_SWIGLU_FWD, L.EPI_SWIGLU_BWD])
+def test_gmm_swiglu_colwise_copy(sz, K, F, epi):
+    """The column-wise copy the SwiGLU epilogues write (Ct) holds exactly the
+    bf16 values of the row-wise output, in the padded group layout, zeros in
+    each group's padding, nothing past the last group; the row-wise outputs
+    are bit-identical to a launch without the copy.  Rows of A past the groups
+    are NaN: a tile's rows past its expert must reach the copy as zeros."""
+    bwd = epi == L.EPI_SWIGLU_BWD
+    rng, off, rows_cap, a_bits, b_bits, a64, b64 = _setup(SIZES[sz], K, F if bwd else 2 * F,
+                                                          int(bwd), seed=5 * K + F)
+    E, R = len(SIZES[sz]), int(off[-1])
+    offd = torch.from_numpy(off).cuda()
+    A = dev_bf16(a_bits)
+    A[R:] = float("nan")
+    Bw = dev_bf16(b_bits)
+    P = L.moe_fp8_padded_rows(rows_cap, E)
+    width = 2 * F if bwd else F
+    outs = []
+    for with_copy in (False, True):
+        H = torch.full((rows_cap, 2 * F), 5.0, dtype=torch.bfloat16, device="cuda")
+        Act = torch.full((rows_cap, F), 5.0, dtype=torch.bfloat16, device="cuda")
+        Ct = torch.full((width, P + 8), float("nan"), dtype=torch.bfloat16, device="cuda")
+        kw = dict(Ct=Ct[:, :P]) if with_copy else {}
+        if bwd:
+            aux = dev_bf16(_bf(rng, (rows_cap, 2 * F), 2.0)) if not outs else outs[0][3]
+            L.moe_gmm(A, Bw, 1, offd, H, L.EPI_SWIGLU_BWD, aux=aux, **kw)
+        else:
+            aux = None
+            L.moe_gmm(A, Bw, 0, offd, H, L.EPI_SWIGLU_FWD, C2=Act, **kw)
+        torch.cuda.synchronize()
+        outs.append((H, Act, Ct, aux))
+    (H0, A0, _, _), (H1, A1, Ct, aux) = outs
+    assert torch.equal(H0[:R].view(torch.int16), H1[:R].view(torch.int16))
+    src = H1 if bwd else A1           # dH or Act, row-wise
+    if not bwd:
+        assert torch.equal(A0[:R].view(torch.int16), A1[:R].view(torch.int16))
+        assert_close("Act", A1[:R], moe_ref.swiglu(moe_ref.gmm(a64[:R], b64, off)))
+    else:
+        d_act = moe_ref.gmm(a64[:R], b64, off, transpose_rhs=True)
+        assert_close("dH", H1[:R], moe_ref.swiglu_bwd(host_f64(aux)[:R], d_act))
+    got = Ct.view(torch.int16).cpu().numpy()
+    rows = src.view(torch.int16).cpu().numpy()
+    po = _poff(SIZES[sz])
+    for e in range(E):
+        a, b = int(off[e]), int(off[e + 1])
+        assert (got[:, po[e]:po[e] + b - a] == rows[a:b, :width].T).all(), e
+        assert (got[:, po[e] + b - a:po[e + 1]] == 0).all(), e
+    # columns past the last group (and past P) are not written: still NaN (0x7fc0)
+    assert (got[:, po[-1]:] == np.int16(0x7FC0)).all()
+
+
 TGMM_CASES = [("mixed", 256, 384), ("one", 136, 200), ("tiny", 64, 64), ("empty_tail", 128, 520),
               ("mixed", 1024, 128)]
 
@@ -138,10 +191,14 @@ def test_tgmm(sz, M, N, mode):
     dt = torch.bfloat16 if mode == "bf16" else torch.float32
     W0 = rng.standard_normal((E, M, N)).astype(np.float32)
     W = torch.from_numpy(W0).cuda().to(dt)
-    L.moe_tgmm(dev_bf16(a_bits), dev_bf16(b_bits), torch.from_numpy(off).cuda(), W,
-               accumulate=(mode == "f32_acc"))
-    torch.cuda.synchronize()
     R = int(off[-1])
+    A, B = dev_bf16(a_bits), dev_bf16(b_bits)
+    # rows past the groups are never read: NaN there would reach W through
+    # the ragged last K block of the last expert unless its tail is zeroed
+    A[R:] = float("nan")
+    B[R:] = float("nan")
+    L.moe_tgmm(A, B, torch.from_numpy(off).cuda(), W, accumulate=(mode == "f32_acc"))
+    torch.cuda.synchronize()
     ps = W0.astype(np.float64) if mode == "f32_acc" else None
     want = moe_ref.tgmm(moe_synth.bits_to_f64(a_bits)[:R], moe_synth.bits_to_f64(b_bits)[:R],
                         off, E, partial_sum=ps)

@@ -32,10 +32,13 @@ SMALL = {
 
 
 @pytest.mark.parametrize("name", list(SMALL))
-def test_layer_small(name):
+@pytest.mark.parametrize("wgrad_colwise", [False, True])
+def test_layer_small(name, wgrad_colwise):
+    """Every output element by element; with wgrad_colwise the weight
+    gradients read the column-wise copies the epilogues write."""
     cfg = SMALL[name]
     inp = moe_synth.make_inputs(cfg, seed=0)
-    b = run_gpu_layer(cfg, inp)
+    b = run_gpu_layer(cfg, inp, wgrad_colwise=wgrad_colwise)
     assert int(b.dev_status.item()) == 0
     fw, bw = run_oracle(cfg, inp)
     check_layout(b, fw, cfg.T, cfg.k)
@@ -58,6 +61,33 @@ def test_layer_small(name):
     empty = np.nonzero(fw["layout"]["group_sizes"] == 0)[0]
     for e in empty:
         assert (b.dwi[e].float() == 0).all() and (b.dwo[e].float() == 0).all()
+
+
+@pytest.mark.parametrize("name", ["dsv3", "mixtral"])
+def test_layer_expert_bias(name):
+    """DeepSeek-V3's selection bias through the layer (MaxText PR #2579, the
+    routing that keeps pre-bias logits): experts ranked by logit + bias, the
+    weights from the unbiased logits; every output against the oracle."""
+    cfg = SMALL[name]
+    inp = moe_synth.make_inputs(cfg, seed=3)
+    bias = np.random.default_rng(11).standard_normal(cfg.E).astype(np.float32)
+    b = run_gpu_layer(cfg, inp, expert_bias=bias)
+    assert int(b.dev_status.item()) == 0
+    fw, bw = run_oracle(cfg, inp, expert_bias=bias)
+    # the bias must change the selection, or this test checks nothing new
+    plain_idx, _ = moe_ref.route_topk(inp["logits"], cfg.k, cfg.score_fn, cfg.renorm)
+    assert (plain_idx != fw["topk_idx"]).any()
+    check_layout(b, fw, cfg.T, cfg.k)
+    R = fw["layout"]["R"]
+    assert_close("out", b.out, fw["out"])
+    assert_close("d_topk_w", b.d_topk_w, bw["d_topk_w"])
+    assert_close("d_logits", b.d_logits,
+                 moe_ref.route_topk_bwd(inp["logits"], fw["topk_idx"], bw["d_topk_w"],
+                                        cfg.score_fn, cfg.renorm))
+    assert_close("dh", b.dh[:R], bw["dh"])
+    assert_close("dx", b.dx, bw["dx"])
+    assert_close("dwo", b.dwo, bw["d_wo"])
+    assert_close("dwi", b.dwi, bw["d_wi"])
 
 
 # ---------------------------------------------------------------------------

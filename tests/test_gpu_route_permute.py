@@ -131,12 +131,33 @@ def test_permute_no_tokens():
     assert (r["s2f"].cpu().numpy() == -1).all()
 
 
-def test_permute_bad_expert_sets_status_without_fault():
-    idx = np.array([[0, 1], [2, 9], [1, 1]], np.int32)   # 9 out of range; token 2 repeats 1
-    r = run_permute(idx, 4, 0, 0, d=16)
+@pytest.mark.parametrize("align", [0, 8])
+def test_permute_bad_expert_sets_status_without_fault(align):
+    """An id out of range and a repeated id are both dropped, by the counts as
+    well as the ranks: the groups hold only the valid assignments, every kept
+    row is written and padding rows are zero.  Expected layout by hand: valid
+    assignments a0 (token 0, expert 0), a1 (0, 1), a2 (1, 2), a4 (2, 1); a3
+    (expert 9) and a5 (token 2 repeats expert 1) are dropped."""
+    idx = np.array([[0, 1], [2, 9], [1, 1]], np.int32)
+    r = run_permute(idx, 4, align, 0, d=16)
     assert int(r["st"].item()) == L.MOE_ERR_DEVICE
+    assert r["kc"].cpu().numpy().tolist() == [1, 2, 1, 0]
+    if align == 8:
+        gs, s2f = [8, 8, 8, 0], [0] + [-1] * 7 + [1, 4] + [-1] * 6 + [2] + [-1] * 7
+    else:
+        gs, s2f = [1, 2, 1, 0], [0, 1, 4, 2]
+    assert r["gs"].cpu().numpy().tolist() == gs
+    assert r["off"].cpu().numpy().tolist() == np.concatenate([[0], np.cumsum(gs)]).tolist()
+    R = sum(gs)
+    got_s2f = r["s2f"].cpu().numpy()
+    assert got_s2f[:R].tolist() == s2f and (got_s2f[R:] == -1).all()
     f2s = r["f2s"].cpu().numpy()
     assert f2s[3] == -1 and f2s[5] == -1
+    assert [f2s[a] for a in (0, 1, 2, 4)] == [s2f.index(a) for a in (0, 1, 2, 4)]
+    xs_bits = r["xs"][:R].view(torch.int16).cpu().numpy().astype(np.uint16)
+    for p_, a in enumerate(s2f):
+        want = r["x_bits"][a // 2] if a >= 0 else np.zeros(16, np.uint16)
+        assert (xs_bits[p_] == want).all(), p_
 
 
 BIAS_CASES = [(300, 8, 2, 1, 1), (513, 64, 8, 1, 1), (100, 256, 4, 0, 0), (77, 32, 3, 0, 1)]

@@ -152,3 +152,43 @@ def test_fp8_layer_close_to_bf16_layer():
     assert rel(b8["d_wo"], br["d_wo"]) < 0.15
     # ... and the error is really there (quantization happened)
     assert rel(f8["out"], fr["out"]) > 1e-3
+
+
+@pytest.mark.parametrize("fmt", [q8.E4M3, q8.E5M2])
+def test_encode_lib_is_encode(fmt):
+    """The library path of the codes gives encode()'s codes: every fp32 around
+    each grid value (ties, both neighbours), subnormals, zeros of both signs,
+    values past the largest finite one (saturated), infinities and NaN, and a
+    wide random sample."""
+    grid, _ = q8._finite_grid(fmt)
+    mids = (grid[1:] + grid[:-1]) / 2
+    pts = np.concatenate([grid, mids, np.nextafter(mids.astype(np.float32), np.float32(0)),
+                          np.nextafter(mids.astype(np.float32), np.float32(1e9)),
+                          [q8.fp8_max(fmt) * 1.03, q8.fp8_max(fmt) * 7, 1e30, np.inf]])
+    rng = np.random.default_rng(5)
+    rnd = rng.standard_normal(200000) * np.exp(rng.uniform(-12, 12, 200000))
+    x = np.concatenate([pts, -pts, rnd, [0.0, -0.0, np.nan, -np.inf]]).astype(np.float32)
+    assert (q8.encode_lib(x, fmt) == q8.encode(x, fmt)).all()
+
+
+def test_layer_scales_are_the_layer_scales():
+    """The blockwise scale computation for full-size layers gives exactly the
+    scales forward() / backward() take from whole tensors (blocks smaller than
+    an expert's rows, so that several blocks meet in one amax)."""
+    from moe_synth import bits_to_f64, make_inputs, scaled, CONFIGS
+    cfg = scaled(CONFIGS["skewed"], T=2048, d=128, f=96, capacity=48)
+    inp = make_inputs(cfg, seed=2)
+    x, wi, wo, dout = (bits_to_f64(inp[n]) for n in ("x", "wi", "wo", "dout"))
+    fw = q8.forward(x, inp["logits"], wi, wo, cfg.k, cfg.score_fn, cfg.renorm, cfg.align,
+                    cfg.capacity)
+    bw = q8.backward(fw, dout, cfg.k)
+    sc = q8.layer_scales(x, inp["logits"], wi, wo, dout, cfg.k, cfg.score_fn, cfg.renorm,
+                         cfg.align, cfg.capacity, block_rows=7)
+    want = dict(fw["scales"], **bw["scales"])
+    for key in ("x", "act", "dy", "dh"):
+        assert sc["scales"][key] == want[key], key
+    for key in ("wi", "wo"):
+        assert (sc["scales"][key] == want[key]).all(), key
+    R = fw["layout"]["R"]
+    assert (sc["xs_q"] == fw["xs_q"]).all()
+    assert (sc["dy_q"] == bw["dy_q"][:R]).all()
