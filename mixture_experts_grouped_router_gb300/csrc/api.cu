@@ -579,6 +579,132 @@ moe_status_t moe_tgmm_fp8(const uint8_t *At, int64_t ldat, int a_fmt, const floa
   return moe::launch_tgmm_f8(a, (cudaStream_t)stream);
 }
 
+size_t moe_mx_scale_bytes(int64_t rows, int cols, int row_map, int E) {
+  if (rows < 0 || cols <= 0 || cols % 128 != 0 || row_map < MOE_MX_ROWS_PLAIN ||
+      row_map > MOE_MX_ROWS_SWIGLU || (row_map == MOE_MX_ROWS_GROUPED && E <= 0))
+    return 0;
+  return (size_t)moe::mx_atom_rows(rows, row_map, E) * (size_t)(cols / 128) * 512u;
+}
+
+moe_status_t moe_mx_quantize(const uint16_t *x, int64_t ldx, int64_t rows, int cols, int fmt,
+                             int row_map, const int32_t *group_offsets, int E, uint8_t *q,
+                             int64_t ldq, uint8_t *sf, size_t sf_bytes, moe_stream_t stream) {
+  set_error("");
+  REQUIRE(rows >= 0 && cols > 0, MOE_ERR_INVALID_ARG, "moe_mx_quantize: rows=%lld cols=%d",
+          (long long)rows, cols);
+  REQUIRE(fmt == MOE_FP8_E4M3 || fmt == MOE_FP8_E5M2, MOE_ERR_INVALID_ARG,
+          "moe_mx_quantize: bad format %d", fmt);
+  REQUIRE(row_map >= MOE_MX_ROWS_PLAIN && row_map <= MOE_MX_ROWS_SWIGLU, MOE_ERR_INVALID_ARG,
+          "moe_mx_quantize: bad row_map %d", row_map);
+  REQUIRE(cols % 128 == 0 && ldx % 8 == 0 && ldq % 16 == 0, MOE_ERR_UNSUPPORTED,
+          "moe_mx_quantize: cols must be a multiple of 128, ldx of 8, ldq of 16");
+  REQUIRE(ldx >= cols && ldq >= cols, MOE_ERR_INVALID_ARG, "moe_mx_quantize: ld < cols");
+  REQUIRE(rows < (1ll << 31), MOE_ERR_UNSUPPORTED, "moe_mx_quantize: more than 2^31 rows");
+  if (row_map == MOE_MX_ROWS_GROUPED)
+    REQUIRE(group_offsets != nullptr && E > 0 && E <= 256, MOE_ERR_INVALID_ARG,
+            "moe_mx_quantize: GROUPED needs group_offsets and 0 < E <= 256");
+  if (row_map == MOE_MX_ROWS_SWIGLU)
+    REQUIRE(rows % 128 == 0, MOE_ERR_UNSUPPORTED,
+            "moe_mx_quantize: SWIGLU needs 2F rows with F a multiple of 64");
+  if (rows == 0) return MOE_OK;
+  REQUIRE(x && q && sf, MOE_ERR_INVALID_ARG, "moe_mx_quantize: null pointer");
+  REQUIRE(aligned16(x) && aligned16(q), MOE_ERR_UNSUPPORTED,
+          "moe_mx_quantize: x and q must be 16-byte aligned");
+  REQUIRE(sf_bytes >= moe_mx_scale_bytes(rows, cols, row_map, E), MOE_ERR_INVALID_ARG,
+          "moe_mx_quantize: sf of %zu bytes < %zu", sf_bytes,
+          moe_mx_scale_bytes(rows, cols, row_map, E));
+  return cuda_status(moe::launch_mx_quantize(x, ldx, rows, cols, fmt, row_map, group_offsets, E,
+                                             q, ldq, sf, (cudaStream_t)stream),
+                     "moe_mx_quantize launch");
+}
+
+moe_status_t moe_gmm_mx(const uint8_t *A, int64_t lda, const uint8_t *sfa, int a_fmt,
+                        const uint8_t *B, int64_t ldb, int64_t stride_b, const uint8_t *sfb,
+                        int64_t sfb_nstride, int64_t sfb_estride, int b_fmt,
+                        const int32_t *group_offsets, int E, int64_t rows_cap, int K, int N,
+                        int epilogue, const uint16_t *aux, int64_t ld_aux, void *C, int c_dtype,
+                        int64_t ldc, uint16_t *C2, int64_t ldc2, int32_t *dev_status,
+                        moe_stream_t stream) {
+  set_error("");
+  REQUIRE(E > 0 && rows_cap >= 0 && K > 0 && N > 0, MOE_ERR_INVALID_ARG,
+          "moe_gmm_mx: E=%d rows_cap=%lld K=%d N=%d", E, (long long)rows_cap, K, N);
+  REQUIRE(E <= 256, MOE_ERR_UNSUPPORTED, "moe_gmm_mx: E=%d > 256", E);
+  REQUIRE((a_fmt == MOE_FP8_E4M3 || a_fmt == MOE_FP8_E5M2) &&
+              (b_fmt == MOE_FP8_E4M3 || b_fmt == MOE_FP8_E5M2),
+          MOE_ERR_INVALID_ARG, "moe_gmm_mx: bad operand format");
+  REQUIRE(epilogue >= MOE_EPI_NONE && epilogue <= MOE_EPI_SWIGLU_BWD, MOE_ERR_INVALID_ARG,
+          "moe_gmm_mx: bad epilogue %d", epilogue);
+  REQUIRE(c_dtype == MOE_DTYPE_BF16 || c_dtype == MOE_DTYPE_F32, MOE_ERR_INVALID_ARG,
+          "moe_gmm_mx: bad c_dtype");
+  REQUIRE(K % 128 == 0 && N % 128 == 0 && lda % 16 == 0 && ldb % 16 == 0 && stride_b % 16 == 0,
+          MOE_ERR_UNSUPPORTED,
+          "moe_gmm_mx: K, N must be multiples of 128 and lda, ldb, stride_b of 16");
+  REQUIRE(lda >= K && ldb >= K, MOE_ERR_INVALID_ARG, "moe_gmm_mx: lda, ldb < K");
+  REQUIRE(stride_b >= (int64_t)N * ldb || E == 1 || stride_b == K, MOE_ERR_INVALID_ARG,
+          "moe_gmm_mx: stride_b overlaps experts");
+  REQUIRE(sfb_nstride >= K / 128 && sfb_estride >= 0, MOE_ERR_INVALID_ARG,
+          "moe_gmm_mx: bad scale-factor strides of B");
+  int outN = N;
+  if (epilogue == MOE_EPI_SWIGLU_FWD) {
+    REQUIRE((C2 != nullptr || rows_cap == 0) && ldc2 >= N / 2 && ldc2 % 8 == 0,
+            MOE_ERR_INVALID_ARG, "moe_gmm_mx: SWIGLU_FWD needs C2 with ldc2 >= F");
+    REQUIRE(c_dtype == MOE_DTYPE_BF16, MOE_ERR_INVALID_ARG, "moe_gmm_mx: SWIGLU_FWD writes bf16");
+  }
+  if (epilogue == MOE_EPI_SWIGLU_BWD) {
+    outN = 2 * N;
+    REQUIRE((aux != nullptr || rows_cap == 0) && ld_aux >= 2 * N && ld_aux % 8 == 0,
+            MOE_ERR_INVALID_ARG, "moe_gmm_mx: SWIGLU_BWD needs aux = H with ld_aux >= 2N");
+    REQUIRE(c_dtype == MOE_DTYPE_BF16, MOE_ERR_INVALID_ARG, "moe_gmm_mx: SWIGLU_BWD writes bf16");
+  }
+  REQUIRE(ldc >= outN && ldc % 4 == 0, MOE_ERR_INVALID_ARG, "moe_gmm_mx: ldc too small");
+  REQUIRE(rows_cap < (1ll << 31), MOE_ERR_UNSUPPORTED, "moe_gmm_mx: more than 2^31 rows");
+  if (rows_cap == 0) return MOE_OK;
+  REQUIRE(A && sfa && B && sfb && group_offsets && C, MOE_ERR_INVALID_ARG,
+          "moe_gmm_mx: null pointer");
+  REQUIRE(aligned16(A) && aligned16(B) && aligned16(C) && aligned16(C2) && aligned16(aux) &&
+              aligned16(sfa) && aligned16(sfb),
+          MOE_ERR_UNSUPPORTED, "moe_gmm_mx: operands must be 16-byte aligned");
+  moe::GmmMxArgs a{A, lda, sfa, a_fmt, B, ldb, stride_b, sfb, sfb_nstride, sfb_estride, b_fmt,
+                   group_offsets, E, rows_cap, K, N, epilogue, aux, ld_aux, C, c_dtype, ldc, C2,
+                   ldc2, dev_status};
+  return moe::launch_gmm_mx(a, (cudaStream_t)stream);
+}
+
+moe_status_t moe_tgmm_mx(const uint8_t *At, int64_t ldat, const uint8_t *sfa, int a_fmt,
+                         const uint8_t *Bt, int64_t ldbt, const uint8_t *sfb, int b_fmt,
+                         const int32_t *group_offsets, int E, int64_t rows_cap, int M, int N,
+                         void *W, int w_dtype, int64_t ldw, int64_t stride_w, int accumulate,
+                         int32_t *dev_status, moe_stream_t stream) {
+  set_error("");
+  REQUIRE(E > 0 && rows_cap >= 0 && M > 0 && N > 0, MOE_ERR_INVALID_ARG,
+          "moe_tgmm_mx: E=%d rows_cap=%lld M=%d N=%d", E, (long long)rows_cap, M, N);
+  REQUIRE(E <= 256, MOE_ERR_UNSUPPORTED, "moe_tgmm_mx: E=%d > 256", E);
+  REQUIRE((a_fmt == MOE_FP8_E4M3 || a_fmt == MOE_FP8_E5M2) &&
+              (b_fmt == MOE_FP8_E4M3 || b_fmt == MOE_FP8_E5M2),
+          MOE_ERR_INVALID_ARG, "moe_tgmm_mx: bad operand format");
+  REQUIRE(w_dtype == MOE_DTYPE_BF16 || w_dtype == MOE_DTYPE_F32, MOE_ERR_INVALID_ARG,
+          "moe_tgmm_mx: bad w_dtype");
+  REQUIRE(!accumulate || w_dtype == MOE_DTYPE_F32, MOE_ERR_INVALID_ARG,
+          "moe_tgmm_mx: accumulate needs fp32 W");
+  const int64_t P = moe::f8_padded_rows(rows_cap, E);
+  REQUIRE(P / moe::kF8PadRows < 65536, MOE_ERR_UNSUPPORTED,
+          "moe_tgmm_mx: more than 2^16 blocks of 128 rows");
+  REQUIRE(ldat >= P && ldbt >= P && ldat % 16 == 0 && ldbt % 16 == 0, MOE_ERR_INVALID_ARG,
+          "moe_tgmm_mx: ldat, ldbt must be >= moe_fp8_padded_rows (%lld) and multiples of 16",
+          (long long)P);
+  REQUIRE(M % 128 == 0 && N % 128 == 0 && ldw >= N && ldw % 8 == 0, MOE_ERR_UNSUPPORTED,
+          "moe_tgmm_mx: M, N must be multiples of 128, ldw >= N a multiple of 8");
+  REQUIRE(stride_w >= (int64_t)M * ldw || E == 1, MOE_ERR_INVALID_ARG,
+          "moe_tgmm_mx: stride_w overlaps experts");
+  REQUIRE(At && sfa && Bt && sfb && group_offsets && W, MOE_ERR_INVALID_ARG,
+          "moe_tgmm_mx: null pointer");
+  REQUIRE(aligned16(At) && aligned16(Bt) && aligned16(W) && aligned16(sfa) && aligned16(sfb),
+          MOE_ERR_UNSUPPORTED, "moe_tgmm_mx: operands must be 16-byte aligned");
+  moe::TgmmMxArgs a{At, ldat, sfa, a_fmt, Bt, ldbt, sfb, b_fmt, group_offsets, E, rows_cap, M, N,
+                    W, w_dtype, ldw, stride_w, accumulate, dev_status};
+  return moe::launch_tgmm_mx(a, (cudaStream_t)stream);
+}
+
 int64_t moe_ep_recv_rows_cap(int T, int num_ep, int E, int k, int align) {
   if (T < 0 || num_ep <= 0 || E <= 0 || k <= 0 || E % num_ep != 0) return -1;
   return moe::ep_recv_rows_cap(T, num_ep, E, k, align);

@@ -51,19 +51,21 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, UK = 16;
-constexpr int kStages = 6;  // ring slots of the barrier book (every GEMM uses all six)
+constexpr int BM = 128, BK = 64, UK = 16;
+// output tile width (columns of the pair's 256 x BN tile): 256 for the bf16
+// and current-scaling FP8 GEMMs, 128 for the block-scaled ones (their scale
+// factors need tensor-memory columns beside the two accumulators)
+constexpr int kBN = 256;
+constexpr int kStages = 8;  // ring slots of the barrier book (6 or 7 in use, see Ring)
 constexpr int kMaxEpiWarps = 4;
 constexpr int kPadRows = kF8PadRows;  // group padding of column-wise copies (128 rows)
 constexpr int kStgBytes = 8192;  // per epilogue warp: up to four 32x32 bf16 blocks (or two fp32)
 constexpr int A_BYTES = BM * BK * 2;   // 16 KB
-constexpr int B_BYTES = BN * BK * 2;   // 32 KB
 constexpr int BOX_BYTES = 64 * 64 * 2; // one 64x64 MN-major box, 8 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int kMaxE = 256;
 constexpr int kGroupPairs = 16;  // raster group: 16 row-tile pairs x all column tiles
 
-constexpr int kTmemCols = 2 * BN;                 // two accumulators
+constexpr int kTmemCols = 512;  // two accumulators of BN columns (+ block-scale factors)
 
 // Operand elements: bf16 (K blocks of 64, MMA K = 16) or 8-bit float codes
 // (K blocks of 128, MMA K = 32).  Either way a K block of one tile row is one
@@ -93,14 +95,21 @@ struct Book {
 };
 
 // Per-kernel layout.  Every GEMM runs as 2-SM MMAs whose stage holds this
-// CTA's 128-row (tgmm: 128-column) A tile and half of the B tile (32 KB), 6
-// stages, and 4 epilogue warps (one per TMEM lane quarter).
-template <int KIND, int EPI, bool F8>
+// CTA's 128-row (tgmm: 128-column) A tile and half of the B tile (BN = 256:
+// 32 KB, 6 stages; block-scaled, BN = 128: 24 KB plus 1 KB of scale
+// factors, 7 stages), and 4 epilogue warps (one per TMEM lane quarter).
+template <int KIND, int EPI, bool F8, int BN, bool MX>
 struct Ring {
   static constexpr int epi_warps = 4;
-  static constexpr int stages = 6;
-  static constexpr int b_bytes = B_BYTES / 2;
-  static constexpr int stage_bytes = A_BYTES + b_bytes;
+  static constexpr int stages = MX ? 7 : 6;
+  static constexpr int b_bytes = BN * BK;  // this CTA's BN / 2 columns of B, 128-byte rows
+  // block scaling: the scale factors of A's 128 rows and of the tile's BN
+  // (= 128) columns for the stage's K block, one 512-byte atom each
+  static constexpr int sf_bytes = MX ? 1024 : 0;
+  static constexpr int stage_bytes = A_BYTES + b_bytes + sf_bytes;
+  static_assert(stage_bytes % 1024 == 0, "stage alignment (128-byte swizzle atoms)");
+  static_assert(!MX || (F8 && BN == 128), "block scaling: 8-bit operands, 128-column tiles");
+  static_assert(stages <= kStages, "barrier book");
   static constexpr int threads = 64 + 32 * epi_warps;  // producer, MMA, epilogue
   static constexpr int stg_offset = stages * stage_bytes;  // 1024-aligned
   static constexpr int book_offset = stg_offset + epi_warps * kStgBytes;
@@ -143,6 +152,11 @@ struct TcParams {
   const float *b_sinv;
   int a_fmt, b_fmt;
   float *amax_out;  // or null: max |value| of the bf16 output the epilogue writes
+  // block scaling: atom index of the scale factors of a tile's K block
+  //   A: (row tile) * sfa_stride + K block, the row tile being the padded tile
+  //      of the expert's rows (gmm) or the output row tile (tgmm)
+  //   B: (column tile) * sfb_nstride + expert * sfb_estride + K block
+  int64_t sfa_stride, sfb_nstride, sfb_estride;
 };
 
 struct TileInfo {
@@ -306,7 +320,7 @@ struct OutMaps {
 // Before a tile's accumulator is ready: pull the epilogue's global inputs
 // (SwiGLU-backward H, partial sums) into L2 so that the epilogue's loads do
 // not wait on HBM one after another.  Thread = one output row.
-template <int KIND, int EPI>
+template <int KIND, int EPI, int BN>
 MOE_DEVINL void epilogue_prefetch(const TcParams &p, const TileInfo &ti, int rit, int c_begin,
                                   int c_end) {
   if (KIND == KIND_GMM) {
@@ -380,12 +394,14 @@ MOE_DEVINL void issue_aux_load(OutMaps &om, uint8_t *stg, int nc, int wrow0) {
 // Chunks [c_begin, c_end) of the tile's 32-column chunks are this warp's.
 // amx: the warp thread's running max |value| over the outputs it wrote
 // (Act for the SwiGLU forward, dH for the SwiGLU backward), when amax_out.
-template <int EPI, bool F8>
+template <int EPI, bool F8, int BN, bool MX, bool CT>
 MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t taddr, int q,
                              int lane, uint8_t *stg, OutMaps &om, volatile int *abort_flag,
                              int c_begin, int c_end, float &amx) {
-  // FP8: the accumulator holds code products; dequantize with both scales
-  const float sc = F8 ? __ldg(p.a_sinv) * __ldg(p.b_sinv + ti.e) : 1.0f;
+  // FP8 with current scaling: the accumulator holds code products; dequantize
+  // with both scales (block-scaled MMAs apply their scales themselves)
+  constexpr bool kDeq = F8 && !MX;
+  const float sc = kDeq ? __ldg(p.a_sinv) * __ldg(p.b_sinv + ti.e) : 1.0f;
   const int wrow0 = ti.row0 + q * 32;
   const int64_t row = (int64_t)wrow0 + lane;
   const bool valid = row < ti.row_end;
@@ -396,7 +412,7 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
   // column-wise copy of the activation output: every 32-row block of a tile
   // that starts inside the expert, rows past the expert as zeros (they are the
   // expert's padding in the copy); a tile past the expert writes nothing
-  const bool colwise = !F8 && p.Ct != nullptr && ti.row0 < ti.row_end;
+  const bool colwise = CT && ti.row0 < ti.row_end;
   const int64_t pc0 = (int64_t)ti.pcol0 + q * 32;
   if (EPI == MOE_EPI_SWIGLU_FWD) {
     const int F = p.F;
@@ -422,7 +438,7 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
       float g[32], u[32], act[32];
       tc::tmem_ld32(taddr + c * 32, g);
       tc::tmem_ld32(taddr + BN / 2 + c * 32, u);
-      if (F8) {
+      if (kDeq) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           g[j] *= sc;
@@ -462,6 +478,33 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
 #pragma unroll
       for (int j = 0; j < 32; ++j) act[j] = g[j] * sigmoid_f(g[j]) * u[j];
       if (track) amx = chunk_amax(amx, act, F - nc);
+      if (!CT) {  // (kept apart: the shared form below costs this instance registers)
+        if (bulk) {
+          stage_acquire(lane);
+          stage_bf16(stg, lane, g);
+          stage_bf16(stg + 2048, lane, u);
+          stage_bf16(stg + 4096, lane, act);
+          stage_release();
+          if (lane == 0) {
+            tc::tma_store_2d_hint(om.m0, stg, nc, wrow0, om.stream_pol);
+            tc::tma_store_2d_hint(om.m1, stg + 2048, nc, wrow0, om.stream_pol);
+            tc::tma_store_2d(om.m2, stg + 4096, nc, wrow0);
+            tc::bulk_commit();
+          }
+        } else if (valid) {
+          uint16_t *H = static_cast<uint16_t *>(p.C) + row * p.ldc;
+          uint16_t *A = p.C2 + row * p.ldc2;
+#pragma unroll
+          for (int j8 = 0; j8 < 4; ++j8) {
+            const int n = nc + j8 * 8;
+            if (n >= F) break;
+            st_bf16x8(H + n, g + j8 * 8);
+            st_bf16x8(H + F + n, u + j8 * 8);
+            st_bf16x8(A + n, act + j8 * 8);
+          }
+        }
+        continue;
+      }
       if (bulk || colwise) {
         stage_acquire(lane);
         if (bulk) {
@@ -526,7 +569,7 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
       }
       float v[32];
       tc::tmem_ld32(taddr + c * 32, v);
-      if (F8) {
+      if (kDeq) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] *= sc;
       }
@@ -594,7 +637,7 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
       if (has_in && c + 1 < c_end && nc + 32 < N) load_chunk(c + 1, nxt);
       float v[32];
       tc::tmem_ld32(taddr + c * 32, v);
-      if (F8) {
+      if (kDeq) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] *= sc;
       }
@@ -644,10 +687,11 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
 // tgmm epilogue: warp q owns output rows m in [m_idx*128 + 32q, +32) of W_e.
 // `zero`: the expert had no rows, so TMEM is not read.  Bulk stores, or bulk
 // fp32 reduce-adds into W when accumulating; the box is clipped at M and N.
-template <bool F8>
+template <bool F8, int BN, bool MX>
 MOE_DEVINL void epilogue_tgmm(const TcParams &p, const TileInfo &ti, uint32_t taddr, int q,
                               int lane, uint8_t *stg, const OutMaps &om, bool zero) {
-  const float sc = F8 && !zero ? __ldg(p.a_sinv) * __ldg(p.b_sinv) : 1.0f;
+  constexpr bool kDeq = F8 && !MX;
+  const float sc = kDeq && !zero ? __ldg(p.a_sinv) * __ldg(p.b_sinv) : 1.0f;
   const int wm0 = ti.m_idx * BM + q * 32;
   const int n0 = ti.n_idx * BN;
 #pragma unroll 1
@@ -660,7 +704,7 @@ MOE_DEVINL void epilogue_tgmm(const TcParams &p, const TileInfo &ti, uint32_t ta
       for (int j = 0; j < 32; ++j) v[j] = 0.f;
     } else {
       tc::tmem_ld32(taddr + c * 32, v);
-      if (F8) {
+      if (kDeq) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] *= sc;
       }
@@ -678,26 +722,28 @@ MOE_DEVINL void epilogue_tgmm(const TcParams &p, const TileInfo &ti, uint32_t ta
 }
 
 // ------------------------------------------------------------------ kernel
-template <int KIND, bool B_MN, int EPI, bool F8, bool AK>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Ring<KIND, EPI, F8>::threads, 1)
+template <int KIND, bool B_MN, int EPI, bool F8, bool AK, int BN, bool MX, bool CT>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Ring<KIND, EPI, F8, BN, MX>::threads, 1)
 gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1,
               const __grid_constant__ CUtensorMap tmC2, const __grid_constant__ CUtensorMap tmC3,
+              const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
               const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  Book &bk = *reinterpret_cast<Book *>(smem + Ring<KIND, EPI, F8>::book_offset);
+  Book &bk = *reinterpret_cast<Book *>(smem + Ring<KIND, EPI, F8, BN, MX>::book_offset);
   volatile int *abort_flag = &bk.abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int crank = (int)tc::cluster_ctarank();
   const int cid = (int)tc::cluster_id_x();
   const int ncl = (int)tc::nclusters_x();
   constexpr uint16_t kPair = 0x3;
-  constexpr int kSt = Ring<KIND, EPI, F8>::stages;
-  constexpr int kStageB = Ring<KIND, EPI, F8>::stage_bytes;
+  constexpr int kSt = Ring<KIND, EPI, F8, BN, MX>::stages;
+  constexpr int kStageB = Ring<KIND, EPI, F8, BN, MX>::stage_bytes;
   constexpr int BKE = Elem<F8>::BKE;
-  constexpr int kEW = Ring<KIND, EPI, F8>::epi_warps;
+  constexpr int kEW = Ring<KIND, EPI, F8, BN, MX>::epi_warps;
+  constexpr int kSfOff = A_BYTES + Ring<KIND, EPI, F8, BN, MX>::b_bytes;  // scale factors in a stage
   // bf16 weight gradients read A as stored (MN-major) unless AK: then from a
   // zero-padded column-wise copy (K-major), like FP8 always does
   constexpr bool A_MN = KIND == KIND_TGMM && !AK;
@@ -842,6 +888,21 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
               tc::tma_load_3d_2sm(sb, &tmB, fbl, kb * BKE, nrow, ti.e);
             }
           }
+          if (MX) {
+            // the K block's scale-factor atoms: this CTA's 128 A rows, and the
+            // tile's 128 B columns (both CTAs load the same B atom)
+            int64_t ia, ib;
+            if (KIND == KIND_GMM) {
+              ia = ((int64_t)bk.poff[ti.e] + ti.m_idx) * p.sfa_stride + kb;
+              ib = (int64_t)ti.n_idx * p.sfb_nstride + (int64_t)ti.e * p.sfb_estride + kb;
+            } else {
+              const int kb0 = ti.k0 / BKE + kb;
+              ia = (int64_t)ti.m_idx * p.sfa_stride + kb0;
+              ib = (int64_t)ti.n_idx * p.sfb_nstride + kb0;
+            }
+            tc::tma_load_2d_2sm(sa + kSfOff, &tmSA, fbl, 0, (int)ia);
+            tc::tma_load_2d_2sm(sa + kSfOff + 512, &tmSB, fbl, 0, (int)ib);
+          }
           ++issued;
           if (++s == kSt) {
             s = 0;
@@ -860,6 +921,10 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   } else if (warp == 1 && leader) {
     const uint32_t IDESC = F8 ? tc::idesc_f8(2 * BM, BN, p.a_fmt, p.b_fmt)
                               : tc::idesc_bf16(2 * BM, BN, A_MN, B_MN);
+    // block scaling: the kk-th MMA of a K block reads byte kk of the scale words
+    uint32_t IDESC_MX[4];
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) IDESC_MX[kk] = tc::idesc_mxf8(2 * BM, BN, p.a_fmt, p.b_fmt, kk, kk);
     uint32_t acc_it = 0;
     int s = 0;         // ring slot of the next K block
     uint32_t ph = 0;   // its pass over the ring (parity)
@@ -918,12 +983,26 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                                     : tc::sdesc(tc::smem_u32(sb), 16, 1024);
           constexpr uint64_t kAStep = A_MN ? (UK * 128) >> 4 : 32 >> 4;
           constexpr uint64_t kBStep = B_MN ? (UK * 128) >> 4 : 32 >> 4;
+          if (MX) {
+            // the stage's scale factors -> tensor memory (4 columns each for
+            // A and B, per ring slot, after the two accumulators); the copies
+            // and the MMAs run in issue order
+            const uint32_t sft = tmem + 2 * BN + s * 8;
+            tc::tmem_cp_32x128b_x4_2sm(sft, tc::sdesc_plain(tc::smem_u32(sa + kSfOff), 0, 128));
+            tc::tmem_cp_32x128b_x4_2sm(sft + 4,
+                                       tc::sdesc_plain(tc::smem_u32(sa + kSfOff + 512), 0, 128));
 #pragma unroll
-          for (int kk = 0; kk < BK / UK; ++kk) {
-            const uint64_t ad = ad0 + kk * kAStep;
-            const uint64_t bd = bd0 + kk * kBStep;
-            if (F8) tc::umma_f8_2sm(d_tmem, ad, bd, IDESC, (kb | kk) != 0);
-            else tc::umma_bf16_2sm(d_tmem, ad, bd, IDESC, (kb | kk) != 0);
+            for (int kk = 0; kk < BK / UK; ++kk)
+              tc::umma_mxf8_2sm(d_tmem, ad0 + kk * kAStep, bd0 + kk * kBStep, IDESC_MX[kk], sft,
+                                sft + 4, (kb | kk) != 0);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < BK / UK; ++kk) {
+              const uint64_t ad = ad0 + kk * kAStep;
+              const uint64_t bd = bd0 + kk * kBStep;
+              if (F8) tc::umma_f8_2sm(d_tmem, ad, bd, IDESC, (kb | kk) != 0);
+              else tc::umma_bf16_2sm(d_tmem, ad, bd, IDESC, (kb | kk) != 0);
+            }
           }
           // release the stage in both CTAs
           tc::umma_commit_2sm_mc(&bk.empty[s], kPair);
@@ -950,7 +1029,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   } else if (warp >= 2) {
     const int q = warp & 3;  // TMEM lane quarter this warp may read = its tile rows
     const int rit = q * 32 + lane;
-    uint8_t *stg = smem + Ring<KIND, EPI, F8>::stg_offset + (warp - 2) * kStgBytes;
+    uint8_t *stg = smem + Ring<KIND, EPI, F8, BN, MX>::stg_offset + (warp - 2) * kStgBytes;
     constexpr int kChunks = BN / 32;  // the tile's 32-column chunks, all this warp's
     const int c_begin = 0;
     OutMaps om{&tmC0, &tmC1, &tmC2, &tmC3, &bk.aux_full[warp - 2], 0u, 0u,
@@ -960,10 +1039,10 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     for (int t = cid; t < total; t += ncl) {
       const TileInfo ti = decode_tile<KIND, F8, AK>(bk, p, t, crank);
       if (KIND == KIND_TGMM && ti.kblocks == 0) {
-        if (!p.accumulate) epilogue_tgmm<F8>(p, ti, 0, q, lane, stg, om, true);
+        if (!p.accumulate) epilogue_tgmm<F8, BN, MX>(p, ti, 0, q, lane, stg, om, true);
         continue;
       }
-      epilogue_prefetch<KIND, EPI>(p, ti, rit, c_begin, c_begin + kChunks);
+      epilogue_prefetch<KIND, EPI, BN>(p, ti, rit, c_begin, c_begin + kChunks);
       if (KIND == KIND_GMM && EPI == MOE_EPI_SWIGLU_BWD && lane == 0)
         issue_aux_load(om, stg, ti.n_idx * BN + c_begin * 32, ti.row0 + q * 32);  // first chunk
       const uint32_t a = acc_it & 1;
@@ -972,10 +1051,10 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       tc::tc_fence_after();
       const uint32_t taddr = tmem + a * BN + (static_cast<uint32_t>(q * 32) << 16);
       if (KIND == KIND_GMM)
-        epilogue_gmm<EPI, F8>(p, ti, taddr, q, lane, stg, om, abort_flag, c_begin,
+        epilogue_gmm<EPI, F8, BN, MX, CT>(p, ti, taddr, q, lane, stg, om, abort_flag, c_begin,
                               c_begin + kChunks, amx);
       else
-        epilogue_tgmm<F8>(p, ti, taddr, q, lane, stg, om, false);
+        epilogue_tgmm<F8, BN, MX>(p, ti, taddr, q, lane, stg, om, false);
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -1058,23 +1137,25 @@ bool make_out_map(CUtensorMap *m, const void *base, bool f32, int64_t cols, int6
                   f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-template <int KIND, bool B_MN, int EPI, bool F8 = false, bool AK = F8>
+template <int KIND, bool B_MN, int EPI, bool F8 = false, bool AK = F8, int BN = kBN,
+          bool MX = false, bool CT = false>
 moe_status_t launch_tc(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap *mc,
-                       const TcParams &p, int64_t tiles_upper, cudaStream_t s) {
-  constexpr int kSmem = Ring<KIND, EPI, F8>::smem_bytes;
+                       const TcParams &p, int64_t tiles_upper, cudaStream_t s,
+                       const CUtensorMap *msf = nullptr) {
+  constexpr int kSmem = Ring<KIND, EPI, F8, BN, MX>::smem_bytes;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   static int max_clusters = 0;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gmm_tc_kernel<KIND, B_MN, EPI, F8, AK>,
+    attr_err = cudaFuncSetAttribute(gmm_tc_kernel<KIND, B_MN, EPI, F8, AK, BN, MX, CT>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (attr_err != cudaSuccess) return;
     // clusters of two CTAs (one per SM) that can be resident at once
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (unsigned)num_sms());
-    cfg.blockDim = dim3(Ring<KIND, EPI, F8>::threads);
+    cfg.blockDim = dim3(Ring<KIND, EPI, F8, BN, MX>::threads);
     cfg.dynamicSmemBytes = kSmem;
-    if (cudaOccupancyMaxActiveClusters(&max_clusters, gmm_tc_kernel<KIND, B_MN, EPI, F8, AK>, &cfg) !=
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, gmm_tc_kernel<KIND, B_MN, EPI, F8, AK, BN, MX, CT>, &cfg) !=
             cudaSuccess ||
         max_clusters <= 0) {
       cudaGetLastError();
@@ -1088,8 +1169,9 @@ moe_status_t launch_tc(const CUtensorMap &ma, const CUtensorMap &mb, const CUten
   }
   const int64_t pairs = (tiles_upper + 1) / 2;
   const int grid = 2 * (int)std::max<int64_t>(1, std::min<int64_t>(max_clusters, pairs));
-  gmm_tc_kernel<KIND, B_MN, EPI, F8, AK><<<grid, Ring<KIND, EPI, F8>::threads, kSmem, s>>>(
-      ma, mb, mc[0], mc[1], mc[2], mc[3], p);
+  gmm_tc_kernel<KIND, B_MN, EPI, F8, AK, BN, MX, CT><<<grid, Ring<KIND, EPI, F8, BN, MX>::threads, kSmem, s>>>(
+      ma, mb, mc[0], mc[1], mc[2], mc[3], msf != nullptr ? msf[0] : ma,
+      msf != nullptr ? msf[1] : ma, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_error("grouped GEMM launch: %s", cudaGetErrorString(e));
@@ -1132,7 +1214,7 @@ moe_status_t launch_gmm(const GmmArgs &a, cudaStream_t s) {
   } else {
     const uint64_t dims[3] = {(uint64_t)a.K, (uint64_t)a.N, (uint64_t)a.E};
     const uint64_t st[2] = {(uint64_t)a.ldb * 2, (uint64_t)stride_b * 2};
-    const uint32_t box[3] = {BK, BN / 2, 1};
+    const uint32_t box[3] = {BK, kBN / 2, 1};
     if (!make_map(&mb, a.B, 3, dims, st, box)) {
       set_error("moe_gmm: cannot encode the TMA descriptor of B");
       return MOE_ERR_CUDA;
@@ -1144,7 +1226,7 @@ moe_status_t launch_gmm(const GmmArgs &a, cudaStream_t s) {
   p.K = a.K;
   p.N = a.N;
   p.F = a.epilogue == MOE_EPI_SWIGLU_FWD ? a.N / 2 : a.N;
-  p.n_tiles = a.epilogue == MOE_EPI_SWIGLU_FWD ? (p.F + BN / 2 - 1) / (BN / 2) : (a.N + BN - 1) / BN;
+  p.n_tiles = a.epilogue == MOE_EPI_SWIGLU_FWD ? (p.F + kBN / 2 - 1) / (kBN / 2) : (a.N + kBN - 1) / kBN;
   p.offsets = a.offsets;
   p.C = a.C;
   p.ldc = a.ldc;
@@ -1192,6 +1274,20 @@ moe_status_t launch_gmm(const GmmArgs &a, cudaStream_t s) {
     return MOE_ERR_CUDA;
   }
   const int64_t tiles_upper = ((a.rows_cap + BM - 1) / BM + a.E) * p.n_tiles;
+  // the column-wise copies (Ct) come from instances of their own, so that the
+  // default epilogues keep their registers
+  if (a.Ct != nullptr) {
+    if (a.epilogue == MOE_EPI_SWIGLU_FWD && b_mn)
+      return launch_tc<KIND_GMM, true, MOE_EPI_SWIGLU_FWD, false, false, kBN, false, true>(
+          ma, mb, mc, p, tiles_upper, s);
+    if (a.epilogue == MOE_EPI_SWIGLU_BWD)
+      return b_mn ? launch_tc<KIND_GMM, true, MOE_EPI_SWIGLU_BWD, false, false, kBN, false, true>(
+                        ma, mb, mc, p, tiles_upper, s)
+                  : launch_tc<KIND_GMM, false, MOE_EPI_SWIGLU_BWD, false, false, kBN, false,
+                              true>(ma, mb, mc, p, tiles_upper, s);
+    set_error("moe_gmm: no column-wise copy for this epilogue / layout");
+    return MOE_ERR_UNSUPPORTED;
+  }
   switch (a.epilogue * 2 + (b_mn ? 1 : 0)) {
     case MOE_EPI_NONE * 2 + 1:
       return launch_tc<KIND_GMM, true, MOE_EPI_NONE>(ma, mb, mc, p, tiles_upper, s);
@@ -1238,7 +1334,7 @@ static moe_status_t tgmm_impl(const TgmmArgs &a, const uint16_t *At, int64_t lda
   if (b_colwise) {
     const uint64_t dims[2] = {(uint64_t)f8_padded_rows(a.rows_cap, a.E), (uint64_t)a.N};
     const uint64_t st[1] = {(uint64_t)a.ldb * 2};
-    const uint32_t bbox[2] = {BK, BN / 2};
+    const uint32_t bbox[2] = {BK, kBN / 2};
     if (!make_map(&mb, a.B, 2, dims, st, bbox)) {
       set_error("moe_tgmm: cannot encode the TMA descriptor of B");
       return MOE_ERR_CUDA;
@@ -1257,7 +1353,7 @@ static moe_status_t tgmm_impl(const TgmmArgs &a, const uint16_t *At, int64_t lda
   p.M = a.M;
   p.N = a.N;
   p.m_tiles = (a.M + BM - 1) / BM;
-  p.n_tiles = (a.N + BN - 1) / BN;
+  p.n_tiles = (a.N + kBN - 1) / kBN;
   p.offsets = a.offsets;
   p.C = a.W;
   p.ldc = a.ldw;
@@ -1346,7 +1442,7 @@ moe_status_t launch_gmm_f8(const GmmF8Args &a, cudaStream_t s) {
   {
     const uint64_t dims[3] = {(uint64_t)a.K, (uint64_t)a.N, (uint64_t)a.E};
     const uint64_t st[2] = {(uint64_t)a.ldb, (uint64_t)stride_b};
-    const uint32_t box[3] = {Elem<true>::BKE, BN / 2, 1};
+    const uint32_t box[3] = {Elem<true>::BKE, kBN / 2, 1};
     if (!make_map(&mb, a.B, 3, dims, st, box, CU_TENSOR_MAP_DATA_TYPE_UINT8)) {
       set_error("moe_gmm_fp8: cannot encode the TMA descriptor of B");
       return MOE_ERR_CUDA;
@@ -1358,7 +1454,7 @@ moe_status_t launch_gmm_f8(const GmmF8Args &a, cudaStream_t s) {
   p.K = a.K;
   p.N = a.N;
   p.F = a.epilogue == MOE_EPI_SWIGLU_FWD ? a.N / 2 : a.N;
-  p.n_tiles = a.epilogue == MOE_EPI_SWIGLU_FWD ? (p.F + BN / 2 - 1) / (BN / 2) : (a.N + BN - 1) / BN;
+  p.n_tiles = a.epilogue == MOE_EPI_SWIGLU_FWD ? (p.F + kBN / 2 - 1) / (kBN / 2) : (a.N + kBN - 1) / kBN;
   p.offsets = a.offsets;
   p.C = a.C;
   p.ldc = a.ldc;
@@ -1432,7 +1528,7 @@ moe_status_t launch_tgmm_f8(const TgmmF8Args &a, cudaStream_t s) {
   p.M = a.M;
   p.N = a.N;
   p.m_tiles = (a.M + BM - 1) / BM;
-  p.n_tiles = (a.N + BN - 1) / BN;
+  p.n_tiles = (a.N + kBN - 1) / kBN;
   p.offsets = a.offsets;
   p.C = a.W;
   p.ldc = a.ldw;
@@ -1464,6 +1560,173 @@ moe_status_t launch_tgmm_f8(const TgmmF8Args &a, cudaStream_t s) {
   }
   const int64_t tiles_upper = (int64_t)a.E * p.m_tiles * p.n_tiles;
   return launch_tc<KIND_TGMM, false, MOE_EPI_NONE, true>(ma, mb, mc, p, tiles_upper, s);
+}
+
+// Scale-factor map of a block-scaled operand: `atoms` 512-byte atoms viewed
+// as [atoms, 128] 32-bit words, one atom per TMA box.
+static bool make_sf_map(CUtensorMap *m, const uint8_t *sf, int64_t atoms) {
+  const uint64_t dims[2] = {128, (uint64_t)atoms};
+  const uint64_t st[1] = {512};
+  const uint32_t box[2] = {128, 1};
+  return make_map(m, sf, 2, dims, st, box, CU_TENSOR_MAP_DATA_TYPE_UINT32,
+                  CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+constexpr int kBNmx = 128;  // tile width of the block-scaled GEMMs
+
+moe_status_t launch_gmm_mx(const GmmMxArgs &a, cudaStream_t s) {
+  if (a.E > kMaxE) {
+    set_error("moe_gmm_mx: E=%d > %d", a.E, kMaxE);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  const int64_t stride_b = a.E > 1 ? a.stride_b : (int64_t)a.N * a.ldb;
+  const int KB = a.K / 128;
+  CUtensorMap ma, mb, msf[2];
+  {
+    const uint64_t dims[2] = {(uint64_t)a.K, (uint64_t)a.rows_cap};
+    const uint64_t st[1] = {(uint64_t)a.lda};
+    const uint32_t box[2] = {Elem<true>::BKE, BM};
+    if (!make_map(&ma, a.A, 2, dims, st, box, CU_TENSOR_MAP_DATA_TYPE_UINT8)) {
+      set_error("moe_gmm_mx: cannot encode the TMA descriptor of A");
+      return MOE_ERR_CUDA;
+    }
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)a.K, (uint64_t)a.N, (uint64_t)a.E};
+    const uint64_t st[2] = {(uint64_t)a.ldb, (uint64_t)stride_b};
+    const uint32_t box[3] = {Elem<true>::BKE, kBNmx / 2, 1};
+    if (!make_map(&mb, a.B, 3, dims, st, box, CU_TENSOR_MAP_DATA_TYPE_UINT8)) {
+      set_error("moe_gmm_mx: cannot encode the TMA descriptor of B");
+      return MOE_ERR_CUDA;
+    }
+  }
+  // A's atoms: the expert-padded row tiles; B's: every (column tile, expert, K block)
+  const int64_t a_atoms = f8_padded_rows(a.rows_cap, a.E) / 128 * KB;
+  const int n_tiles_b = a.epilogue == MOE_EPI_SWIGLU_FWD ? a.N / kBNmx : (a.N + kBNmx - 1) / kBNmx;
+  const int64_t b_atoms = (int64_t)(n_tiles_b - 1) * a.sfb_nstride +
+                          (int64_t)(a.E - 1) * a.sfb_estride + KB;
+  if (!make_sf_map(&msf[0], a.sfa, a_atoms) || !make_sf_map(&msf[1], a.sfb, b_atoms)) {
+    set_error("moe_gmm_mx: cannot encode the TMA descriptors of the scale factors");
+    return MOE_ERR_CUDA;
+  }
+  TcParams p{};
+  p.E = a.E;
+  p.rows_cap = (int)a.rows_cap;
+  p.K = a.K;
+  p.N = a.N;
+  p.F = a.epilogue == MOE_EPI_SWIGLU_FWD ? a.N / 2 : a.N;
+  p.n_tiles = a.epilogue == MOE_EPI_SWIGLU_FWD ? (p.F + kBNmx / 2 - 1) / (kBNmx / 2)
+                                               : (a.N + kBNmx - 1) / kBNmx;
+  p.offsets = a.offsets;
+  p.C = a.C;
+  p.ldc = a.ldc;
+  p.c_f32 = a.c_dtype == MOE_DTYPE_F32;
+  p.C2 = a.C2;
+  p.ldc2 = a.ldc2;
+  p.aux = a.aux;
+  p.ld_aux = a.ld_aux;
+  p.dev_status = a.dev_status;
+  p.wait_limit_ns = wait_limit_ns();
+  p.stall_loads = test_stall_loads();
+  p.a_fmt = a.a_fmt;
+  p.b_fmt = a.b_fmt;
+  p.sfa_stride = KB;
+  p.sfb_nstride = a.sfb_nstride;
+  p.sfb_estride = a.sfb_estride;
+  CUtensorMap mc[4];
+  if (!gmm_out_maps(mc, a.epilogue, a.C, a.c_dtype, a.ldc, a.C2, a.ldc2, a.aux, a.ld_aux, a.N,
+                    p.F, a.rows_cap)) {
+    set_error("moe_gmm_mx: cannot encode the TMA descriptor of the output");
+    return MOE_ERR_CUDA;
+  }
+  const int64_t tiles_upper = ((a.rows_cap + BM - 1) / BM + a.E) * p.n_tiles;
+  switch (a.epilogue) {
+    case MOE_EPI_NONE:
+      return launch_tc<KIND_GMM, false, MOE_EPI_NONE, true, true, kBNmx, true>(
+          ma, mb, mc, p, tiles_upper, s, msf);
+    case MOE_EPI_SWIGLU_FWD:
+      return launch_tc<KIND_GMM, false, MOE_EPI_SWIGLU_FWD, true, true, kBNmx, true>(
+          ma, mb, mc, p, tiles_upper, s, msf);
+    case MOE_EPI_SWIGLU_BWD:
+      return launch_tc<KIND_GMM, false, MOE_EPI_SWIGLU_BWD, true, true, kBNmx, true>(
+          ma, mb, mc, p, tiles_upper, s, msf);
+    default:
+      set_error("moe_gmm_mx: unsupported epilogue");
+      return MOE_ERR_UNSUPPORTED;
+  }
+}
+
+moe_status_t launch_tgmm_mx(const TgmmMxArgs &a, cudaStream_t s) {
+  if (a.E > kMaxE) {
+    set_error("moe_tgmm_mx: E=%d > %d", a.E, kMaxE);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  const int64_t P = f8_padded_rows(a.rows_cap, a.E);
+  CUtensorMap ma, mb, msf[2];
+  const uint32_t abox[2] = {Elem<true>::BKE, BM};
+  const uint32_t bbox[2] = {Elem<true>::BKE, kBNmx / 2};
+  {
+    const uint64_t dims[2] = {(uint64_t)P, (uint64_t)a.M};
+    const uint64_t st[1] = {(uint64_t)a.ldat};
+    if (!make_map(&ma, a.At, 2, dims, st, abox, CU_TENSOR_MAP_DATA_TYPE_UINT8)) {
+      set_error("moe_tgmm_mx: cannot encode the TMA descriptor of A");
+      return MOE_ERR_CUDA;
+    }
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)P, (uint64_t)a.N};
+    const uint64_t st[1] = {(uint64_t)a.ldbt};
+    if (!make_map(&mb, a.Bt, 2, dims, st, bbox, CU_TENSOR_MAP_DATA_TYPE_UINT8)) {
+      set_error("moe_tgmm_mx: cannot encode the TMA descriptor of B");
+      return MOE_ERR_CUDA;
+    }
+  }
+  // both copies were quantized as plain [rows, P] matrices: atom (row tile, K block)
+  const int64_t pk = P / 128;
+  if (!make_sf_map(&msf[0], a.sfa, (a.M + 127) / 128 * pk) ||
+      !make_sf_map(&msf[1], a.sfb, (a.N + 127) / 128 * pk)) {
+    set_error("moe_tgmm_mx: cannot encode the TMA descriptors of the scale factors");
+    return MOE_ERR_CUDA;
+  }
+  TcParams p{};
+  p.E = a.E;
+  p.rows_cap = (int)a.rows_cap;
+  p.M = a.M;
+  p.N = a.N;
+  p.m_tiles = (a.M + BM - 1) / BM;
+  p.n_tiles = (a.N + kBNmx - 1) / kBNmx;
+  p.offsets = a.offsets;
+  p.C = a.W;
+  p.ldc = a.ldw;
+  p.c_f32 = a.w_dtype == MOE_DTYPE_F32;
+  p.stride_w = a.stride_w;
+  p.accumulate = a.accumulate;
+  p.dev_status = a.dev_status;
+  p.wait_limit_ns = wait_limit_ns();
+  p.stall_loads = test_stall_loads();
+  p.a_fmt = a.a_fmt;
+  p.b_fmt = a.b_fmt;
+  p.sfa_stride = pk;
+  p.sfb_nstride = pk;
+  CUtensorMap mc[4];
+  {
+    const bool f32 = a.w_dtype == MOE_DTYPE_F32;
+    const int64_t es = f32 ? 4 : 2;
+    const int64_t stride_w = a.E > 1 ? a.stride_w : (int64_t)a.M * a.ldw;
+    const uint64_t dims[3] = {(uint64_t)a.N, (uint64_t)a.M, (uint64_t)a.E};
+    const uint64_t st[2] = {(uint64_t)(a.ldw * es), (uint64_t)(stride_w * es)};
+    const uint32_t wbox[3] = {32, 32, 1};
+    if (!make_map(&mc[0], a.W, 3, dims, st, wbox,
+                  f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                  f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B)) {
+      set_error("moe_tgmm_mx: cannot encode the TMA descriptor of W");
+      return MOE_ERR_CUDA;
+    }
+    mc[1] = mc[2] = mc[3] = mc[0];
+  }
+  const int64_t tiles_upper = (int64_t)a.E * p.m_tiles * p.n_tiles;
+  return launch_tc<KIND_TGMM, false, MOE_EPI_NONE, true, true, kBNmx, true>(
+      ma, mb, mc, p, tiles_upper, s, msf);
 }
 
 }  // namespace moe

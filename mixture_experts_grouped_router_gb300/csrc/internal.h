@@ -80,6 +80,12 @@ cudaError_t launch_sort_chunks(const uint16_t *src, int64_t ld_src, uint16_t *ds
                                int d, const int64_t *src_off, const int64_t *dst_off,
                                const int64_t *len, int n_chunks, int64_t rows, cudaStream_t s);
 
+// mx.cu (block-scaled 8-bit quantization)
+int64_t mx_atom_rows(int64_t rows, int row_map, int E);
+cudaError_t launch_mx_quantize(const uint16_t *x, int64_t ldx, int64_t rows, int cols, int fmt,
+                               int row_map, const int32_t *offsets, int E, uint8_t *q,
+                               int64_t ldq, uint8_t *sf, cudaStream_t s);
+
 // gmm_sm103.cu
 struct GmmArgs {
   const uint16_t *A; int64_t lda;
@@ -131,5 +137,28 @@ struct TgmmF8Args {
   int32_t *dev_status;
 };
 moe_status_t launch_tgmm_f8(const TgmmF8Args &a, cudaStream_t s);
+
+// block-scaled (MXFP8): scale atoms beside the codes (mx.cu layout)
+struct GmmMxArgs {
+  const uint8_t *A; int64_t lda; const uint8_t *sfa; int a_fmt;
+  const uint8_t *B; int64_t ldb; int64_t stride_b; const uint8_t *sfb;
+  int64_t sfb_nstride; int64_t sfb_estride; int b_fmt;
+  const int32_t *offsets; int E; int64_t rows_cap; int K; int N;
+  int epilogue;
+  const uint16_t *aux; int64_t ld_aux;
+  void *C; int c_dtype; int64_t ldc;
+  uint16_t *C2; int64_t ldc2;
+  int32_t *dev_status;
+};
+moe_status_t launch_gmm_mx(const GmmMxArgs &a, cudaStream_t s);
+
+struct TgmmMxArgs {
+  const uint8_t *At; int64_t ldat; const uint8_t *sfa; int a_fmt;
+  const uint8_t *Bt; int64_t ldbt; const uint8_t *sfb; int b_fmt;
+  const int32_t *offsets; int E; int64_t rows_cap; int M; int N;
+  void *W; int w_dtype; int64_t ldw; int64_t stride_w; int accumulate;
+  int32_t *dev_status;
+};
+moe_status_t launch_tgmm_mx(const TgmmMxArgs &a, cudaStream_t s);
 
 }  // namespace moe

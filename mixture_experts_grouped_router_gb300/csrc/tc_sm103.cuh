@@ -273,6 +273,52 @@ __host__ __device__ constexpr uint32_t idesc_f8(int M, int N, int a_fmt, int b_f
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Instruction descriptor of kind::mxf8f6f4 with block scaling (one E8M0
+// scale per 32 elements along K for A rows and B columns), fp32 accumulation,
+// both operands K-major: bits 4-5 which byte of B's 32-bit scale words this
+// MMA uses, 7-9 / 10-12 A / B format (0 = E4M3, 1 = E5M2), 17-22 N >> 3, 23
+// scale format (1 = UE8M0), 24-28 M >> 4, 29-30 the byte of A's scale words.
+__host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N, int a_fmt, int b_fmt, int a_sf_id,
+                                                  int b_sf_id) {
+  return (static_cast<uint32_t>(b_sf_id) << 4) | (static_cast<uint32_t>(a_fmt) << 7) |
+         (static_cast<uint32_t>(b_fmt) << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24) |
+         (static_cast<uint32_t>(a_sf_id) << 29);
+}
+
+// Shared-memory descriptor without swizzling (descriptor version 1): 8-row x
+// 16-byte core matrices, `sbo` bytes between consecutive 8-row groups.
+MOE_DEVINL uint64_t sdesc_plain(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
+
+// Shared -> tensor memory copy of 32 rows x 128 bits, replicated into the
+// four 32-lane quarters (warpx4), issued by the pair's leader for both CTAs:
+// each CTA's own shared memory at the descriptor's address lands in its own
+// tensor memory at taddr (4 columns).
+MOE_DEVINL void tmem_cp_32x128b_x4_2sm(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
+// Block-scaled MMA over both CTAs of the pair: D (+)= (A . 2^sfa) x (B . 2^sfb)
+// with the scale factors read from tensor memory at sfa / sfb.
+MOE_DEVINL void umma_mxf8_2sm(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                              uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
+      "r"(accumulate)
+      : "memory");
+}
+
 // Tensor-memory columns for the CTA pair (warp-collective, both CTAs), the
 // permit release after it, and the matching deallocation.
 MOE_DEVINL void tmem_alloc_2sm(uint32_t *dst_smem, uint32_t ncols) {

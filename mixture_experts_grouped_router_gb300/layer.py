@@ -29,6 +29,14 @@ With bias=True the expert FFN carries biases (bi [E, 2f] on [gate | up],
 bo [E, d] on the output), added in the GEMM epilogues; their gradients are
 per-expert column sums of dH and dY (moe_group_colsum).
 
+With mxfp8=True the four GEMM pairs run block-scaled (MXFP8, TE-2912's
+wi-fusion commit names the recipe; the arithmetic is the OCP MX definition):
+every operand is quantized with one power-of-two scale per 32 elements along
+the contraction of the GEMM it feeds, E4M3 in the forward (Xs, Act, wi, wo),
+E5M2 for the gradients (dY, dH); the weights are quantized twice (along each
+of their two contractions), the weight gradients read block-scaled
+column-wise copies of Xs, Act, dY and dH.
+
 Weight gradients (bf16): by default the weight-gradient GEMMs read the
 row-wise tensors as stored (MN-major operands).  With wgrad_colwise both
 operands of dWo = Act^T dY and dWi = Xs^T dH are read K-major from
@@ -70,6 +78,7 @@ class LayerShape:
     aux_coeff: float = 0.0
     fp8: bool = False
     wgrad_colwise: bool = False
+    mxfp8: bool = False
 
 
 class MoEBuffers:
@@ -113,7 +122,13 @@ class MoEBuffers:
         self.dbi = torch.empty(E, 2 * f, dtype=f32, device=dev) if s.bias else None
         self.dbo = torch.empty(E, d, dtype=f32, device=dev) if s.bias else None
         self.dev_status = torch.zeros(1, dtype=i32, device=dev)
-        self.colwise = s.wgrad_colwise and not s.fp8
+        if s.mxfp8:
+            if s.fp8 or s.bias or s.num_chunks > 1:
+                raise ValueError("the MXFP8 layer takes neither biases, K-chunks nor fp8")
+            if d % 128 or f % 128:
+                raise ValueError("MXFP8 needs d_model and d_ff multiples of 128")
+            self._alloc_mx(dev)
+        self.colwise = s.wgrad_colwise and not s.fp8 and not s.mxfp8
         if self.colwise:
             # column-wise copies (padded group layout) of the weight gradients' operands
             P = L.moe_fp8_padded_rows(R, E)
@@ -150,8 +165,120 @@ class MoEBuffers:
                                       device=dev)
 
 
+    def _alloc_mx(self, dev):
+        """Codes and scale atoms of every block-scaled operand (row-wise copies
+        for the forward / dgrad GEMMs, column-wise ones for the weight
+        gradients, the weights along both of their contractions)."""
+        s = self.s
+        d, f, E, R = s.d, s.f, s.E, self.rows_cap
+        u8, bf = torch.uint8, torch.bfloat16
+        P = L.moe_fp8_padded_rows(R, E)
+        self.mx_P = P
+        G, PL, SW = L.MX_ROWS_GROUPED, L.MX_ROWS_PLAIN, L.MX_ROWS_SWIGLU
+
+        def q(rows, cols, row_map):
+            return (torch.empty(rows, cols, dtype=u8, device=dev),
+                    torch.empty(L.moe_mx_scale_bytes(rows, cols, row_map, E), dtype=u8,
+                                device=dev))
+        self.mx = dict(xs=q(R, d, G), act=q(R, f, G), dy=q(R, d, G), dh=q(R, 2 * f, G),
+                       xs_t=q(d, P, PL), act_t=q(f, P, PL), dy_t=q(d, P, PL),
+                       dh_t=q(2 * f, P, PL),
+                       wi_t=q(2 * f, E * d, SW), wi=q(E * d, 2 * f, PL),
+                       wo_t=q(d, E * f, PL), wo=q(E * f, d, PL))
+        # bf16 column-wise copies (the transposes the quantizer reads)
+        self.mx_bf = dict(xs_t=torch.empty(d, P, dtype=bf, device=dev),
+                          act_t=torch.empty(f, P, dtype=bf, device=dev),
+                          dy_t=torch.empty(d, P, dtype=bf, device=dev),
+                          dh_t=torch.empty(2 * f, P, dtype=bf, device=dev),
+                          wi_t=torch.empty(2 * f, L.moe_fp8_padded_rows(E * d, E), dtype=bf,
+                                           device=dev),
+                          wo_t=torch.empty(d, L.moe_fp8_padded_rows(E * f, E), dtype=bf,
+                                           device=dev))
+        # the experts' weight rows as groups, for their transposes
+        self.mx_woff_d = torch.arange(0, E * d + 1, d, dtype=torch.int32, device=dev)
+        self.mx_woff_f = torch.arange(0, E * f + 1, f, dtype=torch.int32, device=dev)
+
+
 def _noop(_name):
     pass
+
+
+def _mx_rows(b, name, x, fmt, stream, mark=None):
+    """Block-scaled codes of a permuted activation (blocks along its row)."""
+    q, sf = b.mx[name]
+    L.moe_mx_quantize(x, fmt, q, sf, L.MX_ROWS_GROUPED, b.group_offsets, stream)
+    if mark is not None:
+        mark("mxquant_" + name)
+
+
+def _mx_cols(b, name, x, fmt, stream, mark):
+    """Block-scaled codes of the column-wise copy of a permuted activation
+    (blocks along each expert's rows)."""
+    t = b.mx_bf[name + "_t"]
+    L.moe_transpose_act(x, b.group_offsets, t, stream)
+    q, sf = b.mx[name + "_t"]
+    L.moe_mx_quantize(t[:, :b.mx_P], fmt, q, sf, L.MX_ROWS_PLAIN, None, stream)
+    mark("mxquant_" + name + "_t")
+
+
+def _forward_mx(b, wi, wo, stream, mark):
+    s = b.s
+    d, f, E = s.d, s.f, s.E
+    e4, e5 = L.FP8_E4M3, L.FP8_E5M2
+    _mx_rows(b, "xs", b.xs, e4, stream, mark)
+    # weights along both contractions: wi^T ([2f, E d], SwiGLU tile order) for the
+    # up-projection, wi ([E d, 2f]) for its dgrad; wo^T for the down-projection, wo
+    # for its dgrad
+    L.moe_transpose_act(wi.view(E * d, 2 * f), b.mx_woff_d, b.mx_bf["wi_t"], stream)
+    L.moe_mx_quantize(b.mx_bf["wi_t"][:, :E * d], e4, *b.mx["wi_t"], L.MX_ROWS_SWIGLU, None,
+                      stream)
+    L.moe_mx_quantize(wi.view(E * d, 2 * f), e4, *b.mx["wi"], L.MX_ROWS_PLAIN, None, stream)
+    L.moe_transpose_act(wo.view(E * f, d), b.mx_woff_f, b.mx_bf["wo_t"], stream)
+    L.moe_mx_quantize(b.mx_bf["wo_t"][:, :E * f], e4, *b.mx["wo_t"], L.MX_ROWS_PLAIN, None,
+                      stream)
+    L.moe_mx_quantize(wo.view(E * f, d), e4, *b.mx["wo"], L.MX_ROWS_PLAIN, None, stream)
+    mark("mxquant_weights")
+    qx, sx = b.mx["xs"]
+    qw, sw = b.mx["wi_t"]
+    L.moe_gmm_mx(qx, sx, e4, qw, sw, E * d // 128, d // 128, e4, b.group_offsets, b.h,
+                 L.EPI_SWIGLU_FWD, C2=b.act, dev_status=b.dev_status, stream=stream, E=E,
+                 N=2 * f, K=d, ldb=E * d, stride_b=d)
+    mark("gmm_up_swiglu")
+    _mx_rows(b, "act", b.act, e4, stream, mark)
+    qa, sa = b.mx["act"]
+    qw, sw = b.mx["wo_t"]
+    L.moe_gmm_mx(qa, sa, e4, qw, sw, E * f // 128, f // 128, e4, b.group_offsets, b.y,
+                 dev_status=b.dev_status, stream=stream, E=E, N=d, K=f, ldb=E * f, stride_b=f)
+    mark("gmm_down")
+
+
+def _backward_mx(b, stream, mark):
+    s = b.s
+    d, f, E = s.d, s.f, s.E
+    e4, e5 = L.FP8_E4M3, L.FP8_E5M2
+    _mx_rows(b, "dy", b.dy, e5, stream, mark)
+    qd, sd = b.mx["dy"]
+    qw, sw = b.mx["wo"]
+    L.moe_gmm_mx(qd, sd, e5, qw.view(E, f, d), sw, d // 128, f * d // 16384, e4,
+                 b.group_offsets, b.dh, L.EPI_SWIGLU_BWD, aux=b.h, dev_status=b.dev_status,
+                 stream=stream)
+    mark("gmm_dgrad_down_swiglu_bwd")
+    _mx_cols(b, "act", b.act, e4, stream, mark)
+    _mx_cols(b, "dy", b.dy, e5, stream, mark)
+    L.moe_tgmm_mx(*b.mx["act_t"], e4, *b.mx["dy_t"], e5, b.group_offsets, b.rows_cap, b.dwo,
+                  dev_status=b.dev_status, stream=stream)
+    mark("tgmm_dwo")
+    _mx_rows(b, "dh", b.dh, e5, stream, mark)
+    qh, sh = b.mx["dh"]
+    qw, sw = b.mx["wi"]
+    L.moe_gmm_mx(qh, sh, e5, qw.view(E, d, 2 * f), sw, 2 * f // 128, d * 2 * f // 16384, e4,
+                 b.group_offsets, b.dxs, dev_status=b.dev_status, stream=stream)
+    mark("gmm_dgrad_up")
+    _mx_cols(b, "xs", b.xs, e4, stream, mark)
+    _mx_cols(b, "dh", b.dh, e5, stream, mark)
+    L.moe_tgmm_mx(*b.mx["xs_t"], e4, *b.mx["dh_t"], e5, b.group_offsets, b.rows_cap, b.dwi,
+                  dev_status=b.dev_status, stream=stream)
+    mark("tgmm_dwi")
 
 
 def _fp8_slots(b):
@@ -236,6 +363,11 @@ def forward(b: MoEBuffers, x, logits, wi, wo, stream=None, mark=_noop, bi=None, 
     L.moe_permute(x, b.topk_idx, s.E, s.align, s.capacity, b.xs, b.group_sizes, b.kept_counts,
                   b.group_offsets, b.s2f, b.f2s, b.ws, b.dev_status, stream)
     mark("permute")
+    if s.mxfp8:
+        _forward_mx(b, wi, wo, stream, mark)
+        L.moe_combine(b.y, b.f2s, b.topk_w, b.out, s.k, stream)
+        mark("combine")
+        return b.out
     if s.fp8:
         _forward_fp8(b, x, logits, wi, wo, stream, mark)
         L.moe_combine(b.y, b.f2s, b.topk_w, b.out, s.k, stream)
@@ -283,6 +415,11 @@ def backward(b: MoEBuffers, dout, wi, wo, stream=None, mark=_noop):
         L.moe_aux_loss_bwd(b.logits, b.aux_counts, s.k, s.score_fn, s.aux_coeff, b.d_logits,
                            d_loss=1.0, accumulate=True, stream=stream)
         mark("aux_loss_bwd")
+    if s.mxfp8:
+        _backward_mx(b, stream, mark)
+        L.moe_combine(b.dxs, b.f2s, None, b.dx, s.k, stream)
+        mark("dispatch_bwd")
+        return b.dx, b.dwi, b.dwo, b.d_topk_w
     if s.fp8:
         _backward_fp8(b, stream, mark)
         L.moe_combine(b.dxs, b.f2s, None, b.dx, s.k, stream)
@@ -347,6 +484,9 @@ def kernels_per_step(s: LayerShape) -> int:
     if s.fp8:   # amax + quantize for x, wi, wo; quantize for act (amax in the GEMM);
         fwd += 7   # amax + quantize for dy; quantize for dh
         bwd += 3
+    elif s.mxfp8:  # quantize xs, act (+2 transposes, 4 quantizes of the weights);
+        fwd += 2 + 6  # quantize dy, dh; transpose + quantize act, dy, xs, dh
+        bwd += 2 + 8
     elif s.wgrad_colwise:
         bwd += 2
     return fwd + bwd

@@ -34,6 +34,7 @@ from __future__ import annotations
 import numpy as np
 
 from oracle import moe_fp8_ref as q8
+from oracle import moe_ref
 
 BLOCK = 32
 E8M0_BIAS = 127
@@ -58,17 +59,16 @@ def mx_quantize(x, fmt: str):
     K = x32.shape[-1]
     assert K % BLOCK == 0, "the contraction axis must hold whole blocks of 32"
     blocks = x32.reshape(-1, K // BLOCK, BLOCK).astype(np.float64)
-    codes = np.zeros(blocks.shape, np.uint8)
-    scales = np.zeros(blocks.shape[:2], np.uint8)
-    for r in range(blocks.shape[0]):
-        for b in range(blocks.shape[1]):
-            v = blocks[r, b]
-            if not np.isfinite(v).all():
-                scales[r, b] = E8M0_NAN
-                continue
-            s = scale_exponent(float(np.abs(v).max()), fmt)
-            scales[r, b] = s + E8M0_BIAS
-            codes[r, b] = q8.encode(v / np.ldexp(1.0, s), fmt)   # exact power-of-two division
+    finite = np.isfinite(blocks).all(axis=-1)
+    amax = np.where(finite, np.abs(np.where(np.isfinite(blocks), blocks, 0.0)).max(axis=-1), 0.0)
+    # scale_exponent of every block at once: floor(log2 amax) = e - 1 from frexp
+    _, e = np.frexp(amax)
+    s = np.where(amax == 0.0, -E8M0_BIAS,
+                 np.clip(e.astype(np.int64) - 1 - _EMAX[fmt], -E8M0_BIAS, E8M0_BIAS))
+    scaled = blocks / np.ldexp(1.0, s)[..., None]          # exact power-of-two division
+    codes = np.where(finite[..., None], q8.encode(np.where(finite[..., None], scaled, 0.0), fmt),
+                     0).astype(np.uint8)
+    scales = np.where(finite, s + E8M0_BIAS, E8M0_NAN).astype(np.uint8)
     return codes.reshape(x32.shape), scales.reshape(x32.shape[:-1] + (K // BLOCK,))
 
 
@@ -91,3 +91,77 @@ def mx_qdq(x, fmt: str) -> np.ndarray:
     """Quantize and dequantize (the values a block-scaled GEMM multiplies)."""
     c, s = mx_quantize(x, fmt)
     return mx_dequantize(c, s, fmt)
+
+
+# ----------------------------------------------------------------------------
+# the layer with block-scaled GEMM operands
+# ----------------------------------------------------------------------------
+def qdq_along(x, axis: int, fmt: str) -> np.ndarray:
+    """mx_qdq with the blocks of 32 along `axis` (the contraction axis of the
+    GEMM the tensor feeds)."""
+    x = np.moveaxis(np.asarray(x, dtype=np.float64), axis, -1)
+    return np.moveaxis(mx_qdq(x, fmt), -1, axis)
+
+
+def qdq_group_rows(x, group_offsets, fmt: str) -> np.ndarray:
+    """Blocks of 32 along the rows of each expert's group (the contraction of
+    the weight-gradient GEMMs), aligned at the group's first row; the last
+    block of a group is completed with zeros, never with the next group's
+    rows."""
+    x = np.asarray(x, dtype=np.float64)
+    out = np.zeros_like(x)
+    for e in range(len(group_offsets) - 1):
+        lo, hi = int(group_offsets[e]), int(group_offsets[e + 1])
+        if hi == lo:
+            continue
+        n = (hi - lo + BLOCK - 1) // BLOCK * BLOCK
+        g = np.zeros((n, x.shape[1]))
+        g[:hi - lo] = x[lo:hi]
+        out[lo:hi] = qdq_along(g, 0, fmt)[:hi - lo]
+    return out
+
+
+def forward(x, logits, wi, wo, k, score_fn, renorm, align=0, capacity=0):
+    """The layer's forward with MXFP8 GEMM operands: every GEMM multiplies the
+    block-scaled E4M3 values of its operands, blocks along the contraction
+    (Xs and wi along d_model, Act and wo along d_ff); the stored activations
+    are bf16 (Act rounded to bf16 before it is quantized), as in the
+    current-scaling oracle (oracle/moe_fp8_ref.py)."""
+    E = wi.shape[0]
+    topk_idx, topk_w = moe_ref.route_topk(logits, k, score_fn, renorm)
+    lay = moe_ref.permute_layout(topk_idx, E, align, capacity)
+    off = lay["group_offsets"]
+    R = lay["R"]
+    xs = moe_ref.permute_rows(x, lay, k)[:R]
+    h = moe_ref.gmm(qdq_along(xs, 1, q8.E4M3), qdq_along(wi, 1, q8.E4M3), off)
+    act = q8.round_bf16(moe_ref.swiglu(h))
+    y = moe_ref.gmm(qdq_along(act, 1, q8.E4M3), qdq_along(wo, 1, q8.E4M3), off)
+    out = moe_ref.combine(y, lay["flat_to_sorted"], topk_w)
+    return dict(topk_idx=topk_idx, topk_w=topk_w, layout=lay, xs=xs, h=h, act=act, y=y,
+                out=out)
+
+
+def backward(fw: dict, d_out, wi, wo, k):
+    """The backward with MXFP8 operands: dY and dH in E5M2 (blocks along
+    d_model for dY, along 2 d_ff for dH), the weights re-quantized along the
+    dgrad GEMMs' contraction (wo along d_model, wi along 2 d_ff), and the
+    weight gradients' operands quantized along the expert's rows (Act, Xs in
+    E4M3, dY, dH in E5M2)."""
+    lay = fw["layout"]
+    off = lay["group_offsets"]
+    E = wi.shape[0]
+    T = d_out.shape[0]
+    R = lay["R"]
+    dy, d_topk_w = moe_ref.combine_bwd(d_out, fw["y"], lay["flat_to_sorted"], fw["topk_w"], R)
+    dy = q8.round_bf16(dy[:R])
+    d_act = moe_ref.gmm(qdq_along(dy, 1, q8.E5M2), qdq_along(wo, 2, q8.E4M3), off,
+                        transpose_rhs=True)
+    dh = q8.round_bf16(moe_ref.swiglu_bwd(q8.round_bf16(fw["h"]), d_act))
+    d_wo = moe_ref.tgmm(qdq_group_rows(fw["act"], off, q8.E4M3),
+                        qdq_group_rows(dy, off, q8.E5M2), off, E)
+    d_xs = moe_ref.gmm(qdq_along(dh, 1, q8.E5M2), qdq_along(wi, 2, q8.E4M3), off,
+                       transpose_rhs=True)
+    d_wi = moe_ref.tgmm(qdq_group_rows(fw["xs"], off, q8.E4M3),
+                        qdq_group_rows(dh, off, q8.E5M2), off, E)
+    dx = moe_ref.dispatch_bwd(d_xs, lay["flat_to_sorted"], T, k)
+    return dict(dy=dy, d_topk_w=d_topk_w, dh=dh, d_wo=d_wo, d_xs=d_xs, d_wi=d_wi, dx=dx)

@@ -123,3 +123,66 @@ def test_scale_exponent_is_clamped():
     assert mx.scale_exponent(np.ldexp(1.0, 1020), "e4m3") == 127
     assert mx.scale_exponent(np.ldexp(1.0, -1070), "e4m3") == -127
     assert mx.scale_exponent(1.0, "e4m3") == -8 and mx.scale_exponent(1.0, "e5m2") == -15
+
+
+def _mx_layer_inputs(seed, T=160, d=128, f=128, E=5):
+    from moe_synth import bf16_bits, bits_to_f64
+    rng = np.random.default_rng(seed)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    x = bits_to_f64(bf16_bits(rng.standard_normal((T, d)).astype(np.float32)))
+    wi = bits_to_f64(bf16_bits((rng.standard_normal((E, d, 2 * f)) * 0.05).astype(np.float32)))
+    wo = bits_to_f64(bf16_bits((rng.standard_normal((E, f, d)) * 0.05).astype(np.float32)))
+    dout = bits_to_f64(bf16_bits(rng.standard_normal((T, d)).astype(np.float32)))
+    return logits, x, wi, wo, dout
+
+
+def test_without_quantization_mx_layer_is_bf16_layer(monkeypatch):
+    """Identity block quantizers and no bf16 rounding: the MXFP8 layer's forward
+    and backward reduce exactly to the bf16 oracle's (every GEMM takes the same
+    operands, the weight gradients the same rows)."""
+    from oracle import moe_ref
+    monkeypatch.setattr(q8, "round_bf16", lambda x: np.asarray(x, np.float64))
+    monkeypatch.setattr(mx, "mx_qdq", lambda x, fmt: np.asarray(x, np.float64))
+    logits, x, wi, wo, dout = _mx_layer_inputs(3)
+    for (k, sfn, ren, align, cap) in [(2, 0, 1, 0, 0), (3, 1, 0, 4, 20)]:
+        fm = mx.forward(x, logits, wi, wo, k, sfn, ren, align, cap)
+        bm = mx.backward(fm, dout, wi, wo, k)
+        fr = moe_ref.forward(x, logits, wi, wo, k, sfn, ren, align, cap)
+        br = moe_ref.backward(fr, dout, wi, wo, k)
+        np.testing.assert_array_equal(fm["out"], fr["out"])
+        for key in ("dx", "d_wi", "d_wo", "d_topk_w"):
+            np.testing.assert_array_equal(bm[key], br[key])
+
+
+def test_group_rows_blocks_stay_in_their_group():
+    """The weight gradients' blocks run along each expert's rows from its first
+    row: changing another expert's rows leaves a group's values unchanged, and a
+    group of one row is quantized alone (its scale from that row only)."""
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((70, 32)) * np.ldexp(1.0, rng.integers(-6, 6, size=(70, 1)))
+    off = np.array([0, 1, 33, 70])
+    a = mx.qdq_group_rows(x, off, q8.E4M3)
+    y = x.copy()
+    y[1:33] *= 1024.0                       # group 1 much larger
+    b = mx.qdq_group_rows(y, off, q8.E4M3)
+    assert (a[0] == b[0]).all() and (a[33:] == b[33:]).all()
+    # row 0 alone: each column is its own one-element block -> exact up to the format
+    np.testing.assert_array_equal(a[0], mx.qdq_along(np.vstack([x[:1], np.zeros((31, 32))]), 0,
+                                                     q8.E4M3)[0])
+
+
+def test_mx_layer_close_to_bf16_layer():
+    """Quantization noise only: outputs and gradients within a few percent of
+    the unquantized layer, and the noise is there."""
+    from oracle import moe_ref
+    logits, x, wi, wo, dout = _mx_layer_inputs(5)
+    fm = mx.forward(x, logits, wi, wo, 2, 0, 1)
+    bm = mx.backward(fm, dout, wi, wo, 2)
+    fr = moe_ref.forward(x, logits, wi, wo, 2, 0, 1)
+    br = moe_ref.backward(fr, dout, wi, wo, 2)
+
+    def rel(a, b):
+        return np.linalg.norm(a - b) / np.linalg.norm(b)
+    assert 1e-3 < rel(fm["out"], fr["out"]) < 0.08
+    for key in ("dx", "d_wi", "d_wo"):
+        assert rel(bm[key], br[key]) < 0.15, key
