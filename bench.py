@@ -239,7 +239,7 @@ def run_ours(args, cfg, ws, rank, local):
                              cfg.align, cfg.capacity, cfg.num_chunks, args.bias,
                              num_groups=args.num_groups, topk_group=args.topk_group,
                              aux_coeff=args.aux_coeff, fp8=args.fp8,
-                             wgrad_colwise=args.wgrad_colwise)
+                             wgrad_colwise=args.wgrad_colwise, mxfp8=args.mxfp8)
     b = layer.MoEBuffers(shape, device=dev)
     stream = torch.cuda.current_stream(dev)
     bi = bo = None
@@ -385,7 +385,8 @@ def run_ours(args, cfg, ws, rank, local):
     gemm_names = [n for n in kernels if n in fl]
     dom = max(gemm_names, key=lambda n: kernels[n]["share"])
     peak_t = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
-    if args.fp8:   # measured bf16 peak x the nominal dense fp8 / bf16 ratio (4.5 / 2.25)
+    low = args.fp8 or args.mxfp8
+    if low:   # measured bf16 peak x the nominal dense fp8 / bf16 ratio (4.5 / 2.25)
         peak_t *= 2.0
     traffic = None
     tp = os.path.join(ROOT, "profiles", "traffic.json")
@@ -393,12 +394,12 @@ def run_ours(args, cfg, ws, rank, local):
         tj = json.load(open(tp))
         ent = tj.get(cfg.name, {}).get(dom)
         if ent and ent.get("source_hash") == gemm_source_hash() and not args.bias \
-                and not args.fp8:
+                and not low:
             traffic = ent["dram_bytes_per_launch"]
     roofline = {"bound": "tensor", "kernel": dom, "achieved": kernels[dom]["tflops"],
                 "peak": peak_t, "unit": "TFLOP/s", "frac": kernels[dom]["tflops"] / peak_t,
                 "traffic": traffic, "peak_kind": "%s sustained bf16 (burst %.1f)%s"
-                % (pk_kind, pk["bf16_tflops"], " x 2 (nominal fp8 / bf16)" if args.fp8 else ""),
+                % (pk_kind, pk["bf16_tflops"], " x 2 (nominal fp8 / bf16)" if low else ""),
                 "algorithmic_per_launch": fl[dom], "algorithmic_unit": "FLOP"}
     gemm_ms = sum(kernels[n]["avg_ms"] * kernels[n]["launches_per_step"] for n in gemm_names)
     mem = {}
@@ -410,14 +411,16 @@ def run_ours(args, cfg, ws, rank, local):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "tokens_per_s": tokens_s,
         "n_gpus": ws, "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "fp8 (e4m3 forward, e5m2 gradients), fp32 accumulation" if args.fp8 else "bf16",
+        "dtype": ("mxfp8 (e4m3 forward, e5m2 gradients, e8m0 scale per 32 elements), fp32 "
+                  "accumulation" if args.mxfp8 else
+                  "fp8 (e4m3 forward, e5m2 gradients), fp32 accumulation" if args.fp8 else "bf16"),
         "data": "synthetic (seeded N(0,1) activations / N(0,0.02) weights, rank-seeded)",
         "config": {"workload": cfg.name, "T": cfg.T, "d_model": cfg.d, "d_ff": cfg.f,
                    "experts": cfg.E, "top_k": cfg.k,
                    "score": "sigmoid" if cfg.score_fn else "softmax", "renorm": cfg.renorm,
                    "align": cfg.align, "capacity": cfg.capacity, "num_chunks": cfg.num_chunks,
-                   "mlp_bias": bool(args.bias), "fp8": bool(args.fp8),
-                   "wgrad_operands": ("column-wise FP8 codes (K-major)" if args.fp8 else
+                   "mlp_bias": bool(args.bias), "fp8": bool(args.fp8), "mxfp8": bool(args.mxfp8),
+                   "wgrad_operands": ("column-wise FP8 codes (K-major)" if low else
                                       "column-wise bf16 copies (K-major)"
                                       if args.wgrad_colwise else "row-wise (MN-major)"),
                    "num_groups": args.num_groups, "topk_group": args.topk_group,
@@ -497,6 +500,8 @@ def main():
                     help="FP8 expert GEMMs with current tensor scaling")
     ap.add_argument("--bias", action="store_true",
                     help="expert FFN with biases (bi on [gate | up], bo on the output)")
+    ap.add_argument("--mxfp8", action="store_true",
+                    help="block-scaled FP8 expert GEMMs (one E8M0 scale per 32 elements)")
     ap.add_argument("--wgrad-colwise", action="store_true",
                     help="bf16 weight gradients read K-major column-wise copies written "
                          "by the SwiGLU epilogues (default: the row-wise tensors)")

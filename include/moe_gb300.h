@@ -56,7 +56,8 @@ enum { MOE_EPI_NONE = 0, MOE_EPI_SWIGLU_FWD = 1, MOE_EPI_SWIGLU_BWD = 2 };
 /* 8-bit float formats (OCP): E4M3FN (max 448, no infinities), E5M2 (max 57344) */
 enum { MOE_FP8_E4M3 = 0, MOE_FP8_E5M2 = 1 };
 /* row orders of block-scale atoms (moe_mx_quantize) */
-enum { MOE_MX_ROWS_PLAIN = 0, MOE_MX_ROWS_GROUPED = 1, MOE_MX_ROWS_SWIGLU = 2 };
+enum { MOE_MX_ROWS_PLAIN = 0, MOE_MX_ROWS_GROUPED = 1, MOE_MX_ROWS_SWIGLU = 2,
+       MOE_MX_ROWS_TILES = 3 };
 
 /* Static description of a status code. */
 const char *moe_status_string(int status);
@@ -447,14 +448,21 @@ moe_status_t moe_tgmm_fp8(const uint8_t *At, int64_t ldat, int a_fmt, const floa
  * Scales are kept in 512-byte atoms of 128 rows x 4 blocks (128 columns):
  * row r0 + 32 r1 (r0 < 32, r1 < 4), block j at byte 16 r0 + 4 r1 + j; atom
  * (ar, ac) at byte (ar * cols / 128 + ac) * 512.  The atom row of a matrix
- * row follows how the GEMMs tile it (row_map):
- *   MOE_MX_ROWS_PLAIN    r / 128 (weights, column-wise activation copies)
- *   MOE_MX_ROWS_GROUPED  permuted activations: the rows of group e start at
- *                        atom row poff_e / 128, poff_e the group starts
- *                        rounded up to 128 (moe_fp8_padded_rows layout)
- *   MOE_MX_ROWS_SWIGLU   a fused [gate | up] weight with 2F rows (F % 64 ==
- *                        0): atom row t holds gate rows [64t, 64t + 64) then
- *                        up rows [F + 64t, F + 64t + 64), the SwiGLU tiles
+ * row follows how the GEMMs tile it (row_map).  A operands come in tiles of
+ * 128 rows, B operands in tiles of 192 rows (the GEMMs' 192-column output
+ * tiles), each B tile taking two atom rows (padded row 256 t + i):
+ *   MOE_MX_ROWS_PLAIN    r / 128: the column-wise activation copy that is a
+ *                        weight gradient's A operand
+ *   MOE_MX_ROWS_GROUPED  permuted activations (A operands): the rows of group
+ *                        e start at atom row poff_e / 128, poff_e the group
+ *                        starts rounded up to 128 (moe_fp8_padded_rows layout)
+ *   MOE_MX_ROWS_TILES    B operands: E equal groups of G = rows / E rows (the
+ *                        experts' weights, or E = 1: a weight gradient's B
+ *                        copy); row n of group e in tile t = n / 192 at
+ *                        padded row 256 (e ceil(G/192) + t) + n % 192
+ *   MOE_MX_ROWS_SWIGLU   the fused [gate | up] up-projection weight, 2F rows,
+ *                        in SwiGLU tiles: tile t holds gate rows [96t, 96t +
+ *                        96) then up rows [F + 96t, F + 96t + 96)
  */
 
 /* Bytes of scale atoms for a [rows, cols] matrix (cols % 128 == 0); 0 for bad arguments. */
@@ -473,23 +481,22 @@ moe_status_t moe_mx_quantize(const uint16_t *x, int64_t ldx, int64_t rows, int c
 
 /*
  * moe_gmm_mx -- moe_gmm on block-scaled codes (fp32 accumulation of
- * (a * 2^sa) (b * 2^sb) in the tensor cores; 256 x 128 tiles):
+ * (a * 2^sa) (b * 2^sb) in the tensor cores; 256 x 192 output tiles):
  *   A    uint8 codes [rows_cap, lda >= K] with scales sfa from moe_mx_quantize
  *        (GROUPED, E groups of group_offsets)
- *   B    uint8 codes, K-major: row n of expert e at B + e*stride_b + n*ldb;
- *        the scale atom of (column tile j of 128, expert e, K block kb) at
- *        sfb + (j * sfb_nstride + e * sfb_estride + kb) * 512:
- *          B quantized as one [E*N, K] matrix (PLAIN): sfb_nstride = K/128,
- *            sfb_estride = N*K/16384;
- *          B a [N, E*K] matrix (expert e's K columns at e*K; stride_b = K):
- *            sfb_nstride = E*K/128, sfb_estride = K/128 (SWIGLU_FWD: quantized
- *            with MOE_MX_ROWS_SWIGLU, the column tile being the SwiGLU tile)
- *   K, N multiples of 128 (SWIGLU_FWD: N = 2F, F % 64 == 0); epilogues,
- *   aux, C, C2 as moe_gmm (no partial sum, no bias).
+ *   B    uint8 codes, K-major: row n of expert e at B + e*stride_b + n*ldb,
+ *        scales sfb from moe_mx_quantize of either
+ *          sfb_by_cols = 0: the [E*N, K] matrix (stride_b = N*ldb), TILES
+ *            with E groups;
+ *          sfb_by_cols = 1: the [N, E*K] matrix of the transposed weights
+ *            (expert e's K columns at e*K, stride_b = K), SWIGLU for the
+ *            SWIGLU_FWD epilogue (N = 2F), else TILES with one group
+ *   K % 128 == 0, N % 32 == 0 (SWIGLU_FWD: N = 2F, F % 32 == 0, and
+ *   sfb_by_cols = 1); epilogues, aux, C, C2 as moe_gmm (no partial sum, no bias).
  */
 moe_status_t moe_gmm_mx(const uint8_t *A, int64_t lda, const uint8_t *sfa, int a_fmt,
                         const uint8_t *B, int64_t ldb, int64_t stride_b, const uint8_t *sfb,
-                        int64_t sfb_nstride, int64_t sfb_estride, int b_fmt,
+                        int sfb_by_cols, int b_fmt,
                         const int32_t *group_offsets, int E, int64_t rows_cap, int K, int N,
                         int epilogue, const uint16_t *aux, int64_t ld_aux, void *C, int c_dtype,
                         int64_t ldc, uint16_t *C2, int64_t ldc2, int32_t *dev_status,
@@ -497,10 +504,11 @@ moe_status_t moe_gmm_mx(const uint8_t *A, int64_t lda, const uint8_t *sfa, int a
 
 /*
  * moe_tgmm_mx -- moe_tgmm on block-scaled codes of the column-wise copies
- * (moe_transpose_act layout, then moe_mx_quantize PLAIN of the [M, P] and
- * [N, P] copies, P = moe_fp8_padded_rows(rows_cap, E)): blocks of 32 along the
- * expert's rows, zeros in its padding.  M, N multiples of 128; W as moe_tgmm
- * (exact zeros for experts without rows, or W kept when accumulating).
+ * (moe_transpose_act layout, P = moe_fp8_padded_rows(rows_cap, E); blocks of
+ * 32 along the expert's rows, zeros in its padding): At [M, P] quantized
+ * PLAIN, Bt [N, P] quantized TILES with one group.  M % 128 == 0, N % 32 ==
+ * 0; W as moe_tgmm (exact zeros for experts without rows, or W kept when
+ * accumulating).
  */
 moe_status_t moe_tgmm_mx(const uint8_t *At, int64_t ldat, const uint8_t *sfa, int a_fmt,
                          const uint8_t *Bt, int64_t ldbt, const uint8_t *sfb, int b_fmt,

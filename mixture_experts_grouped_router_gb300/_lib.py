@@ -92,7 +92,7 @@ _SIGS = {
                                _I64, _P, _P]),
     "moe_mx_scale_bytes": (_SZ, [_I64, _I, _I, _I]),
     "moe_mx_quantize": (_I, [_P, _I64, _I64, _I, _I, _I, _P, _I, _P, _I64, _P, _SZ, _P]),
-    "moe_gmm_mx": (_I, [_P, _I64, _P, _I, _P, _I64, _I64, _P, _I64, _I64, _I, _P, _I, _I64, _I,
+    "moe_gmm_mx": (_I, [_P, _I64, _P, _I, _P, _I64, _I64, _P, _I, _I, _P, _I, _I64, _I,
                         _I, _I, _P, _I64, _P, _I, _I64, _P, _I64, _P, _P]),
     "moe_tgmm_mx": (_I, [_P, _I64, _P, _I, _P, _I64, _P, _I, _P, _I, _I64, _I, _I, _P, _I, _I64,
                          _I64, _I, _P, _P]),
@@ -361,32 +361,36 @@ def moe_unpermute_bwd(d_out, Y, flat_to_sorted, sorted_to_flat, group_offsets, t
 MX_ROWS_PLAIN = 0
 MX_ROWS_GROUPED = 1
 MX_ROWS_SWIGLU = 2
+MX_ROWS_TILES = 3
 
 
 def moe_mx_scale_bytes(rows: int, cols: int, row_map: int, E: int = 1) -> int:
     return int(LIB.moe_mx_scale_bytes(rows, cols, row_map, E))
 
 
-def moe_mx_quantize(x, fmt, q, sf, row_map=MX_ROWS_PLAIN, group_offsets=None, stream=None):
-    """x bf16 [rows, cols] -> q uint8 [rows, cols] codes, sf uint8 scale atoms."""
+def moe_mx_quantize(x, fmt, q, sf, row_map=MX_ROWS_PLAIN, group_offsets=None, stream=None,
+                    groups=1):
+    """x bf16 [rows, cols] -> q uint8 [rows, cols] codes, sf uint8 scale atoms;
+    GROUPED takes group_offsets, TILES the number of equal row groups."""
     rows, cols = x.shape
-    E = 0 if group_offsets is None else group_offsets.shape[0] - 1
+    E = groups if group_offsets is None else group_offsets.shape[0] - 1
     _check(LIB.moe_mx_quantize(_ptr(x), _ld(x), rows, cols, fmt, row_map, _ptr(group_offsets), E,
                                _ptr(q), _ld(q), _ptr(sf), sf.numel() * sf.element_size(),
                                _stream(stream)))
 
 
-def moe_gmm_mx(A, sfa, a_fmt, B, sfb, sfb_nstride, sfb_estride, b_fmt, group_offsets, C,
+def moe_gmm_mx(A, sfa, a_fmt, B, sfb, sfb_by_cols, b_fmt, group_offsets, C,
                epilogue=EPI_NONE, aux=None, C2=None, dev_status=None, stream=None, E=None, N=None,
                K=None, ldb=None, stride_b=None):
-    """A uint8 codes [rows_cap, K]; B uint8 codes, K-major [E, N, K] (or a strided view given
-    by ldb / stride_b with E, N, K); C bf16 or fp32."""
+    """A uint8 codes [rows_cap, K]; B uint8 codes, K-major [E, N, K] (sfb_by_cols 0; or
+    the [N, E*K] matrix given by ldb / stride_b = K with E, N, K: sfb_by_cols 1);
+    C bf16 or fp32."""
     if E is None:
         E, N, K = B.shape
         ldb, stride_b = B.stride(1), B.stride(0)
     c_dtype = DTYPE_F32 if C.dtype == torch.float32 else DTYPE_BF16
     _check(LIB.moe_gmm_mx(_ptr(A), _ld(A), _ptr(sfa), a_fmt, _ptr(B), ldb, stride_b, _ptr(sfb),
-                          sfb_nstride, sfb_estride, b_fmt, _ptr(group_offsets), E, A.shape[0], K,
+                          int(sfb_by_cols), b_fmt, _ptr(group_offsets), E, A.shape[0], K,
                           N, epilogue, _ptr(aux), _ld(aux) if aux is not None else 0, _ptr(C),
                           c_dtype, _ld(C), _ptr(C2), _ld(C2) if C2 is not None else 0,
                           _ptr(dev_status), _stream(stream)))

@@ -581,7 +581,10 @@ moe_status_t moe_tgmm_fp8(const uint8_t *At, int64_t ldat, int a_fmt, const floa
 
 size_t moe_mx_scale_bytes(int64_t rows, int cols, int row_map, int E) {
   if (rows < 0 || cols <= 0 || cols % 128 != 0 || row_map < MOE_MX_ROWS_PLAIN ||
-      row_map > MOE_MX_ROWS_SWIGLU || (row_map == MOE_MX_ROWS_GROUPED && E <= 0))
+      row_map > MOE_MX_ROWS_TILES ||
+      ((row_map == MOE_MX_ROWS_GROUPED || row_map == MOE_MX_ROWS_TILES) && E <= 0) ||
+      (row_map == MOE_MX_ROWS_TILES && rows % E != 0) ||
+      (row_map == MOE_MX_ROWS_SWIGLU && rows % 2 != 0))
     return 0;
   return (size_t)moe::mx_atom_rows(rows, row_map, E) * (size_t)(cols / 128) * 512u;
 }
@@ -594,7 +597,7 @@ moe_status_t moe_mx_quantize(const uint16_t *x, int64_t ldx, int64_t rows, int c
           (long long)rows, cols);
   REQUIRE(fmt == MOE_FP8_E4M3 || fmt == MOE_FP8_E5M2, MOE_ERR_INVALID_ARG,
           "moe_mx_quantize: bad format %d", fmt);
-  REQUIRE(row_map >= MOE_MX_ROWS_PLAIN && row_map <= MOE_MX_ROWS_SWIGLU, MOE_ERR_INVALID_ARG,
+  REQUIRE(row_map >= MOE_MX_ROWS_PLAIN && row_map <= MOE_MX_ROWS_TILES, MOE_ERR_INVALID_ARG,
           "moe_mx_quantize: bad row_map %d", row_map);
   REQUIRE(cols % 128 == 0 && ldx % 8 == 0 && ldq % 16 == 0, MOE_ERR_UNSUPPORTED,
           "moe_mx_quantize: cols must be a multiple of 128, ldx of 8, ldq of 16");
@@ -604,8 +607,11 @@ moe_status_t moe_mx_quantize(const uint16_t *x, int64_t ldx, int64_t rows, int c
     REQUIRE(group_offsets != nullptr && E > 0 && E <= 256, MOE_ERR_INVALID_ARG,
             "moe_mx_quantize: GROUPED needs group_offsets and 0 < E <= 256");
   if (row_map == MOE_MX_ROWS_SWIGLU)
-    REQUIRE(rows % 128 == 0, MOE_ERR_UNSUPPORTED,
-            "moe_mx_quantize: SWIGLU needs 2F rows with F a multiple of 64");
+    REQUIRE(rows % 64 == 0, MOE_ERR_UNSUPPORTED,
+            "moe_mx_quantize: SWIGLU needs 2F rows with F a multiple of 32");
+  if (row_map == MOE_MX_ROWS_TILES)
+    REQUIRE(E > 0 && rows % E == 0, MOE_ERR_INVALID_ARG,
+            "moe_mx_quantize: TILES needs E > 0 groups of equal rows");
   if (rows == 0) return MOE_OK;
   REQUIRE(x && q && sf, MOE_ERR_INVALID_ARG, "moe_mx_quantize: null pointer");
   REQUIRE(aligned16(x) && aligned16(q), MOE_ERR_UNSUPPORTED,
@@ -620,7 +626,7 @@ moe_status_t moe_mx_quantize(const uint16_t *x, int64_t ldx, int64_t rows, int c
 
 moe_status_t moe_gmm_mx(const uint8_t *A, int64_t lda, const uint8_t *sfa, int a_fmt,
                         const uint8_t *B, int64_t ldb, int64_t stride_b, const uint8_t *sfb,
-                        int64_t sfb_nstride, int64_t sfb_estride, int b_fmt,
+                        int sfb_by_cols, int b_fmt,
                         const int32_t *group_offsets, int E, int64_t rows_cap, int K, int N,
                         int epilogue, const uint16_t *aux, int64_t ld_aux, void *C, int c_dtype,
                         int64_t ldc, uint16_t *C2, int64_t ldc2, int32_t *dev_status,
@@ -636,14 +642,18 @@ moe_status_t moe_gmm_mx(const uint8_t *A, int64_t lda, const uint8_t *sfa, int a
           "moe_gmm_mx: bad epilogue %d", epilogue);
   REQUIRE(c_dtype == MOE_DTYPE_BF16 || c_dtype == MOE_DTYPE_F32, MOE_ERR_INVALID_ARG,
           "moe_gmm_mx: bad c_dtype");
-  REQUIRE(K % 128 == 0 && N % 128 == 0 && lda % 16 == 0 && ldb % 16 == 0 && stride_b % 16 == 0,
+  REQUIRE(K % 128 == 0 && N % 32 == 0 && lda % 16 == 0 && ldb % 16 == 0 && stride_b % 16 == 0,
           MOE_ERR_UNSUPPORTED,
-          "moe_gmm_mx: K, N must be multiples of 128 and lda, ldb, stride_b of 16");
+          "moe_gmm_mx: K must be a multiple of 128, N of 32, lda, ldb, stride_b of 16");
   REQUIRE(lda >= K && ldb >= K, MOE_ERR_INVALID_ARG, "moe_gmm_mx: lda, ldb < K");
-  REQUIRE(stride_b >= (int64_t)N * ldb || E == 1 || stride_b == K, MOE_ERR_INVALID_ARG,
-          "moe_gmm_mx: stride_b overlaps experts");
-  REQUIRE(sfb_nstride >= K / 128 && sfb_estride >= 0, MOE_ERR_INVALID_ARG,
-          "moe_gmm_mx: bad scale-factor strides of B");
+  REQUIRE(sfb_by_cols == 0 || sfb_by_cols == 1, MOE_ERR_INVALID_ARG,
+          "moe_gmm_mx: sfb_by_cols must be 0 or 1");
+  REQUIRE(sfb_by_cols ? (stride_b == K && ldb >= (int64_t)E * K)
+                      : (stride_b >= (int64_t)N * ldb || E == 1),
+          MOE_ERR_INVALID_ARG,
+          "moe_gmm_mx: B must be [E*N, K] (sfb_by_cols 0) or [N, E*K] with stride_b = K (1)");
+  REQUIRE(epilogue != MOE_EPI_SWIGLU_FWD || (sfb_by_cols && N % 64 == 0), MOE_ERR_UNSUPPORTED,
+          "moe_gmm_mx: SWIGLU_FWD needs the [2F, E*K] weight (sfb_by_cols 1), F % 32 == 0");
   int outN = N;
   if (epilogue == MOE_EPI_SWIGLU_FWD) {
     REQUIRE((C2 != nullptr || rows_cap == 0) && ldc2 >= N / 2 && ldc2 % 8 == 0,
@@ -664,7 +674,7 @@ moe_status_t moe_gmm_mx(const uint8_t *A, int64_t lda, const uint8_t *sfa, int a
   REQUIRE(aligned16(A) && aligned16(B) && aligned16(C) && aligned16(C2) && aligned16(aux) &&
               aligned16(sfa) && aligned16(sfb),
           MOE_ERR_UNSUPPORTED, "moe_gmm_mx: operands must be 16-byte aligned");
-  moe::GmmMxArgs a{A, lda, sfa, a_fmt, B, ldb, stride_b, sfb, sfb_nstride, sfb_estride, b_fmt,
+  moe::GmmMxArgs a{A, lda, sfa, a_fmt, B, ldb, stride_b, sfb, sfb_by_cols, b_fmt,
                    group_offsets, E, rows_cap, K, N, epilogue, aux, ld_aux, C, c_dtype, ldc, C2,
                    ldc2, dev_status};
   return moe::launch_gmm_mx(a, (cudaStream_t)stream);
@@ -692,8 +702,8 @@ moe_status_t moe_tgmm_mx(const uint8_t *At, int64_t ldat, const uint8_t *sfa, in
   REQUIRE(ldat >= P && ldbt >= P && ldat % 16 == 0 && ldbt % 16 == 0, MOE_ERR_INVALID_ARG,
           "moe_tgmm_mx: ldat, ldbt must be >= moe_fp8_padded_rows (%lld) and multiples of 16",
           (long long)P);
-  REQUIRE(M % 128 == 0 && N % 128 == 0 && ldw >= N && ldw % 8 == 0, MOE_ERR_UNSUPPORTED,
-          "moe_tgmm_mx: M, N must be multiples of 128, ldw >= N a multiple of 8");
+  REQUIRE(M % 128 == 0 && N % 32 == 0 && ldw >= N && ldw % 8 == 0, MOE_ERR_UNSUPPORTED,
+          "moe_tgmm_mx: M must be a multiple of 128, N of 32, ldw >= N a multiple of 8");
   REQUIRE(stride_w >= (int64_t)M * ldw || E == 1, MOE_ERR_INVALID_ARG,
           "moe_tgmm_mx: stride_w overlaps experts");
   REQUIRE(At && sfa && Bt && sfb && group_offsets && W, MOE_ERR_INVALID_ARG,

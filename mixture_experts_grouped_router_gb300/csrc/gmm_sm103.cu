@@ -53,9 +53,12 @@ namespace {
 
 constexpr int BM = 128, BK = 64, UK = 16;
 // output tile width (columns of the pair's 256 x BN tile): 256 for the bf16
-// and current-scaling FP8 GEMMs, 128 for the block-scaled ones (their scale
-// factors need tensor-memory columns beside the two accumulators)
+// and current-scaling FP8 GEMMs, 192 for the block-scaled ones: their scale
+// factors need tensor-memory columns beside the two accumulators (2 x 192 +
+// 6 stages x 12), and a SwiGLU tile's gate and up halves stay whole 32-column
+// chunks
 constexpr int kBN = 256;
+constexpr int kBNmx = 192;  // tile width of the block-scaled GEMMs
 constexpr int kStages = 8;  // ring slots of the barrier book (6 or 7 in use, see Ring)
 constexpr int kMaxEpiWarps = 4;
 constexpr int kPadRows = kF8PadRows;  // group padding of column-wise copies (128 rows)
@@ -96,19 +99,19 @@ struct Book {
 
 // Per-kernel layout.  Every GEMM runs as 2-SM MMAs whose stage holds this
 // CTA's 128-row (tgmm: 128-column) A tile and half of the B tile (BN = 256:
-// 32 KB, 6 stages; block-scaled, BN = 128: 24 KB plus 1 KB of scale
-// factors, 7 stages), and 4 epilogue warps (one per TMEM lane quarter).
+// 32 KB; block-scaled, BN = 192: 28 KB plus 1.5 KB of scale factors, padded
+// to whole KB), 6 stages, and 4 epilogue warps (one per TMEM lane quarter).
 template <int KIND, int EPI, bool F8, int BN, bool MX>
 struct Ring {
   static constexpr int epi_warps = 4;
-  static constexpr int stages = MX ? 7 : 6;
+  static constexpr int stages = 6;
   static constexpr int b_bytes = BN * BK;  // this CTA's BN / 2 columns of B, 128-byte rows
-  // block scaling: the scale factors of A's 128 rows and of the tile's BN
-  // (= 128) columns for the stage's K block, one 512-byte atom each
-  static constexpr int sf_bytes = MX ? 1024 : 0;
-  static constexpr int stage_bytes = A_BYTES + b_bytes + sf_bytes;
-  static_assert(stage_bytes % 1024 == 0, "stage alignment (128-byte swizzle atoms)");
-  static_assert(!MX || (F8 && BN == 128), "block scaling: 8-bit operands, 128-column tiles");
+  // block scaling: the scale factors of the stage's K block, A's 128 rows (one
+  // 512-byte atom) and the tile's 192 columns (two atoms)
+  static constexpr int sf_bytes = MX ? 1536 : 0;
+  static constexpr int tx_bytes = A_BYTES + b_bytes + sf_bytes;  // copied per CTA and stage
+  static constexpr int stage_bytes = (tx_bytes + 1023) / 1024 * 1024;
+  static_assert(!MX || (F8 && BN == kBNmx), "block scaling: 8-bit operands, 192-column tiles");
   static_assert(stages <= kStages, "barrier book");
   static constexpr int threads = 64 + 32 * epi_warps;  // producer, MMA, epilogue
   static constexpr int stg_offset = stages * stage_bytes;  // 1024-aligned
@@ -152,11 +155,13 @@ struct TcParams {
   const float *b_sinv;
   int a_fmt, b_fmt;
   float *amax_out;  // or null: max |value| of the bf16 output the epilogue writes
-  // block scaling: atom index of the scale factors of a tile's K block
-  //   A: (row tile) * sfa_stride + K block, the row tile being the padded tile
-  //      of the expert's rows (gmm) or the output row tile (tgmm)
-  //   B: (column tile) * sfb_nstride + expert * sfb_estride + K block
-  int64_t sfa_stride, sfb_nstride, sfb_estride;
+  // block scaling: where a tile's scale atoms sit for its K block kb
+  //   A: atom (row tile) * sfa_stride + kb, the row tile being the expert's
+  //      padded tile (gmm) or the output row tile (tgmm)
+  //   B: atom rows 2 n_idx + e * sfb_erow (and the next), atom column
+  //      e * sfb_ecol + kb (each 192-column tile owns two atom rows)
+  int64_t sfa_stride;
+  int sfb_ecol, sfb_erow;
 };
 
 struct TileInfo {
@@ -841,7 +846,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
           // both CTAs' copies complete on the leader's full barrier, which
           // expects the whole pair's stage
           const uint32_t fbl = tc::mapa_shared(tc::smem_u32(fb), 0);
-          if (leader) tc::mbar_expect_tx(fb, 2 * kStageB);
+          if (leader) tc::mbar_expect_tx(fb, 2 * Ring<KIND, EPI, F8, BN, MX>::tx_bytes);
           if (KIND == KIND_TGMM && (F8 || (AK && !B_MN))) {
             // K-major column-wise copies: this CTA's 128 rows of A^T (output
             // rows) and of B^T (its half of the 256 output columns)
@@ -891,17 +896,20 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
           if (MX) {
             // the K block's scale-factor atoms: this CTA's 128 A rows, and the
             // tile's 128 B columns (both CTAs load the same B atom)
-            int64_t ia, ib;
+            int64_t ia;
+            int bc, br;  // B's atom column and first atom row
             if (KIND == KIND_GMM) {
               ia = ((int64_t)bk.poff[ti.e] + ti.m_idx) * p.sfa_stride + kb;
-              ib = (int64_t)ti.n_idx * p.sfb_nstride + (int64_t)ti.e * p.sfb_estride + kb;
+              bc = ti.e * p.sfb_ecol + kb;
+              br = 2 * ti.n_idx + ti.e * p.sfb_erow;
             } else {
               const int kb0 = ti.k0 / BKE + kb;
               ia = (int64_t)ti.m_idx * p.sfa_stride + kb0;
-              ib = (int64_t)ti.n_idx * p.sfb_nstride + kb0;
+              bc = kb0;
+              br = 2 * ti.n_idx;
             }
             tc::tma_load_2d_2sm(sa + kSfOff, &tmSA, fbl, 0, (int)ia);
-            tc::tma_load_2d_2sm(sa + kSfOff + 512, &tmSB, fbl, 0, (int)ib);
+            tc::tma_load_3d_2sm(sa + kSfOff + 512, &tmSB, fbl, 0, bc, br);
           }
           ++issued;
           if (++s == kSt) {
@@ -984,13 +992,15 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
           constexpr uint64_t kAStep = A_MN ? (UK * 128) >> 4 : 32 >> 4;
           constexpr uint64_t kBStep = B_MN ? (UK * 128) >> 4 : 32 >> 4;
           if (MX) {
-            // the stage's scale factors -> tensor memory (4 columns each for
-            // A and B, per ring slot, after the two accumulators); the copies
-            // and the MMAs run in issue order
-            const uint32_t sft = tmem + 2 * BN + s * 8;
-            tc::tmem_cp_32x128b_x4_2sm(sft, tc::sdesc_plain(tc::smem_u32(sa + kSfOff), 0, 128));
-            tc::tmem_cp_32x128b_x4_2sm(sft + 4,
-                                       tc::sdesc_plain(tc::smem_u32(sa + kSfOff + 512), 0, 128));
+            // the stage's scale factors -> tensor memory, 12 columns per ring
+            // slot after the two accumulators (A's atom, then B's two); the
+            // copies and the MMAs run in issue order, and a slot is rewritten
+            // only after the MMAs that read it released the stage
+            const uint32_t sft = tmem + 2 * BN + s * 12;
+            const uint32_t sfs = tc::smem_u32(sa + kSfOff);
+#pragma unroll
+            for (int j = 0; j < 3; ++j)
+              tc::tmem_cp_32x128b_x4_2sm(sft + 4 * j, tc::sdesc_plain(sfs + 512 * j, 0, 128));
 #pragma unroll
             for (int kk = 0; kk < BK / UK; ++kk)
               tc::umma_mxf8_2sm(d_tmem, ad0 + kk * kAStep, bd0 + kk * kBStep, IDESC_MX[kk], sft,
@@ -1562,8 +1572,9 @@ moe_status_t launch_tgmm_f8(const TgmmF8Args &a, cudaStream_t s) {
   return launch_tc<KIND_TGMM, false, MOE_EPI_NONE, true>(ma, mb, mc, p, tiles_upper, s);
 }
 
-// Scale-factor map of a block-scaled operand: `atoms` 512-byte atoms viewed
-// as [atoms, 128] 32-bit words, one atom per TMA box.
+// Scale-factor maps of the block-scaled operands: 512-byte atoms viewed as
+// 32-bit words.  A: [atoms, 128] (one atom per box).  B: [atom rows, atom
+// columns, 128] (the two atom rows of a 192-column tile per box).
 static bool make_sf_map(CUtensorMap *m, const uint8_t *sf, int64_t atoms) {
   const uint64_t dims[2] = {128, (uint64_t)atoms};
   const uint64_t st[1] = {512};
@@ -1572,13 +1583,21 @@ static bool make_sf_map(CUtensorMap *m, const uint8_t *sf, int64_t atoms) {
                   CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-constexpr int kBNmx = 128;  // tile width of the block-scaled GEMMs
+static bool make_sf_map_b(CUtensorMap *m, const uint8_t *sf, int64_t atom_cols,
+                          int64_t atom_rows) {
+  const uint64_t dims[3] = {128, (uint64_t)atom_cols, (uint64_t)atom_rows};
+  const uint64_t st[2] = {512, (uint64_t)atom_cols * 512};
+  const uint32_t box[3] = {128, 1, 2};
+  return make_map(m, sf, 3, dims, st, box, CU_TENSOR_MAP_DATA_TYPE_UINT32,
+                  CU_TENSOR_MAP_SWIZZLE_NONE);
+}
 
 moe_status_t launch_gmm_mx(const GmmMxArgs &a, cudaStream_t s) {
   if (a.E > kMaxE) {
     set_error("moe_gmm_mx: E=%d > %d", a.E, kMaxE);
     return MOE_ERR_UNSUPPORTED;
   }
+  const bool swiglu = a.epilogue == MOE_EPI_SWIGLU_FWD;
   const int64_t stride_b = a.E > 1 ? a.stride_b : (int64_t)a.N * a.ldb;
   const int KB = a.K / 128;
   CUtensorMap ma, mb, msf[2];
@@ -1600,12 +1619,15 @@ moe_status_t launch_gmm_mx(const GmmMxArgs &a, cudaStream_t s) {
       return MOE_ERR_CUDA;
     }
   }
-  // A's atoms: the expert-padded row tiles; B's: every (column tile, expert, K block)
+  // A: the expert-padded row tiles.  B: quantized as [E N, K] (tiles of each
+  // expert's N rows, sfb_by_cols = 0) or as [N, E K] (expert e's K columns at
+  // e K; MOE_MX_ROWS_SWIGLU for the up-projection, sfb_by_cols = 1)
   const int64_t a_atoms = f8_padded_rows(a.rows_cap, a.E) / 128 * KB;
-  const int n_tiles_b = a.epilogue == MOE_EPI_SWIGLU_FWD ? a.N / kBNmx : (a.N + kBNmx - 1) / kBNmx;
-  const int64_t b_atoms = (int64_t)(n_tiles_b - 1) * a.sfb_nstride +
-                          (int64_t)(a.E - 1) * a.sfb_estride + KB;
-  if (!make_sf_map(&msf[0], a.sfa, a_atoms) || !make_sf_map(&msf[1], a.sfb, b_atoms)) {
+  const int64_t tiles_n = swiglu ? (a.N / 2 + kBNmx / 2 - 1) / (kBNmx / 2)
+                                 : (a.N + kBNmx - 1) / kBNmx;
+  const int64_t b_cols = a.sfb_by_cols ? (int64_t)a.E * KB : KB;
+  const int64_t b_rows = a.sfb_by_cols ? 2 * tiles_n : (int64_t)a.E * 2 * tiles_n;
+  if (!make_sf_map(&msf[0], a.sfa, a_atoms) || !make_sf_map_b(&msf[1], a.sfb, b_cols, b_rows)) {
     set_error("moe_gmm_mx: cannot encode the TMA descriptors of the scale factors");
     return MOE_ERR_CUDA;
   }
@@ -1614,9 +1636,8 @@ moe_status_t launch_gmm_mx(const GmmMxArgs &a, cudaStream_t s) {
   p.rows_cap = (int)a.rows_cap;
   p.K = a.K;
   p.N = a.N;
-  p.F = a.epilogue == MOE_EPI_SWIGLU_FWD ? a.N / 2 : a.N;
-  p.n_tiles = a.epilogue == MOE_EPI_SWIGLU_FWD ? (p.F + kBNmx / 2 - 1) / (kBNmx / 2)
-                                               : (a.N + kBNmx - 1) / kBNmx;
+  p.F = swiglu ? a.N / 2 : a.N;
+  p.n_tiles = (int)tiles_n;
   p.offsets = a.offsets;
   p.C = a.C;
   p.ldc = a.ldc;
@@ -1631,8 +1652,8 @@ moe_status_t launch_gmm_mx(const GmmMxArgs &a, cudaStream_t s) {
   p.a_fmt = a.a_fmt;
   p.b_fmt = a.b_fmt;
   p.sfa_stride = KB;
-  p.sfb_nstride = a.sfb_nstride;
-  p.sfb_estride = a.sfb_estride;
+  p.sfb_ecol = a.sfb_by_cols ? KB : 0;
+  p.sfb_erow = a.sfb_by_cols ? 0 : (int)(2 * tiles_n);
   CUtensorMap mc[4];
   if (!gmm_out_maps(mc, a.epilogue, a.C, a.c_dtype, a.ldc, a.C2, a.ldc2, a.aux, a.ld_aux, a.N,
                     p.F, a.rows_cap)) {
@@ -1681,10 +1702,12 @@ moe_status_t launch_tgmm_mx(const TgmmMxArgs &a, cudaStream_t s) {
       return MOE_ERR_CUDA;
     }
   }
-  // both copies were quantized as plain [rows, P] matrices: atom (row tile, K block)
+  // At [M, P] quantized PLAIN (atom per 128 rows), Bt [N, P] quantized in
+  // 192-row tiles (MOE_MX_ROWS_TILES, one group)
   const int64_t pk = P / 128;
+  const int64_t tiles_n = (a.N + kBNmx - 1) / kBNmx;
   if (!make_sf_map(&msf[0], a.sfa, (a.M + 127) / 128 * pk) ||
-      !make_sf_map(&msf[1], a.sfb, (a.N + 127) / 128 * pk)) {
+      !make_sf_map_b(&msf[1], a.sfb, pk, 2 * tiles_n)) {
     set_error("moe_tgmm_mx: cannot encode the TMA descriptors of the scale factors");
     return MOE_ERR_CUDA;
   }
@@ -1694,7 +1717,7 @@ moe_status_t launch_tgmm_mx(const TgmmMxArgs &a, cudaStream_t s) {
   p.M = a.M;
   p.N = a.N;
   p.m_tiles = (a.M + BM - 1) / BM;
-  p.n_tiles = (a.N + kBNmx - 1) / kBNmx;
+  p.n_tiles = (int)tiles_n;
   p.offsets = a.offsets;
   p.C = a.W;
   p.ldc = a.ldw;
@@ -1707,7 +1730,6 @@ moe_status_t launch_tgmm_mx(const TgmmMxArgs &a, cudaStream_t s) {
   p.a_fmt = a.a_fmt;
   p.b_fmt = a.b_fmt;
   p.sfa_stride = pk;
-  p.sfb_nstride = pk;
   CUtensorMap mc[4];
   {
     const bool f32 = a.w_dtype == MOE_DTYPE_F32;

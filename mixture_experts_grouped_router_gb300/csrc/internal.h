@@ -142,7 +142,7 @@ moe_status_t launch_tgmm_f8(const TgmmF8Args &a, cudaStream_t s);
 struct GmmMxArgs {
   const uint8_t *A; int64_t lda; const uint8_t *sfa; int a_fmt;
   const uint8_t *B; int64_t ldb; int64_t stride_b; const uint8_t *sfb;
-  int64_t sfb_nstride; int64_t sfb_estride; int b_fmt;
+  int sfb_by_cols; int b_fmt;
   const int32_t *offsets; int E; int64_t rows_cap; int K; int N;
   int epilogue;
   const uint16_t *aux; int64_t ld_aux;

@@ -15,15 +15,19 @@
 // row r = r0 + 32 r1 (r0 < 32, r1 < 4), block j < 4 at byte 16 r0 + 4 r1 + j.
 // Atom (ar, ac) covers atom row ar (128 rows) and columns [128 ac, 128 ac +
 // 128) and sits at byte (ar * cols / 128 + ac) * 512.  The atom row of a
-// matrix row depends on how the GEMM tiles it (row_map):
-//   PLAIN    r / 128 (weights, column-wise copies of activations)
+// matrix row depends on how the GEMM tiles it (row_map; the B operands are
+// tiled by 192 rows, which take two atom rows each, the second half used):
+//   PLAIN    r / 128 (A operands: weight-gradient copies of activations)
 //   GROUPED  the expert's padded tile: rows of group e start at atom row
 //            poff_e / 128 (poff_e = the group starts rounded up to 128, as in
 //            the column-wise copies), so a GEMM row tile of one expert reads
 //            one atom row
-//   SWIGLU   rows of a fused [gate | up] weight (2F rows, F % 64 == 0) in the
-//            order of the SwiGLU tiles: atom row t holds gate rows [64 t, 64 t
-//            + 64) then up rows [F + 64 t, F + 64 t + 64)
+//   TILES    E equal groups of G = rows / E rows (experts' weights, or one
+//            group): row n of group e in tile t = n / 192 at padded row
+//            256 (e ceil(G / 192) + t) + n % 192
+//   SWIGLU   a fused [gate | up] weight (2F rows) in the order of the SwiGLU
+//            tiles: tile t holds gate rows [96 t, 96 t + 96) then up rows
+//            [F + 96 t, F + 96 t + 96), at padded rows 256 t ...
 #include "common.cuh"
 #include "internal.h"
 
@@ -95,7 +99,11 @@ mx_quantize_kernel(const uint16_t *__restrict__ x, int64_t ldx, int64_t rows, in
   } else if (row_map == MOE_MX_ROWS_SWIGLU) {
     const int64_t F = rows / 2;
     const int64_t n = r < F ? r : r - F;
-    pr = (n / 64) * 128 + (r < F ? 0 : 64) + n % 64;
+    pr = (n / 96) * 256 + (r < F ? 0 : 96) + n % 96;
+  } else if (row_map == MOE_MX_ROWS_TILES) {
+    const int64_t G = rows / E;
+    const int64_t e = r / G, n = r - e * G;
+    pr = (e * ((G + 191) / 192) + n / 192) * 256 + n % 192;
   }
   const uint4 *src = reinterpret_cast<const uint4 *>(x + r * ldx + cb * 32);
   float v[32];
@@ -137,6 +145,8 @@ mx_quantize_kernel(const uint16_t *__restrict__ x, int64_t ldx, int64_t rows, in
 
 int64_t mx_atom_rows(int64_t rows, int row_map, int E) {
   if (row_map == MOE_MX_ROWS_GROUPED) return f8_padded_rows(rows, E) / 128;
+  if (row_map == MOE_MX_ROWS_SWIGLU) return 2 * ((rows / 2 + 95) / 96);
+  if (row_map == MOE_MX_ROWS_TILES) return 2 * (int64_t)E * ((rows / E + 191) / 192);
   return (rows + 127) / 128;
 }
 

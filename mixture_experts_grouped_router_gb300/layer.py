@@ -174,17 +174,19 @@ class MoEBuffers:
         u8, bf = torch.uint8, torch.bfloat16
         P = L.moe_fp8_padded_rows(R, E)
         self.mx_P = P
-        G, PL, SW = L.MX_ROWS_GROUPED, L.MX_ROWS_PLAIN, L.MX_ROWS_SWIGLU
+        G, PL, SW, TL = L.MX_ROWS_GROUPED, L.MX_ROWS_PLAIN, L.MX_ROWS_SWIGLU, L.MX_ROWS_TILES
 
-        def q(rows, cols, row_map):
+        def q(rows, cols, row_map, groups=E):
             return (torch.empty(rows, cols, dtype=u8, device=dev),
-                    torch.empty(L.moe_mx_scale_bytes(rows, cols, row_map, E), dtype=u8,
+                    torch.empty(L.moe_mx_scale_bytes(rows, cols, row_map, groups), dtype=u8,
                                 device=dev))
+        # A operands (grouped activations, the weight gradients' A copies) and
+        # B operands (weights; the weight gradients' B copies) in their tilings
         self.mx = dict(xs=q(R, d, G), act=q(R, f, G), dy=q(R, d, G), dh=q(R, 2 * f, G),
-                       xs_t=q(d, P, PL), act_t=q(f, P, PL), dy_t=q(d, P, PL),
-                       dh_t=q(2 * f, P, PL),
-                       wi_t=q(2 * f, E * d, SW), wi=q(E * d, 2 * f, PL),
-                       wo_t=q(d, E * f, PL), wo=q(E * f, d, PL))
+                       xs_t=q(d, P, PL), act_t=q(f, P, PL), dy_t=q(d, P, TL, 1),
+                       dh_t=q(2 * f, P, TL, 1),
+                       wi_t=q(2 * f, E * d, SW), wi=q(E * d, 2 * f, TL),
+                       wo_t=q(d, E * f, TL, 1), wo=q(E * f, d, TL))
         # bf16 column-wise copies (the transposes the quantizer reads)
         self.mx_bf = dict(xs_t=torch.empty(d, P, dtype=bf, device=dev),
                           act_t=torch.empty(f, P, dtype=bf, device=dev),
@@ -211,13 +213,15 @@ def _mx_rows(b, name, x, fmt, stream, mark=None):
         mark("mxquant_" + name)
 
 
-def _mx_cols(b, name, x, fmt, stream, mark):
+def _mx_cols(b, name, x, fmt, stream, mark, as_b):
     """Block-scaled codes of the column-wise copy of a permuted activation
-    (blocks along each expert's rows)."""
+    (blocks along each expert's rows); as_b: the weight gradient's B operand
+    (192-row tiles), else its A operand."""
     t = b.mx_bf[name + "_t"]
     L.moe_transpose_act(x, b.group_offsets, t, stream)
     q, sf = b.mx[name + "_t"]
-    L.moe_mx_quantize(t[:, :b.mx_P], fmt, q, sf, L.MX_ROWS_PLAIN, None, stream)
+    L.moe_mx_quantize(t[:, :b.mx_P], fmt, q, sf, L.MX_ROWS_TILES if as_b else L.MX_ROWS_PLAIN,
+                      None, stream, groups=1)
     mark("mxquant_" + name + "_t")
 
 
@@ -232,23 +236,25 @@ def _forward_mx(b, wi, wo, stream, mark):
     L.moe_transpose_act(wi.view(E * d, 2 * f), b.mx_woff_d, b.mx_bf["wi_t"], stream)
     L.moe_mx_quantize(b.mx_bf["wi_t"][:, :E * d], e4, *b.mx["wi_t"], L.MX_ROWS_SWIGLU, None,
                       stream)
-    L.moe_mx_quantize(wi.view(E * d, 2 * f), e4, *b.mx["wi"], L.MX_ROWS_PLAIN, None, stream)
+    L.moe_mx_quantize(wi.view(E * d, 2 * f), e4, *b.mx["wi"], L.MX_ROWS_TILES, None, stream,
+                      groups=E)
     L.moe_transpose_act(wo.view(E * f, d), b.mx_woff_f, b.mx_bf["wo_t"], stream)
-    L.moe_mx_quantize(b.mx_bf["wo_t"][:, :E * f], e4, *b.mx["wo_t"], L.MX_ROWS_PLAIN, None,
-                      stream)
-    L.moe_mx_quantize(wo.view(E * f, d), e4, *b.mx["wo"], L.MX_ROWS_PLAIN, None, stream)
+    L.moe_mx_quantize(b.mx_bf["wo_t"][:, :E * f], e4, *b.mx["wo_t"], L.MX_ROWS_TILES, None,
+                      stream, groups=1)
+    L.moe_mx_quantize(wo.view(E * f, d), e4, *b.mx["wo"], L.MX_ROWS_TILES, None, stream,
+                      groups=E)
     mark("mxquant_weights")
     qx, sx = b.mx["xs"]
     qw, sw = b.mx["wi_t"]
-    L.moe_gmm_mx(qx, sx, e4, qw, sw, E * d // 128, d // 128, e4, b.group_offsets, b.h,
-                 L.EPI_SWIGLU_FWD, C2=b.act, dev_status=b.dev_status, stream=stream, E=E,
-                 N=2 * f, K=d, ldb=E * d, stride_b=d)
+    L.moe_gmm_mx(qx, sx, e4, qw, sw, 1, e4, b.group_offsets, b.h, L.EPI_SWIGLU_FWD, C2=b.act,
+                 dev_status=b.dev_status, stream=stream, E=E, N=2 * f, K=d, ldb=E * d,
+                 stride_b=d)
     mark("gmm_up_swiglu")
     _mx_rows(b, "act", b.act, e4, stream, mark)
     qa, sa = b.mx["act"]
     qw, sw = b.mx["wo_t"]
-    L.moe_gmm_mx(qa, sa, e4, qw, sw, E * f // 128, f // 128, e4, b.group_offsets, b.y,
-                 dev_status=b.dev_status, stream=stream, E=E, N=d, K=f, ldb=E * f, stride_b=f)
+    L.moe_gmm_mx(qa, sa, e4, qw, sw, 1, e4, b.group_offsets, b.y, dev_status=b.dev_status,
+                 stream=stream, E=E, N=d, K=f, ldb=E * f, stride_b=f)
     mark("gmm_down")
 
 
@@ -259,23 +265,22 @@ def _backward_mx(b, stream, mark):
     _mx_rows(b, "dy", b.dy, e5, stream, mark)
     qd, sd = b.mx["dy"]
     qw, sw = b.mx["wo"]
-    L.moe_gmm_mx(qd, sd, e5, qw.view(E, f, d), sw, d // 128, f * d // 16384, e4,
-                 b.group_offsets, b.dh, L.EPI_SWIGLU_BWD, aux=b.h, dev_status=b.dev_status,
-                 stream=stream)
+    L.moe_gmm_mx(qd, sd, e5, qw.view(E, f, d), sw, 0, e4, b.group_offsets, b.dh,
+                 L.EPI_SWIGLU_BWD, aux=b.h, dev_status=b.dev_status, stream=stream)
     mark("gmm_dgrad_down_swiglu_bwd")
-    _mx_cols(b, "act", b.act, e4, stream, mark)
-    _mx_cols(b, "dy", b.dy, e5, stream, mark)
+    _mx_cols(b, "act", b.act, e4, stream, mark, as_b=False)
+    _mx_cols(b, "dy", b.dy, e5, stream, mark, as_b=True)
     L.moe_tgmm_mx(*b.mx["act_t"], e4, *b.mx["dy_t"], e5, b.group_offsets, b.rows_cap, b.dwo,
                   dev_status=b.dev_status, stream=stream)
     mark("tgmm_dwo")
     _mx_rows(b, "dh", b.dh, e5, stream, mark)
     qh, sh = b.mx["dh"]
     qw, sw = b.mx["wi"]
-    L.moe_gmm_mx(qh, sh, e5, qw.view(E, d, 2 * f), sw, 2 * f // 128, d * 2 * f // 16384, e4,
-                 b.group_offsets, b.dxs, dev_status=b.dev_status, stream=stream)
+    L.moe_gmm_mx(qh, sh, e5, qw.view(E, d, 2 * f), sw, 0, e4, b.group_offsets, b.dxs,
+                 dev_status=b.dev_status, stream=stream)
     mark("gmm_dgrad_up")
-    _mx_cols(b, "xs", b.xs, e4, stream, mark)
-    _mx_cols(b, "dh", b.dh, e5, stream, mark)
+    _mx_cols(b, "xs", b.xs, e4, stream, mark, as_b=False)
+    _mx_cols(b, "dh", b.dh, e5, stream, mark, as_b=True)
     L.moe_tgmm_mx(*b.mx["xs_t"], e4, *b.mx["dh_t"], e5, b.group_offsets, b.rows_cap, b.dwi,
                   dev_status=b.dev_status, stream=stream)
     mark("tgmm_dwi")

@@ -51,10 +51,20 @@ def _atom_rows_grouped(off):
 
 
 def _atom_rows_swiglu(rows):
+    """SwiGLU tiles of the B operand: tile t = gate rows [96t, 96t + 96) then up
+    rows, at padded rows 256 t (192-row tiles take two atom rows)."""
     F = rows // 2
     r = np.arange(rows)
     n = np.where(r < F, r, r - F)
-    return (n // 64) * 128 + np.where(r < F, 0, 64) + n % 64
+    return (n // 96) * 256 + np.where(r < F, 0, 96) + n % 96
+
+
+def _atom_rows_tiles(rows, groups):
+    """B operands in 192-row tiles per group of rows / groups rows."""
+    G = rows // groups
+    r = np.arange(rows)
+    e, n = r // G, r % G
+    return (e * ((G + 191) // 192) + n // 192) * 256 + n % 192
 
 
 def _expected_sf(scales, pos, cols, nbytes):
@@ -70,23 +80,24 @@ def _expected_sf(scales, pos, cols, nbytes):
     return out
 
 
-def _quantize_gpu(x_bits, fmt, row_map=L.MX_ROWS_PLAIN, off=None):
+def _quantize_gpu(x_bits, fmt, row_map=L.MX_ROWS_PLAIN, off=None, groups=1):
     rows, cols = x_bits.shape
     x = dev_bf16(x_bits)
     q = torch.full((rows, cols), 0xAB, dtype=torch.uint8, device="cuda")
-    E = 1 if off is None else len(off) - 1
+    E = groups if off is None else len(off) - 1
     nb = L.moe_mx_scale_bytes(rows, cols, row_map, E)
     sf = torch.full((nb,), 0xCD, dtype=torch.uint8, device="cuda")
     offd = None if off is None else torch.from_numpy(np.asarray(off, np.int32)).cuda()
-    L.moe_mx_quantize(x, fmt, q, sf, row_map=row_map, group_offsets=offd)
+    L.moe_mx_quantize(x, fmt, q, sf, row_map=row_map, group_offsets=offd, groups=groups)
     return q, sf
 
 
 @pytest.mark.parametrize("fmt", [L.FP8_E4M3, L.FP8_E5M2])
-@pytest.mark.parametrize("row_map", [L.MX_ROWS_PLAIN, L.MX_ROWS_GROUPED, L.MX_ROWS_SWIGLU])
+@pytest.mark.parametrize("row_map", [L.MX_ROWS_PLAIN, L.MX_ROWS_GROUPED, L.MX_ROWS_SWIGLU,
+                                     L.MX_ROWS_TILES])
 def test_mx_quantize(fmt, row_map):
     rng = np.random.default_rng(fmt * 3 + row_map)
-    rows, cols = (256, 384) if row_map == L.MX_ROWS_SWIGLU else (300, 256)
+    rows, cols = (448, 384) if row_map == L.MX_ROWS_SWIGLU else (300, 256)
     x_bits = _blocky(rng, rows, cols, spread=40)
     # special blocks: zeros, a subnormal-range block, saturating values, NaN, infinity
     x_bits[3, 0:32] = 0
@@ -101,9 +112,11 @@ def test_mx_quantize(fmt, row_map):
         n_rows = int(off[-1])
     elif row_map == L.MX_ROWS_SWIGLU:
         pos, n_rows = _atom_rows_swiglu(rows), rows
+    elif row_map == L.MX_ROWS_TILES:
+        pos, n_rows = _atom_rows_tiles(rows, 3), rows      # 3 groups of 100 rows
     else:
         pos, n_rows = _atom_rows_plain(rows), rows
-    q, sf = _quantize_gpu(x_bits, fmt, row_map, off)
+    q, sf = _quantize_gpu(x_bits, fmt, row_map, off, groups=3 if row_map == L.MX_ROWS_TILES else 1)
     torch.cuda.synchronize()
     codes, scales = mx.mx_quantize(moe_synth.bits_to_f64(x_bits[:n_rows]), FMT[fmt])
     got_q = q.cpu().numpy()
@@ -127,26 +140,38 @@ def _deq_rows(bits, fmt):
     return mx.mx_qdq(moe_synth.bits_to_f64(bits), FMT[fmt])
 
 
-@pytest.mark.parametrize("sz,K,N", [("mixed", 256, 256), ("one", 384, 128), ("tiny", 128, 384)])
+@pytest.mark.parametrize("sz,K,N", [("mixed", 256, 256), ("one", 384, 160), ("tiny", 128, 416),
+                                    ("mixed", 128, 192)])
 @pytest.mark.parametrize("fmts", [(L.FP8_E4M3, L.FP8_E4M3), (L.FP8_E5M2, L.FP8_E4M3)])
 @pytest.mark.parametrize("c_f32", [False, True])
-def test_gmm_mx_none(sz, K, N, fmts, c_f32):
+@pytest.mark.parametrize("by_cols", [False, True])
+def test_gmm_mx_none(sz, K, N, fmts, c_f32, by_cols):
+    """B [E, N, K] quantized as the [E*N, K] matrix (192-row tiles per expert),
+    or (by_cols) as the [N, E*K] matrix of the transposed weights (expert e's
+    K columns at e*K)."""
     rng = np.random.default_rng(K + N + fmts[0])
     off = _off(SIZES[sz])
     E, R = len(SIZES[sz]), int(off[-1])
     rows_cap = R + 29
     a_bits = _blocky(rng, rows_cap, K)
-    b_bits = _blocky(rng, E * N, K)                 # B [E, N, K] as one [E*N, K] matrix
     qa, sfa = _quantize_gpu(a_bits, fmts[0], L.MX_ROWS_GROUPED, off)
-    qb, sfb = _quantize_gpu(b_bits, fmts[1])
     C = torch.full((rows_cap, N), 7.0, dtype=torch.float32 if c_f32 else torch.bfloat16,
                    device="cuda")
     offd = torch.from_numpy(off.astype(np.int32)).cuda()
-    L.moe_gmm_mx(qa, sfa, fmts[0], qb.view(E, N, K), sfb, K // 128, N * K // 16384, fmts[1],
-                 offd, C)
+    if by_cols:
+        bt_bits = _blocky(rng, N, E * K)
+        qb, sfb = _quantize_gpu(bt_bits, fmts[1], L.MX_ROWS_TILES, groups=1)
+        L.moe_gmm_mx(qa, sfa, fmts[0], qb, sfb, 1, fmts[1], offd, C, E=E, N=N, K=K,
+                     ldb=E * K, stride_b=K)
+        bt_dq = _deq_rows(bt_bits, fmts[1])
+        b_dq = np.stack([bt_dq[:, e * K:(e + 1) * K] for e in range(E)])   # [E, N, K]
+    else:
+        b_bits = _blocky(rng, E * N, K)             # B [E, N, K] as one [E*N, K] matrix
+        qb, sfb = _quantize_gpu(b_bits, fmts[1], L.MX_ROWS_TILES, groups=E)
+        L.moe_gmm_mx(qa, sfa, fmts[0], qb.view(E, N, K), sfb, 0, fmts[1], offd, C)
+        b_dq = _deq_rows(b_bits, fmts[1]).reshape(E, N, K)
     torch.cuda.synchronize()
     a_dq = _deq_rows(a_bits[:R], fmts[0])
-    b_dq = _deq_rows(b_bits, fmts[1]).reshape(E, N, K)
     want = moe_ref.gmm(a_dq, b_dq, off, transpose_rhs=True)
     # fp32 output: only the order of the fp32 sums differs; bf16: one rounding more
     tol = dict(rel_fro=1e-4, max_rel=1e-3) if c_f32 else dict(rel_fro=4e-3, max_rel=1e-2)
@@ -154,7 +179,8 @@ def test_gmm_mx_none(sz, K, N, fmts, c_f32):
     assert (C[R:].float() == 7.0).all()
 
 
-@pytest.mark.parametrize("sz,K,F", [("mixed", 256, 128), ("one", 128, 192), ("tiny", 384, 64)])
+@pytest.mark.parametrize("sz,K,F", [("mixed", 256, 128), ("one", 128, 224), ("tiny", 384, 96),
+                                    ("mixed", 128, 320)])
 def test_gmm_mx_swiglu_fwd(sz, K, F):
     """B is the [2F, E*K] matrix of the transposed fused weight (expert e's K
     columns at e*K), scales in SwiGLU tile order."""
@@ -169,7 +195,7 @@ def test_gmm_mx_swiglu_fwd(sz, K, F):
     H = torch.empty(rows_cap, 2 * F, dtype=torch.bfloat16, device="cuda")
     Act = torch.empty(rows_cap, F, dtype=torch.bfloat16, device="cuda")
     offd = torch.from_numpy(off.astype(np.int32)).cuda()
-    L.moe_gmm_mx(qa, sfa, L.FP8_E4M3, qb, sfb, E * K // 128, K // 128, L.FP8_E4M3, offd, H,
+    L.moe_gmm_mx(qa, sfa, L.FP8_E4M3, qb, sfb, 1, L.FP8_E4M3, offd, H,
                  L.EPI_SWIGLU_FWD, C2=Act, E=E, N=2 * F, K=K, ldb=E * K, stride_b=K)
     torch.cuda.synchronize()
     a_dq = _deq_rows(a_bits[:R], L.FP8_E4M3)
@@ -180,7 +206,7 @@ def test_gmm_mx_swiglu_fwd(sz, K, F):
     assert_close("Act", Act[:R], moe_ref.swiglu(h), rel_fro=4e-3, max_rel=1e-2)
 
 
-@pytest.mark.parametrize("sz,K,F", [("mixed", 256, 128), ("one", 128, 256)])
+@pytest.mark.parametrize("sz,K,F", [("mixed", 256, 128), ("one", 128, 256), ("tiny", 256, 224)])
 def test_gmm_mx_swiglu_bwd(sz, K, F):
     rng = np.random.default_rng(K + 3 * F)
     off = _off(SIZES[sz])
@@ -190,11 +216,11 @@ def test_gmm_mx_swiglu_bwd(sz, K, F):
     b_bits = _blocky(rng, E * F, K, spread=3)        # wo [E, F, K]: dgrad reads it K-major
     h_bits = moe_synth.bf16_bits((rng.standard_normal((rows_cap, 2 * F)) * 2).astype(np.float32))
     qa, sfa = _quantize_gpu(a_bits, L.FP8_E5M2, L.MX_ROWS_GROUPED, off)
-    qb, sfb = _quantize_gpu(b_bits, L.FP8_E4M3)
+    qb, sfb = _quantize_gpu(b_bits, L.FP8_E4M3, L.MX_ROWS_TILES, groups=E)
     dH = torch.empty(rows_cap, 2 * F, dtype=torch.bfloat16, device="cuda")
     offd = torch.from_numpy(off.astype(np.int32)).cuda()
-    L.moe_gmm_mx(qa, sfa, L.FP8_E5M2, qb.view(E, F, K), sfb, K // 128, F * K // 16384,
-                 L.FP8_E4M3, offd, dH, L.EPI_SWIGLU_BWD, aux=dev_bf16(h_bits))
+    L.moe_gmm_mx(qa, sfa, L.FP8_E5M2, qb.view(E, F, K), sfb, 0, L.FP8_E4M3, offd, dH,
+                 L.EPI_SWIGLU_BWD, aux=dev_bf16(h_bits))
     torch.cuda.synchronize()
     d_act = moe_ref.gmm(_deq_rows(a_bits[:R], L.FP8_E5M2),
                         _deq_rows(b_bits, L.FP8_E4M3).reshape(E, F, K), off, transpose_rhs=True)
@@ -213,7 +239,7 @@ def _padded_colwise(bits, off):
     return out, pos
 
 
-@pytest.mark.parametrize("sz,M,N", [("mixed", 256, 128), ("one", 128, 256), ("tiny", 128, 128)])
+@pytest.mark.parametrize("sz,M,N", [("mixed", 256, 128), ("one", 128, 256), ("tiny", 128, 416)])
 @pytest.mark.parametrize("mode", ["bf16", "f32_acc"])
 def test_tgmm_mx(sz, M, N, mode):
     rng = np.random.default_rng(M + N + len(mode))
@@ -225,7 +251,7 @@ def test_tgmm_mx(sz, M, N, mode):
     At_bits, pos = _padded_colwise(a_bits, off)
     Bt_bits, _ = _padded_colwise(b_bits, off)
     qa, sfa = _quantize_gpu(At_bits, L.FP8_E4M3)
-    qb, sfb = _quantize_gpu(Bt_bits, L.FP8_E5M2)
+    qb, sfb = _quantize_gpu(Bt_bits, L.FP8_E5M2, L.MX_ROWS_TILES, groups=1)
     dt = torch.float32 if mode == "f32_acc" else torch.bfloat16
     W0 = rng.standard_normal((E, M, N)).astype(np.float32)
     W = torch.from_numpy(W0).cuda().to(dt)
@@ -243,3 +269,68 @@ def test_tgmm_mx(sz, M, N, mode):
             assert (got[e] == (W0[e] if mode == "f32_acc" else 0)).all()
         else:
             assert_close("tgmm_mx[%d]" % e, got[e], want[e], rel_fro=4e-3, max_rel=1e-2)
+
+
+# ---------------------------------------------------------------------------
+# the MXFP8 layer against the MXFP8 oracle
+# ---------------------------------------------------------------------------
+C = moe_synth.CONFIGS
+MX_LAYERS = {
+    "mixtral": moe_synth.scaled(C["mixtral"], T=1024, d=256, f=384),
+    "dsv3": moe_synth.scaled(C["dsv3"], T=512, d=384, f=256),
+    "skewed": moe_synth.scaled(C["skewed"], T=4096, d=256, f=128, capacity=64),
+    "odd": moe_synth.MoEConfig("odd", T=999, d=256, f=128, E=7, k=3, score_fn=1, renorm=0,
+                               align=16, capacity=300),
+}
+
+
+def _rel(a, b):
+    a = a.detach().float().cpu().numpy().astype(np.float64) if isinstance(a, torch.Tensor) else a
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
+
+
+def _max_rel(a, b):
+    a = a.detach().float().cpu().numpy().astype(np.float64) if isinstance(a, torch.Tensor) else a
+    return float(np.abs(a - b).max() / max(np.abs(b).max(), 1e-300))
+
+
+@pytest.mark.parametrize("name", list(MX_LAYERS))
+def test_layer_mxfp8(name):
+    """The MXFP8 layer follows the block-scaled recipe: every output within
+    1e-2 (relative Frobenius) and 5e-2 * max|ref| (elementwise) of the MXFP8
+    oracle, and at most half as far from it as the oracle is from the
+    unquantized layer; the integer layout is exact."""
+    import dataclasses
+    from gpu_helpers import layer_shape
+    from mixture_experts_grouped_router_gb300 import layer
+    cfg = MX_LAYERS[name]
+    inp = moe_synth.make_inputs(cfg, seed=4)
+    f64 = moe_synth.bits_to_f64
+    x, wi, wo, dout = (dev_bf16(inp[n]) for n in ("x", "wi", "wo", "dout"))
+    logits = torch.from_numpy(inp["logits"]).cuda()
+    b = layer.MoEBuffers(dataclasses.replace(layer_shape(cfg), mxfp8=True))
+    layer.forward(b, x, logits, wi, wo)
+    layer.backward(b, dout, wi, wo)
+    torch.cuda.synchronize()
+    assert int(b.dev_status.item()) == 0
+    xs, wis, wos, douts = (f64(inp[n]) for n in ("x", "wi", "wo", "dout"))
+    fm = mx.forward(xs, inp["logits"], wis, wos, cfg.k, cfg.score_fn, cfg.renorm, cfg.align,
+                    cfg.capacity)
+    bm = mx.backward(fm, douts, wis, wos, cfg.k)
+    fr = moe_ref.forward(xs, inp["logits"], wis, wos, cfg.k, cfg.score_fn, cfg.renorm,
+                         cfg.align, cfg.capacity)
+    br = moe_ref.backward(fr, douts, wis, wos, cfg.k)
+    assert (b.topk_idx.cpu().numpy() == fm["topk_idx"]).all()
+    assert b.group_offsets.cpu().numpy().tolist() == fm["layout"]["group_offsets"].tolist()
+    R = fm["layout"]["R"]
+    errs = {}
+    for key, got, want, ref in (
+            ("h", b.h[:R], fm["h"], fr["h"][:R]), ("act", b.act[:R], fm["act"], fr["act"][:R]),
+            ("out", b.out, fm["out"], fr["out"]), ("dy", b.dy[:R], bm["dy"], br["dy"][:R]),
+            ("dh", b.dh[:R], bm["dh"], br["dh"][:R]), ("dx", b.dx, bm["dx"], br["dx"]),
+            ("dwi", b.dwi, bm["d_wi"], br["d_wi"]), ("dwo", b.dwo, bm["d_wo"], br["d_wo"]),
+            ("d_topk_w", b.d_topk_w, bm["d_topk_w"], br["d_topk_w"])):
+        errs[key] = (_rel(got, want), _rel(want, ref), _max_rel(got, want))
+    bad = {k: v for k, v in errs.items()
+           if not (v[0] <= 1e-2 and v[0] <= 0.5 * max(v[1], 1e-3) and v[2] <= 5e-2)}
+    assert not bad, errs
