@@ -480,6 +480,32 @@ moe_status_t moe_mx_quantize(const uint16_t *x, int64_t ldx, int64_t rows, int c
                              int64_t ldq, uint8_t *sf, size_t sf_bytes, moe_stream_t stream);
 
 /*
+ * moe_mx_quantize_2x -- both block-scaled copies of a grouped bf16 matrix x
+ * [rows, ldx >= cols] from one read (the GEMM operands that the forward /
+ * dgrad and the weight gradient take from one tensor):
+ *   q   (or NULL) row-wise codes [rows, ldq >= cols], blocks of 32 along each
+ *       row; scales sfq in the atoms of q_map: GROUPED (permuted activations,
+ *       groups of group_offsets) or TILES (E equal groups: weights)
+ *   qt  (or NULL) column-wise codes [cols, ldqt >= qt_cols]: qt[c, poff_e + i]
+ *       = code of x[group_offsets[e] + i, c], blocks of 32 along each group's
+ *       rows from its first one, zeros past the group up to its next multiple
+ *       of 128 (poff_e: the group starts rounded up to 128, the layout of
+ *       moe_transpose_act); scales sfqt for the [cols, qt_cols] matrix in the
+ *       atoms of qt_map: PLAIN (a weight gradient's A), TILES with one group
+ *       (a B operand) or SWIGLU (the up-projection's transposed weight)
+ *   group_offsets int32 [E+1] on the device (TILES: 0, G, 2G, ... with G =
+ *   rows / E); qt_cols % 128 == 0 and at least the padded extent of the
+ *   groups (e.g. moe_fp8_padded_rows(rows, E); E*G for 128-aligned equal
+ *   groups): column blocks past qt_cols are not written.
+ * Codes and scales are those of moe_mx_quantize of the two matrices.
+ */
+moe_status_t moe_mx_quantize_2x(const uint16_t *x, int64_t ldx, int64_t rows, int cols, int fmt,
+                                const int32_t *group_offsets, int E, uint8_t *q, int64_t ldq,
+                                int q_map, uint8_t *sfq, size_t sfq_bytes, uint8_t *qt,
+                                int64_t ldqt, int qt_cols, int qt_map, uint8_t *sfqt,
+                                size_t sfqt_bytes, moe_stream_t stream);
+
+/*
  * moe_gmm_mx -- moe_gmm on block-scaled codes (fp32 accumulation of
  * (a * 2^sa) (b * 2^sb) in the tensor cores; 256 x 192 output tiles):
  *   A    uint8 codes [rows_cap, lda >= K] with scales sfa from moe_mx_quantize

@@ -92,6 +92,8 @@ _SIGS = {
                                _I64, _P, _P]),
     "moe_mx_scale_bytes": (_SZ, [_I64, _I, _I, _I]),
     "moe_mx_quantize": (_I, [_P, _I64, _I64, _I, _I, _I, _P, _I, _P, _I64, _P, _SZ, _P]),
+    "moe_mx_quantize_2x": (_I, [_P, _I64, _I64, _I, _I, _P, _I, _P, _I64, _I, _P, _SZ, _P, _I64,
+                                _I, _I, _P, _SZ, _P]),
     "moe_gmm_mx": (_I, [_P, _I64, _P, _I, _P, _I64, _I64, _P, _I, _I, _P, _I, _I64, _I,
                         _I, _I, _P, _I64, _P, _I, _I64, _P, _I64, _P, _P]),
     "moe_tgmm_mx": (_I, [_P, _I64, _P, _I, _P, _I64, _P, _I, _P, _I, _I64, _I, _I, _P, _I, _I64,
@@ -377,6 +379,22 @@ def moe_mx_quantize(x, fmt, q, sf, row_map=MX_ROWS_PLAIN, group_offsets=None, st
     _check(LIB.moe_mx_quantize(_ptr(x), _ld(x), rows, cols, fmt, row_map, _ptr(group_offsets), E,
                                _ptr(q), _ld(q), _ptr(sf), sf.numel() * sf.element_size(),
                                _stream(stream)))
+
+
+def moe_mx_quantize_2x(x, fmt, group_offsets, q=None, sfq=None, q_map=MX_ROWS_GROUPED,
+                       qt=None, sfqt=None, qt_map=MX_ROWS_PLAIN, qt_cols=None, stream=None):
+    """Row-wise codes q [rows, cols] and column-wise codes qt [cols, qt_cols] (padded
+    group layout) of x bf16 [rows, cols] from one read; either may be None."""
+    rows, cols = x.shape
+    E = group_offsets.shape[0] - 1
+    if qt_cols is None and qt is not None:
+        qt_cols = qt.shape[1]
+    _check(LIB.moe_mx_quantize_2x(_ptr(x), _ld(x), rows, cols, fmt, _ptr(group_offsets), E,
+                                  _ptr(q), _ld(q) if q is not None else 16, q_map, _ptr(sfq),
+                                  sfq.numel() if sfq is not None else 0, _ptr(qt),
+                                  _ld(qt) if qt is not None else 128,
+                                  int(qt_cols or 128), qt_map, _ptr(sfqt),
+                                  sfqt.numel() if sfqt is not None else 0, _stream(stream)))
 
 
 def moe_gmm_mx(A, sfa, a_fmt, B, sfb, sfb_by_cols, b_fmt, group_offsets, C,

@@ -624,6 +624,49 @@ moe_status_t moe_mx_quantize(const uint16_t *x, int64_t ldx, int64_t rows, int c
                      "moe_mx_quantize launch");
 }
 
+moe_status_t moe_mx_quantize_2x(const uint16_t *x, int64_t ldx, int64_t rows, int cols, int fmt,
+                                const int32_t *group_offsets, int E, uint8_t *q, int64_t ldq,
+                                int q_map, uint8_t *sfq, size_t sfq_bytes, uint8_t *qt,
+                                int64_t ldqt, int qt_cols, int qt_map, uint8_t *sfqt,
+                                size_t sfqt_bytes, moe_stream_t stream) {
+  set_error("");
+  REQUIRE(rows >= 0 && cols > 0 && E > 0 && E <= 256, MOE_ERR_INVALID_ARG,
+          "moe_mx_quantize_2x: rows=%lld cols=%d E=%d", (long long)rows, cols, E);
+  REQUIRE(fmt == MOE_FP8_E4M3 || fmt == MOE_FP8_E5M2, MOE_ERR_INVALID_ARG,
+          "moe_mx_quantize_2x: bad format %d", fmt);
+  REQUIRE(q_map == MOE_MX_ROWS_GROUPED || q_map == MOE_MX_ROWS_TILES, MOE_ERR_INVALID_ARG,
+          "moe_mx_quantize_2x: q_map must be GROUPED or TILES");
+  REQUIRE(qt_map == MOE_MX_ROWS_PLAIN || qt_map == MOE_MX_ROWS_TILES ||
+              qt_map == MOE_MX_ROWS_SWIGLU,
+          MOE_ERR_INVALID_ARG, "moe_mx_quantize_2x: qt_map must be PLAIN, TILES or SWIGLU");
+  REQUIRE(cols % 128 == 0 && ldx % 8 == 0 && ldq % 16 == 0 && ldqt % 16 == 0 &&
+              qt_cols % 128 == 0,
+          MOE_ERR_UNSUPPORTED,
+          "moe_mx_quantize_2x: cols and qt_cols multiples of 128, ldx of 8, ldq and ldqt of 16");
+  REQUIRE(ldx >= cols && ldq >= cols && ldqt >= qt_cols, MOE_ERR_INVALID_ARG,
+          "moe_mx_quantize_2x: leading dimension too small");
+  REQUIRE(q_map != MOE_MX_ROWS_TILES || rows % E == 0, MOE_ERR_INVALID_ARG,
+          "moe_mx_quantize_2x: TILES needs E equal groups");
+  REQUIRE(qt_map != MOE_MX_ROWS_SWIGLU || cols % 64 == 0, MOE_ERR_UNSUPPORTED,
+          "moe_mx_quantize_2x: SWIGLU needs 2F columns with F a multiple of 32");
+  REQUIRE(rows < (1ll << 31), MOE_ERR_UNSUPPORTED, "moe_mx_quantize_2x: more than 2^31 rows");
+  if (rows == 0 || (q == nullptr && qt == nullptr)) return MOE_OK;
+  REQUIRE(x && group_offsets && (q == nullptr || sfq) && (qt == nullptr || sfqt),
+          MOE_ERR_INVALID_ARG, "moe_mx_quantize_2x: null pointer");
+  REQUIRE(aligned16(x) && aligned16(q) && aligned16(qt), MOE_ERR_UNSUPPORTED,
+          "moe_mx_quantize_2x: x, q and qt must be 16-byte aligned");
+  REQUIRE(q == nullptr || sfq_bytes >= moe_mx_scale_bytes(rows, cols, q_map, E),
+          MOE_ERR_INVALID_ARG, "moe_mx_quantize_2x: sfq of %zu bytes < %zu", sfq_bytes,
+          moe_mx_scale_bytes(rows, cols, q_map, E));
+  REQUIRE(qt == nullptr || sfqt_bytes >= moe_mx_scale_bytes(cols, qt_cols, qt_map, 1),
+          MOE_ERR_INVALID_ARG, "moe_mx_quantize_2x: sfqt of %zu bytes < %zu", sfqt_bytes,
+          moe_mx_scale_bytes(cols, qt_cols, qt_map, 1));
+  return cuda_status(moe::launch_mx_quantize_2x(x, ldx, rows, cols, fmt, group_offsets, E, q, ldq,
+                                                q_map, sfq, qt, ldqt, qt_cols, qt_map, sfqt,
+                                                (cudaStream_t)stream),
+                     "moe_mx_quantize_2x launch");
+}
+
 moe_status_t moe_gmm_mx(const uint8_t *A, int64_t lda, const uint8_t *sfa, int a_fmt,
                         const uint8_t *B, int64_t ldb, int64_t stride_b, const uint8_t *sfb,
                         int sfb_by_cols, int b_fmt,

@@ -85,6 +85,10 @@ int64_t mx_atom_rows(int64_t rows, int row_map, int E);
 cudaError_t launch_mx_quantize(const uint16_t *x, int64_t ldx, int64_t rows, int cols, int fmt,
                                int row_map, const int32_t *offsets, int E, uint8_t *q,
                                int64_t ldq, uint8_t *sf, cudaStream_t s);
+cudaError_t launch_mx_quantize_2x(const uint16_t *x, int64_t ldx, int64_t rows, int cols, int fmt,
+                                  const int32_t *offsets, int E, uint8_t *q, int64_t ldq,
+                                  int q_map, uint8_t *sfq, uint8_t *qt, int64_t ldqt,
+                                  int qt_cols, int qt_map, uint8_t *sfqt, cudaStream_t s);
 
 // gmm_sm103.cu
 struct GmmArgs {

@@ -46,6 +46,30 @@ MOE_DEVINL uint32_t cvt_f8x2(float lo, float hi, int fmt) {
   return r;
 }
 
+// Padded (atom-layout) row of row r of a [rows, .] matrix under the row maps
+// that need no group offsets (PLAIN, TILES with E groups, SWIGLU).
+MOE_DEVINL int64_t mapped_row(int64_t r, int64_t rows, int row_map, int E) {
+  if (row_map == MOE_MX_ROWS_SWIGLU) {
+    const int64_t F = rows / 2;
+    const int64_t n = r < F ? r : r - F;
+    return (n / 96) * 256 + (r < F ? 0 : 96) + n % 96;
+  }
+  if (row_map == MOE_MX_ROWS_TILES) {
+    const int64_t G = rows / E;
+    const int64_t e = r / G, n = r - e * G;
+    return (e * ((G + 191) / 192) + n / 192) * 256 + n % 192;
+  }
+  return r;
+}
+
+// Byte of the scale of (padded row pr, 32-column block cb) in atoms of a
+// matrix with `cols` columns.
+MOE_DEVINL int64_t scale_byte(int64_t pr, int cb, int cols) {
+  const int64_t atom = (pr >> 7) * (cols >> 7) + (cb >> 2);
+  const int rw = (int)(pr & 127);
+  return atom * 512 + (rw & 31) * 16 + (rw >> 5) * 4 + (cb & 3);
+}
+
 // floor(log2(a)) of a finite a > 0 from its bit fields (subnormals included).
 MOE_DEVINL int floor_log2(float a) {
   const uint32_t b = __float_as_uint(a);
@@ -96,14 +120,8 @@ mx_quantize_kernel(const uint16_t *__restrict__ x, int64_t ldx, int64_t rows, in
       else hi = mid - 1;
     }
     pr = s_poff[lo] + (r - __ldg(offsets + lo));
-  } else if (row_map == MOE_MX_ROWS_SWIGLU) {
-    const int64_t F = rows / 2;
-    const int64_t n = r < F ? r : r - F;
-    pr = (n / 96) * 256 + (r < F ? 0 : 96) + n % 96;
-  } else if (row_map == MOE_MX_ROWS_TILES) {
-    const int64_t G = rows / E;
-    const int64_t e = r / G, n = r - e * G;
-    pr = (e * ((G + 191) / 192) + n / 192) * 256 + n % 192;
+  } else {
+    pr = mapped_row(r, rows, row_map, E);
   }
   const uint4 *src = reinterpret_cast<const uint4 *>(x + r * ldx + cb * 32);
   float v[32];
@@ -136,9 +154,128 @@ mx_quantize_kernel(const uint16_t *__restrict__ x, int64_t ldx, int64_t rows, in
   uint4 *dst = reinterpret_cast<uint4 *>(q + r * ldq + cb * 32);
   dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
   dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-  const int64_t atom = (pr >> 7) * (cols >> 7) + (cb >> 2);
-  const int rw = (int)(pr & 127);
-  sf[atom * 512 + (rw & 31) * 16 + (rw >> 5) * 4 + (cb & 3)] = code;
+  sf[scale_byte(pr, cb, cols)] = code;
+}
+
+// One 32-element block: its E8M0 code and the codes of its elements (8
+// little-endian words); v is overwritten.
+MOE_DEVINL uint8_t quant_block(float *v, int fmt, uint32_t *w) {
+  float amax = 0.0f;
+  bool finite = true;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float a = fabsf(v[i]);
+    finite &= a <= 3.402823466e38f;
+    amax = fmaxf(amax, a);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) w[i] = 0;
+  if (!finite) return 0xFF;
+  const int emax = fmt == MOE_FP8_E4M3 ? 8 : 15;
+  const int s = amax > 0.0f ? max(-127, min(127, floor_log2(amax) - emax)) : -127;
+  const float inv = __uint_as_float((uint32_t)(127 - s) << 23);
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    w[i] = cvt_f8x2(v[4 * i] * inv, v[4 * i + 1] * inv, fmt) |
+           (cvt_f8x2(v[4 * i + 2] * inv, v[4 * i + 3] * inv, fmt) << 16);
+  return (uint8_t)(s + 127);
+}
+
+// Both block-scaled copies of a grouped matrix from one read.  Block = a
+// tile of 64 padded rows x 128 columns (padded rows: group e's rows at poff_e
+// + i, zeros past the group; 16 KB, four 16-byte loads in flight per thread),
+// staged in shared memory; then every thread quantizes one row's 32-column
+// block (row-wise codes q, blocks along the columns) and one column's 32-row
+// block (column-wise codes qt [cols, padded rows], blocks along each group's
+// rows).
+constexpr int kMx2Rows = 64, kMx2Cols = 128;
+constexpr int kMx2Pitch = kMx2Cols * 2 + 16;  // bytes per staged row: 16 spare keep banks apart
+
+__global__ void __launch_bounds__(256)
+mx_quantize_2x_kernel(const uint16_t *__restrict__ x, int64_t ldx, int64_t rows, int cols,
+                      int fmt, const int32_t *__restrict__ offsets, int E,
+                      uint8_t *__restrict__ q, int64_t ldq, int q_map, uint8_t *__restrict__ sfq,
+                      uint8_t *__restrict__ qt, int64_t ldqt, int qt_cols, int qt_map,
+                      uint8_t *__restrict__ sfqt) {
+  __shared__ int s_poff[kMxMaxE + 1];
+  __shared__ __align__(16) uint8_t tile[kMx2Rows * kMx2Pitch];
+  const int tid = threadIdx.x;
+  if (tid < 32) {  // padded group starts (warp-shuffle scan)
+    int carry = 0;
+    for (int c0 = 0; c0 < E; c0 += 32) {
+      const int e = c0 + tid;
+      const int sz = e < E ? max(__ldg(offsets + e + 1) - __ldg(offsets + e), 0) : 0;
+      const int pad = (sz + 127) / 128 * 128;
+      int incl = pad;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (tid >= o) incl += y;
+      }
+      if (e < E) s_poff[e] = carry + incl - pad;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (tid == 0) s_poff[E] = carry;
+  }
+  __syncthreads();
+  const int64_t pr0 = (int64_t)blockIdx.y * kMx2Rows;
+  if (pr0 >= s_poff[E]) return;  // past the last group (uniform across the block)
+  int e = 0, lo = 0, hi = E - 1;  // the group of this tile (tiles never straddle groups)
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_poff[mid] <= pr0) lo = mid;
+    else hi = mid - 1;
+  }
+  e = lo;
+  const int64_t g0 = min(max((int64_t)__ldg(offsets + e), (int64_t)0), rows);
+  const int64_t gsz = min(max((int64_t)__ldg(offsets + e + 1), g0), rows) - g0;
+  const int64_t i0 = pr0 - s_poff[e];  // first row of the tile within the group
+  const int c0 = blockIdx.x * kMx2Cols;
+  // stage: 64 rows x 16 chunks of 16 bytes, four chunks per thread; rows past
+  // the group are zeros
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    const int idx = tid + 256 * h;
+    const int rr = idx >> 4, ch = idx & 15;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (i0 + rr < gsz)
+      v = ld_nc_v4(x + (g0 + i0 + rr) * ldx + c0 + ch * 8);
+    *reinterpret_cast<uint4 *>(tile + rr * kMx2Pitch + ch * 16) = v;
+  }
+  __syncthreads();
+  float v[32];
+  uint32_t w[8];
+  {
+    const int rr = tid >> 2, blk = tid & 3;
+    if (q != nullptr && i0 + rr < gsz) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        bf16x8_to_f32(*reinterpret_cast<const uint4 *>(tile + rr * kMx2Pitch + blk * 64 + i * 16),
+                      v + 8 * i);
+      const uint8_t code = quant_block(v, fmt, w);
+      const int64_t r = g0 + i0 + rr;
+      uint4 *dst = reinterpret_cast<uint4 *>(q + r * ldq + c0 + blk * 32);
+      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      const int64_t pr = q_map == MOE_MX_ROWS_GROUPED ? pr0 + rr : mapped_row(r, rows, q_map, E);
+      sfq[scale_byte(pr, (c0 >> 5) + blk, cols)] = code;
+    }
+  }
+  const int c = tid & 127, half = tid >> 7;  // column, and which 32 of the 64 rows
+  const int64_t pb = pr0 + 32 * half;        // the block's first padded row
+  if (qt != nullptr && pb + 32 <= qt_cols) {
+    const uint16_t *col = reinterpret_cast<const uint16_t *>(tile + 32 * half * kMx2Pitch) + c;
+#pragma unroll
+    for (int rr = 0; rr < 32; ++rr)
+      v[rr] = __uint_as_float((uint32_t)col[rr * (kMx2Pitch / 2)] << 16);
+    const uint8_t code = quant_block(v, fmt, w);
+    const int64_t n = c0 + c;  // row of qt
+    uint4 *dst = reinterpret_cast<uint4 *>(qt + n * ldqt + pb);
+    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    const int64_t pr = mapped_row(n, cols, qt_map, 1);
+    sfqt[scale_byte(pr, (int)(pb >> 5), qt_cols)] = code;
+  }
 }
 
 }  // namespace
@@ -148,6 +285,17 @@ int64_t mx_atom_rows(int64_t rows, int row_map, int E) {
   if (row_map == MOE_MX_ROWS_SWIGLU) return 2 * ((rows / 2 + 95) / 96);
   if (row_map == MOE_MX_ROWS_TILES) return 2 * (int64_t)E * ((rows / E + 191) / 192);
   return (rows + 127) / 128;
+}
+
+cudaError_t launch_mx_quantize_2x(const uint16_t *x, int64_t ldx, int64_t rows, int cols, int fmt,
+                                  const int32_t *offsets, int E, uint8_t *q, int64_t ldq,
+                                  int q_map, uint8_t *sfq, uint8_t *qt, int64_t ldqt,
+                                  int qt_cols, int qt_map, uint8_t *sfqt, cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  const dim3 grid(cols / kMx2Cols, (unsigned)(f8_padded_rows(rows, E) / kMx2Rows));
+  mx_quantize_2x_kernel<<<grid, 256, 0, s>>>(x, ldx, rows, cols, fmt, offsets, E, q, ldq, q_map,
+                                             sfq, qt, ldqt, qt_cols, qt_map, sfqt);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_mx_quantize(const uint16_t *x, int64_t ldx, int64_t rows, int cols, int fmt,

@@ -166,12 +166,12 @@ class MoEBuffers:
 
 
     def _alloc_mx(self, dev):
-        """Codes and scale atoms of every block-scaled operand (row-wise copies
-        for the forward / dgrad GEMMs, column-wise ones for the weight
-        gradients, the weights along both of their contractions)."""
+        """Codes and scale atoms of every block-scaled operand: each tensor's
+        row-wise copy (forward / dgrad GEMMs) and column-wise copy (weight
+        gradients; for the weights, the other contraction)."""
         s = self.s
         d, f, E, R = s.d, s.f, s.E, self.rows_cap
-        u8, bf = torch.uint8, torch.bfloat16
+        u8 = torch.uint8
         P = L.moe_fp8_padded_rows(R, E)
         self.mx_P = P
         G, PL, SW, TL = L.MX_ROWS_GROUPED, L.MX_ROWS_PLAIN, L.MX_ROWS_SWIGLU, L.MX_ROWS_TILES
@@ -187,16 +187,7 @@ class MoEBuffers:
                        dh_t=q(2 * f, P, TL, 1),
                        wi_t=q(2 * f, E * d, SW), wi=q(E * d, 2 * f, TL),
                        wo_t=q(d, E * f, TL, 1), wo=q(E * f, d, TL))
-        # bf16 column-wise copies (the transposes the quantizer reads)
-        self.mx_bf = dict(xs_t=torch.empty(d, P, dtype=bf, device=dev),
-                          act_t=torch.empty(f, P, dtype=bf, device=dev),
-                          dy_t=torch.empty(d, P, dtype=bf, device=dev),
-                          dh_t=torch.empty(2 * f, P, dtype=bf, device=dev),
-                          wi_t=torch.empty(2 * f, L.moe_fp8_padded_rows(E * d, E), dtype=bf,
-                                           device=dev),
-                          wo_t=torch.empty(d, L.moe_fp8_padded_rows(E * f, E), dtype=bf,
-                                           device=dev))
-        # the experts' weight rows as groups, for their transposes
+        # the experts' weight rows as groups
         self.mx_woff_d = torch.arange(0, E * d + 1, d, dtype=torch.int32, device=dev)
         self.mx_woff_f = torch.arange(0, E * f + 1, f, dtype=torch.int32, device=dev)
 
@@ -205,44 +196,30 @@ def _noop(_name):
     pass
 
 
-def _mx_rows(b, name, x, fmt, stream, mark=None):
-    """Block-scaled codes of a permuted activation (blocks along its row)."""
-    q, sf = b.mx[name]
-    L.moe_mx_quantize(x, fmt, q, sf, L.MX_ROWS_GROUPED, b.group_offsets, stream)
-    if mark is not None:
-        mark("mxquant_" + name)
-
-
-def _mx_cols(b, name, x, fmt, stream, mark, as_b):
-    """Block-scaled codes of the column-wise copy of a permuted activation
-    (blocks along each expert's rows); as_b: the weight gradient's B operand
-    (192-row tiles), else its A operand."""
-    t = b.mx_bf[name + "_t"]
-    L.moe_transpose_act(x, b.group_offsets, t, stream)
-    q, sf = b.mx[name + "_t"]
-    L.moe_mx_quantize(t[:, :b.mx_P], fmt, q, sf, L.MX_ROWS_TILES if as_b else L.MX_ROWS_PLAIN,
-                      None, stream, groups=1)
-    mark("mxquant_" + name + "_t")
+def _mx_both(b, name, x, fmt, qt_map, stream, mark):
+    """Row-wise and column-wise block-scaled codes of a permuted activation
+    from one read: blocks along its rows' d_model / d_ff, and along each
+    expert's rows (qt_map: PLAIN for a weight gradient's A operand, TILES for
+    its B operand)."""
+    q, sfq = b.mx[name]
+    qt, sfqt = b.mx[name + "_t"]
+    L.moe_mx_quantize_2x(x, fmt, b.group_offsets, q, sfq, L.MX_ROWS_GROUPED, qt, sfqt, qt_map,
+                         qt_cols=b.mx_P, stream=stream)
+    mark("mxquant_" + name)
 
 
 def _forward_mx(b, wi, wo, stream, mark):
     s = b.s
     d, f, E = s.d, s.f, s.E
-    e4, e5 = L.FP8_E4M3, L.FP8_E5M2
-    _mx_rows(b, "xs", b.xs, e4, stream, mark)
-    # weights along both contractions: wi^T ([2f, E d], SwiGLU tile order) for the
-    # up-projection, wi ([E d, 2f]) for its dgrad; wo^T for the down-projection, wo
-    # for its dgrad
-    L.moe_transpose_act(wi.view(E * d, 2 * f), b.mx_woff_d, b.mx_bf["wi_t"], stream)
-    L.moe_mx_quantize(b.mx_bf["wi_t"][:, :E * d], e4, *b.mx["wi_t"], L.MX_ROWS_SWIGLU, None,
-                      stream)
-    L.moe_mx_quantize(wi.view(E * d, 2 * f), e4, *b.mx["wi"], L.MX_ROWS_TILES, None, stream,
-                      groups=E)
-    L.moe_transpose_act(wo.view(E * f, d), b.mx_woff_f, b.mx_bf["wo_t"], stream)
-    L.moe_mx_quantize(b.mx_bf["wo_t"][:, :E * f], e4, *b.mx["wo_t"], L.MX_ROWS_TILES, None,
-                      stream, groups=1)
-    L.moe_mx_quantize(wo.view(E * f, d), e4, *b.mx["wo"], L.MX_ROWS_TILES, None, stream,
-                      groups=E)
+    e4 = L.FP8_E4M3
+    _mx_both(b, "xs", b.xs, e4, L.MX_ROWS_PLAIN, stream, mark)
+    # the weights along both contractions from one read each: wi as [E d, 2f]
+    # (dgrad-up B, blocks along 2f) and wi^T [2f, E d] (up-projection B, blocks
+    # along d, SwiGLU tile order); wo as [E f, d] and wo^T [d, E f]
+    L.moe_mx_quantize_2x(wi.view(E * d, 2 * f), e4, b.mx_woff_d, *b.mx["wi"], L.MX_ROWS_TILES,
+                         *b.mx["wi_t"], L.MX_ROWS_SWIGLU, qt_cols=E * d, stream=stream)
+    L.moe_mx_quantize_2x(wo.view(E * f, d), e4, b.mx_woff_f, *b.mx["wo"], L.MX_ROWS_TILES,
+                         *b.mx["wo_t"], L.MX_ROWS_TILES, qt_cols=E * f, stream=stream)
     mark("mxquant_weights")
     qx, sx = b.mx["xs"]
     qw, sw = b.mx["wi_t"]
@@ -250,7 +227,7 @@ def _forward_mx(b, wi, wo, stream, mark):
                  dev_status=b.dev_status, stream=stream, E=E, N=2 * f, K=d, ldb=E * d,
                  stride_b=d)
     mark("gmm_up_swiglu")
-    _mx_rows(b, "act", b.act, e4, stream, mark)
+    _mx_both(b, "act", b.act, e4, L.MX_ROWS_PLAIN, stream, mark)
     qa, sa = b.mx["act"]
     qw, sw = b.mx["wo_t"]
     L.moe_gmm_mx(qa, sa, e4, qw, sw, 1, e4, b.group_offsets, b.y, dev_status=b.dev_status,
@@ -262,25 +239,21 @@ def _backward_mx(b, stream, mark):
     s = b.s
     d, f, E = s.d, s.f, s.E
     e4, e5 = L.FP8_E4M3, L.FP8_E5M2
-    _mx_rows(b, "dy", b.dy, e5, stream, mark)
+    _mx_both(b, "dy", b.dy, e5, L.MX_ROWS_TILES, stream, mark)
     qd, sd = b.mx["dy"]
     qw, sw = b.mx["wo"]
     L.moe_gmm_mx(qd, sd, e5, qw.view(E, f, d), sw, 0, e4, b.group_offsets, b.dh,
                  L.EPI_SWIGLU_BWD, aux=b.h, dev_status=b.dev_status, stream=stream)
     mark("gmm_dgrad_down_swiglu_bwd")
-    _mx_cols(b, "act", b.act, e4, stream, mark, as_b=False)
-    _mx_cols(b, "dy", b.dy, e5, stream, mark, as_b=True)
     L.moe_tgmm_mx(*b.mx["act_t"], e4, *b.mx["dy_t"], e5, b.group_offsets, b.rows_cap, b.dwo,
                   dev_status=b.dev_status, stream=stream)
     mark("tgmm_dwo")
-    _mx_rows(b, "dh", b.dh, e5, stream, mark)
+    _mx_both(b, "dh", b.dh, e5, L.MX_ROWS_TILES, stream, mark)
     qh, sh = b.mx["dh"]
     qw, sw = b.mx["wi"]
     L.moe_gmm_mx(qh, sh, e5, qw.view(E, d, 2 * f), sw, 0, e4, b.group_offsets, b.dxs,
                  dev_status=b.dev_status, stream=stream)
     mark("gmm_dgrad_up")
-    _mx_cols(b, "xs", b.xs, e4, stream, mark, as_b=False)
-    _mx_cols(b, "dh", b.dh, e5, stream, mark, as_b=True)
     L.moe_tgmm_mx(*b.mx["xs_t"], e4, *b.mx["dh_t"], e5, b.group_offsets, b.rows_cap, b.dwi,
                   dev_status=b.dev_status, stream=stream)
     mark("tgmm_dwi")
@@ -489,9 +462,9 @@ def kernels_per_step(s: LayerShape) -> int:
     if s.fp8:   # amax + quantize for x, wi, wo; quantize for act (amax in the GEMM);
         fwd += 7   # amax + quantize for dy; quantize for dh
         bwd += 3
-    elif s.mxfp8:  # quantize xs, act (+2 transposes, 4 quantizes of the weights);
-        fwd += 2 + 6  # quantize dy, dh; transpose + quantize act, dy, xs, dh
-        bwd += 2 + 8
+    elif s.mxfp8:  # both copies of xs, act and of the two weights; of dy and dh
+        fwd += 4
+        bwd += 2
     elif s.wgrad_colwise:
         bwd += 2
     return fwd + bwd

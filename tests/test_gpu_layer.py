@@ -113,6 +113,7 @@ def _sampled_check(cfg, inp, b, n_tok=6, n_cols=3, seed=0):
     out_ref = np.zeros((n_tok, cfg.d))
     dx_ref = np.zeros((n_tok, cfg.d))
     dw_ref = np.zeros((n_tok, k))
+    rows_p, inter = [], {n: [] for n in ("h", "act", "y", "dy", "dh", "dxs")}
     for i, t in enumerate(toks):
         for j in range(k):
             p = f2s[t, j]
@@ -122,15 +123,26 @@ def _sampled_check(cfg, inp, b, n_tok=6, n_cols=3, seed=0):
             wi_e = f64(inp["wi"][e])
             wo_e = f64(inp["wo"][e])
             h = x[i:i + 1] @ wi_e
-            y = moe_ref.swiglu(h) @ wo_e
+            act = moe_ref.swiglu(h)
+            y = act @ wo_e
             out_ref[i] += w[t, j] * y[0]
             dw_ref[i, j] = dout[i] @ y[0]
             dy = w[t, j] * dout[i:i + 1]
             dh = moe_ref.swiglu_bwd(h, dy @ wo_e.T)
-            dx_ref[i] += (dh @ wi_e.T)[0]
+            dxs = dh @ wi_e.T
+            dx_ref[i] += dxs[0]
+            rows_p.append(p)
+            for n, v in (("h", h), ("act", act), ("y", y), ("dy", dy), ("dh", dh), ("dxs", dxs)):
+                inter[n].append(v[0])
     assert_close("out[sampled]", b.out[torch.from_numpy(toks).cuda()], out_ref)
     assert_close("dx[sampled]", b.dx[torch.from_numpy(toks).cuda()], dx_ref)
     assert_close("d_topk_w[sampled]", b.d_topk_w[torch.from_numpy(toks).cuda()], dw_ref)
+    # the saved intermediates of the sampled tokens' rows, at full size
+    if rows_p:
+        prow = torch.tensor(rows_p, dtype=torch.long, device="cuda")
+        for n, buf in (("h", b.h), ("act", b.act), ("y", b.y), ("dy", b.dy), ("dh", b.dh),
+                       ("dxs", b.dxs)):
+            assert_close("%s[sampled rows]" % n, buf[prow], np.stack(inter[n]))
 
     # weight-gradient columns / rows of sampled experts: whole-group reductions
     nonempty = np.nonzero(lay["group_sizes"] > 0)[0]

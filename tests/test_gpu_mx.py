@@ -129,6 +129,69 @@ def test_mx_quantize(fmt, row_map):
     assert (got[written] == want[written]).all()
 
 
+@pytest.mark.parametrize("case", ["acts_plain", "acts_tiles", "weights_swiglu",
+                                  "weights_tiles"])
+def test_mx_quantize_2x(case):
+    """Both copies from one read equal the oracle's block quantization of the
+    row-wise matrix and of the padded column-wise copy, codes and scales."""
+    rng = np.random.default_rng(len(case))
+    fmt = L.FP8_E5M2 if case == "acts_tiles" else L.FP8_E4M3
+    if case.startswith("acts"):
+        sizes = [0, 7, 300, 128, 129, 0, 1, 64]
+        cols = 256
+        off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+        rows = int(off[-1]) + 21
+        q_map, q_groups = L.MX_ROWS_GROUPED, len(sizes)
+        qt_map = L.MX_ROWS_PLAIN if case == "acts_plain" else L.MX_ROWS_TILES
+        qt_cols = L.moe_fp8_padded_rows(rows, len(sizes))
+    else:
+        E, G = 3, 256
+        cols = 384 if case == "weights_swiglu" else 256
+        off = np.arange(0, E * G + 1, G).astype(np.int64)
+        rows = E * G
+        q_map, q_groups = L.MX_ROWS_TILES, E
+        qt_map = L.MX_ROWS_SWIGLU if case == "weights_swiglu" else L.MX_ROWS_TILES
+        qt_cols = E * G
+    E = len(off) - 1
+    x_bits = _blocky(rng, rows, cols, spread=20)
+    x_bits[2, 0:32] = 0
+    x_bits[int(off[-1]) - 1, 5] = 0x7FC0                  # a NaN in the last group's last row
+    R = int(off[-1])
+    q = torch.full((rows, cols), 0xAB, dtype=torch.uint8, device="cuda")
+    sfq = torch.full((L.moe_mx_scale_bytes(rows, cols, q_map, q_groups),), 0xCD,
+                     dtype=torch.uint8, device="cuda")
+    qt = torch.full((cols, qt_cols), 0xAB, dtype=torch.uint8, device="cuda")
+    sfqt = torch.full((L.moe_mx_scale_bytes(cols, qt_cols, qt_map, 1),), 0xCD, dtype=torch.uint8,
+                      device="cuda")
+    L.moe_mx_quantize_2x(dev_bf16(x_bits), fmt, torch.from_numpy(off.astype(np.int32)).cuda(),
+                         q, sfq, q_map, qt, sfqt, qt_map, qt_cols=qt_cols)
+    torch.cuda.synchronize()
+    # row-wise: the oracle's blocks along each row
+    codes, scales = mx.mx_quantize(moe_synth.bits_to_f64(x_bits[:R]), FMT[fmt])
+    assert (q.cpu().numpy()[:R] == codes).all()
+    assert (q.cpu().numpy()[R:] == 0xAB).all()
+    pos = _atom_rows_grouped(off) if q_map == L.MX_ROWS_GROUPED else _atom_rows_tiles(rows, E)
+    want = _expected_sf(scales, pos[:R], cols, sfq.numel())
+    got = sfq.cpu().numpy().astype(np.int32)
+    assert (got[want >= 0] == want[want >= 0]).all()
+    # column-wise: the oracle's blocks along the padded copy's rows
+    ct_bits = np.zeros((cols, qt_cols), np.uint16)
+    ppos = _atom_rows_grouped(off)
+    ct_bits[:, ppos] = x_bits[:R].T
+    used = (int(ppos[-1]) + 128) // 128 * 128 if R else 0       # through the last group's padding
+    codes_t, scales_t = mx.mx_quantize(moe_synth.bits_to_f64(ct_bits[:, :used]), FMT[fmt])
+    got_t = qt.cpu().numpy()
+    assert (got_t[:, :used] == codes_t).all()
+    assert (got_t[:, used:] == 0xAB).all()
+    tpos = {L.MX_ROWS_PLAIN: _atom_rows_plain, L.MX_ROWS_TILES: lambda n: _atom_rows_tiles(n, 1),
+            L.MX_ROWS_SWIGLU: _atom_rows_swiglu}[qt_map](cols)
+    full_scales = np.full((cols, qt_cols // 32), -1, np.int64)
+    full_scales[:, :used // 32] = scales_t
+    want_t = _expected_sf(full_scales, tpos, qt_cols, sfqt.numel())
+    got_t_sf = sfqt.cpu().numpy().astype(np.int32)
+    assert (got_t_sf[want_t >= 0] == want_t[want_t >= 0]).all()
+
+
 SIZES = {"mixed": [0, 7, 300, 128, 129, 0, 1, 640], "one": [517], "tiny": [1, 2, 3]}
 
 
