@@ -10,8 +10,9 @@ is the Mixtral-like expert layer (T=16384, d=4096, f=14336, E=8, top-2).
 
 Prints one JSON line.  `value` is the expert-GEMM TFLOP/s of the whole job
 (18 * M_kept * d * f per step, kept rows only) with inputs resident in HBM;
-`e2e` is the same metric with the step's inputs copied from pinned host memory
-and its outputs copied back inside the timed region.  With --gpus N > 1 the
+`e2e` is the same metric through the library's host-buffer entry point
+(moe_layer_pipeline_step): each step's inputs are copied from pinned host memory
+and its results copied back inside the timed region.  With --gpus N > 1 the
 script runs under torchrun as N independent replicas (one per GPU, no data
 exchange), timing is the max over ranks and `value` sums the work of all ranks.
 --impl reference times the fp64 CPU oracle on a bounded sample of the same
@@ -197,6 +198,27 @@ def algorithmic_bytes(cfg, m_kept, R, t_kept):
     }
 
 
+def gemm_bytes_per_launch(cfg, R, op_bytes=2):
+    """Least DRAM bytes of each GEMM launch: every operand read once (op_bytes per
+    element: 2 for bf16, 1 for 8-bit codes), every output written once in bf16
+    (the weight gradients too).  R = the permuted rows the GEMMs run over."""
+    d, f, E = cfg.d, cfg.f, cfg.E
+    dc = d // max(1, cfg.num_chunks)
+    o = op_bytes
+    return {
+        "gmm_up_swiglu": o * (R * d + E * d * 2 * f) + 2 * (R * 2 * f + R * f),
+        "gmm_up_chunk": o * (R * dc + E * dc * 2 * f) + 4 * R * 2 * f * 2,
+        "gmm_up_chunk_swiglu": o * (R * dc + E * dc * 2 * f) + 4 * R * 2 * f + 2 * 3 * R * f,
+        "gmm_down": o * (R * f + E * f * d) + 2 * R * d,
+        "gmm_dgrad_down_swiglu_bwd": o * (R * d + E * f * d) + 2 * (R * 2 * f * 2),
+        "tgmm_dwo": o * (R * f + R * d) + 2 * E * f * d,
+        "gmm_dgrad_up": o * (R * 2 * f + E * d * 2 * f) + 2 * R * d,
+        "gmm_dgrad_up_chunk": o * (R * 2 * f + E * dc * 2 * f) + 2 * R * dc,
+        "tgmm_dwi": o * (R * d + R * 2 * f) + 2 * E * d * 2 * f,
+        "tgmm_dwi_chunk": o * (R * dc + R * 2 * f) + 2 * E * dc * 2 * f,
+    }
+
+
 def gemm_flops_per_launch(cfg, m_kept):
     M, d, f = m_kept, cfg.d, cfg.f
     dc = d // max(1, cfg.num_chunks)
@@ -216,7 +238,7 @@ def gemm_flops_per_launch(cfg, m_kept):
 
 def run_ours(args, cfg, ws, rank, local):
     import torch
-    from mixture_experts_grouped_router_gb300 import layer
+    from mixture_experts_grouped_router_gb300 import _lib as L, layer
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
@@ -298,64 +320,48 @@ def run_ours(args, cfg, ws, rank, local):
     if status != 0:
         raise RuntimeError("device status %d after the timed steps" % status)
 
-    # ---- end to end: every step's inputs come from pinned host memory and its
-    # results go back to pinned host memory, inside the timed region.  As in a
-    # training input pipeline, a copy stream moves step i+1's inputs in and
-    # step i's results out while step i+1 computes (double-buffered).
+    # ---- end to end, through the library's host-buffer entry point
+    # (moe_layer_pipeline_step): every step's inputs are copied in from pinned
+    # host memory and its results (out, dx, router-logit gradient) copied back
+    # to pinned host memory, inside the timed region.  The library
+    # double-buffers them on its own copy streams, so that step i+1's inputs
+    # and step i's results move while the neighbouring steps compute.
     hx = bf16(inp["x"]).pin_memory()
     hlog = torch.from_numpy(inp["logits"]).pin_memory()
     hdout = bf16(inp["dout"]).pin_memory()
     hres = [dict(out=torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory(),
                  dx=torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory(),
-                 dw=torch.empty(cfg.T, cfg.k, dtype=torch.float32).pin_memory()) for _ in range(2)]
-    din = [dict(x=torch.empty_like(x), logits=torch.empty_like(logits), dout=torch.empty_like(dout))
-           for _ in range(2)]
-    dres = [dict(out=torch.empty_like(b.out), dx=torch.empty_like(b.dx),
-                 dw=torch.empty_like(b.d_topk_w)) for _ in range(2)]
-    cs = torch.cuda.Stream(dev)
-    ev = lambda: torch.cuda.Event()
-    in_ready = [ev(), ev()]
-    step_done = [ev(), ev()]
-    d2h_done = [ev(), ev()]
+                 d_logits=torch.empty(cfg.T, cfg.E, dtype=torch.float32).pin_memory())
+            for _ in range(2)]
+    staging = torch.empty(L.moe_layer_pipeline_workspace_bytes(b.cfg), dtype=torch.uint8,
+                          device=dev)
+    pipe = L.LayerPipeline(b.cfg, b.workspace, staging)
 
-    def h2d(slot):
-        din[slot]["x"].copy_(hx, non_blocking=True)
-        din[slot]["logits"].copy_(hlog, non_blocking=True)
-        din[slot]["dout"].copy_(hdout, non_blocking=True)
-        in_ready[slot].record(cs)
+    def host_step(i):
+        r = hres[i % 2]
+        pipe.step(wi, wo, hx, hlog, hdout, r["out"], r["dx"], r["d_logits"], bi=bi, bo=bo,
+                  stream=stream)
 
+    for i in range(2):
+        host_step(i)
+    pipe.sync()
+    torch.cuda.synchronize(dev)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize(dev)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    cs.wait_stream(stream)
-    with torch.cuda.stream(cs):
-        for i in range(min(2, args.steps)):
-            h2d(i)
     for i in range(args.steps):
-        sl = i % 2
-        stream.wait_event(in_ready[sl])
-        if i >= 2:
-            stream.wait_event(d2h_done[sl])
-        layer.forward(b, din[sl]["x"], din[sl]["logits"], wi, wo, bi=bi, bo=bo)
-        layer.backward(b, din[sl]["dout"], wi, wo)
-        dres[sl]["out"].copy_(b.out)
-        dres[sl]["dx"].copy_(b.dx)
-        dres[sl]["dw"].copy_(b.d_topk_w)
-        step_done[sl].record(stream)
-        with torch.cuda.stream(cs):
-            cs.wait_event(step_done[sl])
-            for key in ("out", "dx", "dw"):
-                hres[sl][key].copy_(dres[sl][key], non_blocking=True)
-            d2h_done[sl].record(cs)
-            if i + 2 < args.steps:
-                h2d(sl)
-    stream.wait_stream(cs)
+        host_step(i)
+    pipe.join(stream)
     e1.record(stream)
     torch.cuda.synchronize(dev)
+    pipe.close()
     ms_e2e = e0.elapsed_time(e1)
+    status = int(b.dev_status.item())
+    if status != 0:
+        raise RuntimeError("device status %d after the end-to-end steps" % status)
     h2d_bytes = hx.numel() * 2 + hlog.numel() * 4 + hdout.numel() * 2
     d2h_bytes = sum(t.numel() * t.element_size() for t in hres[0].values())
 
@@ -396,11 +402,25 @@ def run_ours(args, cfg, ws, rank, local):
         if ent and ent.get("source_hash") == gemm_source_hash() and not args.bias \
                 and not low:
             traffic = ent["dram_bytes_per_launch"]
-    roofline = {"bound": "tensor", "kernel": dom, "achieved": kernels[dom]["tflops"],
-                "peak": peak_t, "unit": "TFLOP/s", "frac": kernels[dom]["tflops"] / peak_t,
-                "traffic": traffic, "peak_kind": "%s sustained bf16 (burst %.1f)%s"
-                % (pk_kind, pk["bf16_tflops"], " x 2 (nominal fp8 / bf16)" if low else ""),
-                "algorithmic_per_launch": fl[dom], "algorithmic_unit": "FLOP"}
+    # the dominant GEMM's bound: its FLOPs per least DRAM byte against the ridge
+    # point of the two peaks (few rows per expert make the weight gradient a
+    # stream of weight-sized writes: HBM-bound)
+    gb = gemm_bytes_per_launch(cfg, R, 1 if low else 2)
+    ridge = peak_t * 1e12 / (pk["hbm_gbs"] * 1e9)
+    if fl[dom] / gb[dom] >= ridge:
+        roofline = {"bound": "tensor", "kernel": dom, "achieved": kernels[dom]["tflops"],
+                    "peak": peak_t, "unit": "TFLOP/s", "frac": kernels[dom]["tflops"] / peak_t,
+                    "traffic": traffic, "peak_kind": "%s sustained bf16 (burst %.1f)%s"
+                    % (pk_kind, pk["bf16_tflops"], " x 2 (nominal fp8 / bf16)" if low else ""),
+                    "algorithmic_per_launch": fl[dom], "algorithmic_unit": "FLOP"}
+    else:
+        gbs = gb[dom] / (kernels[dom]["avg_ms"] * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "kernel": dom, "achieved": gbs, "peak": pk["hbm_gbs"],
+                    "unit": "GB/s", "frac": gbs / pk["hbm_gbs"], "traffic": traffic,
+                    "peak_kind": "%s copy bandwidth" % pk_kind,
+                    "algorithmic_per_launch": gb[dom], "algorithmic_unit": "byte",
+                    "intensity_flop_per_byte": fl[dom] / gb[dom], "ridge_flop_per_byte": ridge,
+                    "tflops": kernels[dom]["tflops"]}
     gemm_ms = sum(kernels[n]["avg_ms"] * kernels[n]["launches_per_step"] for n in gemm_names)
     mem = {}
     for n in by:
@@ -435,7 +455,8 @@ def run_ours(args, cfg, ws, rank, local):
         "e2e": {"value": flops_job * args.steps / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
                 "ms_per_step": ms_e2e / args.steps,
-                "pipeline": "copy stream overlaps step i+1 inputs / step i results with compute"},
+                "api": "moe_layer_pipeline_step (C ABI, host buffers; the library's copy "
+                       "streams overlap step i+1's inputs and step i's results with compute)"},
         "gpu_launches": layer.kernels_per_step(shape) * args.steps,
         "roofline": roofline,
         "hbm_kernels": mem,

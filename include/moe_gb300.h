@@ -658,6 +658,212 @@ moe_status_t moe_sort_chunks(const uint16_t *src, int64_t ld_src, uint16_t *dst,
                              const int64_t *len, int n_chunks, int64_t rows,
                              moe_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * The whole layer: one forward and one backward call
+ * ------------------------------------------------------------------------
+ * moe_layer_forward / moe_layer_backward run the layer's sequence of the
+ * calls above on `stream` (TE-2912, sequence diagram: route -> permute ->
+ * grouped GEMM (up, SwiGLU) -> grouped GEMM (down) -> combine, and its VJP:
+ * combine backward -> router backward -> dgrad (down, SwiGLU backward) ->
+ * tgmm (dWo) -> dgrad (up) -> tgmm (dWi) -> dispatch backward), every
+ * intermediate in one caller-owned device workspace whose layout the library
+ * plans.  The options are those of the calls above: group-limited routing,
+ * DeepSeek-V3's selection bias (MaxText PR #2579, "Onboard explicit sharding
+ * to deepseek"), the auxiliary load-balancing loss, align_size padding,
+ * capacity dropping, K-chunked up-projection (MT-4295), expert-FFN biases,
+ * FP8 current scaling or block-scaled (MXFP8) GEMMs, and weight gradients
+ * from column-wise copies.
+ */
+enum { MOE_PREC_BF16 = 0, MOE_PREC_FP8 = 1, MOE_PREC_MXFP8 = 2 };
+
+typedef struct moe_layer_config {
+  int32_t T, d, f, E, k;       /* tokens, d_model, d_ff, experts, top-k */
+  int32_t score_fn, renorm;    /* MOE_SCORE_*, renormalise the top-k weights */
+  int32_t num_groups, topk_group; /* group-limited routing (0, 0: off) */
+  int32_t align, capacity;     /* align_size padding, per-expert capacity (0: off) */
+  int32_t num_chunks;          /* K-chunks of the up-projection (<= 1: one GEMM) */
+  float aux_coeff;             /* auxiliary load-balancing loss weight (0: off) */
+  int32_t bias;                /* expert-FFN biases bi [E, 2f], bo [E, d] */
+  int32_t precision;           /* MOE_PREC_* of the expert GEMMs */
+  int32_t wgrad_colwise;       /* bf16: weight gradients from column-wise copies */
+  int32_t dw_dtype;            /* MOE_DTYPE_* of dWi / dWo */
+} moe_layer_config;
+
+/* Buffers of the workspace (moe_layer_buffer).  Shapes: R = rows_cap
+ * (moe_rows_cap), P = moe_fp8_padded_rows(R, E); bf16 unless noted. */
+enum {
+  MOE_BUF_TOPK_IDX = 0,   /* int32 [T, k] */
+  MOE_BUF_TOPK_W,         /* f32 [T, k] */
+  MOE_BUF_XS,             /* [R, d] permuted tokens */
+  MOE_BUF_GROUP_SIZES,    /* int32 [E] */
+  MOE_BUF_KEPT_COUNTS,    /* int32 [E] */
+  MOE_BUF_GROUP_OFFSETS,  /* int32 [E + 1] */
+  MOE_BUF_S2F,            /* int32 [R] sorted_to_flat */
+  MOE_BUF_F2S,            /* int32 [T k] flat_to_sorted */
+  MOE_BUF_PERMUTE_WS,     /* moe_permute_workspace_bytes(T, E) */
+  MOE_BUF_H,              /* [R, 2f] up-projection [gate | up] */
+  MOE_BUF_ACT,            /* [R, f] SwiGLU activation */
+  MOE_BUF_Y,              /* [R, d] expert outputs */
+  MOE_BUF_OUT,            /* [T, d] layer output */
+  MOE_BUF_PARTIAL,        /* f32 [R, 2f] K-chunk partial sum (num_chunks > 1) */
+  MOE_BUF_DY,             /* [R, d] */
+  MOE_BUF_D_TOPK_W,       /* f32 [T, k] */
+  MOE_BUF_D_LOGITS,       /* f32 [T, E] router-logit gradient */
+  MOE_BUF_DH,             /* [R, 2f] */
+  MOE_BUF_DXS,            /* [R, d] */
+  MOE_BUF_DX,             /* [T, d] input gradient */
+  MOE_BUF_DWI,            /* dw_dtype [E, d, 2f] */
+  MOE_BUF_DWO,            /* dw_dtype [E, f, d] */
+  MOE_BUF_DBI,            /* f32 [E, 2f] (bias) */
+  MOE_BUF_DBO,            /* f32 [E, d] (bias) */
+  MOE_BUF_DEV_STATUS,     /* int32 [1] device status word */
+  MOE_BUF_XS_T,           /* [d, P] column-wise copies (wgrad_colwise) */
+  MOE_BUF_ACT_T,          /* [f, P] */
+  MOE_BUF_DY_T,           /* [d, P] */
+  MOE_BUF_DH_T,           /* [2f, P] */
+  MOE_BUF_F8_XS_Q,        /* uint8 [R, d]   FP8: row-wise codes ... */
+  MOE_BUF_F8_XS_QT,       /* uint8 [d, P]   ... and column-wise codes */
+  MOE_BUF_F8_ACT_Q,       /* uint8 [R, f] */
+  MOE_BUF_F8_ACT_QT,      /* uint8 [f, P] */
+  MOE_BUF_F8_DY_Q,        /* uint8 [R, d] */
+  MOE_BUF_F8_DY_QT,       /* uint8 [d, P] */
+  MOE_BUF_F8_DH_Q,        /* uint8 [R, 2f] */
+  MOE_BUF_F8_DH_QT,       /* uint8 [2f, P] */
+  MOE_BUF_F8_WI_Q,        /* uint8 [E, d, 2f] */
+  MOE_BUF_F8_WI_QT,       /* uint8 [E, 2f, d] */
+  MOE_BUF_F8_WO_Q,        /* uint8 [E, f, d] */
+  MOE_BUF_F8_WO_QT,       /* uint8 [E, d, f] */
+  MOE_BUF_F8_AMAX,        /* f32 [4 + 2E]: Xs, Act, dY, dH, wi (E), wo (E) */
+  MOE_BUF_F8_SINV,        /* f32 [4 + 2E]: the matching 1 / scale */
+  /* MXFP8: codes (uint8) and scale atoms of each block-scaled operand; the
+   * atom bytes are moe_mx_scale_bytes(rows, cols, map, groups) */
+  MOE_BUF_MX_XS_Q,        /* [R, d], GROUPED */
+  MOE_BUF_MX_XS_SF,
+  MOE_BUF_MX_ACT_Q,       /* [R, f], GROUPED */
+  MOE_BUF_MX_ACT_SF,
+  MOE_BUF_MX_DY_Q,        /* [R, d], GROUPED */
+  MOE_BUF_MX_DY_SF,
+  MOE_BUF_MX_DH_Q,        /* [R, 2f], GROUPED */
+  MOE_BUF_MX_DH_SF,
+  MOE_BUF_MX_XS_T_Q,      /* [d, P], PLAIN, E groups */
+  MOE_BUF_MX_XS_T_SF,
+  MOE_BUF_MX_ACT_T_Q,     /* [f, P], PLAIN, E groups */
+  MOE_BUF_MX_ACT_T_SF,
+  MOE_BUF_MX_DY_T_Q,      /* [d, P], TILES, 1 group */
+  MOE_BUF_MX_DY_T_SF,
+  MOE_BUF_MX_DH_T_Q,      /* [2f, P], TILES, 1 group */
+  MOE_BUF_MX_DH_T_SF,
+  MOE_BUF_MX_WI_T_Q,      /* [2f, E d], SWIGLU, E groups */
+  MOE_BUF_MX_WI_T_SF,
+  MOE_BUF_MX_WI_Q,        /* [E d, 2f], TILES, E groups */
+  MOE_BUF_MX_WI_SF,
+  MOE_BUF_MX_WO_T_Q,      /* [d, E f], TILES, 1 group */
+  MOE_BUF_MX_WO_T_SF,
+  MOE_BUF_MX_WO_Q,        /* [E f, d], TILES, E groups */
+  MOE_BUF_MX_WO_SF,
+  MOE_BUF_MX_WOFF_D,      /* int32 [E + 1]: e * d (the weights' rows as groups) */
+  MOE_BUF_MX_WOFF_F,      /* int32 [E + 1]: e * f */
+  MOE_BUF_AUX_COUNTS,     /* int32 [E] (aux_coeff > 0) */
+  MOE_BUF_AUX_PROBS,      /* f32 [E] */
+  MOE_BUF_AUX_LOSS,       /* f32 [1] */
+  MOE_BUF_AUX_WS,         /* moe_aux_loss_workspace_bytes(T, E) */
+  MOE_BUF_COUNT
+};
+
+/* Called after each enqueued call with the call's name (e.g. "permute",
+ * "gmm_up_swiglu", "tgmm_dwi"), on the calling thread; a profiler records an
+ * event on the stream there.  May be NULL. */
+typedef void (*moe_mark_fn)(void *ctx, const char *name);
+
+/*
+ * moe_layer_workspace_bytes -- bytes of the layer's device workspace for `cfg`
+ * (0 and the reason in moe_last_error() for an invalid configuration).
+ * moe_layer_buffer -- where buffer `id` (MOE_BUF_*) lives in it: byte offset
+ * (a multiple of 256) and size; size 0 for a buffer the configuration does
+ * not use.  Both are host computations.
+ */
+size_t moe_layer_workspace_bytes(const moe_layer_config *cfg);
+moe_status_t moe_layer_buffer(const moe_layer_config *cfg, int id, size_t *offset,
+                              size_t *bytes);
+
+/*
+ * moe_layer_init -- once per workspace, before the first forward: zeroes the
+ * device status word and writes the constant tables (MXFP8 weight-row
+ * offsets).  workspace: 256-byte aligned, >= moe_layer_workspace_bytes(cfg).
+ */
+moe_status_t moe_layer_init(const moe_layer_config *cfg, void *workspace,
+                            size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * moe_layer_forward -- x bf16 [T, d], logits f32 [T, E], wi bf16 [E, d, 2f]
+ * ([wi_0 | wi_1] along the last axis), wo bf16 [E, f, d], all contiguous;
+ * bi bf16 [E, 2f] and bo bf16 [E, d] exactly when cfg->bias; expert_bias f32
+ * [E] or NULL (selection bias: experts ranked by logit + bias, weights from
+ * the unbiased logits).  The output is MOE_BUF_OUT of the workspace (and, with
+ * aux_coeff, the loss in MOE_BUF_AUX_LOSS).  The backward reads `logits`
+ * again (pass the same, unchanged array) and the tensors the forward saved in
+ * the workspace; x is not read after the forward.
+ */
+moe_status_t moe_layer_forward(const moe_layer_config *cfg, void *workspace,
+                               size_t workspace_bytes, const uint16_t *x, const float *logits,
+                               const uint16_t *wi, const uint16_t *wo, const uint16_t *bi,
+                               const uint16_t *bo, const float *expert_bias, moe_mark_fn mark,
+                               void *mark_ctx, moe_stream_t stream);
+
+/*
+ * moe_layer_backward -- dout bf16 [T, d] (contiguous), logits the forward's;
+ * writes MOE_BUF_DX, MOE_BUF_DWI, MOE_BUF_DWO, MOE_BUF_D_LOGITS (the router
+ * gradient, with the auxiliary loss's part when aux_coeff > 0),
+ * MOE_BUF_D_TOPK_W and, with biases, MOE_BUF_DBI / MOE_BUF_DBO.
+ */
+moe_status_t moe_layer_backward(const moe_layer_config *cfg, void *workspace,
+                                size_t workspace_bytes, const uint16_t *dout,
+                                const float *logits, const uint16_t *wi, const uint16_t *wo,
+                                moe_mark_fn mark, void *mark_ctx, moe_stream_t stream);
+
+/*
+ * The layer from HOST buffers: a training step's inputs (x, logits, dout) are
+ * copied in from host memory and its results (out, dx, d_logits) copied back,
+ * double-buffered so that step i + 1's input copies and step i's result
+ * copies overlap the compute of the steps next to them.  The weights, the
+ * weight gradients and every intermediate stay on the device (the layer's
+ * workspace).
+ *
+ * moe_layer_pipeline_workspace_bytes -- device bytes of the staging slots
+ *   (two of each: x, logits, dout, out, dx, d_logits).
+ * moe_layer_pipeline_create -- a pipeline over one layer workspace (set up
+ *   by moe_layer_init) and one staging workspace (both caller-owned device
+ *   memory; the pipeline keeps the pointers until destroyed).  Unlike the calls above it holds state:
+ *   two copy streams and its events on the current device (no device memory).
+ * moe_layer_pipeline_step -- enqueue one step: host -> device copies of h_x
+ *   bf16 [T, d], h_logits f32 [T, E], h_dout bf16 [T, d] on the input copy
+ *   stream; forward + backward on `stream` once they have landed; device ->
+ *   host copies into h_out bf16 [T, d], h_dx bf16 [T, d], h_d_logits f32
+ *   [T, E] on the output copy stream once the step has finished.  Returns
+ *   without waiting.  Host buffers should be page-locked (cudaHostAlloc /
+ *   pinned) for the copies to overlap; the caller keeps them unchanged (inputs)
+ *   and unread (results) until moe_layer_pipeline_join's stream has passed or
+ *   moe_layer_pipeline_sync returned.  dWi / dWo are the workspace's and are
+ *   overwritten by every step.
+ * moe_layer_pipeline_join -- make `stream` wait for every copy enqueued so far.
+ * moe_layer_pipeline_sync -- block the host until every copy has completed.
+ * moe_layer_pipeline_destroy -- synchronise and release the streams / events.
+ */
+typedef struct moe_layer_pipeline moe_layer_pipeline;
+size_t moe_layer_pipeline_workspace_bytes(const moe_layer_config *cfg);
+moe_status_t moe_layer_pipeline_create(const moe_layer_config *cfg, void *workspace,
+                                       size_t workspace_bytes, void *staging,
+                                       size_t staging_bytes, moe_layer_pipeline **out);
+moe_status_t moe_layer_pipeline_step(moe_layer_pipeline *pipe, const uint16_t *wi,
+                                     const uint16_t *wo, const uint16_t *bi, const uint16_t *bo,
+                                     const float *expert_bias, const uint16_t *h_x,
+                                     const float *h_logits, const uint16_t *h_dout,
+                                     uint16_t *h_out, uint16_t *h_dx, float *h_d_logits,
+                                     moe_stream_t stream);
+moe_status_t moe_layer_pipeline_join(moe_layer_pipeline *pipe, moe_stream_t stream);
+moe_status_t moe_layer_pipeline_sync(moe_layer_pipeline *pipe);
+void moe_layer_pipeline_destroy(moe_layer_pipeline *pipe);
+
 #ifdef __cplusplus
 }
 #endif

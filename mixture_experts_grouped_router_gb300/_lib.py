@@ -102,6 +102,17 @@ _SIGS = {
     "moe_ep_a2a_params": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_ep_local_layout": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
     "moe_sort_chunks": (_I, [_P, _I64, _P, _I64, _I, _P, _P, _P, _I, _I64, _P]),
+    "moe_layer_workspace_bytes": (_SZ, [_P]),
+    "moe_layer_buffer": (_I, [_P, _I, _P, _P]),
+    "moe_layer_init": (_I, [_P, _P, _SZ, _P]),
+    "moe_layer_forward": (_I, [_P, _P, _SZ, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_layer_backward": (_I, [_P, _P, _SZ, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_layer_pipeline_workspace_bytes": (_SZ, [_P]),
+    "moe_layer_pipeline_create": (_I, [_P, _P, _SZ, _P, _SZ, _P]),
+    "moe_layer_pipeline_step": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_layer_pipeline_join": (_I, [_P, _P]),
+    "moe_layer_pipeline_sync": (_I, [_P]),
+    "moe_layer_pipeline_destroy": (None, [_P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(LIB, _name)
@@ -478,3 +489,125 @@ def moe_sort_chunks(src, dst, src_off, dst_off, length, rows=None, stream=None):
     _check(LIB.moe_sort_chunks(_ptr(src), _ld(src), _ptr(dst), _ld(dst), d, _ptr(src_off),
                                _ptr(dst_off), _ptr(length), src_off.shape[0],
                                src.shape[0] if rows is None else rows, _stream(stream)))
+
+
+# ------------------------------------------------------------ the whole layer
+PREC_BF16 = 0
+PREC_FP8 = 1
+PREC_MXFP8 = 2
+
+# MOE_BUF_* of include/moe_gb300.h, in order
+BUFFERS = (
+    "topk_idx", "topk_w", "xs", "group_sizes", "kept_counts", "group_offsets", "s2f", "f2s",
+    "permute_ws", "h", "act", "y", "out", "partial", "dy", "d_topk_w", "d_logits", "dh", "dxs",
+    "dx", "dwi", "dwo", "dbi", "dbo", "dev_status", "xs_t", "act_t", "dy_t", "dh_t",
+    "f8_xs_q", "f8_xs_qt", "f8_act_q", "f8_act_qt", "f8_dy_q", "f8_dy_qt", "f8_dh_q",
+    "f8_dh_qt", "f8_wi_q", "f8_wi_qt", "f8_wo_q", "f8_wo_qt", "f8_amax", "f8_sinv",
+    "mx_xs_q", "mx_xs_sf", "mx_act_q", "mx_act_sf", "mx_dy_q", "mx_dy_sf", "mx_dh_q",
+    "mx_dh_sf", "mx_xs_t_q", "mx_xs_t_sf", "mx_act_t_q", "mx_act_t_sf", "mx_dy_t_q",
+    "mx_dy_t_sf", "mx_dh_t_q", "mx_dh_t_sf", "mx_wi_t_q", "mx_wi_t_sf", "mx_wi_q", "mx_wi_sf",
+    "mx_wo_t_q", "mx_wo_t_sf", "mx_wo_q", "mx_wo_sf", "mx_woff_d", "mx_woff_f", "aux_counts",
+    "aux_probs", "aux_loss", "aux_ws")
+BUF = {n: i for i, n in enumerate(BUFFERS)}
+
+
+class LayerConfig(ctypes.Structure):
+    """moe_layer_config."""
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "T", "d", "f", "E", "k", "score_fn", "renorm", "num_groups", "topk_group", "align",
+        "capacity", "num_chunks")] + [("aux_coeff", ctypes.c_float)] + [
+        (n, ctypes.c_int32) for n in ("bias", "precision", "wgrad_colwise", "dw_dtype")]
+
+
+MARK_FN = ctypes.CFUNCTYPE(None, ctypes.c_void_p, ctypes.c_char_p)
+
+
+def _cfg(cfg):
+    return ctypes.byref(cfg)
+
+
+def _nbytes(t):
+    return t.numel() * t.element_size()
+
+
+def moe_layer_workspace_bytes(cfg: LayerConfig) -> int:
+    """0 for an invalid configuration (reason: last_error())."""
+    return int(LIB.moe_layer_workspace_bytes(_cfg(cfg)))
+
+
+def moe_layer_buffer(cfg: LayerConfig, name: str):
+    """(byte offset, bytes) of buffer `name` (BUFFERS) in the layer workspace."""
+    off, nb = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(LIB.moe_layer_buffer(_cfg(cfg), BUF[name], ctypes.byref(off), ctypes.byref(nb)))
+    return int(off.value), int(nb.value)
+
+
+def moe_layer_init(cfg, workspace, stream=None):
+    _check(LIB.moe_layer_init(_cfg(cfg), _ptr(workspace), _nbytes(workspace), _stream(stream)))
+
+
+def _contig(*ts):
+    for t in ts:
+        assert t is None or t.is_contiguous(), "contiguous tensors only"
+
+
+def _mark_fn(mark):
+    """A C callback that calls mark(name), or None; keep it alive for the call."""
+    if mark is None:
+        return None
+    return MARK_FN(lambda _ctx, name: mark(name.decode()))
+
+
+def moe_layer_forward(cfg, workspace, x, logits, wi, wo, bi=None, bo=None, expert_bias=None,
+                      mark=None, stream=None):
+    _contig(x, logits, wi, wo, bi, bo, expert_bias)
+    cb = _mark_fn(mark)
+    _check(LIB.moe_layer_forward(_cfg(cfg), _ptr(workspace), _nbytes(workspace), _ptr(x),
+                                 _ptr(logits), _ptr(wi), _ptr(wo), _ptr(bi), _ptr(bo),
+                                 _ptr(expert_bias), ctypes.cast(cb, _P) if cb else None, None,
+                                 _stream(stream)))
+
+
+def moe_layer_backward(cfg, workspace, dout, logits, wi, wo, mark=None, stream=None):
+    _contig(dout, logits, wi, wo)
+    cb = _mark_fn(mark)
+    _check(LIB.moe_layer_backward(_cfg(cfg), _ptr(workspace), _nbytes(workspace), _ptr(dout),
+                                  _ptr(logits), _ptr(wi), _ptr(wo),
+                                  ctypes.cast(cb, _P) if cb else None, None, _stream(stream)))
+
+
+def moe_layer_pipeline_workspace_bytes(cfg) -> int:
+    return int(LIB.moe_layer_pipeline_workspace_bytes(_cfg(cfg)))
+
+
+class LayerPipeline:
+    """moe_layer_pipeline: training steps from host buffers (see the header)."""
+
+    def __init__(self, cfg, workspace, staging):
+        self.cfg, self.workspace, self.staging = cfg, workspace, staging
+        h = ctypes.c_void_p()
+        _check(LIB.moe_layer_pipeline_create(_cfg(cfg), _ptr(workspace), _nbytes(workspace),
+                                             _ptr(staging), _nbytes(staging), ctypes.byref(h)))
+        self._h = h
+
+    def step(self, wi, wo, h_x, h_logits, h_dout, h_out, h_dx, h_d_logits, bi=None, bo=None,
+             expert_bias=None, stream=None):
+        _contig(wi, wo, h_x, h_logits, h_dout, h_out, h_dx, h_d_logits, bi, bo, expert_bias)
+        _check(LIB.moe_layer_pipeline_step(self._h, _ptr(wi), _ptr(wo), _ptr(bi), _ptr(bo),
+                                           _ptr(expert_bias), _ptr(h_x), _ptr(h_logits),
+                                           _ptr(h_dout), _ptr(h_out), _ptr(h_dx),
+                                           _ptr(h_d_logits), _stream(stream)))
+
+    def join(self, stream=None):
+        _check(LIB.moe_layer_pipeline_join(self._h, _stream(stream)))
+
+    def sync(self):
+        _check(LIB.moe_layer_pipeline_sync(self._h))
+
+    def close(self):
+        if getattr(self, "_h", None):
+            LIB.moe_layer_pipeline_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        self.close()

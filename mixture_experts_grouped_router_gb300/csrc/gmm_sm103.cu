@@ -441,8 +441,18 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
       if (nc >= F) break;
       if (has_ps && c + 1 < min(c_end, BN / 2 / 32) && nc + 32 < F) load_ps(c + 1, ng, nu);
       float g[32], u[32], act[32];
-      tc::tmem_ld32(taddr + c * 32, g);
-      tc::tmem_ld32(taddr + BN / 2 + c * 32, u);
+      {  // both halves in flight, one wait
+        uint32_t rg[32], ru[32];
+        tc::tmem_ld32_issue(taddr + c * 32, rg);
+        tc::tmem_ld32_issue(taddr + BN / 2 + c * 32, ru);
+        tc::tmem_wait_ld(rg);
+        tc::reg_after(ru);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          g[j] = __uint_as_float(rg[j]);
+          u[j] = __uint_as_float(ru[j]);
+        }
+      }
       if (kDeq) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
@@ -557,9 +567,12 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
     for (int c = c_begin; c < c_end; ++c) {
       const int nc = n0 + c * 32;
       if (nc >= N) break;
-      // this chunk's H blocks (issued one chunk ahead) -> registers
+      // this chunk's H blocks (issued one chunk ahead) -> registers, while
+      // its TMEM load is in flight
       if (!tc::mbar_wait_warp(om.aux_bar, om.aux_phase & 1, abort_flag, p.wait_limit_ns)) return;
       ++om.aux_phase;
+      uint32_t rv[32];
+      tc::tmem_ld32_issue(taddr + c * 32, rv);
       float g[32], u[32];
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
@@ -572,8 +585,10 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
         tc::fence_proxy_async_smem();
         issue_aux_load(om, stg, nc + 32, wrow0);
       }
+      tc::tmem_wait_ld(rv);
       float v[32];
-      tc::tmem_ld32(taddr + c * 32, v);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(rv[j]);
       if (kDeq) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] *= sc;

@@ -65,3 +65,33 @@ def test_bytes_match_the_counts_of_a_routed_layout():
     assert got["combine"] == combine
     assert got["unpermute_bwd"] == unperm
     assert got["dispatch_bwd"] == dispatch
+
+
+def test_gemm_bytes_and_bound():
+    """Least DRAM bytes of the GEMM launches (operands read once, outputs written
+    once): at Mixtral size every GEMM is far above the ridge point of the measured
+    peaks (tensor-bound); in the skewed workload (about 100 rows per expert) the
+    weight gradients fall below it (HBM-bound: writing 64 bf16 weight gradients
+    takes longer than their FLOPs)."""
+    cfg = moe_synth.CONFIGS["mixtral"]
+    R = M = cfg.T * cfg.k
+    d, f, E = cfg.d, cfg.f, cfg.E
+    gb = bench.gemm_bytes_per_launch(cfg, R)
+    # dWi: Xs and dH read, dWi written
+    assert gb["tgmm_dwi"] == 2 * (R * d + R * 2 * f) + 2 * E * d * 2 * f
+    assert abs(gb["tgmm_dwi"] / 1e9 - 4.027) < 1e-3   # 0.268 + 1.879 + 1.879 GB
+    # SwiGLU backward: dY, wo and H read, dH written
+    assert gb["gmm_dgrad_down_swiglu_bwd"] == 2 * (R * d + E * f * d) + 4 * R * 2 * f
+    pk, _ = bench.peaks()
+    ridge = pk["bf16_tflops_sustained"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    fl = bench.gemm_flops_per_launch(cfg, M)
+    assert all(fl[n] / gb[n] > 4 * ridge for n in ("gmm_up_swiglu", "gmm_down", "tgmm_dwo",
+                                                   "gmm_dgrad_up", "tgmm_dwi"))
+    sk = moe_synth.CONFIGS["skewed"]
+    M_sk, R_sk = 5405, 53 * 128          # kept rows and aligned rows of the skewed layer
+    fl_sk = bench.gemm_flops_per_launch(sk, M_sk)
+    gb_sk = bench.gemm_bytes_per_launch(sk, R_sk)
+    assert fl_sk["tgmm_dwi"] / gb_sk["tgmm_dwi"] < ridge / 2
+    # 8-bit operands halve the operand bytes, not the bf16 outputs
+    gb8 = bench.gemm_bytes_per_launch(cfg, R, 1)
+    assert gb["tgmm_dwi"] - gb8["tgmm_dwi"] == R * d + R * 2 * f
