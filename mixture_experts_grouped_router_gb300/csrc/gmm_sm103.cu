@@ -253,6 +253,14 @@ MOE_DEVINL void stage_bf16(uint8_t *buf, int r, const float *v) {
         f32_to_bf16x8(v + 8 * c);
 }
 
+// 64 bf16 values of row r as one 128-byte row under the 128-byte swizzle (the
+// layout of stage_f32, 8 values per 16-byte chunk).
+MOE_DEVINL void stage_bf16_64(uint8_t *buf, int r, const float *v) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    *reinterpret_cast<uint4 *>(buf + r * 128 + ((c ^ (r & 7)) << 4)) = f32_to_bf16x8(v + 8 * c);
+}
+
 MOE_DEVINL void stage_f32(uint8_t *buf, int r, const float *v) {
 #pragma unroll
   for (int c = 0; c < 8; ++c)
@@ -707,6 +715,9 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
 // tgmm epilogue: warp q owns output rows m in [m_idx*128 + 32q, +32) of W_e.
 // `zero`: the expert had no rows, so TMEM is not read.  Bulk stores, or bulk
 // fp32 reduce-adds into W when accumulating; the box is clipped at M and N.
+// A bf16 W leaves in 32 x 64 boxes (128-byte rows, two TMEM loads in flight
+// per box): with few rows per expert this epilogue sets the pace, and half as
+// many boxes per tile means half the staging waits, fences and store issues.
 template <bool F8, int BN, bool MX>
 MOE_DEVINL void epilogue_tgmm(const TcParams &p, const TileInfo &ti, uint32_t taddr, int q,
                               int lane, uint8_t *stg, const OutMaps &om, bool zero) {
@@ -714,6 +725,37 @@ MOE_DEVINL void epilogue_tgmm(const TcParams &p, const TileInfo &ti, uint32_t ta
   const float sc = kDeq && !zero ? __ldg(p.a_sinv) * __ldg(p.b_sinv) : 1.0f;
   const int wm0 = ti.m_idx * BM + q * 32;
   const int n0 = ti.n_idx * BN;
+  if (!p.c_f32) {
+#pragma unroll 1
+    for (int c = 0; c < BN / 64; ++c) {
+      const int nc = n0 + c * 64;
+      if (nc >= p.N) break;
+      float v[64];
+      if (zero) {
+#pragma unroll
+        for (int j = 0; j < 64; ++j) v[j] = 0.f;
+      } else {
+        uint32_t r0[32], r1[32];
+        tc::tmem_ld32_issue(taddr + c * 64, r0);
+        tc::tmem_ld32_issue(taddr + c * 64 + 32, r1);
+        tc::tmem_wait_ld(r0);
+        tc::reg_after(r1);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          v[j] = __uint_as_float(r0[j]) * sc;
+          v[32 + j] = __uint_as_float(r1[j]) * sc;
+        }
+      }
+      stage_acquire(lane);
+      stage_bf16_64(stg, lane, v);
+      stage_release();
+      if (lane == 0) {
+        tc::tma_store_3d(om.m0, stg, nc, wm0, ti.e);
+        tc::bulk_commit();
+      }
+    }
+    return;
+  }
 #pragma unroll 1
   for (int c = 0; c < BN / 32; ++c) {
     const int nc = n0 + c * 32;
@@ -1395,10 +1437,10 @@ static moe_status_t tgmm_impl(const TgmmArgs &a, const uint16_t *At, int64_t lda
     const int64_t stride_w = a.E > 1 ? a.stride_w : (int64_t)a.M * a.ldw;
     const uint64_t dims[3] = {(uint64_t)a.N, (uint64_t)a.M, (uint64_t)a.E};
     const uint64_t st[2] = {(uint64_t)(a.ldw * es), (uint64_t)(stride_w * es)};
-    const uint32_t box[3] = {32, 32, 1};
+    const uint32_t box[3] = {f32 ? 32u : 64u, 32, 1};
     if (!make_map(&mc[0], a.W, 3, dims, st, box,
                   f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                  f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B)) {
+                  CU_TENSOR_MAP_SWIZZLE_128B)) {
       set_error("moe_tgmm: cannot encode the TMA descriptor of W");
       return MOE_ERR_CUDA;
     }
@@ -1574,10 +1616,10 @@ moe_status_t launch_tgmm_f8(const TgmmF8Args &a, cudaStream_t s) {
     const int64_t stride_w = a.E > 1 ? a.stride_w : (int64_t)a.M * a.ldw;
     const uint64_t dims[3] = {(uint64_t)a.N, (uint64_t)a.M, (uint64_t)a.E};
     const uint64_t st[2] = {(uint64_t)(a.ldw * es), (uint64_t)(stride_w * es)};
-    const uint32_t wbox[3] = {32, 32, 1};
+    const uint32_t wbox[3] = {f32 ? 32u : 64u, 32, 1};
     if (!make_map(&mc[0], a.W, 3, dims, st, wbox,
                   f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                  f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B)) {
+                  CU_TENSOR_MAP_SWIZZLE_128B)) {
       set_error("moe_tgmm_fp8: cannot encode the TMA descriptor of W");
       return MOE_ERR_CUDA;
     }
@@ -1752,10 +1794,10 @@ moe_status_t launch_tgmm_mx(const TgmmMxArgs &a, cudaStream_t s) {
     const int64_t stride_w = a.E > 1 ? a.stride_w : (int64_t)a.M * a.ldw;
     const uint64_t dims[3] = {(uint64_t)a.N, (uint64_t)a.M, (uint64_t)a.E};
     const uint64_t st[2] = {(uint64_t)(a.ldw * es), (uint64_t)(stride_w * es)};
-    const uint32_t wbox[3] = {32, 32, 1};
+    const uint32_t wbox[3] = {f32 ? 32u : 64u, 32, 1};
     if (!make_map(&mc[0], a.W, 3, dims, st, wbox,
                   f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                  f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B)) {
+                  CU_TENSOR_MAP_SWIZZLE_128B)) {
       set_error("moe_tgmm_mx: cannot encode the TMA descriptor of W");
       return MOE_ERR_CUDA;
     }
