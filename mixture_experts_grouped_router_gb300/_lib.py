@@ -605,9 +605,13 @@ class LayerPipeline:
         _check(LIB.moe_layer_pipeline_sync(self._h))
 
     def close(self):
+        """Synchronise the copy streams and release them (idempotent)."""
         if getattr(self, "_h", None):
             LIB.moe_layer_pipeline_destroy(self._h)
             self._h = None
 
     def __del__(self):
-        self.close()
+        try:
+            self.close()
+        except Exception:   # interpreter shutdown: the library may already be unloaded
+            pass

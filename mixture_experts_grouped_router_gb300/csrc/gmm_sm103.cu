@@ -718,9 +718,13 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
 // A bf16 W leaves in 32 x 64 boxes (128-byte rows, two TMEM loads in flight
 // per box): with few rows per expert this epilogue sets the pace, and half as
 // many boxes per tile means half the staging waits, fences and store issues.
+// The warp's 8 KB of staging holds two such boxes, used in turn (`slot`
+// counts the warp's boxes across tiles), so that the previous box's store may
+// still be reading shared memory while the next one is staged.
 template <bool F8, int BN, bool MX>
 MOE_DEVINL void epilogue_tgmm(const TcParams &p, const TileInfo &ti, uint32_t taddr, int q,
-                              int lane, uint8_t *stg, const OutMaps &om, bool zero) {
+                              int lane, uint8_t *stg, const OutMaps &om, bool zero,
+                              uint32_t &slot) {
   constexpr bool kDeq = F8 && !MX;
   const float sc = kDeq && !zero ? __ldg(p.a_sinv) * __ldg(p.b_sinv) : 1.0f;
   const int wm0 = ti.m_idx * BM + q * 32;
@@ -746,13 +750,16 @@ MOE_DEVINL void epilogue_tgmm(const TcParams &p, const TileInfo &ti, uint32_t ta
           v[32 + j] = __uint_as_float(r1[j]) * sc;
         }
       }
-      stage_acquire(lane);
-      stage_bf16_64(stg, lane, v);
+      uint8_t *buf = stg + (slot & 1) * 4096;
+      if (lane == 0) tc::bulk_wait_read<1>();
+      __syncwarp();
+      stage_bf16_64(buf, lane, v);
       stage_release();
       if (lane == 0) {
-        tc::tma_store_3d(om.m0, stg, nc, wm0, ti.e);
+        tc::tma_store_3d(om.m0, buf, nc, wm0, ti.e);
         tc::bulk_commit();
       }
+      ++slot;
     }
     return;
   }
@@ -1102,11 +1109,12 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     OutMaps om{&tmC0, &tmC1, &tmC2, &tmC3, &bk.aux_full[warp - 2], 0u, 0u,
                tc::l2_evict_first_policy()};
     uint32_t acc_it = 0;
+    uint32_t stg_slot = 0;  // tgmm: boxes staged so far (which half of the staging is next)
     float amx = 0.0f;
     for (int t = cid; t < total; t += ncl) {
       const TileInfo ti = decode_tile<KIND, F8, AK>(bk, p, t, crank);
       if (KIND == KIND_TGMM && ti.kblocks == 0) {
-        if (!p.accumulate) epilogue_tgmm<F8, BN, MX>(p, ti, 0, q, lane, stg, om, true);
+        if (!p.accumulate) epilogue_tgmm<F8, BN, MX>(p, ti, 0, q, lane, stg, om, true, stg_slot);
         continue;
       }
       epilogue_prefetch<KIND, EPI, BN>(p, ti, rit, c_begin, c_begin + kChunks);
@@ -1121,7 +1129,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         epilogue_gmm<EPI, F8, BN, MX, CT>(p, ti, taddr, q, lane, stg, om, abort_flag, c_begin,
                               c_begin + kChunks, amx);
       else
-        epilogue_tgmm<F8, BN, MX>(p, ti, taddr, q, lane, stg, om, false);
+        epilogue_tgmm<F8, BN, MX>(p, ti, taddr, q, lane, stg, om, false, stg_slot);
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) {

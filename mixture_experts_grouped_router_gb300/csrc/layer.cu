@@ -7,7 +7,6 @@
 // Add an MoE Block (Layer) that compound router, permutation, groupedGEMM and
 // communication", sequence diagram) on one GPU: route -> permute -> grouped
 // GEMM (up, SwiGLU) -> grouped GEMM (down) -> combine, and its VJP.
-#include <stdio.h>
 
 #include <new>
 

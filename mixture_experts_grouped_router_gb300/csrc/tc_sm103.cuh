@@ -162,6 +162,11 @@ MOE_DEVINL void tma_reduce_add_3d(const CUtensorMap *map, const void *src, int c
 
 MOE_DEVINL void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 MOE_DEVINL void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// at most N of this thread's most recent bulk groups may still be reading shared memory
+template <int N>
+MOE_DEVINL void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
 MOE_DEVINL void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // ------------------------------------------------------------- clusters

@@ -74,3 +74,55 @@ def test_pipeline_steps(name):
                                             cfg.score_fn, cfg.renorm))
     # the weight gradients left in the workspace are the last step's
     assert torch.equal(b.dwi, ref.dwi) and torch.equal(b.dwo, ref.dwo)
+
+
+@pytest.mark.parametrize("opts", [
+    dict(fp8=True),
+    dict(mxfp8=True),
+    dict(bias=True, num_groups=4, topk_group=2, aux_coeff=1e-3, num_chunks=2),
+    dict(wgrad_colwise=True),
+], ids=["fp8", "mxfp8", "bias_groups_aux_chunks", "colwise"])
+def test_pipeline_options(opts):
+    """Every layer option through the host-buffer pipeline: two steps with
+    different inputs, host results bit for bit against the device-buffer calls
+    (whose parity with the oracles the layer tests of each option check)."""
+    import dataclasses
+    from mixture_experts_grouped_router_gb300 import layer
+    cfg = moe_synth.scaled(C["mixtral"], T=512, d=256, f=384)
+    shape = dataclasses.replace(layer_shape(cfg), **opts)
+    inps = [moe_synth.make_inputs(cfg, seed=s) for s in range(2)]
+    wi, wo = dev_bf16(inps[0]["wi"]), dev_bf16(inps[0]["wo"])
+    bi = bo = None
+    if shape.bias:
+        bs = moe_synth.make_biases(cfg, seed=0)
+        bi, bo = dev_bf16(bs["bi"]), dev_bf16(bs["bo"])
+    b = layer.MoEBuffers(shape)
+    staging = torch.empty(L.moe_layer_pipeline_workspace_bytes(b.cfg), dtype=torch.uint8,
+                          device="cuda")
+    pipe = L.LayerPipeline(b.cfg, b.workspace, staging)
+    h_in = [dict(x=_pinned_bf16(i["x"]), logits=torch.from_numpy(i["logits"]).pin_memory(),
+                 dout=_pinned_bf16(i["dout"])) for i in inps]
+    h_res = [dict(out=torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory(),
+                  dx=torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory(),
+                  d_logits=torch.empty(cfg.T, cfg.E, dtype=torch.float32).pin_memory())
+             for _ in inps]
+    for s in range(len(inps)):
+        pipe.step(wi, wo, h_in[s]["x"], h_in[s]["logits"], h_in[s]["dout"], h_res[s]["out"],
+                  h_res[s]["dx"], h_res[s]["d_logits"], bi=bi, bo=bo)
+    pipe.sync()
+    torch.cuda.synchronize()
+    pipe.close()
+    assert int(b.dev_status.item()) == 0
+    ref = layer.MoEBuffers(shape)
+    for s, inp in enumerate(inps):
+        layer.forward(ref, dev_bf16(inp["x"]), torch.from_numpy(inp["logits"]).cuda(), wi, wo,
+                      bi=bi, bo=bo)
+        layer.backward(ref, dev_bf16(inp["dout"]), wi, wo)
+        torch.cuda.synchronize()
+        for key, dev in (("out", ref.out), ("dx", ref.dx), ("d_logits", ref.d_logits)):
+            got = h_res[s][key]
+            assert torch.isfinite(got.float()).all(), (s, key)
+            assert torch.equal(got, dev.cpu()), (s, key)
+    assert torch.equal(b.dwi, ref.dwi) and torch.equal(b.dwo, ref.dwo)
+    if shape.bias:
+        assert torch.equal(b.dbi, ref.dbi) and torch.equal(b.dbo, ref.dbo)
