@@ -80,6 +80,8 @@ PROFILE_CONFIGS = {
                             renorm=0),
     "dsv3_e8": MoEConfig("dsv3_e8", T=2048, d=7168, f=2048, E=8, k=8, score_fn=SIGMOID,
                          renorm=1),
+    "dsv3_e8_chunked": MoEConfig("dsv3_e8_chunked", T=2048, d=7168, f=2048, E=8, k=8,
+                                 score_fn=SIGMOID, renorm=1, num_chunks=4),
     # the skewed-routing layer's expert shape and routing on 16 experts
     "skewed_e16": MoEConfig("skewed_e16", T=8192, d=4096, f=2048, E=16, k=1, score_fn=SOFTMAX,
                             renorm=0, align=128, capacity=512, zipf_s=1.2, zipf_kappa=0.92),
