@@ -63,6 +63,12 @@ constexpr int kStages = 8;  // ring slots of the barrier book (6 or 7 in use, se
 constexpr int kMaxEpiWarps = 4;
 constexpr int kPadRows = kF8PadRows;  // group padding of column-wise copies (128 rows)
 constexpr int kStgBytes = 8192;  // per epilogue warp: up to four 32x32 bf16 blocks (or two fp32)
+// Internal epilogue: the SwiGLU forward that adds an fp32 partial sum (the last
+// K-chunk of a chunked up-projection), its partial-sum blocks brought into the
+// warp's staging by TMA loads one chunk ahead (16 KB of staging per warp, so 5
+// stages)
+constexpr int kEpiSwigluPs = 3;
+constexpr bool is_swiglu_fwd(int epi) { return epi == MOE_EPI_SWIGLU_FWD || epi == kEpiSwigluPs; }
 constexpr int A_BYTES = BM * BK * 2;   // 16 KB
 constexpr int BOX_BYTES = 64 * 64 * 2; // one 64x64 MN-major box, 8 KB
 constexpr int kMaxE = 256;
@@ -104,7 +110,8 @@ struct Book {
 template <int KIND, int EPI, bool F8, int BN, bool MX>
 struct Ring {
   static constexpr int epi_warps = 4;
-  static constexpr int stages = 6;
+  static constexpr int stages = EPI == kEpiSwigluPs ? 5 : 6;
+  static constexpr int stg_bytes = EPI == kEpiSwigluPs ? 2 * kStgBytes : kStgBytes;  // per warp
   static constexpr int b_bytes = BN * BK;  // this CTA's BN / 2 columns of B, 128-byte rows
   // block scaling: the scale factors of the stage's K block, A's 128 rows (one
   // 512-byte atom) and the tile's 192 columns (two atoms)
@@ -115,7 +122,7 @@ struct Ring {
   static_assert(stages <= kStages, "barrier book");
   static constexpr int threads = 64 + 32 * epi_warps;  // producer, MMA, epilogue
   static constexpr int stg_offset = stages * stage_bytes;  // 1024-aligned
-  static constexpr int book_offset = stg_offset + epi_warps * kStgBytes;
+  static constexpr int book_offset = stg_offset + epi_warps * stg_bytes;
   static constexpr int smem_bytes =
       1024 + book_offset + (int)((sizeof(Book) + 127) / 128 * 128);
   static_assert(stg_offset % 1024 == 0, "staging alignment");
@@ -348,7 +355,7 @@ MOE_DEVINL void epilogue_prefetch(const TcParams &p, const TileInfo &ti, int rit
       }
     } else if (p.ps != nullptr) {
       const float *q = p.ps + row * p.ld_ps;
-      if (EPI == MOE_EPI_SWIGLU_FWD) {
+      if (is_swiglu_fwd(EPI)) {
         const int n0 = ti.n_idx * (BN / 2);
         for (int n = n0; n < min(n0 + BN / 2, p.F); n += 32) {
           prefetch_l2(q + n);
@@ -402,6 +409,29 @@ MOE_DEVINL void issue_aux_load(OutMaps &om, uint8_t *stg, int nc, int wrow0) {
   tc::tma_load_2d_hint(stg + 6144, om.m3, om.aux_bar, nc, wrow0, om.stream_pol);
 }
 
+// SwiGLU forward with a partial sum: TMA loads of the warp's 32 x 32 fp32
+// blocks of P (gate columns nc.., up columns F + nc..) into the second half of
+// its staging (lane 0 issues; m3 is the map of P).
+MOE_DEVINL void issue_ps_load(OutMaps &om, uint8_t *stg, int nc, int F, int wrow0) {
+  ++om.aux_issued;
+  tc::mbar_expect_tx(om.aux_bar, 8192);
+  tc::tma_load_2d_hint(stg + kStgBytes, om.m3, om.aux_bar, nc, wrow0, om.stream_pol);
+  tc::tma_load_2d_hint(stg + kStgBytes + 4096, om.m3, om.aux_bar, F + nc, wrow0, om.stream_pol);
+}
+
+// Row r's 32 fp32 values of a 32 x 32 block staged under the 128-byte swizzle
+// (the inverse of stage_f32).
+MOE_DEVINL void unstage_f32(const uint8_t *buf, int r, float *v) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint4 w = *reinterpret_cast<const uint4 *>(buf + r * 128 + ((c ^ (r & 7)) << 4));
+    v[4 * c] = __uint_as_float(w.x);
+    v[4 * c + 1] = __uint_as_float(w.y);
+    v[4 * c + 2] = __uint_as_float(w.z);
+    v[4 * c + 3] = __uint_as_float(w.w);
+  }
+}
+
 // One tile's epilogue for the ragged-M GEMM.  Warp q owns tile rows
 // [32q, 32q+32), thread = one row; 32-column chunks.
 // Chunks [c_begin, c_end) of the tile's 32-column chunks are this warp's.
@@ -427,10 +457,14 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
   // expert's padding in the copy); a tile past the expert writes nothing
   const bool colwise = CT && ti.row0 < ti.row_end;
   const int64_t pc0 = (int64_t)ti.pcol0 + q * 32;
-  if (EPI == MOE_EPI_SWIGLU_FWD) {
+  if (is_swiglu_fwd(EPI)) {
+    // kPsTma: the partial sum arrives by TMA in the staging (first chunk's
+    // load issued at the tile's start); otherwise a partial sum is loaded
+    // into registers one chunk ahead
+    constexpr bool kPsTma = EPI == kEpiSwigluPs;
     const int F = p.F;
     const int n0 = ti.n_idx * (BN / 2);
-    const bool has_ps = !F8 && valid && p.ps != nullptr;
+    const bool has_ps = !kPsTma && !F8 && valid && p.ps != nullptr;
     auto load_ps = [&](int c, uint4 *g4, uint4 *u4) {
       const int nc = n0 + c * 32;
 #pragma unroll
@@ -448,6 +482,20 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
       const int nc = n0 + c * 32;
       if (nc >= F) break;
       if (has_ps && c + 1 < min(c_end, BN / 2 / 32) && nc + 32 < F) load_ps(c + 1, ng, nu);
+      float pgv[32], puv[32];
+      if (kPsTma) {
+        // this chunk's P blocks -> registers, then the next chunk's loads
+        if (!tc::mbar_wait_warp(om.aux_bar, om.aux_phase & 1, abort_flag, p.wait_limit_ns))
+          return;
+        ++om.aux_phase;
+        unstage_f32(stg + kStgBytes, lane, pgv);
+        unstage_f32(stg + kStgBytes + 4096, lane, puv);
+        __syncwarp();
+        if (lane == 0 && c + 1 < min(c_end, BN / 2 / 32) && nc + 32 < F) {
+          tc::fence_proxy_async_smem();
+          issue_ps_load(om, stg, nc + 32, F, wrow0);
+        }
+      }
       float g[32], u[32], act[32];
       {  // both halves in flight, one wait
         uint32_t rg[32], ru[32];
@@ -466,6 +514,13 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
         for (int j = 0; j < 32; ++j) {
           g[j] *= sc;
           u[j] *= sc;
+        }
+      }
+      if (kPsTma) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          g[j] += pgv[j];
+          u[j] += puv[j];
         }
       }
       if (has_ps) {
@@ -939,11 +994,11 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             tc::tma_load_2d_2sm(sa, &tmA, fbl, kb * BKE, ti.row0);
             if (B_MN) {
               // this CTA's 128 columns of B: two 64-column boxes
-              const int n0 = EPI == MOE_EPI_SWIGLU_FWD ? ti.n_idx * (BN / 2) : ti.n_idx * BN;
+              const int n0 = is_swiglu_fwd(EPI) ? ti.n_idx * (BN / 2) : ti.n_idx * BN;
 #pragma unroll
               for (int j = 0; j < 2; ++j) {
                 const int i = 2 * crank + j;
-                const int x = EPI == MOE_EPI_SWIGLU_FWD
+                const int x = is_swiglu_fwd(EPI)
                                   ? (i < 2 ? n0 + 64 * i : p.F + n0 + 64 * (i - 2))
                                   : n0 + 64 * i;
                 tc::tma_load_3d_2sm(sb + j * BOX_BYTES, &tmB, fbl, x, kb * BKE, ti.e);
@@ -951,7 +1006,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             } else {
               // K-major B: this CTA's 128 of the tile's 256 columns (SwiGLU
               // forward: gate columns in the first CTA, up columns in the second)
-              const int nrow = EPI == MOE_EPI_SWIGLU_FWD
+              const int nrow = is_swiglu_fwd(EPI)
                                    ? (crank == 0 ? 0 : p.F) + ti.n_idx * (BN / 2)
                                    : ti.n_idx * BN + crank * (BN / 2);
               tc::tma_load_3d_2sm(sb, &tmB, fbl, kb * BKE, nrow, ti.e);
@@ -1103,7 +1158,8 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   } else if (warp >= 2) {
     const int q = warp & 3;  // TMEM lane quarter this warp may read = its tile rows
     const int rit = q * 32 + lane;
-    uint8_t *stg = smem + Ring<KIND, EPI, F8, BN, MX>::stg_offset + (warp - 2) * kStgBytes;
+    uint8_t *stg = smem + Ring<KIND, EPI, F8, BN, MX>::stg_offset +
+                   (warp - 2) * Ring<KIND, EPI, F8, BN, MX>::stg_bytes;
     constexpr int kChunks = BN / 32;  // the tile's 32-column chunks, all this warp's
     const int c_begin = 0;
     OutMaps om{&tmC0, &tmC1, &tmC2, &tmC3, &bk.aux_full[warp - 2], 0u, 0u,
@@ -1120,6 +1176,10 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       epilogue_prefetch<KIND, EPI, BN>(p, ti, rit, c_begin, c_begin + kChunks);
       if (KIND == KIND_GMM && EPI == MOE_EPI_SWIGLU_BWD && lane == 0)
         issue_aux_load(om, stg, ti.n_idx * BN + c_begin * 32, ti.row0 + q * 32);  // first chunk
+      if (KIND == KIND_GMM && EPI == kEpiSwigluPs && lane == 0) {
+        tc::fence_proxy_async_smem();  // the previous tile's reads of the P blocks came first
+        issue_ps_load(om, stg, ti.n_idx * (BN / 2) + c_begin * 32, p.F, ti.row0 + q * 32);
+      }
       const uint32_t a = acc_it & 1;
       const uint32_t aph = (acc_it >> 1) & 1;
       if (!tc::mbar_wait_warp(&bk.tfull[a], aph, abort_flag, p.wait_limit_ns)) break;
@@ -1150,7 +1210,7 @@ gmm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     }
     // every bulk store and H load of this warp has completed before the CTA exits
     if (lane == 0) tc::bulk_wait0();
-    if (KIND == KIND_GMM && EPI == MOE_EPI_SWIGLU_BWD &&
+    if (KIND == KIND_GMM && (EPI == MOE_EPI_SWIGLU_BWD || EPI == kEpiSwigluPs) &&
         __shfl_sync(0xffffffffu, om.aux_issued, 0) != om.aux_phase)
       tc::mbar_wait_drain(om.aux_bar, om.aux_phase & 1, p.wait_limit_ns / 4);
     __syncwarp();
@@ -1362,6 +1422,14 @@ moe_status_t launch_gmm(const GmmArgs &a, cudaStream_t s) {
                               true>(ma, mb, mc, p, tiles_upper, s);
     set_error("moe_gmm: no column-wise copy for this epilogue / layout");
     return MOE_ERR_UNSUPPORTED;
+  }
+  if (a.epilogue == MOE_EPI_SWIGLU_FWD && a.ps != nullptr && b_mn) {
+    // m3: the partial sum P [rows_cap, 2F] fp32, read in 32 x 32 blocks
+    if (!make_out_map(&mc[3], a.ps, true, 2 * p.F, a.rows_cap, a.ld_ps)) {
+      set_error("moe_gmm: cannot encode the TMA descriptor of the partial sum");
+      return MOE_ERR_CUDA;
+    }
+    return launch_tc<KIND_GMM, true, kEpiSwigluPs>(ma, mb, mc, p, tiles_upper, s);
   }
   switch (a.epilogue * 2 + (b_mn ? 1 : 0)) {
     case MOE_EPI_NONE * 2 + 1:
