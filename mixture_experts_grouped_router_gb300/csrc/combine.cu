@@ -39,19 +39,28 @@ combine_kernel(const uint16_t *__restrict__ Y, int64_t ldy, const int32_t *__res
   uint4 *dst = reinterpret_cast<uint4 *>(out + (int64_t)t * ldo);
   for (int i = lane; i < nvec; i += 64) {
     const bool two = i + 32 < nvec;
+    // every slot's loads in flight before the first is used
+    uint4 yq[KT][2];
+#pragma unroll
+    for (int j = 0; j < KT; ++j) {
+      if (j < k && p[j] >= 0) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(Y + (int64_t)p[j] * ldy);
+        yq[j][0] = ld_nc_v4(src + i);
+        if (two) yq[j][1] = ld_nc_v4(src + i + 32);
+      }
+    }
     float acc0[8], acc1[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) acc0[q] = acc1[q] = 0.f;
 #pragma unroll
     for (int j = 0; j < KT; ++j) {
       if (j < k && p[j] >= 0) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(Y + (int64_t)p[j] * ldy);
         float f[8];
-        bf16x8_to_f32(ld_nc_v4(src + i), f);
+        bf16x8_to_f32(yq[j][0], f);
 #pragma unroll
         for (int q = 0; q < 8; ++q) acc0[q] = fmaf(wj[j], f[q], acc0[q]);
         if (two) {
-          bf16x8_to_f32(ld_nc_v4(src + i + 32), f);
+          bf16x8_to_f32(yq[j][1], f);
 #pragma unroll
           for (int q = 0; q < 8; ++q) acc1[q] = fmaf(wj[j], f[q], acc1[q]);
         }

@@ -459,12 +459,13 @@ MOE_DEVINL void epilogue_gmm(const TcParams &p, const TileInfo &ti, uint32_t tad
   const int64_t pc0 = (int64_t)ti.pcol0 + q * 32;
   if (is_swiglu_fwd(EPI)) {
     // kPsTma: the partial sum arrives by TMA in the staging (first chunk's
-    // load issued at the tile's start); otherwise a partial sum is loaded
-    // into registers one chunk ahead
+    // load issued at the tile's start); the column-wise-copy instance, whose
+    // fourth map is the copy's, loads it into registers one chunk ahead (the
+    // plain instance never gets one: the host sends partial sums to kPsTma)
     constexpr bool kPsTma = EPI == kEpiSwigluPs;
     const int F = p.F;
     const int n0 = ti.n_idx * (BN / 2);
-    const bool has_ps = !kPsTma && !F8 && valid && p.ps != nullptr;
+    const bool has_ps = CT && !F8 && valid && p.ps != nullptr;
     auto load_ps = [&](int c, uint4 *g4, uint4 *u4) {
       const int nc = n0 + c * 32;
 #pragma unroll
