@@ -28,6 +28,8 @@
 //   SWIGLU   a fused [gate | up] weight (2F rows) in the order of the SwiGLU
 //            tiles: tile t holds gate rows [96 t, 96 t + 96) then up rows
 //            [F + 96 t, F + 96 t + 96), at padded rows 256 t ...
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -191,14 +193,36 @@ MOE_DEVINL uint8_t quant_block(float *v, int fmt, uint32_t *w) {
 constexpr int kMx2Rows = 64, kMx2Cols = 128;
 constexpr int kMx2Pitch = kMx2Cols * 2 + 16;  // bytes per staged row: 16 spare keep banks apart
 
-__global__ void __launch_bounds__(256)
+// Loads tile (tile_x, tile_y) of x into a staging buffer with 16-byte
+// asynchronous copies, rows past the group as zeros (a copy of 0 source bytes
+// fills its 16 bytes with zeros).
+MOE_DEVINL void mx2_load_tile(uint8_t *buf, const uint16_t *x, int64_t ldx, int64_t g0,
+                              int64_t gsz, int64_t i0, int c0, int tid) {
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    const int idx = tid + 256 * h;
+    const int rr = idx >> 4, ch = idx & 15;
+    const bool in = i0 + rr < gsz;
+    const uint16_t *src = in ? x + (g0 + i0 + rr) * ldx + c0 + ch * 8 : x;
+    const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(buf + rr * kMx2Pitch + ch * 16));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                 "r"(in ? 16 : 0)
+                 : "memory");
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Persistent: block b quantizes tiles b, b + grid, ... (64 padded rows x 128
+// columns each, tile t at column tile t % col_tiles, row tile t / col_tiles);
+// the next tile's load runs while this one is quantized (two staging buffers).
+__global__ void __launch_bounds__(256, 4)
 mx_quantize_2x_kernel(const uint16_t *__restrict__ x, int64_t ldx, int64_t rows, int cols,
                       int fmt, const int32_t *__restrict__ offsets, int E,
                       uint8_t *__restrict__ q, int64_t ldq, int q_map, uint8_t *__restrict__ sfq,
                       uint8_t *__restrict__ qt, int64_t ldqt, int qt_cols, int qt_map,
-                      uint8_t *__restrict__ sfqt) {
+                      uint8_t *__restrict__ sfqt, int64_t n_tiles) {
   __shared__ int s_poff[kMxMaxE + 1];
-  __shared__ __align__(16) uint8_t tile[kMx2Rows * kMx2Pitch];
+  __shared__ __align__(16) uint8_t tiles[2][kMx2Rows * kMx2Pitch];
   const int tid = threadIdx.x;
   if (tid < 32) {  // padded group starts (warp-shuffle scan)
     int carry = 0;
@@ -218,64 +242,82 @@ mx_quantize_2x_kernel(const uint16_t *__restrict__ x, int64_t ldx, int64_t rows,
     if (tid == 0) s_poff[E] = carry;
   }
   __syncthreads();
-  const int64_t pr0 = (int64_t)blockIdx.y * kMx2Rows;
-  if (pr0 >= s_poff[E]) return;  // past the last group (uniform across the block)
-  int e = 0, lo = 0, hi = E - 1;  // the group of this tile (tiles never straddle groups)
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (s_poff[mid] <= pr0) lo = mid;
-    else hi = mid - 1;
-  }
-  e = lo;
-  const int64_t g0 = min(max((int64_t)__ldg(offsets + e), (int64_t)0), rows);
-  const int64_t gsz = min(max((int64_t)__ldg(offsets + e + 1), g0), rows) - g0;
-  const int64_t i0 = pr0 - s_poff[e];  // first row of the tile within the group
-  const int c0 = blockIdx.x * kMx2Cols;
-  // stage: 64 rows x 16 chunks of 16 bytes, four chunks per thread; rows past
-  // the group are zeros
+  const int col_tiles = cols / kMx2Cols;
+  const int64_t prows = s_poff[E];
+  // tile t -> (group, its first row in the group, first padded row, first column)
+  struct Tile {
+    int64_t g0, gsz, i0, pr0;
+    int c0;
+    bool live;
+  };
+  auto locate = [&](int64_t t) {
+    Tile ti;
+    ti.pr0 = (t / col_tiles) * kMx2Rows;
+    ti.c0 = (int)(t % col_tiles) * kMx2Cols;
+    ti.live = t < n_tiles && ti.pr0 < prows;
+    int lo = 0, hi = E - 1;  // the group of the tile (tiles never straddle groups)
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_poff[mid] <= ti.pr0) lo = mid;
+      else hi = mid - 1;
+    }
+    ti.g0 = min(max((int64_t)__ldg(offsets + lo), (int64_t)0), rows);
+    ti.gsz = min(max((int64_t)__ldg(offsets + lo + 1), ti.g0), rows) - ti.g0;
+    ti.i0 = ti.pr0 - s_poff[lo];
+    return ti;
+  };
+  int64_t t = blockIdx.x;
+  Tile cur = locate(t);
+  if (cur.live) mx2_load_tile(tiles[0], x, ldx, cur.g0, cur.gsz, cur.i0, cur.c0, tid);
+  for (int it = 0; cur.live; ++it) {
+    uint8_t *tile = tiles[it & 1];
+    const Tile nxt = locate(t + gridDim.x);
+    // this tile's copies landed (every thread's), and every thread is done
+    // with the buffer the next load overwrites (quantized one iteration ago)
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+    if (nxt.live) mx2_load_tile(tiles[(it + 1) & 1], x, ldx, nxt.g0, nxt.gsz, nxt.i0, nxt.c0, tid);
+    const int64_t g0 = cur.g0, gsz = cur.gsz, i0 = cur.i0, pr0 = cur.pr0;
+    const int c0 = cur.c0;
+    float v[32];
+    uint32_t w[8];
+    {
+      const int rr = tid >> 2, blk = tid & 3;
+      if (q != nullptr && i0 + rr < gsz) {
 #pragma unroll
-  for (int h = 0; h < 4; ++h) {
-    const int idx = tid + 256 * h;
-    const int rr = idx >> 4, ch = idx & 15;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (i0 + rr < gsz)
-      v = ld_nc_v4(x + (g0 + i0 + rr) * ldx + c0 + ch * 8);
-    *reinterpret_cast<uint4 *>(tile + rr * kMx2Pitch + ch * 16) = v;
-  }
-  __syncthreads();
-  float v[32];
-  uint32_t w[8];
-  {
-    const int rr = tid >> 2, blk = tid & 3;
-    if (q != nullptr && i0 + rr < gsz) {
+        for (int i = 0; i < 4; ++i)
+          bf16x8_to_f32(
+              *reinterpret_cast<const uint4 *>(tile + rr * kMx2Pitch + blk * 64 + i * 16),
+              v + 8 * i);
+        const uint8_t code = quant_block(v, fmt, w);
+        const int64_t r = g0 + i0 + rr;
+        uint4 *dst = reinterpret_cast<uint4 *>(q + r * ldq + c0 + blk * 32);
+        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        const int64_t pr =
+            q_map == MOE_MX_ROWS_GROUPED ? pr0 + rr : mapped_row(r, rows, q_map, E);
+        sfq[scale_byte(pr, (c0 >> 5) + blk, cols)] = code;
+      }
+    }
+    const int c = tid & 127, half = tid >> 7;  // column, and which 32 of the 64 rows
+    const int64_t pb = pr0 + 32 * half;        // the block's first padded row
+    if (qt != nullptr && pb + 32 <= qt_cols) {
+      const uint16_t *col = reinterpret_cast<const uint16_t *>(tile + 32 * half * kMx2Pitch) + c;
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        bf16x8_to_f32(*reinterpret_cast<const uint4 *>(tile + rr * kMx2Pitch + blk * 64 + i * 16),
-                      v + 8 * i);
+      for (int rr = 0; rr < 32; ++rr)
+        v[rr] = __uint_as_float((uint32_t)col[rr * (kMx2Pitch / 2)] << 16);
       const uint8_t code = quant_block(v, fmt, w);
-      const int64_t r = g0 + i0 + rr;
-      uint4 *dst = reinterpret_cast<uint4 *>(q + r * ldq + c0 + blk * 32);
+      const int64_t n = c0 + c;  // row of qt
+      uint4 *dst = reinterpret_cast<uint4 *>(qt + n * ldqt + pb);
       dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
       dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-      const int64_t pr = q_map == MOE_MX_ROWS_GROUPED ? pr0 + rr : mapped_row(r, rows, q_map, E);
-      sfq[scale_byte(pr, (c0 >> 5) + blk, cols)] = code;
+      const int64_t pr = mapped_row(n, cols, qt_map, 1);
+      sfqt[scale_byte(pr, (int)(pb >> 5), qt_cols)] = code;
     }
+    cur = nxt;
+    t += gridDim.x;
   }
-  const int c = tid & 127, half = tid >> 7;  // column, and which 32 of the 64 rows
-  const int64_t pb = pr0 + 32 * half;        // the block's first padded row
-  if (qt != nullptr && pb + 32 <= qt_cols) {
-    const uint16_t *col = reinterpret_cast<const uint16_t *>(tile + 32 * half * kMx2Pitch) + c;
-#pragma unroll
-    for (int rr = 0; rr < 32; ++rr)
-      v[rr] = __uint_as_float((uint32_t)col[rr * (kMx2Pitch / 2)] << 16);
-    const uint8_t code = quant_block(v, fmt, w);
-    const int64_t n = c0 + c;  // row of qt
-    uint4 *dst = reinterpret_cast<uint4 *>(qt + n * ldqt + pb);
-    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-    const int64_t pr = mapped_row(n, cols, qt_map, 1);
-    sfqt[scale_byte(pr, (int)(pb >> 5), qt_cols)] = code;
-  }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
 }  // namespace
@@ -292,9 +334,19 @@ cudaError_t launch_mx_quantize_2x(const uint16_t *x, int64_t ldx, int64_t rows, 
                                   int q_map, uint8_t *sfq, uint8_t *qt, int64_t ldqt,
                                   int qt_cols, int qt_map, uint8_t *sfqt, cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
-  const dim3 grid(cols / kMx2Cols, (unsigned)(f8_padded_rows(rows, E) / kMx2Rows));
-  mx_quantize_2x_kernel<<<grid, 256, 0, s>>>(x, ldx, rows, cols, fmt, offsets, E, q, ldq, q_map,
-                                             sfq, qt, ldqt, qt_cols, qt_map, sfqt);
+  // tiles over the padded rows (an upper bound: the groups' padded total is
+  // known on the device only), a persistent grid of resident blocks
+  const int64_t n_tiles = (int64_t)(cols / kMx2Cols) * (f8_padded_rows(rows, E) / kMx2Rows);
+  static int per_sm = 0;
+  if (per_sm == 0 &&
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mx_quantize_2x_kernel, 256, 0) !=
+          cudaSuccess)
+    per_sm = 1;
+  const int64_t grid = std::min<int64_t>(n_tiles, (int64_t)std::max(per_sm, 1) * num_sms());
+  if (grid == 0) return cudaSuccess;
+  mx_quantize_2x_kernel<<<(unsigned)grid, 256, 0, s>>>(x, ldx, rows, cols, fmt, offsets, E, q, ldq,
+                                                       q_map, sfq, qt, ldqt, qt_cols, qt_map,
+                                                       sfqt, n_tiles);
   return cudaGetLastError();
 }
 
