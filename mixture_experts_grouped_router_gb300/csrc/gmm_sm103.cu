@@ -17,7 +17,8 @@
 //   warp 0      TMA producer: each CTA loads its own 128-row A tile and its
 //               half (128 columns) of the B tile for every K block, both
 //               completing on the leader CTA's barrier (32 KB per CTA and
-//               stage, 6 stages for every GEMM).  128-byte
+//               stage, 6 stages; 5 for the SwiGLU forward that adds a
+//               partial sum, whose epilogue needs more staging).  128-byte
 //               swizzle throughout; a K block is one 128-byte row per tile
 //               row (64 bf16 or 128 8-bit codes).
 //   warp 1      TMEM owner; in the leader CTA the MMA issuer: kind::f16
@@ -30,11 +31,14 @@
 //               tcgen05.ld of one
 //               TMEM lane (= one output row) per thread, fused SwiGLU /
 //               partial-sum / bias / FP8-dequantization / cast; each warp
-//               stages its 32x32 output blocks in swizzled shared memory and
-//               writes them with TMA bulk stores (bulk reduce-add for fp32
-//               partial sums), so that outputs leave as whole lines and never
-//               contend with the mainloop's operand loads (a block that
-//               straddles the expert's last row is written with plain stores).
+//               stages its 32x32 output blocks (32x64 for a bf16 weight
+//               gradient) in swizzled shared memory and writes them with TMA
+//               bulk stores (bulk reduce-add for fp32 partial sums), so that
+//               outputs leave as whole lines and never contend with the
+//               mainloop's operand loads (a block that straddles the expert's
+//               last row is written with plain stores); the SwiGLU backward's
+//               H blocks and a partial sum's blocks arrive by TMA loads one
+//               chunk ahead.
 // Tiles never straddle two experts.  The tile list is derived on the device
 // from group_offsets (no host synchronisation); tiles are visited expert by
 // expert in groups of 32 row tiles so that concurrently running CTAs share
@@ -59,7 +63,7 @@ constexpr int BM = 128, BK = 64, UK = 16;
 // chunks
 constexpr int kBN = 256;
 constexpr int kBNmx = 192;  // tile width of the block-scaled GEMMs
-constexpr int kStages = 8;  // ring slots of the barrier book (6 or 7 in use, see Ring)
+constexpr int kStages = 8;  // ring slots of the barrier book (5 or 6 in use, see Ring)
 constexpr int kMaxEpiWarps = 4;
 constexpr int kPadRows = kF8PadRows;  // group padding of column-wise copies (128 rows)
 constexpr int kStgBytes = 8192;  // per epilogue warp: up to four 32x32 bf16 blocks (or two fp32)
