@@ -223,7 +223,14 @@ mx_quantize_2x_kernel(const uint16_t *__restrict__ x, int64_t ldx, int64_t rows,
                       uint8_t *__restrict__ sfqt, int64_t n_tiles) {
   __shared__ int s_poff[kMxMaxE + 1];
   __shared__ __align__(16) uint8_t tiles[2][kMx2Rows * kMx2Pitch];
+  __shared__ __align__(16) uint8_t s_code[kMx2Rows][4];  // row-wise scale codes of a tile
   const int tid = threadIdx.x;
+  // TILES (the weights): a tile's 64 rows are 64 consecutive padded rows
+  // from a multiple of 64, so its row-wise scale codes fill 8 consecutive
+  // bytes of each of 32 atom lines (rows r0 and r0 + 32, blocks 0-3): written
+  // as 32 8-byte stores instead of 256 single bytes (weights 6% faster; the
+  // same for GROUPED, whose rows share that property, measured 1-2% slower)
+  const bool sc_packed = q_map == MOE_MX_ROWS_TILES;
   if (tid < 32) {  // padded group starts (warp-shuffle scan)
     int carry = 0;
     for (int c0 = 0; c0 < E; c0 += 32) {
@@ -281,22 +288,39 @@ mx_quantize_2x_kernel(const uint16_t *__restrict__ x, int64_t ldx, int64_t rows,
     const int c0 = cur.c0;
     float v[32];
     uint32_t w[8];
-    {
+    if (q != nullptr) {
       const int rr = tid >> 2, blk = tid & 3;
-      if (q != nullptr && i0 + rr < gsz) {
+      uint8_t code = 0;  // rows past the group: the smallest scale, no codes written
+      if (i0 + rr < gsz) {
 #pragma unroll
         for (int i = 0; i < 4; ++i)
           bf16x8_to_f32(
               *reinterpret_cast<const uint4 *>(tile + rr * kMx2Pitch + blk * 64 + i * 16),
               v + 8 * i);
-        const uint8_t code = quant_block(v, fmt, w);
+        code = quant_block(v, fmt, w);
         const int64_t r = g0 + i0 + rr;
         uint4 *dst = reinterpret_cast<uint4 *>(q + r * ldq + c0 + blk * 32);
         dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
         dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-        const int64_t pr =
-            q_map == MOE_MX_ROWS_GROUPED ? pr0 + rr : mapped_row(r, rows, q_map, E);
-        sfq[scale_byte(pr, (c0 >> 5) + blk, cols)] = code;
+        if (!sc_packed) {
+          const int64_t pr =
+              q_map == MOE_MX_ROWS_GROUPED ? pr0 + rr : mapped_row(r, rows, q_map, E);
+          sfq[scale_byte(pr, (c0 >> 5) + blk, cols)] = code;
+        }
+      }
+      if (sc_packed) {
+        s_code[rr][blk] = code;
+        __syncthreads();
+        if (tid < 32) {
+          // the tile's first padded row (a multiple of 64) and its atom line
+          const int64_t pf = mapped_row(g0 + i0, rows, q_map, E);
+          const uint32_t lo = *reinterpret_cast<const uint32_t *>(s_code[tid]);
+          const uint32_t hi = *reinterpret_cast<const uint32_t *>(s_code[tid + 32]);
+          // byte of (row pf + tid, block c0 / 32), 8-byte aligned; the next
+          // four bytes hold row pf + tid + 32
+          *reinterpret_cast<uint2 *>(sfq + scale_byte(pf + tid, c0 >> 5, cols)) =
+              make_uint2(lo, hi);
+        }
       }
     }
     const int c = tid & 127, half = tid >> 7;  // column, and which 32 of the 64 rows
