@@ -847,7 +847,9 @@ moe_status_t moe_layer_backward(const moe_layer_config *cfg, void *workspace,
  *   overwritten by every step.
  * moe_layer_pipeline_join -- make `stream` wait for every copy enqueued so far.
  * moe_layer_pipeline_sync -- block the host until every copy has completed.
- * moe_layer_pipeline_destroy -- synchronise and release the streams / events.
+ * moe_layer_pipeline_destroy -- synchronise the copy streams and release them
+ *   and the events (the caller synchronises its compute stream before it frees
+ *   the workspaces).
  */
 typedef struct moe_layer_pipeline moe_layer_pipeline;
 size_t moe_layer_pipeline_workspace_bytes(const moe_layer_config *cfg);
