@@ -763,8 +763,9 @@ moe_status_t moe_layer_pipeline_step(moe_layer_pipeline *p, const uint16_t *wi,
                                      uint16_t *h_out, uint16_t *h_dx, float *h_d_logits,
                                      moe_stream_t stream) {
   set_error("");
-  if (p == nullptr || h_x == nullptr || h_logits == nullptr || h_dout == nullptr ||
-      h_out == nullptr || h_dx == nullptr || h_d_logits == nullptr) {
+  if (p == nullptr ||
+      (p->cfg.T > 0 && (h_x == nullptr || h_logits == nullptr || h_dout == nullptr ||
+                        h_out == nullptr || h_dx == nullptr || h_d_logits == nullptr))) {
     set_error("moe_layer_pipeline_step: null pipeline or host buffer");
     return MOE_ERR_INVALID_ARG;
   }
@@ -784,7 +785,8 @@ moe_status_t moe_layer_pipeline_step(moe_layer_pipeline *p, const uint16_t *wi,
   const void *src[3] = {h_x, h_logits, h_dout};
   const int kind[3] = {kSlotX, kSlotLogits, kSlotDout};
   for (int i = 0; i < 3; ++i)
-    if ((e = cudaMemcpyAsync(sl[kind[i]], src[i], sz[kind[i]], cudaMemcpyHostToDevice,
+    if (sz[kind[i]] > 0 &&
+        (e = cudaMemcpyAsync(sl[kind[i]], src[i], sz[kind[i]], cudaMemcpyHostToDevice,
                              p->in_stream)) != cudaSuccess)
       return fail(e);
   if ((e = cudaEventRecord(p->in_ready[j], p->in_stream)) != cudaSuccess) return fail(e);
@@ -808,7 +810,8 @@ moe_status_t moe_layer_pipeline_step(moe_layer_pipeline *p, const uint16_t *wi,
   void *dst[3] = {h_out, h_dx, h_d_logits};
   const int okind[3] = {kSlotOut, kSlotDx, kSlotDLogits};
   for (int i = 0; i < 3; ++i)
-    if ((e = cudaMemcpyAsync(dst[i], sl[okind[i]], sz[okind[i]], cudaMemcpyDeviceToHost,
+    if (sz[okind[i]] > 0 &&
+        (e = cudaMemcpyAsync(dst[i], sl[okind[i]], sz[okind[i]], cudaMemcpyDeviceToHost,
                              p->out_stream)) != cudaSuccess)
       return fail(e);
   if ((e = cudaEventRecord(p->out_done[j], p->out_stream)) != cudaSuccess) return fail(e);

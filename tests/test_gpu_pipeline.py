@@ -126,3 +126,24 @@ def test_pipeline_options(opts):
     assert torch.equal(b.dwi, ref.dwi) and torch.equal(b.dwo, ref.dwo)
     if shape.bias:
         assert torch.equal(b.dbi, ref.dbi) and torch.equal(b.dbo, ref.dbo)
+
+
+def test_pipeline_no_tokens():
+    """A step of no tokens through the pipeline: empty host buffers, zero
+    weight gradients, no error."""
+    from mixture_experts_grouped_router_gb300 import layer
+    cfg = moe_synth.MoEConfig("empty", T=0, d=64, f=64, E=4, k=2)
+    inp = moe_synth.make_inputs(cfg, seed=0)
+    wi, wo = dev_bf16(inp["wi"]), dev_bf16(inp["wo"])
+    b = layer.MoEBuffers(layer_shape(cfg))
+    staging = torch.empty(max(1, L.moe_layer_pipeline_workspace_bytes(b.cfg)), dtype=torch.uint8,
+                          device="cuda")
+    pipe = L.LayerPipeline(b.cfg, b.workspace, staging)
+    empty_bf = torch.empty(0, cfg.d, dtype=torch.bfloat16).pin_memory()
+    empty_f = torch.empty(0, cfg.E, dtype=torch.float32).pin_memory()
+    pipe.step(wi, wo, empty_bf, empty_f, empty_bf, empty_bf, empty_bf, empty_f)
+    pipe.sync()
+    torch.cuda.synchronize()
+    pipe.close()
+    assert int(b.dev_status.item()) == 0
+    assert (b.dwi.float() == 0).all() and (b.dwo.float() == 0).all()
