@@ -5,7 +5,9 @@
   of every row order (plain, grouped with padded expert tiles, SwiGLU tiles),
   with zero, subnormal, saturating and non-finite blocks;
 * moe_gmm_mx (each epilogue) and moe_tgmm_mx against the oracle's grouped
-  GEMMs of the dequantized operands.  Every 32-element block is scaled by its
+  GEMMs of the dequantized operands;
+* the MXFP8 layer on reduced workloads element by element, and at full size
+  on sampled columns and weight-gradient entries.  Every 32-element block is scaled by its
   own random power of two, so a scale applied to the wrong rows, columns or
   blocks changes the result by factors of 2 and more.
 
@@ -397,3 +399,72 @@ def test_layer_mxfp8(name):
     bad = {k: v for k, v in errs.items()
            if not (v[0] <= 1e-2 and v[0] <= 0.5 * max(v[1], 1e-3) and v[2] <= 5e-2)}
     assert not bad, errs
+
+
+def _qdq_rows(col, fmt):
+    """Blocks of 32 along a column of one expert's rows, aligned at its first
+    row and completed with zeros (the weight gradients' operands)."""
+    n = col.shape[0]
+    pad = np.zeros(((n + 31) // 32 * 32,) + col.shape[1:])
+    pad[:n] = col
+    return mx.qdq_along(pad, 0, fmt)[:n]
+
+
+def test_layer_mxfp8_full_size_sampled():
+    """The Mixtral-like layer at full size with block-scaled GEMMs, as
+    `bench.py --mxfp8` runs it, against the MXFP8 oracle at sampled positions
+    the oracle computes one by one (block scaling is local: a sampled column
+    needs only its own blocks): the layout exactly; H, Act and dH of expert 0
+    and 5 on sampled columns (every row of the expert); dWi and dWo on sampled
+    rows x columns.  Tolerances 1e-2 (relative Frobenius) and 5e-2 * max|ref|
+    over each sampled block."""
+    import dataclasses
+    from gpu_helpers import layer_shape
+    from mixture_experts_grouped_router_gb300 import layer
+    cfg = C["mixtral"]
+    T, d, f, E, k = cfg.T, cfg.d, cfg.f, cfg.E, cfg.k
+    inp = moe_synth.make_inputs(cfg, seed=0)
+    x, wi, wo, dout = (dev_bf16(inp[n]) for n in ("x", "wi", "wo", "dout"))
+    logits = torch.from_numpy(inp["logits"]).cuda()
+    b = layer.MoEBuffers(dataclasses.replace(layer_shape(cfg), mxfp8=True))
+    layer.forward(b, x, logits, wi, wo)
+    layer.backward(b, dout, wi, wo)
+    torch.cuda.synchronize()
+    assert int(b.dev_status.item()) == 0
+    del wi, wo, x, dout
+    idx, w = moe_ref.route_topk(inp["logits"], k, cfg.score_fn, cfg.renorm)
+    lay = moe_ref.permute_layout(idx, E)
+    off = lay["group_offsets"]
+    assert b.group_offsets.cpu().numpy().tolist() == off.tolist()
+    assert b.s2f.cpu().numpy()[:lay["R"]].tolist() == lay["sorted_to_flat"].tolist()
+    f64 = moe_synth.bits_to_f64
+    e4, e5 = q8.E4M3, q8.E5M2
+    rng = np.random.default_rng(11)
+    for e in (0, 5):
+        lo, hi = int(off[e]), int(off[e + 1])
+        a = lay["sorted_to_flat"][lo:hi]                 # the expert's assignments, in order
+        t, j = a // k, a % k
+        xs = f64(inp["x"][t])                            # [n_e, d]
+        xsq = mx.qdq_along(xs, 1, e4)                     # blocks along d (up-projection A)
+        cg = np.sort(rng.choice(f, 4, replace=False))     # sampled gate / up columns
+        cols = np.concatenate([cg, f + cg])
+        ci = torch.as_tensor(cols, device="cuda")
+        wiq = mx.qdq_along(f64(inp["wi"][e][:, cols]), 0, e4)  # [d, 8], blocks along d
+        h = xsq @ wiq                                     # [n_e, 2 * 4]: gate cols, up cols
+        assert_close("h[e=%d]" % e, b.h[lo:hi][:, ci], h)
+        act = q8.round_bf16(moe_ref.swiglu(h))            # [n_e, 4]
+        assert_close("act[e=%d]" % e, b.act[lo:hi][:, ci[:4]], act)
+        # backward: dY rows = w * dOut of the token (bf16), blocks along d
+        dy = q8.round_bf16(w[t, j][:, None] * f64(inp["dout"][t]))
+        dyq = mx.qdq_along(dy, 1, e5)
+        woq = mx.qdq_along(f64(inp["wo"][e][cg]), 1, e4)  # rows cg of [f, d], blocks along d
+        d_act = dyq @ woq.T                               # [n_e, 4]
+        dh = q8.round_bf16(moe_ref.swiglu_bwd(q8.round_bf16(h), d_act))   # [dg | du]
+        assert_close("dh[e=%d]" % e, b.dh[lo:hi][:, ci], dh)
+        # weight gradients on sampled rows x columns, operands blocked along the expert's rows
+        rd = np.sort(rng.choice(d, 3, replace=False))
+        ri = torch.as_tensor(rd, device="cuda")
+        dwi = _qdq_rows(xs[:, rd], e4).T @ _qdq_rows(dh, e5)          # [3, 8]
+        assert_close("dwi[e=%d]" % e, b.dwi[e][ri][:, ci], dwi)
+        dwo = _qdq_rows(act, e4).T @ _qdq_rows(dy[:, rd], e5)          # [4, 3]
+        assert_close("dwo[e=%d]" % e, b.dwo[e][ci[:4]][:, ri], dwo)
